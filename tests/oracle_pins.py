@@ -1,0 +1,324 @@
+"""Checks that pin the CPU oracle to facts outside itself.
+
+Each ``check_*`` takes an oracle handle and raises ``AssertionError`` when the
+oracle disagrees with a closed form, an independent formulation, a structural
+invariant or f64 finite differences of the definition in baracuda-kernels
+``selective_scan.rs`` (module doc, "Algorithm summary").  None of the
+expected values below comes from the oracle's own code path: closed forms are
+evaluated here with numpy, softplus through ``np.logaddexp`` and silu as
+``z / (1 + exp(-z))``.
+
+``tests/test_oracle_pins.py`` runs them against the real oracle;
+``tests/test_oracle_mutants.py`` runs them against copies of the oracle with
+one planted mistake each and requires that some check fails.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+from mamba_selective_scan_fwd_gb300.inputs import small_inputs
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def softplus_np(x):
+    return np.logaddexp(0.0, x)
+
+
+def silu_np(z):
+    return z / (1.0 + np.exp(-z))
+
+
+def normwise(got, ref):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    if ref.size == 0:
+        return 0.0
+    scale = np.max(np.abs(ref))
+    err = np.max(np.abs(got - ref))
+    return err / scale if scale > 0 else err
+
+
+def _inputs(seed, Bsz, L, Dch, N, **kw):
+    x = small_inputs(Bsz, L, Dch, N, io="f32", seed=seed, **kw)
+    return {k: (None if v is None else v.astype(np.float64)) for k, v in x.items()}
+
+
+def _decay_without_softplus(x):
+    """With softplus off, Delta = delta + bias is used as is; keep it positive so that
+    exp(Delta * A) with A < 0 stays a decay and the checks stay well conditioned."""
+    x["delta"] = np.abs(x["delta"]) * 0.5
+    if x["delta_bias"] is not None:
+        x["delta_bias"] = np.abs(x["delta_bias"]) * 0.02
+
+
+def _fwd(orc, x, softplus=True, rows=None):
+    return orc.fwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], softplus, rows=rows,
+                   nthreads=2)
+
+
+def _bwd(orc, x, softplus=True):
+    return orc.bwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], softplus, dy=x["dy"],
+                   nthreads=2)
+
+
+VARIANTS = [
+    dict(softplus=True, has_D=True, has_z=True, has_bias=True),
+    dict(softplus=False, has_D=True, has_z=True, has_bias=True),
+    dict(softplus=True, has_D=False, has_z=False, has_bias=False),
+    dict(softplus=False, has_D=False, has_z=True, has_bias=False),
+    dict(softplus=True, has_D=True, has_z=False, has_bias=True),
+]
+
+
+# ----------------------------------------------------------------------------- forward
+
+
+def check_L1_closed_form(orc):
+    """L = 1: y = (Delta*u*sum_n B_n C_n + D*u) * silu(z), last_state = Delta*B*u."""
+    for i, v in enumerate(VARIANTS):
+        sp = v["softplus"]
+        x = _inputs(10 + i, 2, 1, 5, 4, has_D=v["has_D"], has_z=v["has_z"], has_bias=v["has_bias"])
+        if not sp:
+            _decay_without_softplus(x)
+        r = _fwd(orc, x, softplus=sp)
+        xin = x["delta"][:, 0, :] + (x["delta_bias"][None, :] if x["delta_bias"] is not None else 0.0)
+        dlt = softplus_np(xin) if sp else xin  # [Bsz, Dch]
+        u = x["u"][:, 0, :]
+        bc = np.sum(x["B"][:, 0, :] * x["C"][:, 0, :], axis=1)  # [Bsz]
+        y0 = dlt * u * bc[:, None]
+        if x["D"] is not None:
+            y0 = y0 + x["D"][None, :] * u
+        y = y0 * silu_np(x["z"][:, 0, :]) if x["z"] is not None else y0
+        assert normwise(r.y[:, 0, :], y) < 1e-14, ("L=1 y", v, normwise(r.y[:, 0, :], y))
+        last = dlt[:, :, None] * x["B"][:, 0, None, :] * u[:, :, None]
+        assert normwise(r.last_state, last) < 1e-14, ("L=1 last_state", v)
+
+
+def check_N1_geometric(orc):
+    """N = 1, inputs constant in t: h_t = beta (1 - alpha^(t+1)) / (1 - alpha)."""
+    L = 57
+    u0, d0, B0, C0, z0, A0, D0, bias0 = 0.75, 0.3, -1.25, 0.5, 0.625, -0.8, 1.125, -0.5
+    x = {
+        "u": np.full((1, L, 1), u0), "delta": np.full((1, L, 1), d0), "A": np.full((1, 1), A0),
+        "B": np.full((1, L, 1), B0), "C": np.full((1, L, 1), C0), "D": np.array([D0]), "z": np.full((1, L, 1), z0),
+        "delta_bias": np.array([bias0]),
+    }
+    for sp in (True, False):
+        dl = softplus_np(d0 + bias0) if sp else d0 + bias0
+        alpha = np.exp(dl * A0)
+        beta = dl * B0 * u0
+        t = np.arange(L)
+        h = beta * (1.0 - alpha ** (t + 1)) / (1.0 - alpha)
+        y = (C0 * h + D0 * u0) * silu_np(z0)
+        r = _fwd(orc, x, softplus=sp)
+        assert normwise(r.y[0, :, 0], y) < 1e-13, ("N=1 geometric y", sp)
+        assert abs(r.last_state[0, 0, 0] - h[-1]) < 1e-13 * abs(h[-1]), ("N=1 geometric last_state", sp)
+
+
+def check_A0_prefix_sum(orc):
+    """A = 0: h_t = sum_{s<=t} Delta_s B_s u_s, y = sum_n C h (no D, no z)."""
+    x = _inputs(21, 2, 33, 3, 4, has_D=False, has_z=False)
+    x["A"] = np.zeros_like(x["A"])
+    r = _fwd(orc, x)
+    dl = softplus_np(x["delta"] + x["delta_bias"][None, None, :])  # [B, L, D]
+    contrib = dl[..., None] * x["B"][:, :, None, :] * x["u"][..., None]  # [B, L, D, N]
+    h = np.cumsum(contrib, axis=1)
+    y = np.einsum("bldn,bln->bld", h, x["C"])
+    assert normwise(r.y, y) < 1e-13, "A=0 prefix sum"
+    assert normwise(r.last_state, h[:, -1]) < 1e-13, "A=0 last_state"
+
+
+def check_u0_zero(orc):
+    """u = 0 with no D: y = 0 and last_state = 0 exactly."""
+    x = _inputs(22, 2, 17, 3, 4, has_D=False)
+    x["u"] = np.zeros_like(x["u"])
+    r = _fwd(orc, x)
+    assert np.all(r.y == 0.0) and np.all(r.last_state == 0.0), "u=0 must give y=0"
+
+
+def quadratic_form(x, softplus=True):
+    """Independent O(L^2) formulation of the forward:
+    y0_t = sum_{s<=t} sum_n C_{t,n} exp(A_n * sum_{r=s+1..t} Delta_r) Delta_s B_{s,n} u_s + D u_t.
+    Returns (y, last_state)."""
+    u, dlt_raw = x["u"], x["delta"]
+    Bsz, L, Dch = u.shape
+    N = x["A"].shape[1]
+    xin = dlt_raw + (x["delta_bias"][None, None, :] if x["delta_bias"] is not None else 0.0)
+    dl = softplus_np(xin) if softplus else xin
+    y = np.zeros((Bsz, L, Dch))
+    last = np.zeros((Bsz, Dch, N))
+    for b in range(Bsz):
+        for d in range(Dch):
+            for t in range(L):
+                acc = 0.0
+                for s in range(t + 1):
+                    span = np.sum(dl[b, s + 1:t + 1, d])
+                    w = np.exp(x["A"][d] * span) * dl[b, s, d] * x["B"][b, s] * u[b, s, d]  # [N]
+                    acc += np.sum(x["C"][b, t] * w)
+                    if t == L - 1:
+                        last[b, d] += w
+                if x["D"] is not None:
+                    acc += x["D"][d] * u[b, t, d]
+                y[b, t, d] = acc * (silu_np(x["z"][b, t, d]) if x["z"] is not None else 1.0)
+    return y, last
+
+
+def check_quadratic_form(orc):
+    for i, v in enumerate(VARIANTS[:3]):
+        x = _inputs(30 + i, 2, 13, 3, 5, has_D=v["has_D"], has_z=v["has_z"], has_bias=v["has_bias"])
+        # a general (not -(n+1)) A, including positive entries, to pin the exponent
+        x["A"] = _rng(40 + i).uniform(-2.0, 0.3, size=x["A"].shape)
+        if not v["softplus"]:
+            _decay_without_softplus(x)
+        r = _fwd(orc, x, softplus=v["softplus"])
+        y, last = quadratic_form(x, v["softplus"])
+        assert normwise(r.y, y) < 1e-12, ("quadratic form y", v, normwise(r.y, y))
+        assert normwise(r.last_state, last) < 1e-12, ("quadratic form last_state", v)
+
+
+def check_invariants(orc):
+    x = _inputs(50, 3, 20, 4, 3)
+    base = _fwd(orc, x)
+    # causality: perturb every input at t' > 9 -> y[:, :10] unchanged
+    p = {k: (None if v is None else v.copy()) for k, v in x.items()}
+    for k in ("u", "delta", "B", "C", "z"):
+        p[k][:, 10:] += 0.37
+    r = _fwd(orc, p)
+    assert np.array_equal(r.y[:, :10], base.y[:, :10]), "causality"
+    assert not np.array_equal(r.y[:, 10:], base.y[:, 10:])
+    # channel independence: perturb channel 2's u/delta/z/D/bias/A -> other channels unchanged
+    p = {k: (None if v is None else v.copy()) for k, v in x.items()}
+    p["u"][:, :, 2] += 1.0
+    p["delta"][:, :, 2] -= 0.5
+    p["z"][:, :, 2] *= -1.0
+    p["D"][2] += 1.0
+    p["delta_bias"][2] += 0.3
+    p["A"][2] *= 0.5
+    r = _fwd(orc, p)
+    others = [0, 1, 3]
+    assert np.array_equal(r.y[:, :, others], base.y[:, :, others]), "channel independence"
+    # batch independence: perturb batch 1's B and C -> batches 0 and 2 unchanged
+    p = {k: (None if v is None else v.copy()) for k, v in x.items()}
+    p["B"][1] += 0.5
+    p["C"][1] -= 0.25
+    r = _fwd(orc, p)
+    assert np.array_equal(r.y[[0, 2]], base.y[[0, 2]]), "batch independence"
+    assert not np.array_equal(r.y[1], base.y[1])
+    # gate factorisation: y(z) = y(no z) * silu(z)
+    q = dict(x)
+    q["z"] = None
+    r0 = _fwd(orc, q)
+    assert normwise(base.y, r0.y * silu_np(x["z"])) < 1e-15, "gate factorisation"
+    assert normwise(base.y0, r0.y) < 1e-15
+    # linearity in u with no D and no z (Delta does not depend on u)
+    q = dict(x)
+    q["D"], q["z"] = None, None
+    rng = _rng(51)
+    u1 = np.round(rng.normal(size=x["u"].shape) * 64) / 64
+    u2 = np.round(rng.normal(size=x["u"].shape) * 64) / 64
+    ys = []
+    for uu in (u1, u2, 2.0 * u1 + u2):
+        q["u"] = uu
+        ys.append(_fwd(orc, q).y)
+    assert normwise(ys[2], 2.0 * ys[0] + ys[1]) < 1e-13, "linearity in u"
+
+
+def check_rows_subset(orc):
+    """A row-subset call reproduces the full call's rows exactly."""
+    x = _inputs(60, 2, 11, 5, 3)
+    full = _fwd(orc, x)
+    rows = np.array([7, 0, 3, 9])
+    r = _fwd(orc, x, rows=rows)
+    for i, row in enumerate(rows):
+        b, d = divmod(row, 5)
+        assert np.array_equal(r.y[i], full.y[b, :, d])
+        assert np.array_equal(r.last_state[i], full.last_state[b, d])
+
+
+# ----------------------------------------------------------------------------- backward
+
+_GRAD_NAMES = {"u": "du", "delta": "ddelta", "A": "dA", "B": "dB", "C": "dC", "D": "dD", "z": "dz",
+               "delta_bias": "ddelta_bias"}
+
+
+def _loss(orc, x, softplus):
+    return float(np.sum(x["dy"] * _fwd(orc, x, softplus).y))
+
+
+def check_finite_differences(orc):
+    """Every gradient against f64 central differences of sum(dy * y) on tiny shapes."""
+    cases = [
+        (1, 7, 2, 3, VARIANTS[0]),
+        (1, 6, 2, 2, VARIANTS[1]),
+        (2, 5, 1, 3, VARIANTS[2]),
+        (1, 8, 2, 1, VARIANTS[3]),
+        (1, 1, 2, 3, VARIANTS[4]),
+    ]
+    for ci, (Bsz, L, Dch, N, v) in enumerate(cases):
+        x = _inputs(70 + ci, Bsz, L, Dch, N, has_D=v["has_D"], has_z=v["has_z"], has_bias=v["has_bias"])
+        x["A"] = _rng(80 + ci).uniform(-1.5, -0.1, size=x["A"].shape)
+        sp = v["softplus"]
+        if not sp:
+            _decay_without_softplus(x)
+        g = _bwd(orc, x, sp)
+        for name, gname in _GRAD_NAMES.items():
+            if x[name] is None:
+                assert getattr(g, gname) is None, (gname, "should be absent")
+                continue
+            got = np.asarray(getattr(g, gname))
+            fd = np.zeros_like(x[name])
+            flat = x[name].reshape(-1)
+            for i in range(flat.size):
+                old = flat[i]
+                h = 1e-6 * max(1.0, abs(old))
+                flat[i] = old + h
+                fp = _loss(orc, x, sp)
+                flat[i] = old - h
+                fm = _loss(orc, x, sp)
+                flat[i] = old
+                fd.reshape(-1)[i] = (fp - fm) / (2 * h)
+            err = normwise(got, fd)
+            assert err < 1e-6, (f"finite differences {gname}", ci, v, err)
+
+
+def check_adjoint_dot(orc):
+    """<grad, v> against the directional derivative of sum(dy*y) along a random v."""
+    x = _inputs(90, 2, 48, 3, 4)
+    g = _bwd(orc, x)
+    rng = _rng(91)
+    dirs = {k: rng.normal(size=x[k].shape) for k in _GRAD_NAMES}
+    lhs = sum(float(np.sum(np.asarray(getattr(g, _GRAD_NAMES[k])) * dirs[k])) for k in _GRAD_NAMES)
+    eps = 1e-6
+
+    def shifted(s):
+        return {k: (v + s * dirs[k] if k in dirs else v) for k, v in x.items()}
+
+    rhs = (_loss(orc, shifted(eps), True) - _loss(orc, shifted(-eps), True)) / (2 * eps)
+    assert abs(lhs - rhs) <= 1e-7 * max(1.0, abs(rhs)), ("adjoint dot product", lhs, rhs)
+
+
+def check_identities(orc):
+    """ddelta_bias = sum_{b,t} ddelta and dD = sum_{b,t} dy*silu(z)*u."""
+    x = _inputs(95, 3, 21, 4, 4)
+    g = _bwd(orc, x)
+    assert normwise(g.ddelta_bias, g.ddelta.sum(axis=(0, 1))) < 1e-13, "dbias identity"
+    gate = x["dy"] * silu_np(x["z"])
+    assert normwise(g.dD, (gate * x["u"]).sum(axis=(0, 1))) < 1e-13, "dD identity"
+
+
+ALL_CHECKS = [
+    check_L1_closed_form,
+    check_N1_geometric,
+    check_A0_prefix_sum,
+    check_u0_zero,
+    check_quadratic_form,
+    check_invariants,
+    check_rows_subset,
+    check_finite_differences,
+    check_adjoint_dot,
+    check_identities,
+]
