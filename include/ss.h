@@ -1,0 +1,119 @@
+/*
+ * ss.h -- C ABI of the GB300 (sm_103a) Mamba-1 selective scan.
+ *
+ * The operation (baracuda-kernels `selective_scan.rs`, module doc
+ * "Algorithm summary"), per batch b, channel d and state n:
+ *
+ *   delta_eff = softplus(delta[b,t,d] + delta_bias[d])     (bias and softplus optional)
+ *   dA        = exp(delta_eff * A[d,n])
+ *   h[n]      = dA * h[n] + delta_eff * B[b,t,n] * u[b,t,d]  (h starts at zero)
+ *   y[b,t,d]  = (sum_n h[n] * C[b,t,n] + D[d] * u[b,t,d]) * silu(z[b,t,d])  (D, z optional)
+ *   last_state[b,d,n] = h[n] after t = L-1
+ *
+ * softplus(x) = log(1 + e^x), silu(z) = z / (1 + e^-z).
+ *
+ * Layouts ("Shape contract" of the same page): every tensor is contiguous and
+ * row-major.  u, delta, z, y, dy: [Bsz, L, Dch].  A: [Dch, N].  B, C:
+ * [Bsz, L, N].  D, delta_bias: [Dch].  last_state: [Bsz, Dch, N].
+ *
+ * Element types.  "io" tensors (u, delta, B, C, z, y, dy) are f32 or bf16 as
+ * selected by `dtype`.  A, D, delta_bias, last_state and every gradient are
+ * f32.  Arithmetic and the recurrence state are f32.
+ *
+ * Ownership and execution.  Every pointer is caller-owned DEVICE memory of
+ * the current CUDA device.  The library allocates nothing, never
+ * synchronises and enqueues all work on `stream` (a cudaStream_t passed as
+ * void*; NULL is the legacy default stream).  Returning SS_OK means the work
+ * was enqueued; a fault during execution surfaces at the caller's next
+ * synchronisation.  Inputs are read only; outputs are fully overwritten (no
+ * caller zeroing is needed); input and output ranges must not overlap.
+ *
+ * Errors are reported before anything is launched; nothing is written then.
+ * Results are deterministic: the same arguments on the same GPU give
+ * bit-identical outputs, forward and backward (no atomics anywhere).
+ */
+#ifndef SS_H
+#define SS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element-type ids; the numbering follows the dtype ids of the
+ * `..._workspace_bytes(.., dtype_id)` query on the baracuda-kernels page
+ * (0 = f32, 1 = f16, 2 = bf16).  SS_F16 is reserved and returns
+ * SS_ERR_UNSUPPORTED. */
+typedef enum { SS_F32 = 0, SS_F16 = 1, SS_BF16 = 2 } ss_dtype;
+
+/* Status codes; the first three mirror the page's error kinds
+ * (Unsupported, InvalidProblem, WorkspaceTooSmall). */
+typedef enum {
+    SS_OK = 0,
+    SS_ERR_INVALID_PROBLEM = 1,     /* negative extent, missing required pointer, optional-term mismatch */
+    SS_ERR_UNSUPPORTED = 2,         /* dtype, N outside {1,2,4,8,16,32}, size limit, pointer not 16-byte aligned */
+    SS_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes below the matching *_workspace_bytes() query */
+    SS_ERR_CUDA = 4                 /* a CUDA runtime call or launch failed */
+} ss_status;
+
+/* Bytes of device workspace ss_fwd needs for these sizes (0 when the scan
+ * runs without cross-block carries).  A pure function of its arguments. */
+size_t ss_fwd_workspace_bytes(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype);
+
+/*
+ * Forward selective scan.
+ *   u, delta      io  [Bsz, L, Dch]          required
+ *   A             f32 [Dch, N]               required
+ *   B, C          io  [Bsz, L, N]            required
+ *   D             f32 [Dch]                  optional (NULL: no skip term)
+ *   z             io  [Bsz, L, Dch]          optional (NULL: no gate)
+ *   delta_bias    f32 [Dch]                  optional (NULL: no bias)
+ *   softplus      nonzero: delta_eff = softplus(delta + bias); zero: delta + bias
+ *   y             io  [Bsz, L, Dch]          output, required
+ *   last_state    f32 [Bsz, Dch, N]          output, optional (L = 0 writes zeros)
+ *   workspace     device scratch of at least ss_fwd_workspace_bytes(...) bytes
+ *                 (may be NULL when that is 0); contents on entry are ignored.
+ * Bsz, L or Dch equal to 0 is valid; nothing but a zero last_state is written.
+ */
+int ss_fwd(const void *u, const void *delta, const float *A, const void *B, const void *C, const float *D,
+           const void *z, const float *delta_bias, int softplus, void *y, float *last_state, int64_t Bsz, int64_t L,
+           int64_t Dch, int64_t N, int dtype, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of device workspace ss_bwd needs for these sizes.  A pure function
+ * of its arguments. */
+size_t ss_bwd_workspace_bytes(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype);
+
+/*
+ * Backward of the forward above for the loss sum(dy * y); the gradient
+ * structure follows mamba-rs `gpu/backward.rs` (B2 gating backward, B3 SSM
+ * BPTT, B4 softplus backward on the raw delta).  Inputs are the forward's
+ * inputs plus dy (io, [Bsz, L, Dch]).  last_state receives no gradient.
+ * Outputs, all f32 and fully overwritten:
+ *   du, ddelta, dz   [Bsz, L, Dch]   (ddelta is the gradient w.r.t. the raw delta)
+ *   dA               [Dch, N]        summed over batch and time
+ *   dB, dC           [Bsz, L, N]     summed over channels
+ *   dD, ddelta_bias  [Dch]           summed over batch and time
+ * dD, dz and ddelta_bias must be given exactly when D, z and delta_bias are
+ * (else SS_ERR_INVALID_PROBLEM).  The backward recomputes the forward states
+ * instead of reading any saved by ss_fwd.
+ *   workspace     device scratch of at least ss_bwd_workspace_bytes(...) bytes;
+ *                 contents on entry are ignored.
+ */
+int ss_bwd(const void *u, const void *delta, const float *A, const void *B, const void *C, const float *D,
+           const void *z, const float *delta_bias, int softplus, const void *dy, float *du, float *ddelta, float *dA,
+           float *dB, float *dC, float *dD, float *dz, float *ddelta_bias, int64_t Bsz, int64_t L, int64_t Dch,
+           int64_t N, int dtype, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Static description of a status code. */
+const char *ss_status_string(int status);
+
+/* ABI version; bumped on any incompatible change. */
+int ss_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SS_H */

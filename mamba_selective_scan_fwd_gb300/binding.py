@@ -1,0 +1,200 @@
+"""Thin ctypes binding over ``libss.so`` (C ABI in include/ss.h).
+
+Argument marshalling only: every step of the scan runs in the library's CUDA
+kernels.  Tensors are torch CUDA tensors used as device buffers; the current
+torch stream is passed through.  There is no fallback: if the library is
+missing or fails to load, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libss.so")
+
+SS_F32, SS_F16, SS_BF16 = 0, 1, 2
+SS_OK = 0
+STATUS_NAMES = {0: "SS_OK", 1: "SS_ERR_INVALID_PROBLEM", 2: "SS_ERR_UNSUPPORTED", 3: "SS_ERR_WORKSPACE_TOO_SMALL",
+                4: "SS_ERR_CUDA"}
+
+# Every function include/ss.h declares.
+EXPORTS = ["ss_fwd", "ss_bwd", "ss_fwd_workspace_bytes", "ss_bwd_workspace_bytes", "ss_status_string",
+           "ss_abi_version"]
+
+
+class SSError(RuntimeError):
+    def __init__(self, fn, status, text):
+        super().__init__(f"{fn} returned {STATUS_NAMES.get(status, status)}: {text}")
+        self.status = status
+
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+
+
+def lib() -> ctypes.CDLL:
+    """Load libss.so (built by ``build.build()``); raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with mamba_selective_scan_fwd_gb300.build.build() "
+                          "(the selective scan has no non-CUDA implementation)")
+    L = ctypes.CDLL(LIB_PATH)
+    L.ss_fwd.restype = ctypes.c_int
+    L.ss_fwd.argtypes = [_P] * 8 + [ctypes.c_int, _P, _P] + [_I64] * 4 + [ctypes.c_int, _P, _SZ, _P]
+    L.ss_bwd.restype = ctypes.c_int
+    L.ss_bwd.argtypes = [_P] * 8 + [ctypes.c_int] + [_P] * 9 + [_I64] * 4 + [ctypes.c_int, _P, _SZ, _P]
+    for fn in ("ss_fwd_workspace_bytes", "ss_bwd_workspace_bytes"):
+        getattr(L, fn).restype = _SZ
+        getattr(L, fn).argtypes = [_I64] * 4 + [ctypes.c_int]
+    L.ss_status_string.restype = ctypes.c_char_p
+    L.ss_status_string.argtypes = [ctypes.c_int]
+    L.ss_abi_version.restype = ctypes.c_int
+    L.ss_abi_version.argtypes = []
+    _lib = L
+    return L
+
+
+def status_string(status: int) -> str:
+    return lib().ss_status_string(int(status)).decode()
+
+
+def _check(fn, rc):
+    if rc != SS_OK:
+        raise SSError(fn, rc, status_string(rc))
+
+
+def dtype_id(t) -> int:
+    import torch
+
+    if t.dtype == torch.float32:
+        return SS_F32
+    if t.dtype == torch.bfloat16:
+        return SS_BF16
+    if t.dtype == torch.float16:
+        return SS_F16
+    raise TypeError(f"unsupported io dtype {t.dtype}")
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def stream_handle(stream=None):
+    import torch
+
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _require(t, name, shape, dtype, device):
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)} != {tuple(shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype} != {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def fwd_workspace_bytes(Bsz, L, Dch, N, dtype) -> int:
+    return int(lib().ss_fwd_workspace_bytes(Bsz, L, Dch, N, dtype))
+
+
+def bwd_workspace_bytes(Bsz, L, Dch, N, dtype) -> int:
+    return int(lib().ss_bwd_workspace_bytes(Bsz, L, Dch, N, dtype))
+
+
+def _workspace(nbytes, device, workspace):
+    import torch
+
+    if workspace is None and nbytes > 0:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    size = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return workspace, size
+
+
+def ss_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, y=None, last_state=None,
+           return_last_state=True, workspace=None, stream=None):
+    """Forward selective scan.  Returns (y, last_state or None)."""
+    import torch
+
+    Bsz, L, Dch = u.shape
+    N = A.shape[1]
+    dev = u.device
+    io = u.dtype
+    _require(u, "u", (Bsz, L, Dch), io, dev)
+    _require(delta, "delta", (Bsz, L, Dch), io, dev)
+    _require(A, "A", (Dch, N), torch.float32, dev)
+    _require(B, "B", (Bsz, L, N), io, dev)
+    _require(C, "C", (Bsz, L, N), io, dev)
+    if D is not None:
+        _require(D, "D", (Dch,), torch.float32, dev)
+    if z is not None:
+        _require(z, "z", (Bsz, L, Dch), io, dev)
+    if delta_bias is not None:
+        _require(delta_bias, "delta_bias", (Dch,), torch.float32, dev)
+    if y is None:
+        y = torch.empty((Bsz, L, Dch), dtype=io, device=dev)
+    _require(y, "y", (Bsz, L, Dch), io, dev)
+    if last_state is None and return_last_state:
+        last_state = torch.empty((Bsz, Dch, N), dtype=torch.float32, device=dev)
+    if last_state is not None:
+        _require(last_state, "last_state", (Bsz, Dch, N), torch.float32, dev)
+    dt = dtype_id(u)
+    workspace, wsb = _workspace(fwd_workspace_bytes(Bsz, L, Dch, N, dt), dev, workspace)
+    rc = lib().ss_fwd(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias), int(bool(softplus)),
+                      _p(y), _p(last_state), Bsz, L, Dch, N, dt, _p(workspace), wsb, stream_handle(stream))
+    _check("ss_fwd", rc)
+    return y, last_state
+
+
+GRAD_SHAPES = ("du", "ddelta", "dA", "dB", "dC", "dD", "dz", "ddelta_bias")
+
+
+def ss_bwd(u, delta, A, B, C, D, z, delta_bias, softplus, dy, out=None, workspace=None, stream=None):
+    """Backward selective scan.  Returns a dict du, ddelta, dA, dB, dC, dD, dz,
+    ddelta_bias (f32; the optional ones are None when their input is None)."""
+    import torch
+
+    Bsz, L, Dch = u.shape
+    N = A.shape[1]
+    dev = u.device
+    io = u.dtype
+    for name, t, shape, dtype in (("u", u, (Bsz, L, Dch), io), ("delta", delta, (Bsz, L, Dch), io),
+                                  ("A", A, (Dch, N), torch.float32), ("B", B, (Bsz, L, N), io),
+                                  ("C", C, (Bsz, L, N), io), ("dy", dy, (Bsz, L, Dch), io)):
+        _require(t, name, shape, dtype, dev)
+    if D is not None:
+        _require(D, "D", (Dch,), torch.float32, dev)
+    if z is not None:
+        _require(z, "z", (Bsz, L, Dch), io, dev)
+    if delta_bias is not None:
+        _require(delta_bias, "delta_bias", (Dch,), torch.float32, dev)
+    f32 = torch.float32
+    shapes = {"du": (Bsz, L, Dch), "ddelta": (Bsz, L, Dch), "dA": (Dch, N), "dB": (Bsz, L, N), "dC": (Bsz, L, N),
+              "dD": (Dch,), "dz": (Bsz, L, Dch), "ddelta_bias": (Dch,)}
+    present = {"dD": D is not None, "dz": z is not None, "ddelta_bias": delta_bias is not None}
+    out = dict(out or {})
+    for k, shp in shapes.items():
+        if not present.get(k, True):
+            out[k] = None
+            continue
+        if out.get(k) is None:
+            out[k] = torch.empty(shp, dtype=f32, device=dev)
+        _require(out[k], k, shp, f32, dev)
+    dt = dtype_id(u)
+    workspace, wsb = _workspace(bwd_workspace_bytes(Bsz, L, Dch, N, dt), dev, workspace)
+    rc = lib().ss_bwd(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias), int(bool(softplus)),
+                      _p(dy), _p(out["du"]), _p(out["ddelta"]), _p(out["dA"]), _p(out["dB"]), _p(out["dC"]),
+                      _p(out["dD"]), _p(out["dz"]), _p(out["ddelta_bias"]), Bsz, L, Dch, N, dt, _p(workspace), wsb,
+                      stream_handle(stream))
+    _check("ss_bwd", rc)
+    return out

@@ -1,0 +1,74 @@
+"""Helpers shared by the GPU parity tests: move seeded inputs to the GPU, run
+the CUDA path through the C ABI binding, run the oracle on the same values,
+and compare.
+
+Tolerances (Mamba-1 selective scan accuracy targets):
+* f32 I/O: forward (y, last_state) max normwise relative error <= 1e-5,
+  gradients <= 1e-4;
+* bf16 I/O with f32 state: <= 2e-2 against the oracle fed the same
+  bf16-rounded inputs, with the oracle's y rounded to bf16.
+
+"Normwise relative error" of a tensor is max|got - ref| / max|ref| (a
+reference tensor that is all zero is compared absolutely).  An elementwise
+ratio is not used because y = sum_n h C cancels: near-zero outputs would
+measure the cancellation, not the kernel.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import mamba_selective_scan_fwd_gb300 as ss
+from mamba_selective_scan_fwd_gb300.inputs import round_bf16
+
+TOL = {"f32": {"fwd": 1e-5, "bwd": 1e-4}, "bf16": {"fwd": 2e-2, "bwd": 2e-2}}
+IO_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
+IO_KEYS = ("u", "delta", "B", "C", "z", "dy")
+
+
+def to_device(x: dict, io: str, dev="cuda"):
+    out = {}
+    for k, v in x.items():
+        if v is None:
+            out[k] = None
+            continue
+        t = torch.from_numpy(np.ascontiguousarray(v))
+        if k in IO_KEYS:
+            t = t.to(IO_DTYPE[io])
+        out[k] = t.to(dev)
+    return out
+
+
+def normwise(got, ref) -> float:
+    if isinstance(got, torch.Tensor):
+        got = got.detach().float().cpu().double().numpy()
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    if ref.size == 0:
+        return 0.0
+    scale = np.max(np.abs(ref))
+    err = np.max(np.abs(got - ref))
+    return float(err / scale) if scale > 0 else float(err)
+
+
+def gpu_fwd(t, softplus=True):
+    return ss.ss_fwd(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"], softplus)
+
+
+def gpu_bwd(t, softplus=True):
+    return ss.ss_bwd(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"], softplus, t["dy"])
+
+
+def oracle_fwd(orc, x, softplus=True, rows=None):
+    return orc.fwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], softplus, rows=rows)
+
+
+def oracle_bwd(orc, x, softplus=True, rows=None, want_dBdC=True):
+    return orc.bwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], softplus, dy=x["dy"],
+                   rows=rows, want_dBdC=want_dBdC)
+
+
+def ref_y(y, io):
+    """The oracle's y as the kernel must return it: rounded to bf16 for bf16 I/O."""
+    return round_bf16(y.astype(np.float32)).astype(np.float64) if io == "bf16" else y

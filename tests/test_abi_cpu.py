@@ -1,0 +1,130 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/ss.h declares, and rejects bad arguments before touching CUDA.
+
+Every call below fails validation, which happens before the first CUDA
+runtime call, so these run on a machine without a GPU.
+"""
+
+import os
+import re
+
+import pytest
+
+import mamba_selective_scan_fwd_gb300 as ss
+from mamba_selective_scan_fwd_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+INCLUDE = os.path.join(ROOT, "include")
+
+OK, INVALID, UNSUPPORTED, WS_SMALL = 0, 1, 2, 3
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: every call here fails validation first
+
+
+def declared_functions():
+    names = set()
+    for h in os.listdir(INCLUDE):
+        if h.endswith(".h"):
+            text = re.sub(r"/\*.*?\*/", "", open(os.path.join(INCLUDE, h)).read(), flags=re.S)
+            names.update(re.findall(r"\b(ss_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_header_matches_binding_exports():
+    assert declared_functions() == sorted(binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ss.lib()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert lib.ss_abi_version() == 1
+
+
+def test_status_strings():
+    for code in range(5):
+        assert len(ss.status_string(code)) >= 2
+    assert "unknown" in ss.status_string(99)
+
+
+def test_workspace_queries_are_pure_and_sized():
+    a = ss.bwd_workspace_bytes(4, 4096, 5120, 16, ss.SS_BF16)
+    assert a == ss.bwd_workspace_bytes(4, 4096, 5120, 16, ss.SS_BF16) > 0
+    assert ss.fwd_workspace_bytes(4, 4096, 5120, 16, ss.SS_BF16) == 0  # batch x channels fill the GPU: one chunk
+    assert ss.fwd_workspace_bytes(1, 131072, 1024, 16, ss.SS_BF16) > 0  # long sequence: chunk carries
+    assert ss.fwd_workspace_bytes(1, 8, 8, 3, ss.SS_F32) == 0  # unsupported N
+    assert ss.bwd_workspace_bytes(0, 8, 8, 4, ss.SS_F32) == 0
+    assert ss.fwd_workspace_bytes(1, 8, 8, 4, ss.SS_F16) == 0
+
+
+def _fwd(**kw):
+    a = dict(u=FAKE, delta=FAKE, A=FAKE, B=FAKE, C=FAKE, D=None, z=None, bias=None, softplus=1, y=FAKE, last=None,
+             Bsz=2, L=16, Dch=8, N=4, dtype=0, ws=None, wsb=0, stream=None)
+    a.update(kw)
+    return ss.lib().ss_fwd(a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"], a["bias"], a["softplus"], a["y"],
+                           a["last"], a["Bsz"], a["L"], a["Dch"], a["N"], a["dtype"], a["ws"], a["wsb"], a["stream"])
+
+
+def _bwd(**kw):
+    a = dict(u=FAKE, delta=FAKE, A=FAKE, B=FAKE, C=FAKE, D=None, z=None, bias=None, softplus=1, dy=FAKE, du=FAKE,
+             dd=FAKE, dA=FAKE, dB=FAKE, dC=FAKE, dD=None, dz=None, dbias=None, Bsz=2, L=16, Dch=8, N=4, dtype=0,
+             ws=None, wsb=0, stream=None)
+    a.update(kw)
+    return ss.lib().ss_bwd(a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"], a["bias"], a["softplus"],
+                           a["dy"], a["du"], a["dd"], a["dA"], a["dB"], a["dC"], a["dD"], a["dz"], a["dbias"], a["Bsz"],
+                           a["L"], a["Dch"], a["N"], a["dtype"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Bsz=-1), INVALID), (dict(L=-3), INVALID), (dict(Dch=-1), INVALID), (dict(N=-1), INVALID),
+    (dict(dtype=1), UNSUPPORTED), (dict(dtype=7), UNSUPPORTED), (dict(N=3), UNSUPPORTED), (dict(N=0), UNSUPPORTED),
+    (dict(N=64), UNSUPPORTED), (dict(u=None), INVALID), (dict(delta=None), INVALID), (dict(A=None), INVALID),
+    (dict(B=None), INVALID), (dict(C=None), INVALID), (dict(y=None), INVALID),
+    (dict(u=FAKE + 4), UNSUPPORTED), (dict(B=FAKE + 2), UNSUPPORTED), (dict(D=FAKE + 8), UNSUPPORTED),
+    (dict(last=FAKE + 12), UNSUPPORTED),
+    (dict(Bsz=1, L=131072, Dch=1024, N=16, dtype=2), WS_SMALL),
+])
+def test_fwd_rejects(kw, code):
+    assert _fwd(**kw) == code
+
+
+def test_fwd_workspace_too_small_reports_before_launch():
+    need = ss.fwd_workspace_bytes(1, 131072, 1024, 16, 2)
+    assert need > 0
+    assert _fwd(Bsz=1, L=131072, Dch=1024, N=16, dtype=2, ws=FAKE, wsb=need - 256) == WS_SMALL
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Bsz=-1), INVALID), (dict(dtype=1), UNSUPPORTED), (dict(N=5), UNSUPPORTED),
+    (dict(D=FAKE), INVALID), (dict(dD=FAKE), INVALID),            # D <-> dD presence must match
+    (dict(z=FAKE), INVALID), (dict(dz=FAKE), INVALID),            # z <-> dz
+    (dict(bias=FAKE), INVALID), (dict(dbias=FAKE), INVALID),      # delta_bias <-> ddelta_bias
+    (dict(dy=None), INVALID), (dict(du=None), INVALID), (dict(dd=None), INVALID), (dict(dA=None), INVALID),
+    (dict(dB=None), INVALID), (dict(dC=None), INVALID),
+    (dict(dB=FAKE + 4), UNSUPPORTED), (dict(dy=FAKE + 2), UNSUPPORTED),
+    (dict(), WS_SMALL),                                            # no workspace given
+])
+def test_bwd_rejects(kw, code):
+    assert _bwd(**kw) == code
+
+
+def test_bwd_workspace_one_byte_short():
+    need = ss.bwd_workspace_bytes(2, 16, 8, 4, 0)
+    assert _bwd(ws=FAKE, wsb=need - 1) == WS_SMALL
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        binding.lib()
+
+
+def test_product_does_not_import_oracle():
+    """The CUDA path's sources never reference the oracle."""
+    pkg = os.path.join(ROOT, "mamba_selective_scan_fwd_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "ss_oracle" not in text, f
