@@ -1,0 +1,401 @@
+"""Benchmark of the selective-scan hot path: one step = ss_fwd + ss_bwd over
+one batch of the Mamba-2.8B-layer workload (Bsz=4, L=4096, Dch=5120, N=16,
+bf16 I/O, f32 state and gradients), through the C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  ``value`` is whole-job throughput in B*L*D
+elements per second of forward+backward with inputs resident in HBM;
+``e2e`` is the same metric with host<->device copies of each step's inputs
+and results inside the timed region.  ``--impl reference`` times the CPU
+oracle (the plain f64 reference the tests compare against) on a bounded
+sample of the same workload on this host's cores.  Under torchrun every rank
+runs an independent replica (the scan shards over batch and channels with no
+exchange); rank 0 reports.
+"""
+
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from mamba_selective_scan_fwd_gb300.inputs import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "selective-scan fwd+bwd elements/s (B·L·D) and HBM GB/s vs GB300 peak"
+UNIT = "elements/s"
+WORKLOAD = WORKLOADS[3]  # mamba2.8b-layer-bf16
+
+# Algorithmic bytes per element (B*L*D unit) for bf16 I/O, f32 gradients:
+#   forward  = u, delta, z read + y write (4 x 2 B) = 8 B  (+ B, C, A, D, bias, last_state: per-(b,t) / per-d terms)
+#   backward = u, delta, z, dy read (4 x 2 B) + du, ddelta, dz write (3 x 4 B) = 20 B  (+ B, C, dB, dC, dA, ...)
+# The small per-(b, t, n) and per-(d, n) terms are added exactly below.
+
+
+def algorithmic_bytes(w):
+    e = 2 if w.io == "bf16" else 4
+    bld, bln, dn, d = w.Bsz * w.L * w.Dch, w.Bsz * w.L * w.N, w.Dch * w.N, w.Dch
+    fwd = 4 * bld * e + 2 * bln * e + 4 * (dn + 2 * d) + 4 * w.Bsz * w.Dch * w.N
+    bwd = 4 * bld * e + 3 * bld * 4 + 2 * bln * (e + 4) + 8 * (dn + 2 * d)
+    return fwd, bwd
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# MUFU ex2 results per clock per SM on GB300 (sm_103a), measured by a
+# dependent-free ex2.approx.f32 throughput loop; the SFU roofline of the scan
+# is B*L*D*N exponentials per direction at SMs x this rate x SM clock.
+EX2_PER_CLK_PER_SM = 32.0
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for row in csv.reader(io.StringIO(out)):
+            if len(row) < 8:
+                continue
+            try:
+                sm.append(float(row[0]))
+                smax.append(float(row[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, row[4:8]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_ours(args):
+    import torch
+
+    import mamba_selective_scan_fwd_gb300 as ss
+    from mamba_selective_scan_fwd_gb300 import binding
+
+    world, rank, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local if world > 1 else 0)
+    w = WORKLOAD
+    x = make_inputs(w)
+    io_dt = torch.bfloat16 if w.io == "bf16" else torch.float32
+    io_keys = ("u", "delta", "B", "C", "z", "dy")
+    host = {}
+    for k, v in x.items():
+        if v is None:
+            continue
+        t = torch.from_numpy(v)
+        if k in io_keys:
+            t = t.to(io_dt)
+        host[k] = t.pin_memory()
+    d = {k: v.to(dev, non_blocking=False) for k, v in host.items()}
+    for k in ("D", "z", "delta_bias"):
+        d.setdefault(k, None)
+    dtid = binding.dtype_id(d["u"])
+    plan = ss.plan_info(w.Bsz, w.L, w.Dch, w.N, dtid)
+    ws_f = torch.empty(max(ss.fwd_workspace_bytes(w.Bsz, w.L, w.Dch, w.N, dtid), 256), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(ss.bwd_workspace_bytes(w.Bsz, w.L, w.Dch, w.N, dtid), dtype=torch.uint8, device=dev)
+    y = torch.empty((w.Bsz, w.L, w.Dch), dtype=io_dt, device=dev)
+    last = torch.empty((w.Bsz, w.Dch, w.N), dtype=torch.float32, device=dev)
+    grads = {}
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ss.ss_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"], w.softplus, y=y,
+                  last_state=last, workspace=ws_f, stream=stream)
+        g = ss.ss_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"], w.softplus,
+                      d["dy"], out=grads, workspace=ws_b, stream=stream)
+        grads.update(g)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    # ---- device-resident timing, per-call events on the launching stream
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local if world > 1 else 0)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for i in range(K):
+        evs[i][0].record(stream)
+        ss.ss_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"], w.softplus, y=y,
+                  last_state=last, workspace=ws_f, stream=stream)
+        evs[i][1].record(stream)
+        ss.ss_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"], w.softplus, d["dy"],
+                  out=grads, workspace=ws_b, stream=stream)
+        evs[i][2].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    total_ms = start.elapsed_time(end)
+    t_fwd = sum(e[0].elapsed_time(e[1]) for e in evs) / K
+    t_bwd = sum(e[1].elapsed_time(e[2]) for e in evs) / K
+    total_ms = max_over_ranks(total_ms, world)
+    ms_per_step = total_ms / K
+    value = world * w.bld * K / (total_ms / 1e3)
+
+    # ---- end to end through the public API with host buffers
+    in_keys = [k for k in ("u", "delta", "A", "B", "C", "D", "z", "delta_bias", "dy") if k in host]
+    h2d = sum(host[k].numel() * host[k].element_size() for k in in_keys)
+    out_host = {"y": torch.empty(y.shape, dtype=y.dtype).pin_memory(),
+                "last_state": torch.empty(last.shape, dtype=last.dtype).pin_memory()}
+    for k, v in grads.items():
+        if v is not None:
+            out_host[k] = torch.empty(v.shape, dtype=v.dtype).pin_memory()
+    d2h = sum(v.numel() * v.element_size() for v in out_host.values())
+    e2e_steps = max(2, min(args.e2e_steps, K))
+
+    def e2e_step():
+        for k in in_keys:
+            d[k].copy_(host[k], non_blocking=True)
+        step()
+        out_host["y"].copy_(y, non_blocking=True)
+        out_host["last_state"].copy_(last, non_blocking=True)
+        for k, v in grads.items():
+            if v is not None:
+                out_host[k].copy_(v, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    e2e_value = world * w.bld * e2e_steps / (e2e_ms / 1e3)
+
+    # ---- roofline of the dominant call (the backward) and of the forward
+    hbm_peak, peak_kind = load_peaks()
+    fwd_bytes, bwd_bytes = algorithmic_bytes(w)
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    sm_mhz = clk.get("sm_mhz") or 2070.0
+    exp_peak = sms * EX2_PER_CLK_PER_SM * sm_mhz * 1e6  # ex2 / s
+    exps = w.bld * w.N
+
+    def roof(bytes_, t_ms):
+        t_hbm = bytes_ / (hbm_peak * 1e9)
+        t_sfu = exps / exp_peak
+        if t_hbm >= t_sfu:
+            ach = bytes_ / (t_ms / 1e3) / 1e9
+            return {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
+                    "frac": round(ach / hbm_peak, 4), "peak_kind": f"{peak_kind} HBM copy",
+                    "roofline_ms": round(t_hbm * 1e3, 4)}
+        ach = exps / (t_ms / 1e3) / 1e9
+        pk = exp_peak / 1e9
+        return {"bound": "alu", "achieved": round(ach, 1), "peak": round(pk, 1), "unit": "Gexp2/s",
+                "frac": round(ach / pk, 4),
+                "peak_kind": f"MUFU ex2: {sms} SMs x {EX2_PER_CLK_PER_SM:g}/clk x {sm_mhz:g} MHz (median sampled)",
+                "roofline_ms": round(t_sfu * 1e3, 4)}
+
+    r_bwd = roof(bwd_bytes, t_bwd)
+    r_bwd.update({"kernel": "ss_bwd (k_bwd_main + 2 reductions)", "traffic": None, "ms": round(t_bwd, 4)})
+    r_fwd = roof(fwd_bytes, t_fwd)
+    r_fwd.update({"kernel": "ss_fwd (k_fwd_main)", "traffic": None, "ms": round(t_fwd, 4)})
+    t_roof = r_fwd["roofline_ms"] + r_bwd["roofline_ms"]
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "Bsz": w.Bsz, "L": w.L, "Dch": w.Dch, "N": w.N, "io": w.io,
+                   "terms": "D, z, delta_bias, softplus, last_state", "chunks": plan["chunks"],
+                   "l2": "no flush: each step reads and writes > 2 GB, far above the 129 MB L2",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "hbm_gbs": round((fwd_bytes + bwd_bytes) / (ms_per_step / 1e3) / 1e9, 1),
+        "roofline": r_bwd, "roofline_fwd": r_fwd,
+        "roofline_step_frac": round(t_roof / ms_per_step, 4),
+        "clocks": clk,
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps},
+        "gpu_launches": K * (plan["fwd_kernels"] + plan["bwd_kernels"]),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, x, budget_s=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def _oracle_sample(orc, w, x, rows):
+    """The oracle's forward and backward on a row sample of the workload; returns seconds."""
+    t0 = time.perf_counter()
+    orc.fwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], w.softplus, rows=rows)
+    orc.bwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], w.softplus, dy=x["dy"],
+            rows=rows, want_dBdC=True)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, x, budget_s=15.0):
+    """The oracle, as it stands, on a bounded row sample of the workload (all host cores).
+
+    Row batches of growing size run until about ``budget_s`` seconds of oracle
+    work have been timed; the rate is rows x L over the summed time."""
+    import numpy as np
+
+    import oracle
+
+    orc = oracle.get()
+    cores = oracle.default_threads()
+    # f64 copies once, outside the timed sample
+    x64 = {k: (None if v is None else np.ascontiguousarray(v, dtype=np.float64)) for k, v in x.items()}
+    rng = np.random.default_rng(0)
+    perm = rng.permutation(w.Bsz * w.Dch)
+    _oracle_sample(orc, w, x64, perm[:cores])  # untimed: first-call overheads
+    done, spent, n = 0, 0.0, cores
+    while spent < budget_s and done < perm.size:
+        rows = perm[done:done + n]
+        spent += _oracle_sample(orc, w, x64, rows)
+        done += rows.size
+        n = min(2 * n, perm.size - done)
+    return {"value": round(done * w.L / spent, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{done} of {w.Bsz * w.Dch} (b, d) rows, full L={w.L}, forward + backward incl. dB/dC "
+                      f"contributions, f64, {spent:.1f} s"}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+
+    w = WORKLOAD
+    x = make_inputs(w)
+    x64 = {k: (None if v is None else np.ascontiguousarray(v, dtype=np.float64)) for k, v in x.items()}
+    orc = oracle.get()
+    cores = oracle.default_threads()
+    rng = np.random.default_rng(1)
+    # size each step's row sample so that warmup + steps fit in about two minutes
+    probe = _oracle_sample(orc, w, x64, rng.choice(w.Bsz * w.Dch, cores, replace=False)) / cores
+    per_step_budget = 120.0 / max(1, args.steps + args.warmup)
+    n = int(max(cores, min(w.Bsz * w.Dch, per_step_budget / max(probe, 1e-6))))
+    n = max(1, n // cores * cores) if n >= cores else n
+    for _ in range(args.warmup):
+        _oracle_sample(orc, w, x64, rng.choice(w.Bsz * w.Dch, n, replace=False))
+    total = 0.0
+    for _ in range(args.steps):
+        total += _oracle_sample(orc, w, x64, rng.choice(w.Bsz * w.Dch, n, replace=False))
+    value = args.steps * n * w.L / total
+    sample = f"{n} of {w.Bsz * w.Dch} (b, d) rows per step, full L={w.L}, forward + backward, f64 oracle"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "Bsz": w.Bsz, "L": w.L, "Dch": w.Dch, "N": w.N, "io": w.io},
+        "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

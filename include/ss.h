@@ -106,6 +106,14 @@ int ss_bwd(const void *u, const void *delta, const float *A, const void *B, cons
            float *dB, float *dC, float *dD, float *dz, float *ddelta_bias, int64_t Bsz, int64_t L, int64_t Dch,
            int64_t N, int dtype, void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * Launch plan for these sizes, as ss_fwd / ss_bwd will use it: the number of
+ * time chunks the sequence is cut into and how many kernels each call
+ * enqueues (0 for an empty problem).  Pointers may be NULL.  Returns a status.
+ */
+int ss_plan_info(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype, int64_t *chunks, int *fwd_kernels,
+                 int *bwd_kernels);
+
 /* Static description of a status code. */
 const char *ss_status_string(int status);
 

@@ -6,8 +6,8 @@ library is loaded on first use and every entry point raises if it is
 missing -- there is no other implementation to fall back on.
 """
 
-from .binding import (SS_BF16, SS_F16, SS_F32, SSError, bwd_workspace_bytes, fwd_workspace_bytes, lib, ss_bwd,
-                      ss_fwd, status_string)
+from .binding import (SS_BF16, SS_F16, SS_F32, SSError, bwd_workspace_bytes, fwd_workspace_bytes, lib, plan_info,
+                      ss_bwd, ss_fwd, status_string)
 
-__all__ = ["ss_fwd", "ss_bwd", "fwd_workspace_bytes", "bwd_workspace_bytes", "status_string", "lib", "SSError",
+__all__ = ["ss_fwd", "ss_bwd", "fwd_workspace_bytes", "bwd_workspace_bytes", "status_string", "plan_info", "lib", "SSError",
            "SS_F32", "SS_F16", "SS_BF16"]

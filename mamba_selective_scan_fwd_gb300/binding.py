@@ -20,8 +20,8 @@ STATUS_NAMES = {0: "SS_OK", 1: "SS_ERR_INVALID_PROBLEM", 2: "SS_ERR_UNSUPPORTED"
                 4: "SS_ERR_CUDA"}
 
 # Every function include/ss.h declares.
-EXPORTS = ["ss_fwd", "ss_bwd", "ss_fwd_workspace_bytes", "ss_bwd_workspace_bytes", "ss_status_string",
-           "ss_abi_version"]
+EXPORTS = ["ss_fwd", "ss_bwd", "ss_fwd_workspace_bytes", "ss_bwd_workspace_bytes", "ss_plan_info",
+           "ss_status_string", "ss_abi_version"]
 
 
 class SSError(RuntimeError):
@@ -53,6 +53,8 @@ def lib() -> ctypes.CDLL:
     for fn in ("ss_fwd_workspace_bytes", "ss_bwd_workspace_bytes"):
         getattr(L, fn).restype = _SZ
         getattr(L, fn).argtypes = [_I64] * 4 + [ctypes.c_int]
+    L.ss_plan_info.restype = ctypes.c_int
+    L.ss_plan_info.argtypes = [_I64] * 4 + [ctypes.c_int, _P, _P, _P]
     L.ss_status_string.restype = ctypes.c_char_p
     L.ss_status_string.argtypes = [ctypes.c_int]
     L.ss_abi_version.restype = ctypes.c_int
@@ -110,6 +112,16 @@ def fwd_workspace_bytes(Bsz, L, Dch, N, dtype) -> int:
 
 def bwd_workspace_bytes(Bsz, L, Dch, N, dtype) -> int:
     return int(lib().ss_bwd_workspace_bytes(Bsz, L, Dch, N, dtype))
+
+
+def plan_info(Bsz, L, Dch, N, dtype) -> dict:
+    """Chunk count and kernels per call that ss_fwd / ss_bwd use for these sizes."""
+    k = ctypes.c_int64()
+    nf = ctypes.c_int()
+    nb = ctypes.c_int()
+    _check("ss_plan_info", lib().ss_plan_info(Bsz, L, Dch, N, dtype, ctypes.byref(k), ctypes.byref(nf),
+                                              ctypes.byref(nb)))
+    return {"chunks": k.value, "fwd_kernels": nf.value, "bwd_kernels": nb.value}
 
 
 def _workspace(nbytes, device, workspace):

@@ -65,6 +65,19 @@ size_t ss_bwd_workspace_bytes(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, in
     return bwd_layout(p, Bsz, L, Dch, N).total;
 }
 
+int ss_plan_info(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype, int64_t* chunks, int* fwd_kernels,
+                 int* bwd_kernels) {
+    int rc = check_sizes(Bsz, L, Dch, N, dtype);
+    if (rc != SS_OK) return rc;
+    const bool empty = Bsz == 0 || L == 0 || Dch == 0;
+    const Plan p = make_plan(Bsz, L, Dch, N);
+    if (chunks) *chunks = empty ? 0 : p.K;
+    // forward: [summary if K > 1] + main; backward: [fwd summary + rev summary if K > 1] + main + 2 reductions
+    if (fwd_kernels) *fwd_kernels = empty ? 0 : (p.K > 1 ? 2 : 1);
+    if (bwd_kernels) *bwd_kernels = empty ? 0 : (p.K > 1 ? 5 : 3);
+    return SS_OK;
+}
+
 int ss_fwd(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
            const void* z, const float* delta_bias, int softplus, void* y, float* last_state, int64_t Bsz, int64_t L,
            int64_t Dch, int64_t N, int dtype, void* workspace, size_t workspace_bytes, void* stream) {
