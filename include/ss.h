@@ -81,6 +81,28 @@ int ss_fwd(const void *u, const void *delta, const float *A, const void *B, cons
            const void *z, const float *delta_bias, int softplus, void *y, float *last_state, int64_t Bsz, int64_t L,
            int64_t Dch, int64_t N, int dtype, void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * ss_fwd for callers that cannot allocate device memory (no counterpart on
+ * the pages this library follows; it exists for callers such as code
+ * replayed from a captured CUDA graph, a custom allocator that must not be
+ * bypassed, or a runtime that forbids cudaMalloc on its hot path).
+ * Arguments and results are those of ss_fwd without the workspace: the
+ * chunk-carry scratch lives in a library-owned device array of
+ * SS_FWD_NOALLOC_MAX_SCRATCH_BYTES, reserved on every GPU that loads the
+ * library until the process exits.  Problems whose ss_fwd_workspace_bytes()
+ * exceeds that size are rejected with SS_ERR_WORKSPACE_TOO_SMALL before
+ * anything is launched.  The function allocates nothing.  All calls share
+ * the one array: calls that overlap on the GPU (unordered streams) race;
+ * calls on one stream are safe.  Nothing in the array needs clearing between
+ * calls.  The first call on a device that uses the scratch looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture.
+ */
+#define SS_FWD_NOALLOC_MAX_SCRATCH_BYTES ((size_t)2 << 20)
+int ss_fwd_noalloc(const void *u, const void *delta, const float *A, const void *B, const void *C, const float *D,
+                   const void *z, const float *delta_bias, int softplus, void *y, float *last_state, int64_t Bsz,
+                   int64_t L, int64_t Dch, int64_t N, int dtype, void *stream);
+
 /* Bytes of device workspace ss_bwd needs for these sizes.  A pure function
  * of its arguments. */
 size_t ss_bwd_workspace_bytes(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype);

@@ -21,7 +21,10 @@ STATUS_NAMES = {0: "SS_OK", 1: "SS_ERR_INVALID_PROBLEM", 2: "SS_ERR_UNSUPPORTED"
 
 # Every function include/ss.h declares.
 EXPORTS = ["ss_fwd", "ss_bwd", "ss_fwd_workspace_bytes", "ss_bwd_workspace_bytes", "ss_plan_info",
-           "ss_status_string", "ss_abi_version"]
+           "ss_status_string", "ss_abi_version", "ss_fwd_noalloc"]
+
+# Size of the library-owned scratch behind ss_fwd_noalloc (SS_FWD_NOALLOC_MAX_SCRATCH_BYTES).
+FWD_NOALLOC_MAX_SCRATCH_BYTES = 2 << 20
 
 
 class SSError(RuntimeError):
@@ -59,6 +62,8 @@ def lib() -> ctypes.CDLL:
     L.ss_status_string.argtypes = [ctypes.c_int]
     L.ss_abi_version.restype = ctypes.c_int
     L.ss_abi_version.argtypes = []
+    L.ss_fwd_noalloc.restype = ctypes.c_int
+    L.ss_fwd_noalloc.argtypes = [_P] * 8 + [ctypes.c_int, _P, _P] + [_I64] * 4 + [ctypes.c_int, _P]
     _lib = L
     return L
 
@@ -165,6 +170,21 @@ def ss_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, y=
     rc = lib().ss_fwd(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias), int(bool(softplus)),
                       _p(y), _p(last_state), Bsz, L, Dch, N, dt, _p(workspace), wsb, stream_handle(stream))
     _check("ss_fwd", rc)
+    return y, last_state
+
+
+def ss_fwd_noalloc(u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state=None, stream=None):
+    """Forward selective scan that allocates nothing, for callers that cannot
+    allocate device memory at the call site: y (and last_state, if given) must
+    be preallocated, and the chunk-carry scratch is the library's own fixed
+    device array instead of a workspace.  Raises SSError when the problem
+    needs more scratch than that array holds."""
+    Bsz, L, Dch = u.shape
+    N = A.shape[1]
+    rc = lib().ss_fwd_noalloc(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias),
+                              int(bool(softplus)), _p(y), _p(last_state), Bsz, L, Dch, N, dtype_id(u),
+                              stream_handle(stream))
+    _check("ss_fwd_noalloc", rc)
     return y, last_state
 
 
