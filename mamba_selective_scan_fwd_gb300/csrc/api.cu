@@ -31,8 +31,6 @@ int check_sizes(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype) {
     return SS_OK;
 }
 
-bool grid_ok(const Plan& p, int64_t Bsz) { return p.tiles * Bsz * p.K < (1ll << 31); }
-
 }  // namespace
 
 extern "C" {
@@ -53,7 +51,7 @@ const char* ss_status_string(int status) {
 size_t ss_fwd_workspace_bytes(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype) {
     if (check_sizes(Bsz, L, Dch, N, dtype) != SS_OK) return 0;
     if (Bsz == 0 || L == 0 || Dch == 0) return 0;
-    const Plan p = make_plan(Bsz, L, Dch, N);
+    const FPlan p = make_fplan(Bsz, L, Dch, N);
     if (p.K <= 1) return 0;
     return align_up((size_t)Bsz * Dch * p.K * N * 2 * sizeof(float), 256);
 }
@@ -61,8 +59,8 @@ size_t ss_fwd_workspace_bytes(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, in
 size_t ss_bwd_workspace_bytes(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype) {
     if (check_sizes(Bsz, L, Dch, N, dtype) != SS_OK) return 0;
     if (Bsz == 0 || L == 0 || Dch == 0) return 0;
-    const Plan p = make_plan(Bsz, L, Dch, N);
-    return bwd_layout(p, Bsz, L, Dch, N).total;
+    const FPlan p = make_fplan(Bsz, L, Dch, N);
+    return bwd_layout2(p, Bsz, L, Dch, N).total;
 }
 
 int ss_plan_info(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype, int64_t* chunks, int* fwd_kernels,
@@ -70,11 +68,12 @@ int ss_plan_info(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype, int6
     int rc = check_sizes(Bsz, L, Dch, N, dtype);
     if (rc != SS_OK) return rc;
     const bool empty = Bsz == 0 || L == 0 || Dch == 0;
-    const Plan p = make_plan(Bsz, L, Dch, N);
-    if (chunks) *chunks = empty ? 0 : p.K;
-    // forward: [summary if K > 1] + main; backward: [fwd summary + rev summary if K > 1] + main + 2 reductions
-    if (fwd_kernels) *fwd_kernels = empty ? 0 : (p.K > 1 ? 2 : 1);
-    if (bwd_kernels) *bwd_kernels = empty ? 0 : (p.K > 1 ? 5 : 3);
+    const FPlan fp = make_fplan(Bsz, L, Dch, N);
+    if (chunks) *chunks = empty ? 0 : fp.K;
+    // forward: [summary if K > 1] + main;
+    // backward: [forward summary if K > 1] + checkpoints + [reverse summary if K > 1] + main + 2 reductions
+    if (fwd_kernels) *fwd_kernels = empty ? 0 : (fp.K > 1 ? 2 : 1);
+    if (bwd_kernels) *bwd_kernels = empty ? 0 : (fp.K > 1 ? 6 : 4);
     return SS_OK;
 }
 
@@ -96,8 +95,8 @@ int ss_fwd(const void* u, const void* delta, const float* A, const void* B, cons
         }
         return SS_OK;
     }
-    const Plan p = make_plan(Bsz, L, Dch, N);
-    if (!grid_ok(p, Bsz)) return SS_ERR_UNSUPPORTED;
+    const FPlan p = make_fplan(Bsz, L, Dch, N);
+    if (p.tiles * Bsz * p.K >= (1ll << 31)) return SS_ERR_UNSUPPORTED;
     const size_t need = ss_fwd_workspace_bytes(Bsz, L, Dch, N, dtype);
     if (workspace_bytes < need || (need > 0 && workspace == nullptr)) return SS_ERR_WORKSPACE_TOO_SMALL;
     FwdArgs a;
@@ -108,7 +107,7 @@ int ss_fwd(const void* u, const void* delta, const float* A, const void* B, cons
     a.softplus = softplus ? 1 : 0;
     a.dtype = dtype;
     a.ws_fsum = static_cast<float*>(workspace);
-    return launch_fwd(a, p, st) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+    return launch_fwd2(a, p, st, kModeY, nullptr) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
 int ss_bwd(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
@@ -147,9 +146,9 @@ int ss_bwd(const void* u, const void* delta, const float* A, const void* B, cons
         }
         return SS_OK;
     }
-    const Plan p = make_plan(Bsz, L, Dch, N);
-    if (!grid_ok(p, Bsz)) return SS_ERR_UNSUPPORTED;
-    const BwdLayout w = bwd_layout(p, Bsz, L, Dch, N);
+    const FPlan p = make_fplan(Bsz, L, Dch, N);
+    if (p.tiles * Bsz * p.K >= (1ll << 31)) return SS_ERR_UNSUPPORTED;
+    const BwdLayout w = bwd_layout2(p, Bsz, L, Dch, N);
     if (workspace_bytes < w.total || workspace == nullptr) return SS_ERR_WORKSPACE_TOO_SMALL;
     char* ws = static_cast<char*>(workspace);
     BwdArgs a;
@@ -169,7 +168,7 @@ int ss_bwd(const void* u, const void* delta, const float* A, const void* B, cons
     a.ws_dA = reinterpret_cast<float*>(ws + w.dA);
     a.ws_dD = reinterpret_cast<float*>(ws + w.dD);
     a.ws_db = reinterpret_cast<float*>(ws + w.db);
-    return launch_bwd(a, p, st) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+    return launch_bwd2(a, p, st) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -1,0 +1,511 @@
+// Backward selective scan: the chain rule of the forward definition
+// (baracuda-kernels `selective_scan.rs`, "Algorithm summary") for the loss
+// sum(dy * y), with the gradient structure of mamba-rs `gpu/backward.rs`
+// (B2 gating backward, B3 SSM BPTT with local gradients then fixed-order
+// reductions, B4 softplus backward on the raw delta), fused into one reverse
+// pass per channel tile, recomputing states instead of storing them, and
+// without atomics.
+//
+// Per step t, state n of channel d (lam = adjoint of h, "carry" = a_{t+1} lam_{t+1}):
+//   g      = dy * silu(z)               dz     = dy * y0 * sig(z) * (1 + z (1 - sig(z)))
+//   lam_n  = g * C_n + carry_n          carry_n <- a_{t,n} * lam_n
+//   du     = g * D + Delta * sum_n lam_n B_n
+//   dDelta = sum_n A_n q_n + u * sum_n lam_n B_n      with q_n = a_{t,n} lam_n h_{t-1,n}
+//   ddelta = dDelta * sig(delta + bias) under softplus, else dDelta
+//   dA_n  += Delta * q_n;   dB_n += lam_n * Delta * u;   dC_n += g * h_{t,n}
+//
+// Work split (one warp = CH channels of one batch row and one time chunk,
+// the same lane layout as the forward):
+//   * a checkpoint pass (the forward kernel in checkpoint mode) stores the
+//     state at the start of every kSub-step sub-chunk;
+//   * this kernel visits 16-step tiles from the end of the chunk backwards.
+//     The tile prologue computes the per-(t, d) terms once (softplus and its
+//     derivative, the gate, g, the dz factor) into shared memory; then each
+//     sub-chunk is recomputed forward from its checkpoint with its decays and
+//     states in registers, and the adjoint walks it backwards;
+//   * per step the G lanes of a channel combine their partial sums with two
+//     xor shuffles, and the warp sums dB / dC over its channels through
+//     shared memory in a fixed order; a second kernel adds the per-tile
+//     partials, a third the per-(batch, chunk) dA / dD / ddelta_bias
+//     partials.  Every sum has a fixed order: the result is bit-reproducible.
+// Chunks (only when batch x channels cannot fill the GPU): the forward
+// summaries (P, H) give each chunk's carry-in state; reverse summaries
+// M_k = a_{s_k} lam_{s_k} (lam from a zero incoming carry) combine as
+// rho_{k-1} = M_k + P_k rho_k into each chunk's carry-in adjoint.
+#include "common.cuh"
+#include "kernels.h"
+#include "simd.cuh"
+
+namespace ss {
+
+constexpr int kTT = 16;  // backward tile: steps staged per prologue
+
+template <typename T, int N>
+struct BCfg {
+    static constexpr int S = N < 8 ? N : 8;
+    static constexpr int G = N / S;
+    static constexpr int CH = 32 / G;
+    static constexpr int CPL = CH / 2;              // channels per prologue lane (two lanes per step)
+    static constexpr int RWH = CPL * (int)sizeof(T) / 4 > 0 ? CPL * (int)sizeof(T) / 4 : 1;
+    static constexpr int NB = N * (int)sizeof(T);
+    static constexpr int NW = NB >= 4 ? NB / 4 : 1;
+    static constexpr int NP = N + 4;
+    static constexpr int RP = N + 1;                // padded row of the per-step dB / dC scratch
+};
+
+template <typename T>
+__device__ __forceinline__ float belem(const uint32_t* w, int j) {
+    if constexpr (sizeof(T) == 4) {
+        return __uint_as_float(w[j]);
+    } else {
+        return (j & 1) ? bf16hi(w[j >> 1]) : bf16lo(w[j >> 1]);
+    }
+}
+
+template <int NBYTES, int NWORDS>
+__device__ __forceinline__ void bload_words(const void* p, uint32_t (&w)[NWORDS]) {
+    if constexpr (NBYTES % 16 == 0) {
+#pragma unroll
+        for (int v = 0; v < NBYTES / 16; v++) {
+            const uint4 q = __ldg(reinterpret_cast<const uint4*>(p) + v);
+            w[4 * v] = q.x; w[4 * v + 1] = q.y; w[4 * v + 2] = q.z; w[4 * v + 3] = q.w;
+        }
+    } else if constexpr (NBYTES == 8) {
+        const uint2 q = __ldg(reinterpret_cast<const uint2*>(p));
+        w[0] = q.x; w[1] = q.y;
+    } else if constexpr (NBYTES == 4) {
+        w[0] = __ldg(reinterpret_cast<const unsigned int*>(p));
+    } else {
+        w[0] = __ldg(reinterpret_cast<const unsigned short*>(p));
+    }
+}
+
+// CPL contiguous io elements at (row offset off, channel c0): vector loads when
+// aligned and complete, else element loads zero-filled past Dch.
+template <typename T, int CPL, int RWH>
+__device__ __forceinline__ void bload_half(const T* base, int64_t off, int64_t c0, int64_t Dch, bool fast,
+                                           uint32_t (&w)[RWH]) {
+    if (fast) {
+        bload_words<CPL * (int)sizeof(T), RWH>(base + off, w);
+    } else {
+#pragma unroll
+        for (int i = 0; i < RWH; i++) w[i] = 0u;
+#pragma unroll
+        for (int c = 0; c < CPL; c++) {
+            if (c0 + c < Dch) {
+                if constexpr (sizeof(T) == 4) {
+                    w[c] = __ldg(reinterpret_cast<const unsigned int*>(base + off) + c);
+                } else {
+                    const uint32_t v = __ldg(reinterpret_cast<const unsigned short*>(base + off) + c);
+                    w[c >> 1] |= (c & 1) ? (v << 16) : v;
+                }
+            }
+        }
+    }
+}
+
+template <int S>
+__device__ __forceinline__ void bld_shared(const float* p, float (&v)[S]) {
+    if constexpr (S % 4 == 0) {
+#pragma unroll
+        for (int q = 0; q < S; q += 4) {
+            const float4 f = *reinterpret_cast<const float4*>(p + q);
+            v[q] = f.x; v[q + 1] = f.y; v[q + 2] = f.z; v[q + 3] = f.w;
+        }
+    } else if constexpr (S == 2) {
+        const float2 f = *reinterpret_cast<const float2*>(p);
+        v[0] = f.x; v[1] = f.y;
+    } else {
+        v[0] = p[0];
+    }
+}
+
+// softplus(x) (as in simd.cuh) together with sigmoid(x), sharing e = e^-|x|.
+__device__ __forceinline__ void softplus_and_sigmoid(float x, float& sp, float& sg) {
+    const float e = ex2a(-fabsf(x) * kLog2eF);
+    const float s = e * rcpa(2.f + e);
+    const float s2 = s * s;
+    float p = 1.f / 15.f;
+    p = fmaf(p, s2, 1.f / 13.f);
+    p = fmaf(p, s2, 1.f / 11.f);
+    p = fmaf(p, s2, 1.f / 9.f);
+    p = fmaf(p, s2, 1.f / 7.f);
+    p = fmaf(p, s2, 1.f / 5.f);
+    p = fmaf(p, s2, 1.f / 3.f);
+    p = fmaf(p, s2, 1.f);
+    sp = fmaxf(x, 0.f) + 2.f * s * p;
+    const float r = rcpa(1.f + e);
+    sg = x >= 0.f ? r : e * r;
+}
+
+template <int G>
+__device__ __forceinline__ float gsum(float v) {
+#pragma unroll
+    for (int m = 1; m < G; m <<= 1) v += __shfl_xor_sync(kFull, v, m);
+    return v;
+}
+
+// MODE kRevMain: the backward proper.  MODE kRevSummary: only the adjoint
+// walk of chunks 1..K-1 from a zero carry, writing M_k.
+constexpr int kRevMain = 0, kRevSummary = 1;
+
+template <typename T, int N, int MODE>
+__global__ void __launch_bounds__(32) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_t k_hi) {
+    using C = BCfg<T, N>;
+    constexpr bool MAIN = MODE == kRevMain;
+    constexpr int S = C::S, G = C::G, CH = C::CH, CPL = C::CPL, RWH = C::RWH, NWd = C::NW, NP = C::NP,
+                  RP = C::RP;
+    __shared__ float4 sS[kTT][CH];                  // (Delta, Delta*u, g, -)    swizzled columns
+    __shared__ float4 sE[MAIN ? kTT : 1][CH];       // (sig(x), u, dz factor, -) swizzled columns
+    __shared__ __align__(16) float sB[kTT][NP];
+    __shared__ __align__(16) float sC[kTT][NP];
+    __shared__ float sR[MAIN ? 2 : 1][CH][RP];      // one step's dB / dC contributions
+    __shared__ float sP[MAIN ? kTT : 1][2 * N];     // the tile's dB / dC sums over this warp's channels
+    __shared__ float sBias[CH];
+
+    const FwdArgs& f = a.f;
+    const int lane = threadIdx.x;
+    int64_t blk = blockIdx.x;
+    const int64_t tile = blk % p.tiles;
+    blk /= p.tiles;
+    const int64_t nk = k_hi - k_lo;
+    const int64_t k = k_lo + blk % nk;
+    const int64_t b = blk / nk;
+    const int64_t L = f.L, Dch = f.Dch;
+    const int64_t d0 = tile * CH;
+    const T* u = static_cast<const T*>(f.u);
+    const T* delta = static_cast<const T*>(f.delta);
+    const T* Bm = static_cast<const T*>(f.B);
+    const T* Cm = static_cast<const T*>(f.C);
+    const T* z = static_cast<const T*>(f.z);
+    const T* dy = static_cast<const T*>(a.dy);
+
+    if (lane < CH) {
+        const int64_t dc = d0 + lane < Dch ? d0 + lane : Dch - 1;
+        sBias[lane] = f.delta_bias ? f.delta_bias[dc] : 0.f;
+    }
+
+    // scan-lane identity
+    const int ch = lane / G, g = lane % G;
+    const bool ch_ok = d0 + ch < Dch;
+    const int64_t d = ch_ok ? d0 + ch : Dch - 1;
+    const int n0 = g * S;
+    const int64_t row = b * Dch + d;
+    const float Dd = f.D ? f.D[d] : 0.f;
+    float Av[S], A2[S], carry[S], dA[S];
+#pragma unroll
+    for (int s = 0; s < S; s++) {
+        Av[s] = f.A[d * N + n0 + s];
+        A2[s] = Av[s] * kLog2eF;
+        carry[s] = 0.f;
+        dA[s] = 0.f;
+    }
+    if (MAIN && k + 1 < p.K) {
+        const float2* fs = reinterpret_cast<const float2*>(f.ws_fsum) + row * p.K * N + n0;
+        const float* rs = a.ws_rsum + row * p.K * N + n0;
+        for (int64_t j = p.K - 1; j > k; j--) {
+#pragma unroll
+            for (int s = 0; s < S; s++) carry[s] = fmaf(fs[j * N + s].x, carry[s], rs[j * N + s]);
+        }
+    }
+    float dD_acc = 0.f, db_acc = 0.f;
+
+    // prologue-lane identity: step pr of the tile, channels pc0 .. pc0 + CPL
+    const int pr = lane % kTT, ph = lane / kTT;
+    const int pc0 = ph * CPL;
+    const bool pfast = ((Dch * (int64_t)sizeof(T)) % 16 == 0) && (d0 + CH <= Dch) &&
+                       ((CPL * (int)sizeof(T)) % 4 == 0);
+
+    const int64_t t_begin = k * p.Lc;
+    const int64_t t_end = t_begin + p.Lc < L ? t_begin + p.Lc : L;
+    const int64_t ntile = (t_end - t_begin + kTT - 1) / kTT;
+    const float* ck = a.ws_ckpt + ((row * G + g) * p.K + k) * (p.Lc / kSub) * S;
+
+    for (int64_t m = ntile - 1; m >= 0; m--) {
+        const int64_t t0 = t_begin + m * kTT;
+        // ---- prologue: per-(t, d) terms of the tile's steps, staged in shared memory
+        {
+            const int64_t t = t0 + pr;
+            const bool rv = t < t_end;
+            uint32_t rd[RWH], ru[RWH], rz[RWH], rg[RWH], rbc[NWd];
+            if (rv) {
+                const int64_t off = (b * L + t) * Dch + d0 + pc0;
+                bload_half<T, CPL, RWH>(delta, off, d0 + pc0, Dch, pfast, rd);
+                bload_half<T, CPL, RWH>(u, off, d0 + pc0, Dch, pfast, ru);
+                bload_half<T, CPL, RWH>(dy, off, d0 + pc0, Dch, pfast, rg);
+                if (z) bload_half<T, CPL, RWH>(z, off, d0 + pc0, Dch, pfast, rz);
+                if (MAIN || ph == 1) bload_words<C::NB, NWd>((ph == 0 ? Bm : Cm) + (b * L + t) * N, rbc);
+            }
+            const int swz = pr & (CH - 1);
+#pragma unroll
+            for (int c = 0; c < CPL; c++) {
+                const int cc = pc0 + c;
+                float dl = 0.f, sgx = 0.f, uu = 0.f, gg = 0.f, dzf = 0.f;
+                if (rv) {
+                    const float x = belem<T>(rd, c) + sBias[cc];
+                    if (f.softplus) {
+                        softplus_and_sigmoid(x, dl, sgx);
+                    } else {
+                        dl = x;
+                        sgx = 1.f;
+                    }
+                    uu = belem<T>(ru, c);
+                    const float dyv = belem<T>(rg, c);
+                    gg = dyv;
+                    dzf = 0.f;
+                    if (z) {
+                        const float zz = belem<T>(rz, c);
+                        const float sz = sigmoid_fast(zz);
+                        gg = dyv * zz * sz;
+                        dzf = dyv * sz * fmaf(zz, 1.f - sz, 1.f);
+                    }
+                }
+                sS[pr][cc ^ swz] = make_float4(dl, dl * uu, gg, 0.f);
+                if (MAIN) sE[pr][cc ^ swz] = make_float4(sgx, uu, dzf, 0.f);
+            }
+            if (ph == 1) {
+#pragma unroll
+                for (int n = 0; n < N; n++) sC[pr][n] = rv ? belem<T>(rbc, n) : 0.f;
+            } else if (MAIN) {
+#pragma unroll
+                for (int n = 0; n < N; n++) sB[pr][n] = rv ? belem<T>(rbc, n) : 0.f;
+            }
+        }
+        __syncwarp();
+
+        if constexpr (!MAIN) {
+            // ---- reverse summary: adjoint walk from a zero carry, no states needed
+            for (int i = kTT - 1; i >= 0; i--) {
+                if (t0 + i >= t_end) continue;
+                const float4 ss = sS[i][ch ^ (i & (CH - 1))];
+                float Cv[S];
+                bld_shared<S>(&sC[i][n0], Cv);
+#pragma unroll
+                for (int s = 0; s < S; s++) {
+                    const float lam = fmaf(ss.z, Cv[s], carry[s]);
+                    carry[s] = ex2a(ss.x * A2[s]) * lam;
+                }
+            }
+        } else {
+            // ---- two sub-chunks of kSub steps, last one first
+#pragma unroll 1
+            for (int sub = kTT / kSub - 1; sub >= 0; sub--) {
+                const int64_t ts = t0 + sub * kSub;
+                if (ts >= t_end) continue;
+                float hs[S];
+                const float* src = ck + ((ts - t_begin) / kSub) * S;
+#pragma unroll
+                for (int s = 0; s < S; s++) hs[s] = src[s];
+                // recompute decays and states of the sub-chunk
+                float av[kSub][S], hv[kSub][S];
+                {
+                    float hh[S];
+#pragma unroll
+                    for (int s = 0; s < S; s++) hh[s] = hs[s];
+#pragma unroll
+                    for (int i = 0; i < kSub; i++) {
+                        const int r = sub * kSub + i;
+                        const float4 ss = sS[r][ch ^ (r & (CH - 1))];  // padded steps hold Delta = 0
+                        float Bv[S];
+                        bld_shared<S>(&sB[r][n0], Bv);
+                        if constexpr (S >= 2) {
+#pragma unroll
+                            for (int s = 0; s < S; s += 2) {
+                                const float2 e = mul2(splat2(ss.x), make_float2(A2[s], A2[s + 1]));
+                                const float2 da = make_float2(ex2a(e.x), ex2a(e.y));
+                                const float2 x = mul2(splat2(ss.y), make_float2(Bv[s], Bv[s + 1]));
+                                const float2 nh = fma2(da, make_float2(hh[s], hh[s + 1]), x);
+                                av[i][s] = da.x; av[i][s + 1] = da.y;
+                                hh[s] = nh.x; hh[s + 1] = nh.y;
+                                hv[i][s] = nh.x; hv[i][s + 1] = nh.y;
+                            }
+                        } else {
+                            av[i][0] = ex2a(ss.x * A2[0]);
+                            hh[0] = fmaf(av[i][0], hh[0], ss.y * Bv[0]);
+                            hv[i][0] = hh[0];
+                        }
+                    }
+                }
+                // adjoint walk
+#pragma unroll
+                for (int i = kSub - 1; i >= 0; i--) {
+                    const int r = sub * kSub + i;
+                    const int64_t t = t0 + r;
+                    if (t >= t_end) continue;
+                    const float4 ss = sS[r][ch ^ (r & (CH - 1))];
+                    float Bv[S], Cv[S];
+                    bld_shared<S>(&sB[r][n0], Bv);
+                    bld_shared<S>(&sC[r][n0], Cv);
+                    float du_p = 0.f, dd_p = 0.f, y0_p = 0.f;
+                    float cB[S], cC[S];
+                    if constexpr (S >= 2) {
+                        float2 dup = make_float2(0.f, 0.f), ddp = dup, y0p = dup;
+                        const float2 g2 = splat2(ss.z), dl2 = splat2(ss.x), dlu2 = splat2(ss.y);
+#pragma unroll
+                        for (int s = 0; s < S; s += 2) {
+                            const float2 Cp = make_float2(Cv[s], Cv[s + 1]);
+                            const float2 hcur = make_float2(hv[i][s], hv[i][s + 1]);
+                            const float2 hprev = i > 0 ? make_float2(hv[i - 1][s], hv[i - 1][s + 1])
+                                                       : make_float2(hs[s], hs[s + 1]);
+                            const float2 lam = fma2(g2, Cp, make_float2(carry[s], carry[s + 1]));
+                            dup = fma2(lam, make_float2(Bv[s], Bv[s + 1]), dup);
+                            const float2 cn = mul2(make_float2(av[i][s], av[i][s + 1]), lam);
+                            const float2 q = mul2(cn, hprev);
+                            ddp = fma2(make_float2(Av[s], Av[s + 1]), q, ddp);
+                            const float2 na = fma2(dl2, q, make_float2(dA[s], dA[s + 1]));
+                            dA[s] = na.x; dA[s + 1] = na.y;
+                            y0p = fma2(Cp, hcur, y0p);
+                            const float2 cb = mul2(lam, dlu2), cc = mul2(g2, hcur);
+                            cB[s] = cb.x; cB[s + 1] = cb.y;
+                            cC[s] = cc.x; cC[s + 1] = cc.y;
+                            carry[s] = cn.x; carry[s + 1] = cn.y;
+                        }
+                        du_p = dup.x + dup.y;
+                        dd_p = ddp.x + ddp.y;
+                        y0_p = y0p.x + y0p.y;
+                    } else {
+                        const float hprev = i > 0 ? hv[i - 1][0] : hs[0];
+                        const float lam = fmaf(ss.z, Cv[0], carry[0]);
+                        du_p = lam * Bv[0];
+                        const float cn = av[i][0] * lam;
+                        const float q = cn * hprev;
+                        dd_p = Av[0] * q;
+                        dA[0] = fmaf(ss.x, q, dA[0]);
+                        y0_p = Cv[0] * hv[i][0];
+                        cB[0] = lam * ss.y;
+                        cC[0] = ss.z * hv[i][0];
+                        carry[0] = cn;
+                    }
+                    du_p = gsum<G>(du_p);
+                    dd_p = gsum<G>(dd_p);
+                    y0_p = gsum<G>(y0_p);
+                    // per-(t, d) outputs
+                    if (ch_ok && g == 0) {
+                        const float4 se = sE[r][ch ^ (r & (CH - 1))];
+                        const int64_t idx = (b * L + t) * Dch + d;
+                        a.du[idx] = fmaf(ss.z, Dd, ss.x * du_p);
+                        const float dx = fmaf(se.y, du_p, dd_p) * se.x;
+                        a.ddelta[idx] = dx;
+                        if (z) a.dz[idx] = se.z * fmaf(Dd, se.y, y0_p);
+                        dD_acc = fmaf(ss.z, se.y, dD_acc);
+                        db_acc += dx;
+                    }
+                    // dB / dC: this warp's channels, fixed order
+#pragma unroll
+                    for (int s = 0; s < S; s++) {
+                        sR[0][ch][n0 + s] = ch_ok ? cB[s] : 0.f;
+                        sR[1][ch][n0 + s] = ch_ok ? cC[s] : 0.f;
+                    }
+                    __syncwarp();
+                    for (int o = lane; o < 2 * N; o += 32) {
+                        const int tau = o / N, n = o % N;
+                        float acc = 0.f;
+#pragma unroll 8
+                        for (int c = 0; c < CH; c++) acc += sR[tau][c][n];
+                        sP[r][o] = acc;
+                    }
+                    __syncwarp();
+                }
+            }
+            // this tile's per-warp dB / dC sums -> partial buffer
+            for (int e = lane; e < kTT * 2 * N; e += 32) {
+                const int r = e / (2 * N), o = e % (2 * N);
+                const int64_t t = t0 + r;
+                if (t < t_end) {
+                    const int tau = o / N, n = o % N;
+                    a.ws_bc[(((int64_t)tau * p.tiles + tile) * f.Bsz + b) * L * N + t * N + n] = sP[r][o];
+                }
+            }
+        }
+        __syncwarp();
+    }
+
+    if constexpr (!MAIN) {
+        if (ch_ok) {
+            float* out = a.ws_rsum + (row * p.K + k) * N + n0;
+#pragma unroll
+            for (int s = 0; s < S; s++) out[s] = carry[s];
+        }
+    } else if (ch_ok) {
+        float* o = a.ws_dA + ((b * p.K + k) * Dch + d) * N + n0;
+#pragma unroll
+        for (int s = 0; s < S; s++) o[s] = dA[s];
+        if (g == 0) {
+            a.ws_dD[(b * p.K + k) * Dch + d] = dD_acc;
+            a.ws_db[(b * p.K + k) * Dch + d] = db_acc;
+        }
+    }
+}
+
+// dB / dC: sum of the per-tile partials, tiles in ascending order.
+__global__ void k_bwd2_reduce_bc(BwdArgs a, FPlan p) {
+    const int64_t bln = a.f.Bsz * a.f.L * a.f.N;
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= 2 * bln) return;
+    const int tensor = e >= bln ? 1 : 0;
+    const int64_t r = e - tensor * bln;
+    const float* src = a.ws_bc + (size_t)tensor * p.tiles * bln + r;
+    float acc = 0.f;
+    for (int64_t tl = 0; tl < p.tiles; tl++) acc += src[tl * bln];
+    (tensor ? a.dC : a.dB)[r] = acc;
+}
+
+// dA / dD / ddelta_bias: sum over (batch, chunk) partials in ascending order.
+__global__ void k_bwd2_reduce_params(BwdArgs a, FPlan p) {
+    const int64_t Dch = a.f.Dch, N = a.f.N;
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t parts = a.f.Bsz * p.K;
+    if (e < Dch * N) {
+        float acc = 0.f;
+        for (int64_t q = 0; q < parts; q++) acc += a.ws_dA[q * Dch * N + e];
+        a.dA[e] = acc;
+    }
+    if (e < Dch) {
+        if (a.dD) {
+            float acc = 0.f;
+            for (int64_t q = 0; q < parts; q++) acc += a.ws_dD[q * Dch + e];
+            a.dD[e] = acc;
+        }
+        if (a.ddelta_bias) {
+            float acc = 0.f;
+            for (int64_t q = 0; q < parts; q++) acc += a.ws_db[q * Dch + e];
+            a.ddelta_bias[e] = acc;
+        }
+    }
+}
+
+template <typename T, int N>
+cudaError_t launch_bwd2_t(const BwdArgs& a, const FPlan& p, cudaStream_t st) {
+    // checkpoint pass (with forward summaries first when the sequence is chunked)
+    cudaError_t e = launch_fwd2(a.f, p, st, kModeCkpt, a.ws_ckpt);
+    if (e != cudaSuccess) return e;
+    if (p.K > 1) {
+        const int64_t blocks = p.tiles * a.f.Bsz * (p.K - 1);
+        k_bwd2<T, N, kRevSummary><<<(unsigned)blocks, 32, 0, st>>>(a, p, 1, p.K);
+    }
+    const int64_t blocks = p.tiles * a.f.Bsz * p.K;
+    k_bwd2<T, N, kRevMain><<<(unsigned)blocks, 32, 0, st>>>(a, p, 0, p.K);
+    const int64_t n_bc = 2 * a.f.Bsz * a.f.L * a.f.N;
+    k_bwd2_reduce_bc<<<(unsigned)ceil_div(n_bc, 256), 256, 0, st>>>(a, p);
+    const int64_t n_par = a.f.Dch * a.f.N;
+    k_bwd2_reduce_params<<<(unsigned)ceil_div(n_par, 256), 256, 0, st>>>(a, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd2(const BwdArgs& a, const FPlan& p, cudaStream_t st) {
+#define SS_BWD2_N(T)                                          \
+    switch (a.f.N) {                                          \
+        case 1: return launch_bwd2_t<T, 1>(a, p, st);         \
+        case 2: return launch_bwd2_t<T, 2>(a, p, st);         \
+        case 4: return launch_bwd2_t<T, 4>(a, p, st);         \
+        case 8: return launch_bwd2_t<T, 8>(a, p, st);         \
+        case 16: return launch_bwd2_t<T, 16>(a, p, st);       \
+        case 32: return launch_bwd2_t<T, 32>(a, p, st);       \
+        default: return cudaErrorInvalidValue;                \
+    }
+    if (a.f.dtype == 0) { SS_BWD2_N(float) }
+    SS_BWD2_N(__nv_bfloat16)
+#undef SS_BWD2_N
+}
+
+}  // namespace ss

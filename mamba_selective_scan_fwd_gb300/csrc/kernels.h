@@ -24,7 +24,7 @@ struct BwdArgs {
     const void* dy;
     float *du, *ddelta, *dA, *dB, *dC, *dD, *dz, *ddelta_bias;
     float* ws_rsum;   // reverse chunk summaries M: [Bsz*Dch][K][N]
-    float* ws_ckpt;   // sub-chunk start states: [Bsz*Dch*G][K][nsub][S]
+    float* ws_ckpt;   // sub-chunk start states: [Bsz*Dch*G][K][Lc/kSub][S]
     float* ws_bc;     // per-tile dB/dC partials: [2][tiles][Bsz][L][N]
     float* ws_dA;     // per-(b,k) dA partials: [Bsz][K][Dch][N]
     float* ws_dD;     // per-(b,k) dD partials: [Bsz][K][Dch]
@@ -36,7 +36,44 @@ struct BwdLayout {
     size_t fsum, rsum, ckpt, bc, dA, dD, db, total;
 };
 
-inline BwdLayout bwd_layout(const Plan& p, int64_t Bsz, int64_t L, int64_t Dch, int64_t N) {
+// Forward launch plan: one warp per (batch, CH-channel tile, time chunk).
+struct FPlan {
+    int64_t tiles;   // channel tiles of CH = 32 / G channels
+    int64_t K;       // time chunks
+    int64_t Lc;      // chunk length (multiple of 32); the last chunk may be shorter
+};
+
+constexpr int64_t kFwdTargetWarps = 1216;  // 8 warps on each of 152 SMs
+constexpr int64_t kFwdMinChunk = 128;
+
+// A pure function of the sizes (the same sizes always chunk the same way).
+inline FPlan make_fplan(int64_t Bsz, int64_t L, int64_t Dch, int64_t N) {
+    FPlan p;
+    const int64_t S = N < 8 ? N : 8, G = N / S, CH = 32 / G;
+    p.tiles = ceil_div(Dch, CH);
+    const int64_t warps = Bsz * p.tiles;
+    int64_t K = 1;
+    if (warps > 0 && warps < kFwdTargetWarps) K = ceil_div(kFwdTargetWarps, warps);
+    const int64_t kmax = ceil_div(L, kFwdMinChunk);
+    if (K > kmax) K = kmax;
+    if (K < 1) K = 1;
+    p.Lc = ceil_div(ceil_div(L, K), 32) * 32;
+    if (p.Lc < 32) p.Lc = 32;
+    p.K = ceil_div(L, p.Lc);
+    if (p.K < 1) p.K = 1;
+    return p;
+}
+
+constexpr int kModeY = 0, kModeSummary = 1, kModeCkpt = 2;
+constexpr int kSub = 8;  // backward sub-chunk: steps whose decays and states stay in registers
+
+cudaError_t launch_fwd2(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt);
+cudaError_t launch_bwd2(const BwdArgs& a, const FPlan& p, cudaStream_t st);
+
+// Workspace of the backward (byte offsets, each 256-aligned): forward and
+// reverse chunk summaries (only when chunked), sub-chunk start states, per
+// channel-tile dB / dC partials, per-(batch, chunk) dA / dD / ddelta_bias partials.
+inline BwdLayout bwd_layout2(const FPlan& p, int64_t Bsz, int64_t L, int64_t Dch, int64_t N) {
     BwdLayout w;
     size_t off = 0;
     const size_t rows = (size_t)(Bsz * Dch);
@@ -47,7 +84,7 @@ inline BwdLayout bwd_layout(const Plan& p, int64_t Bsz, int64_t L, int64_t Dch, 
     };
     w.fsum = take(p.K > 1 ? rows * p.K * N * 2 * sizeof(float) : 0);
     w.rsum = take(p.K > 1 ? rows * p.K * N * sizeof(float) : 0);
-    w.ckpt = take(rows * p.K * p.nsub * N * sizeof(float));
+    w.ckpt = take(rows * p.K * (p.Lc / kSub) * N * sizeof(float));
     w.bc = take(2 * (size_t)p.tiles * Bsz * L * N * sizeof(float));
     w.dA = take((size_t)Bsz * p.K * Dch * N * sizeof(float));
     w.dD = take((size_t)Bsz * p.K * Dch * sizeof(float));
@@ -55,9 +92,5 @@ inline BwdLayout bwd_layout(const Plan& p, int64_t Bsz, int64_t L, int64_t Dch, 
     w.total = off;
     return w;
 }
-
-cudaError_t launch_fwd(const FwdArgs& a, const Plan& p, cudaStream_t st);
-cudaError_t launch_fwd_summary(const FwdArgs& a, const Plan& p, cudaStream_t st);
-cudaError_t launch_bwd(const BwdArgs& a, const Plan& p, cudaStream_t st);
 
 }  // namespace ss

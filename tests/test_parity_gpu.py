@@ -30,6 +30,8 @@ VARIANTS = {
     "full": dict(softplus=True, has_D=True, has_z=True, has_bias=True),
     "no_softplus": dict(softplus=False, has_D=True, has_z=True, has_bias=True),
     "bare": dict(softplus=True, has_D=False, has_z=False, has_bias=False),
+    # raw delta ~ N(0, 8^2), no bias: softplus inputs across [-30, 30], both tails
+    "wide_delta": dict(softplus=True, has_D=True, has_z=True, has_bias=False),
 }
 
 
@@ -37,6 +39,8 @@ def make(shape, io, variant, seed):
     Bsz, L, Dch, N = shape
     v = VARIANTS[variant]
     x = small_inputs(Bsz, L, Dch, N, io=io, seed=seed, has_D=v["has_D"], has_z=v["has_z"], has_bias=v["has_bias"])
+    if variant == "wide_delta":
+        x["delta"] = x["delta"] * np.float32(16.0)  # N(0, 0.5^2) -> N(0, 8^2); exact scaling by a power of two
     if not v["softplus"]:
         # Delta = delta + bias is used as is: keep it positive so exp(Delta*A) decays
         x["delta"] = np.abs(x["delta"]) * np.float32(0.5)
