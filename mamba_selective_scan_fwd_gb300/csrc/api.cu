@@ -9,7 +9,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/ss.h"
+#include "ss.h"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -96,7 +96,7 @@ int ss_fwd(const void* u, const void* delta, const float* A, const void* B, cons
         return SS_OK;
     }
     const FPlan p = make_fplan(Bsz, L, Dch, N);
-    if (p.tiles * Bsz * p.K >= (1ll << 31)) return SS_ERR_UNSUPPORTED;
+    if (ceil_div(Dch, 4) * Bsz * p.K >= (1ll << 31)) return SS_ERR_UNSUPPORTED;
     const size_t need = ss_fwd_workspace_bytes(Bsz, L, Dch, N, dtype);
     if (workspace_bytes < need || (need > 0 && workspace == nullptr)) return SS_ERR_WORKSPACE_TOO_SMALL;
     FwdArgs a;
@@ -147,7 +147,7 @@ int ss_bwd(const void* u, const void* delta, const float* A, const void* B, cons
         return SS_OK;
     }
     const FPlan p = make_fplan(Bsz, L, Dch, N);
-    if (p.tiles * Bsz * p.K >= (1ll << 31)) return SS_ERR_UNSUPPORTED;
+    if (ceil_div(Dch, 4) * Bsz * p.K >= (1ll << 31)) return SS_ERR_UNSUPPORTED;
     const BwdLayout w = bwd_layout2(p, Bsz, L, Dch, N);
     if (workspace_bytes < w.total || workspace == nullptr) return SS_ERR_WORKSPACE_TOO_SMALL;
     char* ws = static_cast<char*>(workspace);

@@ -39,10 +39,11 @@
 namespace ss {
 
 constexpr int kTT = 16;  // backward tile: steps staged per prologue
+constexpr int kRB = 4;   // steps whose dB / dC contributions are reduced together
 
 template <typename T, int N>
 struct BCfg {
-    static constexpr int S = N < 8 ? N : 8;
+    static constexpr int S = bwd_states_per_lane(N);
     static constexpr int G = N / S;
     static constexpr int CH = 32 / G;
     static constexpr int CPL = CH / 2;              // channels per prologue lane (two lanes per step)
@@ -50,7 +51,7 @@ struct BCfg {
     static constexpr int NB = N * (int)sizeof(T);
     static constexpr int NW = NB >= 4 ? NB / 4 : 1;
     static constexpr int NP = N + 4;
-    static constexpr int RP = N + 1;                // padded row of the per-step dB / dC scratch
+    static constexpr int RP = N >= 4 ? N + 4 : N + 1;  // padded row of the per-step dB / dC scratch
 };
 
 template <typename T>
@@ -145,6 +146,128 @@ __device__ __forceinline__ float gsum(float v) {
     return v;
 }
 
+template <int S>
+__device__ __forceinline__ void ld_state(const float* p, float (&v)[S]) {
+    if constexpr (S % 4 == 0) {
+#pragma unroll
+        for (int q = 0; q < S; q += 4) {
+            const float4 f = *reinterpret_cast<const float4*>(p + q);
+            v[q] = f.x; v[q + 1] = f.y; v[q + 2] = f.z; v[q + 3] = f.w;
+        }
+    } else {
+#pragma unroll
+        for (int s = 0; s < S; s++) v[s] = p[s];
+    }
+}
+
+// Stage one step's dB / dC contributions (slot j of kRB) in shared memory:
+// block (j, tau) holds CH rows of RP floats (the states), blocks padded by 4
+// floats so that the reduction's 16-byte reads of different blocks fall in
+// different banks.
+template <int S, int CH, int RP>
+__device__ __forceinline__ void stage_contrib(float* sR, int j, const float (&cB)[S], const float (&cC)[S],
+                                              bool ch_ok, int ch, int n0) {
+    constexpr int BLK = CH * RP + 4;
+    float* r0 = sR + (2 * j) * BLK + ch * RP + n0;
+    float* r1 = r0 + BLK;
+    if constexpr (S % 4 == 0 && RP % 4 == 0) {
+#pragma unroll
+        for (int s = 0; s < S; s += 4) {
+            *reinterpret_cast<float4*>(r0 + s) =
+                ch_ok ? make_float4(cB[s], cB[s + 1], cB[s + 2], cB[s + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<float4*>(r1 + s) =
+                ch_ok ? make_float4(cC[s], cC[s + 1], cC[s + 2], cC[s + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    } else {
+#pragma unroll
+        for (int s = 0; s < S; s++) {
+            r0[s] = ch_ok ? cB[s] : 0.f;
+            r1[s] = ch_ok ? cC[s] : 0.f;
+        }
+    }
+}
+
+// Sum the kRB staged steps (tile rows r .. r + kRB - 1, slot j holds row
+// r + j) over the CH channels, channel by channel in ascending order, into
+// sP[row][tau * N + n].  Work unit: 4 consecutive outputs of one (step, tensor).
+template <int CH, int N, int RP>
+__device__ __forceinline__ void reduce_staged(const float* sR, float (*sP)[2 * N], int r, int lane) {
+    constexpr int BLK = CH * RP + 4;
+    if constexpr (N % 4 == 0 && RP % 4 == 0) {
+        constexpr int UPB = N / 4;                 // units per (step, tensor) block
+        constexpr int UNITS = kRB * 2 * UPB;
+#pragma unroll
+        for (int u0 = 0; u0 < UNITS; u0 += 32) {
+            const int unit = u0 + lane;
+            if (UNITS % 32 == 0 || unit < UNITS) {
+                const int blk = unit / UPB, n4 = (unit % UPB) * 4;
+                const int j = blk / 2, tau = blk % 2;
+                const float* src = sR + blk * BLK + n4;
+                float2 lo = make_float2(0.f, 0.f), hi = lo;
+#pragma unroll
+                for (int c = 0; c < CH; c++) {
+                    const float4 v = *reinterpret_cast<const float4*>(src + c * RP);
+                    lo = add2(lo, make_float2(v.x, v.y));
+                    hi = add2(hi, make_float2(v.z, v.w));
+                }
+                *reinterpret_cast<float4*>(&sP[r + j][tau * N + n4]) = make_float4(lo.x, lo.y, hi.x, hi.y);
+            }
+        }
+    } else {
+        for (int o = lane; o < kRB * 2 * N; o += 32) {
+            const int blk = o / N, n = o % N;
+            const int j = blk / 2, tau = blk % 2;
+            const float* src = sR + blk * BLK + n;
+            float acc = 0.f;
+#pragma unroll 8
+            for (int c = 0; c < CH; c++) acc += src[c * RP];
+            sP[r + j][tau * N + n] = acc;
+        }
+    }
+}
+
+// CPL consecutive f32 outputs at p (channel c0 of the row): 16-byte stores
+// when aligned and complete, else element stores up to Dch.
+template <int CPL>
+__device__ __forceinline__ void store_half(float* p, const float (&v)[CPL], int64_t c0, int64_t Dch, bool fast) {
+    if constexpr (CPL % 4 == 0) {
+        if (fast) {
+#pragma unroll
+            for (int c = 0; c < CPL; c += 4)
+                *reinterpret_cast<float4*>(p + c) = make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
+            return;
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < CPL; c++)
+        if (c0 + c < Dch) p[c] = v[c];
+}
+
+// One tile's per-warp dB / dC step sums (rows of 2N floats in shared memory)
+// into the partial buffers bc0 (dB) and bc1 (dC), rows t0 .. t_end.
+template <int N>
+__device__ __forceinline__ void store_tile_partials(const float (*sP)[2 * N], float* bc0, float* bc1, int64_t t0,
+                                                    int64_t t_end, int lane) {
+    if constexpr (N % 4 == 0) {
+        constexpr int V = N / 4;  // float4 per row per tensor
+        for (int e = lane; e < kTT * 2 * V; e += 32) {
+            const int r = e / (2 * V), rem = e % (2 * V);
+            const int tau = rem / V, v = rem % V;
+            const int64_t t = t0 + r;
+            if (t < t_end) {
+                float* dst = (tau ? bc1 : bc0) + t * N + 4 * v;
+                *reinterpret_cast<float4*>(dst) = *reinterpret_cast<const float4*>(&sP[r][tau * N + 4 * v]);
+            }
+        }
+    } else {
+        for (int e = lane; e < kTT * 2 * N; e += 32) {
+            const int r = e / (2 * N), o = e % (2 * N);
+            const int64_t t = t0 + r;
+            if (t < t_end) (o >= N ? bc1 : bc0)[t * N + (o % N)] = sP[r][o];
+        }
+    }
+}
+
 // MODE kRevMain: the backward proper.  MODE kRevSummary: only the adjoint
 // walk of chunks 1..K-1 from a zero carry, writing M_k.
 constexpr int kRevMain = 0, kRevSummary = 1;
@@ -159,15 +282,17 @@ __global__ void __launch_bounds__(32) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, i
     __shared__ float4 sE[MAIN ? kTT : 1][CH];       // (sig(x), u, dz factor, -) swizzled columns
     __shared__ __align__(16) float sB[kTT][NP];
     __shared__ __align__(16) float sC[kTT][NP];
-    __shared__ float sR[MAIN ? 2 : 1][CH][RP];      // one step's dB / dC contributions
-    __shared__ float sP[MAIN ? kTT : 1][2 * N];     // the tile's dB / dC sums over this warp's channels
-    __shared__ float sBias[CH];
+    // dB / dC contributions of kRB steps: block (j, tau) holds CH rows of RP floats, blocks padded by 4 floats
+    __shared__ __align__(16) float sR[MAIN ? kRB * 2 * (CH * RP + 4) : 4];
+    __shared__ __align__(16) float sP[MAIN ? kTT : 1][2 * N];  // the tile's dB / dC sums over this warp's channels
+    __shared__ float4 sO[MAIN ? kTT : 1][CH];                  // per-step (sum lam B, sum A q, y0) of each channel
+    __shared__ float sBias[CH], sDv[CH];
 
     const FwdArgs& f = a.f;
     const int lane = threadIdx.x;
     int64_t blk = blockIdx.x;
-    const int64_t tile = blk % p.tiles;
-    blk /= p.tiles;
+    const int64_t tile = blk % p.tiles_b;
+    blk /= p.tiles_b;
     const int64_t nk = k_hi - k_lo;
     const int64_t k = k_lo + blk % nk;
     const int64_t b = blk / nk;
@@ -183,6 +308,7 @@ __global__ void __launch_bounds__(32) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, i
     if (lane < CH) {
         const int64_t dc = d0 + lane < Dch ? d0 + lane : Dch - 1;
         sBias[lane] = f.delta_bias ? f.delta_bias[dc] : 0.f;
+        sDv[lane] = f.D ? f.D[dc] : 0.f;
     }
 
     // scan-lane identity
@@ -208,18 +334,25 @@ __global__ void __launch_bounds__(32) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, i
             for (int s = 0; s < S; s++) carry[s] = fmaf(fs[j * N + s].x, carry[s], rs[j * N + s]);
         }
     }
-    float dD_acc = 0.f, db_acc = 0.f;
+    // per-channel dD / ddelta_bias partials of the epilogue lane (its CPL channels, its rows)
+    float eD[MAIN ? CPL : 1], eb[MAIN ? CPL : 1];
+#pragma unroll
+    for (int c = 0; c < (MAIN ? CPL : 1); c++) { eD[c] = 0.f; eb[c] = 0.f; }
 
     // prologue-lane identity: step pr of the tile, channels pc0 .. pc0 + CPL
     const int pr = lane % kTT, ph = lane / kTT;
     const int pc0 = ph * CPL;
     const bool pfast = ((Dch * (int64_t)sizeof(T)) % 16 == 0) && (d0 + CH <= Dch) &&
                        ((CPL * (int)sizeof(T)) % 4 == 0);
+    const bool ofast = (Dch % 4 == 0) && (d0 + CH <= Dch) && (CPL % 4 == 0);
 
     const int64_t t_begin = k * p.Lc;
     const int64_t t_end = t_begin + p.Lc < L ? t_begin + p.Lc : L;
     const int64_t ntile = (t_end - t_begin + kTT - 1) / kTT;
-    const float* ck = a.ws_ckpt + ((row * G + g) * p.K + k) * (p.Lc / kSub) * S;
+    const float* ck = a.ws_ckpt + (row * p.K + k) * (p.Lc / kSub) * N + n0;
+    const int64_t gbase = b * L * Dch + d;  // (b, t, d) of the per-step outputs is gbase + t * Dch
+    float* bc0 = a.ws_bc + ((int64_t)tile * f.Bsz + b) * L * N;                  // dB partials of this tile
+    float* bc1 = a.ws_bc + ((int64_t)(p.tiles_b + tile) * f.Bsz + b) * L * N;    // dC partials
 
     for (int64_t m = ntile - 1; m >= 0; m--) {
         const int64_t t0 = t_begin + m * kTT;
@@ -287,15 +420,16 @@ __global__ void __launch_bounds__(32) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, i
                 }
             }
         } else {
-            // ---- two sub-chunks of kSub steps, last one first
+            // ---- two sub-chunks of kSub steps, last one first.  Steps past the
+            // chunk end (last tile only) hold Delta = g = 0 and B = C = 0 in the
+            // staging: they leave the state and the adjoint unchanged and add
+            // nothing; only their per-step stores are skipped.
 #pragma unroll 1
             for (int sub = kTT / kSub - 1; sub >= 0; sub--) {
                 const int64_t ts = t0 + sub * kSub;
                 if (ts >= t_end) continue;
                 float hs[S];
-                const float* src = ck + ((ts - t_begin) / kSub) * S;
-#pragma unroll
-                for (int s = 0; s < S; s++) hs[s] = src[s];
+                ld_state<S>(ck + ((ts - t_begin) / kSub) * N, hs);
                 // recompute decays and states of the sub-chunk
                 float av[kSub][S], hv[kSub][S];
                 {
@@ -305,7 +439,7 @@ __global__ void __launch_bounds__(32) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, i
 #pragma unroll
                     for (int i = 0; i < kSub; i++) {
                         const int r = sub * kSub + i;
-                        const float4 ss = sS[r][ch ^ (r & (CH - 1))];  // padded steps hold Delta = 0
+                        const float4 ss = sS[r][ch ^ (r & (CH - 1))];
                         float Bv[S];
                         bld_shared<S>(&sB[r][n0], Bv);
                         if constexpr (S >= 2) {
@@ -331,12 +465,11 @@ __global__ void __launch_bounds__(32) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, i
                 for (int i = kSub - 1; i >= 0; i--) {
                     const int r = sub * kSub + i;
                     const int64_t t = t0 + r;
-                    if (t >= t_end) continue;
                     const float4 ss = sS[r][ch ^ (r & (CH - 1))];
                     float Bv[S], Cv[S];
                     bld_shared<S>(&sB[r][n0], Bv);
                     bld_shared<S>(&sC[r][n0], Cv);
-                    float du_p = 0.f, dd_p = 0.f, y0_p = 0.f;
+                    float du_p, dd_p, y0_p;
                     float cB[S], cC[S];
                     if constexpr (S >= 2) {
                         float2 dup = make_float2(0.f, 0.f), ddp = dup, y0p = dup;
@@ -379,41 +512,43 @@ __global__ void __launch_bounds__(32) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, i
                     du_p = gsum<G>(du_p);
                     dd_p = gsum<G>(dd_p);
                     y0_p = gsum<G>(y0_p);
-                    // per-(t, d) outputs
-                    if (ch_ok && g == 0) {
-                        const float4 se = sE[r][ch ^ (r & (CH - 1))];
-                        const int64_t idx = (b * L + t) * Dch + d;
-                        a.du[idx] = fmaf(ss.z, Dd, ss.x * du_p);
-                        const float dx = fmaf(se.y, du_p, dd_p) * se.x;
-                        a.ddelta[idx] = dx;
-                        if (z) a.dz[idx] = se.z * fmaf(Dd, se.y, y0_p);
-                        dD_acc = fmaf(ss.z, se.y, dD_acc);
-                        db_acc += dx;
+                    // per-step sums for the tile epilogue
+                    if (g == 0) sO[r][ch ^ (r & (CH - 1))] = make_float4(du_p, dd_p, y0_p, 0.f);
+                    // stage dB / dC contributions; every kRB steps sum them over the channels
+                    stage_contrib<S, CH, RP>(sR, i % kRB, cB, cC, ch_ok, ch, n0);
+                    if (i % kRB == 0) {
+                        __syncwarp();
+                        reduce_staged<CH, N, RP>(sR, sP, r, lane);
+                        __syncwarp();
                     }
-                    // dB / dC: this warp's channels, fixed order
-#pragma unroll
-                    for (int s = 0; s < S; s++) {
-                        sR[0][ch][n0 + s] = ch_ok ? cB[s] : 0.f;
-                        sR[1][ch][n0 + s] = ch_ok ? cC[s] : 0.f;
-                    }
-                    __syncwarp();
-                    for (int o = lane; o < 2 * N; o += 32) {
-                        const int tau = o / N, n = o % N;
-                        float acc = 0.f;
-#pragma unroll 8
-                        for (int c = 0; c < CH; c++) acc += sR[tau][c][n];
-                        sP[r][o] = acc;
-                    }
-                    __syncwarp();
                 }
             }
-            // this tile's per-warp dB / dC sums -> partial buffer
-            for (int e = lane; e < kTT * 2 * N; e += 32) {
-                const int r = e / (2 * N), o = e % (2 * N);
-                const int64_t t = t0 + r;
+            __syncwarp();
+            // this tile's per-warp dB / dC sums -> partial buffer (float4 rows of N/4)
+            store_tile_partials<N>(sP, bc0, bc1, t0, t_end, lane);
+            // ---- epilogue: du, ddelta, dz of step t0 + pr for channels pc0 .. pc0 + CPL
+            {
+                const int64_t t = t0 + pr;
+                const int swz = pr & (CH - 1);
+                float vdu[CPL], vdx[CPL], vdz[CPL];
+#pragma unroll
+                for (int c = 0; c < CPL; c++) {
+                    const int cc = pc0 + c;
+                    const float4 so = sO[pr][cc ^ swz];
+                    const float4 ss = sS[pr][cc ^ swz];
+                    const float4 se = sE[pr][cc ^ swz];
+                    vdu[c] = fmaf(ss.z, sDv[cc], ss.x * so.x);
+                    vdx[c] = fmaf(se.y, so.x, so.y) * se.x;
+                    vdz[c] = se.z * fmaf(sDv[cc], se.y, so.z);
+                    // padded steps carry g = 0 and sig = 0: they add nothing
+                    eD[c] = fmaf(ss.z, se.y, eD[c]);
+                    eb[c] += vdx[c];
+                }
                 if (t < t_end) {
-                    const int tau = o / N, n = o % N;
-                    a.ws_bc[(((int64_t)tau * p.tiles + tile) * f.Bsz + b) * L * N + t * N + n] = sP[r][o];
+                    const int64_t off = (b * L + t) * Dch + d0 + pc0;
+                    store_half<CPL>(a.du + off, vdu, d0 + pc0, Dch, ofast);
+                    store_half<CPL>(a.ddelta + off, vdx, d0 + pc0, Dch, ofast);
+                    if (z) store_half<CPL>(a.dz + off, vdz, d0 + pc0, Dch, ofast);
                 }
             }
         }
@@ -426,13 +561,32 @@ __global__ void __launch_bounds__(32) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, i
 #pragma unroll
             for (int s = 0; s < S; s++) out[s] = carry[s];
         }
-    } else if (ch_ok) {
-        float* o = a.ws_dA + ((b * p.K + k) * Dch + d) * N + n0;
+    } else {
+        if (ch_ok) {
+            float* o = a.ws_dA + ((b * p.K + k) * Dch + d) * N + n0;
 #pragma unroll
-        for (int s = 0; s < S; s++) o[s] = dA[s];
-        if (g == 0) {
-            a.ws_dD[(b * p.K + k) * Dch + d] = dD_acc;
-            a.ws_db[(b * p.K + k) * Dch + d] = db_acc;
+            for (int s = 0; s < S; s++) o[s] = dA[s];
+        }
+        // dD / ddelta_bias: the kTT lanes sharing a channel set hold partials over
+        // their rows; combine them (xor butterfly over the row bits, fixed order)
+#pragma unroll
+        for (int c = 0; c < CPL; c++) {
+#pragma unroll
+            for (int m = 1; m < kTT; m <<= 1) {
+                const float oD = __shfl_xor_sync(kFull, eD[c], m), ob = __shfl_xor_sync(kFull, eb[c], m);
+                const bool low = (pr & m) == 0;
+                eD[c] = low ? eD[c] + oD : oD + eD[c];
+                eb[c] = low ? eb[c] + ob : ob + eb[c];
+            }
+        }
+        if (pr == 0) {
+#pragma unroll
+            for (int c = 0; c < CPL; c++) {
+                if (d0 + pc0 + c < Dch) {
+                    a.ws_dD[(b * p.K + k) * Dch + d0 + pc0 + c] = eD[c];
+                    a.ws_db[(b * p.K + k) * Dch + d0 + pc0 + c] = eb[c];
+                }
+            }
         }
     }
 }
@@ -444,9 +598,9 @@ __global__ void k_bwd2_reduce_bc(BwdArgs a, FPlan p) {
     if (e >= 2 * bln) return;
     const int tensor = e >= bln ? 1 : 0;
     const int64_t r = e - tensor * bln;
-    const float* src = a.ws_bc + (size_t)tensor * p.tiles * bln + r;
+    const float* src = a.ws_bc + (size_t)tensor * p.tiles_b * bln + r;
     float acc = 0.f;
-    for (int64_t tl = 0; tl < p.tiles; tl++) acc += src[tl * bln];
+    for (int64_t tl = 0; tl < p.tiles_b; tl++) acc += src[tl * bln];
     (tensor ? a.dC : a.dB)[r] = acc;
 }
 
@@ -480,10 +634,10 @@ cudaError_t launch_bwd2_t(const BwdArgs& a, const FPlan& p, cudaStream_t st) {
     cudaError_t e = launch_fwd2(a.f, p, st, kModeCkpt, a.ws_ckpt);
     if (e != cudaSuccess) return e;
     if (p.K > 1) {
-        const int64_t blocks = p.tiles * a.f.Bsz * (p.K - 1);
+        const int64_t blocks = p.tiles_b * a.f.Bsz * (p.K - 1);
         k_bwd2<T, N, kRevSummary><<<(unsigned)blocks, 32, 0, st>>>(a, p, 1, p.K);
     }
-    const int64_t blocks = p.tiles * a.f.Bsz * p.K;
+    const int64_t blocks = p.tiles_b * a.f.Bsz * p.K;
     k_bwd2<T, N, kRevMain><<<(unsigned)blocks, 32, 0, st>>>(a, p, 0, p.K);
     const int64_t n_bc = 2 * a.f.Bsz * a.f.L * a.f.N;
     k_bwd2_reduce_bc<<<(unsigned)ceil_div(n_bc, 256), 256, 0, st>>>(a, p);

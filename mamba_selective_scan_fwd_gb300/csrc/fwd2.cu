@@ -28,9 +28,9 @@ namespace ss {
 
 constexpr int kRow = 32;  // time steps per tile
 
-template <typename T, int N>
+template <typename T, int N, int MODE>
 struct FCfg {
-    static constexpr int S = N < 8 ? N : 8;        // states per lane
+    static constexpr int S = fwd_states_per_lane(N, MODE);  // states per lane
     static constexpr int G = N / S;                 // lanes per channel
     static constexpr int CH = 32 / G;               // channels per warp
     static constexpr int ESZ = (int)sizeof(T);
@@ -115,11 +115,12 @@ __device__ __forceinline__ void ld_shared_row(const float* p, float (&v)[S]) {
 }
 
 template <typename T, int N, int MODE>
-__global__ void __launch_bounds__(32) k_fwd2(FwdArgs a, FPlan p, int64_t k_lo, int64_t k_hi, float* ckpt) {
+__global__ void __launch_bounds__(32) k_fwd2(FwdArgs a, FPlan p, int64_t ntiles, int64_t k_lo, int64_t k_hi,
+                                             float* ckpt) {
     constexpr bool SUMMARY = MODE == kModeSummary;
     constexpr bool CKPT = MODE == kModeCkpt;
     constexpr bool NOY = SUMMARY || CKPT;  // no readout, gate or y
-    using C = FCfg<T, N>;
+    using C = FCfg<T, N, MODE>;
     constexpr int S = C::S, G = C::G, CH = C::CH, RW = C::RW, NW = C::NW, NP = C::NP, YP = C::YP;
     __shared__ float2 sDU[kRow][CH];   // (delta_eff, delta_eff * u), column swizzled by row
     __shared__ float2 sGD[kRow][CH];   // (gate, D * u), column swizzled by row
@@ -130,8 +131,8 @@ __global__ void __launch_bounds__(32) k_fwd2(FwdArgs a, FPlan p, int64_t k_lo, i
 
     const int lane = threadIdx.x;
     int64_t blk = blockIdx.x;
-    const int64_t tile = blk % p.tiles;
-    blk /= p.tiles;
+    const int64_t tile = blk % ntiles;
+    blk /= ntiles;
     const int64_t nk = k_hi - k_lo;
     const int64_t k = k_lo + blk % nk;
     const int64_t b = blk / nk;
@@ -228,9 +229,15 @@ __global__ void __launch_bounds__(32) k_fwd2(FwdArgs a, FPlan p, int64_t k_lo, i
         for (int i = 0; i < kRow; i++) {
             if (CKPT && (i % kSub) == 0 && ch_ok && t0 + i < t_end) {
                 // state at the start of sub-chunk (t0 + i - t_begin) / kSub of this chunk
-                float* dst = ckpt + (((row * G + g) * p.K + k) * (p.Lc / kSub) + (t0 + i - t_begin) / kSub) * S;
+                float* dst = ckpt + ((row * p.K + k) * (p.Lc / kSub) + (t0 + i - t_begin) / kSub) * N + n0;
+                if constexpr (S % 4 == 0) {
 #pragma unroll
-                for (int s = 0; s < S; s++) dst[s] = h[s];
+                    for (int s = 0; s < S; s += 4)
+                        *reinterpret_cast<float4*>(dst + s) = make_float4(h[s], h[s + 1], h[s + 2], h[s + 3]);
+                } else {
+#pragma unroll
+                    for (int s = 0; s < S; s++) dst[s] = h[s];
+                }
             }
             const float2 du = sDU[i][ch ^ (i & (CH - 1))];
             float Bv[S], Cv[S];
@@ -312,17 +319,23 @@ __global__ void __launch_bounds__(32) k_fwd2(FwdArgs a, FPlan p, int64_t k_lo, i
     }
 }
 
+template <typename T, int N, int MODE>
+int64_t fwd_tiles(int64_t Dch) {
+    return ceil_div(Dch, FCfg<T, N, MODE>::CH);
+}
+
 template <typename T, int N>
 cudaError_t launch_fwd2_t(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt) {
     if (p.K > 1) {
-        const int64_t blocks = p.tiles * a.Bsz * (p.K - 1);
-        k_fwd2<T, N, kModeSummary><<<(unsigned)blocks, 32, 0, st>>>(a, p, 0, p.K - 1, nullptr);
+        const int64_t nt = fwd_tiles<T, N, kModeSummary>(a.Dch);
+        k_fwd2<T, N, kModeSummary><<<(unsigned)(nt * a.Bsz * (p.K - 1)), 32, 0, st>>>(a, p, nt, 0, p.K - 1, nullptr);
     }
-    const int64_t blocks = p.tiles * a.Bsz * p.K;
     if (mode == kModeCkpt) {
-        k_fwd2<T, N, kModeCkpt><<<(unsigned)blocks, 32, 0, st>>>(a, p, 0, p.K, ckpt);
+        const int64_t nt = fwd_tiles<T, N, kModeCkpt>(a.Dch);
+        k_fwd2<T, N, kModeCkpt><<<(unsigned)(nt * a.Bsz * p.K), 32, 0, st>>>(a, p, nt, 0, p.K, ckpt);
     } else {
-        k_fwd2<T, N, kModeY><<<(unsigned)blocks, 32, 0, st>>>(a, p, 0, p.K, nullptr);
+        const int64_t nt = fwd_tiles<T, N, kModeY>(a.Dch);
+        k_fwd2<T, N, kModeY><<<(unsigned)(nt * a.Bsz * p.K), 32, 0, st>>>(a, p, nt, 0, p.K, nullptr);
     }
     return cudaGetLastError();
 }

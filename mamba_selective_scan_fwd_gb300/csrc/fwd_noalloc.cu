@@ -27,7 +27,7 @@
 
 #include <mutex>
 
-#include "../../include/ss.h"
+#include "ss.h"
 #include "common.cuh"
 #include "kernels.h"
 

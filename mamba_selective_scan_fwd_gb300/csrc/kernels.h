@@ -24,7 +24,7 @@ struct BwdArgs {
     const void* dy;
     float *du, *ddelta, *dA, *dB, *dC, *dD, *dz, *ddelta_bias;
     float* ws_rsum;   // reverse chunk summaries M: [Bsz*Dch][K][N]
-    float* ws_ckpt;   // sub-chunk start states: [Bsz*Dch*G][K][Lc/kSub][S]
+    float* ws_ckpt;   // sub-chunk start states: [Bsz*Dch][K][Lc/kSub][N]
     float* ws_bc;     // per-tile dB/dC partials: [2][tiles][Bsz][L][N]
     float* ws_dA;     // per-(b,k) dA partials: [Bsz][K][Dch][N]
     float* ws_dD;     // per-(b,k) dD partials: [Bsz][K][Dch]
@@ -36,9 +36,22 @@ struct BwdLayout {
     size_t fsum, rsum, ckpt, bc, dA, dD, db, total;
 };
 
-// Forward launch plan: one warp per (batch, CH-channel tile, time chunk).
+constexpr int kModeY = 0, kModeSummary = 1, kModeCkpt = 2;
+
+// States held by one lane (S): G = N / S lanes share a channel and a warp
+// covers 32 / G channels.  The forward with readout and the backward keep 8
+// states per lane; the checkpoint walk (no readout) runs faster with 4.
+__host__ __device__ constexpr int fwd_states_per_lane(int64_t N, int mode) {
+    return mode == kModeCkpt ? (N < 4 ? (int)N : 4) : (N < 8 ? (int)N : 8);
+}
+__host__ __device__ constexpr int bwd_states_per_lane(int64_t N) { return N < 8 ? (int)N : 8; }
+__host__ __device__ constexpr int64_t channels_per_warp(int64_t N, int S) { return 32 / (N / S); }
+
+// Launch plan: one warp per (batch, channel tile, time chunk).  The time
+// chunking (K, Lc) is shared by every kernel of a call; each launcher derives
+// its own channel-tile count from its lanes per channel.
 struct FPlan {
-    int64_t tiles;   // channel tiles of CH = 32 / G channels
+    int64_t tiles_b; // channel tiles of the backward kernels (sizes the dB / dC partials)
     int64_t K;       // time chunks
     int64_t Lc;      // chunk length (multiple of 32); the last chunk may be shorter
 };
@@ -49,9 +62,8 @@ constexpr int64_t kFwdMinChunk = 128;
 // A pure function of the sizes (the same sizes always chunk the same way).
 inline FPlan make_fplan(int64_t Bsz, int64_t L, int64_t Dch, int64_t N) {
     FPlan p;
-    const int64_t S = N < 8 ? N : 8, G = N / S, CH = 32 / G;
-    p.tiles = ceil_div(Dch, CH);
-    const int64_t warps = Bsz * p.tiles;
+    p.tiles_b = ceil_div(Dch, channels_per_warp(N, bwd_states_per_lane(N)));
+    const int64_t warps = Bsz * ceil_div(Dch, channels_per_warp(N, fwd_states_per_lane(N, kModeY)));
     int64_t K = 1;
     if (warps > 0 && warps < kFwdTargetWarps) K = ceil_div(kFwdTargetWarps, warps);
     const int64_t kmax = ceil_div(L, kFwdMinChunk);
@@ -64,7 +76,6 @@ inline FPlan make_fplan(int64_t Bsz, int64_t L, int64_t Dch, int64_t N) {
     return p;
 }
 
-constexpr int kModeY = 0, kModeSummary = 1, kModeCkpt = 2;
 constexpr int kSub = 8;  // backward sub-chunk: steps whose decays and states stay in registers
 
 cudaError_t launch_fwd2(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt);
@@ -85,7 +96,7 @@ inline BwdLayout bwd_layout2(const FPlan& p, int64_t Bsz, int64_t L, int64_t Dch
     w.fsum = take(p.K > 1 ? rows * p.K * N * 2 * sizeof(float) : 0);
     w.rsum = take(p.K > 1 ? rows * p.K * N * sizeof(float) : 0);
     w.ckpt = take(rows * p.K * (p.Lc / kSub) * N * sizeof(float));
-    w.bc = take(2 * (size_t)p.tiles * Bsz * L * N * sizeof(float));
+    w.bc = take(2 * (size_t)p.tiles_b * Bsz * L * N * sizeof(float));
     w.dA = take((size_t)Bsz * p.K * Dch * N * sizeof(float));
     w.dD = take((size_t)Bsz * p.K * Dch * sizeof(float));
     w.db = take((size_t)Bsz * p.K * Dch * sizeof(float));
