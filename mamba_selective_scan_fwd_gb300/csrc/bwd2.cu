@@ -39,7 +39,7 @@
 namespace ss {
 
 constexpr int kTT = 16;  // backward tile: steps staged per prologue
-constexpr int kRB = 4;   // steps whose dB / dC contributions are reduced together
+constexpr int kRB = 2;   // steps whose dB / dC contributions are reduced together
 
 template <typename T, int N>
 struct BCfg {
@@ -273,13 +273,13 @@ __device__ __forceinline__ void store_tile_partials(const float (*sP)[2 * N], fl
 constexpr int kRevMain = 0, kRevSummary = 1;
 
 template <typename T, int N, int MODE>
-__global__ void __launch_bounds__(32) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_t k_hi) {
+__global__ void __maxnreg__(224) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_t k_hi) {
     using C = BCfg<T, N>;
     constexpr bool MAIN = MODE == kRevMain;
     constexpr int S = C::S, G = C::G, CH = C::CH, CPL = C::CPL, RWH = C::RWH, NWd = C::NW, NP = C::NP,
                   RP = C::RP;
-    __shared__ float4 sS[kTT][CH];                  // (Delta, Delta*u, g, -)    swizzled columns
-    __shared__ float4 sE[MAIN ? kTT : 1][CH];       // (sig(x), u, dz factor, -) swizzled columns
+    __shared__ float4 sS[kTT][CH];                  // (Delta, Delta*u, g, sig(x))  swizzled columns
+    __shared__ float2 sE[MAIN ? kTT : 1][CH];       // (u, dz factor)               swizzled columns
     __shared__ __align__(16) float sB[kTT][NP];
     __shared__ __align__(16) float sC[kTT][NP];
     // dB / dC contributions of kRB steps: block (j, tau) holds CH rows of RP floats, blocks padded by 4 floats
@@ -287,6 +287,7 @@ __global__ void __launch_bounds__(32) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, i
     __shared__ __align__(16) float sP[MAIN ? kTT : 1][2 * N];  // the tile's dB / dC sums over this warp's channels
     __shared__ float4 sO[MAIN ? kTT : 1][CH];                  // per-step (sum lam B, sum A q, y0) of each channel
     __shared__ float sBias[CH], sDv[CH];
+    __shared__ float sAcc[MAIN ? 32 : 1][2][CPL];                // per-lane dD / ddelta_bias partials
 
     const FwdArgs& f = a.f;
     const int lane = threadIdx.x;
@@ -318,11 +319,11 @@ __global__ void __launch_bounds__(32) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, i
     const int n0 = g * S;
     const int64_t row = b * Dch + d;
     const float Dd = f.D ? f.D[d] : 0.f;
-    float Av[S], A2[S], carry[S], dA[S];
+    // A2 = A * log2(e); the dDelta partial sum below uses A2 and is scaled back by ln 2 in the epilogue
+    float A2[S], carry[S], dA[S];
 #pragma unroll
     for (int s = 0; s < S; s++) {
-        Av[s] = f.A[d * N + n0 + s];
-        A2[s] = Av[s] * kLog2eF;
+        A2[s] = f.A[d * N + n0 + s] * kLog2eF;
         carry[s] = 0.f;
         dA[s] = 0.f;
     }
@@ -334,10 +335,12 @@ __global__ void __launch_bounds__(32) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, i
             for (int s = 0; s < S; s++) carry[s] = fmaf(fs[j * N + s].x, carry[s], rs[j * N + s]);
         }
     }
-    // per-channel dD / ddelta_bias partials of the epilogue lane (its CPL channels, its rows)
-    float eD[MAIN ? CPL : 1], eb[MAIN ? CPL : 1];
+    // per-channel dD / ddelta_bias partials of each epilogue lane (its CPL channels, its rows),
+    // kept in the lane's own shared slots between tiles
+    if (MAIN) {
 #pragma unroll
-    for (int c = 0; c < (MAIN ? CPL : 1); c++) { eD[c] = 0.f; eb[c] = 0.f; }
+        for (int c = 0; c < CPL; c++) { sAcc[lane][0][c] = 0.f; sAcc[lane][1][c] = 0.f; }
+    }
 
     // prologue-lane identity: step pr of the tile, channels pc0 .. pc0 + CPL
     const int pr = lane % kTT, ph = lane / kTT;
@@ -393,8 +396,8 @@ __global__ void __launch_bounds__(32) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, i
                         dzf = dyv * sz * fmaf(zz, 1.f - sz, 1.f);
                     }
                 }
-                sS[pr][cc ^ swz] = make_float4(dl, dl * uu, gg, 0.f);
-                if (MAIN) sE[pr][cc ^ swz] = make_float4(sgx, uu, dzf, 0.f);
+                sS[pr][cc ^ swz] = make_float4(dl, dl * uu, gg, sgx);
+                if (MAIN) sE[pr][cc ^ swz] = make_float2(uu, dzf);
             }
             if (ph == 1) {
 #pragma unroll
@@ -430,8 +433,8 @@ __global__ void __launch_bounds__(32) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, i
                 if (ts >= t_end) continue;
                 float hs[S];
                 ld_state<S>(ck + ((ts - t_begin) / kSub) * N, hs);
-                // recompute decays and states of the sub-chunk
-                float av[kSub][S], hv[kSub][S];
+                // recompute the states of the sub-chunk (the adjoint walk recomputes the decays)
+                float hv[kSub][S];
                 {
                     float hh[S];
 #pragma unroll
@@ -449,13 +452,11 @@ __global__ void __launch_bounds__(32) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, i
                                 const float2 da = make_float2(ex2a(e.x), ex2a(e.y));
                                 const float2 x = mul2(splat2(ss.y), make_float2(Bv[s], Bv[s + 1]));
                                 const float2 nh = fma2(da, make_float2(hh[s], hh[s + 1]), x);
-                                av[i][s] = da.x; av[i][s + 1] = da.y;
                                 hh[s] = nh.x; hh[s + 1] = nh.y;
                                 hv[i][s] = nh.x; hv[i][s + 1] = nh.y;
                             }
                         } else {
-                            av[i][0] = ex2a(ss.x * A2[0]);
-                            hh[0] = fmaf(av[i][0], hh[0], ss.y * Bv[0]);
+                            hh[0] = fmaf(ex2a(ss.x * A2[0]), hh[0], ss.y * Bv[0]);
                             hv[i][0] = hh[0];
                         }
                     }
@@ -482,9 +483,10 @@ __global__ void __launch_bounds__(32) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, i
                                                        : make_float2(hs[s], hs[s + 1]);
                             const float2 lam = fma2(g2, Cp, make_float2(carry[s], carry[s + 1]));
                             dup = fma2(lam, make_float2(Bv[s], Bv[s + 1]), dup);
-                            const float2 cn = mul2(make_float2(av[i][s], av[i][s + 1]), lam);
+                            const float2 e = mul2(dl2, make_float2(A2[s], A2[s + 1]));
+                            const float2 cn = mul2(make_float2(ex2a(e.x), ex2a(e.y)), lam);
                             const float2 q = mul2(cn, hprev);
-                            ddp = fma2(make_float2(Av[s], Av[s + 1]), q, ddp);
+                            ddp = fma2(make_float2(A2[s], A2[s + 1]), q, ddp);
                             const float2 na = fma2(dl2, q, make_float2(dA[s], dA[s + 1]));
                             dA[s] = na.x; dA[s + 1] = na.y;
                             y0p = fma2(Cp, hcur, y0p);
@@ -500,9 +502,9 @@ __global__ void __launch_bounds__(32) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, i
                         const float hprev = i > 0 ? hv[i - 1][0] : hs[0];
                         const float lam = fmaf(ss.z, Cv[0], carry[0]);
                         du_p = lam * Bv[0];
-                        const float cn = av[i][0] * lam;
+                        const float cn = ex2a(ss.x * A2[0]) * lam;
                         const float q = cn * hprev;
-                        dd_p = Av[0] * q;
+                        dd_p = A2[0] * q;
                         dA[0] = fmaf(ss.x, q, dA[0]);
                         y0_p = Cv[0] * hv[i][0];
                         cB[0] = lam * ss.y;
@@ -530,19 +532,29 @@ __global__ void __launch_bounds__(32) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, i
             {
                 const int64_t t = t0 + pr;
                 const int swz = pr & (CH - 1);
-                float vdu[CPL], vdx[CPL], vdz[CPL];
+                float vdu[CPL], vdx[CPL], vdz[CPL], eD[CPL], eb[CPL];
+#pragma unroll
+                for (int c = 0; c < CPL; c++) {
+                    eD[c] = sAcc[lane][0][c];
+                    eb[c] = sAcc[lane][1][c];
+                }
 #pragma unroll
                 for (int c = 0; c < CPL; c++) {
                     const int cc = pc0 + c;
                     const float4 so = sO[pr][cc ^ swz];
                     const float4 ss = sS[pr][cc ^ swz];
-                    const float4 se = sE[pr][cc ^ swz];
+                    const float2 se = sE[pr][cc ^ swz];
                     vdu[c] = fmaf(ss.z, sDv[cc], ss.x * so.x);
-                    vdx[c] = fmaf(se.y, so.x, so.y) * se.x;
-                    vdz[c] = se.z * fmaf(sDv[cc], se.y, so.z);
+                    vdx[c] = fmaf(se.x, so.x, so.y * kLn2) * ss.w;
+                    vdz[c] = se.y * fmaf(sDv[cc], se.x, so.z);
                     // padded steps carry g = 0 and sig = 0: they add nothing
-                    eD[c] = fmaf(ss.z, se.y, eD[c]);
+                    eD[c] = fmaf(ss.z, se.x, eD[c]);
                     eb[c] += vdx[c];
+                }
+#pragma unroll
+                for (int c = 0; c < CPL; c++) {
+                    sAcc[lane][0][c] = eD[c];
+                    sAcc[lane][1][c] = eb[c];
                 }
                 if (t < t_end) {
                     const int64_t off = (b * L + t) * Dch + d0 + pc0;
@@ -569,6 +581,12 @@ __global__ void __launch_bounds__(32) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, i
         }
         // dD / ddelta_bias: the kTT lanes sharing a channel set hold partials over
         // their rows; combine them (xor butterfly over the row bits, fixed order)
+        float eD[CPL], eb[CPL];
+#pragma unroll
+        for (int c = 0; c < CPL; c++) {
+            eD[c] = sAcc[lane][0][c];
+            eb[c] = sAcc[lane][1][c];
+        }
 #pragma unroll
         for (int c = 0; c < CPL; c++) {
 #pragma unroll
