@@ -273,7 +273,7 @@ __device__ __forceinline__ void store_tile_partials(const float (*sP)[2 * N], fl
 constexpr int kRevMain = 0, kRevSummary = 1;
 
 template <typename T, int N, int MODE>
-__global__ void __maxnreg__(224) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_t k_hi) {
+__global__ void __maxnreg__(184) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_t k_hi) {
     using C = BCfg<T, N>;
     constexpr bool MAIN = MODE == kRevMain;
     constexpr int S = C::S, G = C::G, CH = C::CH, CPL = C::CPL, RWH = C::RWH, NWd = C::NW, NP = C::NP,
@@ -287,7 +287,7 @@ __global__ void __maxnreg__(224) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_
     __shared__ __align__(16) float sP[MAIN ? kTT : 1][2 * N];  // the tile's dB / dC sums over this warp's channels
     __shared__ float4 sO[MAIN ? kTT : 1][CH];                  // per-step (sum lam B, sum A q, y0) of each channel
     __shared__ float sBias[CH], sDv[CH];
-    __shared__ float sAcc[MAIN ? 32 : 1][2][CPL];                // per-lane dD / ddelta_bias partials
+    __shared__ float sAcc[2][MAIN ? CPL : 1][32];                // per-lane dD / ddelta_bias partials (lane fastest)
 
     const FwdArgs& f = a.f;
     const int lane = threadIdx.x;
@@ -328,9 +328,14 @@ __global__ void __maxnreg__(224) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_
         dA[s] = 0.f;
     }
     if (MAIN && k + 1 < p.K) {
+        // carry into the end of chunk k: the last chunk's reverse summary, then
+        // rho_{j-1} = M_j + P_j rho_j down to j = k + 1 (the forward summaries
+        // hold P_j for chunks 0 .. K-2 only, and the last chunk needs none)
         const float2* fs = reinterpret_cast<const float2*>(f.ws_fsum) + row * p.K * N + n0;
         const float* rs = a.ws_rsum + row * p.K * N + n0;
-        for (int64_t j = p.K - 1; j > k; j--) {
+#pragma unroll
+        for (int s = 0; s < S; s++) carry[s] = rs[(p.K - 1) * N + s];
+        for (int64_t j = p.K - 2; j > k; j--) {
 #pragma unroll
             for (int s = 0; s < S; s++) carry[s] = fmaf(fs[j * N + s].x, carry[s], rs[j * N + s]);
         }
@@ -339,7 +344,7 @@ __global__ void __maxnreg__(224) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_
     // kept in the lane's own shared slots between tiles
     if (MAIN) {
 #pragma unroll
-        for (int c = 0; c < CPL; c++) { sAcc[lane][0][c] = 0.f; sAcc[lane][1][c] = 0.f; }
+        for (int c = 0; c < CPL; c++) { sAcc[0][c][lane] = 0.f; sAcc[1][c][lane] = 0.f; }
     }
 
     // prologue-lane identity: step pr of the tile, channels pc0 .. pc0 + CPL
@@ -535,8 +540,8 @@ __global__ void __maxnreg__(224) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_
                 float vdu[CPL], vdx[CPL], vdz[CPL], eD[CPL], eb[CPL];
 #pragma unroll
                 for (int c = 0; c < CPL; c++) {
-                    eD[c] = sAcc[lane][0][c];
-                    eb[c] = sAcc[lane][1][c];
+                    eD[c] = sAcc[0][c][lane];
+                    eb[c] = sAcc[1][c][lane];
                 }
 #pragma unroll
                 for (int c = 0; c < CPL; c++) {
@@ -553,8 +558,8 @@ __global__ void __maxnreg__(224) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_
                 }
 #pragma unroll
                 for (int c = 0; c < CPL; c++) {
-                    sAcc[lane][0][c] = eD[c];
-                    sAcc[lane][1][c] = eb[c];
+                    sAcc[0][c][lane] = eD[c];
+                    sAcc[1][c][lane] = eb[c];
                 }
                 if (t < t_end) {
                     const int64_t off = (b * L + t) * Dch + d0 + pc0;
@@ -584,8 +589,8 @@ __global__ void __maxnreg__(224) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_
         float eD[CPL], eb[CPL];
 #pragma unroll
         for (int c = 0; c < CPL; c++) {
-            eD[c] = sAcc[lane][0][c];
-            eb[c] = sAcc[lane][1][c];
+            eD[c] = sAcc[0][c][lane];
+            eb[c] = sAcc[1][c][lane];
         }
 #pragma unroll
         for (int c = 0; c < CPL; c++) {
@@ -656,6 +661,10 @@ cudaError_t launch_bwd2_t(const BwdArgs& a, const FPlan& p, cudaStream_t st) {
         k_bwd2<T, N, kRevSummary><<<(unsigned)blocks, 32, 0, st>>>(a, p, 1, p.K);
     }
     const int64_t blocks = p.tiles_b * a.f.Bsz * p.K;
+    // prefer the largest shared-memory carveout so that shared memory does not cap residency
+    e = cudaFuncSetAttribute(k_bwd2<T, N, kRevMain>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
     k_bwd2<T, N, kRevMain><<<(unsigned)blocks, 32, 0, st>>>(a, p, 0, p.K);
     const int64_t n_bc = 2 * a.f.Bsz * a.f.L * a.f.N;
     k_bwd2_reduce_bc<<<(unsigned)ceil_div(n_bc, 256), 256, 0, st>>>(a, p);

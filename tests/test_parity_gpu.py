@@ -138,3 +138,38 @@ def test_unsupported_state_size_raises():
     Bm = torch.randn((1, 4, 3), device=dev)
     with pytest.raises(ss.SSError):
         ss.ss_fwd(u, u, A, Bm, Bm)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [(1, 1000, 2, 16), (1, 300, 3, 16), (2, 300, 70, 16), (3, 100, 130, 8)],
+                         ids=lambda s: f"B{s[0]}L{s[1]}D{s[2]}N{s[3]}")
+def test_no_read_of_unwritten_memory(shape, io):
+    """Every workspace byte the kernels read was written in the same call, and
+    every output element is written: a workspace and outputs filled with NaN
+    bit patterns give exactly the results of freshly zeroed ones."""
+    Bsz, L, Dch, N = shape
+    x, sp = make(shape, io, "full", 79)
+    t = to_device(x, io)
+    args = (t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"], sp)
+    dt = ss.binding.dtype_id(t["u"])
+
+    def run(fill):
+        wf = torch.full((max(ss.fwd_workspace_bytes(Bsz, L, Dch, N, dt), 1),), fill, dtype=torch.uint8, device="cuda")
+        wb = torch.full((max(ss.bwd_workspace_bytes(Bsz, L, Dch, N, dt), 1),), fill, dtype=torch.uint8, device="cuda")
+        y = torch.full_like(t["u"], float("nan") if fill else 0.0)
+        last = torch.full((Bsz, Dch, N), float("nan") if fill else 0.0, device="cuda")
+        y, last = ss.ss_fwd(*args, y=y, last_state=last, workspace=wf)
+        out = {"du": t["u"], "ddelta": t["delta"], "dA": t["A"], "dB": t["B"], "dC": t["C"], "dD": t["D"],
+               "dz": t["z"], "ddelta_bias": t["delta_bias"]}
+        out = {k: torch.full(v.shape, float("nan") if fill else 0.0, dtype=torch.float32, device="cuda")
+               for k, v in out.items()}
+        g = ss.ss_bwd(*args, t["dy"], out=out, workspace=wb)
+        torch.cuda.synchronize()
+        return y, last, g
+
+    y0, l0, g0 = run(0)
+    y1, l1, g1 = run(0xFF)
+    assert torch.equal(y0, y1) and torch.equal(l0, l1)
+    for k, v in g0.items():
+        assert torch.isfinite(v).all(), k
+        assert torch.equal(v, g1[k]), k
