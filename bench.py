@@ -1,6 +1,7 @@
-"""Benchmark of the selective-scan hot path: one step = ss_fwd + ss_bwd over
-one batch of the Mamba-2.8B-layer workload (Bsz=4, L=4096, Dch=5120, N=16,
-bf16 I/O, f32 state and gradients), through the C ABI.
+"""Benchmark of the selective-scan hot path: one training step = ss_fwd_save
+(forward, keeping the backward's restart states) + ss_bwd_saved (backward)
+over one batch of the Mamba-2.8B-layer workload (Bsz=4, L=4096, Dch=5120,
+N=16, bf16 I/O, f32 state and gradients), through the C ABI.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -48,6 +49,22 @@ def algorithmic_bytes(w):
     fwd = 4 * bld * e + 2 * bln * e + 4 * (dn + 2 * d) + 4 * w.Bsz * w.Dch * w.N
     bwd = 4 * bld * e + 3 * bld * 4 + 2 * bln * (e + 4) + 8 * (dn + 2 * d)
     return fwd, bwd
+
+
+# DRAM bytes (read + write) per launch of the timed kernels on this workload,
+# from one ncu capture (profiles/ holds the summaries and the commands), and
+# the digest of the kernel sources they were taken on: a source change since
+# then makes the figure stale, and it is reported as null.
+TRAFFIC = {}
+TRAFFIC_SRC_DIGEST = None
+
+
+def measured_traffic(kernel, w):
+    from mamba_selective_scan_fwd_gb300 import build
+
+    if TRAFFIC_SRC_DIGEST is None or build.source_digest() != TRAFFIC_SRC_DIGEST:
+        return None
+    return TRAFFIC.get((kernel, w.name))
 
 
 def load_peaks():
@@ -110,7 +127,9 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def dist_setup(n_gpus):
+def dist_setup(backend="nccl"):
+    """One process per GPU (torchrun env).  Replicas only: the process group
+    carries the barrier and the max-over-ranks timing, never data."""
     import torch
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -119,9 +138,12 @@ def dist_setup(n_gpus):
     if world > 1:
         import torch.distributed as dist
 
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    elif torch.cuda.is_available():
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group(backend)
+    elif backend == "nccl" and torch.cuda.is_available():
         torch.cuda.set_device(0)
     return world, rank, local
 
@@ -133,15 +155,20 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(x, world):
+def max_over_ranks(x, world, device="cuda"):
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
 
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(units_per_rank, world, ms):
+    """Whole-job rate: the units every replica processed over the slowest rank's time."""
+    return world * units_per_rank / (ms / 1e3)
 
 
 def run_ours(args):
@@ -150,7 +177,7 @@ def run_ours(args):
     import mamba_selective_scan_fwd_gb300 as ss
     from mamba_selective_scan_fwd_gb300 import binding
 
-    world, rank, local = dist_setup(args.gpus)
+    world, rank, local = dist_setup("nccl")
     dev = torch.device("cuda", local if world > 1 else 0)
     w = WORKLOAD
     x = make_inputs(w)
@@ -170,26 +197,39 @@ def run_ours(args):
     dtid = binding.dtype_id(d["u"])
     plan = ss.plan_info(w.Bsz, w.L, w.Dch, w.N, dtid)
     ws_f = torch.empty(max(ss.fwd_workspace_bytes(w.Bsz, w.L, w.Dch, w.N, dtid), 256), dtype=torch.uint8, device=dev)
-    ws_b = torch.empty(ss.bwd_workspace_bytes(w.Bsz, w.L, w.Dch, w.N, dtid), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(ss.bwd_saved_workspace_bytes(w.Bsz, w.L, w.Dch, w.N, dtid), dtype=torch.uint8, device=dev)
+    saved = torch.empty(ss.saved_bytes(w.Bsz, w.L, w.Dch, w.N, dtid), dtype=torch.uint8, device=dev)
     y = torch.empty((w.Bsz, w.L, w.Dch), dtype=io_dt, device=dev)
     last = torch.empty((w.Bsz, w.Dch, w.N), dtype=torch.float32, device=dev)
     grads = {}
     stream = torch.cuda.current_stream(dev)
 
-    def step():
-        ss.ss_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"], w.softplus, y=y,
-                  last_state=last, workspace=ws_f, stream=stream)
-        g = ss.ss_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"], w.softplus,
-                      d["dy"], out=grads, workspace=ws_b, stream=stream)
+    def fwd():
+        ss.ss_fwd_save(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"], w.softplus,
+                       y=y, last_state=last, saved=saved, workspace=ws_f, stream=stream)
+
+    def bwd():
+        g = ss.ss_bwd_saved(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"], w.softplus,
+                            d["dy"], saved, out=grads, workspace=ws_b, stream=stream)
         grads.update(g)
+
+    def step():
+        fwd()
+        bwd()
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
 
-    # ---- device-resident timing, per-call events on the launching stream
+    # ---- device-resident timing, per-call and per-kernel events on the launching stream
     K = args.steps
+    nf, nb = plan["fwd_kernels"], plan["bwd_saved_kernels"]
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    kev_f = [[torch.cuda.Event(enable_timing=True) for _ in range(nf + 1)] for _ in range(K)]
+    kev_b = [[torch.cuda.Event(enable_timing=True) for _ in range(nb + 1)] for _ in range(K)]
+    for e in [e for row in kev_f + kev_b for e in row]:
+        e.record(stream)  # creates the event handles the library records
+    torch.cuda.synchronize(dev)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local if world > 1 else 0)
     clocks.start()
@@ -199,22 +239,26 @@ def run_ours(args):
     start.record(stream)
     for i in range(K):
         evs[i][0].record(stream)
-        ss.ss_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"], w.softplus, y=y,
-                  last_state=last, workspace=ws_f, stream=stream)
+        binding.profile_events(kev_f[i])
+        fwd()
         evs[i][1].record(stream)
-        ss.ss_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"], w.softplus, d["dy"],
-                  out=grads, workspace=ws_b, stream=stream)
+        binding.profile_events(kev_b[i])
+        bwd()
         evs[i][2].record(stream)
     end.record(stream)
+    binding.profile_events([])
     torch.cuda.synchronize(dev)
     barrier(world)
     clk = clocks.stop()
     total_ms = start.elapsed_time(end)
     t_fwd = sum(e[0].elapsed_time(e[1]) for e in evs) / K
     t_bwd = sum(e[1].elapsed_time(e[2]) for e in evs) / K
+    # per-kernel averages: kernel j of a call runs between its events j and j + 1
+    k_fwd = [sum(r[j].elapsed_time(r[j + 1]) for r in kev_f) / K for j in range(nf)]
+    k_bwd = [sum(r[j].elapsed_time(r[j + 1]) for r in kev_b) / K for j in range(nb)]
     total_ms = max_over_ranks(total_ms, world)
     ms_per_step = total_ms / K
-    value = world * w.bld * K / (total_ms / 1e3)
+    value = job_throughput(w.bld * K, world, total_ms)
 
     # ---- end to end through the public API with host buffers
     in_keys = [k for k in ("u", "delta", "A", "B", "C", "D", "z", "delta_bias", "dy") if k in host]
@@ -248,11 +292,13 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     barrier(world)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
-    e2e_value = world * w.bld * e2e_steps / (e2e_ms / 1e3)
+    e2e_value = job_throughput(w.bld * e2e_steps, world, e2e_ms)
 
-    # ---- roofline of the dominant call (the backward) and of the forward
+    # ---- roofline of the dominant kernel (the backward's main kernel) and of the forward kernel
     hbm_peak, peak_kind = load_peaks()
     fwd_bytes, bwd_bytes = algorithmic_bytes(w)
+    # the main backward kernel writes everything but dB / dC and dA / dD / ddelta_bias (the reductions do)
+    bwd_main_bytes = bwd_bytes - 2 * w.Bsz * w.L * w.N * 4 - 4 * (w.Dch * w.N + 2 * w.Dch)
     props = torch.cuda.get_device_properties(dev)
     sms = props.multi_processor_count
     sm_mhz = clk.get("sm_mhz") or 2070.0
@@ -266,19 +312,27 @@ def run_ours(args):
             ach = bytes_ / (t_ms / 1e3) / 1e9
             return {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
                     "frac": round(ach / hbm_peak, 4), "peak_kind": f"{peak_kind} HBM copy",
-                    "roofline_ms": round(t_hbm * 1e3, 4)}
+                    "roofline_ms": round(t_hbm * 1e3, 4), "algorithmic_bytes": bytes_}
         ach = exps / (t_ms / 1e3) / 1e9
         pk = exp_peak / 1e9
         return {"bound": "alu", "achieved": round(ach, 1), "peak": round(pk, 1), "unit": "Gexp2/s",
                 "frac": round(ach / pk, 4),
                 "peak_kind": f"MUFU ex2: {sms} SMs x {EX2_PER_CLK_PER_SM:g}/clk x {sm_mhz:g} MHz (median sampled)",
-                "roofline_ms": round(t_sfu * 1e3, 4)}
+                "roofline_ms": round(t_sfu * 1e3, 4), "algorithmic_bytes": bytes_}
 
-    r_bwd = roof(bwd_bytes, t_bwd)
-    r_bwd.update({"kernel": "ss_bwd (k_bwd_main + 2 reductions)", "traffic": None, "ms": round(t_bwd, 4)})
-    r_fwd = roof(fwd_bytes, t_fwd)
-    r_fwd.update({"kernel": "ss_fwd (k_fwd_main)", "traffic": None, "ms": round(t_fwd, 4)})
-    t_roof = r_fwd["roofline_ms"] + r_bwd["roofline_ms"]
+    chunked = plan["chunks"] > 1
+    fwd_names = (["k_fwd2 chunk summary"] if chunked else []) + ["k_fwd2 (y + saved states)"]
+    bwd_names = (["k_bwd2 reverse summary"] if chunked else []) + ["k_bwd2 main", "k_bwd2_reduce_bc",
+                                                                   "k_bwd2_reduce_params"]
+    i_main = 1 if chunked else 0
+    r_bwd = roof(bwd_main_bytes, k_bwd[i_main])
+    r_bwd.update({"kernel": "k_bwd2 main (ss_bwd_saved)", "ms": round(k_bwd[i_main], 4),
+                  "traffic": measured_traffic("k_bwd2_main", w)})
+    r_fwd = roof(fwd_bytes, k_fwd[-1])
+    r_fwd.update({"kernel": "k_fwd2 (ss_fwd_save)", "ms": round(k_fwd[-1], 4),
+                  "traffic": measured_traffic("k_fwd2_y", w)})
+    t_roof = roof(fwd_bytes, t_fwd)["roofline_ms"] + roof(bwd_bytes, t_bwd)["roofline_ms"]
+    kernel_ms = {n: round(v, 4) for n, v in zip(fwd_names + bwd_names, k_fwd + k_bwd)}
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
@@ -291,10 +345,11 @@ def run_ours(args):
         "hbm_gbs": round((fwd_bytes + bwd_bytes) / (ms_per_step / 1e3) / 1e9, 1),
         "roofline": r_bwd, "roofline_fwd": r_fwd,
         "roofline_step_frac": round(t_roof / ms_per_step, 4),
+        "fwd_ms": round(t_fwd, 4), "bwd_ms": round(t_bwd, 4), "kernel_ms": kernel_ms,
         "clocks": clk,
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps},
-        "gpu_launches": K * (plan["fwd_kernels"] + plan["bwd_kernels"]),
+        "gpu_launches": K * (plan["fwd_kernels"] + plan["bwd_saved_kernels"]),
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, x, budget_s=args.cpu_seconds)

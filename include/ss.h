@@ -103,6 +103,25 @@ int ss_fwd_noalloc(const void *u, const void *delta, const float *A, const void 
                    const void *z, const float *delta_bias, int softplus, void *y, float *last_state, int64_t Bsz,
                    int64_t L, int64_t Dch, int64_t N, int dtype, void *stream);
 
+/*
+ * Forward for training: ss_fwd that also stores, in `saved`, the states the
+ * backward restarts its recomputation from, so that ss_bwd_saved can skip
+ * the forward walk ss_bwd has to redo.  The pages this library follows have
+ * a backward-owned record of every state (baracuda-kernels
+ * `selective_scan.rs`, "Workspace": B * D * L * N elements written by the
+ * backward's first pass); here the forward keeps one state in eight steps.
+ *   saved         device buffer of at least ss_saved_bytes(...) bytes, 16-byte
+ *                 aligned, fully overwritten (f32 h of every (b, d) row at
+ *                 every 8th step of each time chunk); opaque to the caller.
+ * All other arguments and results are those of ss_fwd.  A NULL or short
+ * `saved` gives SS_ERR_WORKSPACE_TOO_SMALL before anything is launched.
+ */
+size_t ss_saved_bytes(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype);
+int ss_fwd_save(const void *u, const void *delta, const float *A, const void *B, const void *C, const float *D,
+                const void *z, const float *delta_bias, int softplus, void *y, float *last_state, void *saved,
+                size_t saved_bytes, int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype, void *workspace,
+                size_t workspace_bytes, void *stream);
+
 /* Bytes of device workspace ss_bwd needs for these sizes.  A pure function
  * of its arguments. */
 size_t ss_bwd_workspace_bytes(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype);
@@ -129,17 +148,51 @@ int ss_bwd(const void *u, const void *delta, const float *A, const void *B, cons
            int64_t N, int dtype, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
- * Launch plan for these sizes, as ss_fwd / ss_bwd will use it: the number of
- * time chunks the sequence is cut into and how many kernels each call
- * enqueues (0 for an empty problem).  Pointers may be NULL.  Returns a status.
+ * ss_bwd reading the states ss_fwd_save stored instead of recomputing them.
+ *   saved         the buffer ss_fwd_save filled for THE SAME inputs (u, delta,
+ *                 A, B, delta_bias, softplus, sizes, dtype), at least
+ *                 ss_saved_bytes(...) bytes; read only.  Nothing can check
+ *                 that it matches: states of other inputs give the gradient
+ *                 of a different forward.  NULL or short: SS_ERR_WORKSPACE_TOO_SMALL.
+ *   workspace     device scratch of at least ss_bwd_saved_workspace_bytes(...)
+ *                 bytes (smaller than ss_bwd's: no room for the states).
+ * All other arguments and results are those of ss_bwd; the outputs are
+ * bit-identical to ss_bwd's.
+ */
+size_t ss_bwd_saved_workspace_bytes(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype);
+int ss_bwd_saved(const void *u, const void *delta, const float *A, const void *B, const void *C, const float *D,
+                 const void *z, const float *delta_bias, int softplus, const void *dy, const void *saved,
+                 size_t saved_bytes, float *du, float *ddelta, float *dA, float *dB, float *dC, float *dD, float *dz,
+                 float *ddelta_bias, int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype, void *workspace,
+                 size_t workspace_bytes, void *stream);
+
+/*
+ * Launch plan for these sizes: the number of time chunks the sequence is cut
+ * into and how many kernels each call enqueues (0 for an empty problem):
+ * ss_fwd and ss_fwd_save (fwd_kernels), ss_bwd (bwd_kernels), ss_bwd_saved
+ * (bwd_saved_kernels).  Pointers may be NULL.  Returns a status.
  */
 int ss_plan_info(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype, int64_t *chunks, int *fwd_kernels,
-                 int *bwd_kernels);
+                 int *bwd_kernels, int *bwd_saved_kernels);
+
+/*
+ * Measurement aid (not thread-safe; for benchmarks).  After a call with
+ * count > 0, every call of ss_fwd, ss_fwd_save, ss_bwd or ss_bwd_saved that
+ * returns SS_OK records events[0] on its stream before its first kernel,
+ * events[i] after its i-th kernel (in the order ss_plan_info counts them),
+ * stopping when the list is used up; the list stays set for later calls.
+ * events[] holds up to 16 caller-created cudaEvent_t handles (passed as
+ * void*) of the calling thread's current device.  count = 0 switches the
+ * recording off.  Returns SS_ERR_INVALID_PROBLEM for count outside 0..16 or
+ * a NULL handle.  The pages this library follows have no counterpart.
+ */
+int ss_profile_events(void *const *events, int count);
 
 /* Static description of a status code. */
 const char *ss_status_string(int status);
 
-/* ABI version; bumped on any incompatible change. */
+/* ABI version (2: ss_fwd_save / ss_bwd_saved added, ss_plan_info gained
+ * bwd_saved_kernels); bumped on any incompatible change. */
 int ss_abi_version(void);
 
 #ifdef __cplusplus

@@ -6,8 +6,10 @@ library is loaded on first use and every entry point raises if it is
 missing -- there is no other implementation to fall back on.
 """
 
-from .binding import (SS_BF16, SS_F16, SS_F32, SSError, bwd_workspace_bytes, fwd_workspace_bytes, lib, plan_info,
-                      ss_bwd, ss_fwd, status_string)
+from .binding import (SS_BF16, SS_F16, SS_F32, SSError, bwd_saved_workspace_bytes, bwd_workspace_bytes,
+                      fwd_workspace_bytes, lib, plan_info, saved_bytes, ss_bwd, ss_bwd_saved, ss_fwd, ss_fwd_noalloc,
+                      ss_fwd_save, status_string)
 
-__all__ = ["ss_fwd", "ss_bwd", "fwd_workspace_bytes", "bwd_workspace_bytes", "status_string", "plan_info", "lib", "SSError",
-           "SS_F32", "SS_F16", "SS_BF16"]
+__all__ = ["ss_fwd", "ss_fwd_save", "ss_fwd_noalloc", "ss_bwd", "ss_bwd_saved", "fwd_workspace_bytes",
+           "bwd_workspace_bytes", "saved_bytes", "bwd_saved_workspace_bytes", "status_string", "plan_info", "lib",
+           "SSError", "SS_F32", "SS_F16", "SS_BF16"]

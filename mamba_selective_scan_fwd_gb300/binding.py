@@ -21,7 +21,9 @@ STATUS_NAMES = {0: "SS_OK", 1: "SS_ERR_INVALID_PROBLEM", 2: "SS_ERR_UNSUPPORTED"
 
 # Every function include/ss.h declares.
 EXPORTS = ["ss_fwd", "ss_bwd", "ss_fwd_workspace_bytes", "ss_bwd_workspace_bytes", "ss_plan_info",
-           "ss_status_string", "ss_abi_version", "ss_fwd_noalloc"]
+           "ss_status_string", "ss_abi_version", "ss_fwd_noalloc", "ss_saved_bytes", "ss_fwd_save",
+           "ss_bwd_saved_workspace_bytes", "ss_bwd_saved", "ss_profile_events"]
+ABI_VERSION = 2
 
 # Size of the library-owned scratch behind ss_fwd_noalloc (SS_FWD_NOALLOC_MAX_SCRATCH_BYTES).
 FWD_NOALLOC_MAX_SCRATCH_BYTES = 2 << 20
@@ -53,11 +55,18 @@ def lib() -> ctypes.CDLL:
     L.ss_fwd.argtypes = [_P] * 8 + [ctypes.c_int, _P, _P] + [_I64] * 4 + [ctypes.c_int, _P, _SZ, _P]
     L.ss_bwd.restype = ctypes.c_int
     L.ss_bwd.argtypes = [_P] * 8 + [ctypes.c_int] + [_P] * 9 + [_I64] * 4 + [ctypes.c_int, _P, _SZ, _P]
-    for fn in ("ss_fwd_workspace_bytes", "ss_bwd_workspace_bytes"):
+    L.ss_fwd_save.restype = ctypes.c_int
+    L.ss_fwd_save.argtypes = [_P] * 8 + [ctypes.c_int, _P, _P, _P, _SZ] + [_I64] * 4 + [ctypes.c_int, _P, _SZ, _P]
+    L.ss_bwd_saved.restype = ctypes.c_int
+    L.ss_bwd_saved.argtypes = ([_P] * 8 + [ctypes.c_int, _P, _P, _SZ] + [_P] * 8 + [_I64] * 4 +
+                               [ctypes.c_int, _P, _SZ, _P])
+    for fn in ("ss_fwd_workspace_bytes", "ss_bwd_workspace_bytes", "ss_saved_bytes", "ss_bwd_saved_workspace_bytes"):
         getattr(L, fn).restype = _SZ
         getattr(L, fn).argtypes = [_I64] * 4 + [ctypes.c_int]
     L.ss_plan_info.restype = ctypes.c_int
-    L.ss_plan_info.argtypes = [_I64] * 4 + [ctypes.c_int, _P, _P, _P]
+    L.ss_plan_info.argtypes = [_I64] * 4 + [ctypes.c_int, _P, _P, _P, _P]
+    L.ss_profile_events.restype = ctypes.c_int
+    L.ss_profile_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
     L.ss_status_string.restype = ctypes.c_char_p
     L.ss_status_string.argtypes = [ctypes.c_int]
     L.ss_abi_version.restype = ctypes.c_int
@@ -119,14 +128,33 @@ def bwd_workspace_bytes(Bsz, L, Dch, N, dtype) -> int:
     return int(lib().ss_bwd_workspace_bytes(Bsz, L, Dch, N, dtype))
 
 
+def saved_bytes(Bsz, L, Dch, N, dtype) -> int:
+    """Bytes of the saved-state buffer ss_fwd_save writes and ss_bwd_saved reads."""
+    return int(lib().ss_saved_bytes(Bsz, L, Dch, N, dtype))
+
+
+def bwd_saved_workspace_bytes(Bsz, L, Dch, N, dtype) -> int:
+    return int(lib().ss_bwd_saved_workspace_bytes(Bsz, L, Dch, N, dtype))
+
+
 def plan_info(Bsz, L, Dch, N, dtype) -> dict:
-    """Chunk count and kernels per call that ss_fwd / ss_bwd use for these sizes."""
+    """Chunk count and kernels per call that the entry points use for these sizes."""
     k = ctypes.c_int64()
     nf = ctypes.c_int()
     nb = ctypes.c_int()
+    ns = ctypes.c_int()
     _check("ss_plan_info", lib().ss_plan_info(Bsz, L, Dch, N, dtype, ctypes.byref(k), ctypes.byref(nf),
-                                              ctypes.byref(nb)))
-    return {"chunks": k.value, "fwd_kernels": nf.value, "bwd_kernels": nb.value}
+                                              ctypes.byref(nb), ctypes.byref(ns)))
+    return {"chunks": k.value, "fwd_kernels": nf.value, "bwd_kernels": nb.value, "bwd_saved_kernels": ns.value}
+
+
+def profile_events(events):
+    """Make the following entry-point calls record ``events`` (torch.cuda.Event
+    objects with timing enabled, already recorded once so that they exist)
+    around their kernels: events[0] before the first, events[i] after the
+    i-th.  An empty list switches the recording off."""
+    handles = (ctypes.c_void_p * max(1, len(events)))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    _check("ss_profile_events", lib().ss_profile_events(handles, len(events)))
 
 
 def _workspace(nbytes, device, workspace):
@@ -138,9 +166,11 @@ def _workspace(nbytes, device, workspace):
     return workspace, size
 
 
-def ss_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, y=None, last_state=None,
-           return_last_state=True, workspace=None, stream=None):
-    """Forward selective scan.  Returns (y, last_state or None)."""
+def _nbytes(t):
+    return 0 if t is None else t.numel() * t.element_size()
+
+
+def _fwd_prepare(u, delta, A, B, C, D, z, delta_bias, y, last_state, return_last_state):
     import torch
 
     Bsz, L, Dch = u.shape
@@ -165,12 +195,40 @@ def ss_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, y=
         last_state = torch.empty((Bsz, Dch, N), dtype=torch.float32, device=dev)
     if last_state is not None:
         _require(last_state, "last_state", (Bsz, Dch, N), torch.float32, dev)
+    return (Bsz, L, Dch, N), y, last_state
+
+
+def ss_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, y=None, last_state=None,
+           return_last_state=True, workspace=None, stream=None):
+    """Forward selective scan.  Returns (y, last_state or None)."""
+    (Bsz, L, Dch, N), y, last_state = _fwd_prepare(u, delta, A, B, C, D, z, delta_bias, y, last_state,
+                                                   return_last_state)
     dt = dtype_id(u)
-    workspace, wsb = _workspace(fwd_workspace_bytes(Bsz, L, Dch, N, dt), dev, workspace)
+    workspace, wsb = _workspace(fwd_workspace_bytes(Bsz, L, Dch, N, dt), u.device, workspace)
     rc = lib().ss_fwd(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias), int(bool(softplus)),
                       _p(y), _p(last_state), Bsz, L, Dch, N, dt, _p(workspace), wsb, stream_handle(stream))
     _check("ss_fwd", rc)
     return y, last_state
+
+
+def ss_fwd_save(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, y=None, last_state=None,
+                saved=None, return_last_state=True, workspace=None, stream=None):
+    """Forward that also fills ``saved`` (uint8 device buffer of saved_bytes(...)
+    bytes, allocated when None) with the states ss_bwd_saved restarts from.
+    Returns (y, last_state or None, saved)."""
+    import torch
+
+    (Bsz, L, Dch, N), y, last_state = _fwd_prepare(u, delta, A, B, C, D, z, delta_bias, y, last_state,
+                                                   return_last_state)
+    dt = dtype_id(u)
+    if saved is None:
+        saved = torch.empty(max(saved_bytes(Bsz, L, Dch, N, dt), 16), dtype=torch.uint8, device=u.device)
+    workspace, wsb = _workspace(fwd_workspace_bytes(Bsz, L, Dch, N, dt), u.device, workspace)
+    rc = lib().ss_fwd_save(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias),
+                           int(bool(softplus)), _p(y), _p(last_state), _p(saved), _nbytes(saved), Bsz, L, Dch, N,
+                           dt, _p(workspace), wsb, stream_handle(stream))
+    _check("ss_fwd_save", rc)
+    return y, last_state, saved
 
 
 def ss_fwd_noalloc(u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state=None, stream=None):
@@ -191,9 +249,7 @@ def ss_fwd_noalloc(u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state=
 GRAD_SHAPES = ("du", "ddelta", "dA", "dB", "dC", "dD", "dz", "ddelta_bias")
 
 
-def ss_bwd(u, delta, A, B, C, D, z, delta_bias, softplus, dy, out=None, workspace=None, stream=None):
-    """Backward selective scan.  Returns a dict du, ddelta, dA, dB, dC, dD, dz,
-    ddelta_bias (f32; the optional ones are None when their input is None)."""
+def _bwd_prepare(u, delta, A, B, C, D, z, delta_bias, dy, out):
     import torch
 
     Bsz, L, Dch = u.shape
@@ -222,11 +278,32 @@ def ss_bwd(u, delta, A, B, C, D, z, delta_bias, softplus, dy, out=None, workspac
         if out.get(k) is None:
             out[k] = torch.empty(shp, dtype=f32, device=dev)
         _require(out[k], k, shp, f32, dev)
+    return (Bsz, L, Dch, N), out
+
+
+def _grad_ptrs(out):
+    return [_p(out[k]) for k in GRAD_SHAPES]
+
+
+def ss_bwd(u, delta, A, B, C, D, z, delta_bias, softplus, dy, out=None, workspace=None, stream=None):
+    """Backward selective scan.  Returns a dict du, ddelta, dA, dB, dC, dD, dz,
+    ddelta_bias (f32; the optional ones are None when their input is None)."""
+    (Bsz, L, Dch, N), out = _bwd_prepare(u, delta, A, B, C, D, z, delta_bias, dy, out)
     dt = dtype_id(u)
-    workspace, wsb = _workspace(bwd_workspace_bytes(Bsz, L, Dch, N, dt), dev, workspace)
+    workspace, wsb = _workspace(bwd_workspace_bytes(Bsz, L, Dch, N, dt), u.device, workspace)
     rc = lib().ss_bwd(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias), int(bool(softplus)),
-                      _p(dy), _p(out["du"]), _p(out["ddelta"]), _p(out["dA"]), _p(out["dB"]), _p(out["dC"]),
-                      _p(out["dD"]), _p(out["dz"]), _p(out["ddelta_bias"]), Bsz, L, Dch, N, dt, _p(workspace), wsb,
-                      stream_handle(stream))
+                      _p(dy), *_grad_ptrs(out), Bsz, L, Dch, N, dt, _p(workspace), wsb, stream_handle(stream))
     _check("ss_bwd", rc)
+    return out
+
+
+def ss_bwd_saved(u, delta, A, B, C, D, z, delta_bias, softplus, dy, saved, out=None, workspace=None, stream=None):
+    """ss_bwd reading the states ss_fwd_save stored in ``saved`` for the same inputs."""
+    (Bsz, L, Dch, N), out = _bwd_prepare(u, delta, A, B, C, D, z, delta_bias, dy, out)
+    dt = dtype_id(u)
+    workspace, wsb = _workspace(bwd_saved_workspace_bytes(Bsz, L, Dch, N, dt), u.device, workspace)
+    rc = lib().ss_bwd_saved(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias),
+                            int(bool(softplus)), _p(dy), _p(saved), _nbytes(saved), *_grad_ptrs(out), Bsz, L, Dch, N,
+                            dt, _p(workspace), wsb, stream_handle(stream))
+    _check("ss_bwd_saved", rc)
     return out

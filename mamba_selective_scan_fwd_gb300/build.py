@@ -43,6 +43,11 @@ def _digest() -> str:
     return h.hexdigest()
 
 
+def source_digest() -> str:
+    """Digest of the kernel sources and build flags: changes whenever the compiled kernels may change."""
+    return _digest()[:16]
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile every translation unit and link libss.so; skipped when up to date."""
     os.makedirs(BUILD, exist_ok=True)

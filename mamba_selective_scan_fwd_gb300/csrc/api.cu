@@ -31,60 +31,22 @@ int check_sizes(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype) {
     return SS_OK;
 }
 
-}  // namespace
+// ss_profile_events state: the caller's events and the next one to record.
+constexpr int kMaxProfEvents = 16;
+cudaEvent_t g_prof_ev[kMaxProfEvents];
+int g_prof_n = 0;
+int g_prof_next = 0;
 
-extern "C" {
-
-int ss_abi_version(void) { return 1; }
-
-const char* ss_status_string(int status) {
-    switch (status) {
-        case SS_OK: return "ok";
-        case SS_ERR_INVALID_PROBLEM: return "invalid problem (negative extent, missing pointer or optional-term mismatch)";
-        case SS_ERR_UNSUPPORTED: return "unsupported (dtype, state size, size limit or pointer alignment)";
-        case SS_ERR_WORKSPACE_TOO_SMALL: return "workspace too small (query ss_*_workspace_bytes)";
-        case SS_ERR_CUDA: return "CUDA runtime error";
-        default: return "unknown status";
-    }
-}
-
-size_t ss_fwd_workspace_bytes(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype) {
-    if (check_sizes(Bsz, L, Dch, N, dtype) != SS_OK) return 0;
-    if (Bsz == 0 || L == 0 || Dch == 0) return 0;
-    const FPlan p = make_fplan(Bsz, L, Dch, N);
-    if (p.K <= 1) return 0;
-    return align_up((size_t)Bsz * Dch * p.K * N * 2 * sizeof(float), 256);
-}
-
-size_t ss_bwd_workspace_bytes(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype) {
-    if (check_sizes(Bsz, L, Dch, N, dtype) != SS_OK) return 0;
-    if (Bsz == 0 || L == 0 || Dch == 0) return 0;
-    const FPlan p = make_fplan(Bsz, L, Dch, N);
-    return bwd_layout2(p, Bsz, L, Dch, N).total;
-}
-
-int ss_plan_info(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype, int64_t* chunks, int* fwd_kernels,
-                 int* bwd_kernels) {
-    int rc = check_sizes(Bsz, L, Dch, N, dtype);
-    if (rc != SS_OK) return rc;
-    const bool empty = Bsz == 0 || L == 0 || Dch == 0;
-    const FPlan fp = make_fplan(Bsz, L, Dch, N);
-    if (chunks) *chunks = empty ? 0 : fp.K;
-    // forward: [summary if K > 1] + main;
-    // backward: [forward summary if K > 1] + checkpoints + [reverse summary if K > 1] + main + 2 reductions
-    if (fwd_kernels) *fwd_kernels = empty ? 0 : (fp.K > 1 ? 2 : 1);
-    if (bwd_kernels) *bwd_kernels = empty ? 0 : (fp.K > 1 ? 6 : 4);
-    return SS_OK;
-}
-
-int ss_fwd(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
-           const void* z, const float* delta_bias, int softplus, void* y, float* last_state, int64_t Bsz, int64_t L,
-           int64_t Dch, int64_t N, int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+// Forward with optional checkpoint output (saved == nullptr: plain forward).
+int fwd_impl(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
+             const void* z, const float* delta_bias, int softplus, void* y, float* last_state, int64_t Bsz, int64_t L,
+             int64_t Dch, int64_t N, int dtype, bool save, void* saved, size_t saved_bytes, void* workspace,
+             size_t workspace_bytes, void* stream) {
     int rc = check_sizes(Bsz, L, Dch, N, dtype);
     if (rc != SS_OK) return rc;
     const bool empty = Bsz == 0 || L == 0 || Dch == 0;
     if (!empty && (!u || !delta || !A || !B || !C || !y)) return SS_ERR_INVALID_PROBLEM;
-    const void* ptrs[] = {u, delta, A, B, C, D, z, delta_bias, y, last_state, workspace};
+    const void* ptrs[] = {u, delta, A, B, C, D, z, delta_bias, y, last_state, saved, workspace};
     for (const void* q : ptrs)
         if (!aligned16(q)) return SS_ERR_UNSUPPORTED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -97,6 +59,10 @@ int ss_fwd(const void* u, const void* delta, const float* A, const void* B, cons
     }
     const FPlan p = make_fplan(Bsz, L, Dch, N);
     if (ceil_div(Dch, 4) * Bsz * p.K >= (1ll << 31)) return SS_ERR_UNSUPPORTED;
+    if (save) {
+        const size_t need_s = ckpt_bytes(p, Bsz, Dch, N);
+        if (saved == nullptr || saved_bytes < need_s) return SS_ERR_WORKSPACE_TOO_SMALL;
+    }
     const size_t need = ss_fwd_workspace_bytes(Bsz, L, Dch, N, dtype);
     if (workspace_bytes < need || (need > 0 && workspace == nullptr)) return SS_ERR_WORKSPACE_TOO_SMALL;
     FwdArgs a;
@@ -107,13 +73,16 @@ int ss_fwd(const void* u, const void* delta, const float* A, const void* B, cons
     a.softplus = softplus ? 1 : 0;
     a.dtype = dtype;
     a.ws_fsum = static_cast<float*>(workspace);
-    return launch_fwd2(a, p, st, kModeY, nullptr) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+    float* ck = save ? static_cast<float*>(saved) : nullptr;
+    return launch_fwd2(a, p, st, kModeY, ck) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
-int ss_bwd(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
-           const void* z, const float* delta_bias, int softplus, const void* dy, float* du, float* ddelta, float* dA,
-           float* dB, float* dC, float* dD, float* dz, float* ddelta_bias, int64_t Bsz, int64_t L, int64_t Dch,
-           int64_t N, int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+// Backward; with saved != nullptr the checkpoints come from ss_fwd_save.
+int bwd_impl(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
+             const void* z, const float* delta_bias, int softplus, const void* dy, float* du, float* ddelta,
+             float* dA, float* dB, float* dC, float* dD, float* dz, float* ddelta_bias, int64_t Bsz, int64_t L,
+             int64_t Dch, int64_t N, int dtype, bool from_saved, const void* saved, size_t saved_bytes,
+             void* workspace, size_t workspace_bytes, void* stream) {
     int rc = check_sizes(Bsz, L, Dch, N, dtype);
     if (rc != SS_OK) return rc;
     if ((D == nullptr) != (dD == nullptr) || (z == nullptr) != (dz == nullptr) ||
@@ -124,7 +93,7 @@ int ss_bwd(const void* u, const void* delta, const float* A, const void* B, cons
         return SS_ERR_INVALID_PROBLEM;
     if (empty && Dch > 0 && N > 0 && !dA) return SS_ERR_INVALID_PROBLEM;
     const void* ptrs[] = {u, delta, A, B, C, D, z, delta_bias, dy, du, ddelta, dA, dB, dC, dD, dz, ddelta_bias,
-                          workspace};
+                          saved, workspace};
     for (const void* q : ptrs)
         if (!aligned16(q)) return SS_ERR_UNSUPPORTED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -148,7 +117,9 @@ int ss_bwd(const void* u, const void* delta, const float* A, const void* B, cons
     }
     const FPlan p = make_fplan(Bsz, L, Dch, N);
     if (ceil_div(Dch, 4) * Bsz * p.K >= (1ll << 31)) return SS_ERR_UNSUPPORTED;
-    const BwdLayout w = bwd_layout2(p, Bsz, L, Dch, N);
+    if (from_saved && (saved == nullptr || saved_bytes < ckpt_bytes(p, Bsz, Dch, N)))
+        return SS_ERR_WORKSPACE_TOO_SMALL;
+    const BwdLayout w = bwd_layout2(p, Bsz, L, Dch, N, from_saved);
     if (workspace_bytes < w.total || workspace == nullptr) return SS_ERR_WORKSPACE_TOO_SMALL;
     char* ws = static_cast<char*>(workspace);
     BwdArgs a;
@@ -163,12 +134,140 @@ int ss_bwd(const void* u, const void* delta, const float* A, const void* B, cons
     a.du = du; a.ddelta = ddelta; a.dA = dA; a.dB = dB; a.dC = dC; a.dD = dD; a.dz = dz;
     a.ddelta_bias = ddelta_bias;
     a.ws_rsum = reinterpret_cast<float*>(ws + w.rsum);
-    a.ws_ckpt = reinterpret_cast<float*>(ws + w.ckpt);
+    float* ckpt_out = from_saved ? nullptr : reinterpret_cast<float*>(ws + w.ckpt);
+    a.ws_ckpt = from_saved ? static_cast<const float*>(saved) : ckpt_out;
     a.ws_bc = reinterpret_cast<float*>(ws + w.bc);
     a.ws_dA = reinterpret_cast<float*>(ws + w.dA);
     a.ws_dD = reinterpret_cast<float*>(ws + w.dD);
     a.ws_db = reinterpret_cast<float*>(ws + w.db);
-    return launch_bwd2(a, p, st) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+    return launch_bwd2(a, p, st, ckpt_out) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}
+
+// An entry point's launches between prof_begin and prof_end.
+void prof_begin() { g_prof_next = 0; }
+int prof_end(cudaStream_t st, int rc) {
+    if (rc == SS_OK) ss::prof_mark(st);
+    return rc;
+}
+
+}  // namespace
+
+namespace ss {
+void prof_mark(cudaStream_t st) {
+    if (g_prof_next < g_prof_n) cudaEventRecord(g_prof_ev[g_prof_next++], st);
+}
+}  // namespace ss
+
+extern "C" {
+
+int ss_profile_events(void* const* events, int count) {
+    if (count < 0 || count > kMaxProfEvents || (count > 0 && events == nullptr)) return SS_ERR_INVALID_PROBLEM;
+    for (int i = 0; i < count; i++)
+        if (events[i] == nullptr) return SS_ERR_INVALID_PROBLEM;
+    for (int i = 0; i < count; i++) g_prof_ev[i] = static_cast<cudaEvent_t>(events[i]);
+    g_prof_n = count;
+    g_prof_next = 0;
+    return SS_OK;
+}
+
+int ss_abi_version(void) { return 2; }
+
+const char* ss_status_string(int status) {
+    switch (status) {
+        case SS_OK: return "ok";
+        case SS_ERR_INVALID_PROBLEM: return "invalid problem (negative extent, missing pointer or optional-term mismatch)";
+        case SS_ERR_UNSUPPORTED: return "unsupported (dtype, state size, size limit or pointer alignment)";
+        case SS_ERR_WORKSPACE_TOO_SMALL: return "workspace or saved-state buffer too small (query its *_bytes function)";
+        case SS_ERR_CUDA: return "CUDA runtime error";
+        default: return "unknown status";
+    }
+}
+
+size_t ss_fwd_workspace_bytes(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype) {
+    if (check_sizes(Bsz, L, Dch, N, dtype) != SS_OK) return 0;
+    if (Bsz == 0 || L == 0 || Dch == 0) return 0;
+    const FPlan p = make_fplan(Bsz, L, Dch, N);
+    if (p.K <= 1) return 0;
+    return align_up((size_t)Bsz * Dch * p.K * N * 2 * sizeof(float), 256);
+}
+
+size_t ss_bwd_workspace_bytes(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype) {
+    if (check_sizes(Bsz, L, Dch, N, dtype) != SS_OK) return 0;
+    if (Bsz == 0 || L == 0 || Dch == 0) return 0;
+    const FPlan p = make_fplan(Bsz, L, Dch, N);
+    return bwd_layout2(p, Bsz, L, Dch, N, false).total;
+}
+
+size_t ss_saved_bytes(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype) {
+    if (check_sizes(Bsz, L, Dch, N, dtype) != SS_OK) return 0;
+    if (Bsz == 0 || L == 0 || Dch == 0) return 0;
+    return ckpt_bytes(make_fplan(Bsz, L, Dch, N), Bsz, Dch, N);
+}
+
+size_t ss_bwd_saved_workspace_bytes(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype) {
+    if (check_sizes(Bsz, L, Dch, N, dtype) != SS_OK) return 0;
+    if (Bsz == 0 || L == 0 || Dch == 0) return 0;
+    const FPlan p = make_fplan(Bsz, L, Dch, N);
+    return bwd_layout2(p, Bsz, L, Dch, N, true).total;
+}
+
+int ss_plan_info(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype, int64_t* chunks, int* fwd_kernels,
+                 int* bwd_kernels, int* bwd_saved_kernels) {
+    int rc = check_sizes(Bsz, L, Dch, N, dtype);
+    if (rc != SS_OK) return rc;
+    const bool empty = Bsz == 0 || L == 0 || Dch == 0;
+    const FPlan fp = make_fplan(Bsz, L, Dch, N);
+    const int chunked = fp.K > 1 ? 1 : 0;
+    if (chunks) *chunks = empty ? 0 : fp.K;
+    // forward (with or without saving): [summary if K > 1] + main;
+    // backward: [forward summary if K > 1] + checkpoints + [reverse summary if K > 1] + main + 2 reductions;
+    // backward from saved states: [reverse summary if K > 1] + main + 2 reductions
+    if (fwd_kernels) *fwd_kernels = empty ? 0 : 1 + chunked;
+    if (bwd_kernels) *bwd_kernels = empty ? 0 : 4 + 2 * chunked;
+    if (bwd_saved_kernels) *bwd_saved_kernels = empty ? 0 : 3 + chunked;
+    return SS_OK;
+}
+
+int ss_fwd(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
+           const void* z, const float* delta_bias, int softplus, void* y, float* last_state, int64_t Bsz, int64_t L,
+           int64_t Dch, int64_t N, int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    prof_begin();
+    return prof_end(static_cast<cudaStream_t>(stream),
+                    fwd_impl(u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state, Bsz, L, Dch, N, dtype,
+                             false, nullptr, 0, workspace, workspace_bytes, stream));
+}
+
+int ss_fwd_save(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
+                const void* z, const float* delta_bias, int softplus, void* y, float* last_state, void* saved,
+                size_t saved_bytes, int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype, void* workspace,
+                size_t workspace_bytes, void* stream) {
+    prof_begin();
+    return prof_end(static_cast<cudaStream_t>(stream),
+                    fwd_impl(u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state, Bsz, L, Dch, N, dtype,
+                             true, saved, saved_bytes, workspace, workspace_bytes, stream));
+}
+
+int ss_bwd(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
+           const void* z, const float* delta_bias, int softplus, const void* dy, float* du, float* ddelta, float* dA,
+           float* dB, float* dC, float* dD, float* dz, float* ddelta_bias, int64_t Bsz, int64_t L, int64_t Dch,
+           int64_t N, int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    prof_begin();
+    return prof_end(static_cast<cudaStream_t>(stream),
+                    bwd_impl(u, delta, A, B, C, D, z, delta_bias, softplus, dy, du, ddelta, dA, dB, dC, dD, dz,
+                             ddelta_bias, Bsz, L, Dch, N, dtype, false, nullptr, 0, workspace, workspace_bytes,
+                             stream));
+}
+
+int ss_bwd_saved(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
+                 const void* z, const float* delta_bias, int softplus, const void* dy, const void* saved,
+                 size_t saved_bytes, float* du, float* ddelta, float* dA, float* dB, float* dC, float* dD, float* dz,
+                 float* ddelta_bias, int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+    prof_begin();
+    return prof_end(static_cast<cudaStream_t>(stream),
+                    bwd_impl(u, delta, A, B, C, D, z, delta_bias, softplus, dy, du, ddelta, dA, dB, dC, dD, dz,
+                             ddelta_bias, Bsz, L, Dch, N, dtype, true, saved, saved_bytes, workspace,
+                             workspace_bytes, stream));
 }
 
 }  // extern "C"

@@ -28,10 +28,11 @@
 //     shared memory in a fixed order; a second kernel adds the per-tile
 //     partials, a third the per-(batch, chunk) dA / dD / ddelta_bias
 //     partials.  Every sum has a fixed order: the result is bit-reproducible.
-// Chunks (only when batch x channels cannot fill the GPU): the forward
-// summaries (P, H) give each chunk's carry-in state; reverse summaries
-// M_k = a_{s_k} lam_{s_k} (lam from a zero incoming carry) combine as
-// rho_{k-1} = M_k + P_k rho_k into each chunk's carry-in adjoint.
+// Chunks (only when batch x channels cannot fill the GPU): each chunk's
+// carry-in state is its first checkpoint; reverse summaries (P_k, M_k) -- the
+// chunk's decay product and M_k = a_{s_k} lam_{s_k} with lam from a zero
+// incoming carry -- combine as rho_{k-1} = M_k + P_k rho_k into each chunk's
+// carry-in adjoint.
 #include "common.cuh"
 #include "kernels.h"
 #include "simd.cuh"
@@ -39,7 +40,7 @@
 namespace ss {
 
 constexpr int kTT = 16;  // backward tile: steps staged per prologue
-constexpr int kRB = 2;   // steps whose dB / dC contributions are reduced together
+constexpr int kRB = 4;   // steps whose dB / dC contributions are reduced together
 
 template <typename T, int N>
 struct BCfg {
@@ -51,8 +52,19 @@ struct BCfg {
     static constexpr int NB = N * (int)sizeof(T);
     static constexpr int NW = NB >= 4 ? NB / 4 : 1;
     static constexpr int NP = N + 4;
-    static constexpr int RP = N >= 4 ? N + 4 : N + 1;  // padded row of the per-step dB / dC scratch
+    // dB / dC staging: block (step slot j, tensor tau) holds CH rows of N
+    // floats, padded by N floats so that the blocks read by one quarter warp
+    // in the reduction start in different bank groups
+    static constexpr int BLK = CH * N + (N >= 8 ? N : 1);
 };
+
+// 16-byte column swizzle of the dB / dC staging rows (N >= 8, 8 states per
+// lane): the eight lanes of a quarter warp cover 8 / G channels x G state
+// groups, whose unswizzled 16-byte columns coincide in pairs; flipping the
+// lowest column bit on every other such channel makes the eight stores hit
+// eight different bank groups, and a row stays contiguous for the reduction.
+template <int N>
+__device__ __forceinline__ int bc_swz(int ch) { return ((ch * N / 32) & 1) << 2; }
 
 template <typename T>
 __device__ __forceinline__ float belem(const uint32_t* w, int j) {
@@ -161,39 +173,41 @@ __device__ __forceinline__ void ld_state(const float* p, float (&v)[S]) {
 }
 
 // Stage one step's dB / dC contributions (slot j of kRB) in shared memory:
-// block (j, tau) holds CH rows of RP floats (the states), blocks padded by 4
-// floats so that the reduction's 16-byte reads of different blocks fall in
-// different banks.
-template <int S, int CH, int RP>
+// block (j, tau) holds CH rows of N floats (the states) with the 16-byte
+// columns of a row swizzled by bc_swz.
+template <int S, int CH, int N, int BLK>
 __device__ __forceinline__ void stage_contrib(float* sR, int j, const float (&cB)[S], const float (&cC)[S],
                                               bool ch_ok, int ch, int n0) {
-    constexpr int BLK = CH * RP + 4;
-    float* r0 = sR + (2 * j) * BLK + ch * RP + n0;
+    float* r0 = sR + (2 * j) * BLK + ch * N;
     float* r1 = r0 + BLK;
-    if constexpr (S % 4 == 0 && RP % 4 == 0) {
+    if constexpr (S == 8 && N % 8 == 0) {
+        const int sw = bc_swz<N>(ch);
 #pragma unroll
         for (int s = 0; s < S; s += 4) {
-            *reinterpret_cast<float4*>(r0 + s) =
+            const int col = (n0 + s) ^ sw;
+            *reinterpret_cast<float4*>(r0 + col) =
                 ch_ok ? make_float4(cB[s], cB[s + 1], cB[s + 2], cB[s + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
-            *reinterpret_cast<float4*>(r1 + s) =
+            *reinterpret_cast<float4*>(r1 + col) =
                 ch_ok ? make_float4(cC[s], cC[s + 1], cC[s + 2], cC[s + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
     } else {
 #pragma unroll
         for (int s = 0; s < S; s++) {
-            r0[s] = ch_ok ? cB[s] : 0.f;
-            r1[s] = ch_ok ? cC[s] : 0.f;
+            r0[n0 + s] = ch_ok ? cB[s] : 0.f;
+            r1[n0 + s] = ch_ok ? cC[s] : 0.f;
         }
     }
 }
 
-// Sum the kRB staged steps (tile rows r .. r + kRB - 1, slot j holds row
-// r + j) over the CH channels, channel by channel in ascending order, into
-// sP[row][tau * N + n].  Work unit: 4 consecutive outputs of one (step, tensor).
-template <int CH, int N, int RP>
-__device__ __forceinline__ void reduce_staged(const float* sR, float (*sP)[2 * N], int r, int lane) {
-    constexpr int BLK = CH * RP + 4;
-    if constexpr (N % 4 == 0 && RP % 4 == 0) {
+// Sum the kRB staged steps (slot j holds time step t + j) over the CH
+// channels and store the sums as this warp's dB / dC partial rows bc0[t + j],
+// bc1[t + j] (rows of N floats; steps at or past t_end are not stored).  Work
+// unit: 4 consecutive states of one (step, tensor); the channels are added as
+// a fixed pairwise tree (c, c + 1), then pairs of pairs, ...
+template <int S, int CH, int N, int BLK>
+__device__ __forceinline__ void reduce_staged(const float* sR, float* bc0, float* bc1, int64_t t, int64_t t_end,
+                                              int lane) {
+    if constexpr (S == 8 && N % 8 == 0) {
         constexpr int UPB = N / 4;                 // units per (step, tensor) block
         constexpr int UNITS = kRB * 2 * UPB;
 #pragma unroll
@@ -202,15 +216,25 @@ __device__ __forceinline__ void reduce_staged(const float* sR, float (*sP)[2 * N
             if (UNITS % 32 == 0 || unit < UNITS) {
                 const int blk = unit / UPB, n4 = (unit % UPB) * 4;
                 const int j = blk / 2, tau = blk % 2;
-                const float* src = sR + blk * BLK + n4;
-                float2 lo = make_float2(0.f, 0.f), hi = lo;
+                const float* src = sR + blk * BLK;
+                float2 lo[CH], hi[CH];
 #pragma unroll
                 for (int c = 0; c < CH; c++) {
-                    const float4 v = *reinterpret_cast<const float4*>(src + c * RP);
-                    lo = add2(lo, make_float2(v.x, v.y));
-                    hi = add2(hi, make_float2(v.z, v.w));
+                    const float4 v = *reinterpret_cast<const float4*>(src + c * N + (n4 ^ bc_swz<N>(c)));
+                    lo[c] = make_float2(v.x, v.y);
+                    hi[c] = make_float2(v.z, v.w);
                 }
-                *reinterpret_cast<float4*>(&sP[r + j][tau * N + n4]) = make_float4(lo.x, lo.y, hi.x, hi.y);
+#pragma unroll
+                for (int w = 1; w < CH; w <<= 1) {
+#pragma unroll
+                    for (int c = 0; c < CH; c += 2 * w) {
+                        lo[c] = add2(lo[c], lo[c + w]);
+                        hi[c] = add2(hi[c], hi[c + w]);
+                    }
+                }
+                if (t + j < t_end)
+                    *reinterpret_cast<float4*>((tau ? bc1 : bc0) + (t + j) * N + n4) =
+                        make_float4(lo[0].x, lo[0].y, hi[0].x, hi[0].y);
             }
         }
     } else {
@@ -220,8 +244,8 @@ __device__ __forceinline__ void reduce_staged(const float* sR, float (*sP)[2 * N
             const float* src = sR + blk * BLK + n;
             float acc = 0.f;
 #pragma unroll 8
-            for (int c = 0; c < CH; c++) acc += src[c * RP];
-            sP[r + j][tau * N + n] = acc;
+            for (int c = 0; c < CH; c++) acc += src[c * N];
+            if (t + j < t_end) (tau ? bc1 : bc0)[(t + j) * N + n] = acc;
         }
     }
 }
@@ -243,48 +267,22 @@ __device__ __forceinline__ void store_half(float* p, const float (&v)[CPL], int6
         if (c0 + c < Dch) p[c] = v[c];
 }
 
-// One tile's per-warp dB / dC step sums (rows of 2N floats in shared memory)
-// into the partial buffers bc0 (dB) and bc1 (dC), rows t0 .. t_end.
-template <int N>
-__device__ __forceinline__ void store_tile_partials(const float (*sP)[2 * N], float* bc0, float* bc1, int64_t t0,
-                                                    int64_t t_end, int lane) {
-    if constexpr (N % 4 == 0) {
-        constexpr int V = N / 4;  // float4 per row per tensor
-        for (int e = lane; e < kTT * 2 * V; e += 32) {
-            const int r = e / (2 * V), rem = e % (2 * V);
-            const int tau = rem / V, v = rem % V;
-            const int64_t t = t0 + r;
-            if (t < t_end) {
-                float* dst = (tau ? bc1 : bc0) + t * N + 4 * v;
-                *reinterpret_cast<float4*>(dst) = *reinterpret_cast<const float4*>(&sP[r][tau * N + 4 * v]);
-            }
-        }
-    } else {
-        for (int e = lane; e < kTT * 2 * N; e += 32) {
-            const int r = e / (2 * N), o = e % (2 * N);
-            const int64_t t = t0 + r;
-            if (t < t_end) (o >= N ? bc1 : bc0)[t * N + (o % N)] = sP[r][o];
-        }
-    }
-}
-
 // MODE kRevMain: the backward proper.  MODE kRevSummary: only the adjoint
 // walk of chunks 1..K-1 from a zero carry, writing M_k.
 constexpr int kRevMain = 0, kRevSummary = 1;
 
 template <typename T, int N, int MODE>
-__global__ void __maxnreg__(184) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_t k_hi) {
+__global__ void __maxnreg__(224) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_t k_hi) {
     using C = BCfg<T, N>;
     constexpr bool MAIN = MODE == kRevMain;
     constexpr int S = C::S, G = C::G, CH = C::CH, CPL = C::CPL, RWH = C::RWH, NWd = C::NW, NP = C::NP,
-                  RP = C::RP;
+                  BLK = C::BLK;
     __shared__ float4 sS[kTT][CH];                  // (Delta, Delta*u, g, sig(x))  swizzled columns
     __shared__ float2 sE[MAIN ? kTT : 1][CH];       // (u, dz factor)               swizzled columns
     __shared__ __align__(16) float sB[kTT][NP];
     __shared__ __align__(16) float sC[kTT][NP];
-    // dB / dC contributions of kRB steps: block (j, tau) holds CH rows of RP floats, blocks padded by 4 floats
-    __shared__ __align__(16) float sR[MAIN ? kRB * 2 * (CH * RP + 4) : 4];
-    __shared__ __align__(16) float sP[MAIN ? kTT : 1][2 * N];  // the tile's dB / dC sums over this warp's channels
+    // dB / dC contributions of kRB steps: block (j, tau) holds CH swizzled rows of N floats
+    __shared__ __align__(16) float sR[MAIN ? kRB * 2 * BLK : 4];
     __shared__ float4 sO[MAIN ? kTT : 1][CH];                  // per-step (sum lam B, sum A q, y0) of each channel
     __shared__ float sBias[CH], sDv[CH];
     __shared__ float sAcc[2][MAIN ? CPL : 1][32];                // per-lane dD / ddelta_bias partials (lane fastest)
@@ -320,24 +318,24 @@ __global__ void __maxnreg__(184) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_
     const int64_t row = b * Dch + d;
     const float Dd = f.D ? f.D[d] : 0.f;
     // A2 = A * log2(e); the dDelta partial sum below uses A2 and is scaled back by ln 2 in the epilogue
-    float A2[S], carry[S], dA[S];
+    float A2[S], carry[S], dA[S], Pr[MAIN ? 1 : S];
 #pragma unroll
     for (int s = 0; s < S; s++) {
         A2[s] = f.A[d * N + n0 + s] * kLog2eF;
         carry[s] = 0.f;
         dA[s] = 0.f;
+        if (!MAIN) Pr[s] = 1.f;
     }
     if (MAIN && k + 1 < p.K) {
-        // carry into the end of chunk k: the last chunk's reverse summary, then
-        // rho_{j-1} = M_j + P_j rho_j down to j = k + 1 (the forward summaries
-        // hold P_j for chunks 0 .. K-2 only, and the last chunk needs none)
-        const float2* fs = reinterpret_cast<const float2*>(f.ws_fsum) + row * p.K * N + n0;
-        const float* rs = a.ws_rsum + row * p.K * N + n0;
+        // carry into the end of chunk k: rho_{j-1} = M_j + P_j rho_j from the
+        // reverse summaries (P_j, M_j) of chunks K-1 .. k+1, with rho_{K-1} = 0
+        const float2* rs = reinterpret_cast<const float2*>(a.ws_rsum) + row * p.K * N + n0;
+        for (int64_t j = p.K - 1; j > k; j--) {
 #pragma unroll
-        for (int s = 0; s < S; s++) carry[s] = rs[(p.K - 1) * N + s];
-        for (int64_t j = p.K - 2; j > k; j--) {
-#pragma unroll
-            for (int s = 0; s < S; s++) carry[s] = fmaf(fs[j * N + s].x, carry[s], rs[j * N + s]);
+            for (int s = 0; s < S; s++) {
+                const float2 pm = rs[j * N + s];
+                carry[s] = fmaf(pm.x, carry[s], pm.y);
+            }
         }
     }
     // per-channel dD / ddelta_bias partials of each epilogue lane (its CPL channels, its rows),
@@ -357,7 +355,9 @@ __global__ void __maxnreg__(184) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_
     const int64_t t_begin = k * p.Lc;
     const int64_t t_end = t_begin + p.Lc < L ? t_begin + p.Lc : L;
     const int64_t ntile = (t_end - t_begin + kTT - 1) / kTT;
-    const float* ck = a.ws_ckpt + (row * p.K + k) * (p.Lc / kSub) * N + n0;
+    // checkpoints, step-major: [k * (Lc / kSub) + j][Bsz * Dch][N]
+    const int64_t ck_stride = f.Bsz * Dch * N;
+    const float* ck = a.ws_ckpt + (k * (p.Lc / kSub)) * ck_stride + row * N + n0;
     const int64_t gbase = b * L * Dch + d;  // (b, t, d) of the per-step outputs is gbase + t * Dch
     float* bc0 = a.ws_bc + ((int64_t)tile * f.Bsz + b) * L * N;                  // dB partials of this tile
     float* bc1 = a.ws_bc + ((int64_t)(p.tiles_b + tile) * f.Bsz + b) * L * N;    // dC partials
@@ -415,7 +415,8 @@ __global__ void __maxnreg__(184) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_
         __syncwarp();
 
         if constexpr (!MAIN) {
-            // ---- reverse summary: adjoint walk from a zero carry, no states needed
+            // ---- reverse summary: adjoint walk from a zero carry and the chunk's
+            // decay product, no states needed
             for (int i = kTT - 1; i >= 0; i--) {
                 if (t0 + i >= t_end) continue;
                 const float4 ss = sS[i][ch ^ (i & (CH - 1))];
@@ -424,7 +425,9 @@ __global__ void __maxnreg__(184) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_
 #pragma unroll
                 for (int s = 0; s < S; s++) {
                     const float lam = fmaf(ss.z, Cv[s], carry[s]);
-                    carry[s] = ex2a(ss.x * A2[s]) * lam;
+                    const float da = ex2a(ss.x * A2[s]);
+                    carry[s] = da * lam;
+                    Pr[s] *= da;
                 }
             }
         } else {
@@ -437,7 +440,7 @@ __global__ void __maxnreg__(184) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_
                 const int64_t ts = t0 + sub * kSub;
                 if (ts >= t_end) continue;
                 float hs[S];
-                ld_state<S>(ck + ((ts - t_begin) / kSub) * N, hs);
+                ld_state<S>(ck + ((ts - t_begin) / kSub) * ck_stride, hs);
                 // recompute the states of the sub-chunk (the adjoint walk recomputes the decays)
                 float hv[kSub][S];
                 {
@@ -522,17 +525,15 @@ __global__ void __maxnreg__(184) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_
                     // per-step sums for the tile epilogue
                     if (g == 0) sO[r][ch ^ (r & (CH - 1))] = make_float4(du_p, dd_p, y0_p, 0.f);
                     // stage dB / dC contributions; every kRB steps sum them over the channels
-                    stage_contrib<S, CH, RP>(sR, i % kRB, cB, cC, ch_ok, ch, n0);
+                    stage_contrib<S, CH, N, BLK>(sR, i % kRB, cB, cC, ch_ok, ch, n0);
                     if (i % kRB == 0) {
                         __syncwarp();
-                        reduce_staged<CH, N, RP>(sR, sP, r, lane);
+                        reduce_staged<S, CH, N, BLK>(sR, bc0, bc1, t, t_end, lane);
                         __syncwarp();
                     }
                 }
             }
             __syncwarp();
-            // this tile's per-warp dB / dC sums -> partial buffer (float4 rows of N/4)
-            store_tile_partials<N>(sP, bc0, bc1, t0, t_end, lane);
             // ---- epilogue: du, ddelta, dz of step t0 + pr for channels pc0 .. pc0 + CPL
             {
                 const int64_t t = t0 + pr;
@@ -574,9 +575,9 @@ __global__ void __maxnreg__(184) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_
 
     if constexpr (!MAIN) {
         if (ch_ok) {
-            float* out = a.ws_rsum + (row * p.K + k) * N + n0;
+            float2* out = reinterpret_cast<float2*>(a.ws_rsum) + (row * p.K + k) * N + n0;
 #pragma unroll
-            for (int s = 0; s < S; s++) out[s] = carry[s];
+            for (int s = 0; s < S; s++) out[s] = make_float2(Pr[s], carry[s]);
         }
     } else {
         if (ch_ok) {
@@ -652,12 +653,16 @@ __global__ void k_bwd2_reduce_params(BwdArgs a, FPlan p) {
 }
 
 template <typename T, int N>
-cudaError_t launch_bwd2_t(const BwdArgs& a, const FPlan& p, cudaStream_t st) {
-    // checkpoint pass (with forward summaries first when the sequence is chunked)
-    cudaError_t e = launch_fwd2(a.f, p, st, kModeCkpt, a.ws_ckpt);
-    if (e != cudaSuccess) return e;
+cudaError_t launch_bwd2_t(const BwdArgs& a, const FPlan& p, cudaStream_t st, float* ckpt_out) {
+    cudaError_t e = cudaSuccess;
+    if (ckpt_out) {
+        // checkpoint pass (with forward summaries first when the sequence is chunked)
+        e = launch_fwd2(a.f, p, st, kModeCkpt, ckpt_out);
+        if (e != cudaSuccess) return e;
+    }
     if (p.K > 1) {
         const int64_t blocks = p.tiles_b * a.f.Bsz * (p.K - 1);
+        prof_mark(st);
         k_bwd2<T, N, kRevSummary><<<(unsigned)blocks, 32, 0, st>>>(a, p, 1, p.K);
     }
     const int64_t blocks = p.tiles_b * a.f.Bsz * p.K;
@@ -665,24 +670,27 @@ cudaError_t launch_bwd2_t(const BwdArgs& a, const FPlan& p, cudaStream_t st) {
     e = cudaFuncSetAttribute(k_bwd2<T, N, kRevMain>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
+    prof_mark(st);
     k_bwd2<T, N, kRevMain><<<(unsigned)blocks, 32, 0, st>>>(a, p, 0, p.K);
     const int64_t n_bc = 2 * a.f.Bsz * a.f.L * a.f.N;
+    prof_mark(st);
     k_bwd2_reduce_bc<<<(unsigned)ceil_div(n_bc, 256), 256, 0, st>>>(a, p);
     const int64_t n_par = a.f.Dch * a.f.N;
+    prof_mark(st);
     k_bwd2_reduce_params<<<(unsigned)ceil_div(n_par, 256), 256, 0, st>>>(a, p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_bwd2(const BwdArgs& a, const FPlan& p, cudaStream_t st) {
-#define SS_BWD2_N(T)                                          \
-    switch (a.f.N) {                                          \
-        case 1: return launch_bwd2_t<T, 1>(a, p, st);         \
-        case 2: return launch_bwd2_t<T, 2>(a, p, st);         \
-        case 4: return launch_bwd2_t<T, 4>(a, p, st);         \
-        case 8: return launch_bwd2_t<T, 8>(a, p, st);         \
-        case 16: return launch_bwd2_t<T, 16>(a, p, st);       \
-        case 32: return launch_bwd2_t<T, 32>(a, p, st);       \
-        default: return cudaErrorInvalidValue;                \
+cudaError_t launch_bwd2(const BwdArgs& a, const FPlan& p, cudaStream_t st, float* ckpt_out) {
+#define SS_BWD2_N(T)                                              \
+    switch (a.f.N) {                                              \
+        case 1: return launch_bwd2_t<T, 1>(a, p, st, ckpt_out);   \
+        case 2: return launch_bwd2_t<T, 2>(a, p, st, ckpt_out);   \
+        case 4: return launch_bwd2_t<T, 4>(a, p, st, ckpt_out);   \
+        case 8: return launch_bwd2_t<T, 8>(a, p, st, ckpt_out);   \
+        case 16: return launch_bwd2_t<T, 16>(a, p, st, ckpt_out); \
+        case 32: return launch_bwd2_t<T, 32>(a, p, st, ckpt_out); \
+        default: return cudaErrorInvalidValue;                    \
     }
     if (a.f.dtype == 0) { SS_BWD2_N(float) }
     SS_BWD2_N(__nv_bfloat16)

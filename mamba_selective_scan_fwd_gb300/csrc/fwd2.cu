@@ -27,6 +27,7 @@
 namespace ss {
 
 constexpr int kRow = 32;  // time steps per tile
+static_assert(kRow % kSub == 0, "a tile holds whole checkpoint sub-chunks");
 
 template <typename T, int N, int MODE>
 struct FCfg {
@@ -225,11 +226,13 @@ __global__ void __launch_bounds__(32) k_fwd2(FwdArgs a, FPlan p, int64_t ntiles,
         __syncwarp();
 
         // ---- scan: 32 steps of this lane's S states
-#pragma unroll 4
+#pragma unroll 8
         for (int i = 0; i < kRow; i++) {
-            if (CKPT && (i % kSub) == 0 && ch_ok && t0 + i < t_end) {
-                // state at the start of sub-chunk (t0 + i - t_begin) / kSub of this chunk
-                float* dst = ckpt + ((row * p.K + k) * (p.Lc / kSub) + (t0 + i - t_begin) / kSub) * N + n0;
+            if (ckpt && (i % kSub) == 0 && ch_ok && t0 + i < t_end) {
+                // state at the start of sub-chunk j = (t0 + i - t_begin) / kSub of chunk k,
+                // stored step-major: [k * (Lc / kSub) + j][Bsz * Dch][N]
+                const int64_t j = k * (p.Lc / kSub) + (t0 + i - t_begin) / kSub;
+                float* dst = ckpt + (j * a.Bsz * a.Dch + row) * N + n0;
                 if constexpr (S % 4 == 0) {
 #pragma unroll
                     for (int s = 0; s < S; s += 4)
@@ -258,7 +261,7 @@ __global__ void __launch_bounds__(32) k_fwd2(FwdArgs a, FPlan p, int64_t ntiles,
                         const float2 pp = mul2(make_float2(P[s], P[s + 1]), da);
                         P[s] = pp.x;
                         P[s + 1] = pp.y;
-                    } else if (!CKPT) {
+                    } else if (!NOY) {
                         yacc = fma2(make_float2(Cv[s], Cv[s + 1]), hh, yacc);
                     }
                 }
@@ -267,7 +270,7 @@ __global__ void __launch_bounds__(32) k_fwd2(FwdArgs a, FPlan p, int64_t ntiles,
                 const float da = ex2a(du.x * A2[0]);
                 h[0] = fmaf(da, h[0], du.y * Bv[0]);
                 if (SUMMARY) P[0] *= da;
-                else if (!CKPT) sY[i][lane] = Cv[0] * h[0];
+                else if (!NOY) sY[i][lane] = Cv[0] * h[0];
             }
         }
         __syncwarp();
@@ -307,6 +310,18 @@ __global__ void __launch_bounds__(32) k_fwd2(FwdArgs a, FPlan p, int64_t ntiles,
         }
     }
 
+    if (ckpt && ch_ok) {
+        // sub-chunk slots past the end of the sequence (short last chunk only):
+        // the state no longer changes there, so they hold the final state and
+        // the whole checkpoint buffer is written
+        const int64_t nsub = p.Lc / kSub;
+        for (int64_t jj = (t_end - t_begin + kSub - 1) / kSub; jj < nsub; jj++) {
+            float* dst = ckpt + ((k * nsub + jj) * a.Bsz * a.Dch + row) * N + n0;
+#pragma unroll
+            for (int s = 0; s < S; s++) dst[s] = h[s];
+        }
+    }
+
     if (SUMMARY) {
         if (ch_ok) {
             float2* out = reinterpret_cast<float2*>(a.ws_fsum) + (row * p.K + k) * N + n0;
@@ -328,14 +343,17 @@ template <typename T, int N>
 cudaError_t launch_fwd2_t(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt) {
     if (p.K > 1) {
         const int64_t nt = fwd_tiles<T, N, kModeSummary>(a.Dch);
+        prof_mark(st);
         k_fwd2<T, N, kModeSummary><<<(unsigned)(nt * a.Bsz * (p.K - 1)), 32, 0, st>>>(a, p, nt, 0, p.K - 1, nullptr);
     }
     if (mode == kModeCkpt) {
         const int64_t nt = fwd_tiles<T, N, kModeCkpt>(a.Dch);
+        prof_mark(st);
         k_fwd2<T, N, kModeCkpt><<<(unsigned)(nt * a.Bsz * p.K), 32, 0, st>>>(a, p, nt, 0, p.K, ckpt);
     } else {
         const int64_t nt = fwd_tiles<T, N, kModeY>(a.Dch);
-        k_fwd2<T, N, kModeY><<<(unsigned)(nt * a.Bsz * p.K), 32, 0, st>>>(a, p, nt, 0, p.K, nullptr);
+        prof_mark(st);
+        k_fwd2<T, N, kModeY><<<(unsigned)(nt * a.Bsz * p.K), 32, 0, st>>>(a, p, nt, 0, p.K, ckpt);
     }
     return cudaGetLastError();
 }

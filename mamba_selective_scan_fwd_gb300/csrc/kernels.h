@@ -23,8 +23,8 @@ struct BwdArgs {
     FwdArgs f;        // forward inputs; f.y / f.last_state unused
     const void* dy;
     float *du, *ddelta, *dA, *dB, *dC, *dD, *dz, *ddelta_bias;
-    float* ws_rsum;   // reverse chunk summaries M: [Bsz*Dch][K][N]
-    float* ws_ckpt;   // sub-chunk start states: [Bsz*Dch][K][Lc/kSub][N]
+    float* ws_rsum;   // reverse chunk summaries (P, M): [Bsz*Dch][K][N] float2
+    const float* ws_ckpt;  // sub-chunk start states, step-major: [K * Lc/kSub][Bsz*Dch][N]
     float* ws_bc;     // per-tile dB/dC partials: [2][tiles][Bsz][L][N]
     float* ws_dA;     // per-(b,k) dA partials: [Bsz][K][Dch][N]
     float* ws_dD;     // per-(b,k) dD partials: [Bsz][K][Dch]
@@ -78,13 +78,28 @@ inline FPlan make_fplan(int64_t Bsz, int64_t L, int64_t Dch, int64_t N) {
 
 constexpr int kSub = 8;  // backward sub-chunk: steps whose decays and states stay in registers
 
+// Measurement aid behind ss_profile_events: prof_mark records the next of
+// the caller's events on `st` (nothing when none are set); every launcher
+// marks before each kernel it launches, the entry point once after the last.
+void prof_mark(cudaStream_t st);
+
+// ckpt: where the Y-mode forward also stores the sub-chunk start states (may be null).
 cudaError_t launch_fwd2(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt);
-cudaError_t launch_bwd2(const BwdArgs& a, const FPlan& p, cudaStream_t st);
+// ckpt_out: the checkpoint buffer to fill first, or null when a.ws_ckpt already
+// holds the states saved by the forward.
+cudaError_t launch_bwd2(const BwdArgs& a, const FPlan& p, cudaStream_t st, float* ckpt_out);
+
+// Bytes of the sub-chunk start states of every (b, d) row: the checkpoints the
+// backward recomputes from (ss_fwd_save writes them into the caller's buffer).
+inline size_t ckpt_bytes(const FPlan& p, int64_t Bsz, int64_t Dch, int64_t N) {
+    return (size_t)Bsz * Dch * p.K * (p.Lc / kSub) * N * sizeof(float);
+}
 
 // Workspace of the backward (byte offsets, each 256-aligned): forward and
-// reverse chunk summaries (only when chunked), sub-chunk start states, per
-// channel-tile dB / dC partials, per-(batch, chunk) dA / dD / ddelta_bias partials.
-inline BwdLayout bwd_layout2(const FPlan& p, int64_t Bsz, int64_t L, int64_t Dch, int64_t N) {
+// reverse chunk summaries (only when chunked), sub-chunk start states (unless
+// the forward saved them), per channel-tile dB / dC partials, per-(batch,
+// chunk) dA / dD / ddelta_bias partials.
+inline BwdLayout bwd_layout2(const FPlan& p, int64_t Bsz, int64_t L, int64_t Dch, int64_t N, bool saved) {
     BwdLayout w;
     size_t off = 0;
     const size_t rows = (size_t)(Bsz * Dch);
@@ -93,9 +108,9 @@ inline BwdLayout bwd_layout2(const FPlan& p, int64_t Bsz, int64_t L, int64_t Dch
         off = align_up(off + bytes, 256);
         return at;
     };
-    w.fsum = take(p.K > 1 ? rows * p.K * N * 2 * sizeof(float) : 0);
-    w.rsum = take(p.K > 1 ? rows * p.K * N * sizeof(float) : 0);
-    w.ckpt = take(rows * p.K * (p.Lc / kSub) * N * sizeof(float));
+    w.fsum = take(p.K > 1 && !saved ? rows * p.K * N * 2 * sizeof(float) : 0);
+    w.rsum = take(p.K > 1 ? rows * p.K * N * 2 * sizeof(float) : 0);
+    w.ckpt = take(saved ? 0 : ckpt_bytes(p, Bsz, Dch, N));
     w.bc = take(2 * (size_t)p.tiles_b * Bsz * L * N * sizeof(float));
     w.dA = take((size_t)Bsz * p.K * Dch * N * sizeof(float));
     w.dD = take((size_t)Bsz * p.K * Dch * sizeof(float));

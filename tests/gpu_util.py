@@ -60,6 +60,16 @@ def gpu_bwd(t, softplus=True):
     return ss.ss_bwd(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"], softplus, t["dy"])
 
 
+def gpu_fwd_save(t, softplus=True):
+    """Forward that also stores the backward's restart states: (y, last_state, saved)."""
+    return ss.ss_fwd_save(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"], softplus)
+
+
+def gpu_bwd_saved(t, saved, softplus=True):
+    return ss.ss_bwd_saved(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"], softplus,
+                           t["dy"], saved)
+
+
 def oracle_fwd(orc, x, softplus=True, rows=None):
     return orc.fwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], softplus, rows=rows)
 

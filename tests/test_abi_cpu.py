@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol():
     lib = ss.lib()
     for name in declared_functions():
         assert hasattr(lib, name), name
-    assert lib.ss_abi_version() == 1
+    assert lib.ss_abi_version() == binding.ABI_VERSION == 2
 
 
 def test_status_strings():
@@ -87,6 +87,43 @@ def test_fwd_rejects(kw, code):
     assert _fwd(**kw) == code
 
 
+def _fwd_save(**kw):
+    a = dict(u=FAKE, delta=FAKE, A=FAKE, B=FAKE, C=FAKE, D=None, z=None, bias=None, softplus=1, y=FAKE, last=None,
+             saved=FAKE, savedb=1 << 30, Bsz=2, L=16, Dch=8, N=4, dtype=0, ws=None, wsb=0, stream=None)
+    a.update(kw)
+    return ss.lib().ss_fwd_save(a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"], a["bias"], a["softplus"],
+                                a["y"], a["last"], a["saved"], a["savedb"], a["Bsz"], a["L"], a["Dch"], a["N"],
+                                a["dtype"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Bsz=-1), INVALID), (dict(dtype=1), UNSUPPORTED), (dict(N=3), UNSUPPORTED), (dict(y=None), INVALID),
+    (dict(saved=None), WS_SMALL), (dict(saved=FAKE + 8), UNSUPPORTED), (dict(savedb=0), WS_SMALL),
+])
+def test_fwd_save_rejects(kw, code):
+    assert _fwd_save(**kw) == code
+
+
+def test_saved_sizes():
+    # one f32 state of N per (b, d) row every 8 steps of each (32-step aligned) chunk
+    assert ss.saved_bytes(4, 4096, 5120, 16, ss.SS_BF16) == 4 * 5120 * (4096 // 8) * 16 * 4
+    assert ss.saved_bytes(2, 16, 8, 4, ss.SS_F32) == 2 * 8 * (32 // 8) * 4 * 4
+    assert ss.saved_bytes(0, 16, 8, 4, ss.SS_F32) == 0
+    assert _fwd_save(savedb=ss.saved_bytes(2, 16, 8, 4, 0) - 1) == WS_SMALL
+    # the saved-state backward needs no room for the states
+    full = ss.bwd_workspace_bytes(4, 4096, 5120, 16, ss.SS_BF16)
+    part = ss.bwd_saved_workspace_bytes(4, 4096, 5120, 16, ss.SS_BF16)
+    assert 0 < part <= full - ss.saved_bytes(4, 4096, 5120, 16, ss.SS_BF16)
+
+
+def test_plan_info_counts():
+    p = ss.plan_info(4, 4096, 5120, 16, ss.SS_BF16)
+    assert p == {"chunks": 1, "fwd_kernels": 1, "bwd_kernels": 4, "bwd_saved_kernels": 3}
+    q = ss.plan_info(1, 131072, 1024, 16, ss.SS_BF16)
+    assert q["chunks"] > 1 and q["fwd_kernels"] == 2 and q["bwd_kernels"] == 6 and q["bwd_saved_kernels"] == 4
+    assert ss.plan_info(0, 16, 8, 4, 0)["fwd_kernels"] == 0
+
+
 def test_fwd_workspace_too_small_reports_before_launch():
     need = ss.fwd_workspace_bytes(1, 131072, 1024, 16, 2)
     assert need > 0
@@ -105,6 +142,26 @@ def test_fwd_workspace_too_small_reports_before_launch():
 ])
 def test_bwd_rejects(kw, code):
     assert _bwd(**kw) == code
+
+
+def _bwd_saved(**kw):
+    a = dict(u=FAKE, delta=FAKE, A=FAKE, B=FAKE, C=FAKE, D=None, z=None, bias=None, softplus=1, dy=FAKE, saved=FAKE,
+             savedb=1 << 30, du=FAKE, dd=FAKE, dA=FAKE, dB=FAKE, dC=FAKE, dD=None, dz=None, dbias=None, Bsz=2, L=16,
+             Dch=8, N=4, dtype=0, ws=FAKE, wsb=1 << 30, stream=None)
+    a.update(kw)
+    return ss.lib().ss_bwd_saved(a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"], a["bias"],
+                                 a["softplus"], a["dy"], a["saved"], a["savedb"], a["du"], a["dd"], a["dA"], a["dB"],
+                                 a["dC"], a["dD"], a["dz"], a["dbias"], a["Bsz"], a["L"], a["Dch"], a["N"], a["dtype"],
+                                 a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Bsz=-1), INVALID), (dict(N=5), UNSUPPORTED), (dict(D=FAKE), INVALID), (dict(du=None), INVALID),
+    (dict(saved=None), WS_SMALL), (dict(savedb=16), WS_SMALL), (dict(saved=FAKE + 4), UNSUPPORTED),
+    (dict(ws=None), WS_SMALL), (dict(wsb=16), WS_SMALL),
+])
+def test_bwd_saved_rejects(kw, code):
+    assert _bwd_saved(**kw) == code
 
 
 def test_bwd_workspace_one_byte_short():
@@ -128,3 +185,15 @@ def test_product_does_not_import_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "ss_oracle" not in text, f
+
+
+def test_profile_events_validation():
+    import ctypes
+
+    lib = ss.lib()
+    one = (ctypes.c_void_p * 1)(None)
+    assert lib.ss_profile_events(one, -1) == INVALID
+    assert lib.ss_profile_events(one, 17) == INVALID
+    assert lib.ss_profile_events(None, 2) == INVALID
+    assert lib.ss_profile_events(one, 1) == INVALID  # a NULL handle
+    assert lib.ss_profile_events(None, 0) == OK      # switched off

@@ -1,6 +1,7 @@
 """Parity at the full workload sizes, in the launch configuration the bench
-times.  The CUDA path runs the whole problem; the oracle recomputes sampled
-outputs one row at a time:
+times (the forward that saves the backward's restart states, then the
+backward that reads them).  The CUDA path runs the whole problem; the oracle
+recomputes sampled outputs one row at a time:
 
 * y, last_state, du, ddelta, dz on sampled (b, d) rows;
 * dA, dD, ddelta_bias for sampled channels (every batch row of them);
@@ -8,7 +9,8 @@ outputs one row at a time:
   kernel reduces across the full channel dimension.
 
 Plus properties that hold at any size: ddelta_bias = sum_{b,t} ddelta and
-dD = sum_{b,t} dy silu(z) u, and bit-identical repeated runs.
+dD = sum_{b,t} dy silu(z) u, bit-identical repeated runs, and results
+bit-identical to the entry points that recompute the states.
 """
 
 import numpy as np
@@ -16,7 +18,8 @@ import pytest
 import torch
 
 from mamba_selective_scan_fwd_gb300.inputs import WORKLOADS, make_inputs
-from gpu_util import TOL, gpu_bwd, gpu_fwd, normwise, oracle_bwd, oracle_fwd, ref_y, to_device
+from gpu_util import (TOL, gpu_bwd, gpu_bwd_saved, gpu_fwd, gpu_fwd_save, normwise, oracle_bwd, oracle_fwd, ref_y,
+                      to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -33,8 +36,8 @@ def test_fullsize_sampled(orc, wi):
     w = WORKLOADS[wi]
     x = make_inputs(w)
     t = to_device(x, w.io)
-    y, last = gpu_fwd(t, w.softplus)
-    g = gpu_bwd(t, w.softplus) if w.backward else None
+    y, last, saved = gpu_fwd_save(t, w.softplus)
+    g = gpu_bwd_saved(t, saved, w.softplus) if w.backward else None
     torch.cuda.synchronize()
     tf, tb = TOL[w.io]["fwd"], TOL[w.io]["bwd"]
     rng = np.random.default_rng(wi)
@@ -45,9 +48,12 @@ def test_fullsize_sampled(orc, wi):
     y_rows = y[bi, :, di].float().cpu().numpy()
     assert normwise(y_rows, ref_y(rf.y, w.io)) <= tf
     assert normwise(last[bi, di].cpu().numpy(), rf.last_state) <= tf
-    # forward bit-identical on a second run
-    y2, last2 = gpu_fwd(t, w.softplus)
-    assert torch.equal(y, y2) and torch.equal(last, last2)
+    # forward bit-identical on a second run, and to the forward that saves nothing
+    y2, last2, saved2 = gpu_fwd_save(t, w.softplus)
+    assert torch.equal(y, y2) and torch.equal(last, last2) and torch.equal(saved, saved2)
+    y3, last3 = gpu_fwd(t, w.softplus)
+    assert torch.equal(y, y3) and torch.equal(last, last3)
+    del y2, last2, saved2, y3, last3
     if not w.backward:
         return
     rb = oracle_bwd(orc, x, w.softplus, rows=rows, want_dBdC=False)
@@ -75,11 +81,12 @@ def test_fullsize_sampled(orc, wi):
     assert normwise(g["ddelta_bias"].cpu().numpy(), dl.sum(dim=(0, 1)).cpu().numpy()) <= 1e-5
     gate = t["dy"].double() * torch.nn.functional.silu(t["z"].double())
     assert normwise(g["dD"].cpu().numpy(), (gate * t["u"].double()).sum(dim=(0, 1)).cpu().numpy()) <= 1e-5
-    # backward bit-identical on a second run
-    g2 = gpu_bwd(t, w.softplus)
-    for k, v in g.items():
-        if v is not None:
-            assert torch.equal(v, g2[k]), k
+    # backward bit-identical on a second run, and to the backward that recomputes the states
+    for g2 in (gpu_bwd_saved(t, saved, w.softplus), gpu_bwd(t, w.softplus)):
+        for k, v in g.items():
+            if v is not None:
+                assert torch.equal(v, g2[k]), k
+        del g2
 
 
 def test_tiny_workload_full_parity(orc):

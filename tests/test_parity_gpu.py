@@ -10,7 +10,8 @@ import torch
 
 import mamba_selective_scan_fwd_gb300 as ss
 from mamba_selective_scan_fwd_gb300.inputs import round_bf16, small_inputs
-from gpu_util import TOL, gpu_bwd, gpu_fwd, normwise, oracle_bwd, oracle_fwd, ref_y, to_device
+from gpu_util import (TOL, gpu_bwd, gpu_bwd_saved, gpu_fwd, gpu_fwd_save, normwise, oracle_bwd, oracle_fwd, ref_y,
+                      to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -164,12 +165,44 @@ def test_no_read_of_unwritten_memory(shape, io):
         out = {k: torch.full(v.shape, float("nan") if fill else 0.0, dtype=torch.float32, device="cuda")
                for k, v in out.items()}
         g = ss.ss_bwd(*args, t["dy"], out=out, workspace=wb)
+        # the saved-state pair: saved buffer and workspace poisoned the same way
+        sv = torch.full((ss.saved_bytes(Bsz, L, Dch, N, dt),), fill, dtype=torch.uint8, device="cuda")
+        ys = torch.full_like(t["u"], float("nan") if fill else 0.0)
+        ys, ls, sv = ss.ss_fwd_save(*args, y=ys, saved=sv, workspace=wf.fill_(fill))
+        wsv = torch.full((ss.bwd_saved_workspace_bytes(Bsz, L, Dch, N, dt),), fill, dtype=torch.uint8, device="cuda")
+        outs = {k: torch.full_like(v, float("nan") if fill else 0.0) for k, v in out.items()}
+        gs = ss.ss_bwd_saved(*args, t["dy"], sv, out=outs, workspace=wsv)
         torch.cuda.synchronize()
-        return y, last, g
+        return y, last, g, ys, ls, gs, sv
 
-    y0, l0, g0 = run(0)
-    y1, l1, g1 = run(0xFF)
+    y0, l0, g0, ys0, ls0, gs0, sv0 = run(0)
+    y1, l1, g1, ys1, ls1, gs1, sv1 = run(0xFF)
     assert torch.equal(y0, y1) and torch.equal(l0, l1)
+    assert torch.equal(sv0, sv1)  # the saved-state buffer is fully written
+    assert torch.equal(y0, ys0) and torch.equal(ys0, ys1) and torch.equal(l0, ls0) and torch.equal(ls0, ls1)
     for k, v in g0.items():
         assert torch.isfinite(v).all(), k
         assert torch.equal(v, g1[k]), k
+        assert torch.equal(v, gs0[k]) and torch.equal(v, gs1[k]), k
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", SHAPES, ids=[f"B{s[0]}L{s[1]}D{s[2]}N{s[3]}" for s in SHAPES])
+def test_saved_state_path(orc, shape, io):
+    """ss_fwd_save + ss_bwd_saved give results bit-identical to ss_fwd + ss_bwd
+    (which the test above compares with the oracle), and match the oracle."""
+    seed = 2000 + SHAPES.index(shape)
+    x, sp = make(shape, io, "full", seed)
+    t = to_device(x, io)
+    y0, l0 = gpu_fwd(t, sp)
+    g0 = gpu_bwd(t, sp)
+    y1, l1, saved = gpu_fwd_save(t, sp)
+    g1 = gpu_bwd_saved(t, saved, sp)
+    torch.cuda.synchronize()
+    assert torch.equal(y0, y1) and torch.equal(l0, l1)
+    for k, v in g0.items():
+        if v is not None:
+            assert torch.equal(v, g1[k]), k
+    rb = oracle_bwd(orc, x, sp)
+    for k in ("du", "ddelta", "dA", "dB", "dC"):
+        assert normwise(g1[k], getattr(rb, k)) <= TOL[io]["bwd"], k
