@@ -109,10 +109,10 @@ int ss_fwd_noalloc(const void *u, const void *delta, const float *A, const void 
  * the forward walk ss_bwd has to redo.  The pages this library follows have
  * a backward-owned record of every state (baracuda-kernels
  * `selective_scan.rs`, "Workspace": B * D * L * N elements written by the
- * backward's first pass); here the forward keeps one state in eight steps.
+ * backward's first pass); here the forward keeps one state in four steps.
  *   saved         device buffer of at least ss_saved_bytes(...) bytes, 16-byte
  *                 aligned, fully overwritten (f32 h of every (b, d) row at
- *                 every 8th step of each time chunk); opaque to the caller.
+ *                 every 4th step of each time chunk); opaque to the caller.
  * All other arguments and results are those of ss_fwd.  A NULL or short
  * `saved` gives SS_ERR_WORKSPACE_TOO_SMALL before anything is launched.
  */

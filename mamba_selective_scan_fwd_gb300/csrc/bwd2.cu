@@ -272,7 +272,7 @@ __device__ __forceinline__ void store_half(float* p, const float (&v)[CPL], int6
 constexpr int kRevMain = 0, kRevSummary = 1;
 
 template <typename T, int N, int MODE>
-__global__ void __maxnreg__(224) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_t k_hi) {
+__global__ void __maxnreg__(168) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_t k_hi) {
     using C = BCfg<T, N>;
     constexpr bool MAIN = MODE == kRevMain;
     constexpr int S = C::S, G = C::G, CH = C::CH, CPL = C::CPL, RWH = C::RWH, NWd = C::NW, NP = C::NP,
@@ -362,6 +362,10 @@ __global__ void __maxnreg__(224) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_
     float* bc0 = a.ws_bc + ((int64_t)tile * f.Bsz + b) * L * N;                  // dB partials of this tile
     float* bc1 = a.ws_bc + ((int64_t)(p.tiles_b + tile) * f.Bsz + b) * L * N;    // dC partials
 
+    // start state of the last sub-chunk, loaded ahead of its use (MAIN only)
+    float hpf[S];
+    if (MAIN) ld_state<S>(ck + ((t_end - t_begin + kSub - 1) / kSub - 1) * ck_stride, hpf);
+
     for (int64_t m = ntile - 1; m >= 0; m--) {
         const int64_t t0 = t_begin + m * kTT;
         // ---- prologue: per-(t, d) terms of the tile's steps, staged in shared memory
@@ -439,8 +443,12 @@ __global__ void __maxnreg__(224) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_
             for (int sub = kTT / kSub - 1; sub >= 0; sub--) {
                 const int64_t ts = t0 + sub * kSub;
                 if (ts >= t_end) continue;
+                // this sub-chunk's start state (prefetched one sub-chunk ahead), then the next one's
                 float hs[S];
-                ld_state<S>(ck + ((ts - t_begin) / kSub) * ck_stride, hs);
+#pragma unroll
+                for (int s = 0; s < S; s++) hs[s] = hpf[s];
+                const int64_t jsub = (ts - t_begin) / kSub;
+                if (jsub > 0) ld_state<S>(ck + (jsub - 1) * ck_stride, hpf);
                 // recompute the states of the sub-chunk (the adjoint walk recomputes the decays)
                 float hv[kSub][S];
                 {
@@ -615,17 +623,45 @@ __global__ void __maxnreg__(224) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_
     }
 }
 
-// dB / dC: sum of the per-tile partials, tiles in ascending order.
+// dB / dC: sum of the per-tile partials, tiles in ascending order.  A thread
+// owns 4 consecutive outputs (16-byte streaming loads, 8 tiles in flight)
+// when N is a multiple of 4, one output otherwise.
 __global__ void k_bwd2_reduce_bc(BwdArgs a, FPlan p) {
     const int64_t bln = a.f.Bsz * a.f.L * a.f.N;
-    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (e >= 2 * bln) return;
-    const int tensor = e >= bln ? 1 : 0;
-    const int64_t r = e - tensor * bln;
-    const float* src = a.ws_bc + (size_t)tensor * p.tiles_b * bln + r;
-    float acc = 0.f;
-    for (int64_t tl = 0; tl < p.tiles_b; tl++) acc += src[tl * bln];
-    (tensor ? a.dC : a.dB)[r] = acc;
+    const int64_t tiles = p.tiles_b;
+    if (a.f.N % 4 == 0) {
+        const int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // float4 index over both tensors
+        const int64_t nq = bln / 4;
+        if (q >= 2 * nq) return;
+        const int tensor = q >= nq ? 1 : 0;
+        const int64_t r = q - tensor * nq;
+        const float4* src = reinterpret_cast<const float4*>(a.ws_bc + (size_t)tensor * tiles * bln) + r;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        int64_t tl = 0;
+        for (; tl + 8 <= tiles; tl += 8) {
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; u++) v[u] = __ldcs(src + (tl + u) * nq);
+#pragma unroll
+            for (int u = 0; u < 8; u++) {
+                acc.x += v[u].x; acc.y += v[u].y; acc.z += v[u].z; acc.w += v[u].w;
+            }
+        }
+        for (; tl < tiles; tl++) {
+            const float4 v = __ldcs(src + tl * nq);
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        reinterpret_cast<float4*>(tensor ? a.dC : a.dB)[r] = acc;
+    } else {
+        const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+        if (e >= 2 * bln) return;
+        const int tensor = e >= bln ? 1 : 0;
+        const int64_t r = e - tensor * bln;
+        const float* src = a.ws_bc + (size_t)tensor * tiles * bln + r;
+        float acc = 0.f;
+        for (int64_t tl = 0; tl < tiles; tl++) acc += src[tl * bln];
+        (tensor ? a.dC : a.dB)[r] = acc;
+    }
 }
 
 // dA / dD / ddelta_bias: sum over (batch, chunk) partials in ascending order.
@@ -672,7 +708,7 @@ cudaError_t launch_bwd2_t(const BwdArgs& a, const FPlan& p, cudaStream_t st, flo
     if (e != cudaSuccess) return e;
     prof_mark(st);
     k_bwd2<T, N, kRevMain><<<(unsigned)blocks, 32, 0, st>>>(a, p, 0, p.K);
-    const int64_t n_bc = 2 * a.f.Bsz * a.f.L * a.f.N;
+    const int64_t n_bc = 2 * a.f.Bsz * a.f.L * a.f.N / (N % 4 == 0 ? 4 : 1);  // threads
     prof_mark(st);
     k_bwd2_reduce_bc<<<(unsigned)ceil_div(n_bc, 256), 256, 0, st>>>(a, p);
     const int64_t n_par = a.f.Dch * a.f.N;

@@ -76,7 +76,7 @@ inline FPlan make_fplan(int64_t Bsz, int64_t L, int64_t Dch, int64_t N) {
     return p;
 }
 
-constexpr int kSub = 8;  // backward sub-chunk: steps whose decays and states stay in registers
+constexpr int kSub = 4;  // backward sub-chunk: steps whose states stay in registers (checkpoint interval)
 
 // Measurement aid behind ss_profile_events: prof_mark records the next of
 // the caller's events on `st` (nothing when none are set); every launcher
