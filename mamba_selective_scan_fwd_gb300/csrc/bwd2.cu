@@ -40,7 +40,8 @@
 namespace ss {
 
 constexpr int kTT = 16;  // backward tile: steps staged per prologue
-constexpr int kRB = 4;   // steps whose dB / dC contributions are reduced together
+constexpr int kRB = 4;   // steps whose dB / dC contributions are reduced together (one sub-chunk)
+static_assert(kRB == kSub, "one staged sub-chunk of dB / dC contributions at a time");
 
 template <typename T, int N>
 struct BCfg {
@@ -174,10 +175,12 @@ __device__ __forceinline__ void ld_state(const float* p, float (&v)[S]) {
 
 // Stage one step's dB / dC contributions (slot j of kRB) in shared memory:
 // block (j, tau) holds CH rows of N floats (the states) with the 16-byte
-// columns of a row swizzled by bc_swz.
+// columns of a row swizzled by bc_swz.  Lanes of channels past Dch need no
+// masking: their u, dy and z load as zero, so lam * Delta * u and g * h are
+// exactly zero there.
 template <int S, int CH, int N, int BLK>
-__device__ __forceinline__ void stage_contrib(float* sR, int j, const float (&cB)[S], const float (&cC)[S],
-                                              bool ch_ok, int ch, int n0) {
+__device__ __forceinline__ void stage_contrib(float* sR, int j, const float (&cB)[S], const float (&cC)[S], int ch,
+                                              int n0) {
     float* r0 = sR + (2 * j) * BLK + ch * N;
     float* r1 = r0 + BLK;
     if constexpr (S == 8 && N % 8 == 0) {
@@ -185,16 +188,14 @@ __device__ __forceinline__ void stage_contrib(float* sR, int j, const float (&cB
 #pragma unroll
         for (int s = 0; s < S; s += 4) {
             const int col = (n0 + s) ^ sw;
-            *reinterpret_cast<float4*>(r0 + col) =
-                ch_ok ? make_float4(cB[s], cB[s + 1], cB[s + 2], cB[s + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
-            *reinterpret_cast<float4*>(r1 + col) =
-                ch_ok ? make_float4(cC[s], cC[s + 1], cC[s + 2], cC[s + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<float4*>(r0 + col) = make_float4(cB[s], cB[s + 1], cB[s + 2], cB[s + 3]);
+            *reinterpret_cast<float4*>(r1 + col) = make_float4(cC[s], cC[s + 1], cC[s + 2], cC[s + 3]);
         }
     } else {
 #pragma unroll
         for (int s = 0; s < S; s++) {
-            r0[n0 + s] = ch_ok ? cB[s] : 0.f;
-            r1[n0 + s] = ch_ok ? cC[s] : 0.f;
+            r0[n0 + s] = cB[s];
+            r1[n0 + s] = cC[s];
         }
     }
 }
@@ -277,13 +278,16 @@ __global__ void __maxnreg__(168) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_
     constexpr bool MAIN = MODE == kRevMain;
     constexpr int S = C::S, G = C::G, CH = C::CH, CPL = C::CPL, RWH = C::RWH, NWd = C::NW, NP = C::NP,
                   BLK = C::BLK;
-    __shared__ float4 sS[kTT][CH];                  // (Delta, Delta*u, g, sig(x))  swizzled columns
-    __shared__ float2 sE[MAIN ? kTT : 1][CH];       // (u, dz factor)               swizzled columns
+    // per-(t, d) staging: rows padded by one element, so that both the row-parallel
+    // prologue / epilogue (lane = step) and the scan (lane = channel) access them
+    // without bank conflicts and with constant offsets
+    __shared__ float4 sS[kTT][CH + 1];              // (Delta, Delta*u, g, sig(x))
+    __shared__ float2 sE[MAIN ? kTT : 1][CH + 1];   // (u, dz factor)
     __shared__ __align__(16) float sB[kTT][NP];
     __shared__ __align__(16) float sC[kTT][NP];
     // dB / dC contributions of kRB steps: block (j, tau) holds CH swizzled rows of N floats
     __shared__ __align__(16) float sR[MAIN ? kRB * 2 * BLK : 4];
-    __shared__ float4 sO[MAIN ? kTT : 1][CH];                  // per-step (sum lam B, sum A q, y0) of each channel
+    __shared__ float4 sO[MAIN ? kTT : 1][CH + 1];              // per-step (sum lam B, sum A q, y0) of each channel
     __shared__ float sBias[CH], sDv[CH];
     __shared__ float sAcc[2][MAIN ? CPL : 1][32];                // per-lane dD / ddelta_bias partials (lane fastest)
 
@@ -318,10 +322,14 @@ __global__ void __maxnreg__(168) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_
     const int64_t row = b * Dch + d;
     const float Dd = f.D ? f.D[d] : 0.f;
     // A2 = A * log2(e); the dDelta partial sum below uses A2 and is scaled back by ln 2 in the epilogue
+    // Lanes of channels past Dch run with a zero exponent, state and adjoint: with
+    // u = dy = z = 0 loaded there, every quantity they form stays exactly zero
+    // (whatever A of the clamped channel is), so their dB / dC contributions
+    // need no masking.
     float A2[S], carry[S], dA[S], Pr[MAIN ? 1 : S];
 #pragma unroll
     for (int s = 0; s < S; s++) {
-        A2[s] = f.A[d * N + n0 + s] * kLog2eF;
+        A2[s] = ch_ok ? f.A[d * N + n0 + s] * kLog2eF : 0.f;
         carry[s] = 0.f;
         dA[s] = 0.f;
         if (!MAIN) Pr[s] = 1.f;
@@ -337,6 +345,8 @@ __global__ void __maxnreg__(168) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_
                 carry[s] = fmaf(pm.x, carry[s], pm.y);
             }
         }
+#pragma unroll
+        for (int s = 0; s < S; s++) carry[s] = ch_ok ? carry[s] : 0.f;
     }
     // per-channel dD / ddelta_bias partials of each epilogue lane (its CPL channels, its rows),
     // kept in the lane's own shared slots between tiles
@@ -365,6 +375,10 @@ __global__ void __maxnreg__(168) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_
     // start state of the last sub-chunk, loaded ahead of its use (MAIN only)
     float hpf[S];
     if (MAIN) ld_state<S>(ck + ((t_end - t_begin + kSub - 1) / kSub - 1) * ck_stride, hpf);
+    // first step of the sub-chunk whose dB / dC contributions wait in sR for their
+    // channel sums (-1: none): each reduction is deferred past the next sub-chunk's
+    // recompute, which touches no staging it writes, so that the two overlap
+    int64_t t_pend = -1;
 
     for (int64_t m = ntile - 1; m >= 0; m--) {
         const int64_t t0 = t_begin + m * kTT;
@@ -381,7 +395,6 @@ __global__ void __maxnreg__(168) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_
                 if (z) bload_half<T, CPL, RWH>(z, off, d0 + pc0, Dch, pfast, rz);
                 if (MAIN || ph == 1) bload_words<C::NB, NWd>((ph == 0 ? Bm : Cm) + (b * L + t) * N, rbc);
             }
-            const int swz = pr & (CH - 1);
 #pragma unroll
             for (int c = 0; c < CPL; c++) {
                 const int cc = pc0 + c;
@@ -405,15 +418,25 @@ __global__ void __maxnreg__(168) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_
                         dzf = dyv * sz * fmaf(zz, 1.f - sz, 1.f);
                     }
                 }
-                sS[pr][cc ^ swz] = make_float4(dl, dl * uu, gg, sgx);
-                if (MAIN) sE[pr][cc ^ swz] = make_float2(uu, dzf);
+                sS[pr][cc] = make_float4(dl, dl * uu, gg, sgx);
+                if (MAIN) sE[pr][cc] = make_float2(uu, dzf);
             }
-            if (ph == 1) {
+            // lanes ph = 0 stage the B row of their step, lanes ph = 1 the C row; with
+            // rows padded to N + 4 floats the 16-byte stores of 8 consecutive rows
+            // fall in different bank groups
+            if (MAIN || ph == 1) {
+                float* dst = ph ? &sC[pr][0] : &sB[pr][0];
+                if constexpr (N % 4 == 0) {
 #pragma unroll
-                for (int n = 0; n < N; n++) sC[pr][n] = rv ? belem<T>(rbc, n) : 0.f;
-            } else if (MAIN) {
+                    for (int n = 0; n < N; n += 4)
+                        *reinterpret_cast<float4*>(dst + n) =
+                            rv ? make_float4(belem<T>(rbc, n), belem<T>(rbc, n + 1), belem<T>(rbc, n + 2),
+                                             belem<T>(rbc, n + 3))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+                } else {
 #pragma unroll
-                for (int n = 0; n < N; n++) sB[pr][n] = rv ? belem<T>(rbc, n) : 0.f;
+                    for (int n = 0; n < N; n++) dst[n] = rv ? belem<T>(rbc, n) : 0.f;
+                }
             }
         }
         __syncwarp();
@@ -423,7 +446,7 @@ __global__ void __maxnreg__(168) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_
             // decay product, no states needed
             for (int i = kTT - 1; i >= 0; i--) {
                 if (t0 + i >= t_end) continue;
-                const float4 ss = sS[i][ch ^ (i & (CH - 1))];
+                const float4 ss = sS[i][ch];
                 float Cv[S];
                 bld_shared<S>(&sC[i][n0], Cv);
 #pragma unroll
@@ -446,7 +469,7 @@ __global__ void __maxnreg__(168) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_
                 // this sub-chunk's start state (prefetched one sub-chunk ahead), then the next one's
                 float hs[S];
 #pragma unroll
-                for (int s = 0; s < S; s++) hs[s] = hpf[s];
+                for (int s = 0; s < S; s++) hs[s] = ch_ok ? hpf[s] : 0.f;
                 const int64_t jsub = (ts - t_begin) / kSub;
                 if (jsub > 0) ld_state<S>(ck + (jsub - 1) * ck_stride, hpf);
                 // recompute the states of the sub-chunk (the adjoint walk recomputes the decays)
@@ -458,7 +481,7 @@ __global__ void __maxnreg__(168) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_
 #pragma unroll
                     for (int i = 0; i < kSub; i++) {
                         const int r = sub * kSub + i;
-                        const float4 ss = sS[r][ch ^ (r & (CH - 1))];
+                        const float4 ss = sS[r][ch];
                         float Bv[S];
                         bld_shared<S>(&sB[r][n0], Bv);
                         if constexpr (S >= 2) {
@@ -477,12 +500,16 @@ __global__ void __maxnreg__(168) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_
                         }
                     }
                 }
+                // (no branch, so that it can interleave with the recompute: with nothing
+                // pending the end bound -1 stores nothing)
+                reduce_staged<S, CH, N, BLK>(sR, bc0, bc1, t_pend, t_pend >= 0 ? t_end : (int64_t)-1, lane);
+                __syncwarp();  // the reduction has read sR before the walk below restages it
                 // adjoint walk
 #pragma unroll
                 for (int i = kSub - 1; i >= 0; i--) {
                     const int r = sub * kSub + i;
                     const int64_t t = t0 + r;
-                    const float4 ss = sS[r][ch ^ (r & (CH - 1))];
+                    const float4 ss = sS[r][ch];
                     float Bv[S], Cv[S];
                     bld_shared<S>(&sB[r][n0], Bv);
                     bld_shared<S>(&sC[r][n0], Cv);
@@ -531,21 +558,17 @@ __global__ void __maxnreg__(168) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_
                     dd_p = gsum<G>(dd_p);
                     y0_p = gsum<G>(y0_p);
                     // per-step sums for the tile epilogue
-                    if (g == 0) sO[r][ch ^ (r & (CH - 1))] = make_float4(du_p, dd_p, y0_p, 0.f);
-                    // stage dB / dC contributions; every kRB steps sum them over the channels
-                    stage_contrib<S, CH, N, BLK>(sR, i % kRB, cB, cC, ch_ok, ch, n0);
-                    if (i % kRB == 0) {
-                        __syncwarp();
-                        reduce_staged<S, CH, N, BLK>(sR, bc0, bc1, t, t_end, lane);
-                        __syncwarp();
-                    }
+                    if (g == 0) sO[r][ch] = make_float4(du_p, dd_p, y0_p, 0.f);
+                    // stage dB / dC contributions (summed over the channels after the next recompute)
+                    stage_contrib<S, CH, N, BLK>(sR, i, cB, cC, ch, n0);
                 }
+                __syncwarp();  // staged contributions visible to every lane
+                t_pend = ts;
             }
             __syncwarp();
             // ---- epilogue: du, ddelta, dz of step t0 + pr for channels pc0 .. pc0 + CPL
             {
                 const int64_t t = t0 + pr;
-                const int swz = pr & (CH - 1);
                 float vdu[CPL], vdx[CPL], vdz[CPL], eD[CPL], eb[CPL];
 #pragma unroll
                 for (int c = 0; c < CPL; c++) {
@@ -555,9 +578,9 @@ __global__ void __maxnreg__(168) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_
 #pragma unroll
                 for (int c = 0; c < CPL; c++) {
                     const int cc = pc0 + c;
-                    const float4 so = sO[pr][cc ^ swz];
-                    const float4 ss = sS[pr][cc ^ swz];
-                    const float2 se = sE[pr][cc ^ swz];
+                    const float4 so = sO[pr][cc];
+                    const float4 ss = sS[pr][cc];
+                    const float2 se = sE[pr][cc];
                     vdu[c] = fmaf(ss.z, sDv[cc], ss.x * so.x);
                     vdx[c] = fmaf(se.x, so.x, so.y * kLn2) * ss.w;
                     vdz[c] = se.y * fmaf(sDv[cc], se.x, so.z);
@@ -580,6 +603,8 @@ __global__ void __maxnreg__(168) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo, int64_
         }
         __syncwarp();
     }
+
+    if (MAIN && t_pend >= 0) reduce_staged<S, CH, N, BLK>(sR, bc0, bc1, t_pend, t_end, lane);
 
     if constexpr (!MAIN) {
         if (ch_ok) {

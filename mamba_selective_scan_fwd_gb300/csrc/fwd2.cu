@@ -123,8 +123,10 @@ __global__ void __launch_bounds__(32) k_fwd2(FwdArgs a, FPlan p, int64_t ntiles,
     constexpr bool NOY = SUMMARY || CKPT;  // no readout, gate or y
     using C = FCfg<T, N, MODE>;
     constexpr int S = C::S, G = C::G, CH = C::CH, RW = C::RW, NW = C::NW, NP = C::NP, YP = C::YP;
-    __shared__ float2 sDU[kRow][CH];   // (delta_eff, delta_eff * u), column swizzled by row
-    __shared__ float2 sGD[kRow][CH];   // (gate, D * u), column swizzled by row
+    // per-(t, d) staging, rows padded by one element: conflict-free for the
+    // row-parallel prologue / epilogue (lane = step) and the scan (lane = channel)
+    __shared__ float2 sDU[kRow][CH + 1];  // (delta_eff, delta_eff * u)
+    __shared__ float2 sGD[kRow][CH + 1];  // (gate, D * u)
     __shared__ __align__(16) float sB[kRow][NP];
     __shared__ __align__(16) float sC[kRow][NP];
     __shared__ __align__(16) float sY[kRow][YP];
@@ -178,7 +180,6 @@ __global__ void __launch_bounds__(32) k_fwd2(FwdArgs a, FPlan p, int64_t ntiles,
 
     const int64_t t_begin = k * p.Lc;
     const int64_t t_end = t_begin + p.Lc < L ? t_begin + p.Lc : L;
-    const int sw = lane & (CH - 1);  // this lane's row swizzle in the prologue / epilogue
 
     uint32_t ru[RW], rd[RW], rz[RW], rb[NW], rc[NW];
     auto load_rows = [&](int64_t t) {
@@ -206,14 +207,14 @@ __global__ void __launch_bounds__(32) k_fwd2(FwdArgs a, FPlan p, int64_t ntiles,
                     dl = a.softplus ? softplus_fast(x) : x;
                     dlu = dl * elem<T>(ru, c);
                 }
-                sDU[lane][c ^ sw] = make_float2(dl, dlu);
+                sDU[lane][c] = make_float2(dl, dlu);
                 if (!NOY) {
                     float gate = 1.f;
                     if (z) {
                         const float zz = elem<T>(rz, c);
                         gate = zz * sigmoid_fast(zz);
                     }
-                    sGD[lane][c ^ sw] = make_float2(gate, sDv[c] * elem<T>(ru, c));
+                    sGD[lane][c] = make_float2(gate, sDv[c] * elem<T>(ru, c));
                 }
             }
 #pragma unroll
@@ -242,7 +243,7 @@ __global__ void __launch_bounds__(32) k_fwd2(FwdArgs a, FPlan p, int64_t ntiles,
                     for (int s = 0; s < S; s++) dst[s] = h[s];
                 }
             }
-            const float2 du = sDU[i][ch ^ (i & (CH - 1))];
+            const float2 du = sDU[i][ch];
             float Bv[S], Cv[S];
             ld_shared_row<S>(&sB[i][n0], Bv);
             if (!NOY) ld_shared_row<S>(&sC[i][n0], Cv);
@@ -285,7 +286,7 @@ __global__ void __launch_bounds__(32) k_fwd2(FwdArgs a, FPlan p, int64_t ntiles,
                     float acc = 0.f;
 #pragma unroll
                     for (int q = 0; q < G; q++) acc += sY[lane][c * G + q];
-                    const float2 gd = sGD[lane][c ^ sw];
+                    const float2 gd = sGD[lane][c];
                     yv[c] = (acc + gd.y) * gd.x;
                 }
                 T* yrow = static_cast<T*>(a.y) + (b * L + t) * Dch + d0;

@@ -206,3 +206,24 @@ def test_saved_state_path(orc, shape, io):
     rb = oracle_bwd(orc, x, sp)
     for k in ("du", "ddelta", "dA", "dB", "dC"):
         assert normwise(g1[k], getattr(rb, k)) <= TOL[io]["bwd"], k
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_positive_A_ragged_tile(orc, io):
+    """A > 0 (growth instead of decay) on a shape whose last channel tile is
+    ragged: padded lanes must add nothing to the dB / dC channel sums."""
+    x, sp = make((2, 100, 40, 16), io, "full", 81)
+    A = x["A"].copy()
+    A[:, ::3] = np.float32(0.02) * (1 + np.arange(A.shape[1])[::3])  # some states grow
+    x["A"] = A.astype(np.float32)
+    t = to_device(x, io)
+    y, last = gpu_fwd(t, sp)
+    g = gpu_bwd(t, sp)
+    torch.cuda.synchronize()
+    rf = oracle_fwd(orc, x, sp)
+    rb = oracle_bwd(orc, x, sp)
+    tf, tb = TOL[io]["fwd"], TOL[io]["bwd"]
+    assert normwise(y, ref_y(rf.y, io)) <= tf and normwise(last, rf.last_state) <= tf
+    for k in ("du", "ddelta", "dA", "dB", "dC", "dD", "dz", "ddelta_bias"):
+        assert torch.isfinite(g[k]).all(), k
+        assert normwise(g[k], getattr(rb, k)) <= tb, k
