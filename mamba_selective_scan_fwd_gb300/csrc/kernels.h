@@ -36,36 +36,35 @@ struct BwdLayout {
     size_t fsum, rsum, ckpt, bc, dA, dD, db, total;
 };
 
-constexpr int kModeY = 0, kModeSummary = 1, kModeCkpt = 2;
+constexpr int kModeY = 0, kModeSummary = 1, kModeCkpt = 2, kModeYSave = 3;
 
-// States held by one lane (S): G = N / S lanes share a channel and a warp
-// covers 32 / G channels.  The forward with readout and the backward keep 8
-// states per lane; the checkpoint walk (no readout) runs faster with 4.
-__host__ __device__ constexpr int fwd_states_per_lane(int64_t N, int mode) {
-    return mode == kModeCkpt ? (N < 4 ? (int)N : 4) : (N < 8 ? (int)N : 8);
-}
-__host__ __device__ constexpr int bwd_states_per_lane(int64_t N) { return N < 8 ? (int)N : 8; }
-__host__ __device__ constexpr int64_t channels_per_warp(int64_t N, int S) { return 32 / (N / S); }
+// Block layout shared by the forward and backward scans: a block covers
+// kChannelsPerBlock channels (32 for N = 1) of one batch row and one time
+// chunk.  For N >= 16 it has two warps that split the states of every
+// channel; within a warp G = 2 adjacent lanes share a channel (one lane for
+// N = 1), so a lane holds N / (2 * warps) states.
+constexpr int kChannelsPerBlock = 16;
+__host__ __device__ constexpr int fwd_warps(int64_t N) { return N >= 16 ? 2 : 1; }
+__host__ __device__ constexpr int64_t channels_per_block(int64_t N) { return N >= 2 ? kChannelsPerBlock : 32; }
 
-// Launch plan: one warp per (batch, channel tile, time chunk).  The time
-// chunking (K, Lc) is shared by every kernel of a call; each launcher derives
-// its own channel-tile count from its lanes per channel.
+// Launch plan: one block per (batch, channel tile, time chunk).  The time
+// chunking (K, Lc) is shared by every kernel of a call.
 struct FPlan {
-    int64_t tiles_b; // channel tiles of the backward kernels (sizes the dB / dC partials)
+    int64_t tiles_b; // channel tiles (sizes the per-tile dB / dC partials)
     int64_t K;       // time chunks
     int64_t Lc;      // chunk length (multiple of 32); the last chunk may be shorter
 };
 
-constexpr int64_t kFwdTargetWarps = 1216;  // 8 warps on each of 152 SMs
+constexpr int64_t kTargetWarps = 2432;  // 16 warps on each of 152 SMs
 constexpr int64_t kFwdMinChunk = 128;
 
 // A pure function of the sizes (the same sizes always chunk the same way).
 inline FPlan make_fplan(int64_t Bsz, int64_t L, int64_t Dch, int64_t N) {
     FPlan p;
-    p.tiles_b = ceil_div(Dch, channels_per_warp(N, bwd_states_per_lane(N)));
-    const int64_t warps = Bsz * ceil_div(Dch, channels_per_warp(N, fwd_states_per_lane(N, kModeY)));
+    p.tiles_b = ceil_div(Dch, channels_per_block(N));
+    const int64_t warps = Bsz * p.tiles_b * fwd_warps(N);
     int64_t K = 1;
-    if (warps > 0 && warps < kFwdTargetWarps) K = ceil_div(kFwdTargetWarps, warps);
+    if (warps > 0 && warps < kTargetWarps) K = ceil_div(kTargetWarps, warps);
     const int64_t kmax = ceil_div(L, kFwdMinChunk);
     if (K > kmax) K = kmax;
     if (K < 1) K = 1;
