@@ -39,6 +39,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "simd.cuh"
+#include "tiles.cuh"
 
 namespace ss {
 
@@ -51,91 +52,39 @@ template <typename T, int N>
 struct BCfg {
     static constexpr int NW = fwd_warps(N);         // warps per block (they split the states)
     static constexpr int NPW = N / NW;              // states per warp
-    static constexpr int G = NPW >= 2 ? 2 : 1;      // lanes per channel
-    static constexpr int S = NPW / G;               // states per lane
-    static constexpr int CH = 32 / G;               // channels per block
+    static constexpr int G = NPW >= 2 ? 2 : 1;      // lanes per channel pair
+    static constexpr int S = NPW / G;               // states per lane (of each of its two channels)
+    static constexpr int PAIRS = 32 / G;            // channel pairs per block
+    static constexpr int CH = 2 * PAIRS;            // channels per block
     static constexpr int THREADS = 32 * NW;
-    static constexpr int PARTS = THREADS / kTT;     // prologue / epilogue threads per step
-    static constexpr int CPL = CH / PARTS;          // channels per prologue / epilogue thread
-    static constexpr int RWH = CPL * (int)sizeof(T) / 4 > 0 ? CPL * (int)sizeof(T) / 4 : 1;
-    static constexpr int NB = N * (int)sizeof(T);
+    static constexpr int ESZ = (int)sizeof(T);
+    static constexpr int GRP = 4;                   // channels per prologue / epilogue item
+    static constexpr int NGRP = CH / GRP;           // items per step
+    static constexpr int ITEMS = kTT * NGRP / THREADS;  // items per thread per tile
+    static constexpr int RWH = GRP * ESZ / 4;       // 32-bit words of an item's run of one tensor
+    static constexpr int NB = N * ESZ;
     static constexpr int NWd = NB >= 4 ? NB / 4 : 1;
-    static constexpr int NP = N + 4;
-    // dB / dC staging of one warp: block (step slot j, tensor tau) holds CH
-    // rows of NPW floats (the warp's states); blocks are padded by 8 floats
-    // so that the 16 lanes of a half warp reading 8-byte pairs of four
-    // consecutive blocks hit 32 different banks
-    static constexpr int BLK = CH * NPW + 8;
-    static constexpr int MINB = N >= 32 ? 1 : 9;    // blocks per SM the register budget must allow
-    static_assert(CPL >= 2, "prologue runs of at least two channels");
-    static_assert(CH == kChannelsPerBlock || N == 1, "channel tile of the plan");
+    static constexpr int NSG = N / S;               // state groups of a step
+    static constexpr int SGB = 2 * S * ESZ;         // bytes of a state group: S values of B, then S of C
+    static constexpr int BCROW = NSG * SGB;
+    static constexpr int EP = CH + 4;               // padded per-channel rows (floats)
+    static constexpr int GP = PAIRS + 8;            // padded per-pair float2 rows
+    // dB / dC staging of one warp: block (step slot j, tensor tau) holds PAIRS
+    // rows of NPW floats (the warp's states, summed over the pair's two
+    // channels); blocks are padded by 8 floats so that the 16 lanes of a half
+    // warp reading 8-byte pairs of four consecutive blocks hit 32 banks
+    static constexpr int BLK = PAIRS * NPW + 8;
+    static constexpr int MINB = N >= 32 ? 4 : 12 / NW;  // blocks per SM the register budget must allow
+    static_assert(kTT * NGRP % THREADS == 0, "whole items per thread");
+    static_assert(CH == channels_per_block(N), "channel tile of the plan");
 };
 
-template <typename T>
-__device__ __forceinline__ float belem(const uint32_t* w, int j) {
-    if constexpr (sizeof(T) == 4) {
-        return __uint_as_float(w[j]);
-    } else {
-        return (j & 1) ? bf16hi(w[j >> 1]) : bf16lo(w[j >> 1]);
-    }
-}
-
-template <int NBYTES, int NWORDS>
-__device__ __forceinline__ void bload_words(const void* p, uint32_t (&w)[NWORDS]) {
-    if constexpr (NBYTES % 16 == 0) {
-#pragma unroll
-        for (int v = 0; v < NBYTES / 16; v++) {
-            const uint4 q = __ldg(reinterpret_cast<const uint4*>(p) + v);
-            w[4 * v] = q.x; w[4 * v + 1] = q.y; w[4 * v + 2] = q.z; w[4 * v + 3] = q.w;
-        }
-    } else if constexpr (NBYTES == 8) {
-        const uint2 q = __ldg(reinterpret_cast<const uint2*>(p));
-        w[0] = q.x; w[1] = q.y;
-    } else if constexpr (NBYTES == 4) {
-        w[0] = __ldg(reinterpret_cast<const unsigned int*>(p));
-    } else {
-        w[0] = __ldg(reinterpret_cast<const unsigned short*>(p));
-    }
-}
-
-// CPL contiguous io elements at (row offset off, channel c0): vector loads when
-// aligned and complete, else element loads zero-filled past Dch.
-template <typename T, int CPL, int RWH>
-__device__ __forceinline__ void bload_half(const T* base, int64_t off, int64_t c0, int64_t Dch, bool fast,
-                                           uint32_t (&w)[RWH]) {
-    if (fast) {
-        bload_words<CPL * (int)sizeof(T), RWH>(base + off, w);
-    } else {
-#pragma unroll
-        for (int i = 0; i < RWH; i++) w[i] = 0u;
-#pragma unroll
-        for (int c = 0; c < CPL; c++) {
-            if (c0 + c < Dch) {
-                if constexpr (sizeof(T) == 4) {
-                    w[c] = __ldg(reinterpret_cast<const unsigned int*>(base + off) + c);
-                } else {
-                    const uint32_t v = __ldg(reinterpret_cast<const unsigned short*>(base + off) + c);
-                    w[c >> 1] |= (c & 1) ? (v << 16) : v;
-                }
-            }
-        }
-    }
-}
-
-template <int S>
-__device__ __forceinline__ void bld_shared(const float* p, float (&v)[S]) {
-    if constexpr (S % 4 == 0) {
-#pragma unroll
-        for (int q = 0; q < S; q += 4) {
-            const float4 f = *reinterpret_cast<const float4*>(p + q);
-            v[q] = f.x; v[q + 1] = f.y; v[q + 2] = f.z; v[q + 3] = f.w;
-        }
-    } else if constexpr (S == 2) {
-        const float2 f = *reinterpret_cast<const float2*>(p);
-        v[0] = f.x; v[1] = f.y;
-    } else {
-        v[0] = p[0];
-    }
+// Slot of channel pair pp in a per-step staging row: the two pairs of a
+// 4-channel item go to slots q and q + PAIRS / 2; a quarter warp of prologue
+// threads (eight items of one step) then hits eight different bank groups.
+template <int PAIRS>
+__device__ __forceinline__ int bpair_slot(int pp) {
+    return (pp >> 1) + (PAIRS / 2) * (pp & 1);
 }
 
 // softplus(x) (as in simd.cuh) together with sigmoid(x), sharing e = e^-|x|.
@@ -168,8 +117,9 @@ __device__ __forceinline__ void cp_async_state(float* dst, const float* src) {
     } else {
         asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(sa), "l"(src), "n"(S * 4) : "memory");
     }
-    asm volatile("cp.async.commit_group;" ::: "memory");
 }
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
 template <int PENDING>
 __device__ __forceinline__ void cp_async_wait() {
@@ -193,13 +143,14 @@ __device__ __forceinline__ void ld_state(const float* p, float (&v)[S]) {
 }
 
 // Stage one step's dB / dC contributions (slot j of kRB) in shared memory:
-// block (j, tau) holds CH rows of NPW floats, the warp's states of each
-// channel.  Lanes of channels past Dch need no masking: their u, dy and z
-// load as zero, so lam * Delta * u and g * h are exactly zero there.
+// block (j, tau) holds one row of NPW floats per channel pair, the warp's
+// states summed over the pair's two channels.  Channels past Dch need no
+// masking: their u, dy and z load as zero, so lam * Delta * u and g * h are
+// exactly zero there.
 template <int S, int NPW, int BLK>
-__device__ __forceinline__ void stage_contrib(float* sR, int j, const float (&cB)[S], const float (&cC)[S], int ch,
+__device__ __forceinline__ void stage_contrib(float* sR, int j, const float (&cB)[S], const float (&cC)[S], int pp,
                                               int gs) {
-    float* r0 = sR + (2 * j) * BLK + ch * NPW + gs;
+    float* r0 = sR + (2 * j) * BLK + pp * NPW + gs;
     float* r1 = r0 + BLK;
     if constexpr (S % 4 == 0) {
 #pragma unroll
@@ -217,11 +168,11 @@ __device__ __forceinline__ void stage_contrib(float* sR, int j, const float (&cB
 }
 
 // Sum the kRB staged steps of one warp (slot j holds time step t + j) over
-// the CH channels and store the sums as the warp's states n_w .. n_w + NPW of
-// the dB / dC partial rows bc0[t + j], bc1[t + j] (rows of N floats; steps
-// at or past t_end are not stored).  Work unit: a pair of consecutive states
-// of one (step, tensor); the channels are added as a fixed pairwise tree
-// (c, c + 1), then pairs of pairs, ...
+// the CH staged rows (channel pairs) and store the sums as the warp's states
+// n_w .. n_w + NPW of the dB / dC partial rows bc0[t + j], bc1[t + j] (rows
+// of N floats; steps at or past t_end are not stored).  Work unit: a pair of
+// consecutive states of one (step, tensor); the rows are added as a fixed
+// pairwise tree (c, c + 1), then pairs of pairs, ...
 template <int CH, int NPW, int N, int BLK>
 __device__ __forceinline__ void reduce_staged(const float* sR, float* bc0, float* bc1, int n_w, int64_t t,
                                               int64_t t_end, int lane) {
@@ -294,25 +245,28 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                                                                                int64_t k_hi) {
     using C = BCfg<T, N>;
     constexpr bool MAIN = MODE == kRevMain;
-    constexpr int NW = C::NW, NPW = C::NPW, S = C::S, G = C::G, CH = C::CH, CPL = C::CPL, RWH = C::RWH,
-                  NWd = C::NWd, NP = C::NP, BLK = C::BLK;
-    // per-(t, d) staging: rows padded by one element, so that both the row-parallel
-    // prologue / epilogue (thread = step) and the scan (lane = channel) access them
-    // without bank conflicts and with constant offsets
-    __shared__ float4 sS[kTT][CH + 1];                    // (Delta, Delta*u, g, sig(x))
-    __shared__ float2 sE[MAIN ? kTT : 1][CH + 1];         // (u, dz factor)
-    __shared__ __align__(16) float sB[MAIN ? kTT : 1][NP];
-    __shared__ __align__(16) float sC[kTT][NP];
-    // dB / dC contributions of kRB steps, per warp: block (j, tau) holds CH rows of NPW floats
+    constexpr int NW = C::NW, NPW = C::NPW, S = C::S, G = C::G, PAIRS = C::PAIRS, CH = C::CH,
+                  THREADS = C::THREADS, GRP = C::GRP, NGRP = C::NGRP, ITEMS = C::ITEMS, RWH = C::RWH,
+                  NWd = C::NWd, SGB = C::SGB, BCROW = C::BCROW, EP = C::EP, GP = C::GP, BLK = C::BLK;
+    // per-(t, d) staging of the scan, one entry per channel pair at bpair_slot
+    __shared__ float4 sDU[kTT][PAIRS + 1];  // (Delta, Delta*u) of both channels
+    __shared__ float2 sG[kTT][GP];          // g of both channels
+    __shared__ __align__(16) unsigned char sBC[kTT][BCROW];  // raw B / C values by state group
+    // per-(t, d) terms only the epilogue reads, channel fastest: u, sig(x), dz factor
+    __shared__ __align__(16) float sEu[MAIN ? kTT : 1][MAIN ? EP : 4];
+    __shared__ __align__(16) float sEs[MAIN ? kTT : 1][MAIN ? EP : 4];
+    __shared__ __align__(16) float sEz[MAIN ? kTT : 1][MAIN ? EP : 4];
+    // dB / dC contributions of kRB steps, per warp: block (j, tau) holds a row of NPW floats per pair
     __shared__ __align__(16) float sR[MAIN ? NW : 1][MAIN ? kRB * 2 * BLK : 4];
-    // per-step, per-warp sums over the warp's states: (sum lam B, sum A q) and y0
-    __shared__ float2 sOa[MAIN ? NW : 1][MAIN ? kTT : 1][CH + 1];
-    __shared__ float sOb[MAIN ? NW : 1][MAIN ? kTT : 1][CH + 1];
+    // per-step, per-warp sums over the warp's states: sum lam B, sum A q, y0 (channel fastest)
+    __shared__ __align__(16) float sOu[MAIN ? NW : 1][MAIN ? kTT : 1][MAIN ? EP : 4];
+    __shared__ __align__(16) float sOd[MAIN ? NW : 1][MAIN ? kTT : 1][MAIN ? EP : 4];
+    __shared__ __align__(16) float sOy[MAIN ? NW : 1][MAIN ? kTT : 1][MAIN ? EP : 4];
+    // dD / ddelta_bias partials of each epilogue thread's items (thread fastest)
+    __shared__ float sAcc[MAIN ? 2 : 1][MAIN ? ITEMS * GRP : 1][THREADS];
+    // restart states of the next two sub-chunks: 2 S floats per lane (double buffered)
+    __shared__ __align__(16) float sH[MAIN ? 2 : 1][MAIN ? THREADS * 2 * S : 4];
     __shared__ float sBias[CH], sDv[CH];
-    // per-thread dD / ddelta_bias partials of the epilogue threads (thread fastest)
-    __shared__ float sAcc[MAIN ? 2 : 1][MAIN ? CPL : 1][C::THREADS];
-    // restart states of the next two sub-chunks, one S-float slot per lane (double buffered)
-    __shared__ __align__(16) float sH[MAIN ? 2 : 1][C::THREADS * S];
 
     const FwdArgs& f = a.f;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -331,135 +285,145 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
     const T* z = static_cast<const T*>(f.z);
     const T* dy = static_cast<const T*>(a.dy);
 
-    if (tid < CH) {
-        const int64_t dc = d0 + tid < Dch ? d0 + tid : Dch - 1;
-        sBias[tid] = f.delta_bias ? f.delta_bias[dc] : 0.f;
-        sDv[tid] = f.D ? f.D[dc] : 0.f;
+    for (int c = tid; c < CH; c += THREADS) {
+        const int64_t dc = d0 + c < Dch ? d0 + c : Dch - 1;
+        sBias[c] = f.delta_bias ? f.delta_bias[dc] : 0.f;
+        sDv[c] = f.D ? f.D[dc] : 0.f;
     }
 
-    // scan-lane identity: channel ch, states n0 .. n0 + S (warp w holds n_w .. n_w + NPW)
-    const int ch = lane / G, g = lane % G;
-    const bool ch_ok = d0 + ch < Dch;
-    const int64_t d = ch_ok ? d0 + ch : Dch - 1;
+    // scan-lane identity: channel pair pp (channels c0, c0 + 1 of the block),
+    // states n0 .. n0 + S of both (warp w holds n_w .. n_w + NPW)
+    const int pp = lane / G, g = lane % G;
+    const int c0 = 2 * pp;
+    const bool ok[2] = {d0 + c0 < Dch, d0 + c0 + 1 < Dch};
+    const int64_t dd[2] = {ok[0] ? d0 + c0 : Dch - 1, ok[1] ? d0 + c0 + 1 : Dch - 1};
     const int n_w = w * NPW;
     const int n0 = n_w + g * S;
-    const int64_t row = b * Dch + d;
-    // A2 = A * log2(e); the dDelta partial sum below uses A2 and is scaled back by ln 2 in the epilogue.
-    // Lanes of channels past Dch run with a zero exponent, state and adjoint: with
-    // u = dy = z = 0 loaded there, every quantity they form stays exactly zero
-    // (whatever A of the clamped channel is), so their dB / dC contributions
-    // need no masking.
-    float A2[S], carry[S], dA[S], Pr[MAIN ? 1 : S];
+    const int sg = n0 / S;
+    const int pslot = bpair_slot<PAIRS>(pp);
+    const int64_t row[2] = {b * Dch + dd[0], b * Dch + dd[1]};
+    // A2 = A * log2(e); the dDelta partial sums below use A2 and are scaled back
+    // by ln 2 in the epilogue.  Channels past Dch run with a zero exponent, state
+    // and adjoint: with u = dy = z = 0 loaded there, everything they form stays
+    // exactly zero, so their dB / dC contributions need no masking.
+    float A2[2][S], carry[2][S], dA[2][S], Pr[2][MAIN ? 1 : S];
 #pragma unroll
-    for (int s = 0; s < S; s++) {
-        A2[s] = ch_ok ? f.A[d * N + n0 + s] * kLog2eF : 0.f;
-        carry[s] = 0.f;
-        dA[s] = 0.f;
-        if (!MAIN) Pr[s] = 1.f;
+    for (int e = 0; e < 2; e++) {
+#pragma unroll
+        for (int s = 0; s < S; s++) {
+            A2[e][s] = ok[e] ? f.A[dd[e] * N + n0 + s] * kLog2eF : 0.f;
+            carry[e][s] = 0.f;
+            dA[e][s] = 0.f;
+            if (!MAIN) Pr[e][s] = 1.f;
+        }
     }
     if (MAIN && k + 1 < p.K) {
         // carry into the end of chunk k: rho_{j-1} = M_j + P_j rho_j from the
         // reverse summaries (P_j, M_j) of chunks K-1 .. k+1, with rho_{K-1} = 0
-        const float2* rs = reinterpret_cast<const float2*>(a.ws_rsum) + row * p.K * N + n0;
-        for (int64_t j = p.K - 1; j > k; j--) {
 #pragma unroll
-            for (int s = 0; s < S; s++) {
-                const float2 pm = rs[j * N + s];
-                carry[s] = fmaf(pm.x, carry[s], pm.y);
+        for (int e = 0; e < 2; e++) {
+            const float2* rs = reinterpret_cast<const float2*>(a.ws_rsum) + row[e] * p.K * N + n0;
+            for (int64_t j = p.K - 1; j > k; j--) {
+#pragma unroll
+                for (int s = 0; s < S; s++) {
+                    const float2 pm = rs[j * N + s];
+                    carry[e][s] = fmaf(pm.x, carry[e][s], pm.y);
+                }
             }
-        }
 #pragma unroll
-        for (int s = 0; s < S; s++) carry[s] = ch_ok ? carry[s] : 0.f;
+            for (int s = 0; s < S; s++) carry[e][s] = ok[e] ? carry[e][s] : 0.f;
+        }
     }
-
-    // prologue / epilogue thread identity: step pr of the tile, channels pc0 .. pc0 + CPL
-    const int pr = tid % kTT, ph = tid / kTT;
-    const int pc0 = ph * CPL;
-    const bool pfast = ((Dch * (int64_t)sizeof(T)) % 16 == 0) && (d0 + CH <= Dch) &&
-                       ((CPL * (int)sizeof(T)) % 4 == 0);
-    const bool ofast = (Dch % 4 == 0) && (d0 + CH <= Dch);
-    // per-channel dD / ddelta_bias partials of this epilogue thread over its rows,
-    // kept in the thread's own shared slots between tiles
     if (MAIN) {
 #pragma unroll
-        for (int c = 0; c < CPL; c++) { sAcc[0][c][tid] = 0.f; sAcc[1][c][tid] = 0.f; }
+        for (int c = 0; c < ITEMS * GRP; c++) { sAcc[0][c][tid] = 0.f; sAcc[1][c][tid] = 0.f; }
     }
 
+    const bool pfast = ((Dch * (int64_t)sizeof(T)) % 16 == 0) && (d0 + CH <= Dch);
+    const bool ofast = (Dch % 4 == 0) && (d0 + CH <= Dch);
     const int64_t t_begin = k * p.Lc;
     const int64_t t_end = t_begin + p.Lc < L ? t_begin + p.Lc : L;
     const int64_t ntile = (t_end - t_begin + kTT - 1) / kTT;
     // saved states, step-major: [k * (Lc / kSub) + j][Bsz * Dch][N]
     const int64_t ck_stride = f.Bsz * Dch * N;
-    const float* ck = a.ws_ckpt + (k * (p.Lc / kSub)) * ck_stride + row * N + n0;
+    const float* ck0 = a.ws_ckpt + (k * (p.Lc / kSub)) * ck_stride + row[0] * N + n0;
+    const float* ck1 = a.ws_ckpt + (k * (p.Lc / kSub)) * ck_stride + row[1] * N + n0;
     float* bc0 = a.ws_bc + ((int64_t)tile * f.Bsz + b) * L * N;                  // dB partials of this tile
     float* bc1 = a.ws_bc + ((int64_t)(p.tiles_b + tile) * f.Bsz + b) * L * N;    // dC partials
     float* sRw = &sR[MAIN ? w : 0][0];
-    __syncthreads();  // sBias / sDv and the sAcc slots before the first prologue
-
-    // restart state of sub-chunk j lives in sH[j & 1][tid * S ..]; each lane copies
-    // and reads only its own slot, so the copies need no barrier.  The last
-    // sub-chunk's is requested here, each earlier one a sub-chunk ahead.
+    // restart state of sub-chunk j lives in sH[j & 1][tid * 2S ..] (S floats per
+    // channel); each lane copies and reads only its own slots, so the copies need
+    // no barrier.  The last sub-chunk's is requested here, each earlier one a
+    // sub-chunk ahead.
     if (MAIN) {
         const int64_t jlast = (t_end - t_begin + kSub - 1) / kSub - 1;
-        cp_async_state<S>(&sH[jlast & 1][tid * S], ck + jlast * ck_stride);
+        cp_async_state<S>(&sH[jlast & 1][tid * 2 * S], ck0 + jlast * ck_stride);
+        cp_async_state<S>(&sH[jlast & 1][tid * 2 * S + S], ck1 + jlast * ck_stride);
+        cp_async_commit();
     }
+    __syncthreads();  // sBias / sDv / sAcc before the first prologue
 
     for (int64_t m = ntile - 1; m >= 0; m--) {
         const int64_t t0 = t_begin + m * kTT;
-        // ---- prologue: per-(t, d) terms of the tile's steps, staged in shared memory
-        {
-            const int64_t t = t0 + pr;
+        // ---- prologue: (step, 4-channel group) items of the tile
+#pragma unroll
+        for (int it = 0; it < ITEMS; it++) {
+            const int id = tid + it * THREADS;
+            const int r = id / NGRP, q = id % NGRP;
+            const int cg = q * GRP;
+            const int64_t t = t0 + r;
             const bool rv = t < t_end;
-            const bool stage_b = MAIN && ph == 0, stage_c = ph == (MAIN ? 1 : 0);
-            uint32_t rd[RWH], ru[RWH], rz[RWH], rg[RWH], rbc[NWd];
+            uint32_t rd[RWH], ru[RWH], rz[RWH], rg[RWH];
             if (rv) {
-                const int64_t off = (b * L + t) * Dch + d0 + pc0;
-                bload_half<T, CPL, RWH>(delta, off, d0 + pc0, Dch, pfast, rd);
-                bload_half<T, CPL, RWH>(u, off, d0 + pc0, Dch, pfast, ru);
-                bload_half<T, CPL, RWH>(dy, off, d0 + pc0, Dch, pfast, rg);
-                if (z) bload_half<T, CPL, RWH>(z, off, d0 + pc0, Dch, pfast, rz);
-                if (stage_b || stage_c) bload_words<C::NB, NWd>((stage_b ? Bm : Cm) + (b * L + t) * N, rbc);
+                const int64_t off = (b * L + t) * Dch + d0 + cg;
+                load_run<T, GRP, RWH>(delta, off, d0 + cg, Dch, pfast, rd);
+                load_run<T, GRP, RWH>(u, off, d0 + cg, Dch, pfast, ru);
+                load_run<T, GRP, RWH>(dy, off, d0 + cg, Dch, pfast, rg);
+                if (z) load_run<T, GRP, RWH>(z, off, d0 + cg, Dch, pfast, rz);
             }
+            float dl[GRP], dlu[GRP], gg[GRP], uu[GRP], sgx[GRP], dzf[GRP];
 #pragma unroll
-            for (int c = 0; c < CPL; c++) {
-                const int cc = pc0 + c;
-                float dl = 0.f, sgx = 0.f, uu = 0.f, gg = 0.f, dzf = 0.f;
+            for (int c = 0; c < GRP; c++) {
+                dl[c] = dlu[c] = gg[c] = uu[c] = sgx[c] = dzf[c] = 0.f;
                 if (rv) {
-                    const float x = belem<T>(rd, c) + sBias[cc];
+                    const float x = elem<T>(rd, c) + sBias[cg + c];
                     if (f.softplus) {
-                        softplus_and_sigmoid(x, dl, sgx);
+                        softplus_and_sigmoid(x, dl[c], sgx[c]);
                     } else {
-                        dl = x;
-                        sgx = 1.f;
+                        dl[c] = x;
+                        sgx[c] = 1.f;
                     }
-                    uu = belem<T>(ru, c);
-                    const float dyv = belem<T>(rg, c);
-                    gg = dyv;
+                    uu[c] = elem<T>(ru, c);
+                    dlu[c] = dl[c] * uu[c];
+                    const float dyv = elem<T>(rg, c);
+                    gg[c] = dyv;
                     if (z) {
-                        const float zz = belem<T>(rz, c);
+                        const float zz = elem<T>(rz, c);
                         const float sz = sigmoid_fast(zz);
-                        gg = dyv * zz * sz;
-                        dzf = dyv * sz * fmaf(zz, 1.f - sz, 1.f);
+                        gg[c] = dyv * zz * sz;
+                        dzf[c] = dyv * sz * fmaf(zz, 1.f - sz, 1.f);
                     }
                 }
-                sS[pr][cc] = make_float4(dl, dl * uu, gg, sgx);
-                if (MAIN) sE[pr][cc] = make_float2(uu, dzf);
             }
-            // B row (MAIN) / C row of the thread's step; rows padded to N + 4 floats
-            if (stage_b || stage_c) {
-                float* dst = stage_b ? &sB[pr][0] : &sC[pr][0];
-                if constexpr (N % 4 == 0) {
 #pragma unroll
-                    for (int n = 0; n < N; n += 4)
-                        *reinterpret_cast<float4*>(dst + n) =
-                            rv ? make_float4(belem<T>(rbc, n), belem<T>(rbc, n + 1), belem<T>(rbc, n + 2),
-                                             belem<T>(rbc, n + 3))
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
-                } else {
-#pragma unroll
-                    for (int n = 0; n < N; n++) dst[n] = rv ? belem<T>(rbc, n) : 0.f;
-                }
+            for (int c = 0; c < GRP; c += 2) {
+                const int slot = bpair_slot<PAIRS>((cg + c) / 2);
+                sDU[r][slot] = make_float4(dl[c], dlu[c], dl[c + 1], dlu[c + 1]);
+                sG[r][slot] = make_float2(gg[c], gg[c + 1]);
             }
+            if (MAIN) {
+                *reinterpret_cast<float4*>(&sEu[r][cg]) = make_float4(uu[0], uu[1], uu[2], uu[3]);
+                *reinterpret_cast<float4*>(&sEs[r][cg]) = make_float4(sgx[0], sgx[1], sgx[2], sgx[3]);
+                *reinterpret_cast<float4*>(&sEz[r][cg]) = make_float4(dzf[0], dzf[1], dzf[2], dzf[3]);
+            }
+        }
+        // B / C rows of the tile's steps (the reverse summary needs only C)
+        for (int id = tid; id < (MAIN ? 2 : 1) * kTT; id += THREADS) {
+            const int half = MAIN ? id / kTT : 1, r = id % kTT;
+            const int64_t t = t0 + r;
+            uint32_t wv[NWd];
+            if (t < t_end) load_words<C::NB, NWd>((half ? Cm : Bm) + (b * L + t) * N, wv);
+            stage_bc_row<T, N, S, NWd>(&sBC[r][0], half, wv, t < t_end);
         }
         __syncthreads();
 
@@ -468,15 +432,19 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
             // decay product, no states needed
             for (int i = kTT - 1; i >= 0; i--) {
                 if (t0 + i >= t_end) continue;
-                const float4 ss = sS[i][ch];
-                float Cv[S];
-                bld_shared<S>(&sC[i][n0], Cv);
+                const float4 du = sDU[i][pslot];
+                const float2 g2 = sG[i][pslot];
+                float Bv[S], Cv[S];
+                ld_bc<T, S>(&sBC[i][sg * SGB], Bv, Cv);
 #pragma unroll
-                for (int s = 0; s < S; s++) {
-                    const float lam = fmaf(ss.z, Cv[s], carry[s]);
-                    const float da = ex2a(ss.x * A2[s]);
-                    carry[s] = da * lam;
-                    Pr[s] *= da;
+                for (int e = 0; e < 2; e++) {
+#pragma unroll
+                    for (int s = 0; s < S; s++) {
+                        const float lam = fmaf(e ? g2.y : g2.x, Cv[s], carry[e][s]);
+                        const float da = ex2a((e ? du.z : du.x) * A2[e][s]);
+                        carry[e][s] = da * lam;
+                        Pr[e][s] *= da;
+                    }
                 }
             }
         } else {
@@ -490,45 +458,51 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                 if (ts >= t_end) continue;
                 // request the previous sub-chunk's restart state, then wait for this one's
                 const int64_t jsub = (ts - t_begin) / kSub;
-                const float* hsrc = &sH[jsub & 1][tid * S];
+                const float* hsrc = &sH[jsub & 1][tid * 2 * S];
                 if (jsub > 0) {
-                    cp_async_state<S>(&sH[(jsub - 1) & 1][tid * S], ck + (jsub - 1) * ck_stride);
+                    cp_async_state<S>(&sH[(jsub - 1) & 1][tid * 2 * S], ck0 + (jsub - 1) * ck_stride);
+                    cp_async_state<S>(&sH[(jsub - 1) & 1][tid * 2 * S + S], ck1 + (jsub - 1) * ck_stride);
+                    cp_async_commit();
                     cp_async_wait<1>();
                 } else {
                     cp_async_wait<0>();
                 }
-                float hs[S];
-                ld_state<S>(hsrc, hs);
-#pragma unroll
-                for (int s = 0; s < S; s++) hs[s] = ch_ok ? hs[s] : 0.f;
                 // recompute the states and decays of the sub-chunk
-                float hv[kSub][S], av[kSub][S];
+                float hv[kSub][2][S], av[kSub][2][S];
                 {
-                    float hh[S];
+                    float hh[2][S];
 #pragma unroll
-                    for (int s = 0; s < S; s++) hh[s] = hs[s];
+                    for (int e = 0; e < 2; e++) {
+                        ld_state<S>(hsrc + e * S, hh[e]);
+#pragma unroll
+                        for (int s = 0; s < S; s++) hh[e][s] = ok[e] ? hh[e][s] : 0.f;
+                    }
 #pragma unroll
                     for (int i = 0; i < kSub; i++) {
                         const int r = sub * kSub + i;
-                        const float4 ss = sS[r][ch];
+                        const float4 du = sDU[r][pslot];
                         float Bv[S];
-                        bld_shared<S>(&sB[r][n0], Bv);
-                        if constexpr (S >= 2) {
+                        ld_b<T, S>(&sBC[r][sg * SGB], Bv);
 #pragma unroll
-                            for (int s = 0; s < S; s += 2) {
-                                const float2 e = mul2(splat2(ss.x), make_float2(A2[s], A2[s + 1]));
-                                const float2 da = make_float2(ex2a(e.x), ex2a(e.y));
-                                const float2 x = mul2(splat2(ss.y), make_float2(Bv[s], Bv[s + 1]));
-                                const float2 nh = fma2(da, make_float2(hh[s], hh[s + 1]), x);
-                                hh[s] = nh.x; hh[s + 1] = nh.y;
-                                hv[i][s] = nh.x; hv[i][s + 1] = nh.y;
-                                av[i][s] = da.x; av[i][s + 1] = da.y;
+                        for (int e = 0; e < 2; e++) {
+                            if constexpr (S >= 2) {
+                                const float2 dl2 = splat2(e ? du.z : du.x), dlu2 = splat2(e ? du.w : du.y);
+#pragma unroll
+                                for (int s = 0; s < S; s += 2) {
+                                    const float2 ex = mul2(dl2, make_float2(A2[e][s], A2[e][s + 1]));
+                                    const float2 da = make_float2(ex2a(ex.x), ex2a(ex.y));
+                                    const float2 x = mul2(dlu2, make_float2(Bv[s], Bv[s + 1]));
+                                    const float2 nh = fma2(da, make_float2(hh[e][s], hh[e][s + 1]), x);
+                                    hh[e][s] = nh.x; hh[e][s + 1] = nh.y;
+                                    hv[i][e][s] = nh.x; hv[i][e][s + 1] = nh.y;
+                                    av[i][e][s] = da.x; av[i][e][s + 1] = da.y;
+                                }
+                            } else {
+                                const float da = ex2a((e ? du.z : du.x) * A2[e][0]);
+                                hh[e][0] = fmaf(da, hh[e][0], (e ? du.w : du.y) * Bv[0]);
+                                hv[i][e][0] = hh[e][0];
+                                av[i][e][0] = da;
                             }
-                        } else {
-                            const float da = ex2a(ss.x * A2[0]);
-                            hh[0] = fmaf(da, hh[0], ss.y * Bv[0]);
-                            hv[i][0] = hh[0];
-                            av[i][0] = da;
                         }
                     }
                 }
@@ -536,160 +510,183 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
 #pragma unroll
                 for (int i = kSub - 1; i >= 0; i--) {
                     const int r = sub * kSub + i;
-                    const float4 ss = sS[r][ch];
+                    const float4 du = sDU[r][pslot];
+                    const float2 g2 = sG[r][pslot];
                     float Bv[S], Cv[S];
-                    bld_shared<S>(&sB[r][n0], Bv);
-                    bld_shared<S>(&sC[r][n0], Cv);
-                    float du_p, dd_p, y0_p;
+                    ld_bc<T, S>(&sBC[r][sg * SGB], Bv, Cv);
+                    float sumB[2], sumQ[2], y0[2];
                     float cB[S], cC[S];
                     if constexpr (S >= 2) {
-                        float2 dup = make_float2(0.f, 0.f), ddp = dup, y0p = dup;
-                        const float2 g2 = splat2(ss.z), dl2 = splat2(ss.x), dlu2 = splat2(ss.y);
+                        float2 cb2[S / 2], cc2[S / 2];
+#pragma unroll
+                        for (int e = 0; e < 2; e++) {
+                            const float2 g2e = splat2(e ? g2.y : g2.x), dl2 = splat2(e ? du.z : du.x),
+                                         dlu2 = splat2(e ? du.w : du.y);
+                            float2 dup = make_float2(0.f, 0.f), ddp = dup, y0p = dup;
+#pragma unroll
+                            for (int s = 0; s < S; s += 2) {
+                                const float2 Cp = make_float2(Cv[s], Cv[s + 1]);
+                                const float2 hcur = make_float2(hv[i][e][s], hv[i][e][s + 1]);
+                                float2 hprev;
+                                if (i > 0) {
+                                    hprev = make_float2(hv[i - 1][e][s], hv[i - 1][e][s + 1]);
+                                } else {
+                                    hprev = ok[e] ? *reinterpret_cast<const float2*>(hsrc + e * S + s)
+                                                  : make_float2(0.f, 0.f);
+                                }
+                                const float2 lam = fma2(g2e, Cp, make_float2(carry[e][s], carry[e][s + 1]));
+                                dup = fma2(lam, make_float2(Bv[s], Bv[s + 1]), dup);
+                                const float2 cn = mul2(make_float2(av[i][e][s], av[i][e][s + 1]), lam);
+                                const float2 q = mul2(cn, hprev);
+                                ddp = fma2(make_float2(A2[e][s], A2[e][s + 1]), q, ddp);
+                                const float2 na = fma2(dl2, q, make_float2(dA[e][s], dA[e][s + 1]));
+                                dA[e][s] = na.x; dA[e][s + 1] = na.y;
+                                y0p = fma2(Cp, hcur, y0p);
+                                // dB / dC contributions summed over the pair's two channels
+                                cb2[s / 2] = e ? fma2(lam, dlu2, cb2[s / 2]) : mul2(lam, dlu2);
+                                cc2[s / 2] = e ? fma2(g2e, hcur, cc2[s / 2]) : mul2(g2e, hcur);
+                                carry[e][s] = cn.x; carry[e][s + 1] = cn.y;
+                            }
+                            sumB[e] = dup.x + dup.y;
+                            sumQ[e] = ddp.x + ddp.y;
+                            y0[e] = y0p.x + y0p.y;
+                        }
 #pragma unroll
                         for (int s = 0; s < S; s += 2) {
-                            const float2 Cp = make_float2(Cv[s], Cv[s + 1]);
-                            const float2 hcur = make_float2(hv[i][s], hv[i][s + 1]);
-                            const float2 hprev = i > 0 ? make_float2(hv[i - 1][s], hv[i - 1][s + 1])
-                                                       : make_float2(ch_ok ? hsrc[s] : 0.f, ch_ok ? hsrc[s + 1] : 0.f);
-                            const float2 lam = fma2(g2, Cp, make_float2(carry[s], carry[s + 1]));
-                            dup = fma2(lam, make_float2(Bv[s], Bv[s + 1]), dup);
-                            const float2 cn = mul2(make_float2(av[i][s], av[i][s + 1]), lam);
-                            const float2 q = mul2(cn, hprev);
-                            ddp = fma2(make_float2(A2[s], A2[s + 1]), q, ddp);
-                            const float2 na = fma2(dl2, q, make_float2(dA[s], dA[s + 1]));
-                            dA[s] = na.x; dA[s + 1] = na.y;
-                            y0p = fma2(Cp, hcur, y0p);
-                            const float2 cb = mul2(lam, dlu2), cc = mul2(g2, hcur);
-                            cB[s] = cb.x; cB[s + 1] = cb.y;
-                            cC[s] = cc.x; cC[s + 1] = cc.y;
-                            carry[s] = cn.x; carry[s + 1] = cn.y;
+                            cB[s] = cb2[s / 2].x; cB[s + 1] = cb2[s / 2].y;
+                            cC[s] = cc2[s / 2].x; cC[s + 1] = cc2[s / 2].y;
                         }
-                        du_p = dup.x + dup.y;
-                        dd_p = ddp.x + ddp.y;
-                        y0_p = y0p.x + y0p.y;
                     } else {
-                        const float hprev = i > 0 ? hv[i - 1][0] : (ch_ok ? hsrc[0] : 0.f);
-                        const float lam = fmaf(ss.z, Cv[0], carry[0]);
-                        du_p = lam * Bv[0];
-                        const float cn = av[i][0] * lam;
-                        const float q = cn * hprev;
-                        dd_p = A2[0] * q;
-                        dA[0] = fmaf(ss.x, q, dA[0]);
-                        y0_p = Cv[0] * hv[i][0];
-                        cB[0] = lam * ss.y;
-                        cC[0] = ss.z * hv[i][0];
-                        carry[0] = cn;
+#pragma unroll
+                        for (int e = 0; e < 2; e++) {
+                            const float ge = e ? g2.y : g2.x, dle = e ? du.z : du.x, dlue = e ? du.w : du.y;
+                            const float hprev =
+                                i > 0 ? hv[i - 1][e][0] : (ok[e] ? hsrc[e * S] : 0.f);
+                            const float lam = fmaf(ge, Cv[0], carry[e][0]);
+                            sumB[e] = lam * Bv[0];
+                            const float cn = av[i][e][0] * lam;
+                            const float q = cn * hprev;
+                            sumQ[e] = A2[e][0] * q;
+                            dA[e][0] = fmaf(dle, q, dA[e][0]);
+                            y0[e] = Cv[0] * hv[i][e][0];
+                            cB[0] = e ? fmaf(lam, dlue, cB[0]) : lam * dlue;
+                            cC[0] = e ? fmaf(ge, hv[i][e][0], cC[0]) : ge * hv[i][e][0];
+                            carry[e][0] = cn;
+                        }
                     }
-                    // sums over the warp's states of the channel: lane g = 0 keeps
-                    // (sum lam B, sum A q), lane g = 1 keeps y0
+                    // sums over the warp's states: lane g of a pair keeps channel c0 + g
+                    // and adds the partner's partial sums of that channel
                     if constexpr (G == 2) {
-                        const float x1 = __shfl_xor_sync(kFull, g == 0 ? y0_p : du_p, 1);
-                        const float x2 = __shfl_xor_sync(kFull, dd_p, 1);
-                        if (g == 0) sOa[w][r][ch] = make_float2(du_p + x1, dd_p + x2);
-                        else sOb[w][r][ch] = x1 + y0_p;
+                        const float xB = __shfl_xor_sync(kFull, g ? sumB[0] : sumB[1], 1);
+                        const float xQ = __shfl_xor_sync(kFull, g ? sumQ[0] : sumQ[1], 1);
+                        const float xY = __shfl_xor_sync(kFull, g ? y0[0] : y0[1], 1);
+                        sOu[w][r][lane] = (g ? sumB[1] : sumB[0]) + xB;
+                        sOd[w][r][lane] = (g ? sumQ[1] : sumQ[0]) + xQ;
+                        sOy[w][r][lane] = (g ? y0[1] : y0[0]) + xY;
                     } else {
-                        sOa[w][r][ch] = make_float2(du_p, dd_p);
-                        sOb[w][r][ch] = y0_p;
+                        *reinterpret_cast<float2*>(&sOu[w][r][c0]) = make_float2(sumB[0], sumB[1]);
+                        *reinterpret_cast<float2*>(&sOd[w][r][c0]) = make_float2(sumQ[0], sumQ[1]);
+                        *reinterpret_cast<float2*>(&sOy[w][r][c0]) = make_float2(y0[0], y0[1]);
                     }
-                    // stage dB / dC contributions (summed over the channels below)
-                    stage_contrib<S, NPW, BLK>(sRw, i, cB, cC, ch, g * S);
+                    // stage dB / dC contributions (summed over the pairs below)
+                    stage_contrib<S, NPW, BLK>(sRw, i, cB, cC, pp, g * S);
                 }
                 __syncwarp();  // staged contributions visible to every lane of the warp
-                reduce_staged<CH, NPW, N, BLK>(sRw, bc0, bc1, n_w, ts, t_end, lane);
+                reduce_staged<PAIRS, NPW, N, BLK>(sRw, bc0, bc1, n_w, ts, t_end, lane);
                 __syncwarp();  // the sums have read the staging before the next sub-chunk restages it
             }
-            __syncthreads();  // every warp's per-step sums are in sOa / sOb
-            // ---- epilogue: du, ddelta, dz of step t0 + pr for channels pc0 .. pc0 + CPL
-            {
-                // steps past t_end (last tile only) are not stored and add nothing; their
-                // per-step sums may be unwritten (a sub-chunk wholly past the end is skipped)
-                const int64_t t = t0 + pr;
+            __syncthreads();  // every warp's per-step sums are in sOu / sOd / sOy
+            // ---- epilogue: du, ddelta, dz of the (step, 4-channel group) items.
+            // Steps past t_end (last tile only) are not stored and add nothing;
+            // their per-step sums may be unwritten (a sub-chunk wholly past the
+            // end is skipped).
+#pragma unroll
+            for (int it = 0; it < ITEMS; it++) {
+                const int id = tid + it * THREADS;
+                const int r = id / NGRP, q = id % NGRP;
+                const int cg = q * GRP;
+                const int64_t t = t0 + r;
                 const bool tv = t < t_end;
-                float vdu[CPL], vdx[CPL], vdz[CPL], eD[CPL], eb[CPL];
+                float4 su = *reinterpret_cast<const float4*>(&sOu[0][r][cg]);
+                float4 sd = *reinterpret_cast<const float4*>(&sOd[0][r][cg]);
+                float4 sy = *reinterpret_cast<const float4*>(&sOy[0][r][cg]);
 #pragma unroll
-                for (int c = 0; c < CPL; c++) {
-                    eD[c] = sAcc[0][c][tid];
-                    eb[c] = sAcc[1][c][tid];
+                for (int ww = 1; ww < NW; ww++) {
+                    const float4 ou = *reinterpret_cast<const float4*>(&sOu[ww][r][cg]);
+                    const float4 od = *reinterpret_cast<const float4*>(&sOd[ww][r][cg]);
+                    const float4 oy = *reinterpret_cast<const float4*>(&sOy[ww][r][cg]);
+                    su.x += ou.x; su.y += ou.y; su.z += ou.z; su.w += ou.w;
+                    sd.x += od.x; sd.y += od.y; sd.z += od.z; sd.w += od.w;
+                    sy.x += oy.x; sy.y += oy.y; sy.z += oy.z; sy.w += oy.w;
                 }
+                const float4 dua = sDU[r][bpair_slot<PAIRS>(cg / 2)], dub = sDU[r][bpair_slot<PAIRS>(cg / 2 + 1)];
+                const float2 gga = sG[r][bpair_slot<PAIRS>(cg / 2)], ggb = sG[r][bpair_slot<PAIRS>(cg / 2 + 1)];
+                const float4 u4 = *reinterpret_cast<const float4*>(&sEu[r][cg]);
+                const float4 s4 = *reinterpret_cast<const float4*>(&sEs[r][cg]);
+                const float4 z4 = *reinterpret_cast<const float4*>(&sEz[r][cg]);
+                const float vsu[4] = {su.x, su.y, su.z, su.w}, vsd[4] = {sd.x, sd.y, sd.z, sd.w},
+                            vsy[4] = {sy.x, sy.y, sy.z, sy.w};
+                const float vdl[4] = {dua.x, dua.z, dub.x, dub.z}, vg[4] = {gga.x, gga.y, ggb.x, ggb.y};
+                const float vu[4] = {u4.x, u4.y, u4.z, u4.w}, vs[4] = {s4.x, s4.y, s4.z, s4.w},
+                            vz[4] = {z4.x, z4.y, z4.z, z4.w};
+                float vdu[GRP], vdx[GRP], vdz[GRP];
 #pragma unroll
-                for (int c = 0; c < CPL; c++) {
-                    const int cc = pc0 + c;
-                    float2 so = sOa[0][pr][cc];
-                    float y0 = sOb[0][pr][cc];
-#pragma unroll
-                    for (int q = 1; q < NW; q++) {
-                        const float2 o = sOa[q][pr][cc];
-                        so.x += o.x;
-                        so.y += o.y;
-                        y0 += sOb[q][pr][cc];
-                    }
-                    const float4 ss = sS[pr][cc];
-                    const float2 se = sE[pr][cc];
-                    vdu[c] = fmaf(ss.z, sDv[cc], ss.x * so.x);
-                    vdx[c] = fmaf(se.x, so.x, so.y * kLn2) * ss.w;
-                    vdz[c] = se.y * fmaf(sDv[cc], se.x, y0);
-                    eD[c] = fmaf(ss.z, se.x, eD[c]);  // g = u = 0 on padded steps
-                    eb[c] += tv ? vdx[c] : 0.f;
-                }
-#pragma unroll
-                for (int c = 0; c < CPL; c++) {
-                    sAcc[0][c][tid] = eD[c];
-                    sAcc[1][c][tid] = eb[c];
+                for (int c = 0; c < GRP; c++) {
+                    const float Dv = sDv[cg + c];
+                    vdu[c] = fmaf(vg[c], Dv, vdl[c] * vsu[c]);
+                    vdx[c] = fmaf(vu[c], vsu[c], vsd[c] * kLn2) * vs[c];
+                    vdz[c] = vz[c] * fmaf(Dv, vu[c], vsy[c]);
+                    sAcc[0][it * GRP + c][tid] = fmaf(vg[c], vu[c], sAcc[0][it * GRP + c][tid]);  // g = u = 0 past t_end
+                    sAcc[1][it * GRP + c][tid] += tv ? vdx[c] : 0.f;
                 }
                 if (tv) {
-                    const int64_t off = (b * L + t) * Dch + d0 + pc0;
-                    store_run<CPL>(a.du + off, vdu, d0 + pc0, Dch, ofast);
-                    store_run<CPL>(a.ddelta + off, vdx, d0 + pc0, Dch, ofast);
-                    if (z) store_run<CPL>(a.dz + off, vdz, d0 + pc0, Dch, ofast);
+                    const int64_t off = (b * L + t) * Dch + d0 + cg;
+                    store_run<GRP>(a.du + off, vdu, d0 + cg, Dch, ofast);
+                    store_run<GRP>(a.ddelta + off, vdx, d0 + cg, Dch, ofast);
+                    if (z) store_run<GRP>(a.dz + off, vdz, d0 + cg, Dch, ofast);
                 }
             }
         }
-        __syncthreads();  // the next prologue restages sS / sE / sB / sC
+        __syncthreads();  // the next prologue restages the tile
     }
 
     if constexpr (!MAIN) {
-        if (ch_ok) {
-            float2* out = reinterpret_cast<float2*>(a.ws_rsum) + (row * p.K + k) * N + n0;
 #pragma unroll
-            for (int s = 0; s < S; s++) out[s] = make_float2(Pr[s], carry[s]);
-        }
-    } else {
-        if (ch_ok) {
-            float* o = a.ws_dA + ((b * p.K + k) * Dch + d) * N + n0;
+        for (int e = 0; e < 2; e++) {
+            if (ok[e]) {
+                float2* out = reinterpret_cast<float2*>(a.ws_rsum) + (row[e] * p.K + k) * N + n0;
 #pragma unroll
-            for (int s = 0; s < S; s++) o[s] = dA[s];
-        }
-        // dD / ddelta_bias: the kTT threads sharing a channel set (consecutive
-        // lanes of one warp) hold partials over their rows; combine them (xor
-        // butterfly over the row bits, fixed order)
-        float eD[CPL], eb[CPL];
-#pragma unroll
-        for (int c = 0; c < CPL; c++) {
-            eD[c] = sAcc[0][c][tid];
-            eb[c] = sAcc[1][c][tid];
-        }
-#pragma unroll
-        for (int c = 0; c < CPL; c++) {
-#pragma unroll
-            for (int mk = 1; mk < kTT; mk <<= 1) {
-                const float oD = __shfl_xor_sync(kFull, eD[c], mk), ob = __shfl_xor_sync(kFull, eb[c], mk);
-                const bool low = (pr & mk) == 0;
-                eD[c] = low ? eD[c] + oD : oD + eD[c];
-                eb[c] = low ? eb[c] + ob : ob + eb[c];
+                for (int s = 0; s < S; s++) out[s] = make_float2(Pr[e][s], carry[e][s]);
             }
         }
-        if (pr == 0) {
+    } else {
 #pragma unroll
-            for (int c = 0; c < CPL; c++) {
-                if (d0 + pc0 + c < Dch) {
-                    a.ws_dD[(b * p.K + k) * Dch + d0 + pc0 + c] = eD[c];
-                    a.ws_db[(b * p.K + k) * Dch + d0 + pc0 + c] = eb[c];
+        for (int e = 0; e < 2; e++) {
+            if (ok[e]) {
+                float* o = a.ws_dA + ((b * p.K + k) * Dch + dd[e]) * N + n0;
+#pragma unroll
+                for (int s = 0; s < S; s++) o[s] = dA[e][s];
+            }
+        }
+        // dD / ddelta_bias of each channel: the partials of the items that own it
+        // (one per step of the tile) added in step order
+        for (int cc = tid; cc < CH; cc += THREADS) {
+            if (d0 + cc < Dch) {
+                const int q = cc / GRP, c = cc % GRP;
+                float aD = 0.f, ab = 0.f;
+#pragma unroll
+                for (int r = 0; r < kTT; r++) {
+                    const int id = r * NGRP + q;
+                    const int th = id % THREADS, itr = id / THREADS;
+                    aD += sAcc[0][itr * GRP + c][th];
+                    ab += sAcc[1][itr * GRP + c][th];
                 }
+                a.ws_dD[(b * p.K + k) * Dch + d0 + cc] = aD;
+                a.ws_db[(b * p.K + k) * Dch + d0 + cc] = ab;
             }
         }
     }
 }
-
 // dB / dC: sum of the per-tile partials, tiles in ascending order.  A thread
 // owns 4 consecutive outputs (16-byte streaming loads, 8 tiles in flight)
 // when N is a multiple of 4, one output otherwise.

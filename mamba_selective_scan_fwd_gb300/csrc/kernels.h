@@ -38,14 +38,15 @@ struct BwdLayout {
 
 constexpr int kModeY = 0, kModeSummary = 1, kModeCkpt = 2, kModeYSave = 3;
 
-// Block layout shared by the forward and backward scans: a block covers
-// kChannelsPerBlock channels (32 for N = 1) of one batch row and one time
-// chunk.  For N >= 16 it has two warps that split the states of every
-// channel; within a warp G = 2 adjacent lanes share a channel (one lane for
-// N = 1), so a lane holds N / (2 * warps) states.
-constexpr int kChannelsPerBlock = 16;
+// Block layout shared by the forward and backward scans.  A lane holds S
+// states of two adjacent channels (a channel pair), so every B / C value it
+// reads from shared memory serves two channels.  For N >= 16 a block has two
+// warps that split the states of every channel; within a warp G = 2 adjacent
+// lanes share a channel pair (one lane for N = 1).  A block therefore covers
+// 2 * 32 / G channels (32, or 64 for N = 1) of one batch row and one time
+// chunk.
 __host__ __device__ constexpr int fwd_warps(int64_t N) { return N >= 16 ? 2 : 1; }
-__host__ __device__ constexpr int64_t channels_per_block(int64_t N) { return N >= 2 ? kChannelsPerBlock : 32; }
+__host__ __device__ constexpr int64_t channels_per_block(int64_t N) { return N >= 2 ? 32 : 64; }
 
 // Launch plan: one block per (batch, channel tile, time chunk).  The time
 // chunking (K, Lc) is shared by every kernel of a call.
@@ -55,7 +56,7 @@ struct FPlan {
     int64_t Lc;      // chunk length (multiple of 32); the last chunk may be shorter
 };
 
-constexpr int64_t kTargetWarps = 2432;  // 16 warps on each of 152 SMs
+constexpr int64_t kTargetWarps = 1216;  // 8 warps on each of 152 SMs
 constexpr int64_t kFwdMinChunk = 128;
 
 // A pure function of the sizes (the same sizes always chunk the same way).
