@@ -105,27 +105,6 @@ __device__ __forceinline__ void softplus_and_sigmoid(float x, float& sp, float& 
     sg = x >= 0.f ? r : e * r;
 }
 
-// Asynchronous copy of S floats (a lane's saved state) from global to shared
-// memory; both addresses are aligned to the copy size.
-template <int S>
-__device__ __forceinline__ void cp_async_state(float* dst, const float* src) {
-    const unsigned sa = (unsigned)__cvta_generic_to_shared(dst);
-    if constexpr (S % 4 == 0) {
-#pragma unroll
-        for (int q = 0; q < S; q += 4)
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa + 4 * q), "l"(src + q) : "memory");
-    } else {
-        asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(sa), "l"(src), "n"(S * 4) : "memory");
-    }
-}
-
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-
-template <int PENDING>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(PENDING) : "memory");
-}
-
 template <int S>
 __device__ __forceinline__ void ld_state(const float* p, float (&v)[S]) {
     if constexpr (S % 4 == 0) {
@@ -251,7 +230,12 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
     // per-(t, d) staging of the scan, one entry per channel pair at bpair_slot
     __shared__ float4 sDU[kTT][PAIRS + 1];  // (Delta, Delta*u) of both channels
     __shared__ float2 sG[kTT][GP];          // g of both channels
-    __shared__ __align__(16) unsigned char sBC[kTT][BCROW];  // raw B / C values by state group
+    // raw B / C values by state group, double buffered: the next tile's rows are
+    // copied in while the current tile is walked
+    __shared__ __align__(16) unsigned char sBC[2][kTT][BCROW];
+    // raw runs of delta, u, dy, z of the next tile, copied in asynchronously by
+    // the thread that later converts them
+    __shared__ __align__(16) T sRaw[4][kTT][CH];
     // per-(t, d) terms only the epilogue reads, channel fastest: u, sig(x), dz factor
     __shared__ __align__(16) float sEu[MAIN ? kTT : 1][MAIN ? EP : 4];
     __shared__ __align__(16) float sEs[MAIN ? kTT : 1][MAIN ? EP : 4];
@@ -264,8 +248,8 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
     __shared__ __align__(16) float sOy[MAIN ? NW : 1][MAIN ? kTT : 1][MAIN ? EP : 4];
     // dD / ddelta_bias partials of each epilogue thread's items (thread fastest)
     __shared__ float sAcc[MAIN ? 2 : 1][MAIN ? ITEMS * GRP : 1][THREADS];
-    // restart states of the next two sub-chunks: 2 S floats per lane (double buffered)
-    __shared__ __align__(16) float sH[MAIN ? 2 : 1][MAIN ? THREADS * 2 * S : 4];
+    // restart states of a tile's sub-chunks, 2 S floats per lane, double buffered by tile
+    __shared__ __align__(16) float sH[MAIN ? 2 : 1][MAIN ? kTT / kSub : 1][MAIN ? THREADS * 2 * S : 4];
     __shared__ float sBias[CH], sDv[CH];
 
     const FwdArgs& f = a.f;
@@ -351,20 +335,60 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
     float* bc0 = a.ws_bc + ((int64_t)tile * f.Bsz + b) * L * N;                  // dB partials of this tile
     float* bc1 = a.ws_bc + ((int64_t)(p.tiles_b + tile) * f.Bsz + b) * L * N;    // dC partials
     float* sRw = &sR[MAIN ? w : 0][0];
-    // restart state of sub-chunk j lives in sH[j & 1][tid * 2S ..] (S floats per
-    // channel); each lane copies and reads only its own slots, so the copies need
-    // no barrier.  The last sub-chunk's is requested here, each earlier one a
-    // sub-chunk ahead.
-    if (MAIN) {
-        const int64_t jlast = (t_end - t_begin + kSub - 1) / kSub - 1;
-        cp_async_state<S>(&sH[jlast & 1][tid * 2 * S], ck0 + jlast * ck_stride);
-        cp_async_state<S>(&sH[jlast & 1][tid * 2 * S + S], ck1 + jlast * ck_stride);
+
+    // Asynchronous copies of tile mm, one commit group: the thread's item runs
+    // (when the tile's rows are whole aligned vectors), the B / C rows into
+    // sBC[mm & 1] (when a state group half is at least 4 bytes), and the
+    // restart states of the tile's sub-chunks into the lane's own slots of
+    // sH[mm & 1] (S floats per channel).  Each thread converts the runs it
+    // copied; the states are read by the lane that copied them.
+    constexpr bool ASYNC_BC = S * C::ESZ >= 4;
+    auto issue = [&](int64_t mm) {
+        const int64_t tt = t_begin + mm * kTT;
+        const int buf = (int)(mm & 1);
+        if (pfast) {
+#pragma unroll
+            for (int it = 0; it < ITEMS; it++) {
+                const int id = tid + it * THREADS;
+                const int r = id / NGRP, cg = (id % NGRP) * GRP;
+                const int64_t t = tt + r;
+                if (t < t_end) {
+                    const int64_t off = (b * L + t) * Dch + d0 + cg;
+                    cp_async_bytes<GRP * C::ESZ>(&sRaw[0][r][cg], delta + off);
+                    cp_async_bytes<GRP * C::ESZ>(&sRaw[1][r][cg], u + off);
+                    cp_async_bytes<GRP * C::ESZ>(&sRaw[2][r][cg], dy + off);
+                    if (z) cp_async_bytes<GRP * C::ESZ>(&sRaw[3][r][cg], z + off);
+                }
+            }
+        }
+        if constexpr (ASYNC_BC) {
+            for (int id = tid; id < (MAIN ? 2 : 1) * kTT; id += THREADS) {
+                const int half = MAIN ? id / kTT : 1, r = id % kTT;
+                const int64_t t = tt + r;
+                cp_async_bc_row<T, N, S>(&sBC[buf][r][0], half, (half ? Cm : Bm) + (b * L + (t < t_end ? t : 0)) * N,
+                                         t < t_end);
+            }
+        }
+        if (MAIN) {
+#pragma unroll
+            for (int sub = 0; sub < kTT / kSub; sub++) {
+                const int64_t ts = tt + sub * kSub;
+                if (ts < t_end) {
+                    const int64_t j = (ts - t_begin) / kSub;
+                    cp_async_bytes<S * 4>(&sH[buf][sub][tid * 2 * S], ck0 + j * ck_stride);
+                    cp_async_bytes<S * 4>(&sH[buf][sub][tid * 2 * S + S], ck1 + j * ck_stride);
+                }
+            }
+        }
         cp_async_commit();
-    }
+    };
+    issue(ntile - 1);
     __syncthreads();  // sBias / sDv / sAcc before the first prologue
 
     for (int64_t m = ntile - 1; m >= 0; m--) {
         const int64_t t0 = t_begin + m * kTT;
+        const int buf = (int)(m & 1);
+        cp_async_wait<0>();  // this thread's copies of the tile
         // ---- prologue: (step, 4-channel group) items of the tile
 #pragma unroll
         for (int it = 0; it < ITEMS; it++) {
@@ -375,11 +399,18 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
             const bool rv = t < t_end;
             uint32_t rd[RWH], ru[RWH], rz[RWH], rg[RWH];
             if (rv) {
-                const int64_t off = (b * L + t) * Dch + d0 + cg;
-                load_run<T, GRP, RWH>(delta, off, d0 + cg, Dch, pfast, rd);
-                load_run<T, GRP, RWH>(u, off, d0 + cg, Dch, pfast, ru);
-                load_run<T, GRP, RWH>(dy, off, d0 + cg, Dch, pfast, rg);
-                if (z) load_run<T, GRP, RWH>(z, off, d0 + cg, Dch, pfast, rz);
+                if (pfast) {
+                    lds_words<GRP * C::ESZ, RWH>(&sRaw[0][r][cg], rd);
+                    lds_words<GRP * C::ESZ, RWH>(&sRaw[1][r][cg], ru);
+                    lds_words<GRP * C::ESZ, RWH>(&sRaw[2][r][cg], rg);
+                    if (z) lds_words<GRP * C::ESZ, RWH>(&sRaw[3][r][cg], rz);
+                } else {
+                    const int64_t off = (b * L + t) * Dch + d0 + cg;
+                    load_run<T, GRP, RWH>(delta, off, d0 + cg, Dch, false, rd);
+                    load_run<T, GRP, RWH>(u, off, d0 + cg, Dch, false, ru);
+                    load_run<T, GRP, RWH>(dy, off, d0 + cg, Dch, false, rg);
+                    if (z) load_run<T, GRP, RWH>(z, off, d0 + cg, Dch, false, rz);
+                }
             }
             float dl[GRP], dlu[GRP], gg[GRP], uu[GRP], sgx[GRP], dzf[GRP];
 #pragma unroll
@@ -417,15 +448,18 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                 *reinterpret_cast<float4*>(&sEz[r][cg]) = make_float4(dzf[0], dzf[1], dzf[2], dzf[3]);
             }
         }
-        // B / C rows of the tile's steps (the reverse summary needs only C)
-        for (int id = tid; id < (MAIN ? 2 : 1) * kTT; id += THREADS) {
-            const int half = MAIN ? id / kTT : 1, r = id % kTT;
-            const int64_t t = t0 + r;
-            uint32_t wv[NWd];
-            if (t < t_end) load_words<C::NB, NWd>((half ? Cm : Bm) + (b * L + t) * N, wv);
-            stage_bc_row<T, N, S, NWd>(&sBC[r][0], half, wv, t < t_end);
+        if constexpr (!ASYNC_BC) {
+            // B / C rows of the tile's steps (the reverse summary needs only C), staged here
+            for (int id = tid; id < (MAIN ? 2 : 1) * kTT; id += THREADS) {
+                const int half = MAIN ? id / kTT : 1, r = id % kTT;
+                const int64_t t = t0 + r;
+                uint32_t wv[NWd];
+                if (t < t_end) load_words<C::NB, NWd>((half ? Cm : Bm) + (b * L + t) * N, wv);
+                stage_bc_row<T, N, S, NWd>(&sBC[buf][r][0], half, wv, t < t_end);
+            }
         }
-        __syncthreads();
+        __syncthreads();  // staging complete; every thread is done reading sRaw
+        if (m > 0) issue(m - 1);
 
         if constexpr (!MAIN) {
             // ---- reverse summary: adjoint walk from a zero carry and the chunk's
@@ -435,7 +469,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                 const float4 du = sDU[i][pslot];
                 const float2 g2 = sG[i][pslot];
                 float Bv[S], Cv[S];
-                ld_bc<T, S>(&sBC[i][sg * SGB], Bv, Cv);
+                ld_bc<T, S>(&sBC[buf][i][sg * SGB], Bv, Cv);
 #pragma unroll
                 for (int e = 0; e < 2; e++) {
 #pragma unroll
@@ -456,17 +490,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
             for (int sub = kTT / kSub - 1; sub >= 0; sub--) {
                 const int64_t ts = t0 + sub * kSub;
                 if (ts >= t_end) continue;
-                // request the previous sub-chunk's restart state, then wait for this one's
-                const int64_t jsub = (ts - t_begin) / kSub;
-                const float* hsrc = &sH[jsub & 1][tid * 2 * S];
-                if (jsub > 0) {
-                    cp_async_state<S>(&sH[(jsub - 1) & 1][tid * 2 * S], ck0 + (jsub - 1) * ck_stride);
-                    cp_async_state<S>(&sH[(jsub - 1) & 1][tid * 2 * S + S], ck1 + (jsub - 1) * ck_stride);
-                    cp_async_commit();
-                    cp_async_wait<1>();
-                } else {
-                    cp_async_wait<0>();
-                }
+                const float* hsrc = &sH[buf][sub][tid * 2 * S];  // copied with the tile's rows
                 // recompute the states and decays of the sub-chunk
                 float hv[kSub][2][S], av[kSub][2][S];
                 {
@@ -482,7 +506,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                         const int r = sub * kSub + i;
                         const float4 du = sDU[r][pslot];
                         float Bv[S];
-                        ld_b<T, S>(&sBC[r][sg * SGB], Bv);
+                        ld_b<T, S>(&sBC[buf][r][sg * SGB], Bv);
 #pragma unroll
                         for (int e = 0; e < 2; e++) {
                             if constexpr (S >= 2) {
@@ -513,7 +537,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                     const float4 du = sDU[r][pslot];
                     const float2 g2 = sG[r][pslot];
                     float Bv[S], Cv[S];
-                    ld_bc<T, S>(&sBC[r][sg * SGB], Bv, Cv);
+                    ld_bc<T, S>(&sBC[buf][r][sg * SGB], Bv, Cv);
                     float sumB[2], sumQ[2], y0[2];
                     float cB[S], cC[S];
                     if constexpr (S >= 2) {

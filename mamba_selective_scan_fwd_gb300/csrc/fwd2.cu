@@ -85,7 +85,12 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(F
     // delta_eff * u) and (gate, D * u) of both channels; rows of PAIRS + 1 units
     __shared__ float4 sDU[kRow][C::PAIRS + 1];
     __shared__ float4 sGD[NOY ? 1 : kRow][NOY ? 1 : C::PAIRS + 1];
-    __shared__ __align__(16) unsigned char sBC[kRow][BCROW];  // raw B / C values by state group
+    // raw B / C values by state group, double buffered: the next tile's rows are
+    // copied in while the scan reads the current one's
+    __shared__ __align__(16) unsigned char sBC[2][kRow][BCROW];
+    // raw runs of delta, u, z of the next tile, copied in asynchronously by the
+    // thread that later converts them
+    __shared__ __align__(16) T sRaw[NOY ? 2 : 3][kRow][CH];
     __shared__ __align__(16) float sY[NOY ? 1 : NW][NOY ? 1 : kRow][YP];  // per-warp partial readouts
     __shared__ float sBias[CH], sDv[CH];
 
@@ -148,9 +153,42 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(F
     const int64_t ck_stride = a.Bsz * Dch * N;
     float* ck0 = SAVE ? ckpt + (k * (p.Lc / kSub)) * ck_stride + row0 * N + n0 : nullptr;
     float* ck1 = SAVE ? ckpt + (k * (p.Lc / kSub)) * ck_stride + row1 * N + n0 : nullptr;
+
+    // Asynchronous copies of the tile starting at tt: the thread's item runs
+    // (when the tile's rows are whole aligned vectors) and the B / C rows into
+    // sBC[buf] (when a state group half is at least 4 bytes); one commit group.
+    constexpr bool ASYNC_BC = S * C::ESZ >= 4;
+    auto issue = [&](int64_t tt, int buf) {
+        if (fast) {
+#pragma unroll
+            for (int it = 0; it < ITEMS; it++) {
+                const int id = tid + it * THREADS;
+                const int r = id / NGRP, cg = (id % NGRP) * GRP;
+                const int64_t t = tt + r;
+                if (t < t_end) {
+                    const int64_t off = (b * L + t) * Dch + d0 + cg;
+                    cp_async_bytes<GRP * C::ESZ>(&sRaw[0][r][cg], delta + off);
+                    cp_async_bytes<GRP * C::ESZ>(&sRaw[1][r][cg], u + off);
+                    if (!NOY && z) cp_async_bytes<GRP * C::ESZ>(&sRaw[NOY ? 1 : 2][r][cg], z + off);
+                }
+            }
+        }
+        if constexpr (ASYNC_BC) {
+            for (int id = tid; id < (NOY ? 1 : 2) * kRow; id += THREADS) {
+                const int half = id / kRow, r = id % kRow;
+                const int64_t t = tt + r;
+                cp_async_bc_row<T, N, S>(&sBC[buf][r][0], half, (half ? Cm : Bm) + (b * L + (t < t_end ? t : 0)) * N,
+                                         t < t_end);
+            }
+        }
+        cp_async_commit();
+    };
+    issue(t_begin, 0);
     __syncthreads();  // sBias / sDv
 
     for (int64_t t0 = t_begin; t0 < t_end; t0 += kRow) {
+        const int buf = (int)(((t0 - t_begin) / kRow) & 1);
+        cp_async_wait<0>();  // this thread's copies of the tile
         // ---- prologue: (step, 8-channel group) items, then the B / C rows
 #pragma unroll
         for (int it = 0; it < ITEMS; it++) {
@@ -161,10 +199,16 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(F
             const int cg = q * GRP;  // first channel of the group
             uint32_t rd[RW], ru[RW], rz[RW];
             if (rv) {
-                const int64_t off = (b * L + t) * Dch + d0 + cg;
-                load_run<T, GRP, RW>(delta, off, d0 + cg, Dch, fast, rd);
-                load_run<T, GRP, RW>(u, off, d0 + cg, Dch, fast, ru);
-                if (!NOY && z) load_run<T, GRP, RW>(z, off, d0 + cg, Dch, fast, rz);
+                if (fast) {
+                    lds_words<GRP * C::ESZ, RW>(&sRaw[0][r][cg], rd);
+                    lds_words<GRP * C::ESZ, RW>(&sRaw[1][r][cg], ru);
+                    if (!NOY && z) lds_words<GRP * C::ESZ, RW>(&sRaw[NOY ? 1 : 2][r][cg], rz);
+                } else {
+                    const int64_t off = (b * L + t) * Dch + d0 + cg;
+                    load_run<T, GRP, RW>(delta, off, d0 + cg, Dch, false, rd);
+                    load_run<T, GRP, RW>(u, off, d0 + cg, Dch, false, ru);
+                    if (!NOY && z) load_run<T, GRP, RW>(z, off, d0 + cg, Dch, false, rz);
+                }
             }
 #pragma unroll
             for (int c = 0; c < GRP; c += 2) {
@@ -190,15 +234,18 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(F
                 if (!NOY) sGD[r][slot] = make_float4(gt[0], du_[0], gt[1], du_[1]);
             }
         }
-        // B / C rows of the tile's steps: row id = (tensor, step)
-        for (int id = tid; id < (NOY ? 1 : 2) * kRow; id += THREADS) {
-            const int half = id / kRow, r = id % kRow;
-            const int64_t t = t0 + r;
-            uint32_t wv[NWd];
-            if (t < t_end) load_words<C::NB, NWd>((half ? Cm : Bm) + (b * L + t) * N, wv);
-            stage_bc_row<T, N, S, NWd>(&sBC[r][0], half, wv, t < t_end);
+        if constexpr (!ASYNC_BC) {
+            // B / C rows of the tile's steps, row id = (tensor, step), staged here
+            for (int id = tid; id < (NOY ? 1 : 2) * kRow; id += THREADS) {
+                const int half = id / kRow, r = id % kRow;
+                const int64_t t = t0 + r;
+                uint32_t wv[NWd];
+                if (t < t_end) load_words<C::NB, NWd>((half ? Cm : Bm) + (b * L + t) * N, wv);
+                stage_bc_row<T, N, S, NWd>(&sBC[buf][r][0], half, wv, t < t_end);
+            }
         }
-        __syncthreads();
+        __syncthreads();  // staging complete; every thread is done reading sRaw
+        if (t0 + kRow < t_end) issue(t0 + kRow, buf ^ 1);
 
         // ---- scan: 32 steps of the lane's 2 x S states.  Steps past t_end (last
         // tile only) carry delta_eff = 0 and B = 0: the state stays unchanged.
@@ -227,7 +274,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(F
             }
             const float4 du = sDU[i][pslot];
             float Bv[S], Cv[S];
-            ld_bc<T, S>(&sBC[i][sg * SGB], Bv, Cv);
+            ld_bc<T, S>(&sBC[buf][i][sg * SGB], Bv, Cv);
             float yp[2];
             if constexpr (S >= 2) {
                 float2 ya[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};

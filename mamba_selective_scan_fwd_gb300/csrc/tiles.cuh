@@ -152,4 +152,48 @@ __device__ __forceinline__ void ld_b(const unsigned char* g, float (&Bv)[S]) {
     }
 }
 
+// Asynchronous global -> shared copy of NBYTES (4, 8 or a multiple of 16)
+// bytes; both addresses are aligned to min(NBYTES, 16).  Completion is
+// awaited per thread with cp_async_wait after cp_async_commit.
+template <int NBYTES>
+__device__ __forceinline__ void cp_async_bytes(void* dst, const void* src) {
+    const unsigned sa = (unsigned)__cvta_generic_to_shared(dst);
+    if constexpr (NBYTES % 16 == 0) {
+#pragma unroll
+        for (int q = 0; q < NBYTES; q += 16)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa + q),
+                         "l"(static_cast<const char*>(src) + q)
+                         : "memory");
+    } else {
+        static_assert(NBYTES == 4 || NBYTES == 8, "cp.async copies 4, 8 or 16 bytes");
+        asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(sa), "l"(src), "n"(NBYTES) : "memory");
+    }
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+template <int PENDING>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(PENDING) : "memory");
+}
+
+// Issue the copies of a B or C row (N io values at src) into the state
+// groups of a step's staging row (the layout of stage_bc_row), or zero the
+// groups of a step past the chunk end.  Needs S * esz >= 4 bytes.
+template <typename T, int N, int S>
+__device__ __forceinline__ void cp_async_bc_row(unsigned char* row, int half, const T* src, bool valid) {
+    constexpr int GB = S * (int)sizeof(T);
+    static_assert(GB >= 4, "a state group half of at least 4 bytes");
+#pragma unroll
+    for (int q = 0; q < N / S; q++) {
+        unsigned char* dst = row + q * 2 * GB + half * GB;
+        if (valid) {
+            cp_async_bytes<GB>(dst, src + q * S);
+        } else {
+#pragma unroll
+            for (int i = 0; i < GB; i += 4) *reinterpret_cast<unsigned int*>(dst + i) = 0u;
+        }
+    }
+}
+
 }  // namespace ss
