@@ -64,9 +64,11 @@ struct BCfg {
     static constexpr int RWH = GRP * ESZ / 4;       // 32-bit words of an item's run of one tensor
     static constexpr int NB = N * ESZ;
     static constexpr int NWd = NB >= 4 ? NB / 4 : 1;
-    static constexpr int NSG = N / S;               // state groups of a step
-    static constexpr int SGB = 2 * S * ESZ;         // bytes of a state group: S values of B, then S of C
-    static constexpr int BCROW = NSG * SGB;
+    // B / C staging as in the forward: N / S state groups of 2 S floats per step
+    static constexpr int BCF = 2 * N + 4;
+    static constexpr bool BC_DIRECT = ESZ == 4;
+    static constexpr bool BC_RAW = !BC_DIRECT && N * ESZ >= 4;
+    static constexpr int BC_BUFS = BC_DIRECT ? 2 : 1;
     static constexpr int EP = CH + 4;               // padded per-channel rows (floats)
     static constexpr int GP = PAIRS + 8;            // padded per-pair float2 rows
     // dB / dC staging of one warp: block (step slot j, tensor tau) holds PAIRS
@@ -226,13 +228,15 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
     constexpr bool MAIN = MODE == kRevMain;
     constexpr int NW = C::NW, NPW = C::NPW, S = C::S, G = C::G, PAIRS = C::PAIRS, CH = C::CH,
                   THREADS = C::THREADS, GRP = C::GRP, NGRP = C::NGRP, ITEMS = C::ITEMS, RWH = C::RWH,
-                  NWd = C::NWd, SGB = C::SGB, BCROW = C::BCROW, EP = C::EP, GP = C::GP, BLK = C::BLK;
+                  NWd = C::NWd, BCF = C::BCF, EP = C::EP, GP = C::GP, BLK = C::BLK;
     // per-(t, d) staging of the scan, one entry per channel pair at bpair_slot
     __shared__ float4 sDU[kTT][PAIRS + 1];  // (Delta, Delta*u) of both channels
     __shared__ float2 sG[kTT][GP];          // g of both channels
-    // raw B / C values by state group, double buffered: the next tile's rows are
-    // copied in while the current tile is walked
-    __shared__ __align__(16) unsigned char sBC[2][kTT][BCROW];
+    // B / C values by state group (f32); with f32 io double buffered, the next
+    // tile's rows being copied in while the current tile is walked
+    __shared__ __align__(16) float sBC[C::BC_BUFS][kTT][BCF];
+    // raw bf16 B / C rows of the next tile (converted into sBC by the prologue)
+    __shared__ __align__(16) T sBCraw[C::BC_RAW ? kTT : 1][2][C::BC_RAW ? N : 2];
     // raw runs of delta, u, dy, z of the next tile, copied in asynchronously by
     // the thread that later converts them
     __shared__ __align__(16) T sRaw[4][kTT][CH];
@@ -337,12 +341,11 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
     float* sRw = &sR[MAIN ? w : 0][0];
 
     // Asynchronous copies of tile mm, one commit group: the thread's item runs
-    // (when the tile's rows are whole aligned vectors), the B / C rows into
-    // sBC[mm & 1] (when a state group half is at least 4 bytes), and the
+    // (when the tile's rows are whole aligned vectors), the B / C rows (f32 into
+    // sBC[mm & 1]; bf16 raw into sBCraw), and the
     // restart states of the tile's sub-chunks into the lane's own slots of
     // sH[mm & 1] (S floats per channel).  Each thread converts the runs it
     // copied; the states are read by the lane that copied them.
-    constexpr bool ASYNC_BC = S * C::ESZ >= 4;
     auto issue = [&](int64_t mm) {
         const int64_t tt = t_begin + mm * kTT;
         const int buf = (int)(mm & 1);
@@ -361,12 +364,14 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                 }
             }
         }
-        if constexpr (ASYNC_BC) {
-            for (int id = tid; id < (MAIN ? 2 : 1) * kTT; id += THREADS) {
-                const int half = MAIN ? id / kTT : 1, r = id % kTT;
-                const int64_t t = tt + r;
-                cp_async_bc_row<T, N, S>(&sBC[buf][r][0], half, (half ? Cm : Bm) + (b * L + (t < t_end ? t : 0)) * N,
-                                         t < t_end);
+        for (int id = tid; id < (MAIN ? 2 : 1) * kTT; id += THREADS) {
+            const int half = MAIN ? id / kTT : 1, r = id % kTT;
+            const int64_t t = tt + r;
+            const T* src = (half ? Cm : Bm) + (b * L + (t < t_end ? t : 0)) * N;
+            if constexpr (C::BC_DIRECT) {
+                cp_async_bc_row<T, N, S>(reinterpret_cast<unsigned char*>(&sBC[buf][r][0]), half, src, t < t_end);
+            } else if constexpr (C::BC_RAW) {
+                if (t < t_end) cp_async_bytes<N * C::ESZ>(&sBCraw[r][half][0], src);
             }
         }
         if (MAIN) {
@@ -448,14 +453,18 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                 *reinterpret_cast<float4*>(&sEz[r][cg]) = make_float4(dzf[0], dzf[1], dzf[2], dzf[3]);
             }
         }
-        if constexpr (!ASYNC_BC) {
-            // B / C rows of the tile's steps (the reverse summary needs only C), staged here
+        if constexpr (!C::BC_DIRECT) {
+            // bf16 B / C rows of the tile's steps (the reverse summary needs only C),
+            // converted by the thread that copied them (or loaded here when too short to copy)
             for (int id = tid; id < (MAIN ? 2 : 1) * kTT; id += THREADS) {
                 const int half = MAIN ? id / kTT : 1, r = id % kTT;
                 const int64_t t = t0 + r;
                 uint32_t wv[NWd];
-                if (t < t_end) load_words<C::NB, NWd>((half ? Cm : Bm) + (b * L + t) * N, wv);
-                stage_bc_row<T, N, S, NWd>(&sBC[buf][r][0], half, wv, t < t_end);
+                if (t < t_end) {
+                    if constexpr (C::BC_RAW) lds_words<C::NB, NWd>(&sBCraw[r][half][0], wv);
+                    else load_words<C::NB, NWd>((half ? Cm : Bm) + (b * L + t) * N, wv);
+                }
+                stage_bc_row_f32<T, N, S, NWd>(&sBC[0][r][0], half, wv, t < t_end);
             }
         }
         __syncthreads();  // staging complete; every thread is done reading sRaw
@@ -469,7 +478,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                 const float4 du = sDU[i][pslot];
                 const float2 g2 = sG[i][pslot];
                 float Bv[S], Cv[S];
-                ld_bc<T, S>(&sBC[buf][i][sg * SGB], Bv, Cv);
+                ld_bc_f32<S>(&sBC[C::BC_DIRECT ? buf : 0][i][sg * 2 * S], Bv, Cv);
 #pragma unroll
                 for (int e = 0; e < 2; e++) {
 #pragma unroll
@@ -506,7 +515,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                         const int r = sub * kSub + i;
                         const float4 du = sDU[r][pslot];
                         float Bv[S];
-                        ld_b<T, S>(&sBC[buf][r][sg * SGB], Bv);
+                        ld_b_f32<S>(&sBC[C::BC_DIRECT ? buf : 0][r][sg * 2 * S], Bv);
 #pragma unroll
                         for (int e = 0; e < 2; e++) {
                             if constexpr (S >= 2) {
@@ -537,7 +546,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                     const float4 du = sDU[r][pslot];
                     const float2 g2 = sG[r][pslot];
                     float Bv[S], Cv[S];
-                    ld_bc<T, S>(&sBC[buf][r][sg * SGB], Bv, Cv);
+                    ld_bc_f32<S>(&sBC[C::BC_DIRECT ? buf : 0][r][sg * 2 * S], Bv, Cv);
                     float sumB[2], sumQ[2], y0[2];
                     float cB[S], cC[S];
                     if constexpr (S >= 2) {

@@ -53,9 +53,14 @@ struct FCfg {
     static constexpr int RW = GRP * ESZ / 4;        // 32-bit words of an item's run of one tensor
     static constexpr int NB = N * ESZ;              // bytes of a B / C row
     static constexpr int NWd = NB >= 4 ? NB / 4 : 1;  // 32-bit words per B / C row
-    static constexpr int NSG = N / S;               // state groups of a step
-    static constexpr int SGB = 2 * S * ESZ;         // bytes of a state group: S values of B, then S of C
-    static constexpr int BCROW = NSG * SGB;         // bytes of a step's B / C staging row
+    // B / C staging: a step's row holds N / S state groups of 2 S floats (S of
+    // B, then S of C), padded by 4 floats so that rows staged by consecutive
+    // threads start in different bank groups.  f32 io is copied straight into
+    // it (double buffered); bf16 rows are copied raw and converted once.
+    static constexpr int BCF = 2 * N + 4;
+    static constexpr bool BC_DIRECT = ESZ == 4;
+    static constexpr bool BC_RAW = !BC_DIRECT && N * ESZ >= 4;
+    static constexpr int BC_BUFS = BC_DIRECT ? 2 : 1;
     static constexpr int YP = CH + 4;               // padded shared row of partial readouts (floats)
     static_assert(kRow * NGRP % THREADS == 0, "whole items per thread");
     static_assert(CH == channels_per_block(N), "channel tile of the plan");
@@ -79,15 +84,16 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(F
     constexpr bool SAVE = MODE == kModeYSave || MODE == kModeCkpt;   // store the sub-chunk start states
     using C = FCfg<T, N>;
     constexpr int NW = C::NW, NPW = C::NPW, S = C::S, G = C::G, CH = C::CH, THREADS = C::THREADS, GRP = C::GRP,
-                  NGRP = C::NGRP, ITEMS = C::ITEMS, RW = C::RW, NWd = C::NWd, BCROW = C::BCROW, YP = C::YP,
-                  SGB = C::SGB;
+                  NGRP = C::NGRP, ITEMS = C::ITEMS, RW = C::RW, NWd = C::NWd, YP = C::YP, BCF = C::BCF;
     // per-(t, d) staging, one float4 per channel pair at pair_slot: (delta_eff,
     // delta_eff * u) and (gate, D * u) of both channels; rows of PAIRS + 1 units
     __shared__ float4 sDU[kRow][C::PAIRS + 1];
     __shared__ float4 sGD[NOY ? 1 : kRow][NOY ? 1 : C::PAIRS + 1];
-    // raw B / C values by state group, double buffered: the next tile's rows are
-    // copied in while the scan reads the current one's
-    __shared__ __align__(16) unsigned char sBC[2][kRow][BCROW];
+    // B / C values by state group (f32); with f32 io double buffered, the next
+    // tile's rows being copied in while the scan reads the current one's
+    __shared__ __align__(16) float sBC[C::BC_BUFS][kRow][BCF];
+    // raw bf16 B / C rows of the next tile (converted into sBC by the prologue)
+    __shared__ __align__(16) T sBCraw[C::BC_RAW ? kRow : 1][2][C::BC_RAW ? N : 2];
     // raw runs of delta, u, z of the next tile, copied in asynchronously by the
     // thread that later converts them
     __shared__ __align__(16) T sRaw[NOY ? 2 : 3][kRow][CH];
@@ -155,9 +161,8 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(F
     float* ck1 = SAVE ? ckpt + (k * (p.Lc / kSub)) * ck_stride + row1 * N + n0 : nullptr;
 
     // Asynchronous copies of the tile starting at tt: the thread's item runs
-    // (when the tile's rows are whole aligned vectors) and the B / C rows into
-    // sBC[buf] (when a state group half is at least 4 bytes); one commit group.
-    constexpr bool ASYNC_BC = S * C::ESZ >= 4;
+    // (when the tile's rows are whole aligned vectors) and the B / C rows (f32
+    // into sBC[buf]; bf16 raw into sBCraw); one commit group.
     auto issue = [&](int64_t tt, int buf) {
         if (fast) {
 #pragma unroll
@@ -173,12 +178,14 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(F
                 }
             }
         }
-        if constexpr (ASYNC_BC) {
-            for (int id = tid; id < (NOY ? 1 : 2) * kRow; id += THREADS) {
-                const int half = id / kRow, r = id % kRow;
-                const int64_t t = tt + r;
-                cp_async_bc_row<T, N, S>(&sBC[buf][r][0], half, (half ? Cm : Bm) + (b * L + (t < t_end ? t : 0)) * N,
-                                         t < t_end);
+        for (int id = tid; id < (NOY ? 1 : 2) * kRow; id += THREADS) {
+            const int half = id / kRow, r = id % kRow;
+            const int64_t t = tt + r;
+            const T* src = (half ? Cm : Bm) + (b * L + (t < t_end ? t : 0)) * N;
+            if constexpr (C::BC_DIRECT) {
+                cp_async_bc_row<T, N, S>(reinterpret_cast<unsigned char*>(&sBC[buf][r][0]), half, src, t < t_end);
+            } else if constexpr (C::BC_RAW) {
+                if (t < t_end) cp_async_bytes<N * C::ESZ>(&sBCraw[r][half][0], src);
             }
         }
         cp_async_commit();
@@ -234,14 +241,18 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(F
                 if (!NOY) sGD[r][slot] = make_float4(gt[0], du_[0], gt[1], du_[1]);
             }
         }
-        if constexpr (!ASYNC_BC) {
-            // B / C rows of the tile's steps, row id = (tensor, step), staged here
+        if constexpr (!C::BC_DIRECT) {
+            // bf16 B / C rows of the tile's steps, row id = (tensor, step), converted
+            // by the thread that copied them (or loaded here when too short to copy)
             for (int id = tid; id < (NOY ? 1 : 2) * kRow; id += THREADS) {
                 const int half = id / kRow, r = id % kRow;
                 const int64_t t = t0 + r;
                 uint32_t wv[NWd];
-                if (t < t_end) load_words<C::NB, NWd>((half ? Cm : Bm) + (b * L + t) * N, wv);
-                stage_bc_row<T, N, S, NWd>(&sBC[buf][r][0], half, wv, t < t_end);
+                if (t < t_end) {
+                    if constexpr (C::BC_RAW) lds_words<C::NB, NWd>(&sBCraw[r][half][0], wv);
+                    else load_words<C::NB, NWd>((half ? Cm : Bm) + (b * L + t) * N, wv);
+                }
+                stage_bc_row_f32<T, N, S, NWd>(&sBC[0][r][0], half, wv, t < t_end);
             }
         }
         __syncthreads();  // staging complete; every thread is done reading sRaw
@@ -274,7 +285,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(F
             }
             const float4 du = sDU[i][pslot];
             float Bv[S], Cv[S];
-            ld_bc<T, S>(&sBC[buf][i][sg * SGB], Bv, Cv);
+            ld_bc_f32<S>(&sBC[C::BC_DIRECT ? buf : 0][i][sg * 2 * S], Bv, Cv);
             float yp[2];
             if constexpr (S >= 2) {
                 float2 ya[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};

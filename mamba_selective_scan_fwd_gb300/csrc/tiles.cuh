@@ -1,7 +1,8 @@
 // Tile staging helpers shared by the forward and backward scans: io
 // elements held as 32-bit words (bf16 unpacks exactly to f32), vector loads
-// of row runs of the [B, L, D] tensors, and the raw B / C staging rows whose
-// state groups hold S values of B followed by S values of C.
+// of row runs of the [B, L, D] tensors, asynchronous copies into shared
+// memory, and the f32 B / C staging rows whose state groups hold S values of
+// B followed by S values of C.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -97,58 +98,61 @@ __device__ __forceinline__ void sts_words(void* p, const uint32_t* w) {
     }
 }
 
-// B and C values of one state group (S raw io values of B, then S of C) as floats.
-template <typename T, int S>
-__device__ __forceinline__ void ld_bc(const unsigned char* g, float (&Bv)[S], float (&Cv)[S]) {
-    constexpr int NB = 2 * S * (int)sizeof(T), NW = NB / 4;
-    uint32_t w[NW];
-    lds_words<NB, NW>(g, w);
+// B and C values of one f32 state group (S floats of B, then S of C).
+template <int S>
+__device__ __forceinline__ void ld_bc_f32(const float* g, float (&Bv)[S], float (&Cv)[S]) {
+    if constexpr (S % 4 == 0) {
 #pragma unroll
-    for (int s = 0; s < S; s++) {
-        Bv[s] = elem<T>(w, s);
-        Cv[s] = elem<T>(w, S + s);
+        for (int s = 0; s < S; s += 4) {
+            const float4 b = *reinterpret_cast<const float4*>(g + s), c = *reinterpret_cast<const float4*>(g + S + s);
+            Bv[s] = b.x; Bv[s + 1] = b.y; Bv[s + 2] = b.z; Bv[s + 3] = b.w;
+            Cv[s] = c.x; Cv[s + 1] = c.y; Cv[s + 2] = c.z; Cv[s + 3] = c.w;
+        }
+    } else if constexpr (S == 2) {
+        const float4 v = *reinterpret_cast<const float4*>(g);
+        Bv[0] = v.x; Bv[1] = v.y; Cv[0] = v.z; Cv[1] = v.w;
+    } else {
+        const float2 v = *reinterpret_cast<const float2*>(g);
+        Bv[0] = v.x; Cv[0] = v.y;
     }
 }
 
-// Copy a B or C row (N io values held as words) into the state groups of a
-// step's staging row: group q gets values q S .. q S + S at byte offset
-// q * 2 S esz + half * S esz (half 0: B, 1: C).  A row past the chunk end is
-// staged as zeros.
+// B values only of one f32 state group.
+template <int S>
+__device__ __forceinline__ void ld_b_f32(const float* g, float (&Bv)[S]) {
+    if constexpr (S % 4 == 0) {
+#pragma unroll
+        for (int s = 0; s < S; s += 4) {
+            const float4 b = *reinterpret_cast<const float4*>(g + s);
+            Bv[s] = b.x; Bv[s + 1] = b.y; Bv[s + 2] = b.z; Bv[s + 3] = b.w;
+        }
+    } else if constexpr (S == 2) {
+        const float2 b = *reinterpret_cast<const float2*>(g);
+        Bv[0] = b.x; Bv[1] = b.y;
+    } else {
+        Bv[0] = g[0];
+    }
+}
+
+// Write a B or C row (N io values held as words) as f32 into the state groups
+// of a step's staging row: group q holds floats q S .. q S + S of B, then of
+// C.  A row past the chunk end is staged as zeros.
 template <typename T, int N, int S, int NWd>
-__device__ __forceinline__ void stage_bc_row(unsigned char* row, int half, const uint32_t (&w)[NWd], bool valid) {
-    constexpr int ESZ = (int)sizeof(T);
-    constexpr int GB = S * ESZ;  // bytes of one half of a group
-    if constexpr (GB % 4 == 0) {
-        constexpr int GW = GB / 4;
+__device__ __forceinline__ void stage_bc_row_f32(float* row, int half, const uint32_t (&w)[NWd], bool valid) {
 #pragma unroll
-        for (int q = 0; q < N / S; q++) {
-            uint32_t v[GW];
+    for (int q = 0; q < N / S; q++) {
+        float* dst = row + q * 2 * S + half * S;
+        if constexpr (S % 4 == 0) {
 #pragma unroll
-            for (int i = 0; i < GW; i++) v[i] = valid ? w[q * GW + i] : 0u;
-            sts_words<GB, GW>(row + q * 2 * GB + half * GB, v);
+            for (int s = 0; s < S; s += 4)
+                *reinterpret_cast<float4*>(dst + s) =
+                    valid ? make_float4(elem<T>(w, q * S + s), elem<T>(w, q * S + s + 1), elem<T>(w, q * S + s + 2),
+                                        elem<T>(w, q * S + s + 3))
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+#pragma unroll
+            for (int s = 0; s < S; s++) dst[s] = valid ? elem<T>(w, q * S + s) : 0.f;
         }
-    } else {
-        // S = 1 with 2-byte values: one element per group half
-#pragma unroll
-        for (int q = 0; q < N; q++) {
-            const uint32_t word = w[q >> 1];
-            const unsigned short v = (unsigned short)((q & 1) ? (word >> 16) : (word & 0xffffu));
-            *reinterpret_cast<unsigned short*>(row + q * 2 * GB + half * GB) = valid ? v : (unsigned short)0;
-        }
-    }
-}
-
-// B values only of one state group (the first half of the group).
-template <typename T, int S>
-__device__ __forceinline__ void ld_b(const unsigned char* g, float (&Bv)[S]) {
-    constexpr int NB = S * (int)sizeof(T), NW = NB >= 4 ? NB / 4 : 1;
-    if constexpr (NB >= 4) {
-        uint32_t w[NW];
-        lds_words<NB, NW>(g, w);
-#pragma unroll
-        for (int s = 0; s < S; s++) Bv[s] = elem<T>(w, s);
-    } else {
-        Bv[0] = bf16lo(*reinterpret_cast<const unsigned short*>(g));
     }
 }
 
@@ -177,9 +181,9 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(PENDING) : "memory");
 }
 
-// Issue the copies of a B or C row (N io values at src) into the state
-// groups of a step's staging row (the layout of stage_bc_row), or zero the
-// groups of a step past the chunk end.  Needs S * esz >= 4 bytes.
+// Issue the copies of an f32 B or C row (N values at src) into the state
+// groups of a step's staging row (the layout of stage_bc_row_f32), or zero
+// the groups of a step past the chunk end.
 template <typename T, int N, int S>
 __device__ __forceinline__ void cp_async_bc_row(unsigned char* row, int half, const T* src, bool valid) {
     constexpr int GB = S * (int)sizeof(T);
