@@ -11,7 +11,7 @@
  *
  *   x_t     = delta[b,t,d] + delta_bias[d]        (bias term only if given)
  *   Delta_t = softplus(x_t)  if softplus, else x_t
- *   h_{-1}  = 0
+ *   h_{-1}  = h0[b,d,:]  if an initial state is given, else 0
  *   a_{t,n} = exp(Delta_t * A[d,n])
  *   h_{t,n} = a_{t,n} * h_{t-1,n} + Delta_t * B[b,t,n] * u[b,t,d]
  *   y0_t    = sum_n h_{t,n} * C[b,t,n]  +  D[d] * u[b,t,d]   (D term if given)
@@ -19,13 +19,14 @@
  *   last_state[b,d,n] = h_{L-1,n}
  *
  * The backward is the chain rule of that definition for the loss
- * sum_t dy_t * y_t, with the structure of mamba-rs `gpu/backward.rs`
+ * sum_t dy_t * y_t + sum_n dlast_n * last_state_n (dlast optional, else 0),
+ * with the structure of mamba-rs `gpu/backward.rs`
  * (B2 gating backward, B3 SSM BPTT with per-row local gradients followed by
  * reductions, B4 softplus backward taking the raw pre-softplus input):
  *
  *   g_t        = dy_t * silu(z_t)                      (dy_t if no z)
  *   dz_t       = dy_t * y0_t * sig(z_t) * (1 + z_t * (1 - sig(z_t)))
- *   lam_{t,n}  = g_t * C[b,t,n] + a_{t+1,n} * lam_{t+1,n},   lam_{L,n} = 0
+ *   lam_{t,n}  = g_t * C[b,t,n] + a_{t+1,n} * lam_{t+1,n},   a_{L,n} lam_{L,n} = dlast_n
  *   du_t       = g_t * D[d] + sum_n lam_{t,n} * Delta_t * B[b,t,n]
  *   dDelta_t   = sum_n lam_{t,n} * (A[d,n] * a_{t,n} * h_{t-1,n} + B[b,t,n] * u_t)
  *   ddelta_t   = dDelta_t * sig(x_t)  if softplus, else dDelta_t
@@ -34,11 +35,12 @@
  *   dbias[d]  += ddelta_t                                    (summed over b, t)
  *   dB[b,t,n] += lam_{t,n} * Delta_t * u_t                   (summed over d)
  *   dC[b,t,n] += g_t * h_{t,n}                               (summed over d)
+ *   dh0[b,d,n] = a_{0,n} * lam_{0,n}   (dlast_n when L = 0)
  *
  * Readings where the pages say nothing: softplus(x) = log(1 + e^x) (stable
- * form), silu(z) = z * sig(z), the initial state is zero, the bias is added
- * even when softplus is off, D is added before the gate, and last_state
- * receives no incoming gradient.
+ * form), silu(z) = z * sig(z), the initial state is zero unless one is
+ * given, the bias is added even when softplus is off, D is added before the
+ * gate, and last_state receives no incoming gradient unless dlast is given.
  *
  * Inputs are f64 arrays (values of the I/O precision convert exactly);
  * every operation is carried out in f64.  Rows are independent and are
@@ -56,6 +58,7 @@ typedef struct {
     const double *u, *delta, *A, *B, *C, *D, *z, *bias, *dy;
     int softplus;
     int64_t Bsz, L, Dch, N;
+    const double *h0, *dlast; /* [Bsz][Dch][N], nullable */
 } problem;
 
 static double softplus_f64(double x) { return x > 0.0 ? x + log1p(exp(-x)) : log1p(exp(x)); }
@@ -73,6 +76,10 @@ static double silu_f64(double z) { return z * sigmoid_f64(z); }
 static int64_t at_bld(const problem *p, int64_t b, int64_t t, int64_t d) { return (b * p->L + t) * p->Dch + d; }
 static int64_t at_bln(const problem *p, int64_t b, int64_t t, int64_t n) { return (b * p->L + t) * p->N + n; }
 static int64_t at_dn(const problem *p, int64_t d, int64_t n) { return d * p->N + n; }
+static int64_t at_bdn(const problem *p, int64_t b, int64_t d, int64_t n) { return (b * p->Dch + d) * p->N + n; }
+
+/* h_{-1,n} of row (b, d) */
+static double h_init(const problem *p, int64_t b, int64_t d, int64_t n) { return p->h0 ? p->h0[at_bdn(p, b, d, n)] : 0.0; }
 
 static double delta_eff(const problem *p, int64_t b, int64_t t, int64_t d, double *x_out)
 {
@@ -85,7 +92,7 @@ static double delta_eff(const problem *p, int64_t b, int64_t t, int64_t d, doubl
 /* Forward over one row.  h: scratch [N].  y, y0: [L] (nullable).  last: [N] (nullable). */
 static void fwd_row(const problem *p, int64_t b, int64_t d, double *h, double *y, double *y0, double *last)
 {
-    for (int64_t n = 0; n < p->N; n++) h[n] = 0.0;
+    for (int64_t n = 0; n < p->N; n++) h[n] = h_init(p, b, d, n);
     for (int64_t t = 0; t < p->L; t++) {
         double dt = delta_eff(p, b, t, d, NULL);
         double ut = p->u[at_bld(p, b, t, d)];
@@ -111,10 +118,10 @@ typedef struct {
     double *lam; /* [N]     running adjoint      */
 } row_scratch;
 
-/* Backward over one row.  Per-row outputs are written; dB/dC contributions are added
- * into dB_acc/dC_acc ([Bsz][L][N], nullable). */
+/* Backward over one row.  Per-row outputs are written (dh0: [N], nullable); dB/dC
+ * contributions are added into dB_acc/dC_acc ([Bsz][L][N], nullable). */
 static void bwd_row(const problem *p, int64_t b, int64_t d, row_scratch *s, double *du, double *ddelta,
-                    double *dz, double *dA, double *dD, double *dbias, double *dB_acc, double *dC_acc)
+                    double *dz, double *dA, double *dD, double *dbias, double *dh0, double *dB_acc, double *dC_acc)
 {
     const int64_t L = p->L, N = p->N;
     /* forward sweep, keeping every a_{t,n} and h_{t,n} */
@@ -122,13 +129,14 @@ static void bwd_row(const problem *p, int64_t b, int64_t d, row_scratch *s, doub
         double dt = delta_eff(p, b, t, d, NULL);
         double ut = p->u[at_bld(p, b, t, d)];
         for (int64_t n = 0; n < N; n++) {
-            double hprev = t > 0 ? s->h[(t - 1) * N + n] : 0.0;
+            double hprev = t > 0 ? s->h[(t - 1) * N + n] : h_init(p, b, d, n);
             double a = exp(dt * p->A[at_dn(p, d, n)]);
             s->a[t * N + n] = a;
             s->h[t * N + n] = a * hprev + dt * p->B[at_bln(p, b, t, n)] * ut;
         }
     }
-    for (int64_t n = 0; n < N; n++) { s->lam[n] = 0.0; dA[n] = 0.0; }
+    /* lam holds lam_{t+1}; a_{L} lam_{L} stands for the incoming gradient of h_{L-1} */
+    for (int64_t n = 0; n < N; n++) { s->lam[n] = p->dlast ? p->dlast[at_bdn(p, b, d, n)] : 0.0; dA[n] = 0.0; }
     double dD_sum = 0.0, dbias_sum = 0.0;
     /* reverse sweep */
     for (int64_t t = L - 1; t >= 0; t--) {
@@ -151,10 +159,10 @@ static void bwd_row(const problem *p, int64_t b, int64_t d, row_scratch *s, doub
         for (int64_t n = 0; n < N; n++) {
             double Bn = p->B[at_bln(p, b, t, n)];
             double Cn = p->C[at_bln(p, b, t, n)];
-            double a_next = t + 1 < L ? s->a[(t + 1) * N + n] : 0.0;
+            double a_next = t + 1 < L ? s->a[(t + 1) * N + n] : 1.0;
             double lam = g * Cn + a_next * s->lam[n];
             s->lam[n] = lam;
-            double hprev = t > 0 ? s->h[(t - 1) * N + n] : 0.0;
+            double hprev = t > 0 ? s->h[(t - 1) * N + n] : h_init(p, b, d, n);
             double a = s->a[t * N + n];
             du_t += lam * dt * Bn;
             dDelta += lam * (p->A[at_dn(p, d, n)] * a * hprev + Bn * ut);
@@ -170,6 +178,9 @@ static void bwd_row(const problem *p, int64_t b, int64_t d, row_scratch *s, doub
     }
     *dD = dD_sum;
     *dbias = dbias_sum;
+    /* h_0 = a_0 h_{-1} + ..., so the gradient of h_{-1} is a_0 lam_0 (lam_0 is in s->lam) */
+    if (dh0)
+        for (int64_t n = 0; n < N; n++) dh0[n] = L > 0 ? s->a[n] * s->lam[n] : s->lam[n];
 }
 
 /* ---------------------------------------------------------------- threading */
@@ -182,7 +193,7 @@ typedef struct {
     /* fwd */
     double *y_rows, *y0_rows, *last_rows;
     /* bwd */
-    double *du_rows, *ddelta_rows, *dz_rows, *dA_rows, *dD_rows, *dbias_rows;
+    double *du_rows, *ddelta_rows, *dz_rows, *dA_rows, *dD_rows, *dbias_rows, *dh0_rows;
     double *dB_part, *dC_part; /* private [Bsz][L][N] accumulators, or NULL */
     int failed;
 } job;
@@ -217,7 +228,8 @@ static void *run_job(void *arg)
         for (int64_t i = j->lo; i < j->hi; i++) {
             int64_t r = row_id(j, i), b = r / p->Dch, d = r % p->Dch;
             bwd_row(p, b, d, &s, j->du_rows + i * L, j->ddelta_rows + i * L, j->dz_rows ? j->dz_rows + i * L : NULL,
-                    j->dA_rows + i * N, j->dD_rows + i, j->dbias_rows + i, j->dB_part, j->dC_part);
+                    j->dA_rows + i * N, j->dD_rows + i, j->dbias_rows + i, j->dh0_rows ? j->dh0_rows + i * N : NULL,
+                    j->dB_part, j->dC_part);
         }
         free(s.a); free(s.h); free(s.lam);
     }
@@ -270,16 +282,17 @@ static int run_threads(job *proto, int64_t n_rows, int nthreads, double *dB, dou
 
 /*
  * Forward.  rows: list of row ids r = b*Dch + d (NULL: every row in order).
+ * h0 (nullable) [Bsz][Dch][N]: the state before t = 0.
  * y_rows [n_rows][L], y0_rows (pre-gate, nullable) [n_rows][L], last_rows (nullable) [n_rows][N].
  * Returns 0 on success, 1 on bad arguments, 2 on allocation failure, 3 on thread failure.
  */
 int ss_oracle_fwd(const double *u, const double *delta, const double *A, const double *B, const double *C,
                   const double *D, const double *z, const double *delta_bias, int softplus, int64_t Bsz,
                   int64_t L, int64_t Dch, int64_t N, const int64_t *rows, int64_t n_rows, double *y_rows,
-                  double *y0_rows, double *last_rows, int nthreads)
+                  double *y0_rows, double *last_rows, int nthreads, const double *h0)
 {
     if (Bsz < 0 || L < 0 || Dch < 0 || N < 0) return 1;
-    problem p = {u, delta, A, B, C, D, z, delta_bias, NULL, softplus, Bsz, L, Dch, N};
+    problem p = {u, delta, A, B, C, D, z, delta_bias, NULL, softplus, Bsz, L, Dch, N, h0, NULL};
     if (!rows) n_rows = Bsz * Dch;
     if (n_rows == 0) return 0;
     if (!u || !delta || !A || !B || !C) return 1;
@@ -300,15 +313,18 @@ int ss_oracle_fwd(const double *u, const double *delta, const double *A, const d
  * Backward.  Per-row outputs: du/ddelta/dz [n_rows][L] (dz nullable), dA_rows [n_rows][N],
  * dD_rows [n_rows], dbias_rows [n_rows] -- the row's own contributions to dA[d], dD[d], dbias[d].
  * dB, dC (nullable) [Bsz][L][N]: the given rows' contributions are ADDED into them.
+ * h0, dlast (nullable) [Bsz][Dch][N]: initial state and incoming gradient of last_state;
+ * dh0_rows (nullable) [n_rows][N]: gradient of the initial state.
  */
 int ss_oracle_bwd(const double *u, const double *delta, const double *A, const double *B, const double *C,
                   const double *D, const double *z, const double *delta_bias, int softplus, const double *dy,
                   int64_t Bsz, int64_t L, int64_t Dch, int64_t N, const int64_t *rows, int64_t n_rows,
                   double *du_rows, double *ddelta_rows, double *dz_rows, double *dA_rows, double *dD_rows,
-                  double *dbias_rows, double *dB, double *dC, int nthreads)
+                  double *dbias_rows, double *dB, double *dC, int nthreads, const double *h0, const double *dlast,
+                  double *dh0_rows)
 {
     if (Bsz < 0 || L < 0 || Dch < 0 || N < 0) return 1;
-    problem p = {u, delta, A, B, C, D, z, delta_bias, dy, softplus, Bsz, L, Dch, N};
+    problem p = {u, delta, A, B, C, D, z, delta_bias, dy, softplus, Bsz, L, Dch, N, h0, dlast};
     if (!rows) n_rows = Bsz * Dch;
     if (n_rows == 0) return 0;
     if (!u || !delta || !A || !B || !C || !dy || !du_rows || !ddelta_rows || !dA_rows || !dD_rows || !dbias_rows)
@@ -326,5 +342,6 @@ int ss_oracle_bwd(const double *u, const double *delta, const double *A, const d
     proto.dA_rows = dA_rows;
     proto.dD_rows = dD_rows;
     proto.dbias_rows = dbias_rows;
+    proto.dh0_rows = dh0_rows;
     return run_threads(&proto, n_rows, nthreads, dB, dC);
 }

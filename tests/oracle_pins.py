@@ -310,6 +310,119 @@ def check_identities(orc):
     assert normwise(g.dD, (gate * x["u"]).sum(axis=(0, 1))) < 1e-13, "dD identity"
 
 
+# ----------------------------------------------------------------------------- initial state, last_state
+# gradient, A_log (the extensions: an initial state h0 replaces the zero start, a gradient dlast reaches
+# last_state, and A may be given as A_log with A = -exp(A_log))
+
+
+def _fwd_s(orc, x, softplus=True, h0=None, A_log=None):
+    return orc.fwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], softplus,
+                   nthreads=2, h0=h0, A_log=A_log)
+
+
+def _bwd_s(orc, x, softplus=True, h0=None, dlast=None, A_log=None):
+    return orc.bwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], softplus,
+                   dy=x["dy"], nthreads=2, h0=h0, dlast_state=dlast, A_log=A_log)
+
+
+def check_h0_one_step(orc):
+    """One step from a given state: h = exp(Delta A) h0 + Delta B u, y = (C . h + D u) silu(z);
+    with L = 0 the state passes through (last_state = h0, dh0 = dlast)."""
+    x = _inputs(110, 2, 1, 3, 4)
+    rng = _rng(111)
+    h0 = rng.normal(size=(2, 3, 4))
+    r = _fwd_s(orc, x, h0=h0)
+    dl = softplus_np(x["delta"][:, 0, :] + x["delta_bias"][None, :])          # [B, D]
+    a = np.exp(dl[..., None] * x["A"][None])                                  # [B, D, N]
+    h = a * h0 + dl[..., None] * x["B"][:, 0, None, :] * x["u"][:, 0, :, None]
+    y0 = np.einsum("bdn,bn->bd", h, x["C"][:, 0]) + x["D"][None, :] * x["u"][:, 0]
+    assert normwise(r.y[:, 0], y0 * silu_np(x["z"][:, 0])) < 1e-14, "one step from h0: y"
+    assert normwise(r.last_state, h) < 1e-14, "one step from h0: last_state"
+    # its backward: dh0 = a * (g C + dlast) with g = dy silu(z)
+    dlast = rng.normal(size=(2, 3, 4))
+    g = _bwd_s(orc, x, h0=h0, dlast=dlast)
+    gate = x["dy"][:, 0] * silu_np(x["z"][:, 0])                              # [B, D]
+    lam = gate[..., None] * x["C"][:, 0, None, :] + dlast
+    assert normwise(g.dh0, a * lam) < 1e-14, "one step: dh0"
+    e = {k: (None if v is None else v[:, :0].copy() if k in ("u", "delta", "B", "C", "z", "dy") else v)
+         for k, v in x.items()}
+    r0 = _fwd_s(orc, e, h0=h0)
+    assert np.array_equal(r0.last_state, h0), "L = 0: last_state is h0"
+    assert np.array_equal(_bwd_s(orc, e, h0=h0, dlast=dlast).dh0, dlast), "L = 0: dh0 is dlast"
+
+
+def check_h0_split(orc):
+    """Cutting the sequence at L1 and starting the later part from the earlier part's
+    last_state gives the same forward; running the later part's backward first and
+    feeding its dh0 to the earlier part as dlast gives the same gradients."""
+    Bsz, L, Dch, N, L1 = 2, 23, 3, 4, 9
+    x = _inputs(120, Bsz, L, Dch, N)
+    rng = _rng(121)
+    h0 = rng.normal(size=(Bsz, Dch, N))
+    dlast = rng.normal(size=(Bsz, Dch, N))
+    seq = ("u", "delta", "B", "C", "z", "dy")
+
+    def part(lo, hi):
+        return {k: (v[:, lo:hi].copy() if k in seq and v is not None else v) for k, v in x.items()}
+
+    x1, x2 = part(0, L1), part(L1, L)
+    full = _fwd_s(orc, x, h0=h0)
+    f1 = _fwd_s(orc, x1, h0=h0)
+    f2 = _fwd_s(orc, x2, h0=f1.last_state)
+    assert normwise(np.concatenate([f1.y, f2.y], axis=1), full.y) < 1e-13, "split forward: y"
+    assert normwise(f2.last_state, full.last_state) < 1e-13, "split forward: last_state"
+    gf = _bwd_s(orc, x, h0=h0, dlast=dlast)
+    g2 = _bwd_s(orc, x2, h0=f1.last_state, dlast=dlast)
+    g1 = _bwd_s(orc, x1, h0=h0, dlast=g2.dh0)
+    for k in ("du", "ddelta", "dz", "dB", "dC"):
+        got = np.concatenate([getattr(g1, k), getattr(g2, k)], axis=1)
+        assert normwise(got, getattr(gf, k)) < 1e-12, ("split backward", k)
+    for k in ("dA", "dD", "ddelta_bias"):
+        assert normwise(getattr(g1, k) + getattr(g2, k), getattr(gf, k)) < 1e-12, ("split backward", k)
+    assert normwise(g1.dh0, gf.dh0) < 1e-12, "split backward: dh0"
+
+
+def check_finite_differences_state(orc):
+    """f64 central differences of sum(dy * y) + sum(dlast * last_state) with an initial state and
+    A given as A_log: every gradient, dh0 and dA_log included."""
+    cases = [(1, 5, 2, 3, VARIANTS[0]), (2, 1, 1, 2, VARIANTS[1]), (1, 4, 2, 2, VARIANTS[2])]
+    for ci, (Bsz, L, Dch, N, v) in enumerate(cases):
+        x = _inputs(130 + ci, Bsz, L, Dch, N, has_D=v["has_D"], has_z=v["has_z"], has_bias=v["has_bias"])
+        sp = v["softplus"]
+        if not sp:
+            _decay_without_softplus(x)
+        rng = _rng(140 + ci)
+        x["A_log"] = rng.uniform(-2.0, 0.4, size=x["A"].shape)
+        x["h0"] = rng.normal(size=(Bsz, Dch, N))
+        dlast = rng.normal(size=(Bsz, Dch, N))
+
+        def loss():
+            r = _fwd_s(orc, x, sp, h0=x["h0"], A_log=x["A_log"])
+            return float(np.sum(x["dy"] * r.y) + np.sum(dlast * r.last_state))
+
+        g = _bwd_s(orc, x, sp, h0=x["h0"], dlast=dlast, A_log=x["A_log"])
+        names = dict(_GRAD_NAMES)
+        names.pop("A")
+        names.update({"A_log": "dA", "h0": "dh0"})
+        for name, gname in names.items():
+            if x[name] is None:
+                continue
+            got = np.asarray(getattr(g, gname))
+            fd = np.zeros_like(x[name])
+            flat = x[name].reshape(-1)
+            for i in range(flat.size):
+                old = flat[i]
+                hh = 1e-6 * max(1.0, abs(old))
+                flat[i] = old + hh
+                fp = loss()
+                flat[i] = old - hh
+                fm = loss()
+                flat[i] = old
+                fd.reshape(-1)[i] = (fp - fm) / (2 * hh)
+            err = normwise(got, fd)
+            assert err < 1e-6, (f"finite differences {gname} (h0, dlast, A_log)", ci, v, err)
+
+
 ALL_CHECKS = [
     check_L1_closed_form,
     check_N1_geometric,
@@ -321,4 +434,7 @@ ALL_CHECKS = [
     check_finite_differences,
     check_adjoint_dot,
     check_identities,
+    check_h0_one_step,
+    check_h0_split,
+    check_finite_differences_state,
 ]

@@ -33,10 +33,10 @@ MUTANTS = [
      "for (int64_t n = 0; n < p->N; n++) last[n] = h[n] - p->B[at_bln(p, b, p->L - 1, n)] * 0.5;", 0),
     ("bwd: recompute uses C as input", "s->h[t * N + n] = a * hprev + dt * p->B[at_bln(p, b, t, n)] * ut;",
      "s->h[t * N + n] = a * hprev + dt * p->C[at_bln(p, b, t, n)] * ut;", 0),
-    ("bwd: adjoint uses a_t not a_{t+1}", "double a_next = t + 1 < L ? s->a[(t + 1) * N + n] : 0.0;",
-     "double a_next = t + 1 < L ? s->a[t * N + n] : 0.0;", 0),
+    ("bwd: adjoint uses a_t not a_{t+1}", "double a_next = t + 1 < L ? s->a[(t + 1) * N + n] : 1.0;",
+     "double a_next = t + 1 < L ? s->a[t * N + n] : 1.0;", 0),
     ("bwd: adjoint injects B", "double lam = g * Cn + a_next * s->lam[n];", "double lam = g * Bn + a_next * s->lam[n];", 0),
-    ("bwd: h_{t-1} read as h_t", "double hprev = t > 0 ? s->h[(t - 1) * N + n] : 0.0;\n            double a = s->a",
+    ("bwd: h_{t-1} read as h_t", "double hprev = t > 0 ? s->h[(t - 1) * N + n] : h_init(p, b, d, n);\n            double a = s->a",
      "double hprev = s->h[t * N + n];\n            double a = s->a", 0),
     ("bwd: du missing Delta", "du_t += lam * dt * Bn;", "du_t += lam * Bn;", 0),
     ("bwd: du missing D*g", "double du_t = p->D ? g * p->D[d] : 0.0;", "double du_t = 0.0;", 0),
@@ -53,6 +53,14 @@ MUTANTS = [
     ("bwd: softplus grad at Delta", "dDelta * sigmoid_f64(x)", "dDelta * sigmoid_f64(dt)", 0),
     ("bwd: dD ungated", "dD_sum += g * ut;", "dD_sum += dyt * ut;", 0),
     ("bwd: dbias before softplus grad", "dbias_sum += dx;", "dbias_sum += dDelta;", 0),
+    ("fwd: h0 ignored", "h[n] = h_init(p, b, d, n);", "h[n] = 0.0;", 0),
+    ("bwd: recompute starts from zero", "double hprev = t > 0 ? s->h[(t - 1) * N + n] : h_init(p, b, d, n);\n            double a = exp",
+     "double hprev = t > 0 ? s->h[(t - 1) * N + n] : 0.0;\n            double a = exp", 0),
+    ("bwd: dA / dDelta at t = 0 without h0", "double hprev = t > 0 ? s->h[(t - 1) * N + n] : h_init(p, b, d, n);\n            double a = s->a",
+     "double hprev = t > 0 ? s->h[(t - 1) * N + n] : 0.0;\n            double a = s->a", 0),
+    ("bwd: dlast ignored", "s->lam[n] = p->dlast ? p->dlast[at_bdn(p, b, d, n)] : 0.0;", "s->lam[n] = 0.0;", 0),
+    ("bwd: dh0 without the first decay", "dh0[n] = L > 0 ? s->a[n] * s->lam[n] : s->lam[n];", "dh0[n] = s->lam[n];", 0),
+    ("bwd: dh0 with the last decay", "dh0[n] = L > 0 ? s->a[n] * s->lam[n]", "dh0[n] = L > 0 ? s->a[(L - 1) * N + n] * s->lam[n]", 0),
 ]
 
 
