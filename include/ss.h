@@ -177,7 +177,8 @@ int ss_plan_info(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype, int6
 
 /*
  * Measurement aid (not thread-safe; for benchmarks).  After a call with
- * count > 0, every call of ss_fwd, ss_fwd_save, ss_bwd or ss_bwd_saved that
+ * count > 0, every call of ss_fwd, ss_fwd_save, ss_fwd_ex, ss_bwd,
+ * ss_bwd_saved or ss_bwd_ex that
  * returns SS_OK records events[0] on its stream before its first kernel,
  * events[i] after its i-th kernel (in the order ss_plan_info counts them),
  * stopping when the list is used up; the list stays set for later calls.
@@ -188,11 +189,111 @@ int ss_plan_info(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype, int6
  */
 int ss_profile_events(void *const *events, int count);
 
+/*
+ * Extended forward: everything ss_fwd and ss_fwd_save do, plus an initial
+ * state and the A_log parameterisation, through one descriptor (all fields
+ * must be set; unused pointers NULL).
+ *
+ *   h0          f32 [Bsz, Dch, N], optional: the state before t = 0, in place
+ *               of zero (the recurrence continues from it: h_0 = exp(Delta_0 A)
+ *               h0 + Delta_0 B_0 u_0).  Feeding one call's last_state as the
+ *               next call's h0 continues a sequence across calls (streaming
+ *               prefill, sequence splits); the pages define only the zero
+ *               start.
+ *   a_is_log    nonzero: A holds A_log and the scan uses A = -exp(A_log)
+ *               (the parameterisation mamba-rs `gpu/backward.rs` trains).
+ *   saved       NULL: behaves as ss_fwd; else as ss_fwd_save (saved_bytes >=
+ *               ss_saved_bytes(...)).
+ * The other fields are the arguments of ss_fwd with the same meaning, layout
+ * and checks; h0 must be 16-byte aligned like every pointer.  With L = 0 the
+ * state stays h0: last_state receives a copy of it (zeros without h0).
+ */
+typedef struct {
+    const void *u, *delta;    /* io [Bsz, L, Dch] */
+    const float *A;           /* f32 [Dch, N]: A, or A_log when a_is_log */
+    const void *B, *C;        /* io [Bsz, L, N] */
+    const float *D;           /* f32 [Dch] or NULL */
+    const void *z;            /* io [Bsz, L, Dch] or NULL */
+    const float *delta_bias;  /* f32 [Dch] or NULL */
+    const float *h0;          /* f32 [Bsz, Dch, N] or NULL */
+    void *y;                  /* io [Bsz, L, Dch], output */
+    float *last_state;        /* f32 [Bsz, Dch, N], output, or NULL */
+    void *saved;              /* restart states for ss_bwd_ex, or NULL */
+    size_t saved_bytes;
+    void *workspace;          /* >= ss_fwd_workspace_bytes(...) bytes */
+    size_t workspace_bytes;
+    int64_t Bsz, L, Dch, N;
+    int32_t dtype, softplus, a_is_log, reserved; /* reserved: set to 0 */
+} ss_fwd_desc;
+int ss_fwd_ex(const ss_fwd_desc *desc, void *stream);
+
+/*
+ * Extended backward: the gradient of sum(dy * y) + sum(dlast_state *
+ * last_state) for the forward of ss_fwd_ex.
+ *   h0, a_is_log  as in the forward.
+ *   dlast_state   f32 [Bsz, Dch, N], optional: the gradient reaching
+ *                 last_state from later computation (zero when NULL).
+ *   dh0           f32 [Bsz, Dch, N], output: the gradient of h0, given
+ *                 exactly when h0 is (else SS_ERR_INVALID_PROBLEM).  Chaining
+ *                 a later segment's dh0 into the earlier segment's
+ *                 dlast_state reproduces the gradients of the whole sequence.
+ *   dA            with a_is_log, the gradient of A_log (dA * A).
+ *   saved         NULL: recompute the states (as ss_bwd; workspace from
+ *                 ss_bwd_workspace_bytes); else the buffer ss_fwd_ex filled
+ *                 for the same inputs, h0 included (as ss_bwd_saved;
+ *                 workspace from ss_bwd_saved_workspace_bytes).
+ * The other fields are the arguments of ss_bwd with the same meaning, layout
+ * and checks.  With L = 0, dh0 receives a copy of dlast_state (zeros without
+ * it).  The pages this library follows have no counterpart for h0 or
+ * dlast_state.
+ */
+typedef struct {
+    const void *u, *delta;
+    const float *A;
+    const void *B, *C;
+    const float *D;
+    const void *z;
+    const float *delta_bias;
+    const float *h0;
+    const void *dy;              /* io [Bsz, L, Dch] */
+    const float *dlast_state;    /* f32 [Bsz, Dch, N] or NULL */
+    const void *saved;
+    size_t saved_bytes;
+    float *du, *ddelta, *dA, *dB, *dC, *dD, *dz, *ddelta_bias;
+    float *dh0;                  /* f32 [Bsz, Dch, N], iff h0 */
+    void *workspace;
+    size_t workspace_bytes;
+    int64_t Bsz, L, Dch, N;
+    int32_t dtype, softplus, a_is_log, reserved; /* reserved: set to 0 */
+} ss_bwd_desc;
+int ss_bwd_ex(const ss_bwd_desc *desc, void *stream);
+
+/*
+ * One recurrence step for autoregressive decoding, in place on a state kept
+ * between calls (the inference use of the same recurrence; mamba-rs keeps one
+ * such state per layer).  For every (b, d), with the forward's definition at
+ * a single time step:
+ *   state[b,d,n] <- exp(delta_eff * A[d,n]) * state[b,d,n] + delta_eff * B[b,n] * u[b,d]
+ *   y[b,d]        = (sum_n state[b,d,n] * C[b,n] + D[d] * u[b,d]) * silu(z[b,d])   (new state)
+ * Equivalent to ss_fwd_ex with L = 1, h0 = state and last_state = state.
+ *   u, delta, z   io [Bsz, Dch] (z optional)       B, C  io [Bsz, N]
+ *   A             f32 [Dch, N] (A_log when a_is_log)   D, delta_bias  f32 [Dch] optional
+ *   state         f32 [Bsz, Dch, N], read and overwritten
+ *   y             io [Bsz, Dch], output
+ * Checks as ss_fwd (sizes, N in {1,2,4,8,16,32}, required pointers, 16-byte
+ * alignment).  One kernel, no workspace.  The pages this library follows have
+ * no single-step entry point.
+ */
+int ss_decode_step(const void *u, const void *delta, const float *A, const void *B, const void *C, const float *D,
+                   const void *z, const float *delta_bias, int softplus, int a_is_log, float *state, void *y,
+                   int64_t Bsz, int64_t Dch, int64_t N, int dtype, void *stream);
+
 /* Static description of a status code. */
 const char *ss_status_string(int status);
 
 /* ABI version (2: ss_fwd_save / ss_bwd_saved added, ss_plan_info gained
- * bwd_saved_kernels); bumped on any incompatible change. */
+ * bwd_saved_kernels; 3: ss_fwd_ex / ss_bwd_ex / ss_decode_step added); bumped on any
+ * incompatible change. */
 int ss_abi_version(void);
 
 #ifdef __cplusplus

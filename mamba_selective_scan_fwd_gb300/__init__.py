@@ -7,9 +7,10 @@ missing -- there is no other implementation to fall back on.
 """
 
 from .binding import (SS_BF16, SS_F16, SS_F32, SSError, bwd_saved_workspace_bytes, bwd_workspace_bytes,
-                      fwd_workspace_bytes, lib, plan_info, saved_bytes, ss_bwd, ss_bwd_saved, ss_fwd, ss_fwd_noalloc,
-                      ss_fwd_save, status_string)
+                      fwd_workspace_bytes, lib, plan_info, saved_bytes, ss_bwd, ss_bwd_ex, ss_bwd_saved,
+                      ss_decode_step, ss_fwd, ss_fwd_ex, ss_fwd_noalloc, ss_fwd_save, status_string)
 
-__all__ = ["ss_fwd", "ss_fwd_save", "ss_fwd_noalloc", "ss_bwd", "ss_bwd_saved", "fwd_workspace_bytes",
-           "bwd_workspace_bytes", "saved_bytes", "bwd_saved_workspace_bytes", "status_string", "plan_info", "lib",
-           "SSError", "SS_F32", "SS_F16", "SS_BF16"]
+__all__ = ["ss_fwd", "ss_fwd_save", "ss_fwd_ex", "ss_fwd_noalloc", "ss_bwd", "ss_bwd_saved", "ss_bwd_ex",
+           "ss_decode_step",
+           "fwd_workspace_bytes", "bwd_workspace_bytes", "saved_bytes", "bwd_saved_workspace_bytes", "status_string",
+           "plan_info", "lib", "SSError", "SS_F32", "SS_F16", "SS_BF16"]

@@ -22,8 +22,9 @@ STATUS_NAMES = {0: "SS_OK", 1: "SS_ERR_INVALID_PROBLEM", 2: "SS_ERR_UNSUPPORTED"
 # Every function include/ss.h declares.
 EXPORTS = ["ss_fwd", "ss_bwd", "ss_fwd_workspace_bytes", "ss_bwd_workspace_bytes", "ss_plan_info",
            "ss_status_string", "ss_abi_version", "ss_fwd_noalloc", "ss_saved_bytes", "ss_fwd_save",
-           "ss_bwd_saved_workspace_bytes", "ss_bwd_saved", "ss_profile_events"]
-ABI_VERSION = 2
+           "ss_bwd_saved_workspace_bytes", "ss_bwd_saved", "ss_profile_events", "ss_fwd_ex", "ss_bwd_ex",
+           "ss_decode_step"]
+ABI_VERSION = 3
 
 # Size of the library-owned scratch behind ss_fwd_noalloc (SS_FWD_NOALLOC_MAX_SCRATCH_BYTES).
 FWD_NOALLOC_MAX_SCRATCH_BYTES = 2 << 20
@@ -40,6 +41,25 @@ _lib = None
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
 _SZ = ctypes.c_size_t
+_I32 = ctypes.c_int32
+
+
+class FwdDesc(ctypes.Structure):
+    """ss_fwd_desc of include/ss.h (same field order and types)."""
+    _fields_ = [(n, _P) for n in ("u", "delta", "A", "B", "C", "D", "z", "delta_bias", "h0", "y", "last_state",
+                                  "saved")] + [
+        ("saved_bytes", _SZ), ("workspace", _P), ("workspace_bytes", _SZ),
+        ("Bsz", _I64), ("L", _I64), ("Dch", _I64), ("N", _I64),
+        ("dtype", _I32), ("softplus", _I32), ("a_is_log", _I32), ("reserved", _I32)]
+
+
+class BwdDesc(ctypes.Structure):
+    """ss_bwd_desc of include/ss.h (same field order and types)."""
+    _fields_ = [(n, _P) for n in ("u", "delta", "A", "B", "C", "D", "z", "delta_bias", "h0", "dy", "dlast_state",
+                                  "saved")] + [("saved_bytes", _SZ)] + [
+        (n, _P) for n in ("du", "ddelta", "dA", "dB", "dC", "dD", "dz", "ddelta_bias", "dh0", "workspace")] + [
+        ("workspace_bytes", _SZ), ("Bsz", _I64), ("L", _I64), ("Dch", _I64), ("N", _I64),
+        ("dtype", _I32), ("softplus", _I32), ("a_is_log", _I32), ("reserved", _I32)]
 
 
 def lib() -> ctypes.CDLL:
@@ -73,6 +93,12 @@ def lib() -> ctypes.CDLL:
     L.ss_abi_version.argtypes = []
     L.ss_fwd_noalloc.restype = ctypes.c_int
     L.ss_fwd_noalloc.argtypes = [_P] * 8 + [ctypes.c_int, _P, _P] + [_I64] * 4 + [ctypes.c_int, _P]
+    L.ss_fwd_ex.restype = ctypes.c_int
+    L.ss_fwd_ex.argtypes = [ctypes.POINTER(FwdDesc), _P]
+    L.ss_bwd_ex.restype = ctypes.c_int
+    L.ss_bwd_ex.argtypes = [ctypes.POINTER(BwdDesc), _P]
+    L.ss_decode_step.restype = ctypes.c_int
+    L.ss_decode_step.argtypes = [_P] * 8 + [ctypes.c_int, ctypes.c_int, _P, _P] + [_I64] * 3 + [ctypes.c_int, _P]
     _lib = L
     return L
 
@@ -307,3 +333,101 @@ def ss_bwd_saved(u, delta, A, B, C, D, z, delta_bias, softplus, dy, saved, out=N
                             dt, _p(workspace), wsb, stream_handle(stream))
     _check("ss_bwd_saved", rc)
     return out
+
+
+def _state_arg(t, name, shape, dev):
+    import torch
+
+    if t is not None:
+        _require(t, name, shape, torch.float32, dev)
+    return t
+
+
+def ss_fwd_ex(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, h0=None, a_is_log=False,
+              y=None, last_state=None, return_last_state=True, saved=None, save=False, workspace=None, stream=None):
+    """Extended forward (ss_fwd_ex): an initial state ``h0`` [Bsz, Dch, N] f32
+    and/or ``A`` given as A_log (``a_is_log``; the scan uses -exp(A_log)).
+    With ``save`` (or a ``saved`` buffer) the restart states for ss_bwd_ex are
+    kept.  Returns (y, last_state or None, saved or None)."""
+    import torch
+
+    (Bsz, L, Dch, N), y, last_state = _fwd_prepare(u, delta, A, B, C, D, z, delta_bias, y, last_state,
+                                                   return_last_state)
+    _state_arg(h0, "h0", (Bsz, Dch, N), u.device)
+    dt = dtype_id(u)
+    if saved is None and save:
+        saved = torch.empty(max(saved_bytes(Bsz, L, Dch, N, dt), 16), dtype=torch.uint8, device=u.device)
+    workspace, wsb = _workspace(fwd_workspace_bytes(Bsz, L, Dch, N, dt), u.device, workspace)
+    d = FwdDesc()
+    for k, t in (("u", u), ("delta", delta), ("A", A), ("B", B), ("C", C), ("D", D), ("z", z),
+                 ("delta_bias", delta_bias), ("h0", h0), ("y", y), ("last_state", last_state), ("saved", saved),
+                 ("workspace", workspace)):
+        setattr(d, k, None if t is None else t.data_ptr())
+    d.saved_bytes, d.workspace_bytes = _nbytes(saved), wsb
+    d.Bsz, d.L, d.Dch, d.N = Bsz, L, Dch, N
+    d.dtype, d.softplus, d.a_is_log, d.reserved = dt, int(bool(softplus)), int(bool(a_is_log)), 0
+    _check("ss_fwd_ex", lib().ss_fwd_ex(ctypes.byref(d), stream_handle(stream)))
+    return y, last_state, saved
+
+
+def ss_bwd_ex(u, delta, A, B, C, D, z, delta_bias, softplus, dy, h0=None, dlast_state=None, a_is_log=False,
+              saved=None, out=None, workspace=None, stream=None):
+    """Extended backward (ss_bwd_ex) of sum(dy * y) + sum(dlast_state * last_state).
+    Returns the ss_bwd dict plus ``dh0`` (present iff h0 is given); with
+    ``a_is_log`` dA is the gradient of A_log.  ``saved``: the buffer ss_fwd_ex
+    filled for the same inputs (None: the states are recomputed)."""
+    import torch
+
+    (Bsz, L, Dch, N), out = _bwd_prepare(u, delta, A, B, C, D, z, delta_bias, dy, out)
+    dev = u.device
+    _state_arg(h0, "h0", (Bsz, Dch, N), dev)
+    _state_arg(dlast_state, "dlast_state", (Bsz, Dch, N), dev)
+    if h0 is None:
+        out["dh0"] = None
+    else:
+        if out.get("dh0") is None:
+            out["dh0"] = torch.empty((Bsz, Dch, N), dtype=torch.float32, device=dev)
+        _require(out["dh0"], "dh0", (Bsz, Dch, N), torch.float32, dev)
+    dt = dtype_id(u)
+    need = (bwd_saved_workspace_bytes if saved is not None else bwd_workspace_bytes)(Bsz, L, Dch, N, dt)
+    workspace, wsb = _workspace(need, dev, workspace)
+    d = BwdDesc()
+    for k, t in (("u", u), ("delta", delta), ("A", A), ("B", B), ("C", C), ("D", D), ("z", z),
+                 ("delta_bias", delta_bias), ("h0", h0), ("dy", dy), ("dlast_state", dlast_state), ("saved", saved),
+                 ("workspace", workspace)):
+        setattr(d, k, None if t is None else t.data_ptr())
+    for k in GRAD_SHAPES + ("dh0",):
+        setattr(d, k, None if out[k] is None else out[k].data_ptr())
+    d.saved_bytes, d.workspace_bytes = _nbytes(saved), wsb
+    d.Bsz, d.L, d.Dch, d.N = Bsz, L, Dch, N
+    d.dtype, d.softplus, d.a_is_log, d.reserved = dt, int(bool(softplus)), int(bool(a_is_log)), 0
+    _check("ss_bwd_ex", lib().ss_bwd_ex(ctypes.byref(d), stream_handle(stream)))
+    return out
+
+
+def ss_decode_step(u, delta, A, B, C, D, z, delta_bias, softplus, state, y=None, a_is_log=False, stream=None):
+    """One decoding step in place on ``state`` [Bsz, Dch, N] f32: u, delta, z
+    [Bsz, Dch] and B, C [Bsz, N] of the new token (io dtype).  Returns y [Bsz, Dch]."""
+    import torch
+
+    Bsz, Dch = u.shape
+    N = A.shape[1]
+    dev, io = u.device, u.dtype
+    for name, t, shape in (("u", u, (Bsz, Dch)), ("delta", delta, (Bsz, Dch)), ("B", B, (Bsz, N)),
+                           ("C", C, (Bsz, N))):
+        _require(t, name, shape, io, dev)
+    _require(A, "A", (Dch, N), torch.float32, dev)
+    _require(state, "state", (Bsz, Dch, N), torch.float32, dev)
+    if z is not None:
+        _require(z, "z", (Bsz, Dch), io, dev)
+    for name, t in (("D", D), ("delta_bias", delta_bias)):
+        if t is not None:
+            _require(t, name, (Dch,), torch.float32, dev)
+    if y is None:
+        y = torch.empty((Bsz, Dch), dtype=io, device=dev)
+    _require(y, "y", (Bsz, Dch), io, dev)
+    rc = lib().ss_decode_step(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias),
+                              int(bool(softplus)), int(bool(a_is_log)), _p(state), _p(y), Bsz, Dch, N, dtype_id(u),
+                              stream_handle(stream))
+    _check("ss_decode_step", rc)
+    return y

@@ -21,7 +21,7 @@ LIB = os.path.join(PKG, "libss.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
-SOURCES = ["api.cu", "fwd2.cu", "bwd2.cu", "fwd_noalloc.cu"]
+SOURCES = ["api.cu", "fwd2.cu", "bwd2.cu", "decode.cu", "fwd_noalloc.cu"]
 
 
 def nvcc() -> str:

@@ -37,23 +37,27 @@ cudaEvent_t g_prof_ev[kMaxProfEvents];
 int g_prof_n = 0;
 int g_prof_next = 0;
 
-// Forward with optional checkpoint output (saved == nullptr: plain forward).
+// Forward with optional restart-state output (save == false: plain forward),
+// initial state h0 (nullable) and the A_log form.
 int fwd_impl(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
-             const void* z, const float* delta_bias, int softplus, void* y, float* last_state, int64_t Bsz, int64_t L,
-             int64_t Dch, int64_t N, int dtype, bool save, void* saved, size_t saved_bytes, void* workspace,
-             size_t workspace_bytes, void* stream) {
+             const void* z, const float* delta_bias, const float* h0, int softplus, int a_is_log, void* y,
+             float* last_state, int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype, bool save, void* saved,
+             size_t saved_bytes, void* workspace, size_t workspace_bytes, void* stream) {
     int rc = check_sizes(Bsz, L, Dch, N, dtype);
     if (rc != SS_OK) return rc;
     const bool empty = Bsz == 0 || L == 0 || Dch == 0;
     if (!empty && (!u || !delta || !A || !B || !C || !y)) return SS_ERR_INVALID_PROBLEM;
-    const void* ptrs[] = {u, delta, A, B, C, D, z, delta_bias, y, last_state, saved, workspace};
+    const void* ptrs[] = {u, delta, A, B, C, D, z, delta_bias, h0, y, last_state, saved, workspace};
     for (const void* q : ptrs)
         if (!aligned16(q)) return SS_ERR_UNSUPPORTED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (empty) {
+        // no step: the state stays the initial one
         if (last_state && Bsz > 0 && Dch > 0 && N > 0) {
-            if (cudaMemsetAsync(last_state, 0, (size_t)Bsz * Dch * N * sizeof(float), st) != cudaSuccess)
-                return SS_ERR_CUDA;
+            const size_t bytes = (size_t)Bsz * Dch * N * sizeof(float);
+            const cudaError_t e = h0 ? cudaMemcpyAsync(last_state, h0, bytes, cudaMemcpyDeviceToDevice, st)
+                                     : cudaMemsetAsync(last_state, 0, bytes, st);
+            if (e != cudaSuccess) return SS_ERR_CUDA;
         }
         return SS_OK;
     }
@@ -68,32 +72,37 @@ int fwd_impl(const void* u, const void* delta, const float* A, const void* B, co
     FwdArgs a;
     a.u = u; a.delta = delta; a.B = B; a.C = C; a.z = z;
     a.A = A; a.D = D; a.delta_bias = delta_bias;
+    a.h0 = h0;
     a.y = y; a.last_state = last_state;
     a.Bsz = Bsz; a.L = L; a.Dch = Dch; a.N = N;
     a.softplus = softplus ? 1 : 0;
+    a.a_is_log = a_is_log ? 1 : 0;
     a.dtype = dtype;
     a.ws_fsum = static_cast<float*>(workspace);
     float* ck = save ? static_cast<float*>(saved) : nullptr;
     return launch_fwd2(a, p, st, kModeY, ck) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
-// Backward; with saved != nullptr the checkpoints come from ss_fwd_save.
+// Backward; with from_saved the restart states come from ss_fwd_save /
+// ss_fwd_ex.  h0 / dlast (nullable): initial state and incoming gradient of
+// last_state; dh0 (given iff h0): gradient of the initial state.
 int bwd_impl(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
-             const void* z, const float* delta_bias, int softplus, const void* dy, float* du, float* ddelta,
-             float* dA, float* dB, float* dC, float* dD, float* dz, float* ddelta_bias, int64_t Bsz, int64_t L,
-             int64_t Dch, int64_t N, int dtype, bool from_saved, const void* saved, size_t saved_bytes,
-             void* workspace, size_t workspace_bytes, void* stream) {
+             const void* z, const float* delta_bias, const float* h0, int softplus, int a_is_log, const void* dy,
+             const float* dlast, float* du, float* ddelta, float* dA, float* dB, float* dC, float* dD, float* dz,
+             float* ddelta_bias, float* dh0, int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype,
+             bool from_saved, const void* saved, size_t saved_bytes, void* workspace, size_t workspace_bytes,
+             void* stream) {
     int rc = check_sizes(Bsz, L, Dch, N, dtype);
     if (rc != SS_OK) return rc;
     if ((D == nullptr) != (dD == nullptr) || (z == nullptr) != (dz == nullptr) ||
-        (delta_bias == nullptr) != (ddelta_bias == nullptr))
+        (delta_bias == nullptr) != (ddelta_bias == nullptr) || (h0 == nullptr) != (dh0 == nullptr))
         return SS_ERR_INVALID_PROBLEM;
     const bool empty = Bsz == 0 || L == 0 || Dch == 0;
     if (!empty && (!u || !delta || !A || !B || !C || !dy || !du || !ddelta || !dA || !dB || !dC))
         return SS_ERR_INVALID_PROBLEM;
     if (empty && Dch > 0 && N > 0 && !dA) return SS_ERR_INVALID_PROBLEM;
-    const void* ptrs[] = {u, delta, A, B, C, D, z, delta_bias, dy, du, ddelta, dA, dB, dC, dD, dz, ddelta_bias,
-                          saved, workspace};
+    const void* ptrs[] = {u, delta, A, B, C, D, z, delta_bias, h0, dy, dlast, du, ddelta, dA, dB, dC, dD, dz,
+                          ddelta_bias, dh0, saved, workspace};
     for (const void* q : ptrs)
         if (!aligned16(q)) return SS_ERR_UNSUPPORTED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -105,6 +114,13 @@ int bwd_impl(const void* u, const void* delta, const float* A, const void* B, co
             if (dD && cudaMemsetAsync(dD, 0, (size_t)Dch * sizeof(float), st) != cudaSuccess) return SS_ERR_CUDA;
             if (ddelta_bias && cudaMemsetAsync(ddelta_bias, 0, (size_t)Dch * sizeof(float), st) != cudaSuccess)
                 return SS_ERR_CUDA;
+        }
+        // L == 0: h0 is last_state, so its gradient is the incoming one
+        if (dh0 && Bsz > 0 && Dch > 0 && N > 0) {
+            const size_t bytes = (size_t)Bsz * Dch * N * sizeof(float);
+            const cudaError_t e = dlast ? cudaMemcpyAsync(dh0, dlast, bytes, cudaMemcpyDeviceToDevice, st)
+                                        : cudaMemsetAsync(dh0, 0, bytes, st);
+            if (e != cudaSuccess) return SS_ERR_CUDA;
         }
         // Dch == 0 with Bsz, L > 0: dB and dC are sums over no channels
         if (Dch == 0 && Bsz > 0 && L > 0 && N > 0) {
@@ -125,14 +141,18 @@ int bwd_impl(const void* u, const void* delta, const float* A, const void* B, co
     BwdArgs a;
     a.f.u = u; a.f.delta = delta; a.f.B = B; a.f.C = C; a.f.z = z;
     a.f.A = A; a.f.D = D; a.f.delta_bias = delta_bias;
+    a.f.h0 = h0;
     a.f.y = nullptr; a.f.last_state = nullptr;
     a.f.Bsz = Bsz; a.f.L = L; a.f.Dch = Dch; a.f.N = N;
     a.f.softplus = softplus ? 1 : 0;
+    a.f.a_is_log = a_is_log ? 1 : 0;
     a.f.dtype = dtype;
     a.f.ws_fsum = reinterpret_cast<float*>(ws + w.fsum);
     a.dy = dy;
+    a.dlast = dlast;
     a.du = du; a.ddelta = ddelta; a.dA = dA; a.dB = dB; a.dC = dC; a.dD = dD; a.dz = dz;
     a.ddelta_bias = ddelta_bias;
+    a.dh0 = dh0;
     a.ws_rsum = reinterpret_cast<float*>(ws + w.rsum);
     float* ckpt_out = from_saved ? nullptr : reinterpret_cast<float*>(ws + w.ckpt);
     a.ws_ckpt = from_saved ? static_cast<const float*>(saved) : ckpt_out;
@@ -170,7 +190,7 @@ int ss_profile_events(void* const* events, int count) {
     return SS_OK;
 }
 
-int ss_abi_version(void) { return 2; }
+int ss_abi_version(void) { return 3; }
 
 const char* ss_status_string(int status) {
     switch (status) {
@@ -233,8 +253,8 @@ int ss_fwd(const void* u, const void* delta, const float* A, const void* B, cons
            int64_t Dch, int64_t N, int dtype, void* workspace, size_t workspace_bytes, void* stream) {
     prof_begin();
     return prof_end(static_cast<cudaStream_t>(stream),
-                    fwd_impl(u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state, Bsz, L, Dch, N, dtype,
-                             false, nullptr, 0, workspace, workspace_bytes, stream));
+                    fwd_impl(u, delta, A, B, C, D, z, delta_bias, nullptr, softplus, 0, y, last_state, Bsz, L, Dch,
+                             N, dtype, false, nullptr, 0, workspace, workspace_bytes, stream));
 }
 
 int ss_fwd_save(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
@@ -243,8 +263,8 @@ int ss_fwd_save(const void* u, const void* delta, const float* A, const void* B,
                 size_t workspace_bytes, void* stream) {
     prof_begin();
     return prof_end(static_cast<cudaStream_t>(stream),
-                    fwd_impl(u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state, Bsz, L, Dch, N, dtype,
-                             true, saved, saved_bytes, workspace, workspace_bytes, stream));
+                    fwd_impl(u, delta, A, B, C, D, z, delta_bias, nullptr, softplus, 0, y, last_state, Bsz, L, Dch,
+                             N, dtype, true, saved, saved_bytes, workspace, workspace_bytes, stream));
 }
 
 int ss_bwd(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
@@ -253,9 +273,9 @@ int ss_bwd(const void* u, const void* delta, const float* A, const void* B, cons
            int64_t N, int dtype, void* workspace, size_t workspace_bytes, void* stream) {
     prof_begin();
     return prof_end(static_cast<cudaStream_t>(stream),
-                    bwd_impl(u, delta, A, B, C, D, z, delta_bias, softplus, dy, du, ddelta, dA, dB, dC, dD, dz,
-                             ddelta_bias, Bsz, L, Dch, N, dtype, false, nullptr, 0, workspace, workspace_bytes,
-                             stream));
+                    bwd_impl(u, delta, A, B, C, D, z, delta_bias, nullptr, softplus, 0, dy, nullptr, du, ddelta, dA,
+                             dB, dC, dD, dz, ddelta_bias, nullptr, Bsz, L, Dch, N, dtype, false, nullptr, 0, workspace,
+                             workspace_bytes, stream));
 }
 
 int ss_bwd_saved(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
@@ -265,9 +285,53 @@ int ss_bwd_saved(const void* u, const void* delta, const float* A, const void* B
                  size_t workspace_bytes, void* stream) {
     prof_begin();
     return prof_end(static_cast<cudaStream_t>(stream),
-                    bwd_impl(u, delta, A, B, C, D, z, delta_bias, softplus, dy, du, ddelta, dA, dB, dC, dD, dz,
-                             ddelta_bias, Bsz, L, Dch, N, dtype, true, saved, saved_bytes, workspace,
-                             workspace_bytes, stream));
+                    bwd_impl(u, delta, A, B, C, D, z, delta_bias, nullptr, softplus, 0, dy, nullptr, du, ddelta, dA,
+                             dB, dC, dD, dz, ddelta_bias, nullptr, Bsz, L, Dch, N, dtype, true, saved, saved_bytes,
+                             workspace, workspace_bytes, stream));
+}
+
+int ss_fwd_ex(const ss_fwd_desc* d, void* stream) {
+    if (d == nullptr) return SS_ERR_INVALID_PROBLEM;
+    prof_begin();
+    return prof_end(static_cast<cudaStream_t>(stream),
+                    fwd_impl(d->u, d->delta, d->A, d->B, d->C, d->D, d->z, d->delta_bias, d->h0, d->softplus,
+                             d->a_is_log, d->y, d->last_state, d->Bsz, d->L, d->Dch, d->N, d->dtype,
+                             d->saved != nullptr, d->saved, d->saved_bytes, d->workspace, d->workspace_bytes,
+                             stream));
+}
+
+int ss_bwd_ex(const ss_bwd_desc* d, void* stream) {
+    if (d == nullptr) return SS_ERR_INVALID_PROBLEM;
+    prof_begin();
+    return prof_end(static_cast<cudaStream_t>(stream),
+                    bwd_impl(d->u, d->delta, d->A, d->B, d->C, d->D, d->z, d->delta_bias, d->h0, d->softplus,
+                             d->a_is_log, d->dy, d->dlast_state, d->du, d->ddelta, d->dA, d->dB, d->dC, d->dD, d->dz,
+                             d->ddelta_bias, d->dh0, d->Bsz, d->L, d->Dch, d->N, d->dtype, d->saved != nullptr,
+                             d->saved, d->saved_bytes, d->workspace, d->workspace_bytes, stream));
+}
+
+int ss_decode_step(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
+                   const void* z, const float* delta_bias, int softplus, int a_is_log, float* state, void* y,
+                   int64_t Bsz, int64_t Dch, int64_t N, int dtype, void* stream) {
+    prof_begin();
+    int rc = check_sizes(Bsz, 1, Dch, N, dtype);
+    if (rc != SS_OK) return rc;
+    if (Bsz == 0 || Dch == 0) return SS_OK;
+    if (Bsz * Dch > (1ll << 36)) return SS_ERR_UNSUPPORTED;  // grid of at most 8 threads per (b, d) stays below 2^31 blocks
+    if (!u || !delta || !A || !B || !C || !state || !y) return SS_ERR_INVALID_PROBLEM;
+    const void* ptrs[] = {u, delta, A, B, C, D, z, delta_bias, state, y};
+    for (const void* q : ptrs)
+        if (!aligned16(q)) return SS_ERR_UNSUPPORTED;
+    DecodeArgs a;
+    a.u = u; a.delta = delta; a.B = B; a.C = C; a.z = z;
+    a.A = A; a.D = D; a.delta_bias = delta_bias;
+    a.state = state; a.y = y;
+    a.Bsz = Bsz; a.Dch = Dch; a.N = N;
+    a.softplus = softplus ? 1 : 0;
+    a.a_is_log = a_is_log ? 1 : 0;
+    a.dtype = dtype;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return prof_end(st, launch_decode(a, st) == cudaSuccess ? SS_OK : SS_ERR_CUDA);
 }
 
 }  // extern "C"

@@ -218,10 +218,12 @@ __device__ __forceinline__ void store_run(float* p, const float (&v)[CPL], int64
 }
 
 // MODE kRevMain: the backward proper.  MODE kRevSummary: only the adjoint
-// walk of chunks 1..K-1 from a zero carry, writing (P_k, M_k).
+// walk of chunks 1..K-1 from a zero carry, writing (P_k, M_k).  STATE: the
+// call has an incoming gradient of last_state or wants dh0 (a separate
+// instantiation, so that the plain backward carries none of it).
 constexpr int kRevMain = 0, kRevSummary = 1;
 
-template <typename T, int N, int MODE>
+template <typename T, int N, int MODE, bool STATE>
 __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo,
                                                                                int64_t k_hi) {
     using C = BCfg<T, N>;
@@ -294,20 +296,24 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
     // by ln 2 in the epilogue.  Channels past Dch run with a zero exponent, state
     // and adjoint: with u = dy = z = 0 loaded there, everything they form stays
     // exactly zero, so their dB / dC contributions need no masking.
+    // The adjoint carry into the end of the sequence is the incoming gradient of
+    // last_state (zero without one); a reverse summary starts from zero.
+    const bool from_dlast = MAIN && STATE && a.dlast != nullptr;
     float A2[2][S], carry[2][S], dA[2][S], Pr[2][MAIN ? 1 : S];
 #pragma unroll
     for (int e = 0; e < 2; e++) {
 #pragma unroll
         for (int s = 0; s < S; s++) {
-            A2[e][s] = ok[e] ? f.A[dd[e] * N + n0 + s] * kLog2eF : 0.f;
-            carry[e][s] = 0.f;
+            A2[e][s] = ok[e] ? scan_A(f, dd[e] * N + n0 + s) * kLog2eF : 0.f;
+            carry[e][s] = from_dlast && ok[e] ? a.dlast[row[e] * N + n0 + s] : 0.f;
             dA[e][s] = 0.f;
             if (!MAIN) Pr[e][s] = 1.f;
         }
     }
     if (MAIN && k + 1 < p.K) {
         // carry into the end of chunk k: rho_{j-1} = M_j + P_j rho_j from the
-        // reverse summaries (P_j, M_j) of chunks K-1 .. k+1, with rho_{K-1} = 0
+        // reverse summaries (P_j, M_j) of chunks K-1 .. k+1, with rho_{K-1} the
+        // carry into the end of the sequence
 #pragma unroll
         for (int e = 0; e < 2; e++) {
             const float2* rs = reinterpret_cast<const float2*>(a.ws_rsum) + row[e] * p.K * N + n0;
@@ -699,6 +705,11 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                 float* o = a.ws_dA + ((b * p.K + k) * Dch + dd[e]) * N + n0;
 #pragma unroll
                 for (int s = 0; s < S; s++) o[s] = dA[e][s];
+                // after the walk of the first chunk the carry is a_0 lam_0, the gradient of h0
+                if (STATE && k == 0 && a.dh0) {
+#pragma unroll
+                    for (int s = 0; s < S; s++) a.dh0[row[e] * N + n0 + s] = carry[e][s];
+                }
             }
         }
         // dD / ddelta_bias of each channel: the partials of the items that own it
@@ -769,7 +780,8 @@ __global__ void k_bwd2_reduce_params(BwdArgs a, FPlan p) {
     if (e < Dch * N) {
         float acc = 0.f;
         for (int64_t q = 0; q < parts; q++) acc += a.ws_dA[q * Dch * N + e];
-        a.dA[e] = acc;
+        // A_log form: dA_log = dA * A with A = -exp(A_log)
+        a.dA[e] = a.f.a_is_log ? acc * scan_A(a.f, e) : acc;
     }
     if (e < Dch) {
         if (a.dD) {
@@ -797,15 +809,17 @@ cudaError_t launch_bwd2_t(const BwdArgs& a, const FPlan& p, cudaStream_t st, flo
     if (p.K > 1) {
         const int64_t blocks = p.tiles_b * a.f.Bsz * (p.K - 1);
         prof_mark(st);
-        k_bwd2<T, N, kRevSummary><<<(unsigned)blocks, threads, 0, st>>>(a, p, 1, p.K);
+        k_bwd2<T, N, kRevSummary, false><<<(unsigned)blocks, threads, 0, st>>>(a, p, 1, p.K);
     }
     const int64_t blocks = p.tiles_b * a.f.Bsz * p.K;
+    const bool state = a.dlast != nullptr || a.dh0 != nullptr;
+    auto main_kernel = state ? k_bwd2<T, N, kRevMain, true> : k_bwd2<T, N, kRevMain, false>;
     // prefer the largest shared-memory carveout so that shared memory does not cap residency
-    e = cudaFuncSetAttribute(k_bwd2<T, N, kRevMain>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    e = cudaFuncSetAttribute(main_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     prof_mark(st);
-    k_bwd2<T, N, kRevMain><<<(unsigned)blocks, threads, 0, st>>>(a, p, 0, p.K);
+    main_kernel<<<(unsigned)blocks, threads, 0, st>>>(a, p, 0, p.K);
     const int64_t n_bc = 2 * a.f.Bsz * a.f.L * a.f.N / (N % 4 == 0 ? 4 : 1);  // threads
     prof_mark(st);
     k_bwd2_reduce_bc<<<(unsigned)ceil_div(n_bc, 256), 256, 0, st>>>(a, p);

@@ -131,15 +131,18 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(F
     const int n0 = w * NPW + g * S;
     const int sg = n0 / S;  // the lane's state group
     const int pslot = pair_slot<NGRP>(pp);
+    const int64_t row0 = b * Dch + dA0, row1 = b * Dch + dA1;
+    // the state starts at h0 (zero without one); a chunk summary starts from zero
+    const bool from_h0 = !SUMMARY && a.h0 != nullptr;
     float A2[2][S], h[2][S], P[2][S];
 #pragma unroll
     for (int s = 0; s < S; s++) {
-        A2[0][s] = a.A[dA0 * N + n0 + s] * kLog2eF;
-        A2[1][s] = a.A[dA1 * N + n0 + s] * kLog2eF;
-        h[0][s] = h[1][s] = 0.f;
+        A2[0][s] = scan_A(a, dA0 * N + n0 + s) * kLog2eF;
+        A2[1][s] = scan_A(a, dA1 * N + n0 + s) * kLog2eF;
+        h[0][s] = from_h0 && ok0 ? a.h0[row0 * N + n0 + s] : 0.f;
+        h[1][s] = from_h0 && ok1 ? a.h0[row1 * N + n0 + s] : 0.f;
         P[0][s] = P[1][s] = 1.f;
     }
-    const int64_t row0 = b * Dch + dA0, row1 = b * Dch + dA1;
     if (!SUMMARY && k > 0) {
         const float2* sm0 = reinterpret_cast<const float2*>(a.ws_fsum) + row0 * p.K * N + n0;
         const float2* sm1 = reinterpret_cast<const float2*>(a.ws_fsum) + row1 * p.K * N + n0;

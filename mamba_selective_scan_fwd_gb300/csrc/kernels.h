@@ -11,24 +11,44 @@ namespace ss {
 struct FwdArgs {
     const void *u, *delta, *B, *C, *z;
     const float *A, *D, *delta_bias;
+    const float* h0;  // initial state [Bsz][Dch][N], or null (zero)
     void* y;
     float* last_state;
     int64_t Bsz, L, Dch, N;
     int softplus;
+    int a_is_log;     // A holds A_log: the scan uses A = -exp(A_log)
     int dtype;        // 0 f32, 2 bf16
     float* ws_fsum;   // chunk summaries (P, H): [Bsz*Dch][K][N] float2
 };
 
+// A[d, n] of the scan: the input itself, or -exp(A_log) in the A_log form.
+__device__ __forceinline__ float scan_A(const FwdArgs& a, int64_t i) {
+    const float v = a.A[i];
+    return a.a_is_log ? -expf(v) : v;
+}
+
 struct BwdArgs {
     FwdArgs f;        // forward inputs; f.y / f.last_state unused
     const void* dy;
+    const float* dlast;  // incoming gradient of last_state [Bsz][Dch][N], or null (zero)
     float *du, *ddelta, *dA, *dB, *dC, *dD, *dz, *ddelta_bias;
+    float* dh0;          // gradient of the initial state [Bsz][Dch][N], or null
     float* ws_rsum;   // reverse chunk summaries (P, M): [Bsz*Dch][K][N] float2
     const float* ws_ckpt;  // sub-chunk start states, step-major: [K * Lc/kSub][Bsz*Dch][N]
     float* ws_bc;     // per-tile dB/dC partials: [2][tiles][Bsz][L][N]
     float* ws_dA;     // per-(b,k) dA partials: [Bsz][K][Dch][N]
     float* ws_dD;     // per-(b,k) dD partials: [Bsz][K][Dch]
     float* ws_db;     // per-(b,k) ddelta_bias partials: [Bsz][K][Dch]
+};
+
+// One decoding step in place on the state (ss_decode_step).
+struct DecodeArgs {
+    const void *u, *delta, *B, *C, *z;  // u, delta, z: io [Bsz, Dch]; B, C: io [Bsz, N]
+    const float *A, *D, *delta_bias;
+    float* state;                       // [Bsz][Dch][N], read and rewritten
+    void* y;                            // io [Bsz, Dch]
+    int64_t Bsz, Dch, N;
+    int softplus, a_is_log, dtype;
 };
 
 // Workspace layout of the backward (byte offsets, each 256-aligned).
@@ -88,6 +108,8 @@ cudaError_t launch_fwd2(const FwdArgs& a, const FPlan& p, cudaStream_t st, int m
 // ckpt_out: the checkpoint buffer to fill first, or null when a.ws_ckpt already
 // holds the states saved by the forward.
 cudaError_t launch_bwd2(const BwdArgs& a, const FPlan& p, cudaStream_t st, float* ckpt_out);
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
 
 // Bytes of the sub-chunk start states of every (b, d) row: the checkpoints the
 // backward recomputes from (ss_fwd_save writes them into the caller's buffer).

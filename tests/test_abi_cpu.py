@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol():
     lib = ss.lib()
     for name in declared_functions():
         assert hasattr(lib, name), name
-    assert lib.ss_abi_version() == binding.ABI_VERSION == 2
+    assert lib.ss_abi_version() == binding.ABI_VERSION == 3
 
 
 def test_status_strings():
@@ -197,3 +197,48 @@ def test_profile_events_validation():
     assert lib.ss_profile_events(None, 2) == INVALID
     assert lib.ss_profile_events(one, 1) == INVALID  # a NULL handle
     assert lib.ss_profile_events(None, 0) == OK      # switched off
+
+
+def test_descriptor_layouts_match_the_header(tmp_path):
+    """The ctypes descriptors have the size and field offsets of the C structs."""
+    import ctypes
+    import subprocess
+
+    fields_f = [f for f, _ in binding.FwdDesc._fields_]
+    fields_b = [f for f, _ in binding.BwdDesc._fields_]
+    src = ['#include <stdio.h>', '#include <stddef.h>', '#include "ss.h"', "int main(void) {",
+           'printf("%zu %zu\\n", sizeof(ss_fwd_desc), sizeof(ss_bwd_desc));']
+    src += [f'printf("%zu\\n", offsetof(ss_fwd_desc, {f}));' for f in fields_f]
+    src += [f'printf("%zu\\n", offsetof(ss_bwd_desc, {f}));' for f in fields_b]
+    src += ["return 0; }"]
+    c = tmp_path / "layout.c"
+    c.write_text("\n".join(src))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", INCLUDE, "-o", str(exe), str(c)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
+    sizes, offs = [int(v) for v in out[:2]], [int(v) for v in out[2:]]
+    assert sizes == [ctypes.sizeof(binding.FwdDesc), ctypes.sizeof(binding.BwdDesc)]
+    want = [getattr(binding.FwdDesc, f).offset for f in fields_f] + [getattr(binding.BwdDesc, f).offset for f in fields_b]
+    assert offs == want
+
+
+def test_ex_entry_points_validate_before_cuda():
+    import ctypes
+
+    lib = ss.lib()
+    assert lib.ss_fwd_ex(None, None) == INVALID
+    assert lib.ss_bwd_ex(None, None) == INVALID
+    d = binding.BwdDesc()
+    for f in ("u", "delta", "A", "B", "C", "dy", "du", "ddelta", "dA", "dB", "dC", "h0", "workspace"):
+        setattr(d, f, FAKE)
+    d.workspace_bytes = 1 << 40
+    d.Bsz, d.L, d.Dch, d.N, d.dtype, d.softplus = 1, 8, 8, 4, 0, 1
+    assert lib.ss_bwd_ex(ctypes.byref(d), None) == INVALID  # h0 given without dh0
+    d.h0, d.dh0 = None, FAKE
+    assert lib.ss_bwd_ex(ctypes.byref(d), None) == INVALID  # dh0 without h0
+    f = binding.FwdDesc()
+    for k in ("u", "delta", "A", "B", "C", "y"):
+        setattr(f, k, FAKE)
+    f.h0 = FAKE + 4  # misaligned
+    f.Bsz, f.L, f.Dch, f.N, f.dtype = 1, 8, 8, 4, 0
+    assert lib.ss_fwd_ex(ctypes.byref(f), None) == UNSUPPORTED
