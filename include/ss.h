@@ -16,8 +16,8 @@
  * row-major.  u, delta, z, y, dy: [Bsz, L, Dch].  A: [Dch, N].  B, C:
  * [Bsz, L, N].  D, delta_bias: [Dch].  last_state: [Bsz, Dch, N].
  *
- * Element types.  "io" tensors (u, delta, B, C, z, y, dy) are f32 or bf16 as
- * selected by `dtype`.  A, D, delta_bias, last_state and every gradient are
+ * Element types.  "io" tensors (u, delta, B, C, z, y, dy) are f32, f16 or
+ * bf16 as selected by `dtype`.  A, D, delta_bias, last_state and every gradient are
  * f32.  Arithmetic and the recurrence state are f32.
  *
  * Ownership and execution.  Every pointer is caller-owned DEVICE memory of
@@ -42,10 +42,9 @@
 extern "C" {
 #endif
 
-/* Element-type ids; the numbering follows the dtype ids of the
- * `..._workspace_bytes(.., dtype_id)` query on the baracuda-kernels page
- * (0 = f32, 1 = f16, 2 = bf16).  SS_F16 is reserved and returns
- * SS_ERR_UNSUPPORTED. */
+/* Element-type ids of the io tensors; the numbering follows the dtype ids of
+ * the `..._workspace_bytes(.., dtype_id)` query on the baracuda-kernels page
+ * (0 = f32, 1 = f16, 2 = bf16). */
 typedef enum { SS_F32 = 0, SS_F16 = 1, SS_BF16 = 2 } ss_dtype;
 
 /* Status codes; the first three mirror the page's error kinds

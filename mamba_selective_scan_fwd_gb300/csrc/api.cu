@@ -23,7 +23,7 @@ bool aligned16(const void* p) { return p == nullptr || (reinterpret_cast<uintptr
 
 int check_sizes(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype) {
     if (Bsz < 0 || L < 0 || Dch < 0 || N < 0) return SS_ERR_INVALID_PROBLEM;
-    if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_UNSUPPORTED;
+    if (dtype != SS_F32 && dtype != SS_F16 && dtype != SS_BF16) return SS_ERR_UNSUPPORTED;
     if (!n_supported(N)) return SS_ERR_UNSUPPORTED;
     // index products stay far inside int64; grid sizes stay inside 2^31 - 1 blocks
     if (Bsz > (1ll << 20) || L > (1ll << 31) || Dch > (1ll << 24)) return SS_ERR_UNSUPPORTED;

@@ -36,6 +36,8 @@
 // the chunk's decay product and M_k = a_{s_k} lam_{s_k} with lam from a zero
 // incoming carry -- combine as rho_{k-1} = M_k + P_k rho_k into each chunk's
 // carry-in adjoint.
+#pragma once
+
 #include "common.cuh"
 #include "kernels.h"
 #include "simd.cuh"
@@ -731,72 +733,6 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
         }
     }
 }
-// dB / dC: sum of the per-tile partials, tiles in ascending order.  A thread
-// owns 4 consecutive outputs (16-byte streaming loads, 8 tiles in flight)
-// when N is a multiple of 4, one output otherwise.
-__global__ void k_bwd2_reduce_bc(BwdArgs a, FPlan p) {
-    const int64_t bln = a.f.Bsz * a.f.L * a.f.N;
-    const int64_t tiles = p.tiles_b;
-    if (a.f.N % 4 == 0) {
-        const int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // float4 index over both tensors
-        const int64_t nq = bln / 4;
-        if (q >= 2 * nq) return;
-        const int tensor = q >= nq ? 1 : 0;
-        const int64_t r = q - tensor * nq;
-        const float4* src = reinterpret_cast<const float4*>(a.ws_bc + (size_t)tensor * tiles * bln) + r;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        int64_t tl = 0;
-        for (; tl + 8 <= tiles; tl += 8) {
-            float4 v[8];
-#pragma unroll
-            for (int u = 0; u < 8; u++) v[u] = __ldcs(src + (tl + u) * nq);
-#pragma unroll
-            for (int u = 0; u < 8; u++) {
-                acc.x += v[u].x; acc.y += v[u].y; acc.z += v[u].z; acc.w += v[u].w;
-            }
-        }
-        for (; tl < tiles; tl++) {
-            const float4 v = __ldcs(src + tl * nq);
-            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-        }
-        reinterpret_cast<float4*>(tensor ? a.dC : a.dB)[r] = acc;
-    } else {
-        const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-        if (e >= 2 * bln) return;
-        const int tensor = e >= bln ? 1 : 0;
-        const int64_t r = e - tensor * bln;
-        const float* src = a.ws_bc + (size_t)tensor * tiles * bln + r;
-        float acc = 0.f;
-        for (int64_t tl = 0; tl < tiles; tl++) acc += src[tl * bln];
-        (tensor ? a.dC : a.dB)[r] = acc;
-    }
-}
-
-// dA / dD / ddelta_bias: sum over (batch, chunk) partials in ascending order.
-__global__ void k_bwd2_reduce_params(BwdArgs a, FPlan p) {
-    const int64_t Dch = a.f.Dch, N = a.f.N;
-    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t parts = a.f.Bsz * p.K;
-    if (e < Dch * N) {
-        float acc = 0.f;
-        for (int64_t q = 0; q < parts; q++) acc += a.ws_dA[q * Dch * N + e];
-        // A_log form: dA_log = dA * A with A = -exp(A_log)
-        a.dA[e] = a.f.a_is_log ? acc * scan_A(a.f, e) : acc;
-    }
-    if (e < Dch) {
-        if (a.dD) {
-            float acc = 0.f;
-            for (int64_t q = 0; q < parts; q++) acc += a.ws_dD[q * Dch + e];
-            a.dD[e] = acc;
-        }
-        if (a.ddelta_bias) {
-            float acc = 0.f;
-            for (int64_t q = 0; q < parts; q++) acc += a.ws_db[q * Dch + e];
-            a.ddelta_bias[e] = acc;
-        }
-    }
-}
-
 template <typename T, int N>
 cudaError_t launch_bwd2_t(const BwdArgs& a, const FPlan& p, cudaStream_t st, float* ckpt_out) {
     cudaError_t e = cudaSuccess;
@@ -814,35 +750,34 @@ cudaError_t launch_bwd2_t(const BwdArgs& a, const FPlan& p, cudaStream_t st, flo
     const int64_t blocks = p.tiles_b * a.f.Bsz * p.K;
     const bool state = a.dlast != nullptr || a.dh0 != nullptr;
     auto main_kernel = state ? k_bwd2<T, N, kRevMain, true> : k_bwd2<T, N, kRevMain, false>;
-    // prefer the largest shared-memory carveout so that shared memory does not cap residency
-    e = cudaFuncSetAttribute(main_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
+    // prefer the largest shared-memory carveout so that shared memory does not cap
+    // residency; set once per kernel (a process-wide attribute, not a stream
+    // operation), so that calls recorded in a CUDA graph after a first eager
+    // call make no such call
+    static bool carveout_set[2] = {false, false};
+    if (!carveout_set[state]) {
+        e = cudaFuncSetAttribute(main_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        carveout_set[state] = true;
+    }
     prof_mark(st);
     main_kernel<<<(unsigned)blocks, threads, 0, st>>>(a, p, 0, p.K);
-    const int64_t n_bc = 2 * a.f.Bsz * a.f.L * a.f.N / (N % 4 == 0 ? 4 : 1);  // threads
-    prof_mark(st);
-    k_bwd2_reduce_bc<<<(unsigned)ceil_div(n_bc, 256), 256, 0, st>>>(a, p);
-    const int64_t n_par = a.f.Dch * a.f.N;
-    prof_mark(st);
-    k_bwd2_reduce_params<<<(unsigned)ceil_div(n_par, 256), 256, 0, st>>>(a, p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_bwd2(const BwdArgs& a, const FPlan& p, cudaStream_t st, float* ckpt_out) {
-#define SS_BWD2_N(T)                                              \
-    switch (a.f.N) {                                              \
-        case 1: return launch_bwd2_t<T, 1>(a, p, st, ckpt_out);   \
-        case 2: return launch_bwd2_t<T, 2>(a, p, st, ckpt_out);   \
-        case 4: return launch_bwd2_t<T, 4>(a, p, st, ckpt_out);   \
-        case 8: return launch_bwd2_t<T, 8>(a, p, st, ckpt_out);   \
-        case 16: return launch_bwd2_t<T, 16>(a, p, st, ckpt_out); \
-        case 32: return launch_bwd2_t<T, 32>(a, p, st, ckpt_out); \
-        default: return cudaErrorInvalidValue;                    \
+// Backward launcher of one io type: switches on N.
+template <typename T>
+cudaError_t launch_bwd2_io(const BwdArgs& a, const FPlan& p, cudaStream_t st, float* ckpt_out) {
+    switch (a.f.N) {
+        case 1: return launch_bwd2_t<T, 1>(a, p, st, ckpt_out);
+        case 2: return launch_bwd2_t<T, 2>(a, p, st, ckpt_out);
+        case 4: return launch_bwd2_t<T, 4>(a, p, st, ckpt_out);
+        case 8: return launch_bwd2_t<T, 8>(a, p, st, ckpt_out);
+        case 16: return launch_bwd2_t<T, 16>(a, p, st, ckpt_out);
+        case 32: return launch_bwd2_t<T, 32>(a, p, st, ckpt_out);
+        default: return cudaErrorInvalidValue;
     }
-    if (a.f.dtype == 0) { SS_BWD2_N(float) }
-    SS_BWD2_N(__nv_bfloat16)
-#undef SS_BWD2_N
 }
 
 }  // namespace ss

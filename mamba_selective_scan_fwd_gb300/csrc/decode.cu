@@ -28,6 +28,8 @@ template <typename T>
 __device__ __forceinline__ float ld_io(const T* p, int64_t i) {
     if constexpr (sizeof(T) == 4) {
         return __ldg(reinterpret_cast<const float*>(p) + i);
+    } else if constexpr (std::is_same<T, __half>::value) {
+        return __half2float(__ushort_as_half(__ldg(reinterpret_cast<const unsigned short*>(p) + i)));
     } else {
         return __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short*>(p) + i) << 16);
     }
@@ -116,6 +118,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
         default: return cudaErrorInvalidValue;               \
     }
     if (a.dtype == 0) { SS_DEC_N(float) }
+    if (a.dtype == 1) { SS_DEC_N(__half) }
     SS_DEC_N(__nv_bfloat16)
 #undef SS_DEC_N
 }

@@ -1,0 +1,105 @@
+// Launch dispatch on the io type (the kernels of each io type live in their
+// own translation unit: fwd2_*.cu, bwd2_*.cu), and the two backward
+// reduction kernels, which do not depend on it.
+#include "common.cuh"
+#include "kernels.h"
+#include "simd.cuh"
+
+namespace ss {
+
+// mode kModeY: the forward (summaries when K > 1, then y and last_state),
+// also storing the state at every kSub-step sub-chunk start into ckpt when
+// ckpt is given; mode kModeCkpt: the same walk writing only those states
+// (used by the backward), no y.
+cudaError_t launch_fwd2(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt) {
+    if (a.dtype == 0) return launch_fwd2_io<float>(a, p, st, mode, ckpt);
+    if (a.dtype == 1) return launch_fwd2_io<__half>(a, p, st, mode, ckpt);
+    return launch_fwd2_io<__nv_bfloat16>(a, p, st, mode, ckpt);
+}
+
+__global__ void k_bwd2_reduce_bc(BwdArgs a, FPlan p);
+__global__ void k_bwd2_reduce_params(BwdArgs a, FPlan p);
+
+// The backward's scan kernels (io-typed), then the two reductions.
+cudaError_t launch_bwd2(const BwdArgs& a, const FPlan& p, cudaStream_t st, float* ckpt_out) {
+    cudaError_t e;
+    if (a.f.dtype == 0) e = launch_bwd2_io<float>(a, p, st, ckpt_out);
+    else if (a.f.dtype == 1) e = launch_bwd2_io<__half>(a, p, st, ckpt_out);
+    else e = launch_bwd2_io<__nv_bfloat16>(a, p, st, ckpt_out);
+    if (e != cudaSuccess) return e;
+    const int64_t n_bc = 2 * a.f.Bsz * a.f.L * a.f.N / (a.f.N % 4 == 0 ? 4 : 1);  // threads
+    prof_mark(st);
+    k_bwd2_reduce_bc<<<(unsigned)ceil_div(n_bc, 256), 256, 0, st>>>(a, p);
+    const int64_t n_par = a.f.Dch * a.f.N;
+    prof_mark(st);
+    k_bwd2_reduce_params<<<(unsigned)ceil_div(n_par, 256), 256, 0, st>>>(a, p);
+    return cudaGetLastError();
+}
+
+// dB / dC: sum of the per-tile partials, tiles in ascending order.  A thread
+// owns 4 consecutive outputs (16-byte streaming loads, 8 tiles in flight)
+// when N is a multiple of 4, one output otherwise.
+__global__ void k_bwd2_reduce_bc(BwdArgs a, FPlan p) {
+    const int64_t bln = a.f.Bsz * a.f.L * a.f.N;
+    const int64_t tiles = p.tiles_b;
+    if (a.f.N % 4 == 0) {
+        const int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // float4 index over both tensors
+        const int64_t nq = bln / 4;
+        if (q >= 2 * nq) return;
+        const int tensor = q >= nq ? 1 : 0;
+        const int64_t r = q - tensor * nq;
+        const float4* src = reinterpret_cast<const float4*>(a.ws_bc + (size_t)tensor * tiles * bln) + r;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        int64_t tl = 0;
+        for (; tl + 8 <= tiles; tl += 8) {
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; u++) v[u] = __ldcs(src + (tl + u) * nq);
+#pragma unroll
+            for (int u = 0; u < 8; u++) {
+                acc.x += v[u].x; acc.y += v[u].y; acc.z += v[u].z; acc.w += v[u].w;
+            }
+        }
+        for (; tl < tiles; tl++) {
+            const float4 v = __ldcs(src + tl * nq);
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        reinterpret_cast<float4*>(tensor ? a.dC : a.dB)[r] = acc;
+    } else {
+        const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+        if (e >= 2 * bln) return;
+        const int tensor = e >= bln ? 1 : 0;
+        const int64_t r = e - tensor * bln;
+        const float* src = a.ws_bc + (size_t)tensor * tiles * bln + r;
+        float acc = 0.f;
+        for (int64_t tl = 0; tl < tiles; tl++) acc += src[tl * bln];
+        (tensor ? a.dC : a.dB)[r] = acc;
+    }
+}
+
+// dA / dD / ddelta_bias: sum over (batch, chunk) partials in ascending order.
+__global__ void k_bwd2_reduce_params(BwdArgs a, FPlan p) {
+    const int64_t Dch = a.f.Dch, N = a.f.N;
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t parts = a.f.Bsz * p.K;
+    if (e < Dch * N) {
+        float acc = 0.f;
+        for (int64_t q = 0; q < parts; q++) acc += a.ws_dA[q * Dch * N + e];
+        // A_log form: dA_log = dA * A with A = -exp(A_log)
+        a.dA[e] = a.f.a_is_log ? acc * scan_A(a.f, e) : acc;
+    }
+    if (e < Dch) {
+        if (a.dD) {
+            float acc = 0.f;
+            for (int64_t q = 0; q < parts; q++) acc += a.ws_dD[q * Dch + e];
+            a.dD[e] = acc;
+        }
+        if (a.ddelta_bias) {
+            float acc = 0.f;
+            for (int64_t q = 0; q < parts; q++) acc += a.ws_db[q * Dch + e];
+            a.ddelta_bias[e] = acc;
+        }
+    }
+}
+
+}  // namespace ss

@@ -27,6 +27,8 @@
 // The time axis is cut into K chunks only when batch x channels cannot fill
 // the GPU; a chunk summary (P, H) = (product of a, end state from zero) then
 // gives the carry-in state of the chunks after it.
+#pragma once
+
 #include "common.cuh"
 #include "kernels.h"
 #include "simd.cuh"
@@ -368,7 +370,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(F
                             for (int c = 0; c < GRP; c++) wv[c] = __float_as_uint(yv[c]);
                         } else {
 #pragma unroll
-                            for (int c = 0; c < GRP; c += 2) wv[c >> 1] = pack_bf16x2(yv[c], yv[c + 1]);
+                            for (int c = 0; c < GRP; c += 2) wv[c >> 1] = pack2<T>(yv[c], yv[c + 1]);
                         }
 #pragma unroll
                         for (int v = 0; v < RW / 4; v++)
@@ -443,24 +445,18 @@ cudaError_t launch_fwd2_t(const FwdArgs& a, const FPlan& p, cudaStream_t st, int
     return cudaGetLastError();
 }
 
-// mode kModeY: the forward (summaries when K > 1, then y and last_state),
-// also storing the state at every kSub-step sub-chunk start into ckpt when
-// ckpt is given; mode kModeCkpt: the same walk writing only those states
-// (used by the backward), no y.
-cudaError_t launch_fwd2(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt) {
-#define SS_FWD2_N(T)                                                  \
-    switch (a.N) {                                                    \
-        case 1: return launch_fwd2_t<T, 1>(a, p, st, mode, ckpt);     \
-        case 2: return launch_fwd2_t<T, 2>(a, p, st, mode, ckpt);     \
-        case 4: return launch_fwd2_t<T, 4>(a, p, st, mode, ckpt);     \
-        case 8: return launch_fwd2_t<T, 8>(a, p, st, mode, ckpt);     \
-        case 16: return launch_fwd2_t<T, 16>(a, p, st, mode, ckpt);   \
-        case 32: return launch_fwd2_t<T, 32>(a, p, st, mode, ckpt);   \
-        default: return cudaErrorInvalidValue;                        \
+// Forward launcher of one io type: switches on N.
+template <typename T>
+cudaError_t launch_fwd2_io(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt) {
+    switch (a.N) {
+        case 1: return launch_fwd2_t<T, 1>(a, p, st, mode, ckpt);
+        case 2: return launch_fwd2_t<T, 2>(a, p, st, mode, ckpt);
+        case 4: return launch_fwd2_t<T, 4>(a, p, st, mode, ckpt);
+        case 8: return launch_fwd2_t<T, 8>(a, p, st, mode, ckpt);
+        case 16: return launch_fwd2_t<T, 16>(a, p, st, mode, ckpt);
+        case 32: return launch_fwd2_t<T, 32>(a, p, st, mode, ckpt);
+        default: return cudaErrorInvalidValue;
     }
-    if (a.dtype == 0) { SS_FWD2_N(float) }
-    SS_FWD2_N(__nv_bfloat16)
-#undef SS_FWD2_N
 }
 
 }  // namespace ss

@@ -103,6 +103,13 @@ constexpr int kSub = 4;  // backward sub-chunk: steps whose states stay in regis
 // marks before each kernel it launches, the entry point once after the last.
 void prof_mark(cudaStream_t st);
 
+// Launchers of one io type T (float, __half, __nv_bfloat16), defined in the
+// per-io translation units.
+template <typename T>
+cudaError_t launch_fwd2_io(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt);
+template <typename T>
+cudaError_t launch_bwd2_io(const BwdArgs& a, const FPlan& p, cudaStream_t st, float* ckpt_out);
+
 // ckpt: where the Y-mode forward also stores the sub-chunk start states (may be null).
 cudaError_t launch_fwd2(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt);
 // ckpt_out: the checkpoint buffer to fill first, or null when a.ws_ckpt already

@@ -6,21 +6,41 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <type_traits>
 
 #include "simd.cuh"
 
 namespace ss {
 
-// element j of a row held as 32-bit words
+// element j of a row held as 32-bit words (f32, bf16 or f16 io; both 16-bit
+// types convert to f32 exactly)
 template <typename T>
 __device__ __forceinline__ float elem(const uint32_t* w, int j) {
     if constexpr (sizeof(T) == 4) {
         return __uint_as_float(w[j]);
+    } else if constexpr (std::is_same<T, __half>::value) {
+        const uint32_t v = w[j >> 1];
+        return __half2float(__ushort_as_half((unsigned short)((j & 1) ? (v >> 16) : (v & 0xffffu))));
     } else {
         return (j & 1) ? bf16hi(w[j >> 1]) : bf16lo(w[j >> 1]);
     }
+}
+
+// Two f32 values rounded to nearest (ties to even) into one word of the
+// 16-bit io type, lo | hi << 16.
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    uint32_t r;
+    if constexpr (std::is_same<T, __half>::value) {
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    } else {
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    }
+    return r;
 }
 
 // Load NBYTES contiguous bytes (naturally aligned) into words.

@@ -132,6 +132,8 @@ def round_io(x: np.ndarray, io: str) -> np.ndarray:
         return np.ascontiguousarray(x, dtype=np.float32)
     if io == "bf16":
         return round_bf16(x)
+    if io == "f16":
+        return x.astype(np.float16).astype(np.float32)  # round to nearest, ties to even
     raise ValueError(f"unknown io dtype {io!r}")
 
 

@@ -76,7 +76,7 @@ def _bwd(**kw):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(Bsz=-1), INVALID), (dict(L=-3), INVALID), (dict(Dch=-1), INVALID), (dict(N=-1), INVALID),
-    (dict(dtype=1), UNSUPPORTED), (dict(dtype=7), UNSUPPORTED), (dict(N=3), UNSUPPORTED), (dict(N=0), UNSUPPORTED),
+    (dict(dtype=3), UNSUPPORTED), (dict(dtype=7), UNSUPPORTED), (dict(N=3), UNSUPPORTED), (dict(N=0), UNSUPPORTED),
     (dict(N=64), UNSUPPORTED), (dict(u=None), INVALID), (dict(delta=None), INVALID), (dict(A=None), INVALID),
     (dict(B=None), INVALID), (dict(C=None), INVALID), (dict(y=None), INVALID),
     (dict(u=FAKE + 4), UNSUPPORTED), (dict(B=FAKE + 2), UNSUPPORTED), (dict(D=FAKE + 8), UNSUPPORTED),
@@ -97,7 +97,7 @@ def _fwd_save(**kw):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(Bsz=-1), INVALID), (dict(dtype=1), UNSUPPORTED), (dict(N=3), UNSUPPORTED), (dict(y=None), INVALID),
+    (dict(Bsz=-1), INVALID), (dict(dtype=3), UNSUPPORTED), (dict(N=3), UNSUPPORTED), (dict(y=None), INVALID),
     (dict(saved=None), WS_SMALL), (dict(saved=FAKE + 8), UNSUPPORTED), (dict(savedb=0), WS_SMALL),
 ])
 def test_fwd_save_rejects(kw, code):
@@ -131,7 +131,7 @@ def test_fwd_workspace_too_small_reports_before_launch():
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(Bsz=-1), INVALID), (dict(dtype=1), UNSUPPORTED), (dict(N=5), UNSUPPORTED),
+    (dict(Bsz=-1), INVALID), (dict(dtype=3), UNSUPPORTED), (dict(N=5), UNSUPPORTED),
     (dict(D=FAKE), INVALID), (dict(dD=FAKE), INVALID),            # D <-> dD presence must match
     (dict(z=FAKE), INVALID), (dict(dz=FAKE), INVALID),            # z <-> dz
     (dict(bias=FAKE), INVALID), (dict(dbias=FAKE), INVALID),      # delta_bias <-> ddelta_bias

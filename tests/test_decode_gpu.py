@@ -16,7 +16,7 @@ SHAPES = [(3, 70, 16), (2, 5, 32), (4, 33, 8), (1, 9, 4), (2, 7, 2), (3, 11, 1),
 
 
 @pytest.mark.parametrize("a_is_log", [False, True])
-@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("io", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("shape", SHAPES, ids=[f"B{s[0]}D{s[1]}N{s[2]}" for s in SHAPES])
 def test_decode_step_parity(orc, shape, io, a_is_log):
     Bsz, Dch, N = shape

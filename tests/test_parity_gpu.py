@@ -53,7 +53,7 @@ def make(shape, io, variant, seed):
 
 
 @pytest.mark.parametrize("variant", list(VARIANTS))
-@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("io", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("shape", SHAPES, ids=[f"B{s[0]}L{s[1]}D{s[2]}N{s[3]}" for s in SHAPES])
 def test_fwd_bwd_parity(orc, shape, io, variant):
     seed = 1000 + SHAPES.index(shape) * 10 + list(VARIANTS).index(variant)
