@@ -340,10 +340,12 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
     const int64_t t_begin = k * p.Lc;
     const int64_t t_end = t_begin + p.Lc < L ? t_begin + p.Lc : L;
     const int64_t ntile = (t_end - t_begin + kTT - 1) / kTT;
-    // saved states, step-major: [k * (Lc / kSub) + j][Bsz * Dch][N]
-    const int64_t ck_stride = f.Bsz * Dch * N;
-    const float* ck0 = a.ws_ckpt + (k * (p.Lc / kSub)) * ck_stride + row[0] * N + n0;
-    const float* ck1 = a.ws_ckpt + (k * (p.Lc / kSub)) * ck_stride + row[1] * N + n0;
+    // saved states (layout of ckpt_bytes): one block of CH x N floats per
+    // (sub-chunk slot, batch, channel tile), the lane's slots in lane order
+    const int64_t ck_stride = f.Bsz * p.tiles_b * CH * N;
+    const float* ck_blk = a.ws_ckpt + (k * (p.Lc / kSub)) * ck_stride + (b * p.tiles_b + tile) * (CH * N);
+    const float* ck0 = ck_blk + ckpt_slot(w, 0, lane, S);
+    const float* ck1 = ck_blk + ckpt_slot(w, 1, lane, S);
     float* bc0 = a.ws_bc + ((int64_t)tile * f.Bsz + b) * L * N;                  // dB partials of this tile
     float* bc1 = a.ws_bc + ((int64_t)(p.tiles_b + tile) * f.Bsz + b) * L * N;    // dC partials
     float* sRw = &sR[MAIN ? w : 0][0];

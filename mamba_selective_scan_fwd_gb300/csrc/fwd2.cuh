@@ -160,10 +160,12 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(F
 
     const int64_t t_begin = k * p.Lc;
     const int64_t t_end = t_begin + p.Lc < L ? t_begin + p.Lc : L;
-    // saved states, step-major: [k * (Lc / kSub) + j][Bsz * Dch][N]
-    const int64_t ck_stride = a.Bsz * Dch * N;
-    float* ck0 = SAVE ? ckpt + (k * (p.Lc / kSub)) * ck_stride + row0 * N + n0 : nullptr;
-    float* ck1 = SAVE ? ckpt + (k * (p.Lc / kSub)) * ck_stride + row1 * N + n0 : nullptr;
+    // saved states (layout of ckpt_bytes): one block of CH x N floats per
+    // (sub-chunk slot, batch, channel tile), the lane's slots in lane order
+    const int64_t ck_stride = a.Bsz * ntiles * CH * N;
+    float* ck_blk = SAVE ? ckpt + (k * (p.Lc / kSub)) * ck_stride + (b * ntiles + tile) * (CH * N) : nullptr;
+    float* ck0 = SAVE ? ck_blk + ckpt_slot(w, 0, lane, S) : nullptr;
+    float* ck1 = SAVE ? ck_blk + ckpt_slot(w, 1, lane, S) : nullptr;
 
     // Asynchronous copies of the tile starting at tt: the thread's item runs
     // (when the tile's rows are whole aligned vectors) and the B / C rows (f32
@@ -270,21 +272,18 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(F
         for (int i = 0; i < kRow; i++) {
             if (SAVE && (i % kSub) == 0) {
                 const int64_t jo = (jt + i / kSub) * ck_stride;
+                // every slot is written: channels past Dch hold a zero state
                 if constexpr (S % 4 == 0) {
 #pragma unroll
                     for (int s = 0; s < S; s += 4) {
-                        if (ok0)
-                            *reinterpret_cast<float4*>(ck0 + jo + s) =
-                                make_float4(h[0][s], h[0][s + 1], h[0][s + 2], h[0][s + 3]);
-                        if (ok1)
-                            *reinterpret_cast<float4*>(ck1 + jo + s) =
-                                make_float4(h[1][s], h[1][s + 1], h[1][s + 2], h[1][s + 3]);
+                        *reinterpret_cast<float4*>(ck0 + jo + s) = make_float4(h[0][s], h[0][s + 1], h[0][s + 2], h[0][s + 3]);
+                        *reinterpret_cast<float4*>(ck1 + jo + s) = make_float4(h[1][s], h[1][s + 1], h[1][s + 2], h[1][s + 3]);
                     }
                 } else {
 #pragma unroll
                     for (int s = 0; s < S; s++) {
-                        if (ok0) ck0[jo + s] = h[0][s];
-                        if (ok1) ck1[jo + s] = h[1][s];
+                        ck0[jo + s] = h[0][s];
+                        ck1[jo + s] = h[1][s];
                     }
                 }
             }
@@ -397,8 +396,8 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(F
         for (int64_t jj = tiles_len / kSub; jj < nsub; jj++) {
 #pragma unroll
             for (int s = 0; s < S; s++) {
-                if (ok0) ck0[jj * ck_stride + s] = h[0][s];
-                if (ok1) ck1[jj * ck_stride + s] = h[1][s];
+                ck0[jj * ck_stride + s] = h[0][s];
+                ck1[jj * ck_stride + s] = h[1][s];
             }
         }
     }

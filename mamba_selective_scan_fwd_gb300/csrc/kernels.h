@@ -120,8 +120,18 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
 
 // Bytes of the sub-chunk start states of every (b, d) row: the checkpoints the
 // backward recomputes from (ss_fwd_save writes them into the caller's buffer).
+// Layout: [k (Lc / kSub) + j][b][channel tile][block of CH x N floats]; within
+// a block, float ((w 2 + e) 32 + lane) S + s is state n0 + s of channel c0 + e
+// of the lane (the scan kernels' lane layout), so that a warp's stores and
+// loads of one channel parity are contiguous.
 inline size_t ckpt_bytes(const FPlan& p, int64_t Bsz, int64_t Dch, int64_t N) {
-    return (size_t)Bsz * Dch * p.K * (p.Lc / kSub) * N * sizeof(float);
+    (void)Dch;
+    return (size_t)Bsz * p.tiles_b * channels_per_block(N) * p.K * (p.Lc / kSub) * N * sizeof(float);
+}
+
+// Float offset of a lane's slot for channel parity e within a saved-state block.
+__host__ __device__ constexpr int64_t ckpt_slot(int w, int e, int lane, int S) {
+    return ((int64_t)(w * 2 + e) * 32 + lane) * S;
 }
 
 // Workspace of the backward (byte offsets, each 256-aligned): forward and
