@@ -91,24 +91,6 @@ __device__ __forceinline__ int bpair_slot(int pp) {
     return (pp >> 1) + (PAIRS / 2) * (pp & 1);
 }
 
-// softplus(x) (as in simd.cuh) together with sigmoid(x), sharing e = e^-|x|.
-__device__ __forceinline__ void softplus_and_sigmoid(float x, float& sp, float& sg) {
-    const float e = ex2a(-fabsf(x) * kLog2eF);
-    const float s = e * rcpa(2.f + e);
-    const float s2 = s * s;
-    float p = 1.f / 15.f;
-    p = fmaf(p, s2, 1.f / 13.f);
-    p = fmaf(p, s2, 1.f / 11.f);
-    p = fmaf(p, s2, 1.f / 9.f);
-    p = fmaf(p, s2, 1.f / 7.f);
-    p = fmaf(p, s2, 1.f / 5.f);
-    p = fmaf(p, s2, 1.f / 3.f);
-    p = fmaf(p, s2, 1.f);
-    sp = fmaxf(x, 0.f) + 2.f * s * p;
-    const float r = rcpa(1.f + e);
-    sg = x >= 0.f ? r : e * r;
-}
-
 template <int S>
 __device__ __forceinline__ void ld_state(const float* p, float (&v)[S]) {
     if constexpr (S % 4 == 0) {
@@ -429,27 +411,33 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
             }
             float dl[GRP], dlu[GRP], gg[GRP], uu[GRP], sgx[GRP], dzf[GRP];
 #pragma unroll
-            for (int c = 0; c < GRP; c++) {
-                dl[c] = dlu[c] = gg[c] = uu[c] = sgx[c] = dzf[c] = 0.f;
+            for (int c = 0; c < GRP; c += 2) {
+                // two channels at a time with packed arithmetic
+                float2 dl2 = make_float2(0.f, 0.f), sg2 = dl2, uu2 = dl2, dlu2 = dl2, gg2 = dl2, dz2 = dl2;
                 if (rv) {
-                    const float x = elem<T>(rd, c) + sBias[cg + c];
+                    const float2 x = make_float2(elem<T>(rd, c) + sBias[cg + c], elem<T>(rd, c + 1) + sBias[cg + c + 1]);
                     if (f.softplus) {
-                        softplus_and_sigmoid(x, dl[c], sgx[c]);
+                        softplus_sigmoid2(x, dl2, sg2);
                     } else {
-                        dl[c] = x;
-                        sgx[c] = 1.f;
+                        dl2 = x;
+                        sg2 = make_float2(1.f, 1.f);
                     }
-                    uu[c] = elem<T>(ru, c);
-                    dlu[c] = dl[c] * uu[c];
-                    const float dyv = elem<T>(rg, c);
-                    gg[c] = dyv;
+                    uu2 = make_float2(elem<T>(ru, c), elem<T>(ru, c + 1));
+                    dlu2 = mul2(dl2, uu2);
+                    const float2 dyv = make_float2(elem<T>(rg, c), elem<T>(rg, c + 1));
+                    gg2 = dyv;
                     if (z) {
-                        const float zz = elem<T>(rz, c);
-                        const float sz = sigmoid_fast(zz);
-                        gg[c] = dyv * zz * sz;
-                        dzf[c] = dyv * sz * fmaf(zz, 1.f - sz, 1.f);
+                        const float2 zz = make_float2(elem<T>(rz, c), elem<T>(rz, c + 1));
+                        const float2 sz = sigmoid2(zz);
+                        const float2 dsz = mul2(dyv, sz);
+                        gg2 = mul2(dsz, zz);
+                        // dz factor dy sig(z) (1 + z (1 - sig(z)))
+                        dz2 = mul2(dsz, fma2(zz, add2(splat2(1.f), make_float2(-sz.x, -sz.y)), splat2(1.f)));
                     }
                 }
+                dl[c] = dl2.x; dl[c + 1] = dl2.y; sgx[c] = sg2.x; sgx[c + 1] = sg2.y;
+                uu[c] = uu2.x; uu[c + 1] = uu2.y; dlu[c] = dlu2.x; dlu[c + 1] = dlu2.y;
+                gg[c] = gg2.x; gg[c + 1] = gg2.y; dzf[c] = dz2.x; dzf[c + 1] = dz2.y;
             }
 #pragma unroll
             for (int c = 0; c < GRP; c += 2) {

@@ -226,26 +226,24 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(F
             }
 #pragma unroll
             for (int c = 0; c < GRP; c += 2) {
-                float dl[2] = {0.f, 0.f}, dlu[2] = {0.f, 0.f}, gt[2] = {1.f, 1.f}, du_[2] = {0.f, 0.f};
-#pragma unroll
-                for (int e = 0; e < 2; e++) {
-                    const int cc = cg + c + e;
-                    if (rv) {
-                        const float x = elem<T>(rd, c + e) + sBias[cc];
-                        dl[e] = a.softplus ? softplus_fast(x) : x;
-                        dlu[e] = dl[e] * elem<T>(ru, c + e);
-                        if (!NOY) {
-                            if (z) {
-                                const float zz = elem<T>(rz, c + e);
-                                gt[e] = zz * sigmoid_fast(zz);
-                            }
-                            du_[e] = sDv[cc] * elem<T>(ru, c + e);
+                // two channels at a time with packed arithmetic
+                float2 dl = make_float2(0.f, 0.f), dlu = dl, gt = make_float2(1.f, 1.f), dun = dl;
+                if (rv) {
+                    const float2 x = make_float2(elem<T>(rd, c) + sBias[cg + c], elem<T>(rd, c + 1) + sBias[cg + c + 1]);
+                    dl = a.softplus ? softplus2(x) : x;
+                    const float2 uu = make_float2(elem<T>(ru, c), elem<T>(ru, c + 1));
+                    dlu = mul2(dl, uu);
+                    if (!NOY) {
+                        if (z) {
+                            const float2 zz = make_float2(elem<T>(rz, c), elem<T>(rz, c + 1));
+                            gt = mul2(zz, sigmoid2(zz));
                         }
+                        dun = mul2(make_float2(sDv[cg + c], sDv[cg + c + 1]), uu);
                     }
                 }
                 const int slot = pair_slot<NGRP>((cg + c) / 2);
-                sDU[r][slot] = make_float4(dl[0], dlu[0], dl[1], dlu[1]);
-                if (!NOY) sGD[r][slot] = make_float4(gt[0], du_[0], gt[1], du_[1]);
+                sDU[r][slot] = make_float4(dl.x, dlu.x, dl.y, dlu.y);
+                if (!NOY) sGD[r][slot] = make_float4(gt.x, dun.x, gt.y, dun.y);
             }
         }
         if constexpr (!C::BC_DIRECT) {

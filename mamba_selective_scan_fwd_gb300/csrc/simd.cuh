@@ -97,6 +97,41 @@ __device__ __forceinline__ float softplus_fast(float x) {
 // sigmoid(x) = 1 / (1 + e^-x)
 __device__ __forceinline__ float sigmoid_fast(float x) { return rcpa(1.f + ex2a(-x * kLog2eF)); }
 
+// Two values at a time with packed f32x2 arithmetic (the MUFU steps stay
+// scalar): the softplus of softplus_fast, together with sigmoid(x) from the
+// same e = e^-|x| (sigmoid(x) = 1 / (1 + e) for x >= 0, e / (1 + e) below).
+__device__ __forceinline__ void softplus_sigmoid2(float2 x, float2& sp, float2& sg) {
+    const float2 e = make_float2(ex2a(-fabsf(x.x) * kLog2eF), ex2a(-fabsf(x.y) * kLog2eF));
+    const float2 t = add2(e, splat2(2.f));
+    const float2 s = mul2(e, make_float2(rcpa(t.x), rcpa(t.y)));
+    const float2 s2 = mul2(s, s);
+    float2 p = splat2(1.f / 15.f);
+    p = fma2(p, s2, splat2(1.f / 13.f));
+    p = fma2(p, s2, splat2(1.f / 11.f));
+    p = fma2(p, s2, splat2(1.f / 9.f));
+    p = fma2(p, s2, splat2(1.f / 7.f));
+    p = fma2(p, s2, splat2(1.f / 5.f));
+    p = fma2(p, s2, splat2(1.f / 3.f));
+    p = fma2(p, s2, splat2(1.f));
+    sp = fma2(add2(s, s), p, make_float2(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f)));
+    const float2 d = add2(e, splat2(1.f));
+    const float2 r = make_float2(rcpa(d.x), rcpa(d.y));
+    const float2 er = mul2(e, r);
+    sg = make_float2(x.x >= 0.f ? r.x : er.x, x.y >= 0.f ? r.y : er.y);
+}
+
+__device__ __forceinline__ float2 softplus2(float2 x) {
+    float2 sp, sg;
+    softplus_sigmoid2(x, sp, sg);
+    return sp;
+}
+
+__device__ __forceinline__ float2 sigmoid2(float2 x) {
+    const float2 e = make_float2(ex2a(-x.x * kLog2eF), ex2a(-x.y * kLog2eF));
+    const float2 d = add2(e, splat2(1.f));
+    return make_float2(rcpa(d.x), rcpa(d.y));
+}
+
 // ---------------------------------------------------------------- bf16 bits
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
