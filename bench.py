@@ -174,6 +174,51 @@ def job_throughput(units_per_rank, world, ms):
     return world * units_per_rank / (ms / 1e3)
 
 
+def measure_decode(dev, hbm_peak, peak_kind, steps=50):
+    """One ss_decode_step per token on a Mamba-2.8B-layer decoding batch whose
+    state (Bsz x Dch x N f32) is larger than the L2: HBM-bound, reported
+    against the measured copy bandwidth."""
+    import torch
+
+    import mamba_selective_scan_fwd_gb300 as ss
+
+    Bsz, Dch, N = 512, 5120, 16
+    g = torch.Generator(device=dev).manual_seed(7)
+    bf = torch.bfloat16
+    u = torch.randn((Bsz, Dch), generator=g, device=dev).to(bf)
+    delta = (0.5 * torch.randn((Bsz, Dch), generator=g, device=dev)).to(bf)
+    z = torch.randn((Bsz, Dch), generator=g, device=dev).to(bf)
+    Bm = torch.randn((Bsz, N), generator=g, device=dev).to(bf)
+    Cm = torch.randn((Bsz, N), generator=g, device=dev).to(bf)
+    A = -torch.arange(1, N + 1, device=dev, dtype=torch.float32).repeat(Dch, 1).contiguous()
+    D = torch.ones(Dch, device=dev)
+    bias = torch.full((Dch,), -4.0, device=dev)
+    state = torch.randn((Bsz, Dch, N), generator=g, device=dev)
+    y = torch.empty((Bsz, Dch), dtype=bf, device=dev)
+
+    def step():
+        ss.ss_decode_step(u, delta, A, Bm, Cm, D, z, bias, True, state, y=y)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    # state read + written, u / delta / z read and y written (bf16), B / C, A, D, bias
+    nbytes = 2 * Bsz * Dch * N * 4 + 4 * Bsz * Dch * 2 + 2 * Bsz * N * 2 + Dch * N * 4 + 2 * Dch * 4
+    ach = nbytes / (ms / 1e3) / 1e9
+    return {"workload": f"mamba2.8b-layer-decode-bf16 (Bsz={Bsz}, Dch={Dch}, N={N}, state {Bsz * Dch * N * 4 >> 20} MiB)",
+            "ms_per_token": round(ms, 5), "tokens_per_s": round(Bsz / (ms / 1e3), 1),
+            "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
+                         "frac": round(ach / hbm_peak, 4), "peak_kind": f"{peak_kind} HBM copy",
+                         "algorithmic_bytes": nbytes}}
+
+
 def run_ours(args):
     import torch
 
@@ -352,8 +397,10 @@ def run_ours(args):
         "clocks": clk,
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps},
-        "gpu_launches": K * (plan["fwd_kernels"] + plan["bwd_saved_kernels"]),
+        "gpu_launches": K * (plan["fwd_kernels"] + plan["bwd_saved_kernels"]),  # the timed region only
     }
+    if not args.no_decode:
+        line["decode"] = measure_decode(dev, hbm_peak, peak_kind)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, x, budget_s=args.cpu_seconds)
     if rank == 0:
@@ -447,6 +494,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true", help="skip the single-step decoding measurement")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.impl == "reference":

@@ -7,10 +7,11 @@
 //   y = (sum_n h[n] * C[n] + D * u) * silu(z)
 //
 // The step reads and rewrites the whole [Bsz, Dch, N] state, so it is bound
-// by HBM: a thread owns S consecutive states of one channel (16-byte vectors
-// of the state and of A), G = N / S adjacent threads share a channel and
-// combine their readouts with shuffles, and a warp covers a contiguous run of
-// the state.
+// by HBM: a thread owns S (up to 16) consecutive states of one channel, moved
+// as 16-byte vectors, G = N / S adjacent threads share a channel and combine
+// their readouts with shuffles, and a warp covers a contiguous run of the
+// state.  The state is touched once per step: its loads and stores are
+// streaming (evict-first) accesses.
 #include "common.cuh"
 #include "kernels.h"
 #include "simd.cuh"
@@ -20,7 +21,7 @@ namespace ss {
 
 template <int N>
 struct DCfg {
-    static constexpr int S = N >= 4 ? 4 : N;  // states per thread
+    static constexpr int S = N >= 16 ? 16 : N;  // states per thread
     static constexpr int G = N / S;           // threads per channel
 };
 
@@ -57,17 +58,32 @@ __global__ void __launch_bounds__(256) k_decode(DecodeArgs a) {
     float x = ld_io(delta, row);
     if (a.delta_bias) x += a.delta_bias[d];
     const float dl = a.softplus ? softplus_fast(x) : x;
-    float h[S], Av[S];
-    if constexpr (S == 4) {
-        const float4 hv = *reinterpret_cast<const float4*>(a.state + row * N + n0);
-        const float4 av = __ldg(reinterpret_cast<const float4*>(a.A + d * N + n0));
-        h[0] = hv.x; h[1] = hv.y; h[2] = hv.z; h[3] = hv.w;
-        Av[0] = av.x; Av[1] = av.y; Av[2] = av.z; Av[3] = av.w;
+    float h[S], Av[S], Bv[S], Cv[S];
+    if constexpr (S % 4 == 0) {
+#pragma unroll
+        for (int q = 0; q < S; q += 4) {
+            const float4 hv = __ldcs(reinterpret_cast<const float4*>(a.state + row * N + n0 + q));
+            const float4 av = __ldg(reinterpret_cast<const float4*>(a.A + d * N + n0 + q));
+            h[q] = hv.x; h[q + 1] = hv.y; h[q + 2] = hv.z; h[q + 3] = hv.w;
+            Av[q] = av.x; Av[q + 1] = av.y; Av[q + 2] = av.z; Av[q + 3] = av.w;
+        }
+        // B and C values of the thread's states: S io elements each, naturally aligned
+        constexpr int BW = S * (int)sizeof(T) / 4;
+        uint32_t wb[BW], wc[BW];
+        load_words<S * (int)sizeof(T), BW>(Bm + b * N + n0, wb);
+        load_words<S * (int)sizeof(T), BW>(Cm + b * N + n0, wc);
+#pragma unroll
+        for (int s = 0; s < S; s++) {
+            Bv[s] = elem<T>(wb, s);
+            Cv[s] = elem<T>(wc, s);
+        }
     } else {
 #pragma unroll
         for (int s = 0; s < S; s++) {
             h[s] = a.state[row * N + n0 + s];
             Av[s] = __ldg(a.A + d * N + n0 + s);
+            Bv[s] = ld_io(Bm, b * N + n0 + s);
+            Cv[s] = ld_io(Cm, b * N + n0 + s);
         }
     }
     float yp = 0.f;
@@ -75,15 +91,17 @@ __global__ void __launch_bounds__(256) k_decode(DecodeArgs a) {
     for (int s = 0; s < S; s++) {
         const float A = a.a_is_log ? -expf(Av[s]) : Av[s];
         const float dA = ex2a(dl * A * kLog2eF);
-        h[s] = fmaf(dA, h[s], dl * ld_io(Bm, b * N + n0 + s) * uu);
-        yp = fmaf(ld_io(Cm, b * N + n0 + s), h[s], yp);
+        h[s] = fmaf(dA, h[s], dl * Bv[s] * uu);
+        yp = fmaf(Cv[s], h[s], yp);
     }
     // readout summed over the G threads of the channel, in a fixed order
 #pragma unroll
     for (int m = 1; m < G; m <<= 1) yp += __shfl_xor_sync(kFull, yp, m);
     if (!live) return;
-    if constexpr (S == 4) {
-        *reinterpret_cast<float4*>(a.state + row * N + n0) = make_float4(h[0], h[1], h[2], h[3]);
+    if constexpr (S % 4 == 0) {
+#pragma unroll
+        for (int q = 0; q < S; q += 4)
+            __stcs(reinterpret_cast<float4*>(a.state + row * N + n0 + q), make_float4(h[q], h[q + 1], h[q + 2], h[q + 3]));
     } else {
 #pragma unroll
         for (int s = 0; s < S; s++) a.state[row * N + n0 + s] = h[s];
