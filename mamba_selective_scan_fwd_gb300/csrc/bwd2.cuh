@@ -502,12 +502,9 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                 float hv[kSub][2][S], av[kSub][2][S];
                 {
                     float hh[2][S];
+                    // (the saved state of a channel past Dch is zero: the forward keeps it so)
 #pragma unroll
-                    for (int e = 0; e < 2; e++) {
-                        ld_state<S>(hsrc + e * S, hh[e]);
-#pragma unroll
-                        for (int s = 0; s < S; s++) hh[e][s] = ok[e] ? hh[e][s] : 0.f;
-                    }
+                    for (int e = 0; e < 2; e++) ld_state<S>(hsrc + e * S, hh[e]);
 #pragma unroll
                     for (int i = 0; i < kSub; i++) {
                         const int r = sub * kSub + i;
@@ -562,8 +559,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                                 if (i > 0) {
                                     hprev = make_float2(hv[i - 1][e][s], hv[i - 1][e][s + 1]);
                                 } else {
-                                    hprev = ok[e] ? *reinterpret_cast<const float2*>(hsrc + e * S + s)
-                                                  : make_float2(0.f, 0.f);
+                                    hprev = *reinterpret_cast<const float2*>(hsrc + e * S + s);
                                 }
                                 const float2 lam = fma2(g2e, Cp, make_float2(carry[e][s], carry[e][s + 1]));
                                 dup = fma2(lam, make_float2(Bv[s], Bv[s + 1]), dup);
@@ -592,7 +588,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                         for (int e = 0; e < 2; e++) {
                             const float ge = e ? g2.y : g2.x, dle = e ? du.z : du.x, dlue = e ? du.w : du.y;
                             const float hprev =
-                                i > 0 ? hv[i - 1][e][0] : (ok[e] ? hsrc[e * S] : 0.f);
+                                i > 0 ? hv[i - 1][e][0] : hsrc[e * S];
                             const float lam = fmaf(ge, Cv[0], carry[e][0]);
                             sumB[e] = lam * Bv[0];
                             const float cn = av[i][e][0] * lam;
@@ -662,11 +658,20 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                             vz[4] = {z4.x, z4.y, z4.z, z4.w};
                 float vdu[GRP], vdx[GRP], vdz[GRP];
 #pragma unroll
+                for (int c = 0; c < GRP; c += 2) {
+                    // two channels at a time with packed arithmetic
+                    const float2 Dv = make_float2(sDv[cg + c], sDv[cg + c + 1]);
+                    const float2 su2 = make_float2(vsu[c], vsu[c + 1]), u2 = make_float2(vu[c], vu[c + 1]);
+                    const float2 du2 = fma2(make_float2(vg[c], vg[c + 1]), Dv, mul2(make_float2(vdl[c], vdl[c + 1]), su2));
+                    const float2 dx2 = mul2(fma2(u2, su2, mul2(make_float2(vsd[c], vsd[c + 1]), splat2(kLn2))),
+                                            make_float2(vs[c], vs[c + 1]));
+                    const float2 dz2 = mul2(make_float2(vz[c], vz[c + 1]), fma2(Dv, u2, make_float2(vsy[c], vsy[c + 1])));
+                    vdu[c] = du2.x; vdu[c + 1] = du2.y;
+                    vdx[c] = dx2.x; vdx[c + 1] = dx2.y;
+                    vdz[c] = dz2.x; vdz[c + 1] = dz2.y;
+                }
+#pragma unroll
                 for (int c = 0; c < GRP; c++) {
-                    const float Dv = sDv[cg + c];
-                    vdu[c] = fmaf(vg[c], Dv, vdl[c] * vsu[c]);
-                    vdx[c] = fmaf(vu[c], vsu[c], vsd[c] * kLn2) * vs[c];
-                    vdz[c] = vz[c] * fmaf(Dv, vu[c], vsy[c]);
                     sAcc[0][it * GRP + c][tid] = fmaf(vg[c], vu[c], sAcc[0][it * GRP + c][tid]);  // g = u = 0 past t_end
                     sAcc[1][it * GRP + c][tid] += tv ? vdx[c] : 0.f;
                 }

@@ -139,8 +139,9 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(F
     float A2[2][S], h[2][S], P[2][S];
 #pragma unroll
     for (int s = 0; s < S; s++) {
-        A2[0][s] = scan_A(a, dA0 * N + n0 + s) * kLog2eF;
-        A2[1][s] = scan_A(a, dA1 * N + n0 + s) * kLog2eF;
+        // channels past Dch run with a zero exponent: their state stays exactly zero
+        A2[0][s] = ok0 ? scan_A(a, dA0 * N + n0 + s) * kLog2eF : 0.f;
+        A2[1][s] = ok1 ? scan_A(a, dA1 * N + n0 + s) * kLog2eF : 0.f;
         h[0][s] = from_h0 && ok0 ? a.h0[row0 * N + n0 + s] : 0.f;
         h[1][s] = from_h0 && ok1 ? a.h0[row1 * N + n0 + s] : 0.f;
         P[0][s] = P[1][s] = 1.f;
@@ -155,6 +156,13 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(F
                 h[0][s] = fmaf(q0.x, h[0][s], q0.y);
                 h[1][s] = fmaf(q1.x, h[1][s], q1.y);
             }
+        }
+        // channels past Dch (read a clamped channel's summaries) keep a zero state,
+        // so that every saved slot of theirs holds zero
+#pragma unroll
+        for (int s = 0; s < S; s++) {
+            h[0][s] = ok0 ? h[0][s] : 0.f;
+            h[1][s] = ok1 ? h[1][s] : 0.f;
         }
     }
 
