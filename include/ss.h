@@ -111,7 +111,8 @@ int ss_fwd_noalloc(const void *u, const void *delta, const float *A, const void 
  * backward's first pass); here the forward keeps one state in four steps.
  *   saved         device buffer of at least ss_saved_bytes(...) bytes, 16-byte
  *                 aligned, fully overwritten (f32 h of every (b, d) row at
- *                 every 4th step of each time chunk); opaque to the caller.
+ *                 every 4th step of L rounded up to 32 steps); opaque to the
+ *                 caller.
  * All other arguments and results are those of ss_fwd.  A NULL or short
  * `saved` gives SS_ERR_WORKSPACE_TOO_SMALL before anything is launched.
  */
@@ -166,13 +167,30 @@ int ss_bwd_saved(const void *u, const void *delta, const float *A, const void *B
                  size_t workspace_bytes, void *stream);
 
 /*
- * Launch plan for these sizes: the number of time chunks the sequence is cut
- * into and how many kernels each call enqueues (0 for an empty problem):
+ * Launch plan for these sizes: the largest number of time chunks a sequence
+ * is cut into (ss_plan_segments gives the whole split) and how many kernels
+ * each call enqueues (0 for an empty problem):
  * ss_fwd and ss_fwd_save (fwd_kernels), ss_bwd (bwd_kernels), ss_bwd_saved
  * (bwd_saved_kernels).  Pointers may be NULL.  Returns a status.
  */
 int ss_plan_info(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype, int64_t *chunks, int *fwd_kernels,
                  int *bwd_kernels, int *bwd_saved_kernels);
+
+/*
+ * How the launch plan splits the work.  A unit is one (batch row, tile of
+ * 32 channels; 64 for N = 1); units are numbered b * ceil(Dch / tile) + tile
+ * and grouped into *nseg (0 for an empty problem, else 1 or 2) consecutive
+ * segments: segment i holds units[i] units, each cut into chunks[i] time
+ * chunks, and every scan kernel launch covers one segment.  A second segment
+ * appears when the units fill the GPU but leave a last partial round of
+ * blocks over its 152 SMs: those units are cut in time so that every SM gets
+ * an equal share.  The kernels of each call run in this order: the summary
+ * passes of the chunked segments, then each segment's main pass (segment 0
+ * first), then, in the backward, the two reductions.  units and chunks point
+ * at 2 entries each (or NULL); nseg may be NULL.  Returns a status.
+ */
+int ss_plan_segments(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype, int *nseg, int64_t *units,
+                     int64_t *chunks);
 
 /*
  * Measurement aid (not thread-safe; for benchmarks).  After a call with
@@ -291,8 +309,9 @@ int ss_decode_step(const void *u, const void *delta, const float *A, const void 
 const char *ss_status_string(int status);
 
 /* ABI version (2: ss_fwd_save / ss_bwd_saved added, ss_plan_info gained
- * bwd_saved_kernels; 3: ss_fwd_ex / ss_bwd_ex / ss_decode_step added); bumped on any
- * incompatible change. */
+ * bwd_saved_kernels; 3: ss_fwd_ex / ss_bwd_ex / ss_decode_step added; 4:
+ * ss_plan_segments added, the saved-state buffer sized by L rounded up to 32
+ * steps); bumped on any incompatible change. */
 int ss_abi_version(void);
 
 #ifdef __cplusplus

@@ -23,8 +23,8 @@ STATUS_NAMES = {0: "SS_OK", 1: "SS_ERR_INVALID_PROBLEM", 2: "SS_ERR_UNSUPPORTED"
 EXPORTS = ["ss_fwd", "ss_bwd", "ss_fwd_workspace_bytes", "ss_bwd_workspace_bytes", "ss_plan_info",
            "ss_status_string", "ss_abi_version", "ss_fwd_noalloc", "ss_saved_bytes", "ss_fwd_save",
            "ss_bwd_saved_workspace_bytes", "ss_bwd_saved", "ss_profile_events", "ss_fwd_ex", "ss_bwd_ex",
-           "ss_decode_step"]
-ABI_VERSION = 3
+           "ss_decode_step", "ss_plan_segments"]
+ABI_VERSION = 4
 
 # Size of the library-owned scratch behind ss_fwd_noalloc (SS_FWD_NOALLOC_MAX_SCRATCH_BYTES).
 FWD_NOALLOC_MAX_SCRATCH_BYTES = 2 << 20
@@ -85,6 +85,8 @@ def lib() -> ctypes.CDLL:
         getattr(L, fn).argtypes = [_I64] * 4 + [ctypes.c_int]
     L.ss_plan_info.restype = ctypes.c_int
     L.ss_plan_info.argtypes = [_I64] * 4 + [ctypes.c_int, _P, _P, _P, _P]
+    L.ss_plan_segments.restype = ctypes.c_int
+    L.ss_plan_segments.argtypes = [_I64] * 4 + [ctypes.c_int, _P, _P, _P]
     L.ss_profile_events.restype = ctypes.c_int
     L.ss_profile_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
     L.ss_status_string.restype = ctypes.c_char_p
@@ -164,14 +166,19 @@ def bwd_saved_workspace_bytes(Bsz, L, Dch, N, dtype) -> int:
 
 
 def plan_info(Bsz, L, Dch, N, dtype) -> dict:
-    """Chunk count and kernels per call that the entry points use for these sizes."""
+    """Launch plan of these sizes: the largest chunk count, kernels per call, and the
+    segments as (units, chunks) pairs (kernel order: summary passes, then each segment's main pass)."""
     k = ctypes.c_int64()
     nf = ctypes.c_int()
     nb = ctypes.c_int()
     ns = ctypes.c_int()
     _check("ss_plan_info", lib().ss_plan_info(Bsz, L, Dch, N, dtype, ctypes.byref(k), ctypes.byref(nf),
                                               ctypes.byref(nb), ctypes.byref(ns)))
-    return {"chunks": k.value, "fwd_kernels": nf.value, "bwd_kernels": nb.value, "bwd_saved_kernels": ns.value}
+    ns2 = ctypes.c_int(0)
+    units, chunks = (ctypes.c_int64 * 2)(), (ctypes.c_int64 * 2)()
+    _check("ss_plan_segments", lib().ss_plan_segments(Bsz, L, Dch, N, dtype, ctypes.byref(ns2), units, chunks))
+    return {"chunks": k.value, "fwd_kernels": nf.value, "bwd_kernels": nb.value, "bwd_saved_kernels": ns.value,
+            "segments": [(units[i], chunks[i]) for i in range(ns2.value)]}
 
 
 def profile_events(events):

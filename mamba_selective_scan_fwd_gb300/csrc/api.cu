@@ -62,7 +62,7 @@ int fwd_impl(const void* u, const void* delta, const float* A, const void* B, co
         return SS_OK;
     }
     const FPlan p = make_fplan(Bsz, L, Dch, N);
-    if (ceil_div(Dch, 4) * Bsz * p.K >= (1ll << 31)) return SS_ERR_UNSUPPORTED;
+    if (ceil_div(Dch, 4) * Bsz * p.Kmax >= (1ll << 31)) return SS_ERR_UNSUPPORTED;
     if (save) {
         const size_t need_s = ckpt_bytes(p, Bsz, Dch, N);
         if (saved == nullptr || saved_bytes < need_s) return SS_ERR_WORKSPACE_TOO_SMALL;
@@ -79,6 +79,7 @@ int fwd_impl(const void* u, const void* delta, const float* A, const void* B, co
     a.a_is_log = a_is_log ? 1 : 0;
     a.dtype = dtype;
     a.ws_fsum = static_cast<float*>(workspace);
+    a.ws_fsd = workspace ? reinterpret_cast<float*>(static_cast<char*>(workspace) + fsum_offset_sd(p, N)) : nullptr;
     float* ck = save ? static_cast<float*>(saved) : nullptr;
     return launch_fwd2(a, p, st, kModeY, ck) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
@@ -132,7 +133,7 @@ int bwd_impl(const void* u, const void* delta, const float* A, const void* B, co
         return SS_OK;
     }
     const FPlan p = make_fplan(Bsz, L, Dch, N);
-    if (ceil_div(Dch, 4) * Bsz * p.K >= (1ll << 31)) return SS_ERR_UNSUPPORTED;
+    if (ceil_div(Dch, 4) * Bsz * p.Kmax >= (1ll << 31)) return SS_ERR_UNSUPPORTED;
     if (from_saved && (saved == nullptr || saved_bytes < ckpt_bytes(p, Bsz, Dch, N)))
         return SS_ERR_WORKSPACE_TOO_SMALL;
     const BwdLayout w = bwd_layout2(p, Bsz, L, Dch, N, from_saved);
@@ -148,12 +149,14 @@ int bwd_impl(const void* u, const void* delta, const float* A, const void* B, co
     a.f.a_is_log = a_is_log ? 1 : 0;
     a.f.dtype = dtype;
     a.f.ws_fsum = reinterpret_cast<float*>(ws + w.fsum);
+    a.f.ws_fsd = reinterpret_cast<float*>(ws + w.fsd);
     a.dy = dy;
     a.dlast = dlast;
     a.du = du; a.ddelta = ddelta; a.dA = dA; a.dB = dB; a.dC = dC; a.dD = dD; a.dz = dz;
     a.ddelta_bias = ddelta_bias;
     a.dh0 = dh0;
     a.ws_rsum = reinterpret_cast<float*>(ws + w.rsum);
+    a.ws_rsd = reinterpret_cast<float*>(ws + w.rsd);
     float* ckpt_out = from_saved ? nullptr : reinterpret_cast<float*>(ws + w.ckpt);
     a.ws_ckpt = from_saved ? static_cast<const float*>(saved) : ckpt_out;
     a.ws_bc = reinterpret_cast<float*>(ws + w.bc);
@@ -190,7 +193,7 @@ int ss_profile_events(void* const* events, int count) {
     return SS_OK;
 }
 
-int ss_abi_version(void) { return 3; }
+int ss_abi_version(void) { return 4; }
 
 const char* ss_status_string(int status) {
     switch (status) {
@@ -206,9 +209,7 @@ const char* ss_status_string(int status) {
 size_t ss_fwd_workspace_bytes(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype) {
     if (check_sizes(Bsz, L, Dch, N, dtype) != SS_OK) return 0;
     if (Bsz == 0 || L == 0 || Dch == 0) return 0;
-    const FPlan p = make_fplan(Bsz, L, Dch, N);
-    if (p.K <= 1) return 0;
-    return align_up((size_t)Bsz * Dch * p.K * N * 2 * sizeof(float), 256);
+    return fsum_bytes(make_fplan(Bsz, L, Dch, N), N);
 }
 
 size_t ss_bwd_workspace_bytes(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype) {
@@ -237,14 +238,33 @@ int ss_plan_info(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype, int6
     if (rc != SS_OK) return rc;
     const bool empty = Bsz == 0 || L == 0 || Dch == 0;
     const FPlan fp = make_fplan(Bsz, L, Dch, N);
-    const int chunked = fp.K > 1 ? 1 : 0;
-    if (chunks) *chunks = empty ? 0 : fp.K;
-    // forward (with or without saving): [summary if K > 1] + main;
-    // backward: [forward summary if K > 1] + checkpoints + [reverse summary if K > 1] + main + 2 reductions;
-    // backward from saved states: [reverse summary if K > 1] + main + 2 reductions
-    if (fwd_kernels) *fwd_kernels = empty ? 0 : 1 + chunked;
-    if (bwd_kernels) *bwd_kernels = empty ? 0 : 4 + 2 * chunked;
-    if (bwd_saved_kernels) *bwd_saved_kernels = empty ? 0 : 3 + chunked;
+    if (chunks) *chunks = empty ? 0 : fp.Kmax;
+    // per segment: [a summary pass if it is chunked] + its main pass; the forward
+    // (with or without saving) runs the forward passes, the backward from saved
+    // states the reverse ones and 2 reductions, the backward the forward
+    // checkpoint passes first
+    int scans = 0;
+    for (int i = 0; i < fp.nseg; i++) scans += 1 + (fp.seg[i].K > 1 ? 1 : 0);
+    if (fwd_kernels) *fwd_kernels = empty ? 0 : scans;
+    if (bwd_kernels) *bwd_kernels = empty ? 0 : 2 * scans + 2;
+    if (bwd_saved_kernels) *bwd_saved_kernels = empty ? 0 : scans + 2;
+    return SS_OK;
+}
+
+int ss_plan_segments(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype, int* nseg, int64_t* units,
+                     int64_t* chunks) {
+    int rc = check_sizes(Bsz, L, Dch, N, dtype);
+    if (rc != SS_OK) return rc;
+    if (Bsz == 0 || L == 0 || Dch == 0) {
+        if (nseg) *nseg = 0;
+        return SS_OK;
+    }
+    const FPlan fp = make_fplan(Bsz, L, Dch, N);
+    if (nseg) *nseg = fp.nseg;
+    for (int i = 0; i < fp.nseg; i++) {
+        if (units) units[i] = fp.seg[i].nu;
+        if (chunks) chunks[i] = fp.seg[i].K;
+    }
     return SS_OK;
 }
 

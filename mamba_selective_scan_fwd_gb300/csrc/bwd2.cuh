@@ -31,11 +31,11 @@
 //     kernel adds the per-tile dB / dC partials, a third the per-(batch,
 //     chunk) dA / dD / ddelta_bias partials.  Every sum has a fixed order:
 //     the result is bit-reproducible.
-// Chunks (only when batch x channels cannot fill the GPU): each chunk's
-// carry-in state is its first saved state; reverse summaries (P_k, M_k) --
-// the chunk's decay product and M_k = a_{s_k} lam_{s_k} with lam from a zero
-// incoming carry -- combine as rho_{k-1} = M_k + P_k rho_k into each chunk's
-// carry-in adjoint.
+// Chunks (units the plan cuts in time, kernels.h): each chunk's carry-in
+// state is its first saved state; reverse summaries (P_k, M_k) -- the chunk's
+// decay product, from its sum of delta_eff as exp(A sum delta_eff), and
+// M_k = a_{s_k} lam_{s_k} with lam from a zero incoming carry -- combine as
+// rho_{k-1} = M_k + P_k rho_k into each chunk's carry-in adjoint.
 #pragma once
 
 #include "common.cuh"
@@ -208,8 +208,8 @@ __device__ __forceinline__ void store_run(float* p, const float (&v)[CPL], int64
 constexpr int kRevMain = 0, kRevSummary = 1;
 
 template <typename T, int N, int MODE, bool STATE>
-__global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(BwdArgs a, FPlan p, int64_t k_lo,
-                                                                               int64_t k_hi) {
+__global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(BwdArgs a, FPlan p, int si,
+                                                                               int64_t k_lo) {
     using C = BCfg<T, N>;
     constexpr bool MAIN = MODE == kRevMain;
     constexpr int NW = C::NW, NPW = C::NPW, S = C::S, G = C::G, PAIRS = C::PAIRS, CH = C::CH,
@@ -244,12 +244,14 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
 
     const FwdArgs& f = a.f;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    int64_t blk = blockIdx.x;
-    const int64_t tile = blk % p.tiles_b;
-    blk /= p.tiles_b;
-    const int64_t nk = k_hi - k_lo;
-    const int64_t k = k_lo + blk % nk;
-    const int64_t b = blk / nk;
+    // block -> (unit, chunk) of segment si; unit -> (batch row, channel tile)
+    const Seg sgm = seg_at(p, si);
+    const int64_t ul = (int64_t)blockIdx.x % sgm.nu;
+    const int64_t k = k_lo + (int64_t)blockIdx.x / sgm.nu;
+    const int64_t unit = sgm.u_lo + ul;
+    const int64_t tile = unit % p.tiles_b, b = unit / p.tiles_b;
+    const int64_t q_first = sgm.q0 + ul * sgm.K;  // part of the unit's chunk 0
+    const int64_t s_first = sgm.s0 + ul * sgm.K;  // its summary index
     const int64_t L = f.L, Dch = f.Dch;
     const int64_t d0 = tile * CH;
     const T* u = static_cast<const T*>(f.u);
@@ -283,7 +285,8 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
     // The adjoint carry into the end of the sequence is the incoming gradient of
     // last_state (zero without one); a reverse summary starts from zero.
     const bool from_dlast = MAIN && STATE && a.dlast != nullptr;
-    float A2[2][S], carry[2][S], dA[2][S], Pr[2][MAIN ? 1 : S];
+    float A2[2][S], carry[2][S], dA[2][S];
+    float sd[2] = {0.f, 0.f};  // reverse summary: the chunk's sums of delta_eff
 #pragma unroll
     for (int e = 0; e < 2; e++) {
 #pragma unroll
@@ -291,22 +294,21 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
             A2[e][s] = ok[e] ? scan_A(f, dd[e] * N + n0 + s) * kLog2eF : 0.f;
             carry[e][s] = from_dlast && ok[e] ? a.dlast[row[e] * N + n0 + s] : 0.f;
             dA[e][s] = 0.f;
-            if (!MAIN) Pr[e][s] = 1.f;
         }
     }
-    if (MAIN && k + 1 < p.K) {
+    if (MAIN && k + 1 < sgm.K) {
         // carry into the end of chunk k: rho_{j-1} = M_j + P_j rho_j from the
-        // reverse summaries (P_j, M_j) of chunks K-1 .. k+1, with rho_{K-1} the
-        // carry into the end of the sequence
+        // reverse summaries of the unit's chunks K-1 .. k+1 (P_j = exp2(A2 *
+        // sum of delta_eff over chunk j)), with rho_{K-1} the carry into the end
+        // of the sequence
 #pragma unroll
         for (int e = 0; e < 2; e++) {
-            const float2* rs = reinterpret_cast<const float2*>(a.ws_rsum) + row[e] * p.K * N + n0;
-            for (int64_t j = p.K - 1; j > k; j--) {
+            for (int64_t j = sgm.K - 1; j > k; j--) {
+                const int64_t q = s_first + j;
+                const float* M = a.ws_rsum + (q * CH + c0 + e) * N + n0;
+                const float sdj = a.ws_rsd[q * CH + c0 + e];
 #pragma unroll
-                for (int s = 0; s < S; s++) {
-                    const float2 pm = rs[j * N + s];
-                    carry[e][s] = fmaf(pm.x, carry[e][s], pm.y);
-                }
+                for (int s = 0; s < S; s++) carry[e][s] = fmaf(ex2a(A2[e][s] * sdj), carry[e][s], M[s]);
             }
 #pragma unroll
             for (int s = 0; s < S; s++) carry[e][s] = ok[e] ? carry[e][s] : 0.f;
@@ -319,13 +321,13 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
 
     const bool pfast = ((Dch * (int64_t)sizeof(T)) % 16 == 0) && (d0 + CH <= Dch);
     const bool ofast = (Dch % 4 == 0) && (d0 + CH <= Dch);
-    const int64_t t_begin = k * p.Lc;
-    const int64_t t_end = t_begin + p.Lc < L ? t_begin + p.Lc : L;
+    const int64_t t_begin = k * sgm.Lc;
+    const int64_t t_end = t_begin + sgm.Lc < L ? t_begin + sgm.Lc : L;
     const int64_t ntile = (t_end - t_begin + kTT - 1) / kTT;
     // saved states (layout of ckpt_bytes): one block of CH x N floats per
     // (sub-chunk slot, batch, channel tile), the lane's slots in lane order
     const int64_t ck_stride = f.Bsz * p.tiles_b * CH * N;
-    const float* ck_blk = a.ws_ckpt + (k * (p.Lc / kSub)) * ck_stride + (b * p.tiles_b + tile) * (CH * N);
+    const float* ck_blk = a.ws_ckpt + (t_begin / kSub) * ck_stride + (b * p.tiles_b + tile) * (CH * N);
     const float* ck0 = ck_blk + ckpt_slot(w, 0, lane, S);
     const float* ck1 = ck_blk + ckpt_slot(w, 1, lane, S);
     float* bc0 = a.ws_bc + ((int64_t)tile * f.Bsz + b) * L * N;                  // dB partials of this tile
@@ -475,6 +477,8 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                 if (t0 + i >= t_end) continue;
                 const float4 du = sDU[i][pslot];
                 const float2 g2 = sG[i][pslot];
+                sd[0] += du.x;
+                sd[1] += du.z;
                 float Bv[S], Cv[S];
                 ld_bc_f32<S>(&sBC[C::BC_DIRECT ? buf : 0][i][sg * 2 * S], Bv, Cv);
 #pragma unroll
@@ -484,7 +488,6 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                         const float lam = fmaf(e ? g2.y : g2.x, Cv[s], carry[e][s]);
                         const float da = ex2a((e ? du.z : du.x) * A2[e][s]);
                         carry[e][s] = da * lam;
-                        Pr[e][s] *= da;
                     }
                 }
             }
@@ -686,20 +689,22 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
         __syncthreads();  // the next prologue restages the tile
     }
 
+    const int64_t q = q_first + k;  // this block's part
     if constexpr (!MAIN) {
+        // every entry of the summary is written (channels past Dch: zero carry)
+        const int64_t qs = s_first + k;
 #pragma unroll
         for (int e = 0; e < 2; e++) {
-            if (ok[e]) {
-                float2* out = reinterpret_cast<float2*>(a.ws_rsum) + (row[e] * p.K + k) * N + n0;
+            float* M = a.ws_rsum + (qs * CH + c0 + e) * N + n0;
 #pragma unroll
-                for (int s = 0; s < S; s++) out[s] = make_float2(Pr[e][s], carry[e][s]);
-            }
+            for (int s = 0; s < S; s++) M[s] = carry[e][s];
         }
+        if (w == 0 && g == 0) *reinterpret_cast<float2*>(a.ws_rsd + qs * CH + c0) = make_float2(sd[0], sd[1]);
     } else {
 #pragma unroll
         for (int e = 0; e < 2; e++) {
             if (ok[e]) {
-                float* o = a.ws_dA + ((b * p.K + k) * Dch + dd[e]) * N + n0;
+                float* o = a.ws_dA + (q * CH + c0 + e) * N + n0;
 #pragma unroll
                 for (int s = 0; s < S; s++) o[s] = dA[e][s];
                 // after the walk of the first chunk the carry is a_0 lam_0, the gradient of h0
@@ -713,17 +718,17 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
         // (one per step of the tile) added in step order
         for (int cc = tid; cc < CH; cc += THREADS) {
             if (d0 + cc < Dch) {
-                const int q = cc / GRP, c = cc % GRP;
+                const int qg = cc / GRP, c = cc % GRP;
                 float aD = 0.f, ab = 0.f;
 #pragma unroll
                 for (int r = 0; r < kTT; r++) {
-                    const int id = r * NGRP + q;
+                    const int id = r * NGRP + qg;
                     const int th = id % THREADS, itr = id / THREADS;
                     aD += sAcc[0][itr * GRP + c][th];
                     ab += sAcc[1][itr * GRP + c][th];
                 }
-                a.ws_dD[(b * p.K + k) * Dch + d0 + cc] = aD;
-                a.ws_db[(b * p.K + k) * Dch + d0 + cc] = ab;
+                a.ws_dD[q * CH + cc] = aD;
+                a.ws_db[q * CH + cc] = ab;
             }
         }
     }
@@ -737,12 +742,14 @@ cudaError_t launch_bwd2_t(const BwdArgs& a, const FPlan& p, cudaStream_t st, flo
         if (e != cudaSuccess) return e;
     }
     constexpr int threads = BCfg<T, N>::THREADS;
-    if (p.K > 1) {
-        const int64_t blocks = p.tiles_b * a.f.Bsz * (p.K - 1);
-        prof_mark(st);
-        k_bwd2<T, N, kRevSummary, false><<<(unsigned)blocks, threads, 0, st>>>(a, p, 1, p.K);
+    // reverse summaries of every chunked segment (chunks 1 .. K-1)
+    for (int si = 0; si < p.nseg; si++) {
+        const int64_t K = p.seg[si].K;
+        if (K > 1) {
+            prof_mark(st);
+            k_bwd2<T, N, kRevSummary, false><<<(unsigned)(p.seg[si].nu * (K - 1)), threads, 0, st>>>(a, p, si, 1);
+        }
     }
-    const int64_t blocks = p.tiles_b * a.f.Bsz * p.K;
     const bool state = a.dlast != nullptr || a.dh0 != nullptr;
     auto main_kernel = state ? k_bwd2<T, N, kRevMain, true> : k_bwd2<T, N, kRevMain, false>;
     // prefer the largest shared-memory carveout so that shared memory does not cap
@@ -756,8 +763,10 @@ cudaError_t launch_bwd2_t(const BwdArgs& a, const FPlan& p, cudaStream_t st, flo
         if (e != cudaSuccess) return e;
         carveout_set[state] = true;
     }
-    prof_mark(st);
-    main_kernel<<<(unsigned)blocks, threads, 0, st>>>(a, p, 0, p.K);
+    for (int si = 0; si < p.nseg; si++) {
+        prof_mark(st);
+        main_kernel<<<(unsigned)(p.seg[si].nu * p.seg[si].K), threads, 0, st>>>(a, p, si, 0);
+    }
     return cudaGetLastError();
 }
 

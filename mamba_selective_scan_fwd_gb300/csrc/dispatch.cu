@@ -77,28 +77,32 @@ __global__ void k_bwd2_reduce_bc(BwdArgs a, FPlan p) {
     }
 }
 
-// dA / dD / ddelta_bias: sum over (batch, chunk) partials in ascending order.
+// dA / dD / ddelta_bias: sum over the parts of each channel -- batch rows
+// ascending, and within a row the chunks of its unit ascending.
 __global__ void k_bwd2_reduce_params(BwdArgs a, FPlan p) {
-    const int64_t Dch = a.f.Dch, N = a.f.N;
+    const int64_t Dch = a.f.Dch, N = a.f.N, CH = channels_per_block(N);
     const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t parts = a.f.Bsz * p.K;
-    if (e < Dch * N) {
-        float acc = 0.f;
-        for (int64_t q = 0; q < parts; q++) acc += a.ws_dA[q * Dch * N + e];
-        // A_log form: dA_log = dA * A with A = -exp(A_log)
-        a.dA[e] = a.f.a_is_log ? acc * scan_A(a.f, e) : acc;
+    if (e >= Dch * N) return;
+    const int64_t d = e / N, n = e % N;
+    const int64_t tile = d / CH, c = d % CH;
+    float acc = 0.f, accD = 0.f, accb = 0.f;
+    for (int64_t b = 0; b < a.f.Bsz; b++) {
+        const int64_t unit = b * p.tiles_b + tile;
+        const Seg sg = seg_of(p, unit);
+        const int64_t q0 = sg.q0 + (unit - sg.u_lo) * sg.K;
+        for (int64_t k = 0; k < sg.K; k++) {
+            acc += a.ws_dA[((q0 + k) * CH + c) * N + n];
+            if (n == 0) {
+                accD += a.ws_dD[(q0 + k) * CH + c];
+                accb += a.ws_db[(q0 + k) * CH + c];
+            }
+        }
     }
-    if (e < Dch) {
-        if (a.dD) {
-            float acc = 0.f;
-            for (int64_t q = 0; q < parts; q++) acc += a.ws_dD[q * Dch + e];
-            a.dD[e] = acc;
-        }
-        if (a.ddelta_bias) {
-            float acc = 0.f;
-            for (int64_t q = 0; q < parts; q++) acc += a.ws_db[q * Dch + e];
-            a.ddelta_bias[e] = acc;
-        }
+    // A_log form: dA_log = dA * A with A = -exp(A_log)
+    a.dA[e] = a.f.a_is_log ? acc * scan_A(a.f, e) : acc;
+    if (n == 0) {
+        if (a.dD) a.dD[d] = accD;
+        if (a.ddelta_bias) a.ddelta_bias[d] = accb;
     }
 }
 

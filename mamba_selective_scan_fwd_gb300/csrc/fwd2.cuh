@@ -24,9 +24,11 @@
 //   epilogue  threads take (step, 8-channel group) items again: add the
 //             warps' partial readouts, D * u, apply the gate and store the
 //             group's run of y.
-// The time axis is cut into K chunks only when batch x channels cannot fill
-// the GPU; a chunk summary (P, H) = (product of a, end state from zero) then
-// gives the carry-in state of the chunks after it.
+// The time axis of a unit (batch row, channel tile) is cut into K chunks when
+// the plan says so (kernels.h); a chunk summary -- its end state H from a zero
+// start and its sum of delta_eff, which gives the product of its decays
+// P = exp(A sum delta_eff) -- then yields the carry-in state of the chunks
+// after it: h <- P h + H.
 #pragma once
 
 #include "common.cuh"
@@ -79,8 +81,8 @@ __device__ __forceinline__ int pair_slot(int pp) {
 }
 
 template <typename T, int N, int MODE>
-__global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(FwdArgs a, FPlan p, int64_t ntiles, int64_t k_lo,
-                                                               int64_t k_hi, float* ckpt) {
+__global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(FwdArgs a, FPlan p, int si, int64_t k_lo,
+                                                               float* ckpt) {
     constexpr bool SUMMARY = MODE == kModeSummary;
     constexpr bool NOY = MODE == kModeSummary || MODE == kModeCkpt;  // no readout, gate or y
     constexpr bool SAVE = MODE == kModeYSave || MODE == kModeCkpt;   // store the sub-chunk start states
@@ -103,12 +105,14 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(F
     __shared__ float sBias[CH], sDv[CH];
 
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    int64_t blk = blockIdx.x;
-    const int64_t tile = blk % ntiles;
-    blk /= ntiles;
-    const int64_t nk = k_hi - k_lo;
-    const int64_t k = k_lo + blk % nk;
-    const int64_t b = blk / nk;
+    // block -> (unit, chunk) of segment si; unit -> (batch row, channel tile)
+    const Seg sgm = seg_at(p, si);
+    const int64_t ul = (int64_t)blockIdx.x % sgm.nu;
+    const int64_t k = k_lo + (int64_t)blockIdx.x / sgm.nu;
+    const int64_t unit = sgm.u_lo + ul;
+    const int64_t ntiles = p.tiles_b;
+    const int64_t tile = unit % ntiles, b = unit / ntiles;
+    const int64_t s_first = sgm.s0 + ul * sgm.K;  // summary index of the unit's chunk 0
     const int64_t L = a.L, Dch = a.Dch;
     const int64_t d0 = tile * CH;
     const bool fast = ((Dch * (int64_t)sizeof(T)) % 16 == 0) && (d0 + CH <= Dch);
@@ -136,7 +140,8 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(F
     const int64_t row0 = b * Dch + dA0, row1 = b * Dch + dA1;
     // the state starts at h0 (zero without one); a chunk summary starts from zero
     const bool from_h0 = !SUMMARY && a.h0 != nullptr;
-    float A2[2][S], h[2][S], P[2][S];
+    float A2[2][S], h[2][S];
+    float sd0 = 0.f, sd1 = 0.f;  // summary: the chunk's sums of delta_eff
 #pragma unroll
     for (int s = 0; s < S; s++) {
         // channels past Dch run with a zero exponent: their state stays exactly zero
@@ -144,17 +149,18 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(F
         A2[1][s] = ok1 ? scan_A(a, dA1 * N + n0 + s) * kLog2eF : 0.f;
         h[0][s] = from_h0 && ok0 ? a.h0[row0 * N + n0 + s] : 0.f;
         h[1][s] = from_h0 && ok1 ? a.h0[row1 * N + n0 + s] : 0.f;
-        P[0][s] = P[1][s] = 1.f;
     }
     if (!SUMMARY && k > 0) {
-        const float2* sm0 = reinterpret_cast<const float2*>(a.ws_fsum) + row0 * p.K * N + n0;
-        const float2* sm1 = reinterpret_cast<const float2*>(a.ws_fsum) + row1 * p.K * N + n0;
+        // carry-in: h <- P_j h + H_j over the unit's chunks j < k, with
+        // P_j = exp2(A2 * sum of delta_eff over chunk j)
         for (int64_t j = 0; j < k; j++) {
+            const int64_t q = s_first + j;
+            const float* H0 = a.ws_fsum + (q * CH + c0) * N + n0;
+            const float sdj0 = a.ws_fsd[q * CH + c0], sdj1 = a.ws_fsd[q * CH + c0 + 1];
 #pragma unroll
             for (int s = 0; s < S; s++) {
-                const float2 q0 = sm0[j * N + s], q1 = sm1[j * N + s];
-                h[0][s] = fmaf(q0.x, h[0][s], q0.y);
-                h[1][s] = fmaf(q1.x, h[1][s], q1.y);
+                h[0][s] = fmaf(ex2a(A2[0][s] * sdj0), h[0][s], H0[s]);
+                h[1][s] = fmaf(ex2a(A2[1][s] * sdj1), h[1][s], H0[N + s]);
             }
         }
         // channels past Dch (read a clamped channel's summaries) keep a zero state,
@@ -166,12 +172,12 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(F
         }
     }
 
-    const int64_t t_begin = k * p.Lc;
-    const int64_t t_end = t_begin + p.Lc < L ? t_begin + p.Lc : L;
+    const int64_t t_begin = k * sgm.Lc;
+    const int64_t t_end = t_begin + sgm.Lc < L ? t_begin + sgm.Lc : L;
     // saved states (layout of ckpt_bytes): one block of CH x N floats per
-    // (sub-chunk slot, batch, channel tile), the lane's slots in lane order
+    // (sub-chunk slot t / kSub, batch, channel tile), the lane's slots in lane order
     const int64_t ck_stride = a.Bsz * ntiles * CH * N;
-    float* ck_blk = SAVE ? ckpt + (k * (p.Lc / kSub)) * ck_stride + (b * ntiles + tile) * (CH * N) : nullptr;
+    float* ck_blk = SAVE ? ckpt + (t_begin / kSub) * ck_stride + (b * ntiles + tile) * (CH * N) : nullptr;
     float* ck0 = SAVE ? ck_blk + ckpt_slot(w, 0, lane, S) : nullptr;
     float* ck1 = SAVE ? ck_blk + ckpt_slot(w, 1, lane, S) : nullptr;
 
@@ -294,6 +300,10 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(F
                 }
             }
             const float4 du = sDU[i][pslot];
+            if (SUMMARY) {
+                sd0 += du.x;  // delta_eff of steps past t_end is zero
+                sd1 += du.z;
+            }
             float Bv[S], Cv[S];
             ld_bc_f32<S>(&sBC[C::BC_DIRECT ? buf : 0][i][sg * 2 * S], Bv, Cv);
             float yp[2];
@@ -310,13 +320,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(F
                         const float2 hh = fma2(da, make_float2(h[e][s], h[e][s + 1]), x);
                         h[e][s] = hh.x;
                         h[e][s + 1] = hh.y;
-                        if (SUMMARY) {
-                            const float2 pq = mul2(make_float2(P[e][s], P[e][s + 1]), da);
-                            P[e][s] = pq.x;
-                            P[e][s + 1] = pq.y;
-                        } else if (!NOY) {
-                            ya[e] = fma2(make_float2(Cv[s], Cv[s + 1]), hh, ya[e]);
-                        }
+                        if (!NOY) ya[e] = fma2(make_float2(Cv[s], Cv[s + 1]), hh, ya[e]);
                     }
                 }
                 yp[0] = ya[0].x + ya[0].y;
@@ -326,7 +330,6 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(F
                 for (int e = 0; e < 2; e++) {
                     const float da = ex2a((e ? du.z : du.x) * A2[e][0]);
                     h[e][0] = fmaf(da, h[e][0], (e ? du.w : du.y) * Bv[0]);
-                    if (SUMMARY) P[e][0] *= da;
                     yp[e] = Cv[0] * h[e][0];
                 }
             }
@@ -393,29 +396,17 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(F
         // again only after the next prologue's barrier
     }
 
-    if (SAVE) {
-        // sub-chunk slots past the last tile (short last chunk only): the state
-        // no longer changes there, so they hold the final state and the whole
-        // buffer is written
-        const int64_t nsub = p.Lc / kSub;
-        const int64_t tiles_len = ((t_end - t_begin + kRow - 1) / kRow) * kRow;
-        for (int64_t jj = tiles_len / kSub; jj < nsub; jj++) {
-#pragma unroll
-            for (int s = 0; s < S; s++) {
-                ck0[jj * ck_stride + s] = h[0][s];
-                ck1[jj * ck_stride + s] = h[1][s];
-            }
-        }
-    }
-
     if (SUMMARY) {
-        float2* out = reinterpret_cast<float2*>(a.ws_fsum);
+        // every entry of the part is written (channels past Dch: zero state)
+        const int64_t q = s_first + k;
+        float* H0 = a.ws_fsum + (q * CH + c0) * N + n0;
 #pragma unroll
         for (int s = 0; s < S; s++) {
-            if (ok0) out[(row0 * p.K + k) * N + n0 + s] = make_float2(P[0][s], h[0][s]);
-            if (ok1) out[(row1 * p.K + k) * N + n0 + s] = make_float2(P[1][s], h[1][s]);
+            H0[s] = h[0][s];
+            H0[N + s] = h[1][s];
         }
-    } else if (MODE != kModeCkpt && k == p.K - 1 && a.last_state) {
+        if (w == 0 && g == 0) *reinterpret_cast<float2*>(a.ws_fsd + q * CH + c0) = make_float2(sd0, sd1);
+    } else if (MODE != kModeCkpt && k == sgm.K - 1 && a.last_state) {
 #pragma unroll
         for (int s = 0; s < S; s++) {
             if (ok0) a.last_state[row0 * N + n0 + s] = h[0][s];
@@ -424,28 +415,29 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(F
     }
 }
 
-template <typename T, int N>
-int64_t fwd_tiles(int64_t Dch) {
-    return ceil_div(Dch, FCfg<T, N>::CH);
-}
-
+// One launch of mode MODE over chunks k_lo .. k_hi of segment si.
 template <typename T, int N, int MODE>
-void launch_fwd_mode(const FwdArgs& a, const FPlan& p, cudaStream_t st, int64_t k_lo, int64_t k_hi, float* ckpt) {
-    const int64_t nt = fwd_tiles<T, N>(a.Dch);
+void launch_fwd_mode(const FwdArgs& a, const FPlan& p, int si, cudaStream_t st, int64_t k_lo, int64_t k_hi,
+                     float* ckpt) {
     prof_mark(st);
-    k_fwd2<T, N, MODE><<<(unsigned)(nt * a.Bsz * (k_hi - k_lo)), FCfg<T, N>::THREADS, 0, st>>>(a, p, nt, k_lo,
-                                                                                                 k_hi, ckpt);
+    k_fwd2<T, N, MODE><<<(unsigned)(p.seg[si].nu * (k_hi - k_lo)), FCfg<T, N>::THREADS, 0, st>>>(a, p, si, k_lo,
+                                                                                                ckpt);
 }
 
+// The chunk summaries of every chunked segment, then each segment's main pass.
 template <typename T, int N>
 cudaError_t launch_fwd2_t(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt) {
-    if (p.K > 1) launch_fwd_mode<T, N, kModeSummary>(a, p, st, 0, p.K - 1, nullptr);
-    if (mode == kModeCkpt) {
-        launch_fwd_mode<T, N, kModeCkpt>(a, p, st, 0, p.K, ckpt);
-    } else if (ckpt) {
-        launch_fwd_mode<T, N, kModeYSave>(a, p, st, 0, p.K, ckpt);
-    } else {
-        launch_fwd_mode<T, N, kModeY>(a, p, st, 0, p.K, nullptr);
+    for (int si = 0; si < p.nseg; si++)
+        if (p.seg[si].K > 1) launch_fwd_mode<T, N, kModeSummary>(a, p, si, st, 0, p.seg[si].K - 1, nullptr);
+    for (int si = 0; si < p.nseg; si++) {
+        const int64_t K = p.seg[si].K;
+        if (mode == kModeCkpt) {
+            launch_fwd_mode<T, N, kModeCkpt>(a, p, si, st, 0, K, ckpt);
+        } else if (ckpt) {
+            launch_fwd_mode<T, N, kModeYSave>(a, p, si, st, 0, K, ckpt);
+        } else {
+            launch_fwd_mode<T, N, kModeY>(a, p, si, st, 0, K, nullptr);
+        }
     }
     return cudaGetLastError();
 }

@@ -17,8 +17,11 @@ struct FwdArgs {
     int64_t Bsz, L, Dch, N;
     int softplus;
     int a_is_log;     // A holds A_log: the scan uses A = -exp(A_log)
-    int dtype;        // 0 f32, 2 bf16
-    float* ws_fsum;   // chunk summaries (P, H): [Bsz*Dch][K][N] float2
+    int dtype;        // 0 f32, 1 f16, 2 bf16
+    // chunk summaries, per summary index (layout of FPlan): the end state from
+    // a zero start [.][CH][N] and the chunk's sum of delta_eff [.][CH]
+    float* ws_fsum;
+    float* ws_fsd;
 };
 
 // A[d, n] of the scan: the input itself, or -exp(A_log) in the A_log form.
@@ -33,12 +36,15 @@ struct BwdArgs {
     const float* dlast;  // incoming gradient of last_state [Bsz][Dch][N], or null (zero)
     float *du, *ddelta, *dA, *dB, *dC, *dD, *dz, *ddelta_bias;
     float* dh0;          // gradient of the initial state [Bsz][Dch][N], or null
-    float* ws_rsum;   // reverse chunk summaries (P, M): [Bsz*Dch][K][N] float2
-    const float* ws_ckpt;  // sub-chunk start states, step-major: [K * Lc/kSub][Bsz*Dch][N]
+    // reverse chunk summaries per summary index: the carry a chunk passes back
+    // from a zero incoming adjoint [.][CH][N] and the chunk's sum of delta_eff [.][CH]
+    float* ws_rsum;
+    float* ws_rsd;
+    const float* ws_ckpt;  // sub-chunk start states (layout of ckpt_bytes)
     float* ws_bc;     // per-tile dB/dC partials: [2][tiles][Bsz][L][N]
-    float* ws_dA;     // per-(b,k) dA partials: [Bsz][K][Dch][N]
-    float* ws_dD;     // per-(b,k) dD partials: [Bsz][K][Dch]
-    float* ws_db;     // per-(b,k) ddelta_bias partials: [Bsz][K][Dch]
+    float* ws_dA;     // per-part dA partials: [q][CH][N]
+    float* ws_dD;     // per-part dD partials: [q][CH]
+    float* ws_db;     // per-part ddelta_bias partials: [q][CH]
 };
 
 // One decoding step in place on the state (ss_decode_step).
@@ -53,7 +59,7 @@ struct DecodeArgs {
 
 // Workspace layout of the backward (byte offsets, each 256-aligned).
 struct BwdLayout {
-    size_t fsum, rsum, ckpt, bc, dA, dD, db, total;
+    size_t fsum, fsd, rsum, rsd, ckpt, bc, dA, dD, db, total;
 };
 
 constexpr int kModeY = 0, kModeSummary = 1, kModeCkpt = 2, kModeYSave = 3;
@@ -68,35 +74,130 @@ constexpr int kModeY = 0, kModeSummary = 1, kModeCkpt = 2, kModeYSave = 3;
 __host__ __device__ constexpr int fwd_warps(int64_t N) { return N >= 16 ? 2 : 1; }
 __host__ __device__ constexpr int64_t channels_per_block(int64_t N) { return N >= 2 ? 32 : 64; }
 
-// Launch plan: one block per (batch, channel tile, time chunk).  The time
-// chunking (K, Lc) is shared by every kernel of a call.
+constexpr int kSub = 4;  // backward sub-chunk: steps whose states stay in registers (checkpoint interval)
+
+// Launch plan.  A unit is one (batch row, channel tile): unit u = b tiles_b +
+// tile.  Units are grouped into at most two segments; a segment cuts the time
+// axis of each of its units into K chunks of Lc steps (the last may be
+// shorter), and every kernel launch covers one segment, one block per (unit,
+// chunk).  Each (unit, chunk) is a part with an index q (segment order, then
+// unit, then chunk) that places its parameter-gradient partials; the parts
+// of chunked segments (K > 1) also have a summary index that places their
+// chunk summaries.
+struct Seg {
+    int64_t u_lo, nu;  // units u_lo .. u_lo + nu
+    int64_t K, Lc;     // chunks per unit and their length (a multiple of 32)
+    int64_t q0;        // part of (u_lo, chunk 0); part (u, k) = q0 + (u - u_lo) K + k
+    int64_t s0;        // summary index of (u_lo, chunk 0), likewise (K > 1 only)
+};
 struct FPlan {
-    int64_t tiles_b; // channel tiles (sizes the per-tile dB / dC partials)
-    int64_t K;       // time chunks
-    int64_t Lc;      // chunk length (multiple of 32); the last chunk may be shorter
+    int64_t tiles_b;   // channel tiles (sizes the per-tile dB / dC partials)
+    int64_t slots;     // saved-state slots per sequence: one per kSub steps of L rounded up to 32
+    int nseg;
+    Seg seg[2];
+    int64_t parts;     // parts over all segments
+    int64_t sparts;    // parts of the chunked segments (entries of the summary arrays)
+    int64_t Kmax;      // the largest K
 };
 
-constexpr int64_t kTargetWarps = 1216;  // 8 warps on each of 152 SMs
+constexpr int64_t kSMs = 152;                  // SMs of a GB300
+constexpr int64_t kTargetWarps = 8 * kSMs;     // 8 warps on every SM keep each one's pipes busy
 constexpr int64_t kFwdMinChunk = 128;
 
-// A pure function of the sizes (the same sizes always chunk the same way).
-inline FPlan make_fplan(int64_t Bsz, int64_t L, int64_t Dch, int64_t N) {
-    FPlan p;
-    p.tiles_b = ceil_div(Dch, channels_per_block(N));
-    const int64_t warps = Bsz * p.tiles_b * fwd_warps(N);
-    int64_t K = 1;
+// Bytes of chunk summaries (end state and sum of delta_eff per channel) that a
+// split of a plan that needs none may add: within the 2 MiB scratch of the
+// no-allocation forward, so that splitting never takes a problem out of it.
+constexpr int64_t kSplitSummaryMax = 2 << 20;
+
+// Chunking of nunits units that fills the GPU: K time chunks when nunits
+// blocks hold fewer than kTargetWarps warps (at most kcap).
+inline void chunking(int64_t nunits, int64_t L, int64_t N, int64_t& K, int64_t& Lc, int64_t kcap = 1ll << 40) {
+    const int64_t warps = nunits * fwd_warps(N);
+    K = 1;
     if (warps > 0 && warps < kTargetWarps) K = ceil_div(kTargetWarps, warps);
+    if (K > kcap) K = kcap;
     const int64_t kmax = ceil_div(L, kFwdMinChunk);
     if (K > kmax) K = kmax;
     if (K < 1) K = 1;
-    p.Lc = ceil_div(ceil_div(L, K), 32) * 32;
-    if (p.Lc < 32) p.Lc = 32;
-    p.K = ceil_div(L, p.Lc);
-    if (p.K < 1) p.K = 1;
+    Lc = ceil_div(ceil_div(L, K), 32) * 32;
+    if (Lc < 32) Lc = 32;
+    K = ceil_div(L, Lc);
+    if (K < 1) K = 1;
+}
+
+// A pure function of the sizes (the same sizes always plan the same way).
+// One segment chunked to fill the GPU; or, when the units already fill it, one
+// block per unit -- except that a grid of units blocks whose count is not a
+// multiple of the SM count leaves a last partial round: some SMs run one
+// block more than the others and the kernel waits for them (each SM's
+// throughput is the same with 8 or 10 warps resident).  Those last
+// units mod kSMs units then form a second segment cut in time, so that every
+// SM gets an equal share, when that costs less than the partial round (the
+// chunk summaries of the second segment take about 0.6 of a main pass).
+inline FPlan make_fplan(int64_t Bsz, int64_t L, int64_t Dch, int64_t N) {
+    FPlan p;
+    p.tiles_b = ceil_div(Dch, channels_per_block(N));
+    p.slots = ceil_div(L, 32) * (32 / kSub);
+    const int64_t units = Bsz * p.tiles_b;
+    p.nseg = 1;
+    p.seg[0].u_lo = 0;
+    p.seg[0].nu = units;
+    p.seg[0].q0 = 0;
+    p.seg[0].s0 = 0;
+    chunking(units, L, N, p.seg[0].K, p.seg[0].Lc);
+    p.seg[1] = p.seg[0];
+    const int64_t tail = units % kSMs, rounds = units / kSMs;
+    if (p.seg[0].K == 1 && tail > 0 && rounds > 0) {
+        int64_t Kt, Lct;
+        const int64_t kcap = kSplitSummaryMax / (tail * channels_per_block(N) * (N + 1) * 4);
+        chunking(tail, L, N, Kt, Lct, kcap);
+        if (Kt > 1) {
+            const double split = (double)ceil_div(tail * Kt, kSMs) / (double)Kt +
+                                 0.6 * (double)(tail * (Kt - 1)) / (double)(Kt * kSMs);
+            if (split < 0.95) {
+                p.nseg = 2;
+                p.seg[0].nu = units - tail;
+                p.seg[1].u_lo = units - tail;
+                p.seg[1].nu = tail;
+                p.seg[1].K = Kt;
+                p.seg[1].Lc = Lct;
+                p.seg[1].q0 = units - tail;
+            }
+        }
+    }
+    p.parts = 0;
+    p.sparts = 0;
+    p.Kmax = 1;
+    for (int i = 0; i < p.nseg; i++) {
+        p.seg[i].s0 = p.sparts;
+        p.parts += p.seg[i].nu * p.seg[i].K;
+        if (p.seg[i].K > 1) p.sparts += p.seg[i].nu * p.seg[i].K;
+        if (p.seg[i].K > p.Kmax) p.Kmax = p.seg[i].K;
+    }
     return p;
 }
 
-constexpr int kSub = 4;  // backward sub-chunk: steps whose states stay in registers (checkpoint interval)
+// Segment si of the plan, by value (selected field by field, so that a
+// kernel parameter is never indexed at run time).
+__host__ __device__ inline Seg seg_at(const FPlan& p, int si) {
+    Seg s;
+    s.u_lo = si ? p.seg[1].u_lo : p.seg[0].u_lo;
+    s.nu = si ? p.seg[1].nu : p.seg[0].nu;
+    s.K = si ? p.seg[1].K : p.seg[0].K;
+    s.Lc = si ? p.seg[1].Lc : p.seg[0].Lc;
+    s.q0 = si ? p.seg[1].q0 : p.seg[0].q0;
+    s.s0 = si ? p.seg[1].s0 : p.seg[0].s0;
+    return s;
+}
+
+// Segment holding unit u.
+__host__ __device__ inline Seg seg_of(const FPlan& p, int64_t u) {
+    return seg_at(p, (p.nseg > 1 && u >= p.seg[1].u_lo) ? 1 : 0);
+}
+
+// Whether any segment is cut into chunks (the chunk summaries are needed).
+inline bool plan_chunked(const FPlan& p) { return p.Kmax > 1; }
+
 
 // Measurement aid behind ss_profile_events: prof_mark records the next of
 // the caller's events on `st` (nothing when none are set); every launcher
@@ -120,13 +221,13 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
 
 // Bytes of the sub-chunk start states of every (b, d) row: the checkpoints the
 // backward recomputes from (ss_fwd_save writes them into the caller's buffer).
-// Layout: [k (Lc / kSub) + j][b][channel tile][block of CH x N floats]; within
+// Layout: [slot t / kSub][b][channel tile][block of CH x N floats]; within
 // a block, float ((w 2 + e) 32 + lane) S + s is state n0 + s of channel c0 + e
 // of the lane (the scan kernels' lane layout), so that a warp's stores and
 // loads of one channel parity are contiguous.
 inline size_t ckpt_bytes(const FPlan& p, int64_t Bsz, int64_t Dch, int64_t N) {
     (void)Dch;
-    return (size_t)Bsz * p.tiles_b * channels_per_block(N) * p.K * (p.Lc / kSub) * N * sizeof(float);
+    return (size_t)Bsz * p.tiles_b * channels_per_block(N) * p.slots * N * sizeof(float);
 }
 
 // Float offset of a lane's slot for channel parity e within a saved-state block.
@@ -134,26 +235,41 @@ __host__ __device__ constexpr int64_t ckpt_slot(int w, int e, int lane, int S) {
     return ((int64_t)(w * 2 + e) * 32 + lane) * S;
 }
 
+// Bytes of the forward chunk summaries (0 when nothing is chunked): end
+// states [sparts][CH][N], then the sums of delta_eff [sparts][CH] at the
+// 256-aligned offset fsum_offset_sd.
+inline size_t fsum_offset_sd(const FPlan& p, int64_t N) {
+    return align_up((size_t)p.sparts * channels_per_block(N) * N * sizeof(float), 256);
+}
+inline size_t fsum_bytes(const FPlan& p, int64_t N) {
+    if (!plan_chunked(p)) return 0;
+    return fsum_offset_sd(p, N) + align_up((size_t)p.sparts * channels_per_block(N) * sizeof(float), 256);
+}
+
 // Workspace of the backward (byte offsets, each 256-aligned): forward and
 // reverse chunk summaries (only when chunked), sub-chunk start states (unless
-// the forward saved them), per channel-tile dB / dC partials, per-(batch,
-// chunk) dA / dD / ddelta_bias partials.
+// the forward saved them), per channel-tile dB / dC partials, per-part
+// dA / dD / ddelta_bias partials.
 inline BwdLayout bwd_layout2(const FPlan& p, int64_t Bsz, int64_t L, int64_t Dch, int64_t N, bool saved) {
     BwdLayout w;
     size_t off = 0;
-    const size_t rows = (size_t)(Bsz * Dch);
+    const size_t pc = (size_t)p.parts * channels_per_block(N);    // partials
+    const size_t sc = (size_t)p.sparts * channels_per_block(N);   // summaries
     auto take = [&](size_t bytes) {
         size_t at = off;
         off = align_up(off + bytes, 256);
         return at;
     };
-    w.fsum = take(p.K > 1 && !saved ? rows * p.K * N * 2 * sizeof(float) : 0);
-    w.rsum = take(p.K > 1 ? rows * p.K * N * 2 * sizeof(float) : 0);
+    const bool ch = plan_chunked(p);
+    w.fsum = take(ch && !saved ? sc * N * sizeof(float) : 0);
+    w.fsd = take(ch && !saved ? sc * sizeof(float) : 0);
+    w.rsum = take(ch ? sc * N * sizeof(float) : 0);
+    w.rsd = take(ch ? sc * sizeof(float) : 0);
     w.ckpt = take(saved ? 0 : ckpt_bytes(p, Bsz, Dch, N));
     w.bc = take(2 * (size_t)p.tiles_b * Bsz * L * N * sizeof(float));
-    w.dA = take((size_t)Bsz * p.K * Dch * N * sizeof(float));
-    w.dD = take((size_t)Bsz * p.K * Dch * sizeof(float));
-    w.db = take((size_t)Bsz * p.K * Dch * sizeof(float));
+    w.dA = take(pc * N * sizeof(float));
+    w.dD = take(pc * sizeof(float));
+    w.db = take(pc * sizeof(float));
     w.total = off;
     return w;
 }

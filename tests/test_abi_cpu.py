@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol():
     lib = ss.lib()
     for name in declared_functions():
         assert hasattr(lib, name), name
-    assert lib.ss_abi_version() == binding.ABI_VERSION == 3
+    assert lib.ss_abi_version() == binding.ABI_VERSION == 4
 
 
 def test_status_strings():
@@ -49,7 +49,9 @@ def test_status_strings():
 def test_workspace_queries_are_pure_and_sized():
     a = ss.bwd_workspace_bytes(4, 4096, 5120, 16, ss.SS_BF16)
     assert a == ss.bwd_workspace_bytes(4, 4096, 5120, 16, ss.SS_BF16) > 0
-    assert ss.fwd_workspace_bytes(4, 4096, 5120, 16, ss.SS_BF16) == 0  # batch x channels fill the GPU: one chunk
+    assert ss.fwd_workspace_bytes(4, 4096, 4864, 16, ss.SS_BF16) == 0  # 4 whole rounds of units: one chunk each
+    # 640 units: the 32 past 4 whole rounds are cut in time and carry chunk summaries
+    assert 0 < ss.fwd_workspace_bytes(4, 4096, 5120, 16, ss.SS_BF16) <= 2 << 20
     assert ss.fwd_workspace_bytes(1, 131072, 1024, 16, ss.SS_BF16) > 0  # long sequence: chunk carries
     assert ss.fwd_workspace_bytes(1, 8, 8, 3, ss.SS_F32) == 0  # unsupported N
     assert ss.bwd_workspace_bytes(0, 8, 8, 4, ss.SS_F32) == 0
@@ -105,8 +107,10 @@ def test_fwd_save_rejects(kw, code):
 
 
 def test_saved_sizes():
-    # one f32 state of N per (b, d) row every 4 steps of each (32-step aligned) chunk
+    # one f32 state of N per (b, d) row every 4 steps of L rounded up to 32, however the plan cuts time
     assert ss.saved_bytes(4, 4096, 5120, 16, ss.SS_BF16) == 4 * 5120 * (4096 // 4) * 16 * 4
+    assert ss.saved_bytes(1, 131072, 1024, 16, ss.SS_BF16) == 1024 * (131072 // 4) * 16 * 4
+    assert ss.saved_bytes(1, 300, 3, 16, ss.SS_F32) == 32 * (320 // 4) * 16 * 4
     # channels are stored in whole tiles of 32 (8 channels take a tile): 2 x 32 x 8 slots x 4 states
     assert ss.saved_bytes(2, 16, 8, 4, ss.SS_F32) == 2 * 32 * (32 // 4) * 4 * 4
     assert ss.saved_bytes(0, 16, 8, 4, ss.SS_F32) == 0
@@ -118,11 +122,18 @@ def test_saved_sizes():
 
 
 def test_plan_info_counts():
+    # 640 units over 152 SMs: 608 one-chunk units, the last 32 cut into 19 chunks
     p = ss.plan_info(4, 4096, 5120, 16, ss.SS_BF16)
-    assert p == {"chunks": 1, "fwd_kernels": 1, "bwd_kernels": 4, "bwd_saved_kernels": 3}
+    assert p == {"chunks": 19, "fwd_kernels": 3, "bwd_kernels": 8, "bwd_saved_kernels": 5,
+                 "segments": [(608, 1), (32, 19)]}
+    # 608 units: a whole number of rounds, no split
+    p = ss.plan_info(4, 4096, 4864, 16, ss.SS_BF16)
+    assert p == {"chunks": 1, "fwd_kernels": 1, "bwd_kernels": 4, "bwd_saved_kernels": 3, "segments": [(608, 1)]}
     q = ss.plan_info(1, 131072, 1024, 16, ss.SS_BF16)
     assert q["chunks"] > 1 and q["fwd_kernels"] == 2 and q["bwd_kernels"] == 6 and q["bwd_saved_kernels"] == 4
-    assert ss.plan_info(0, 16, 8, 4, 0)["fwd_kernels"] == 0
+    assert q["segments"] == [(32, q["chunks"])]
+    e = ss.plan_info(0, 16, 8, 4, 0)
+    assert e["fwd_kernels"] == 0 and e["segments"] == []
 
 
 def test_fwd_workspace_too_small_reports_before_launch():

@@ -1,0 +1,56 @@
+"""Launch-plan properties (host logic, no GPU): how the units (batch row,
+channel tile) are grouped into segments and cut in time.
+
+* The segments cover every unit once, in order.
+* A split happens only when the units fill the GPU's 152 SMs at least once
+  and leave a partial round: the first segment is then a whole number of
+  rounds of one-chunk units, the second the remaining units cut in time.
+* A split never takes a problem out of the no-allocation forward: its chunk
+  summaries stay within that entry point's 2 MiB scratch.
+* The saved-state buffer does not depend on the split.
+"""
+
+import itertools
+
+import pytest
+
+import mamba_selective_scan_fwd_gb300 as ss
+from mamba_selective_scan_fwd_gb300 import binding
+
+SMS = 152
+
+
+def tile_of(N):
+    return 32 if N >= 2 else 64
+
+
+SHAPES = [(b, L, d, n) for b, L, d, n in itertools.product(
+    (1, 2, 4, 8), (1, 100, 256, 4096), (1, 130, 4864, 5120, 9913, 19488), (1, 4, 16, 32))]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=[f"B{s[0]}L{s[1]}D{s[2]}N{s[3]}" for s in SHAPES])
+def test_plan_segments(shape):
+    Bsz, L, Dch, N = shape
+    p = ss.plan_info(Bsz, L, Dch, N, ss.SS_BF16)
+    units = Bsz * -(-Dch // tile_of(N))
+    segs = p["segments"]
+    assert sum(u for u, _ in segs) == units
+    assert p["chunks"] == max(k for _, k in segs)
+    assert p["fwd_kernels"] == sum(1 + (k > 1) for _, k in segs)
+    assert p["bwd_saved_kernels"] == p["fwd_kernels"] + 2
+    assert p["bwd_kernels"] == 2 * p["fwd_kernels"] + 2
+    if len(segs) == 2:
+        (u0, k0), (u1, k1) = segs
+        assert k0 == 1 and u0 % SMS == 0 and u0 > 0 and 0 < u1 < SMS and k1 > 1
+        assert ss.fwd_workspace_bytes(Bsz, L, Dch, N, ss.SS_BF16) <= binding.FWD_NOALLOC_MAX_SCRATCH_BYTES
+    slots = -(-L // 32) * 8
+    assert ss.saved_bytes(Bsz, L, Dch, N, ss.SS_BF16) == units * tile_of(N) * slots * N * 4
+
+
+def test_split_appears_for_a_partial_round():
+    # 640 units = 4 rounds of 152 + 32: the 32 are cut in time
+    assert ss.plan_info(4, 4096, 5120, 16, ss.SS_BF16)["segments"] == [(608, 1), (32, 19)]
+    # 760 units = 5 whole rounds: no split
+    assert ss.plan_info(4, 4096, 6080, 16, ss.SS_BF16)["segments"] == [(760, 1)]
+    # a partial round of nearly 152 units (758 = 4 x 152 + 150): cutting them costs more than the round
+    assert ss.plan_info(2, 4096, 32 * 379, 16, ss.SS_BF16)["segments"] == [(758, 1)]
