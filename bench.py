@@ -51,10 +51,11 @@ def algorithmic_bytes(w):
     return fwd, bwd
 
 
-# DRAM bytes (read + write) per launch of the timed kernels on this workload,
-# from one ncu capture (profiles/ holds the summaries and the commands), and
-# the digest of the kernel sources they were taken on: a source change since
-# then makes the figure stale, and it is reported as null.
+# DRAM bytes (read + write) of the timed kernels' main passes on this workload
+# (the sum over the launches of one pass: one per plan segment), from one ncu
+# capture (profiles/ holds the summaries and the commands), and the digest of
+# the kernel sources they were taken on: a source change since then makes the
+# figure stale, and it is reported as null.
 TRAFFIC = {
     ("k_bwd2_main", "mamba2.8b-layer-bf16"): 3326893000,  # 2016.2 MB read + 1310.7 MB written
     ("k_fwd2_y", "mamba2.8b-layer-bf16"): 1958770000,     # 505.5 MB read + 1453.3 MB written
@@ -368,17 +369,25 @@ def run_ours(args):
                 "peak_kind": f"MUFU ex2: {sms} SMs x {EX2_PER_CLK_PER_SM:g}/clk x {sm_mhz:g} MHz (median sampled)",
                 "roofline_ms": round(t_sfu * 1e3, 4), "algorithmic_bytes": bytes_}
 
-    chunked = plan["chunks"] > 1
-    fwd_names = (["k_fwd2 chunk summary"] if chunked else []) + ["k_fwd2 (y + saved states)"]
-    bwd_names = (["k_bwd2 reverse summary"] if chunked else []) + ["k_bwd2 main", "k_bwd2_reduce_bc",
-                                                                   "k_bwd2_reduce_params"]
-    i_main = 1 if chunked else 0
-    r_bwd = roof(bwd_main_bytes, k_bwd[i_main])
-    r_bwd.update({"kernel": "k_bwd2 main (ss_bwd_saved)", "ms": round(k_bwd[i_main], 4),
-                  "traffic": measured_traffic("k_bwd2_main", w)})
-    r_fwd = roof(fwd_bytes, k_fwd[-1])
-    r_fwd.update({"kernel": "k_fwd2 (ss_fwd_save)", "ms": round(k_fwd[-1], 4),
-                  "traffic": measured_traffic("k_fwd2_y", w)})
+    # launch order of a call: the summary passes of the chunked segments, then
+    # each segment's main pass (then, in the backward, the two reductions)
+    segs = plan["segments"]
+    seg_tag = [f"{u} units x {k} chunk{'s' if k > 1 else ''}" for u, k in segs]
+    fwd_names = ([f"k_fwd2 chunk summary ({seg_tag[i]})" for i, (_, k) in enumerate(segs) if k > 1] +
+                 [f"k_fwd2 y + saved states ({t})" for t in seg_tag])
+    bwd_names = ([f"k_bwd2 reverse summary ({seg_tag[i]})" for i, (_, k) in enumerate(segs) if k > 1] +
+                 [f"k_bwd2 main ({t})" for t in seg_tag] + ["k_bwd2_reduce_bc", "k_bwd2_reduce_params"])
+    n_sum = sum(1 for _, k in segs if k > 1)
+    main_f = range(n_sum, n_sum + len(segs))  # the forward's main pass: one launch per segment
+    main_b = range(n_sum, n_sum + len(segs))
+    t_main_f = sum(k_fwd[j] for j in main_f)
+    t_main_b = sum(k_bwd[j] for j in main_b)
+    r_bwd = roof(bwd_main_bytes, t_main_b)
+    r_bwd.update({"kernel": f"k_bwd2 main pass (ss_bwd_saved; {len(segs)} launch{'es' if len(segs) > 1 else ''})",
+                  "ms": round(t_main_b, 4), "traffic": measured_traffic("k_bwd2_main", w)})
+    r_fwd = roof(fwd_bytes, t_main_f)
+    r_fwd.update({"kernel": f"k_fwd2 main pass (ss_fwd_save; {len(segs)} launch{'es' if len(segs) > 1 else ''})",
+                  "ms": round(t_main_f, 4), "traffic": measured_traffic("k_fwd2_y", w)})
     t_roof = roof(fwd_bytes, t_fwd)["roofline_ms"] + roof(bwd_bytes, t_bwd)["roofline_ms"]
     kernel_ms = {n: round(v, 4) for n, v in zip(fwd_names + bwd_names, k_fwd + k_bwd)}
 

@@ -71,6 +71,9 @@ struct BCfg {
     static constexpr bool BC_DIRECT = ESZ == 4;
     static constexpr bool BC_RAW = !BC_DIRECT && N * ESZ >= 4;
     static constexpr int BC_BUFS = BC_DIRECT ? 2 : 1;
+    // raw row length (elements): rows of 32 bytes or more padded by 16 bytes, so
+    // that the 16-byte loads of consecutive rows fall in different bank groups
+    static constexpr int RAWP = NB >= 32 ? N + 16 / ESZ : N;
     static constexpr int EP = CH + 4;               // padded per-channel rows (floats)
     static constexpr int GP = PAIRS + 8;            // padded per-pair float2 rows
     // dB / dC staging of one warp: block (step slot j, tensor tau) holds PAIRS
@@ -222,7 +225,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
     // tile's rows being copied in while the current tile is walked
     __shared__ __align__(16) float sBC[C::BC_BUFS][kTT][BCF];
     // raw bf16 B / C rows of the next tile (converted into sBC by the prologue)
-    __shared__ __align__(16) T sBCraw[C::BC_RAW ? kTT : 1][2][C::BC_RAW ? N : 2];
+    __shared__ __align__(16) T sBCraw[2][C::BC_RAW ? kTT : 1][C::BC_RAW ? C::RAWP : 2];
     // raw runs of delta, u, dy, z of the next tile, copied in asynchronously by
     // the thread that later converts them
     __shared__ __align__(16) T sRaw[4][kTT][CH];
@@ -238,8 +241,10 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
     __shared__ __align__(16) float sOy[MAIN ? NW : 1][MAIN ? kTT : 1][MAIN ? EP : 4];
     // dD / ddelta_bias partials of each epilogue thread's items (thread fastest)
     __shared__ float sAcc[MAIN ? 2 : 1][MAIN ? ITEMS * GRP : 1][THREADS];
-    // restart states of a tile's sub-chunks, 2 S floats per lane, double buffered by tile
-    __shared__ __align__(16) float sH[MAIN ? 2 : 1][MAIN ? kTT / kSub : 1][MAIN ? THREADS * 2 * S : 4];
+    // restart states of a tile's sub-chunks, S floats per lane and channel
+    // parity (one plane per parity: a warp's loads are contiguous), double
+    // buffered by tile
+    __shared__ __align__(16) float sH[MAIN ? 2 : 1][MAIN ? kTT / kSub : 1][2][MAIN ? THREADS * S : 4];
     __shared__ float sBias[CH], sDv[CH];
 
     const FwdArgs& f = a.f;
@@ -365,7 +370,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
             if constexpr (C::BC_DIRECT) {
                 cp_async_bc_row<T, N, S>(reinterpret_cast<unsigned char*>(&sBC[buf][r][0]), half, src, t < t_end);
             } else if constexpr (C::BC_RAW) {
-                if (t < t_end) cp_async_bytes<N * C::ESZ>(&sBCraw[r][half][0], src);
+                if (t < t_end) cp_async_bytes<N * C::ESZ>(&sBCraw[half][r][0], src);
             }
         }
         if (MAIN) {
@@ -374,8 +379,8 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                 const int64_t ts = tt + sub * kSub;
                 if (ts < t_end) {
                     const int64_t j = (ts - t_begin) / kSub;
-                    cp_async_bytes<S * 4>(&sH[buf][sub][tid * 2 * S], ck0 + j * ck_stride);
-                    cp_async_bytes<S * 4>(&sH[buf][sub][tid * 2 * S + S], ck1 + j * ck_stride);
+                    cp_async_bytes<S * 4>(&sH[buf][sub][0][tid * S], ck0 + j * ck_stride);
+                    cp_async_bytes<S * 4>(&sH[buf][sub][1][tid * S], ck1 + j * ck_stride);
                 }
             }
         }
@@ -461,7 +466,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                 const int64_t t = t0 + r;
                 uint32_t wv[NWd];
                 if (t < t_end) {
-                    if constexpr (C::BC_RAW) lds_words<C::NB, NWd>(&sBCraw[r][half][0], wv);
+                    if constexpr (C::BC_RAW) lds_words<C::NB, NWd>(&sBCraw[half][r][0], wv);
                     else load_words<C::NB, NWd>((half ? Cm : Bm) + (b * L + t) * N, wv);
                 }
                 stage_bc_row_f32<T, N, S, NWd>(&sBC[0][r][0], half, wv, t < t_end);
@@ -500,14 +505,15 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
             for (int sub = kTT / kSub - 1; sub >= 0; sub--) {
                 const int64_t ts = t0 + sub * kSub;
                 if (ts >= t_end) continue;
-                const float* hsrc = &sH[buf][sub][tid * 2 * S];  // copied with the tile's rows
+                // the lane's restart states of channel parity e: hsrc[e], copied with the tile's rows
+                const float* hsrc[2] = {&sH[buf][sub][0][tid * S], &sH[buf][sub][1][tid * S]};
                 // recompute the states and decays of the sub-chunk
                 float hv[kSub][2][S], av[kSub][2][S];
                 {
                     float hh[2][S];
                     // (the saved state of a channel past Dch is zero: the forward keeps it so)
 #pragma unroll
-                    for (int e = 0; e < 2; e++) ld_state<S>(hsrc + e * S, hh[e]);
+                    for (int e = 0; e < 2; e++) ld_state<S>(hsrc[e], hh[e]);
 #pragma unroll
                     for (int i = 0; i < kSub; i++) {
                         const int r = sub * kSub + i;
@@ -562,7 +568,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                                 if (i > 0) {
                                     hprev = make_float2(hv[i - 1][e][s], hv[i - 1][e][s + 1]);
                                 } else {
-                                    hprev = *reinterpret_cast<const float2*>(hsrc + e * S + s);
+                                    hprev = *reinterpret_cast<const float2*>(hsrc[e] + s);
                                 }
                                 const float2 lam = fma2(g2e, Cp, make_float2(carry[e][s], carry[e][s + 1]));
                                 dup = fma2(lam, make_float2(Bv[s], Bv[s + 1]), dup);
@@ -591,7 +597,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                         for (int e = 0; e < 2; e++) {
                             const float ge = e ? g2.y : g2.x, dle = e ? du.z : du.x, dlue = e ? du.w : du.y;
                             const float hprev =
-                                i > 0 ? hv[i - 1][e][0] : hsrc[e * S];
+                                i > 0 ? hv[i - 1][e][0] : hsrc[e][0];
                             const float lam = fmaf(ge, Cv[0], carry[e][0]);
                             sumB[e] = lam * Bv[0];
                             const float cn = av[i][e][0] * lam;

@@ -65,6 +65,9 @@ struct FCfg {
     static constexpr bool BC_DIRECT = ESZ == 4;
     static constexpr bool BC_RAW = !BC_DIRECT && N * ESZ >= 4;
     static constexpr int BC_BUFS = BC_DIRECT ? 2 : 1;
+    // raw row length (elements): rows of 32 bytes or more padded by 16 bytes, so
+    // that the 16-byte loads of consecutive rows fall in different bank groups
+    static constexpr int RAWP = NB >= 32 ? N + 16 / ESZ : N;
     static constexpr int YP = CH + 4;               // padded shared row of partial readouts (floats)
     static_assert(kRow * NGRP % THREADS == 0, "whole items per thread");
     static_assert(CH == channels_per_block(N), "channel tile of the plan");
@@ -97,7 +100,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(F
     // tile's rows being copied in while the scan reads the current one's
     __shared__ __align__(16) float sBC[C::BC_BUFS][kRow][BCF];
     // raw bf16 B / C rows of the next tile (converted into sBC by the prologue)
-    __shared__ __align__(16) T sBCraw[C::BC_RAW ? kRow : 1][2][C::BC_RAW ? N : 2];
+    __shared__ __align__(16) T sBCraw[2][C::BC_RAW ? kRow : 1][C::BC_RAW ? C::RAWP : 2];
     // raw runs of delta, u, z of the next tile, copied in asynchronously by the
     // thread that later converts them
     __shared__ __align__(16) T sRaw[NOY ? 2 : 3][kRow][CH];
@@ -206,7 +209,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(F
             if constexpr (C::BC_DIRECT) {
                 cp_async_bc_row<T, N, S>(reinterpret_cast<unsigned char*>(&sBC[buf][r][0]), half, src, t < t_end);
             } else if constexpr (C::BC_RAW) {
-                if (t < t_end) cp_async_bytes<N * C::ESZ>(&sBCraw[r][half][0], src);
+                if (t < t_end) cp_async_bytes<N * C::ESZ>(&sBCraw[half][r][0], src);
             }
         }
         cp_async_commit();
@@ -268,7 +271,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), 12 / fwd_warps(N)) k_fwd2(F
                 const int64_t t = t0 + r;
                 uint32_t wv[NWd];
                 if (t < t_end) {
-                    if constexpr (C::BC_RAW) lds_words<C::NB, NWd>(&sBCraw[r][half][0], wv);
+                    if constexpr (C::BC_RAW) lds_words<C::NB, NWd>(&sBCraw[half][r][0], wv);
                     else load_words<C::NB, NWd>((half ? Cm : Bm) + (b * L + t) * N, wv);
                 }
                 stage_bc_row_f32<T, N, S, NWd>(&sBC[0][r][0], half, wv, t < t_end);
