@@ -183,8 +183,8 @@ int ss_plan_info(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype, int6
  * segments: segment i holds units[i] units, each cut into chunks[i] time
  * chunks, and every scan kernel launch covers one segment.  A second segment
  * appears when the units fill the GPU but leave a last partial round of
- * blocks over its 152 SMs: those units are cut in time so that every SM gets
- * an equal share.  The kernels of each call run in this order: the summary
+ * blocks (a round: 8 warps on each of its 152 SMs, 608 blocks for N >= 16):
+ * those units are cut in time so that every SM gets an equal share.  The kernels of each call run in this order: the summary
  * passes of the chunked segments, then each segment's main pass (segment 0
  * first), then, in the backward, the two reductions.  units and chunks point
  * at 2 entries each (or NULL); nseg may be NULL.  Returns a status.

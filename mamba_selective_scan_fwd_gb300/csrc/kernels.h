@@ -125,14 +125,20 @@ inline void chunking(int64_t nunits, int64_t L, int64_t N, int64_t& K, int64_t& 
     if (K < 1) K = 1;
 }
 
+// Blocks of one round: kTargetWarps warps, 8 on every SM.  The scan kernels of
+// two-warp blocks are built for 4 resident blocks per SM (their register
+// budget), those of one-warp blocks for 8 or more, so a round is also what
+// one wave of the GPU holds at that budget.
+inline int64_t round_blocks(int64_t N) { return kTargetWarps / fwd_warps(N); }
+
 // A pure function of the sizes (the same sizes always plan the same way).
 // One segment chunked to fill the GPU; or, when the units already fill it, one
-// block per unit -- except that a grid of units blocks whose count is not a
-// multiple of the SM count leaves a last partial round: some SMs run one
-// block more than the others and the kernel waits for them (each SM's
-// throughput is the same with 8 or 10 warps resident).  Those last
-// units mod kSMs units then form a second segment cut in time, so that every
-// SM gets an equal share, when that costs less than the partial round (the
+// block per unit -- except that a count of units that is not a whole number
+// of rounds leaves a last partial round: its blocks run as a wave of their
+// own on part of the GPU (each SM's throughput does not grow past 8 resident
+// warps, and falls below it).  Those last units mod round units then form a
+// second segment cut in time, so that every SM gets an equal share, when that
+// costs less than the partial round (estimated as at least half a round; the
 // chunk summaries of the second segment take about 0.6 of a main pass).
 inline FPlan make_fplan(int64_t Bsz, int64_t L, int64_t Dch, int64_t N) {
     FPlan p;
@@ -146,15 +152,18 @@ inline FPlan make_fplan(int64_t Bsz, int64_t L, int64_t Dch, int64_t N) {
     p.seg[0].s0 = 0;
     chunking(units, L, N, p.seg[0].K, p.seg[0].Lc);
     p.seg[1] = p.seg[0];
-    const int64_t tail = units % kSMs, rounds = units / kSMs;
+    const int64_t rb = round_blocks(N);
+    const int64_t tail = units % rb, rounds = units / rb;
     if (p.seg[0].K == 1 && tail > 0 && rounds > 0) {
         int64_t Kt, Lct;
         const int64_t kcap = kSplitSummaryMax / (tail * channels_per_block(N) * (N + 1) * 4);
         chunking(tail, L, N, Kt, Lct, kcap);
         if (Kt > 1) {
-            const double split = (double)ceil_div(tail * Kt, kSMs) / (double)Kt +
-                                 0.6 * (double)(tail * (Kt - 1)) / (double)(Kt * kSMs);
-            if (split < 0.95) {
+            // costs in rounds: the tail's chunks (whole rounds of them) and its summaries
+            const double split = (double)ceil_div(tail * Kt, rb) / (double)Kt +
+                                 0.6 * (double)(tail * (Kt - 1)) / (double)(Kt * rb);
+            const double partial = (double)tail / (double)rb > 0.5 ? (double)tail / (double)rb : 0.5;
+            if (split < partial) {
                 p.nseg = 2;
                 p.seg[0].nu = units - tail;
                 p.seg[1].u_lo = units - tail;

@@ -2,9 +2,10 @@
 channel tile) are grouped into segments and cut in time.
 
 * The segments cover every unit once, in order.
-* A split happens only when the units fill the GPU's 152 SMs at least once
-  and leave a partial round: the first segment is then a whole number of
-  rounds of one-chunk units, the second the remaining units cut in time.
+* A split happens only when the units fill at least one round (8 warps on
+  each of the GPU's 152 SMs: 608 two-warp blocks, 1216 one-warp blocks) and
+  leave a partial round: the first segment is then a whole number of rounds
+  of one-chunk units, the second the remaining units cut in time.
 * A split never takes a problem out of the no-allocation forward: its chunk
   summaries stay within that entry point's 2 MiB scratch.
 * The saved-state buffer does not depend on the split.
@@ -24,6 +25,10 @@ def tile_of(N):
     return 32 if N >= 2 else 64
 
 
+def round_of(N):
+    return 8 * SMS // (2 if N >= 16 else 1)
+
+
 SHAPES = [(b, L, d, n) for b, L, d, n in itertools.product(
     (1, 2, 4, 8), (1, 100, 256, 4096), (1, 130, 4864, 5120, 9913, 19488), (1, 4, 16, 32))]
 
@@ -41,7 +46,7 @@ def test_plan_segments(shape):
     assert p["bwd_kernels"] == 2 * p["fwd_kernels"] + 2
     if len(segs) == 2:
         (u0, k0), (u1, k1) = segs
-        assert k0 == 1 and u0 % SMS == 0 and u0 > 0 and 0 < u1 < SMS and k1 > 1
+        assert k0 == 1 and u0 % round_of(N) == 0 and u0 > 0 and 0 < u1 < round_of(N) and k1 > 1
         assert ss.fwd_workspace_bytes(Bsz, L, Dch, N, ss.SS_BF16) <= binding.FWD_NOALLOC_MAX_SCRATCH_BYTES
     slots = -(-L // 32) * 8
     assert ss.saved_bytes(Bsz, L, Dch, N, ss.SS_BF16) == units * tile_of(N) * slots * N * 4
@@ -50,7 +55,9 @@ def test_plan_segments(shape):
 def test_split_appears_for_a_partial_round():
     # 640 units = 4 rounds of 152 + 32: the 32 are cut in time
     assert ss.plan_info(4, 4096, 5120, 16, ss.SS_BF16)["segments"] == [(608, 1), (32, 19)]
-    # 760 units = 5 whole rounds: no split
-    assert ss.plan_info(4, 4096, 6080, 16, ss.SS_BF16)["segments"] == [(760, 1)]
-    # a partial round of nearly 152 units (758 = 4 x 152 + 150): cutting them costs more than the round
-    assert ss.plan_info(2, 4096, 32 * 379, 16, ss.SS_BF16)["segments"] == [(758, 1)]
+    # 1216 units = 2 whole rounds: no split
+    assert ss.plan_info(4, 4096, 32 * 304, 16, ss.SS_BF16)["segments"] == [(1216, 1)]
+    # 760 units = a round of 608 + 152: the 152 are cut into 4 chunks (one more round of blocks)
+    assert ss.plan_info(4, 4096, 6080, 16, ss.SS_BF16)["segments"] == [(608, 1), (152, 4)]
+    # 1064 = 608 + 456: cutting the 456 takes more than the partial round
+    assert ss.plan_info(1, 4096, 32 * 1064, 16, ss.SS_BF16)["segments"] == [(1064, 1)]
