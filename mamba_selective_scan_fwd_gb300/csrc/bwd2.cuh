@@ -76,6 +76,10 @@ struct BCfg {
     static constexpr int RAWP = NB >= 32 ? N + 16 / ESZ : N;
     static constexpr int EP = CH + 4;               // padded per-channel rows (floats)
     static constexpr int GP = PAIRS + 8;            // padded per-pair float2 rows
+    // plane of per-step channel sums of one lane of a pair: kTT rows of EP floats,
+    // planes 16 mod 32 floats apart so that the 8-byte stores of both lanes of
+    // the pairs of a half warp hit 32 banks
+    static constexpr int OPL = kTT * EP + 16;
     // dB / dC staging of one warp: block (step slot j, tensor tau) holds PAIRS
     // rows of NPW floats (the warp's states, summed over the pair's two
     // channels); blocks are padded by 8 floats so that the 16 lanes of a half
@@ -240,10 +244,12 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
     // dB / dC contributions of kRB steps, per warp: block (j, tau) holds a row of NPW floats per pair
     __shared__ __align__(16) float sR[MAIN ? NW : 1][MAIN ? kRB * 2 * BLK : 4];
     // per-step, per-warp sums over the warp's states: sum lam B, sum A q, y0 (channel fastest)
-    __shared__ __align__(16) float sOu[MAIN ? NW : 1][MAIN ? kTT : 1][MAIN ? EP : 4];
-    __shared__ __align__(16) float sOd[MAIN ? NW : 1][MAIN ? kTT : 1][MAIN ? EP : 4];
-    __shared__ __align__(16) float sOy[MAIN ? NW : 1][MAIN ? kTT : 1][MAIN ? EP : 4];
-    // dD / ddelta_bias partials of each epilogue thread's items (thread fastest)
+    // (one plane per lane of a pair: float g OPL + r EP + c is the sum over the
+    // states of lane g, for step r and channel c)
+    __shared__ __align__(16) float sOu[MAIN ? NW : 1][MAIN ? G * C::OPL : 4];
+    __shared__ __align__(16) float sOd[MAIN ? NW : 1][MAIN ? G * C::OPL : 4];
+    __shared__ __align__(16) float sOy[MAIN ? NW : 1][MAIN ? G * C::OPL : 4];
+    // dD / ddelta_bias partials of each epilogue thread's items at the end (thread fastest)
     __shared__ float sAcc[MAIN ? 2 : 1][MAIN ? ITEMS * GRP : 1][THREADS];
     // restart states of a tile's sub-chunks, S floats per lane and channel
     // parity (one plane per parity: a warp's loads are contiguous), double
@@ -323,10 +329,11 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
             for (int s = 0; s < S; s++) carry[e][s] = ok[e] ? carry[e][s] : 0.f;
         }
     }
-    if (MAIN) {
+    // dD / ddelta_bias partials of the thread's epilogue items (the same channels
+    // in every tile), added over the tiles in order; summed per channel at the end
+    float accD[ITEMS * GRP], accB[ITEMS * GRP];
 #pragma unroll
-        for (int c = 0; c < ITEMS * GRP; c++) { sAcc[0][c][tid] = 0.f; sAcc[1][c][tid] = 0.f; }
-    }
+    for (int c = 0; c < ITEMS * GRP; c++) accD[c] = accB[c] = 0.f;
 
     const bool pfast = ((Dch * (int64_t)sizeof(T)) % 16 == 0) && (d0 + CH <= Dch);
     const bool ofast = (Dch % 4 == 0) && (d0 + CH <= Dch);
@@ -391,7 +398,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
         cp_async_commit();
     };
     issue(ntile - 1);
-    __syncthreads();  // sBias / sDv / sAcc before the first prologue
+    __syncthreads();  // sBias / sDv before the first prologue
 
     for (int64_t m = ntile - 1; m >= 0; m--) {
         const int64_t t0 = t_begin + m * kTT;
@@ -614,19 +621,13 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                             carry[e][0] = cn;
                         }
                     }
-                    // sums over the warp's states: lane g of a pair keeps channel c0 + g
-                    // and adds the partner's partial sums of that channel
-                    if constexpr (G == 2) {
-                        const float xB = __shfl_xor_sync(kFull, g ? sumB[0] : sumB[1], 1);
-                        const float xQ = __shfl_xor_sync(kFull, g ? sumQ[0] : sumQ[1], 1);
-                        const float xY = __shfl_xor_sync(kFull, g ? y0[0] : y0[1], 1);
-                        sOu[w][r][lane] = (g ? sumB[1] : sumB[0]) + xB;
-                        sOd[w][r][lane] = (g ? sumQ[1] : sumQ[0]) + xQ;
-                        sOy[w][r][lane] = (g ? y0[1] : y0[0]) + xY;
-                    } else {
-                        *reinterpret_cast<float2*>(&sOu[w][r][c0]) = make_float2(sumB[0], sumB[1]);
-                        *reinterpret_cast<float2*>(&sOd[w][r][c0]) = make_float2(sumQ[0], sumQ[1]);
-                        *reinterpret_cast<float2*>(&sOy[w][r][c0]) = make_float2(y0[0], y0[1]);
+                    // the lane's sums over its states, both channels; the epilogue adds
+                    // the G lanes of the pair and the warps
+                    {
+                        const int o = g * C::OPL + r * EP + c0;
+                        *reinterpret_cast<float2*>(&sOu[w][o]) = make_float2(sumB[0], sumB[1]);
+                        *reinterpret_cast<float2*>(&sOd[w][o]) = make_float2(sumQ[0], sumQ[1]);
+                        *reinterpret_cast<float2*>(&sOy[w][o]) = make_float2(y0[0], y0[1]);
                     }
                     // stage dB / dC contributions (summed over the pairs below)
                     stage_contrib<S, NPW, BLK>(sRw, i, cB, cC, pp, g * S);
@@ -647,17 +648,29 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                 const int cg = q * GRP;
                 const int64_t t = t0 + r;
                 const bool tv = t < t_end;
-                float4 su = *reinterpret_cast<const float4*>(&sOu[0][r][cg]);
-                float4 sd = *reinterpret_cast<const float4*>(&sOd[0][r][cg]);
-                float4 sy = *reinterpret_cast<const float4*>(&sOy[0][r][cg]);
+                // per warp, the sum of its G lanes' planes; then the warps in order
+                float4 su, sd, sy;
 #pragma unroll
-                for (int ww = 1; ww < NW; ww++) {
-                    const float4 ou = *reinterpret_cast<const float4*>(&sOu[ww][r][cg]);
-                    const float4 od = *reinterpret_cast<const float4*>(&sOd[ww][r][cg]);
-                    const float4 oy = *reinterpret_cast<const float4*>(&sOy[ww][r][cg]);
-                    su.x += ou.x; su.y += ou.y; su.z += ou.z; su.w += ou.w;
-                    sd.x += od.x; sd.y += od.y; sd.z += od.z; sd.w += od.w;
-                    sy.x += oy.x; sy.y += oy.y; sy.z += oy.z; sy.w += oy.w;
+                for (int ww = 0; ww < NW; ww++) {
+                    const int o = r * EP + cg;
+                    float4 ou = *reinterpret_cast<const float4*>(&sOu[ww][o]);
+                    float4 od = *reinterpret_cast<const float4*>(&sOd[ww][o]);
+                    float4 oy = *reinterpret_cast<const float4*>(&sOy[ww][o]);
+                    if constexpr (G == 2) {
+                        const float4 pu = *reinterpret_cast<const float4*>(&sOu[ww][C::OPL + o]);
+                        const float4 pd = *reinterpret_cast<const float4*>(&sOd[ww][C::OPL + o]);
+                        const float4 py = *reinterpret_cast<const float4*>(&sOy[ww][C::OPL + o]);
+                        ou.x += pu.x; ou.y += pu.y; ou.z += pu.z; ou.w += pu.w;
+                        od.x += pd.x; od.y += pd.y; od.z += pd.z; od.w += pd.w;
+                        oy.x += py.x; oy.y += py.y; oy.z += py.z; oy.w += py.w;
+                    }
+                    if (ww == 0) {
+                        su = ou; sd = od; sy = oy;
+                    } else {
+                        su.x += ou.x; su.y += ou.y; su.z += ou.z; su.w += ou.w;
+                        sd.x += od.x; sd.y += od.y; sd.z += od.z; sd.w += od.w;
+                        sy.x += oy.x; sy.y += oy.y; sy.z += oy.z; sy.w += oy.w;
+                    }
                 }
                 const float4 dua = sDU[r][bpair_slot<PAIRS>(cg / 2)], dub = sDU[r][bpair_slot<PAIRS>(cg / 2 + 1)];
                 const float2 gga = sG[r][bpair_slot<PAIRS>(cg / 2)], ggb = sG[r][bpair_slot<PAIRS>(cg / 2 + 1)];
@@ -685,8 +698,8 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                 }
 #pragma unroll
                 for (int c = 0; c < GRP; c++) {
-                    sAcc[0][it * GRP + c][tid] = fmaf(vg[c], vu[c], sAcc[0][it * GRP + c][tid]);  // g = u = 0 past t_end
-                    sAcc[1][it * GRP + c][tid] += tv ? vdx[c] : 0.f;
+                    accD[it * GRP + c] = fmaf(vg[c], vu[c], accD[it * GRP + c]);  // g = u = 0 past t_end
+                    accB[it * GRP + c] += tv ? vdx[c] : 0.f;
                 }
                 if (tv) {
                     const int64_t off = (b * L + t) * Dch + d0 + cg;
@@ -726,6 +739,12 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
         }
         // dD / ddelta_bias of each channel: the partials of the items that own it
         // (one per step of the tile) added in step order
+#pragma unroll
+        for (int c = 0; c < ITEMS * GRP; c++) {
+            sAcc[0][c][tid] = accD[c];
+            sAcc[1][c][tid] = accB[c];
+        }
+        __syncthreads();
         for (int cc = tid; cc < CH; cc += THREADS) {
             if (d0 + cc < Dch) {
                 const int qg = cc / GRP, c = cc % GRP;
