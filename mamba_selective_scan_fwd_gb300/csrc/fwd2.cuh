@@ -6,12 +6,11 @@
 //
 // One block owns CH channels of one batch row and one time chunk (the block
 // layout of kernels.h): lane (p, g) of warp w holds S states of the channel
-// pair p, the states n0 = w N/NW + g S .. n0 + S of both channels.  What
-// bounds this kernel is the traffic through the SM's shared-memory / L1 data
-// pipe, so the layout spends it sparingly: every B / C value a lane reads
-// from shared memory (raw io elements, bf16 stays bf16) serves two channels,
-// one 16-byte load brings delta_eff and delta_eff * u of both, and the two
-// lanes of a pair trade halves of their readouts so that each stores one.
+// pair p, the states n0 = w N/NW + g S .. n0 + S of both channels.  The
+// layout spends the SM's shared-memory / L1 data pipe sparingly: every B / C
+// value a lane reads from shared memory serves two channels, and one 16-byte
+// load brings delta_eff and delta_eff * u of both; each lane stores its two
+// channels' partial readouts with one 8-byte store.
 // Work per 32-step tile:
 //   prologue  threads take (step, 8-channel group) items: load the group's
 //             runs of u, delta, z (whole 16-byte vectors, four items per
@@ -20,10 +19,10 @@
 //             items copy the B and C rows of the tile;
 //   scan      each lane walks the 32 steps for its 2 x S states with packed
 //             f32x2 arithmetic (one MUFU ex2 per state per step) and stores
-//             its channel's partial readout per step;
+//             its two channels' partial readouts per step;
 //   epilogue  threads take (step, 8-channel group) items again: add the
-//             warps' partial readouts, D * u, apply the gate and store the
-//             group's run of y.
+//             lanes' and warps' partial readouts, D * u, apply the gate and
+//             store the group's run of y.
 // The time axis of a unit (batch row, channel tile) is cut into K chunks when
 // the plan says so (kernels.h); a chunk summary -- its end state H from a zero
 // start and its sum of delta_eff, which gives the product of its decays
@@ -69,6 +68,10 @@ struct FCfg {
     // that the 16-byte loads of consecutive rows fall in different bank groups
     static constexpr int RAWP = NB >= 32 ? N + 16 / ESZ : N;
     static constexpr int YP = CH + 4;               // padded shared row of partial readouts (floats)
+    // plane of one lane of a pair's partial readouts: kRow rows of YP floats,
+    // planes 16 mod 32 floats apart so that the 8-byte stores of both lanes of
+    // the pairs of a half warp hit 32 banks
+    static constexpr int YPL = kRow * YP + 16;
     static_assert(kRow * NGRP % THREADS == 0, "whole items per thread");
     static_assert(CH == channels_per_block(N), "channel tile of the plan");
 };
@@ -104,7 +107,9 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), fwd_warps(N) == 2 ? 4 : 12)
     // raw runs of delta, u, z of the next tile, copied in asynchronously by the
     // thread that later converts them
     __shared__ __align__(16) T sRaw[NOY ? 2 : 3][kRow][CH];
-    __shared__ __align__(16) float sY[NOY ? 1 : NW][NOY ? 1 : kRow][YP];  // per-warp partial readouts
+    // per-warp partial readouts, one plane per lane of a pair (float g YPL + i YP
+    // + c: lane g's sum over its states, step i, channel c)
+    __shared__ __align__(16) float sY[NOY ? 1 : NW][NOY ? 1 : G * C::YPL];
     __shared__ float sBias[CH], sDv[CH];
 
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -337,13 +342,8 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), fwd_warps(N) == 2 ? 4 : 12)
                 }
             }
             if (!NOY) {
-                if constexpr (G == 2) {
-                    // lane g keeps channel c0 + g: it adds the partner's partial of that channel
-                    const float other = __shfl_xor_sync(kFull, g ? yp[0] : yp[1], 1);
-                    sY[w][i][lane] = (g ? yp[1] : yp[0]) + other;
-                } else {
-                    *reinterpret_cast<float2*>(&sY[w][i][c0]) = make_float2(yp[0], yp[1]);
-                }
+                // both channels' partials of the lane; the epilogue adds the pair's lanes
+                *reinterpret_cast<float2*>(&sY[w][g * C::YPL + i * YP + c0]) = make_float2(yp[0], yp[1]);
             }
         }
         __syncthreads();
@@ -360,11 +360,20 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), fwd_warps(N) == 2 ? 4 : 12)
                     float yv[GRP];
 #pragma unroll
                     for (int c = 0; c < GRP; c += 4) {
-                        float4 acc = *reinterpret_cast<const float4*>(&sY[0][r][cg + c]);
+                        // per warp, the sum of its G lanes' planes; then the warps in order
+                        float4 acc;
 #pragma unroll
-                        for (int ww = 1; ww < NW; ww++) {
-                            const float4 o = *reinterpret_cast<const float4*>(&sY[ww][r][cg + c]);
-                            acc.x += o.x; acc.y += o.y; acc.z += o.z; acc.w += o.w;
+                        for (int ww = 0; ww < NW; ww++) {
+                            float4 o = *reinterpret_cast<const float4*>(&sY[ww][r * YP + cg + c]);
+                            if constexpr (G == 2) {
+                                const float4 q = *reinterpret_cast<const float4*>(&sY[ww][C::YPL + r * YP + cg + c]);
+                                o.x += q.x; o.y += q.y; o.z += q.z; o.w += q.w;
+                            }
+                            if (ww == 0) {
+                                acc = o;
+                            } else {
+                                acc.x += o.x; acc.y += o.y; acc.z += o.z; acc.w += o.w;
+                            }
                         }
                         const float4 g01 = sGD[r][pair_slot<NGRP>((cg + c) / 2)];
                         const float4 g23 = sGD[r][pair_slot<NGRP>((cg + c) / 2 + 1)];
