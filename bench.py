@@ -310,7 +310,13 @@ def run_ours(args):
     ms_per_step = total_ms / K
     value = job_throughput(w.bld * K, world, total_ms)
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers.  Every step copies
+    # its inputs from pinned host memory and its outputs back; two sets of device
+    # input / output buffers and one copy stream per direction let step i's
+    # input copy run during step i - 1's compute and its output copy during
+    # step i + 1's (the restart states and workspaces stay on the compute
+    # stream).  The output copy bounds it (1178 MB per step); splitting each
+    # copy over two streams per direction was no faster.
     in_keys = [k for k in ("u", "delta", "A", "B", "C", "D", "z", "delta_bias", "dy") if k in host]
     h2d = sum(host[k].numel() * host[k].element_size() for k in in_keys)
     out_host = {"y": torch.empty(y.shape, dtype=y.dtype).pin_memory(),
@@ -320,24 +326,66 @@ def run_ours(args):
             out_host[k] = torch.empty(v.shape, dtype=v.dtype).pin_memory()
     d2h = sum(v.numel() * v.element_size() for v in out_host.values())
     e2e_steps = max(2, min(args.e2e_steps, K))
+    sets = []
+    for _ in range(2):
+        di = {k: (None if v is None else torch.empty_like(v)) for k, v in d.items()}
+        sets.append({"d": di, "y": torch.empty_like(y), "last": torch.empty_like(last), "g": {}})
+    NCS = 1  # copy streams per direction
+    s_in = [torch.cuda.Stream(dev) for _ in range(NCS)]
+    s_out = [torch.cuda.Stream(dev) for _ in range(NCS)]
+    ev = {k: [[torch.cuda.Event() for _ in range(NCS)] for _ in range(2)] for k in ("in", "out")}
+    ev["done"] = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        for k in in_keys:
-            d[k].copy_(host[k], non_blocking=True)
-        step()
-        out_host["y"].copy_(y, non_blocking=True)
-        out_host["last_state"].copy_(last, non_blocking=True)
-        for k, v in grads.items():
-            if v is not None:
-                out_host[k].copy_(v, non_blocking=True)
+    def split_copy(dst, src, q):
+        """Part q of NCS of a contiguous tensor copy."""
+        a, b = dst.view(-1), src.view(-1)
+        n = a.numel()
+        lo, hi = n * q // NCS, n * (q + 1) // NCS
+        if hi > lo:
+            a[lo:hi].copy_(b[lo:hi], non_blocking=True)
 
-    e2e_step()
+    def e2e_run(nsteps, start_ev=None):
+        for q in range(NCS):
+            if start_ev is not None:
+                s_in[q].wait_event(start_ev)
+        for i in range(nsteps):
+            j = i % 2
+            bs = sets[j]
+            for q in range(NCS):
+                with torch.cuda.stream(s_in[q]):
+                    if i >= 2:
+                        s_in[q].wait_event(ev["done"][j])  # step i - 2 is done reading this set's inputs
+                    for k in in_keys:
+                        split_copy(bs["d"][k], host[k], q)
+                    ev["in"][j][q].record(s_in[q])
+            for q in range(NCS):
+                stream.wait_event(ev["in"][j][q])
+                if i >= 2:
+                    stream.wait_event(ev["out"][j][q])  # step i - 2's outputs have left this set
+            di = bs["d"]
+            ss.ss_fwd_save(di["u"], di["delta"], di["A"], di["B"], di["C"], di["D"], di["z"], di["delta_bias"],
+                           w.softplus, y=bs["y"], last_state=bs["last"], saved=saved, workspace=ws_f, stream=stream)
+            bs["g"].update(ss.ss_bwd_saved(di["u"], di["delta"], di["A"], di["B"], di["C"], di["D"], di["z"],
+                                           di["delta_bias"], w.softplus, di["dy"], saved, out=bs["g"],
+                                           workspace=ws_b, stream=stream))
+            ev["done"][j].record(stream)
+            outs = [(out_host["y"], bs["y"]), (out_host["last_state"], bs["last"])]
+            outs += [(out_host[k], v) for k, v in bs["g"].items() if v is not None]
+            for q in range(NCS):
+                with torch.cuda.stream(s_out[q]):
+                    s_out[q].wait_event(ev["done"][j])
+                    for dst, src in outs:
+                        split_copy(dst, src, q)
+                    ev["out"][j][q].record(s_out[q])
+        for q in range(NCS):
+            stream.wait_event(ev["out"][(nsteps - 1) % 2][q])
+
+    e2e_run(2)
     torch.cuda.synchronize(dev)
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
+    e2e_run(e2e_steps, start_ev=e0)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
@@ -501,7 +549,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the single-step decoding measurement")
