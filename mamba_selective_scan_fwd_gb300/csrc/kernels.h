@@ -109,20 +109,47 @@ constexpr int64_t kFwdMinChunk = 128;
 // no-allocation forward, so that splitting never takes a problem out of it.
 constexpr int64_t kSplitSummaryMax = 2 << 20;
 
+// Forward declaration: blocks of one round (below).
+inline int64_t round_blocks(int64_t N);
+
+// Cost of cutting nunits units into K chunks of their L steps, in units of
+// one round of full-length blocks: the rounds of chunk blocks, each 1 / K as
+// long (a partial round counted whole), plus the chunk summaries, about 0.6 of
+// a main pass for K - 1 of the K chunks.
+inline double chunk_cost(int64_t nunits, int64_t K, int64_t rb) {
+    return (double)ceil_div(nunits * K, rb) / (double)K +
+           0.6 * (double)nunits / (double)rb * (double)(K - 1) / (double)K;
+}
+
 // Chunking of nunits units that fills the GPU: K time chunks when nunits
-// blocks hold fewer than kTargetWarps warps (at most kcap).
+// blocks make less than one round, chosen by chunk_cost among the counts that
+// fill at least one round (at most kcap; chunks of at least kFwdMinChunk
+// steps; the cost is taken at the chunk length rounded up to 32 steps).
 inline void chunking(int64_t nunits, int64_t L, int64_t N, int64_t& K, int64_t& Lc, int64_t kcap = 1ll << 40) {
-    const int64_t warps = nunits * fwd_warps(N);
+    const int64_t rb = round_blocks(N);
+    int64_t kmax = ceil_div(L, kFwdMinChunk);
+    if (kmax > kcap) kmax = kcap;
+    if (kmax < 1) kmax = 1;
+    auto length = [&](int64_t k) {
+        const int64_t lc = ceil_div(ceil_div(L, k), 32) * 32;
+        return lc < 32 ? (int64_t)32 : lc;
+    };
     K = 1;
-    if (warps > 0 && warps < kTargetWarps) K = ceil_div(kTargetWarps, warps);
-    if (K > kcap) K = kcap;
-    const int64_t kmax = ceil_div(L, kFwdMinChunk);
-    if (K > kmax) K = kmax;
-    if (K < 1) K = 1;
-    Lc = ceil_div(ceil_div(L, K), 32) * 32;
-    if (Lc < 32) Lc = 32;
-    K = ceil_div(L, Lc);
-    if (K < 1) K = 1;
+    Lc = length(1);
+    if (nunits <= 0 || nunits >= rb) return;
+    const int64_t kmin = ceil_div(rb, nunits);
+    double best = 0.0;
+    bool have = false;
+    for (int64_t k = kmin < kmax ? kmin : kmax; k <= kmax && k <= 3 * kmin; k++) {
+        const int64_t lc = length(k), keff = ceil_div(L, lc);
+        const double c = chunk_cost(nunits, keff, rb);
+        if (!have || c < best - 1e-9) {
+            best = c;
+            have = true;
+            K = keff;
+            Lc = lc;
+        }
+    }
 }
 
 // Blocks of one round: kTargetWarps warps, 8 on every SM.  The scan kernels of
@@ -160,8 +187,7 @@ inline FPlan make_fplan(int64_t Bsz, int64_t L, int64_t Dch, int64_t N) {
         chunking(tail, L, N, Kt, Lct, kcap);
         if (Kt > 1) {
             // costs in rounds: the tail's chunks (whole rounds of them) and its summaries
-            const double split = (double)ceil_div(tail * Kt, rb) / (double)Kt +
-                                 0.6 * (double)(tail * (Kt - 1)) / (double)(Kt * rb);
+            const double split = chunk_cost(tail, Kt, rb);
             const double partial = (double)tail / (double)rb > 0.5 ? (double)tail / (double)rb : 0.5;
             if (split < partial) {
                 p.nseg = 2;
