@@ -271,15 +271,9 @@ def run_ours(args):
         step()
     torch.cuda.synchronize(dev)
 
-    # ---- device-resident timing, per-call and per-kernel events on the launching stream
+    # ---- device-resident timing: exactly K steps between two events on the
+    # launching stream, nothing else in between
     K = args.steps
-    nf, nb = plan["fwd_kernels"], plan["bwd_saved_kernels"]
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
-    kev_f = [[torch.cuda.Event(enable_timing=True) for _ in range(nf + 1)] for _ in range(K)]
-    kev_b = [[torch.cuda.Event(enable_timing=True) for _ in range(nb + 1)] for _ in range(K)]
-    for e in [e for row in kev_f + kev_b for e in row]:
-        e.record(stream)  # creates the event handles the library records
-    torch.cuda.synchronize(dev)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local if world > 1 else 0)
     clocks.start()
@@ -288,6 +282,22 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     start.record(stream)
     for i in range(K):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+
+    # ---- attribution: the same K steps again with per-call and per-kernel
+    # events (the library records them between its own launches)
+    nf, nb = plan["fwd_kernels"], plan["bwd_saved_kernels"]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    kev_f = [[torch.cuda.Event(enable_timing=True) for _ in range(nf + 1)] for _ in range(K)]
+    kev_b = [[torch.cuda.Event(enable_timing=True) for _ in range(nb + 1)] for _ in range(K)]
+    for e in [e for row in kev_f + kev_b for e in row]:
+        e.record(stream)  # creates the event handles the library records
+    torch.cuda.synchronize(dev)
+    for i in range(K):
         evs[i][0].record(stream)
         binding.profile_events(kev_f[i])
         fwd()
@@ -295,11 +305,8 @@ def run_ours(args):
         binding.profile_events(kev_b[i])
         bwd()
         evs[i][2].record(stream)
-    end.record(stream)
     binding.profile_events([])
     torch.cuda.synchronize(dev)
-    barrier(world)
-    clk = clocks.stop()
     total_ms = start.elapsed_time(end)
     t_fwd = sum(e[0].elapsed_time(e[1]) for e in evs) / K
     t_bwd = sum(e[1].elapsed_time(e[2]) for e in evs) / K

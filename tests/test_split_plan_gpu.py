@@ -17,8 +17,9 @@ from gpu_util import (TOL, gpu_bwd, gpu_bwd_saved, gpu_fwd, gpu_fwd_save, normwi
 
 pytestmark = pytest.mark.gpu
 
-# 2 x 310 = 620 units: 608 of one chunk, then 12 (batch row 1, tiles 298..309,
-# the last one 25 channels wide) cut into chunks of 128, 128 and 44 steps
+# Two-warp blocks (N = 16): a round is 608 blocks.  2 x 310 = 620 units: 608
+# of one chunk, then 12 (batch row 1, tiles 298..309, the last one 25 channels
+# wide) cut into chunks of 128, 128 and 44 steps
 SHAPE = (2, 300, 9913, 16)
 GRADS = ("du", "ddelta", "dA", "dB", "dC", "dD", "dz", "ddelta_bias")
 
@@ -86,3 +87,30 @@ def test_split_plan_state_parity(orc):
     d0 = 298 * 32
     assert normwise(g["dh0"][1, d0:], rb.dh0[1, d0:]) <= tb
     assert normwise(last[1, d0:], rf.last_state[1, d0:]) <= tf
+
+
+# One-warp blocks (N = 8): a round is 1216 blocks.  2 x 658 = 1316 units: 1216
+# of one chunk, then 100 (batch row 1, tiles 558..657) cut into 4 chunks.
+SHAPE8 = (2, 512, 21056, 8)
+
+
+def test_split_plan_parity_one_warp_blocks(orc):
+    assert ss.plan_info(*SHAPE8, ss.SS_BF16)["segments"] == [(1216, 1), (100, 4)]
+    x = small_inputs(*SHAPE8, io="bf16", seed=5300)
+    t = to_device(x, "bf16")
+    y, last, saved = gpu_fwd_save(t)
+    g = gpu_bwd_saved(t, saved)
+    torch.cuda.synchronize()
+    rf = oracle_fwd(orc, x)
+    rb = oracle_bwd(orc, x)
+    tf, tb = TOL["bf16"]["fwd"], TOL["bf16"]["bwd"]
+    errs = {"y": normwise(y, ref_y(rf.y, "bf16")), "last_state": normwise(last, rf.last_state)}
+    for k in GRADS:
+        errs[k] = normwise(g[k], getattr(rb, k))
+    bad = {k: e for k, e in errs.items() if e > (tf if k in ("y", "last_state") else tb)}
+    assert not bad, (bad, errs)
+    d0 = 558 * 32
+    assert normwise(y[1, :, d0:], ref_y(rf.y, "bf16")[1, :, d0:]) <= tf
+    assert normwise(last[1, d0:], rf.last_state[1, d0:]) <= tf
+    for k in ("du", "ddelta", "dz"):
+        assert normwise(g[k][1, :, d0:], getattr(rb, k)[1, :, d0:]) <= tb, k
