@@ -85,11 +85,11 @@ struct BCfg {
     // channels); blocks are padded by 8 floats so that the 16 lanes of a half
     // warp reading 8-byte pairs of four consecutive blocks hit 32 banks
     static constexpr int BLK = PAIRS * NPW + 8;
-    // blocks per SM the register budget must allow: 4 two-warp blocks (8 warps,
-    // one round of the plan on every SM), which leaves the scan up to 255
-    // registers (it takes about 230 and runs 6 % faster than at 168); 12
-    // one-warp blocks
-    static constexpr int MINB = NW == 2 ? 4 : 12;
+    // blocks per SM the register budget must allow: one round of the plan on
+    // every SM (8 warps: 4 two-warp or 8 one-warp blocks), which leaves the
+    // scan up to 255 registers (N = 16 takes about 230 and runs 6 % faster
+    // than at 168)
+    static constexpr int MINB = NW == 2 ? 4 : 8;
     static_assert(kTT * NGRP % THREADS == 0, "whole items per thread");
     static_assert(CH == channels_per_block(N), "channel tile of the plan");
 };

@@ -87,7 +87,7 @@ __device__ __forceinline__ int pair_slot(int pp) {
 }
 
 template <typename T, int N, int MODE>
-__global__ void __launch_bounds__(32 * fwd_warps(N), fwd_warps(N) == 2 ? 4 : 12) k_fwd2(FwdArgs a, FPlan p, int si, int64_t k_lo,
+__global__ void __launch_bounds__(32 * fwd_warps(N), fwd_warps(N) == 2 ? 4 : 8) k_fwd2(FwdArgs a, FPlan p, int si, int64_t k_lo,
                                                                float* ckpt) {
     constexpr bool SUMMARY = MODE == kModeSummary;
     constexpr bool NOY = MODE == kModeSummary || MODE == kModeCkpt;  // no readout, gate or y

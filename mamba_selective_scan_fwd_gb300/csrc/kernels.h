@@ -152,10 +152,9 @@ inline void chunking(int64_t nunits, int64_t L, int64_t N, int64_t& K, int64_t& 
     }
 }
 
-// Blocks of one round: kTargetWarps warps, 8 on every SM.  The scan kernels of
-// two-warp blocks are built for 4 resident blocks per SM (their register
-// budget), those of one-warp blocks for 8 or more, so a round is also what
-// one wave of the GPU holds at that budget.
+// Blocks of one round: kTargetWarps warps, 8 on every SM.  The scan kernels
+// are built for 8 resident warps per SM (4 two-warp or 8 one-warp blocks:
+// their register budget), so a round is also what one wave of the GPU holds.
 inline int64_t round_blocks(int64_t N) { return kTargetWarps / fwd_warps(N); }
 
 // A pure function of the sizes (the same sizes always plan the same way).
