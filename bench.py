@@ -35,7 +35,15 @@ from mamba_selective_scan_fwd_gb300.inputs import WORKLOADS, make_inputs  # noqa
 
 METRIC = "selective-scan fwd+bwd elements/s (B·L·D) and HBM GB/s vs GB300 peak"
 UNIT = "elements/s"
-WORKLOAD = WORKLOADS[3]  # mamba2.8b-layer-bf16
+WORKLOAD = WORKLOADS[3]  # mamba2.8b-layer-bf16: the workload the metric is quoted on
+
+
+def pick_workload(name):
+    """The workload named on the command line (every one runs forward + backward here)."""
+    for w in WORKLOADS:
+        if w.name == name:
+            return w
+    raise SystemExit(f"unknown workload {name!r}; one of {[w.name for w in WORKLOADS]}")
 
 # Algorithmic bytes per element (B*L*D unit) for bf16 I/O, f32 gradients:
 #   forward  = u, delta, z read + y write (4 x 2 B) = 8 B  (+ B, C, A, D, bias, last_state: per-(b,t) / per-d terms)
@@ -58,10 +66,10 @@ def algorithmic_bytes(w):
 # figure stale, and it is reported as null.
 TRAFFIC = {
     # both launches of the main pass (608 one-chunk units; 32 units x 19 chunks)
-    ("k_bwd2_main", "mamba2.8b-layer-bf16"): 3284502528,  # 1914.3 + 102.3 MB read, 1238.4 + 29.5 MB written
-    ("k_fwd2_y", "mamba2.8b-layer-bf16"): 1896676608,     # 479.6 + 26.8 MB read, 1372.9 + 17.3 MB written
+    ("k_bwd2_main", "mamba2.8b-layer-bf16"): 3284427008,  # 1914.3 + 102.3 MB read, 1238.4 + 29.4 MB written
+    ("k_fwd2_y", "mamba2.8b-layer-bf16"): 1897271296,     # 479.7 + 26.8 MB read, 1373.5 + 17.3 MB written
 }
-TRAFFIC_SRC_DIGEST = "9399311360ce0c55"
+TRAFFIC_SRC_DIGEST = "479249c21d6501ec"
 
 
 def measured_traffic(kernel, w):
@@ -229,8 +237,8 @@ def run_ours(args):
 
     world, rank, local = dist_setup("nccl")
     dev = torch.device("cuda", local if world > 1 else 0)
-    w = WORKLOAD
-    x = make_inputs(w)
+    w = pick_workload(args.workload)
+    x = make_inputs(w, with_dy=True)
     io_dt = torch.bfloat16 if w.io == "bf16" else torch.float32
     io_keys = ("u", "delta", "B", "C", "z", "dy")
     host = {}
@@ -337,38 +345,24 @@ def run_ours(args):
     for _ in range(2):
         di = {k: (None if v is None else torch.empty_like(v)) for k, v in d.items()}
         sets.append({"d": di, "y": torch.empty_like(y), "last": torch.empty_like(last), "g": {}})
-    NCS = 1  # copy streams per direction
-    s_in = [torch.cuda.Stream(dev) for _ in range(NCS)]
-    s_out = [torch.cuda.Stream(dev) for _ in range(NCS)]
-    ev = {k: [[torch.cuda.Event() for _ in range(NCS)] for _ in range(2)] for k in ("in", "out")}
-    ev["done"] = [torch.cuda.Event() for _ in range(2)]
-
-    def split_copy(dst, src, q):
-        """Part q of NCS of a contiguous tensor copy."""
-        a, b = dst.view(-1), src.view(-1)
-        n = a.numel()
-        lo, hi = n * q // NCS, n * (q + 1) // NCS
-        if hi > lo:
-            a[lo:hi].copy_(b[lo:hi], non_blocking=True)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "done", "out")}
 
     def e2e_run(nsteps, start_ev=None):
-        for q in range(NCS):
-            if start_ev is not None:
-                s_in[q].wait_event(start_ev)
+        if start_ev is not None:
+            s_in.wait_event(start_ev)
         for i in range(nsteps):
             j = i % 2
             bs = sets[j]
-            for q in range(NCS):
-                with torch.cuda.stream(s_in[q]):
-                    if i >= 2:
-                        s_in[q].wait_event(ev["done"][j])  # step i - 2 is done reading this set's inputs
-                    for k in in_keys:
-                        split_copy(bs["d"][k], host[k], q)
-                    ev["in"][j][q].record(s_in[q])
-            for q in range(NCS):
-                stream.wait_event(ev["in"][j][q])
+            with torch.cuda.stream(s_in):
                 if i >= 2:
-                    stream.wait_event(ev["out"][j][q])  # step i - 2's outputs have left this set
+                    s_in.wait_event(ev["done"][j])  # step i - 2 is done reading this set's inputs
+                for k in in_keys:
+                    bs["d"][k].copy_(host[k], non_blocking=True)
+                ev["in"][j].record(s_in)
+            stream.wait_event(ev["in"][j])
+            if i >= 2:
+                stream.wait_event(ev["out"][j])  # step i - 2's outputs have left this set
             di = bs["d"]
             ss.ss_fwd_save(di["u"], di["delta"], di["A"], di["B"], di["C"], di["D"], di["z"], di["delta_bias"],
                            w.softplus, y=bs["y"], last_state=bs["last"], saved=saved, workspace=ws_f, stream=stream)
@@ -376,16 +370,15 @@ def run_ours(args):
                                            di["delta_bias"], w.softplus, di["dy"], saved, out=bs["g"],
                                            workspace=ws_b, stream=stream))
             ev["done"][j].record(stream)
-            outs = [(out_host["y"], bs["y"]), (out_host["last_state"], bs["last"])]
-            outs += [(out_host[k], v) for k, v in bs["g"].items() if v is not None]
-            for q in range(NCS):
-                with torch.cuda.stream(s_out[q]):
-                    s_out[q].wait_event(ev["done"][j])
-                    for dst, src in outs:
-                        split_copy(dst, src, q)
-                    ev["out"][j][q].record(s_out[q])
-        for q in range(NCS):
-            stream.wait_event(ev["out"][(nsteps - 1) % 2][q])
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev["done"][j])
+                out_host["y"].copy_(bs["y"], non_blocking=True)
+                out_host["last_state"].copy_(bs["last"], non_blocking=True)
+                for k, v in bs["g"].items():
+                    if v is not None:
+                        out_host[k].copy_(v, non_blocking=True)
+                ev["out"][j].record(s_out)
+        stream.wait_event(ev["out"][(nsteps - 1) % 2])
 
     e2e_run(2)
     torch.cuda.synchronize(dev)
@@ -521,8 +514,8 @@ def run_reference(args):
 
     import oracle
 
-    w = WORKLOAD
-    x = make_inputs(w)
+    w = pick_workload(args.workload)
+    x = make_inputs(w, with_dy=True)
     x64 = {k: (None if v is None else np.ascontiguousarray(v, dtype=np.float64)) for k, v in x.items()}
     orc = oracle.get()
     cores = oracle.default_threads()
@@ -560,6 +553,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the single-step decoding measurement")
+    ap.add_argument("--workload", default=WORKLOAD.name,
+                    help="workload to time (default: the one the metric is quoted on)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.impl == "reference":
