@@ -40,6 +40,7 @@ def _noalloc_raw(t, y, last, io):
     ((1, 1000, 2, 16), "f32"),     # 8 time chunks, small scratch use
     ((1, 32768, 64, 16), "bf16"),  # 256 time chunks: the summaries fill half the 2 MiB scratch
     ((2, 777, 5, 32), "f32"),      # N = 32 over four lanes, ragged last chunk
+    ((2, 300, 9913, 16), "bf16"),  # split plan: 608 one-chunk units, then 12 cut into 3 chunks
 ])
 def test_noalloc_matches_regular_forward_twice(shape, io):
     Bsz, L, Dch, N = shape
