@@ -9,6 +9,7 @@ from __future__ import annotations
 
 import hashlib
 import os
+import re
 import shutil
 import subprocess
 from concurrent.futures import ThreadPoolExecutor
@@ -44,9 +45,28 @@ def _digest() -> str:
     return h.hexdigest()
 
 
+# a string or character literal (kept), or a comment (dropped)
+_TOKEN = re.compile(r'"(?:\\.|[^"\\])*"|\'(?:\\.|[^\'\\])*\'|//[^\n]*|/\*.*?\*/', re.S)
+
+
+def _code(text: str) -> str:
+    """Source text without comments, whitespace runs collapsed: what the compiler sees."""
+    text = _TOKEN.sub(lambda m: m.group(0) if m.group(0)[0] in "\"'" else " ", text)
+    return re.sub(r"\s+", " ", text).strip()
+
+
 def source_digest() -> str:
-    """Digest of the kernel sources and build flags: changes whenever the compiled kernels may change."""
-    return _digest()[:16]
+    """Digest of the kernel sources (comments and layout ignored) and build flags:
+    changes whenever the compiled kernels may change, and only then."""
+    h = hashlib.sha256()
+    h.update(" ".join(ARCH + NVCC_FLAGS + SOURCES).encode())
+    deps = sorted(f for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh", ".h")))
+    for name in deps:
+        with open(os.path.join(CSRC, name), encoding="utf-8") as f:
+            h.update(name.encode() + _code(f.read()).encode())
+    with open(os.path.join(ROOT, "include", "ss.h"), encoding="utf-8") as f:
+        h.update(_code(f.read()).encode())
+    return h.hexdigest()[:16]
 
 
 def build(force: bool = False, verbose: bool = False) -> str:

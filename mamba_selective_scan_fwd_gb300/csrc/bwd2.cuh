@@ -24,10 +24,10 @@
 //     derivative, the gate, g, the dz factor) into shared memory; then each
 //     sub-chunk is recomputed forward from its saved state, keeping its
 //     states and decays in registers, and the adjoint walks it backwards;
-//   * per step the G lanes of a channel combine their partial sums with a
-//     shuffle, and each warp sums dB / dC of its states over the block's
+//   * per step each lane stores its two channels' partial sums over its
+//     states, and each warp sums dB / dC of its states over the block's
 //     channels through shared memory in a fixed order; the tile epilogue
-//     adds the warps' per-(t, d) sums and writes du, ddelta, dz; a second
+//     adds the lanes' and warps' per-(t, d) sums and writes du, ddelta, dz; a second
 //     kernel adds the per-tile dB / dC partials, a third the per-(batch,
 //     chunk) dA / dD / ddelta_bias partials.  Every sum has a fixed order:
 //     the result is bit-reproducible.
@@ -213,7 +213,7 @@ __device__ __forceinline__ void store_run(float* p, const float (&v)[CPL], int64
 }
 
 // MODE kRevMain: the backward proper.  MODE kRevSummary: only the adjoint
-// walk of chunks 1..K-1 from a zero carry, writing (P_k, M_k).  STATE: the
+// walk of chunks 1..K-1 from a zero carry, writing (sum of delta_eff, M_k).  STATE: the
 // call has an incoming gradient of last_state or wants dh0 (a separate
 // instantiation, so that the plain backward carries none of it).
 constexpr int kRevMain = 0, kRevSummary = 1;
@@ -243,9 +243,8 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
     __shared__ __align__(16) float sEz[MAIN ? kTT : 1][MAIN ? EP : 4];
     // dB / dC contributions of kRB steps, per warp: block (j, tau) holds a row of NPW floats per pair
     __shared__ __align__(16) float sR[MAIN ? NW : 1][MAIN ? kRB * 2 * BLK : 4];
-    // per-step, per-warp sums over the warp's states: sum lam B, sum A q, y0 (channel fastest)
-    // (one plane per lane of a pair: float g OPL + r EP + c is the sum over the
-    // states of lane g, for step r and channel c)
+    // per-step sums over a lane's states: sum lam B, sum A q, y0, one plane per
+    // lane of a pair (float g OPL + r EP + c: lane g's sum for step r, channel c)
     __shared__ __align__(16) float sOu[MAIN ? NW : 1][MAIN ? G * C::OPL : 4];
     __shared__ __align__(16) float sOd[MAIN ? NW : 1][MAIN ? G * C::OPL : 4];
     __shared__ __align__(16) float sOy[MAIN ? NW : 1][MAIN ? G * C::OPL : 4];
