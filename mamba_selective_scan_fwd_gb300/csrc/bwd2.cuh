@@ -708,7 +708,12 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                 }
             }
         }
-        __syncthreads();  // the next prologue restages the tile
+        // The reverse summary's walk reads what the next prologue restages.  The
+        // main pass needs no barrier here: its epilogue reads only the per-step
+        // sums (the next ones are written after the next prologue's barrier)
+        // and the staging entries of its own items, which the same thread
+        // rewrites next.
+        if constexpr (!MAIN) __syncthreads();
     }
 
     const int64_t q = q_first + k;  // this block's part
