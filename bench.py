@@ -66,10 +66,10 @@ def algorithmic_bytes(w):
 # figure stale, and it is reported as null.
 TRAFFIC = {
     # both launches of the main pass (608 one-chunk units; 32 units x 19 chunks)
-    ("k_bwd2_main", "mamba2.8b-layer-bf16"): 3284427008,  # 1914.3 + 102.3 MB read, 1238.4 + 29.4 MB written
-    ("k_fwd2_y", "mamba2.8b-layer-bf16"): 1897271296,     # 479.7 + 26.8 MB read, 1373.5 + 17.3 MB written
+    ("k_bwd2_main", "mamba2.8b-layer-bf16"): 3285449984,  # 1915.1 + 102.3 MB read, 1238.4 + 29.6 MB written
+    ("k_fwd2_y", "mamba2.8b-layer-bf16"): 1896813056,     # 479.7 + 26.8 MB read, 1373.0 + 17.3 MB written
 }
-TRAFFIC_SRC_DIGEST = "756e5daab0d6c56d"
+TRAFFIC_SRC_DIGEST = "0e5a3859876d5be9"
 
 
 def measured_traffic(kernel, w):
