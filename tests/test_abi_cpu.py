@@ -254,3 +254,13 @@ def test_ex_entry_points_validate_before_cuda():
     f.h0 = FAKE + 4  # misaligned
     f.Bsz, f.L, f.Dch, f.N, f.dtype = 1, 8, 8, 4, 0
     assert lib.ss_fwd_ex(ctypes.byref(f), None) == UNSUPPORTED
+
+
+def test_source_digest_sees_code_not_comments():
+    from mamba_selective_scan_fwd_gb300 import build
+
+    a = 'int f(int x) { return x + 1; }  // add one\n/* block\n comment */\nconst char* s = "a // b";\n'
+    b = 'int f(int x)\n{\n    return x + 1;\n}\nconst char* s = "a // b";  // kept: it is a string\n'
+    assert build._code(a) == build._code(b)
+    assert build._code(a) != build._code(a.replace("x + 1", "x + 2"))
+    assert '"a // b"' in build._code(a)
