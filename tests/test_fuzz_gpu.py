@@ -1,8 +1,10 @@
 """Seeded random problems against the oracle: sizes, state size, io type,
 optional terms and softplus drawn at random, so that the launch plan meets
 shapes the hand-picked cases do not (ragged tiles and chunks of every kind,
-uniform chunking, split plans).  Every output element is compared, and the
-saved-state pair must give the same bits as the recomputing pair."""
+uniform chunking, split plans).  Every output element is compared; the
+saved-state pair must give the same bits as the recomputing pair.  The same
+draws drive the extended entry points (initial state, incoming gradient of
+last_state, A_log) and the single decoding step."""
 
 import numpy as np
 import pytest
@@ -73,3 +75,69 @@ def test_random_problem(orc, i):
     for k in GRADS:
         if g[k] is not None:
             assert torch.equal(g[k], g2[k]), k
+
+
+STATE_GRADS = GRADS + ("dh0",)
+
+
+@pytest.mark.parametrize("i", list(range(12)))
+def test_random_problem_with_state(orc, i):
+    """ss_fwd_ex / ss_bwd_ex on random problems: an initial state, an incoming
+    gradient of last_state and A given as A_log, all terms drawn at random."""
+    (Bsz, L, Dch, N), io, terms, softplus = draw(100 + i)
+    x = small_inputs(Bsz, L, Dch, N, io=io, seed=7300 + i, **terms)
+    if not softplus:
+        x["delta"] = np.abs(x["delta"]) * np.float32(0.5)
+        if x["delta_bias"] is not None:
+            x["delta_bias"] = (np.abs(x["delta_bias"]) * np.float32(0.02)).astype(np.float32)
+    rng = np.random.default_rng(7400 + i)
+    A_log = np.log(-x["A"]).astype(np.float32)
+    h0 = rng.normal(size=(Bsz, Dch, N)).astype(np.float32)
+    dlast = rng.normal(size=(Bsz, Dch, N)).astype(np.float32)
+    t = to_device(x, io)
+    A_d, h0_d, dl_d = (torch.from_numpy(v).cuda() for v in (A_log, h0, dlast))
+    y, last, saved = ss.ss_fwd_ex(t["u"], t["delta"], A_d, t["B"], t["C"], t["D"], t["z"], t["delta_bias"], softplus,
+                                  h0=h0_d, a_is_log=True, save=True)
+    g = ss.ss_bwd_ex(t["u"], t["delta"], A_d, t["B"], t["C"], t["D"], t["z"], t["delta_bias"], softplus, t["dy"],
+                     h0=h0_d, dlast_state=dl_d, a_is_log=True, saved=saved)
+    torch.cuda.synchronize()
+    rf = orc.fwd(x["u"], x["delta"], None, x["B"], x["C"], x["D"], x["z"], x["delta_bias"], softplus, h0=h0,
+                 A_log=A_log)
+    rb = orc.bwd(x["u"], x["delta"], None, x["B"], x["C"], x["D"], x["z"], x["delta_bias"], softplus, dy=x["dy"],
+                 h0=h0, dlast_state=dlast, A_log=A_log)
+    tf, tb = TOL[io]["fwd"], TOL[io]["bwd"]
+    errs = {"y": normwise(y, ref_y(rf.y, io)), "last_state": normwise(last, rf.last_state)}
+    for k in STATE_GRADS:
+        ref = getattr(rb, k)
+        if ref is None:
+            assert g[k] is None, k
+        else:
+            errs[k] = normwise(g[k], ref)
+    bad = {k: e for k, e in errs.items() if e > (tf if k in ("y", "last_state") else tb)}
+    assert not bad, ((Bsz, L, Dch, N), io, terms, softplus, bad, errs)
+
+
+@pytest.mark.parametrize("i", list(range(12)))
+def test_random_decode_step(orc, i):
+    """ss_decode_step on random sizes, io types and terms: one step from a
+    random state against the oracle's one-step forward from that state."""
+    rng = np.random.default_rng(7500 + i)
+    N = int(rng.choice([1, 2, 4, 8, 16, 32]))
+    io = str(rng.choice(["f32", "bf16", "f16"]))
+    Bsz, Dch = int(rng.integers(1, 70)), int(rng.integers(1, 400))
+    terms = dict(has_D=bool(rng.integers(0, 2)), has_z=bool(rng.integers(0, 2)), has_bias=bool(rng.integers(0, 2)))
+    a_is_log = bool(rng.integers(0, 2))
+    x = small_inputs(Bsz, 1, Dch, N, io=io, seed=7600 + i, **terms)
+    state0 = rng.normal(size=(Bsz, Dch, N)).astype(np.float32)
+    A_in = np.log(-x["A"]).astype(np.float32) if a_is_log else x["A"]
+    t = to_device(x, io)
+    state = torch.from_numpy(state0).cuda()
+    z = None if t["z"] is None else t["z"][:, 0]
+    y = ss.ss_decode_step(t["u"][:, 0], t["delta"][:, 0], torch.from_numpy(A_in).cuda(), t["B"][:, 0], t["C"][:, 0],
+                          t["D"], z, t["delta_bias"], True, state, a_is_log=a_is_log)
+    torch.cuda.synchronize()
+    r = orc.fwd(x["u"], x["delta"], None if a_is_log else x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"],
+                True, h0=state0, A_log=A_in if a_is_log else None)
+    tol = TOL[io]["fwd"]
+    assert normwise(y, ref_y(r.y, io)[:, 0]) <= tol, ((Bsz, Dch, N), io, terms, a_is_log)
+    assert normwise(state, r.last_state) <= tol, ((Bsz, Dch, N), io, terms, a_is_log)
