@@ -64,7 +64,7 @@ int fwd_impl(const void* u, const void* delta, const float* A, const void* B, co
     const FPlan p = make_fplan(Bsz, L, Dch, N);
     if (ceil_div(Dch, 4) * Bsz * p.Kmax >= (1ll << 31)) return SS_ERR_UNSUPPORTED;
     if (save) {
-        const size_t need_s = ckpt_bytes(p, Bsz, Dch, N);
+        const size_t need_s = ckpt_bytes(p, Bsz, L, Dch, N);
         if (saved == nullptr || saved_bytes < need_s) return SS_ERR_WORKSPACE_TOO_SMALL;
     }
     const size_t need = ss_fwd_workspace_bytes(Bsz, L, Dch, N, dtype);
@@ -81,6 +81,7 @@ int fwd_impl(const void* u, const void* delta, const float* A, const void* B, co
     a.ws_fsum = static_cast<float*>(workspace);
     a.ws_fsd = workspace ? reinterpret_cast<float*>(static_cast<char*>(workspace) + fsum_offset_sd(p, N)) : nullptr;
     float* ck = save ? static_cast<float*>(saved) : nullptr;
+    a.y0 = save ? reinterpret_cast<float*>(static_cast<char*>(saved) + ckpt_y0_offset(p, Bsz, N)) : nullptr;
     return launch_fwd2(a, p, st, kModeY, ck) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
@@ -134,7 +135,7 @@ int bwd_impl(const void* u, const void* delta, const float* A, const void* B, co
     }
     const FPlan p = make_fplan(Bsz, L, Dch, N);
     if (ceil_div(Dch, 4) * Bsz * p.Kmax >= (1ll << 31)) return SS_ERR_UNSUPPORTED;
-    if (from_saved && (saved == nullptr || saved_bytes < ckpt_bytes(p, Bsz, Dch, N)))
+    if (from_saved && (saved == nullptr || saved_bytes < ckpt_bytes(p, Bsz, L, Dch, N)))
         return SS_ERR_WORKSPACE_TOO_SMALL;
     const BwdLayout w = bwd_layout2(p, Bsz, L, Dch, N, from_saved);
     if (workspace_bytes < w.total || workspace == nullptr) return SS_ERR_WORKSPACE_TOO_SMALL;
@@ -159,6 +160,9 @@ int bwd_impl(const void* u, const void* delta, const float* A, const void* B, co
     a.ws_rsd = reinterpret_cast<float*>(ws + w.rsd);
     float* ckpt_out = from_saved ? nullptr : reinterpret_cast<float*>(ws + w.ckpt);
     a.ws_ckpt = from_saved ? static_cast<const float*>(saved) : ckpt_out;
+    const char* kept = from_saved ? static_cast<const char*>(saved) : ws + w.ckpt;
+    a.y0 = reinterpret_cast<const float*>(kept + ckpt_y0_offset(p, Bsz, N));
+    a.f.y0 = from_saved ? nullptr : reinterpret_cast<float*>(ws + w.ckpt + ckpt_y0_offset(p, Bsz, N));
     a.ws_bc = reinterpret_cast<float*>(ws + w.bc);
     a.ws_dA = reinterpret_cast<float*>(ws + w.dA);
     a.ws_dD = reinterpret_cast<float*>(ws + w.dD);
@@ -222,7 +226,7 @@ size_t ss_bwd_workspace_bytes(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, in
 size_t ss_saved_bytes(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype) {
     if (check_sizes(Bsz, L, Dch, N, dtype) != SS_OK) return 0;
     if (Bsz == 0 || L == 0 || Dch == 0) return 0;
-    return ckpt_bytes(make_fplan(Bsz, L, Dch, N), Bsz, Dch, N);
+    return ckpt_bytes(make_fplan(Bsz, L, Dch, N), Bsz, L, Dch, N);
 }
 
 size_t ss_bwd_saved_workspace_bytes(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype) {

@@ -243,11 +243,13 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
     __shared__ __align__(16) float sEz[MAIN ? kTT : 1][MAIN ? EP : 4];
     // dB / dC contributions of kRB steps, per warp: block (j, tau) holds a row of NPW floats per pair
     __shared__ __align__(16) float sR[MAIN ? NW : 1][MAIN ? kRB * 2 * BLK : 4];
-    // per-step sums over a lane's states: sum lam B, sum A q, y0, one plane per
+    // per-step sums over a lane's states: sum lam B, sum A q, one plane per
     // lane of a pair (float g OPL + r EP + c: lane g's sum for step r, channel c)
     __shared__ __align__(16) float sOu[MAIN ? NW : 1][MAIN ? G * C::OPL : 4];
     __shared__ __align__(16) float sOd[MAIN ? NW : 1][MAIN ? G * C::OPL : 4];
-    __shared__ __align__(16) float sOy[MAIN ? NW : 1][MAIN ? G * C::OPL : 4];
+    // the forward's pre-gate readout y0 of the tile, copied by the epilogue
+    // thread that reads it, double buffered by tile
+    __shared__ __align__(16) float sY0[MAIN ? 2 : 1][MAIN ? kTT : 1][MAIN ? CH : 4];
     // dD / ddelta_bias partials of each epilogue thread's items at the end (thread fastest)
     __shared__ float sAcc[MAIN ? 2 : 1][MAIN ? ITEMS * GRP : 1][THREADS];
     // restart states of a tile's sub-chunks, S floats per lane and channel
@@ -370,6 +372,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                     cp_async_bytes<GRP * C::ESZ>(&sRaw[1][r][cg], u + off);
                     cp_async_bytes<GRP * C::ESZ>(&sRaw[2][r][cg], dy + off);
                     if (z) cp_async_bytes<GRP * C::ESZ>(&sRaw[3][r][cg], z + off);
+                    if (MAIN && z) cp_async_bytes<GRP * 4>(&sY0[buf][r][cg], a.y0 + off);
                 }
             }
         }
@@ -561,7 +564,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                     const float2 g2 = sG[r][pslot];
                     float Bv[S], Cv[S];
                     ld_bc_f32<S>(&sBC[C::BC_DIRECT ? buf : 0][r][sg * 2 * S], Bv, Cv);
-                    float sumB[2], sumQ[2], y0[2];
+                    float sumB[2], sumQ[2];
                     float cB[S], cC[S];
                     if constexpr (S >= 2) {
                         float2 cb2[S / 2], cc2[S / 2];
@@ -569,7 +572,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                         for (int e = 0; e < 2; e++) {
                             const float2 g2e = splat2(e ? g2.y : g2.x), dl2 = splat2(e ? du.z : du.x),
                                          dlu2 = splat2(e ? du.w : du.y);
-                            float2 dup = make_float2(0.f, 0.f), ddp = dup, y0p = dup;
+                            float2 dup = make_float2(0.f, 0.f), ddp = dup;
 #pragma unroll
                             for (int s = 0; s < S; s += 2) {
                                 const float2 Cp = make_float2(Cv[s], Cv[s + 1]);
@@ -587,7 +590,6 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                                 ddp = fma2(make_float2(A2[e][s], A2[e][s + 1]), q, ddp);
                                 const float2 na = fma2(dl2, q, make_float2(dA[e][s], dA[e][s + 1]));
                                 dA[e][s] = na.x; dA[e][s + 1] = na.y;
-                                y0p = fma2(Cp, hcur, y0p);
                                 // dB / dC contributions summed over the pair's two channels
                                 cb2[s / 2] = e ? fma2(lam, dlu2, cb2[s / 2]) : mul2(lam, dlu2);
                                 cc2[s / 2] = e ? fma2(g2e, hcur, cc2[s / 2]) : mul2(g2e, hcur);
@@ -595,7 +597,6 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                             }
                             sumB[e] = dup.x + dup.y;
                             sumQ[e] = ddp.x + ddp.y;
-                            y0[e] = y0p.x + y0p.y;
                         }
 #pragma unroll
                         for (int s = 0; s < S; s += 2) {
@@ -614,7 +615,6 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                             const float q = cn * hprev;
                             sumQ[e] = A2[e][0] * q;
                             dA[e][0] = fmaf(dle, q, dA[e][0]);
-                            y0[e] = Cv[0] * hv[i][e][0];
                             cB[0] = e ? fmaf(lam, dlue, cB[0]) : lam * dlue;
                             cC[0] = e ? fmaf(ge, hv[i][e][0], cC[0]) : ge * hv[i][e][0];
                             carry[e][0] = cn;
@@ -626,7 +626,6 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                         const int o = g * C::OPL + r * EP + c0;
                         *reinterpret_cast<float2*>(&sOu[w][o]) = make_float2(sumB[0], sumB[1]);
                         *reinterpret_cast<float2*>(&sOd[w][o]) = make_float2(sumQ[0], sumQ[1]);
-                        *reinterpret_cast<float2*>(&sOy[w][o]) = make_float2(y0[0], y0[1]);
                     }
                     // stage dB / dC contributions (summed over the pairs below)
                     stage_contrib<S, NPW, BLK>(sRw, i, cB, cC, pp, g * S);
@@ -635,7 +634,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                 reduce_staged<PAIRS, NPW, N, BLK>(sRw, bc0, bc1, n_w, ts, t_end, lane);
                 __syncwarp();  // the sums have read the staging before the next sub-chunk restages it
             }
-            __syncthreads();  // every warp's per-step sums are in sOu / sOd / sOy
+            __syncthreads();  // every warp's per-step sums are in sOu / sOd
             // ---- epilogue: du, ddelta, dz of the (step, 4-channel group) items.
             // Steps past t_end (last tile only) are not stored and add nothing;
             // their per-step sums may be unwritten (a sub-chunk wholly past the
@@ -648,27 +647,37 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                 const int64_t t = t0 + r;
                 const bool tv = t < t_end;
                 // per warp, the sum of its G lanes' planes; then the warps in order
-                float4 su, sd, sy;
+                float4 su, sd;
 #pragma unroll
                 for (int ww = 0; ww < NW; ww++) {
                     const int o = r * EP + cg;
                     float4 ou = *reinterpret_cast<const float4*>(&sOu[ww][o]);
                     float4 od = *reinterpret_cast<const float4*>(&sOd[ww][o]);
-                    float4 oy = *reinterpret_cast<const float4*>(&sOy[ww][o]);
                     if constexpr (G == 2) {
                         const float4 pu = *reinterpret_cast<const float4*>(&sOu[ww][C::OPL + o]);
                         const float4 pd = *reinterpret_cast<const float4*>(&sOd[ww][C::OPL + o]);
-                        const float4 py = *reinterpret_cast<const float4*>(&sOy[ww][C::OPL + o]);
                         ou.x += pu.x; ou.y += pu.y; ou.z += pu.z; ou.w += pu.w;
                         od.x += pd.x; od.y += pd.y; od.z += pd.z; od.w += pd.w;
-                        oy.x += py.x; oy.y += py.y; oy.z += py.z; oy.w += py.w;
                     }
                     if (ww == 0) {
-                        su = ou; sd = od; sy = oy;
+                        su = ou; sd = od;
                     } else {
                         su.x += ou.x; su.y += ou.y; su.z += ou.z; su.w += ou.w;
                         sd.x += od.x; sd.y += od.y; sd.z += od.z; sd.w += od.w;
-                        sy.x += oy.x; sy.y += oy.y; sy.z += oy.z; sy.w += oy.w;
+                    }
+                }
+                // y0 for dz (only with a gate): staged with the tile's rows, else loaded here
+                float vy0[GRP];
+#pragma unroll
+                for (int c = 0; c < GRP; c++) vy0[c] = 0.f;
+                if (z && tv) {
+                    if (pfast) {
+                        const float4 q = *reinterpret_cast<const float4*>(&sY0[buf][r][cg]);
+                        vy0[0] = q.x; vy0[1] = q.y; vy0[2] = q.z; vy0[3] = q.w;
+                    } else {
+                        const float* y0r = a.y0 + (b * L + t) * Dch + d0 + cg;
+#pragma unroll
+                        for (int c = 0; c < GRP; c++) vy0[c] = d0 + cg + c < Dch ? y0r[c] : 0.f;
                     }
                 }
                 const float4 dua = sDU[r][bpair_slot<PAIRS>(cg / 2)], dub = sDU[r][bpair_slot<PAIRS>(cg / 2 + 1)];
@@ -676,8 +685,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                 const float4 u4 = *reinterpret_cast<const float4*>(&sEu[r][cg]);
                 const float4 s4 = *reinterpret_cast<const float4*>(&sEs[r][cg]);
                 const float4 z4 = *reinterpret_cast<const float4*>(&sEz[r][cg]);
-                const float vsu[4] = {su.x, su.y, su.z, su.w}, vsd[4] = {sd.x, sd.y, sd.z, sd.w},
-                            vsy[4] = {sy.x, sy.y, sy.z, sy.w};
+                const float vsu[4] = {su.x, su.y, su.z, su.w}, vsd[4] = {sd.x, sd.y, sd.z, sd.w};
                 const float vdl[4] = {dua.x, dua.z, dub.x, dub.z}, vg[4] = {gga.x, gga.y, ggb.x, ggb.y};
                 const float vu[4] = {u4.x, u4.y, u4.z, u4.w}, vs[4] = {s4.x, s4.y, s4.z, s4.w},
                             vz[4] = {z4.x, z4.y, z4.z, z4.w};
@@ -690,7 +698,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                     const float2 du2 = fma2(make_float2(vg[c], vg[c + 1]), Dv, mul2(make_float2(vdl[c], vdl[c + 1]), su2));
                     const float2 dx2 = mul2(fma2(u2, su2, mul2(make_float2(vsd[c], vsd[c + 1]), splat2(kLn2))),
                                             make_float2(vs[c], vs[c + 1]));
-                    const float2 dz2 = mul2(make_float2(vz[c], vz[c + 1]), fma2(Dv, u2, make_float2(vsy[c], vsy[c + 1])));
+                    const float2 dz2 = mul2(make_float2(vz[c], vz[c + 1]), make_float2(vy0[c], vy0[c + 1]));
                     vdu[c] = du2.x; vdu[c + 1] = du2.y;
                     vdx[c] = dx2.x; vdx[c + 1] = dx2.y;
                     vdz[c] = dz2.x; vdz[c + 1] = dz2.y;

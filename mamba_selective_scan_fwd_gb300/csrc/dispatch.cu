@@ -7,10 +7,11 @@
 
 namespace ss {
 
-// mode kModeY: the forward (summaries when K > 1, then y and last_state),
-// also storing the state at every kSub-step sub-chunk start into ckpt when
-// ckpt is given; mode kModeCkpt: the same walk writing only those states
-// (used by the backward), no y.
+// mode kModeY: the forward (summaries of the chunked segments, then y and
+// last_state), also storing the state at every kSub-step sub-chunk start into
+// ckpt and the pre-gate readout into a.y0 when ckpt is given; mode kModeCkpt:
+// the same walk writing only those states and the pre-gate readout (used by
+// the backward), no y.
 cudaError_t launch_fwd2(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt) {
     if (a.dtype == 0) return launch_fwd2_io<float>(a, p, st, mode, ckpt);
     if (a.dtype == 1) return launch_fwd2_io<__half>(a, p, st, mode, ckpt);

@@ -90,7 +90,8 @@ template <typename T, int N, int MODE>
 __global__ void __launch_bounds__(32 * fwd_warps(N), fwd_warps(N) == 2 ? 4 : 8) k_fwd2(FwdArgs a, FPlan p, int si, int64_t k_lo,
                                                                float* ckpt) {
     constexpr bool SUMMARY = MODE == kModeSummary;
-    constexpr bool NOY = MODE == kModeSummary || MODE == kModeCkpt;  // no readout, gate or y
+    constexpr bool NOY = MODE == kModeSummary;                       // no readout (a chunk summary)
+    constexpr bool GATE = MODE == kModeY || MODE == kModeYSave;      // gate and y (the checkpoint pass has neither)
     constexpr bool SAVE = MODE == kModeYSave || MODE == kModeCkpt;   // store the sub-chunk start states
     using C = FCfg<T, N>;
     constexpr int NW = C::NW, NPW = C::NPW, S = C::S, G = C::G, CH = C::CH, THREADS = C::THREADS, GRP = C::GRP,
@@ -106,7 +107,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), fwd_warps(N) == 2 ? 4 : 8) 
     __shared__ __align__(16) T sBCraw[2][C::BC_RAW ? kRow : 1][C::BC_RAW ? C::RAWP : 2];
     // raw runs of delta, u, z of the next tile, copied in asynchronously by the
     // thread that later converts them
-    __shared__ __align__(16) T sRaw[NOY ? 2 : 3][kRow][CH];
+    __shared__ __align__(16) T sRaw[GATE ? 3 : 2][kRow][CH];
     // per-warp partial readouts, one plane per lane of a pair (float g YPL + i YP
     // + c: lane g's sum over its states, step i, channel c)
     __shared__ __align__(16) float sY[NOY ? 1 : NW][NOY ? 1 : G * C::YPL];
@@ -203,7 +204,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), fwd_warps(N) == 2 ? 4 : 8) 
                     const int64_t off = (b * L + t) * Dch + d0 + cg;
                     cp_async_bytes<GRP * C::ESZ>(&sRaw[0][r][cg], delta + off);
                     cp_async_bytes<GRP * C::ESZ>(&sRaw[1][r][cg], u + off);
-                    if (!NOY && z) cp_async_bytes<GRP * C::ESZ>(&sRaw[NOY ? 1 : 2][r][cg], z + off);
+                    if (GATE && z) cp_async_bytes<GRP * C::ESZ>(&sRaw[GATE ? 2 : 1][r][cg], z + off);
                 }
             }
         }
@@ -238,12 +239,12 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), fwd_warps(N) == 2 ? 4 : 8) 
                 if (fast) {
                     lds_words<GRP * C::ESZ, RW>(&sRaw[0][r][cg], rd);
                     lds_words<GRP * C::ESZ, RW>(&sRaw[1][r][cg], ru);
-                    if (!NOY && z) lds_words<GRP * C::ESZ, RW>(&sRaw[NOY ? 1 : 2][r][cg], rz);
+                    if (GATE && z) lds_words<GRP * C::ESZ, RW>(&sRaw[GATE ? 2 : 1][r][cg], rz);
                 } else {
                     const int64_t off = (b * L + t) * Dch + d0 + cg;
                     load_run<T, GRP, RW>(delta, off, d0 + cg, Dch, false, rd);
                     load_run<T, GRP, RW>(u, off, d0 + cg, Dch, false, ru);
-                    if (!NOY && z) load_run<T, GRP, RW>(z, off, d0 + cg, Dch, false, rz);
+                    if (GATE && z) load_run<T, GRP, RW>(z, off, d0 + cg, Dch, false, rz);
                 }
             }
 #pragma unroll
@@ -256,7 +257,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), fwd_warps(N) == 2 ? 4 : 8) 
                     const float2 uu = make_float2(elem<T>(ru, c), elem<T>(ru, c + 1));
                     dlu = mul2(dl, uu);
                     if (!NOY) {
-                        if (z) {
+                        if (GATE && z) {
                             const float2 zz = make_float2(elem<T>(rz, c), elem<T>(rz, c + 1));
                             gt = mul2(zz, sigmoid2(zz));
                         }
@@ -357,7 +358,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), fwd_warps(N) == 2 ? 4 : 8) 
                 const int64_t t = t0 + r;
                 const int cg = q * GRP;
                 if (t < t_end) {
-                    float yv[GRP];
+                    float yv[GRP], y0v[GRP];
 #pragma unroll
                     for (int c = 0; c < GRP; c += 4) {
                         // per warp, the sum of its G lanes' planes; then the warps in order
@@ -377,12 +378,32 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), fwd_warps(N) == 2 ? 4 : 8) 
                         }
                         const float4 g01 = sGD[r][pair_slot<NGRP>((cg + c) / 2)];
                         const float4 g23 = sGD[r][pair_slot<NGRP>((cg + c) / 2 + 1)];
-                        yv[c] = (acc.x + g01.y) * g01.x;
-                        yv[c + 1] = (acc.y + g01.w) * g01.z;
-                        yv[c + 2] = (acc.z + g23.y) * g23.x;
-                        yv[c + 3] = (acc.w + g23.w) * g23.z;
+                        // the pre-gate readout y0 = sum_n h C + D u, then the gate
+                        y0v[c] = acc.x + g01.y;
+                        y0v[c + 1] = acc.y + g01.w;
+                        y0v[c + 2] = acc.z + g23.y;
+                        y0v[c + 3] = acc.w + g23.w;
+                        yv[c] = y0v[c] * g01.x;
+                        yv[c + 1] = y0v[c + 1] * g01.z;
+                        yv[c + 2] = y0v[c + 2] * g23.x;
+                        yv[c + 3] = y0v[c + 3] * g23.z;
                     }
-                    T* yrow = static_cast<T*>(a.y) + (b * L + t) * Dch + d0 + cg;
+                    const int64_t off = (b * L + t) * Dch + d0 + cg;
+                    if (a.y0 && z) {
+                        // kept for the backward's dz (f32; the same alignment as the io runs)
+                        float* y0row = a.y0 + off;
+                        if (fast) {
+#pragma unroll
+                            for (int c = 0; c < GRP; c += 4)
+                                *reinterpret_cast<float4*>(y0row + c) = make_float4(y0v[c], y0v[c + 1], y0v[c + 2], y0v[c + 3]);
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < GRP; c++)
+                                if (d0 + cg + c < Dch) y0row[c] = y0v[c];
+                        }
+                    }
+                    if (!GATE) continue;
+                    T* yrow = static_cast<T*>(a.y) + off;
                     if (fast) {
                         uint32_t wv[RW];
                         if constexpr (sizeof(T) == 4) {

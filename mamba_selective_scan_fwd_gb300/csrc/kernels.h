@@ -22,6 +22,10 @@ struct FwdArgs {
     // a zero start [.][CH][N] and the chunk's sum of delta_eff [.][CH]
     float* ws_fsum;
     float* ws_fsd;
+    // pre-gate readout y0 = sum_n h C + D u, f32 [Bsz][L][Dch], stored by the
+    // saving and checkpoint passes for the backward's dz when z is given
+    // (null: not stored)
+    float* y0;
 };
 
 // A[d, n] of the scan: the input itself, or -exp(A_log) in the A_log form.
@@ -41,6 +45,7 @@ struct BwdArgs {
     float* ws_rsum;
     float* ws_rsd;
     const float* ws_ckpt;  // sub-chunk start states (layout of ckpt_bytes)
+    const float* y0;       // the forward's pre-gate readout, f32 [Bsz][L][Dch]
     float* ws_bc;     // per-tile dB/dC partials: [2][tiles][Bsz][L][N]
     float* ws_dA;     // per-part dA partials: [q][CH][N]
     float* ws_dD;     // per-part dD partials: [q][CH]
@@ -253,15 +258,19 @@ cudaError_t launch_bwd2(const BwdArgs& a, const FPlan& p, cudaStream_t st, float
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
 
-// Bytes of the sub-chunk start states of every (b, d) row: the checkpoints the
-// backward recomputes from (ss_fwd_save writes them into the caller's buffer).
-// Layout: [slot t / kSub][b][channel tile][block of CH x N floats]; within
-// a block, float ((w 2 + e) 32 + lane) S + s is state n0 + s of channel c0 + e
-// of the lane (the scan kernels' lane layout), so that a warp's stores and
-// loads of one channel parity are contiguous.
-inline size_t ckpt_bytes(const FPlan& p, int64_t Bsz, int64_t Dch, int64_t N) {
-    (void)Dch;
-    return (size_t)Bsz * p.tiles_b * channels_per_block(N) * p.slots * N * sizeof(float);
+// Bytes of what the forward keeps for the backward (ss_fwd_save writes it
+// into the caller's buffer; ss_bwd's checkpoint pass into its workspace):
+// the sub-chunk start states of every (b, d) row, the checkpoints the
+// backward recomputes from, then at ckpt_y0_offset the pre-gate readout y0
+// (f32 [Bsz][L][Dch]).  States layout: [slot t / kSub][b][channel tile][block
+// of CH x N floats]; within a block, float ((w 2 + e) 32 + lane) S + s is
+// state n0 + s of channel c0 + e of the lane (the scan kernels' lane layout),
+// so that a warp's stores and loads of one channel parity are contiguous.
+inline size_t ckpt_y0_offset(const FPlan& p, int64_t Bsz, int64_t N) {
+    return align_up((size_t)Bsz * p.tiles_b * channels_per_block(N) * p.slots * N * sizeof(float), 256);
+}
+inline size_t ckpt_bytes(const FPlan& p, int64_t Bsz, int64_t L, int64_t Dch, int64_t N) {
+    return ckpt_y0_offset(p, Bsz, N) + (size_t)Bsz * L * Dch * sizeof(float);
 }
 
 // Float offset of a lane's slot for channel parity e within a saved-state block.
@@ -299,7 +308,7 @@ inline BwdLayout bwd_layout2(const FPlan& p, int64_t Bsz, int64_t L, int64_t Dch
     w.fsd = take(ch && !saved ? sc * sizeof(float) : 0);
     w.rsum = take(ch ? sc * N * sizeof(float) : 0);
     w.rsd = take(ch ? sc * sizeof(float) : 0);
-    w.ckpt = take(saved ? 0 : ckpt_bytes(p, Bsz, Dch, N));
+    w.ckpt = take(saved ? 0 : ckpt_bytes(p, Bsz, L, Dch, N));
     w.bc = take(2 * (size_t)p.tiles_b * Bsz * L * N * sizeof(float));
     w.dA = take(pc * N * sizeof(float));
     w.dD = take(pc * sizeof(float));

@@ -8,7 +8,8 @@ channel tile) are grouped into segments and cut in time.
   of one-chunk units, the second the remaining units cut in time.
 * A split never takes a problem out of the no-allocation forward: its chunk
   summaries stay within that entry point's 2 MiB scratch.
-* The saved-state buffer does not depend on the split.
+* The saved-state buffer (states, then the pre-gate readout) does not depend
+  on the split.
 """
 
 import itertools
@@ -49,7 +50,8 @@ def test_plan_segments(shape):
         assert k0 == 1 and u0 % round_of(N) == 0 and u0 > 0 and 0 < u1 < round_of(N) and k1 > 1
         assert ss.fwd_workspace_bytes(Bsz, L, Dch, N, ss.SS_BF16) <= binding.FWD_NOALLOC_MAX_SCRATCH_BYTES
     slots = -(-L // 32) * 8
-    assert ss.saved_bytes(Bsz, L, Dch, N, ss.SS_BF16) == units * tile_of(N) * slots * N * 4
+    states = -(-(units * tile_of(N) * slots * N * 4) // 256) * 256
+    assert ss.saved_bytes(Bsz, L, Dch, N, ss.SS_BF16) == states + Bsz * L * Dch * 4  # states, then y0
 
 
 def test_split_appears_for_a_partial_round():
