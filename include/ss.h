@@ -110,9 +110,12 @@ int ss_fwd_noalloc(const void *u, const void *delta, const float *A, const void 
  * `selective_scan.rs`, "Workspace": B * D * L * N elements written by the
  * backward's first pass); here the forward keeps one state in four steps.
  *   saved         device buffer of at least ss_saved_bytes(...) bytes, 16-byte
- *                 aligned, fully overwritten (f32 h of every (b, d) row at
- *                 every 4th step of L rounded up to 32 steps); opaque to the
- *                 caller.
+ *                 aligned; opaque to the caller.  It receives the f32 state h
+ *                 of every (b, d) row at every 4th step of L rounded up to 32
+ *                 steps and, when z is given, the f32 pre-gate readout
+ *                 sum_n h C + D u of every (b, t, d) (which the backward's dz
+ *                 needs); without z that last part is left unwritten and
+ *                 never read.
  * All other arguments and results are those of ss_fwd.  A NULL or short
  * `saved` gives SS_ERR_WORKSPACE_TOO_SMALL before anything is launched.
  */
