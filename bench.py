@@ -66,10 +66,10 @@ def algorithmic_bytes(w):
 # figure stale, and it is reported as null.
 TRAFFIC = {
     # both launches of the main pass (608 one-chunk units; 32 units x 19 chunks)
-    ("k_bwd2_main", "mamba2.8b-layer-bf16"): 3285449984,  # 1915.1 + 102.3 MB read, 1238.4 + 29.6 MB written
-    ("k_fwd2_y", "mamba2.8b-layer-bf16"): 1896813056,     # 479.7 + 26.8 MB read, 1373.0 + 17.3 MB written
+    ("k_bwd2_main", "mamba2.8b-layer-bf16"): 3626531840,  # 2233.1 + 119.1 MB read, 1241.9 + 32.5 MB written
+    ("k_fwd2_y", "mamba2.8b-layer-bf16"): 2228594176,     # 479.8 + 26.8 MB read, 1690.9 + 31.1 MB written
 }
-TRAFFIC_SRC_DIGEST = "0e5a3859876d5be9"
+TRAFFIC_SRC_DIGEST = "e8647069318ce25c"
 
 
 def measured_traffic(kernel, w):
@@ -382,14 +382,20 @@ def run_ours(args):
 
     e2e_run(2)
     torch.cuda.synchronize(dev)
-    barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    e2e_run(e2e_steps, start_ev=e0)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    # three timed runs of e2e_steps steps: the host link is shared with other
+    # work on the machine and its throughput varies from run to run (seen: 2x),
+    # so the median is reported and every run is listed
+    e2e_runs = []
+    for _ in range(3):
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        e2e_run(e2e_steps, start_ev=e0)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e2e_runs.append(max_over_ranks(e0.elapsed_time(e1), world))
+    e2e_ms = sorted(e2e_runs)[1]
     e2e_value = job_throughput(w.bld * e2e_steps, world, e2e_ms)
 
     # ---- roofline of the dominant kernel (the backward's main kernel) and of the forward kernel
@@ -454,7 +460,8 @@ def run_ours(args):
         "fwd_ms": round(t_fwd, 4), "bwd_ms": round(t_bwd, 4), "kernel_ms": kernel_ms,
         "clocks": clk,
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": e2e_steps},
+                "steps": e2e_steps, "runs": [round(job_throughput(w.bld * e2e_steps, world, v), 1) for v in e2e_runs],
+                "of_runs": "median"},
         "gpu_launches": K * (plan["fwd_kernels"] + plan["bwd_saved_kernels"]),  # the timed region only
     }
     if not args.no_decode:
