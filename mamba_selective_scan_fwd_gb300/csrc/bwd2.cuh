@@ -514,7 +514,7 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
             // the chunk end (last tile only) hold Delta = g = 0 and B = C = 0 in the
             // staging: they leave the state and the adjoint unchanged and add
             // nothing; only their per-step stores are skipped.
-#pragma unroll 1
+#pragma unroll
             for (int sub = kTT / kSub - 1; sub >= 0; sub--) {
                 const int64_t ts = t0 + sub * kSub;
                 if (ts >= t_end) continue;
