@@ -18,7 +18,8 @@
 // and one time chunk; for N >= 16 two warps split the states of every
 // channel):
 //   * the forward (ss_fwd_save) or a checkpoint pass stores the state at the
-//     start of every kSub-step sub-chunk;
+//     start of every kSub-step sub-chunk, and the pre-gate readout y0 that
+//     dz needs;
 //   * this kernel visits kTT-step tiles from the end of the chunk backwards.
 //     The tile prologue computes the per-(t, d) terms once (softplus and its
 //     derivative, the gate, g, the dz factor) into shared memory; then each
@@ -27,10 +28,10 @@
 //   * per step each lane stores its two channels' partial sums over its
 //     states, and each warp sums dB / dC of its states over the block's
 //     channels through shared memory in a fixed order; the tile epilogue
-//     adds the lanes' and warps' per-(t, d) sums and writes du, ddelta, dz; a second
-//     kernel adds the per-tile dB / dC partials, a third the per-(batch,
-//     chunk) dA / dD / ddelta_bias partials.  Every sum has a fixed order:
-//     the result is bit-reproducible.
+//     adds the lanes' and warps' per-(t, d) sums, takes y0 from the forward,
+//     and writes du, ddelta, dz; a second kernel adds the per-tile dB / dC
+//     partials, a third the per-(unit, chunk) dA / dD / ddelta_bias
+//     partials.  Every sum has a fixed order: the result is bit-reproducible.
 // Chunks (units the plan cuts in time, kernels.h): each chunk's carry-in
 // state is its first saved state; reverse summaries (P_k, M_k) -- the chunk's
 // decay product, from its sum of delta_eff as exp(A sum delta_eff), and
