@@ -238,10 +238,6 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
     // raw runs of delta, u, dy, z of the next tile, copied in asynchronously by
     // the thread that later converts them
     __shared__ __align__(16) T sRaw[4][kTT][CH];
-    // per-(t, d) terms only the epilogue reads, channel fastest: u, sig(x), dz factor
-    __shared__ __align__(16) float sEu[MAIN ? kTT : 1][MAIN ? EP : 4];
-    __shared__ __align__(16) float sEs[MAIN ? kTT : 1][MAIN ? EP : 4];
-    __shared__ __align__(16) float sEz[MAIN ? kTT : 1][MAIN ? EP : 4];
     // dB / dC contributions of kRB steps, per warp: block (j, tau) holds a row of NPW floats per pair
     __shared__ __align__(16) float sR[MAIN ? NW : 1][MAIN ? kRB * 2 * BLK : 4];
     // per-step sums over a lane's states: sum lam B, sum A q, one plane per
@@ -407,6 +403,9 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
         const int64_t t0 = t_begin + m * kTT;
         const int buf = (int)(m & 1);
         cp_async_wait<0>();  // this thread's copies of the tile
+        // per-(t, d) terms of the thread's own items that its epilogue needs
+        // again (Delta, g, u, sig(delta + bias), the dz factor): kept in registers
+        float kDl[ITEMS][GRP], kG[ITEMS][GRP], kU[ITEMS][GRP], kS[ITEMS][GRP], kZ[ITEMS][GRP];
         // ---- prologue: (step, 4-channel group) items of the tile
 #pragma unroll
         for (int it = 0; it < ITEMS; it++) {
@@ -466,10 +465,13 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                 sDU[r][slot] = make_float4(dl[c], dlu[c], dl[c + 1], dlu[c + 1]);
                 sG[r][slot] = make_float2(gg[c], gg[c + 1]);
             }
-            if (MAIN) {
-                *reinterpret_cast<float4*>(&sEu[r][cg]) = make_float4(uu[0], uu[1], uu[2], uu[3]);
-                *reinterpret_cast<float4*>(&sEs[r][cg]) = make_float4(sgx[0], sgx[1], sgx[2], sgx[3]);
-                *reinterpret_cast<float4*>(&sEz[r][cg]) = make_float4(dzf[0], dzf[1], dzf[2], dzf[3]);
+#pragma unroll
+            for (int c = 0; c < GRP; c++) {
+                kDl[it][c] = dl[c];
+                kG[it][c] = gg[c];
+                kU[it][c] = uu[c];
+                kS[it][c] = sgx[c];
+                kZ[it][c] = dzf[c];
             }
         }
         if constexpr (!C::BC_DIRECT) {
@@ -681,15 +683,12 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
                         for (int c = 0; c < GRP; c++) vy0[c] = d0 + cg + c < Dch ? y0r[c] : 0.f;
                     }
                 }
-                const float4 dua = sDU[r][bpair_slot<PAIRS>(cg / 2)], dub = sDU[r][bpair_slot<PAIRS>(cg / 2 + 1)];
-                const float2 gga = sG[r][bpair_slot<PAIRS>(cg / 2)], ggb = sG[r][bpair_slot<PAIRS>(cg / 2 + 1)];
-                const float4 u4 = *reinterpret_cast<const float4*>(&sEu[r][cg]);
-                const float4 s4 = *reinterpret_cast<const float4*>(&sEs[r][cg]);
-                const float4 z4 = *reinterpret_cast<const float4*>(&sEz[r][cg]);
                 const float vsu[4] = {su.x, su.y, su.z, su.w}, vsd[4] = {sd.x, sd.y, sd.z, sd.w};
-                const float vdl[4] = {dua.x, dua.z, dub.x, dub.z}, vg[4] = {gga.x, gga.y, ggb.x, ggb.y};
-                const float vu[4] = {u4.x, u4.y, u4.z, u4.w}, vs[4] = {s4.x, s4.y, s4.z, s4.w},
-                            vz[4] = {z4.x, z4.y, z4.z, z4.w};
+                const float(&vdl)[GRP] = kDl[it];
+                const float(&vg)[GRP] = kG[it];
+                const float(&vu)[GRP] = kU[it];
+                const float(&vs)[GRP] = kS[it];
+                const float(&vz)[GRP] = kZ[it];
                 float vdu[GRP], vdx[GRP], vdz[GRP];
 #pragma unroll
                 for (int c = 0; c < GRP; c += 2) {
