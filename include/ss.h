@@ -27,6 +27,9 @@
  * was enqueued; a fault during execution surfaces at the caller's next
  * synchronisation.  Inputs are read only; outputs are fully overwritten (no
  * caller zeroing is needed); input and output ranges must not overlap.
+ * Calls may come from several host threads and devices at once: a call's
+ * state lives in its arguments and workspace, except the library-owned
+ * scratch of ss_fwd_noalloc (see there).
  *
  * Errors are reported before anything is launched; nothing is written then.
  * Results are deterministic: the same arguments on the same GPU give
@@ -196,16 +199,17 @@ int ss_plan_segments(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype, 
                      int64_t *chunks);
 
 /*
- * Measurement aid (not thread-safe; for benchmarks).  After a call with
- * count > 0, every call of ss_fwd, ss_fwd_save, ss_fwd_ex, ss_bwd,
- * ss_bwd_saved or ss_bwd_ex that
- * returns SS_OK records events[0] on its stream before its first kernel,
- * events[i] after its i-th kernel (in the order ss_plan_info counts them),
- * stopping when the list is used up; the list stays set for later calls.
- * events[] holds up to 16 caller-created cudaEvent_t handles (passed as
- * void*) of the calling thread's current device.  count = 0 switches the
- * recording off.  Returns SS_ERR_INVALID_PROBLEM for count outside 0..16 or
- * a NULL handle.  The pages this library follows have no counterpart.
+ * Measurement aid (for benchmarks).  After a call with count > 0, every
+ * call of ss_fwd, ss_fwd_save, ss_fwd_ex, ss_bwd, ss_bwd_saved or ss_bwd_ex
+ * made from the same host thread that returns SS_OK records events[0] on its
+ * stream before its first kernel, events[i] after its i-th kernel (in the
+ * order ss_plan_info counts them), stopping when the list is used up; the
+ * list stays set for later calls.  events[] holds up to 16 caller-created
+ * cudaEvent_t handles (passed as void*) of the calling thread's current
+ * device.  count = 0 switches the recording off.  The list is per host
+ * thread: calls from other threads record nothing.  Returns
+ * SS_ERR_INVALID_PROBLEM for count outside 0..16 or a NULL handle.  The
+ * pages this library follows have no counterpart.
  */
 int ss_profile_events(void *const *events, int count);
 

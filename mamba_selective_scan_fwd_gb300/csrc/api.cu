@@ -31,11 +31,12 @@ int check_sizes(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype) {
     return SS_OK;
 }
 
-// ss_profile_events state: the caller's events and the next one to record.
+// ss_profile_events state: the caller's events and the next one to record,
+// per host thread (a list set by one thread applies to that thread's calls).
 constexpr int kMaxProfEvents = 16;
-cudaEvent_t g_prof_ev[kMaxProfEvents];
-int g_prof_n = 0;
-int g_prof_next = 0;
+thread_local cudaEvent_t g_prof_ev[kMaxProfEvents];
+thread_local int g_prof_n = 0;
+thread_local int g_prof_next = 0;
 
 // Forward with optional restart-state output (save == false: plain forward),
 // initial state h0 (nullable) and the A_log form.

@@ -39,6 +39,8 @@
 // rho_{k-1} = M_k + P_k rho_k into each chunk's carry-in adjoint.
 #pragma once
 
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "simd.cuh"
@@ -774,6 +776,24 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), BCfg<T, N>::MINB) k_bwd2(Bw
         }
     }
 }
+// Ask for the largest shared-memory carveout for `kernel`, so that shared
+// memory does not cap residency: once per device (a kernel attribute of the
+// current device, not a stream operation, so that calls captured into a CUDA
+// graph after a first eager call on that device make no such call).  `done`
+// holds one bit per device ordinal; threads that race both set it.
+template <typename K>
+cudaError_t prefer_max_shared(K kernel, std::atomic<uint64_t>& done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev >= 0 && dev < 64 ? uint64_t(1) << dev : 0;
+    if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
+
 template <typename T, int N>
 cudaError_t launch_bwd2_t(const BwdArgs& a, const FPlan& p, cudaStream_t st, float* ckpt_out) {
     cudaError_t e = cudaSuccess;
@@ -793,17 +813,10 @@ cudaError_t launch_bwd2_t(const BwdArgs& a, const FPlan& p, cudaStream_t st, flo
     }
     const bool state = a.dlast != nullptr || a.dh0 != nullptr;
     auto main_kernel = state ? k_bwd2<T, N, kRevMain, true> : k_bwd2<T, N, kRevMain, false>;
-    // prefer the largest shared-memory carveout so that shared memory does not cap
-    // residency; set once per kernel (a process-wide attribute, not a stream
-    // operation), so that calls recorded in a CUDA graph after a first eager
-    // call make no such call
-    static bool carveout_set[2] = {false, false};
-    if (!carveout_set[state]) {
-        e = cudaFuncSetAttribute(main_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 (int)cudaSharedmemCarveoutMaxShared);
-        if (e != cudaSuccess) return e;
-        carveout_set[state] = true;
-    }
+    // one bit per device ordinal: the carveout preference is set on that device
+    static std::atomic<uint64_t> carveout_done[2] = {{0}, {0}};
+    e = prefer_max_shared(main_kernel, carveout_done[state]);
+    if (e != cudaSuccess) return e;
     for (int si = 0; si < p.nseg; si++) {
         prof_mark(st);
         main_kernel<<<(unsigned)(p.seg[si].nu * p.seg[si].K), threads, 0, st>>>(a, p, si, 0);
