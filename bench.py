@@ -51,8 +51,11 @@ def pick_workload(name):
 # The small per-(b, t, n) and per-(d, n) terms are added exactly below.
 
 
+IO_BYTES = {"f32": 4, "bf16": 2, "f16": 2}
+
+
 def algorithmic_bytes(w):
-    e = 2 if w.io == "bf16" else 4
+    e = IO_BYTES[w.io]
     bld, bln, dn, d = w.Bsz * w.L * w.Dch, w.Bsz * w.L * w.N, w.Dch * w.N, w.Dch
     fwd = 4 * bld * e + 2 * bln * e + 4 * (dn + 2 * d) + 4 * w.Bsz * w.Dch * w.N
     bwd = 4 * bld * e + 3 * bld * 4 + 2 * bln * (e + 4) + 8 * (dn + 2 * d)

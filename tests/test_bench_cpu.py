@@ -1,0 +1,66 @@
+"""bench.py's host arithmetic on CPU: the algorithmic bytes that the roofline
+fractions divide by, the whole-job throughput, and the rule that a DRAM
+traffic figure is reported only for the kernel sources it was measured on.
+
+The byte counts are pinned to the per-element rule of the hot path (bf16:
+u, delta, z read and y written, 8 B per B*L*D element forward; u, delta, z,
+dy read as bf16 and du, ddelta, dz written as f32, 20 B backward) plus the
+per-(b, t, n) and per-(d, n) terms, written out here for the headline sizes
+as plain integers (rounded: 673.8 MB forward, 1681.6 MB backward).
+"""
+
+import pytest
+
+import bench
+from mamba_selective_scan_fwd_gb300 import build
+from mamba_selective_scan_fwd_gb300.inputs import Workload
+
+
+def test_headline_algorithmic_bytes():
+    w = bench.pick_workload("mamba2.8b-layer-bf16")
+    assert (w.Bsz, w.L, w.Dch, w.N, w.io) == (4, 4096, 5120, 16, "bf16")
+    fwd, bwd = bench.algorithmic_bytes(w)
+    # 83,886,080 elements; B, C rows 262,144 values each; A 81,920; D and bias 5,120 each; last_state 327,680
+    assert fwd == 8 * 83_886_080 + 2 * 2 * 262_144 + 4 * (81_920 + 2 * 5_120) + 4 * 327_680 == 673_816_576
+    # backward: B, C read (io) and dB, dC written (f32); A, D, bias read and dA, dD, dbias written (f32)
+    assert bwd == 20 * 83_886_080 + 2 * 262_144 * (2 + 4) + 8 * (81_920 + 2 * 5_120) == 1_681_604_608
+    assert round(fwd / 1e6, 1) == 673.8 and round(bwd / 1e6, 1) == 1681.6
+
+
+@pytest.mark.parametrize("io,e", [("f32", 4), ("bf16", 2), ("f16", 2)])
+def test_io_element_size(io, e):
+    w = Workload("probe", 1, 10, 3, 2, io)
+    fwd, bwd = bench.algorithmic_bytes(w)
+    bld, bln, small = 30, 20, 2 * 3 + 3 * 2
+    assert fwd == 4 * bld * e + 2 * bln * e + 4 * small + 4 * 1 * 3 * 2
+    assert bwd == 4 * bld * e + 12 * bld + 2 * bln * (e + 4) + 8 * small
+
+
+def test_job_throughput_is_all_ranks_over_the_slowest():
+    # 3 ranks of 1e6 units each, the slowest took 2 ms
+    assert bench.job_throughput(1e6, 3, 2.0) == pytest.approx(1.5e9)
+
+
+def test_traffic_reported_only_for_its_sources(monkeypatch):
+    w = bench.pick_workload("mamba2.8b-layer-bf16")
+    monkeypatch.setattr(build, "source_digest", lambda: bench.TRAFFIC_SRC_DIGEST)
+    assert bench.measured_traffic("k_bwd2_main", w) == bench.TRAFFIC[("k_bwd2_main", w.name)]
+    assert bench.measured_traffic("k_fwd2_y", w) == bench.TRAFFIC[("k_fwd2_y", w.name)]
+    assert bench.measured_traffic("k_bwd2_main", bench.pick_workload("long-seq-bf16")) is None
+    monkeypatch.setattr(build, "source_digest", lambda: "0" * 16)
+    assert bench.measured_traffic("k_bwd2_main", w) is None
+
+
+def test_traffic_figures_are_plausible():
+    """DRAM bytes of a main pass are at least its algorithmic bytes (the saved
+    states and partials come on top) and within a few times of them."""
+    w = bench.pick_workload("mamba2.8b-layer-bf16")
+    fwd, bwd = bench.algorithmic_bytes(w)
+    bwd_main = bwd - 2 * w.Bsz * w.L * w.N * 4 - 4 * (w.Dch * w.N + 2 * w.Dch)
+    assert bwd_main <= bench.TRAFFIC[("k_bwd2_main", w.name)] <= 3 * bwd_main
+    assert fwd <= bench.TRAFFIC[("k_fwd2_y", w.name)] <= 4 * fwd
+
+
+def test_unknown_workload_exits():
+    with pytest.raises(SystemExit):
+        bench.pick_workload("no-such-workload")
