@@ -22,9 +22,11 @@
 //     dz needs;
 //   * this kernel visits kTT-step tiles from the end of the chunk backwards.
 //     The tile prologue computes the per-(t, d) terms once (softplus and its
-//     derivative, the gate, g, the dz factor) into shared memory; then each
-//     sub-chunk is recomputed forward from its saved state, keeping its
-//     states and decays in registers, and the adjoint walks it backwards;
+//     derivative, the gate, g, the dz factor): the walk's (delta_eff,
+//     delta_eff * u, g) go to shared memory, and the thread keeps its items'
+//     terms in registers for its own epilogue; then each sub-chunk is
+//     recomputed forward from its saved state, keeping its states and decays
+//     in registers, and the adjoint walks it backwards;
 //   * per step each lane stores its two channels' partial sums over its
 //     states, and each warp sums dB / dC of its states over the block's
 //     channels through shared memory in a fixed order; the tile epilogue
@@ -90,7 +92,7 @@ struct BCfg {
     static constexpr int BLK = PAIRS * NPW + 8;
     // blocks per SM the register budget must allow: one round of the plan on
     // every SM (8 warps: 4 two-warp or 8 one-warp blocks), which leaves the
-    // scan up to 255 registers (N = 16 takes about 230 and runs 6 % faster
+    // scan up to 255 registers (N = 16 takes 237 and about 20 % less time
     // than at 168)
     static constexpr int MINB = NW == 2 ? 4 : 8;
     static_assert(kTT * NGRP % THREADS == 0, "whole items per thread");

@@ -21,8 +21,14 @@
 //             f32x2 arithmetic (one MUFU ex2 per state per step) and stores
 //             its two channels' partial readouts per step;
 //   epilogue  threads take (step, 8-channel group) items again: add the
-//             lanes' and warps' partial readouts, D * u, apply the gate and
-//             store the group's run of y.
+//             lanes' and warps' partial readouts and D * u (the pre-gate
+//             readout y0, stored as f32 for the backward's dz when the
+//             states are saved and z is given), apply the gate and store
+//             the group's run of y.
+// Modes: Y (y, last_state), YSave (also the state at every kSub-step
+// sub-chunk start and y0), Ckpt (the backward's checkpoint pass: the states
+// and y0 only, no gate and no y), Summary (a chunk's end state and sum of
+// delta_eff, no readout).
 // The time axis of a unit (batch row, channel tile) is cut into K chunks when
 // the plan says so (kernels.h); a chunk summary -- its end state H from a zero
 // start and its sum of delta_eff, which gives the product of its decays
