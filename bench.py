@@ -62,6 +62,16 @@ def algorithmic_bytes(w):
     return fwd, bwd
 
 
+def mufu_counts(w):
+    """MUFU operations of one call of each direction on workload w (softplus on,
+    z given): the scan's ex2 per (t, d, n), which the roofline counts, and all
+    of them -- per (t, d) the forward's softplus (ex2, rcp) and gate sigmoid
+    (ex2, rcp), the backward's softplus with its derivative (ex2, two rcp) and
+    gate sigmoid (ex2, rcp).  The chunk summaries of time-cut units, which
+    walk their decays once more, are not counted."""
+    return {"scan_ex2_per_direction": w.bld * w.N, "fwd_all": w.bld * (w.N + 4), "bwd_all": w.bld * (w.N + 5)}
+
+
 # DRAM bytes (read + write) of the timed kernels' main passes on this workload
 # (the sum over the launches of one pass: one per plan segment), from one ncu
 # capture (profiles/ holds the summaries and the commands), and the digest of
@@ -459,7 +469,7 @@ def run_ours(args):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "hbm_gbs": round((fwd_bytes + bwd_bytes) / (ms_per_step / 1e3) / 1e9, 1),
         "roofline": r_bwd, "roofline_fwd": r_fwd,
-        "roofline_step_frac": round(t_roof / ms_per_step, 4),
+        "roofline_step_frac": round(t_roof / ms_per_step, 4), "mufu_ops": mufu_counts(w),
         "fwd_ms": round(t_fwd, 4), "bwd_ms": round(t_bwd, 4), "kernel_ms": kernel_ms,
         "clocks": clk,
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

@@ -64,3 +64,11 @@ def test_traffic_figures_are_plausible():
 def test_unknown_workload_exits():
     with pytest.raises(SystemExit):
         bench.pick_workload("no-such-workload")
+
+
+def test_mufu_counts():
+    w = bench.pick_workload("mamba2.8b-layer-bf16")
+    m = bench.mufu_counts(w)
+    # 83,886,080 (t, d) elements x 16 states: the 1.342 G exponentials of each direction's scan
+    assert m["scan_ex2_per_direction"] == 1_342_177_280
+    assert m["fwd_all"] == 83_886_080 * 20 and m["bwd_all"] == 83_886_080 * 21
