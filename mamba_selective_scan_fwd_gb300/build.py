@@ -22,8 +22,8 @@ LIB = os.path.join(PKG, "libss.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
-SOURCES = ["api.cu", "dispatch.cu", "fwd2_f32.cu", "fwd2_bf16.cu", "fwd2_f16.cu", "bwd2_f32.cu",
-           "bwd2_bf16.cu", "bwd2_f16.cu", "decode.cu", "fwd_noalloc.cu"]
+SOURCES = ["api.cu", "dispatch.cu", "fwd_f32.cu", "fwd_bf16.cu", "fwd_f16.cu", "bwd_f32.cu",
+           "bwd_bf16.cu", "bwd_f16.cu", "decode.cu", "fwd_noalloc.cu"]
 
 
 def nvcc() -> str:

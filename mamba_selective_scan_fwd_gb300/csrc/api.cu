@@ -83,7 +83,7 @@ int fwd_impl(const void* u, const void* delta, const float* A, const void* B, co
     a.ws_fsd = workspace ? reinterpret_cast<float*>(static_cast<char*>(workspace) + fsum_offset_sd(p, N)) : nullptr;
     float* ck = save ? static_cast<float*>(saved) : nullptr;
     a.y0 = save ? reinterpret_cast<float*>(static_cast<char*>(saved) + ckpt_y0_offset(p, Bsz, N)) : nullptr;
-    return launch_fwd2(a, p, st, kModeY, ck) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+    return launch_fwd(a, p, st, kModeY, ck) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
 // Backward; with from_saved the restart states come from ss_fwd_save /
@@ -168,7 +168,7 @@ int bwd_impl(const void* u, const void* delta, const float* A, const void* B, co
     a.ws_dA = reinterpret_cast<float*>(ws + w.dA);
     a.ws_dD = reinterpret_cast<float*>(ws + w.dD);
     a.ws_db = reinterpret_cast<float*>(ws + w.db);
-    return launch_bwd2(a, p, st, ckpt_out) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+    return launch_bwd(a, p, st, ckpt_out) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
 // An entry point's launches between prof_begin and prof_end.

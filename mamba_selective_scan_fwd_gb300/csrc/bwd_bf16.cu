@@ -1,6 +1,6 @@
 // Backward kernels for bf16 io (one translation unit per io type, compiled in parallel).
-#include "bwd2.cuh"
+#include "bwd.cuh"
 
 namespace ss {
-template cudaError_t launch_bwd2_io<__nv_bfloat16>(const BwdArgs&, const FPlan&, cudaStream_t, float*);
+template cudaError_t launch_bwd_io<__nv_bfloat16>(const BwdArgs&, const FPlan&, cudaStream_t, float*);
 }  // namespace ss

@@ -1,5 +1,5 @@
 // Launch dispatch on the io type (the kernels of each io type live in their
-// own translation unit: fwd2_*.cu, bwd2_*.cu), and the two backward
+// own translation unit: fwd_*.cu, bwd_*.cu), and the two backward
 // reduction kernels, which do not depend on it.
 #include "common.cuh"
 #include "kernels.h"
@@ -8,39 +8,39 @@
 namespace ss {
 
 // mode kModeY: the forward (summaries of the chunked segments, then y and
-// last_state), also storing the state at every kSub-step sub-chunk start into
-// ckpt and the pre-gate readout into a.y0 when ckpt is given; mode kModeCkpt:
+// last_state), also storing the state entering every kSub-th step into ckpt
+// and the pre-gate readout into a.y0 when ckpt is given; mode kModeCkpt:
 // the same walk writing only those states and the pre-gate readout (used by
 // the backward), no y.
-cudaError_t launch_fwd2(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt) {
-    if (a.dtype == 0) return launch_fwd2_io<float>(a, p, st, mode, ckpt);
-    if (a.dtype == 1) return launch_fwd2_io<__half>(a, p, st, mode, ckpt);
-    return launch_fwd2_io<__nv_bfloat16>(a, p, st, mode, ckpt);
+cudaError_t launch_fwd(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt) {
+    if (a.dtype == 0) return launch_fwd_io<float>(a, p, st, mode, ckpt);
+    if (a.dtype == 1) return launch_fwd_io<__half>(a, p, st, mode, ckpt);
+    return launch_fwd_io<__nv_bfloat16>(a, p, st, mode, ckpt);
 }
 
-__global__ void k_bwd2_reduce_bc(BwdArgs a, FPlan p);
-__global__ void k_bwd2_reduce_params(BwdArgs a, FPlan p);
+__global__ void k_bwd_reduce_bc(BwdArgs a, FPlan p);
+__global__ void k_bwd_reduce_params(BwdArgs a, FPlan p);
 
 // The backward's scan kernels (io-typed), then the two reductions.
-cudaError_t launch_bwd2(const BwdArgs& a, const FPlan& p, cudaStream_t st, float* ckpt_out) {
+cudaError_t launch_bwd(const BwdArgs& a, const FPlan& p, cudaStream_t st, float* ckpt_out) {
     cudaError_t e;
-    if (a.f.dtype == 0) e = launch_bwd2_io<float>(a, p, st, ckpt_out);
-    else if (a.f.dtype == 1) e = launch_bwd2_io<__half>(a, p, st, ckpt_out);
-    else e = launch_bwd2_io<__nv_bfloat16>(a, p, st, ckpt_out);
+    if (a.f.dtype == 0) e = launch_bwd_io<float>(a, p, st, ckpt_out);
+    else if (a.f.dtype == 1) e = launch_bwd_io<__half>(a, p, st, ckpt_out);
+    else e = launch_bwd_io<__nv_bfloat16>(a, p, st, ckpt_out);
     if (e != cudaSuccess) return e;
     const int64_t n_bc = 2 * a.f.Bsz * a.f.L * a.f.N / (a.f.N % 4 == 0 ? 4 : 1);  // threads
     prof_mark(st);
-    k_bwd2_reduce_bc<<<(unsigned)ceil_div(n_bc, 256), 256, 0, st>>>(a, p);
+    k_bwd_reduce_bc<<<(unsigned)ceil_div(n_bc, 256), 256, 0, st>>>(a, p);
     const int64_t n_par = a.f.Dch * a.f.N;
     prof_mark(st);
-    k_bwd2_reduce_params<<<(unsigned)ceil_div(n_par, 256), 256, 0, st>>>(a, p);
+    k_bwd_reduce_params<<<(unsigned)ceil_div(n_par, 256), 256, 0, st>>>(a, p);
     return cudaGetLastError();
 }
 
 // dB / dC: sum of the per-tile partials, tiles in ascending order.  A thread
 // owns 4 consecutive outputs (16-byte streaming loads, 8 tiles in flight)
 // when N is a multiple of 4, one output otherwise.
-__global__ void k_bwd2_reduce_bc(BwdArgs a, FPlan p) {
+__global__ void k_bwd_reduce_bc(BwdArgs a, FPlan p) {
     const int64_t bln = a.f.Bsz * a.f.L * a.f.N;
     const int64_t tiles = p.tiles_b;
     if (a.f.N % 4 == 0) {
@@ -80,7 +80,7 @@ __global__ void k_bwd2_reduce_bc(BwdArgs a, FPlan p) {
 
 // dA / dD / ddelta_bias: sum over the parts of each channel -- batch rows
 // ascending, and within a row the chunks of its unit ascending.
-__global__ void k_bwd2_reduce_params(BwdArgs a, FPlan p) {
+__global__ void k_bwd_reduce_params(BwdArgs a, FPlan p) {
     const int64_t Dch = a.f.Dch, N = a.f.N, CH = channels_per_block(N);
     const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (e >= Dch * N) return;

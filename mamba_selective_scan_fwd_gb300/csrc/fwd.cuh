@@ -6,29 +6,34 @@
 //
 // One block owns CH channels of one batch row and one time chunk (the block
 // layout of kernels.h): lane (p, g) of warp w holds S states of the channel
-// pair p, the states n0 = w N/NW + g S .. n0 + S of both channels.  The
-// layout spends the SM's shared-memory / L1 data pipe sparingly: every B / C
-// value a lane reads from shared memory serves two channels, and one 16-byte
-// load brings delta_eff and delta_eff * u of both; each lane stores its two
-// channels' partial readouts with one 8-byte store.
+// pair p, the states n0 = w NPW + g S .. n0 + S of both channels.
+//
+// The scan is bound by the SM's FP32 pipe and its MUFU together: per state
+// and step it needs one ex2 and four FP32 operations (the exponent, the
+// input term, the recurrence, the readout), and both units run at 32 such
+// (t, d, n) elements per clock on an SM.  So every FP32 operation of the
+// scan is a packed f32x2 instruction whose two halves are the lane's two
+// channels at one state: delta_eff, delta_eff * u and the readout of both
+// channels come and go as natural register pairs, and the B / C value of
+// the state is the same scalar in both halves (a broadcast operand, which
+// costs no instruction).  A lane's partial readout of one step is then one
+// 8-byte store of both channels.
 // Work per 32-step tile:
-//   prologue  threads take (step, 8-channel group) items: load the group's
-//             runs of u, delta, z (whole 16-byte vectors, four items per
-//             64-byte row of the tile), compute delta_eff, delta_eff * u,
-//             silu(z) and D * u once per (t, d) into shared memory; other
-//             items copy the B and C rows of the tile;
-//   scan      each lane walks the 32 steps for its 2 x S states with packed
-//             f32x2 arithmetic (one MUFU ex2 per state per step) and stores
-//             its two channels' partial readouts per step;
-//   epilogue  threads take (step, 8-channel group) items again: add the
-//             lanes' and warps' partial readouts and D * u (the pre-gate
-//             readout y0, stored as f32 for the backward's dz when the
-//             states are saved and z is given), apply the gate and store
-//             the group's run of y.
-// Modes: Y (y, last_state), YSave (also the state at every kSub-step
-// sub-chunk start and y0), Ckpt (the backward's checkpoint pass: the states
-// and y0 only, no gate and no y), Summary (a chunk's end state and sum of
-// delta_eff, no readout).
+//   prologue  threads take (step, 8-channel group) items: the group's runs
+//             of delta, u, z (copied in with the previous tile), delta_eff,
+//             delta_eff * u, the gate and D * u of each channel pair into
+//             shared memory; the B / C rows of the tile become f32 rows;
+//   scan      each lane walks the 32 steps for its 2 x S states, storing the
+//             state entering every kSub-th step when the states are kept
+//             for the backward;
+//   epilogue  the (step, 8-channel group) items add the lanes' and warps'
+//             partial readouts and D * u (the pre-gate readout y0, stored
+//             as f32 for the backward's dz when the states are kept and z
+//             is given), apply the gate and store the group's run of y.
+// Modes: Y (y, last_state), YSave (also the states entering every kSub-th
+// step and y0), Ckpt (the backward's checkpoint pass: the states and y0, no
+// gate and no y), Summary (a chunk's end state and sum of delta_eff, no
+// readout).
 // The time axis of a unit (batch row, channel tile) is cut into K chunks when
 // the plan says so (kernels.h); a chunk summary -- its end state H from a zero
 // start and its sum of delta_eff, which gives the product of its decays
@@ -43,15 +48,15 @@
 
 namespace ss {
 
-constexpr int kRow = 32;  // time steps per tile
-static_assert(kRow % kSub == 0, "a tile holds whole checkpoint sub-chunks");
+constexpr int kRow = 32;  // time steps per forward tile
+static_assert(kRow % kSub == 0, "a tile holds whole save intervals");
 
 template <typename T, int N>
 struct FCfg {
-    static constexpr int NW = fwd_warps(N);         // warps per block (they split the states)
+    static constexpr int NW = scan_warps(N);        // warps per block (they split the states)
     static constexpr int NPW = N / NW;              // states per warp
-    static constexpr int G = NPW >= 2 ? 2 : 1;      // lanes per channel pair
-    static constexpr int S = NPW / G;               // states per lane (of each of its two channels)
+    static constexpr int S = lane_states(N);        // states per lane (of each of its two channels)
+    static constexpr int G = NPW / S;               // lanes per channel pair
     static constexpr int PAIRS = 32 / G;            // channel pairs per block
     static constexpr int CH = 2 * PAIRS;            // channels per block
     static constexpr int THREADS = 32 * NW;
@@ -62,54 +67,46 @@ struct FCfg {
     static constexpr int RW = GRP * ESZ / 4;        // 32-bit words of an item's run of one tensor
     static constexpr int NB = N * ESZ;              // bytes of a B / C row
     static constexpr int NWd = NB >= 4 ? NB / 4 : 1;  // 32-bit words per B / C row
-    // B / C staging: a step's row holds N / S state groups of 2 S floats (S of
-    // B, then S of C), padded by 4 floats so that rows staged by consecutive
-    // threads start in different bank groups.  f32 io is copied straight into
-    // it (double buffered); bf16 rows are copied raw and converted once.
+    // f32 B / C staging: a step's row is the N values of B, then the N of C,
+    // padded by 4 floats.  f32 io is copied straight into it (double
+    // buffered); 16-bit rows are copied raw and converted once.
     static constexpr int BCF = 2 * N + 4;
     static constexpr bool BC_DIRECT = ESZ == 4;
-    static constexpr bool BC_RAW = !BC_DIRECT && N * ESZ >= 4;
+    static constexpr bool BC_RAW = !BC_DIRECT && NB >= 4;
     static constexpr int BC_BUFS = BC_DIRECT ? 2 : 1;
     // raw row length (elements): rows of 32 bytes or more padded by 16 bytes, so
     // that the 16-byte loads of consecutive rows fall in different bank groups
     static constexpr int RAWP = NB >= 32 ? N + 16 / ESZ : N;
-    static constexpr int YP = CH + 4;               // padded shared row of partial readouts (floats)
+    static constexpr int YP = CH + 4;               // padded row of partial readouts (floats)
     // plane of one lane of a pair's partial readouts: kRow rows of YP floats,
-    // planes 16 mod 32 floats apart so that the 8-byte stores of both lanes of
-    // the pairs of a half warp hit 32 banks
+    // planes 16 mod 32 floats apart so that the 8-byte stores of the lanes of
+    // two planes hit different banks
     static constexpr int YPL = kRow * YP + 16;
     static_assert(kRow * NGRP % THREADS == 0, "whole items per thread");
     static_assert(CH == channels_per_block(N), "channel tile of the plan");
+    static_assert(S * G * NW == N, "the lanes cover the states");
 };
 
-// Slot of channel pair pp in a per-step staging row of 16-byte units: pair
-// 4 q + j (j-th pair of 8-channel group q) goes to 2 q + (j & 1) + 2 NGRP (j >> 1).
-// Eight prologue threads of a quarter warp (two steps x four groups, same j)
-// then hit eight different bank groups for a row of an odd number of units.
-template <int NGRP>
-__device__ __forceinline__ int pair_slot(int pp) {
-    const int q = pp >> 2, j = pp & 3;
-    return 2 * q + (j & 1) + 2 * NGRP * (j >> 1);
-}
-
 template <typename T, int N, int MODE>
-__global__ void __launch_bounds__(32 * fwd_warps(N), fwd_warps(N) == 2 ? 4 : 8) k_fwd2(FwdArgs a, FPlan p, int si, int64_t k_lo,
-                                                               float* ckpt) {
+__global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8)
+    k_fwd(FwdArgs a, FPlan p, int si, int64_t k_lo, float* ckpt) {
     constexpr bool SUMMARY = MODE == kModeSummary;
     constexpr bool NOY = MODE == kModeSummary;                       // no readout (a chunk summary)
     constexpr bool GATE = MODE == kModeY || MODE == kModeYSave;      // gate and y (the checkpoint pass has neither)
-    constexpr bool SAVE = MODE == kModeYSave || MODE == kModeCkpt;   // store the sub-chunk start states
+    constexpr bool SAVE = MODE == kModeYSave || MODE == kModeCkpt;   // store the states entering every kSub-th step
     using C = FCfg<T, N>;
-    constexpr int NW = C::NW, NPW = C::NPW, S = C::S, G = C::G, CH = C::CH, THREADS = C::THREADS, GRP = C::GRP,
-                  NGRP = C::NGRP, ITEMS = C::ITEMS, RW = C::RW, NWd = C::NWd, YP = C::YP, BCF = C::BCF;
-    // per-(t, d) staging, one float4 per channel pair at pair_slot: (delta_eff,
-    // delta_eff * u) and (gate, D * u) of both channels; rows of PAIRS + 1 units
-    __shared__ float4 sDU[kRow][C::PAIRS + 1];
-    __shared__ float4 sGD[NOY ? 1 : kRow][NOY ? 1 : C::PAIRS + 1];
-    // B / C values by state group (f32); with f32 io double buffered, the next
-    // tile's rows being copied in while the scan reads the current one's
+    constexpr int NW = C::NW, NPW = C::NPW, S = C::S, G = C::G, PAIRS = C::PAIRS, CH = C::CH,
+                  THREADS = C::THREADS, GRP = C::GRP, NGRP = C::NGRP, ITEMS = C::ITEMS, RW = C::RW,
+                  NWd = C::NWd, YP = C::YP, BCF = C::BCF;
+    // per-(t, d) staging of the scan, one float4 per channel pair:
+    // (delta_eff of both channels, delta_eff * u of both channels)
+    __shared__ float4 sDU[kRow][PAIRS + 1];
+    // (gate of both channels, D * u of both channels), read by the epilogue
+    __shared__ float4 sGD[NOY ? 1 : kRow][NOY ? 1 : PAIRS + 1];
+    // B / C rows as f32; with f32 io double buffered, the next tile's rows
+    // being copied in while the scan reads the current one's
     __shared__ __align__(16) float sBC[C::BC_BUFS][kRow][BCF];
-    // raw bf16 B / C rows of the next tile (converted into sBC by the prologue)
+    // raw 16-bit B / C rows of the next tile (converted into sBC by the prologue)
     __shared__ __align__(16) T sBCraw[2][C::BC_RAW ? kRow : 1][C::BC_RAW ? C::RAWP : 2];
     // raw runs of delta, u, z of the next tile, copied in asynchronously by the
     // thread that later converts them
@@ -150,20 +147,19 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), fwd_warps(N) == 2 ? 4 : 8) 
     const bool ok0 = d0 + c0 < Dch, ok1 = d0 + c0 + 1 < Dch;
     const int64_t dA0 = ok0 ? d0 + c0 : Dch - 1, dA1 = ok1 ? d0 + c0 + 1 : Dch - 1;
     const int n0 = w * NPW + g * S;
-    const int sg = n0 / S;  // the lane's state group
-    const int pslot = pair_slot<NGRP>(pp);
     const int64_t row0 = b * Dch + dA0, row1 = b * Dch + dA1;
-    // the state starts at h0 (zero without one); a chunk summary starts from zero
+    // the state starts at h0 (zero without one); a chunk summary starts from zero.
+    // Registers pair the lane's two channels at one state: (channel c0, c0 + 1).
     const bool from_h0 = !SUMMARY && a.h0 != nullptr;
-    float A2[2][S], h[2][S];
-    float sd0 = 0.f, sd1 = 0.f;  // summary: the chunk's sums of delta_eff
+    float2 A2[S], h[S];
+    float2 sdp = make_float2(0.f, 0.f);  // summary: the chunk's sums of delta_eff
 #pragma unroll
     for (int s = 0; s < S; s++) {
         // channels past Dch run with a zero exponent: their state stays exactly zero
-        A2[0][s] = ok0 ? scan_A(a, dA0 * N + n0 + s) * kLog2eF : 0.f;
-        A2[1][s] = ok1 ? scan_A(a, dA1 * N + n0 + s) * kLog2eF : 0.f;
-        h[0][s] = from_h0 && ok0 ? a.h0[row0 * N + n0 + s] : 0.f;
-        h[1][s] = from_h0 && ok1 ? a.h0[row1 * N + n0 + s] : 0.f;
+        A2[s] = make_float2(ok0 ? scan_A(a, dA0 * N + n0 + s) * kLog2eF : 0.f,
+                            ok1 ? scan_A(a, dA1 * N + n0 + s) * kLog2eF : 0.f);
+        h[s] = make_float2(from_h0 && ok0 ? a.h0[row0 * N + n0 + s] : 0.f,
+                           from_h0 && ok1 ? a.h0[row1 * N + n0 + s] : 0.f);
     }
     if (!SUMMARY && k > 0) {
         // carry-in: h <- P_j h + H_j over the unit's chunks j < k, with
@@ -171,34 +167,30 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), fwd_warps(N) == 2 ? 4 : 8) 
         for (int64_t j = 0; j < k; j++) {
             const int64_t q = s_first + j;
             const float* H0 = a.ws_fsum + (q * CH + c0) * N + n0;
-            const float sdj0 = a.ws_fsd[q * CH + c0], sdj1 = a.ws_fsd[q * CH + c0 + 1];
+            const float2 sdj = make_float2(a.ws_fsd[q * CH + c0], a.ws_fsd[q * CH + c0 + 1]);
 #pragma unroll
             for (int s = 0; s < S; s++) {
-                h[0][s] = fmaf(ex2a(A2[0][s] * sdj0), h[0][s], H0[s]);
-                h[1][s] = fmaf(ex2a(A2[1][s] * sdj1), h[1][s], H0[N + s]);
+                const float2 e = mul2(A2[s], sdj);
+                h[s] = fma2(make_float2(ex2a(e.x), ex2a(e.y)), h[s], make_float2(H0[s], H0[N + s]));
             }
         }
         // channels past Dch (read a clamped channel's summaries) keep a zero state,
         // so that every saved slot of theirs holds zero
 #pragma unroll
-        for (int s = 0; s < S; s++) {
-            h[0][s] = ok0 ? h[0][s] : 0.f;
-            h[1][s] = ok1 ? h[1][s] : 0.f;
-        }
+        for (int s = 0; s < S; s++) h[s] = make_float2(ok0 ? h[s].x : 0.f, ok1 ? h[s].y : 0.f);
     }
 
     const int64_t t_begin = k * sgm.Lc;
     const int64_t t_end = t_begin + sgm.Lc < L ? t_begin + sgm.Lc : L;
     // saved states (layout of ckpt_bytes): one block of CH x N floats per
-    // (sub-chunk slot t / kSub, batch, channel tile), the lane's slots in lane order
+    // (slot t / kSub, batch, channel tile), the lane's 2 S floats at its slot
     const int64_t ck_stride = a.Bsz * ntiles * CH * N;
-    float* ck_blk = SAVE ? ckpt + (t_begin / kSub) * ck_stride + (b * ntiles + tile) * (CH * N) : nullptr;
-    float* ck0 = SAVE ? ck_blk + ckpt_slot(w, 0, lane, S) : nullptr;
-    float* ck1 = SAVE ? ck_blk + ckpt_slot(w, 1, lane, S) : nullptr;
+    float* ck_lane =
+        SAVE ? ckpt + (t_begin / kSub) * ck_stride + (b * ntiles + tile) * (CH * N) + ckpt_slot(w, lane, S) : nullptr;
 
     // Asynchronous copies of the tile starting at tt: the thread's item runs
     // (when the tile's rows are whole aligned vectors) and the B / C rows (f32
-    // into sBC[buf]; bf16 raw into sBCraw); one commit group.
+    // into sBC[buf]; 16-bit raw into sBCraw); one commit group.
     auto issue = [&](int64_t tt, int buf) {
         if (fast) {
 #pragma unroll
@@ -219,7 +211,13 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), fwd_warps(N) == 2 ? 4 : 8) 
             const int64_t t = tt + r;
             const T* src = (half ? Cm : Bm) + (b * L + (t < t_end ? t : 0)) * N;
             if constexpr (C::BC_DIRECT) {
-                cp_async_bc_row<T, N, S>(reinterpret_cast<unsigned char*>(&sBC[buf][r][0]), half, src, t < t_end);
+                float* dst = &sBC[buf][r][half * N];
+                if (t < t_end) {
+                    cp_async_bytes<N * 4>(dst, src);
+                } else {
+#pragma unroll
+                    for (int n = 0; n < N; n++) dst[n] = 0.f;
+                }
             } else if constexpr (C::BC_RAW) {
                 if (t < t_end) cp_async_bytes<N * C::ESZ>(&sBCraw[half][r][0], src);
             }
@@ -270,13 +268,12 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), fwd_warps(N) == 2 ? 4 : 8) 
                         dun = mul2(make_float2(sDv[cg + c], sDv[cg + c + 1]), uu);
                     }
                 }
-                const int slot = pair_slot<NGRP>((cg + c) / 2);
-                sDU[r][slot] = make_float4(dl.x, dlu.x, dl.y, dlu.y);
-                if (!NOY) sGD[r][slot] = make_float4(gt.x, dun.x, gt.y, dun.y);
+                sDU[r][(cg + c) / 2] = make_float4(dl.x, dl.y, dlu.x, dlu.y);
+                if (!NOY) sGD[r][(cg + c) / 2] = make_float4(gt.x, gt.y, dun.x, dun.y);
             }
         }
         if constexpr (!C::BC_DIRECT) {
-            // bf16 B / C rows of the tile's steps, row id = (tensor, step), converted
+            // 16-bit B / C rows of the tile's steps, row id = (tensor, step), converted
             // by the thread that copied them (or loaded here when too short to copy)
             for (int id = tid; id < (NOY ? 1 : 2) * kRow; id += THREADS) {
                 const int half = id / kRow, r = id % kRow;
@@ -286,71 +283,73 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), fwd_warps(N) == 2 ? 4 : 8) 
                     if constexpr (C::BC_RAW) lds_words<C::NB, NWd>(&sBCraw[half][r][0], wv);
                     else load_words<C::NB, NWd>((half ? Cm : Bm) + (b * L + t) * N, wv);
                 }
-                stage_bc_row_f32<T, N, S, NWd>(&sBC[0][r][0], half, wv, t < t_end);
+                float* dst = &sBC[0][r][half * N];
+#pragma unroll
+                for (int n = 0; n < N; n++) dst[n] = t < t_end ? elem<T>(wv, n) : 0.f;
             }
         }
-        __syncthreads();  // staging complete; every thread is done reading sRaw
+        __syncthreads();  // staging complete; every thread is done reading sRaw / sBCraw
         if (t0 + kRow < t_end) issue(t0 + kRow, buf ^ 1);
 
         // ---- scan: 32 steps of the lane's 2 x S states.  Steps past t_end (last
         // tile only) carry delta_eff = 0 and B = 0: the state stays unchanged.
-        const int64_t jt = (t0 - t_begin) / kSub;
-#pragma unroll 8
+        // Software-pipelined by one step: the decays and input terms of step
+        // i + 1 (loads, exponents, MUFU) are formed before the recurrence of
+        // step i, which is the only part that waits on the previous state.
+        const float* bcrow = &sBC[C::BC_DIRECT ? buf : 0][0][0];
+        float2 daN[S], xbN[S];  // decays and input terms of the next step
+        float cN[S] = {};       // its C values
+        auto prep = [&](int i) {
+            const float4 du = sDU[i][pp];
+            const float2 dl2 = make_float2(du.x, du.y), dlu2 = make_float2(du.z, du.w);
+            if (SUMMARY) sdp = add2(sdp, dl2);  // delta_eff of steps past t_end is zero
+            float Bv[S];
+            ld_f32<S>(bcrow + i * BCF + n0, Bv);
+            if (!NOY) ld_f32<S>(bcrow + i * BCF + N + n0, cN);
+#pragma unroll
+            for (int s = 0; s < S; s++) {
+                const float2 ex = mul2(dl2, A2[s]);
+                daN[s] = make_float2(ex2a(ex.x), ex2a(ex.y));
+                xbN[s] = mul2(dlu2, splat2(Bv[s]));
+            }
+        };
+        prep(0);
+#pragma unroll
         for (int i = 0; i < kRow; i++) {
             if (SAVE && (i % kSub) == 0) {
-                const int64_t jo = (jt + i / kSub) * ck_stride;
-                // every slot is written: channels past Dch hold a zero state
-                if constexpr (S % 4 == 0) {
-#pragma unroll
-                    for (int s = 0; s < S; s += 4) {
-                        *reinterpret_cast<float4*>(ck0 + jo + s) = make_float4(h[0][s], h[0][s + 1], h[0][s + 2], h[0][s + 3]);
-                        *reinterpret_cast<float4*>(ck1 + jo + s) = make_float4(h[1][s], h[1][s + 1], h[1][s + 2], h[1][s + 3]);
-                    }
+                // the state entering step t0 + i, channel-major (S states of c0, then of c1);
+                // every slot is written: channels past Dch hold a zero state, and the
+                // slots of the last tile past the sequence end (L rounded up to 32)
+                // the final state
+                float* dst = ck_lane + ((t0 - t_begin + i) / kSub) * ck_stride;
+                if constexpr (S == 4) {
+                    *reinterpret_cast<float4*>(dst) = make_float4(h[0].x, h[1].x, h[2].x, h[3].x);
+                    *reinterpret_cast<float4*>(dst + 4) = make_float4(h[0].y, h[1].y, h[2].y, h[3].y);
                 } else {
 #pragma unroll
                     for (int s = 0; s < S; s++) {
-                        ck0[jo + s] = h[0][s];
-                        ck1[jo + s] = h[1][s];
+                        dst[s] = h[s].x;
+                        dst[S + s] = h[s].y;
                     }
                 }
             }
-            const float4 du = sDU[i][pslot];
-            if (SUMMARY) {
-                sd0 += du.x;  // delta_eff of steps past t_end is zero
-                sd1 += du.z;
+            float2 da[S], xb[S];
+            float Cv[S];
+#pragma unroll
+            for (int s = 0; s < S; s++) {
+                da[s] = daN[s];
+                xb[s] = xbN[s];
+                Cv[s] = cN[s];
             }
-            float Bv[S], Cv[S];
-            ld_bc_f32<S>(&sBC[C::BC_DIRECT ? buf : 0][i][sg * 2 * S], Bv, Cv);
-            float yp[2];
-            if constexpr (S >= 2) {
-                float2 ya[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            if (i + 1 < kRow) prep(i + 1);
 #pragma unroll
-                for (int e = 0; e < 2; e++) {
-                    const float2 dl2 = splat2(e ? du.z : du.x), dlu2 = splat2(e ? du.w : du.y);
-#pragma unroll
-                    for (int s = 0; s < S; s += 2) {
-                        const float2 ex = mul2(dl2, make_float2(A2[e][s], A2[e][s + 1]));
-                        const float2 da = make_float2(ex2a(ex.x), ex2a(ex.y));
-                        const float2 x = mul2(dlu2, make_float2(Bv[s], Bv[s + 1]));
-                        const float2 hh = fma2(da, make_float2(h[e][s], h[e][s + 1]), x);
-                        h[e][s] = hh.x;
-                        h[e][s + 1] = hh.y;
-                        if (!NOY) ya[e] = fma2(make_float2(Cv[s], Cv[s + 1]), hh, ya[e]);
-                    }
-                }
-                yp[0] = ya[0].x + ya[0].y;
-                yp[1] = ya[1].x + ya[1].y;
-            } else {
-#pragma unroll
-                for (int e = 0; e < 2; e++) {
-                    const float da = ex2a((e ? du.z : du.x) * A2[e][0]);
-                    h[e][0] = fmaf(da, h[e][0], (e ? du.w : du.y) * Bv[0]);
-                    yp[e] = Cv[0] * h[e][0];
-                }
-            }
+            for (int s = 0; s < S; s++) h[s] = fma2(da[s], h[s], xb[s]);
             if (!NOY) {
+                float2 ya = mul2(splat2(Cv[0]), h[0]);
+#pragma unroll
+                for (int s = 1; s < S; s++) ya = fma2(splat2(Cv[s]), h[s], ya);
                 // both channels' partials of the lane; the epilogue adds the pair's lanes
-                *reinterpret_cast<float2*>(&sY[w][g * C::YPL + i * YP + c0]) = make_float2(yp[0], yp[1]);
+                *reinterpret_cast<float2*>(&sY[w][g * C::YPL + i * YP + c0]) = ya;
             }
         }
         __syncthreads();
@@ -372,9 +371,10 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), fwd_warps(N) == 2 ? 4 : 8) 
 #pragma unroll
                         for (int ww = 0; ww < NW; ww++) {
                             float4 o = *reinterpret_cast<const float4*>(&sY[ww][r * YP + cg + c]);
-                            if constexpr (G == 2) {
-                                const float4 q = *reinterpret_cast<const float4*>(&sY[ww][C::YPL + r * YP + cg + c]);
-                                o.x += q.x; o.y += q.y; o.z += q.z; o.w += q.w;
+#pragma unroll
+                            for (int gg = 1; gg < G; gg++) {
+                                const float4 v = *reinterpret_cast<const float4*>(&sY[ww][gg * C::YPL + r * YP + cg + c]);
+                                o.x += v.x; o.y += v.y; o.z += v.z; o.w += v.w;
                             }
                             if (ww == 0) {
                                 acc = o;
@@ -382,17 +382,16 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), fwd_warps(N) == 2 ? 4 : 8) 
                                 acc.x += o.x; acc.y += o.y; acc.z += o.z; acc.w += o.w;
                             }
                         }
-                        const float4 g01 = sGD[r][pair_slot<NGRP>((cg + c) / 2)];
-                        const float4 g23 = sGD[r][pair_slot<NGRP>((cg + c) / 2 + 1)];
                         // the pre-gate readout y0 = sum_n h C + D u, then the gate
-                        y0v[c] = acc.x + g01.y;
+                        const float4 g01 = sGD[r][(cg + c) / 2], g23 = sGD[r][(cg + c) / 2 + 1];
+                        y0v[c] = acc.x + g01.z;
                         y0v[c + 1] = acc.y + g01.w;
-                        y0v[c + 2] = acc.z + g23.y;
+                        y0v[c + 2] = acc.z + g23.z;
                         y0v[c + 3] = acc.w + g23.w;
                         yv[c] = y0v[c] * g01.x;
-                        yv[c + 1] = y0v[c + 1] * g01.z;
+                        yv[c + 1] = y0v[c + 1] * g01.y;
                         yv[c + 2] = y0v[c + 2] * g23.x;
-                        yv[c + 3] = y0v[c + 3] * g23.z;
+                        yv[c + 3] = y0v[c + 3] * g23.y;
                     }
                     const int64_t off = (b * L + t) * Dch + d0 + cg;
                     if (a.y0 && z) {
@@ -431,8 +430,10 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), fwd_warps(N) == 2 ? 4 : 8) 
                 }
             }
         }
-        // the next prologue restages sDU / sGD / sBC; sY is read above and written
-        // again only after the next prologue's barrier
+        // the next prologue restages sDU / sGD / sBC only after every thread has
+        // passed the scan barrier above, i.e. after the scan's reads; the epilogue's
+        // reads of sGD / sY come before this thread's next prologue writes, and the
+        // other threads write them again only after the next prologue's barrier
     }
 
     if (SUMMARY) {
@@ -441,15 +442,15 @@ __global__ void __launch_bounds__(32 * fwd_warps(N), fwd_warps(N) == 2 ? 4 : 8) 
         float* H0 = a.ws_fsum + (q * CH + c0) * N + n0;
 #pragma unroll
         for (int s = 0; s < S; s++) {
-            H0[s] = h[0][s];
-            H0[N + s] = h[1][s];
+            H0[s] = h[s].x;
+            H0[N + s] = h[s].y;
         }
-        if (w == 0 && g == 0) *reinterpret_cast<float2*>(a.ws_fsd + q * CH + c0) = make_float2(sd0, sd1);
+        if (w == 0 && g == 0) *reinterpret_cast<float2*>(a.ws_fsd + q * CH + c0) = sdp;
     } else if (MODE != kModeCkpt && k == sgm.K - 1 && a.last_state) {
 #pragma unroll
         for (int s = 0; s < S; s++) {
-            if (ok0) a.last_state[row0 * N + n0 + s] = h[0][s];
-            if (ok1) a.last_state[row1 * N + n0 + s] = h[1][s];
+            if (ok0) a.last_state[row0 * N + n0 + s] = h[s].x;
+            if (ok1) a.last_state[row1 * N + n0 + s] = h[s].y;
         }
     }
 }
@@ -459,13 +460,12 @@ template <typename T, int N, int MODE>
 void launch_fwd_mode(const FwdArgs& a, const FPlan& p, int si, cudaStream_t st, int64_t k_lo, int64_t k_hi,
                      float* ckpt) {
     prof_mark(st);
-    k_fwd2<T, N, MODE><<<(unsigned)(p.seg[si].nu * (k_hi - k_lo)), FCfg<T, N>::THREADS, 0, st>>>(a, p, si, k_lo,
-                                                                                                ckpt);
+    k_fwd<T, N, MODE><<<(unsigned)(p.seg[si].nu * (k_hi - k_lo)), FCfg<T, N>::THREADS, 0, st>>>(a, p, si, k_lo, ckpt);
 }
 
 // The chunk summaries of every chunked segment, then each segment's main pass.
 template <typename T, int N>
-cudaError_t launch_fwd2_t(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt) {
+cudaError_t launch_fwd_t(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt) {
     for (int si = 0; si < p.nseg; si++)
         if (p.seg[si].K > 1) launch_fwd_mode<T, N, kModeSummary>(a, p, si, st, 0, p.seg[si].K - 1, nullptr);
     for (int si = 0; si < p.nseg; si++) {
@@ -483,14 +483,14 @@ cudaError_t launch_fwd2_t(const FwdArgs& a, const FPlan& p, cudaStream_t st, int
 
 // Forward launcher of one io type: switches on N.
 template <typename T>
-cudaError_t launch_fwd2_io(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt) {
+cudaError_t launch_fwd_io(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt) {
     switch (a.N) {
-        case 1: return launch_fwd2_t<T, 1>(a, p, st, mode, ckpt);
-        case 2: return launch_fwd2_t<T, 2>(a, p, st, mode, ckpt);
-        case 4: return launch_fwd2_t<T, 4>(a, p, st, mode, ckpt);
-        case 8: return launch_fwd2_t<T, 8>(a, p, st, mode, ckpt);
-        case 16: return launch_fwd2_t<T, 16>(a, p, st, mode, ckpt);
-        case 32: return launch_fwd2_t<T, 32>(a, p, st, mode, ckpt);
+        case 1: return launch_fwd_t<T, 1>(a, p, st, mode, ckpt);
+        case 2: return launch_fwd_t<T, 2>(a, p, st, mode, ckpt);
+        case 4: return launch_fwd_t<T, 4>(a, p, st, mode, ckpt);
+        case 8: return launch_fwd_t<T, 8>(a, p, st, mode, ckpt);
+        case 16: return launch_fwd_t<T, 16>(a, p, st, mode, ckpt);
+        case 32: return launch_fwd_t<T, 32>(a, p, st, mode, ckpt);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -1,6 +1,6 @@
 // Forward kernels for f32 io (one translation unit per io type, compiled in parallel).
-#include "fwd2.cuh"
+#include "fwd.cuh"
 
 namespace ss {
-template cudaError_t launch_fwd2_io<float>(const FwdArgs&, const FPlan&, cudaStream_t, int, float*);
+template cudaError_t launch_fwd_io<float>(const FwdArgs&, const FPlan&, cudaStream_t, int, float*);
 }  // namespace ss

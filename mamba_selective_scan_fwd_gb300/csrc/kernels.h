@@ -72,14 +72,21 @@ constexpr int kModeY = 0, kModeSummary = 1, kModeCkpt = 2, kModeYSave = 3;
 // Block layout shared by the forward and backward scans.  A lane holds S
 // states of two adjacent channels (a channel pair), so every B / C value it
 // reads from shared memory serves two channels.  For N >= 16 a block has two
-// warps that split the states of every channel; within a warp G = 2 adjacent
-// lanes share a channel pair (one lane for N = 1).  A block therefore covers
-// 2 * 32 / G channels (32, or 64 for N = 1) of one batch row and one time
-// chunk.
-__host__ __device__ constexpr int fwd_warps(int64_t N) { return N >= 16 ? 2 : 1; }
-__host__ __device__ constexpr int64_t channels_per_block(int64_t N) { return N >= 2 ? 32 : 64; }
+// warps that split the states of every channel; within a warp G = NPW / S
+// adjacent lanes share a channel pair, NPW = N / warps being the warp's
+// states.  S is 4 where the warp holds at least four states (the backward
+// keeps an 8-step window of the lane's 2 S states in registers: 64 floats),
+// else all of them.  A block covers 2 * 32 / G channels (16 for N = 32, 32
+// for N = 8 and 16, 64 for N <= 4) of one batch row and one time chunk.
+__host__ __device__ constexpr int scan_warps(int64_t N) { return N >= 16 ? 2 : 1; }
+__host__ __device__ constexpr int lane_states(int64_t N) {
+    return N / scan_warps(N) >= 4 ? 4 : (int)(N / scan_warps(N));
+}
+__host__ __device__ constexpr int64_t channels_per_block(int64_t N) {
+    return 2 * 32 / (N / scan_warps(N) / lane_states(N));
+}
 
-constexpr int kSub = 4;  // backward sub-chunk: steps whose states stay in registers (checkpoint interval)
+constexpr int kSub = 8;  // steps between saved states (the backward's recompute window)
 
 // Launch plan.  A unit is one (batch row, channel tile): unit u = b tiles_b +
 // tile.  Units are grouped into at most two segments; a segment cuts the time
@@ -160,7 +167,7 @@ inline void chunking(int64_t nunits, int64_t L, int64_t N, int64_t& K, int64_t& 
 // Blocks of one round: kTargetWarps warps, 8 on every SM.  The scan kernels
 // are built for 8 resident warps per SM (4 two-warp or 8 one-warp blocks:
 // their register budget), so a round is also what one wave of the GPU holds.
-inline int64_t round_blocks(int64_t N) { return kTargetWarps / fwd_warps(N); }
+inline int64_t round_blocks(int64_t N) { return kTargetWarps / scan_warps(N); }
 
 // A pure function of the sizes (the same sizes always plan the same way).
 // One segment chunked to fill the GPU; or, when the units already fill it, one
@@ -246,26 +253,27 @@ void prof_mark(cudaStream_t st);
 // Launchers of one io type T (float, __half, __nv_bfloat16), defined in the
 // per-io translation units.
 template <typename T>
-cudaError_t launch_fwd2_io(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt);
+cudaError_t launch_fwd_io(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt);
 template <typename T>
-cudaError_t launch_bwd2_io(const BwdArgs& a, const FPlan& p, cudaStream_t st, float* ckpt_out);
+cudaError_t launch_bwd_io(const BwdArgs& a, const FPlan& p, cudaStream_t st, float* ckpt_out);
 
-// ckpt: where the Y-mode forward also stores the sub-chunk start states (may be null).
-cudaError_t launch_fwd2(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt);
+// ckpt: where the Y-mode forward also stores the states entering every kSub-th step (may be null).
+cudaError_t launch_fwd(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt);
 // ckpt_out: the checkpoint buffer to fill first, or null when a.ws_ckpt already
 // holds the states saved by the forward.
-cudaError_t launch_bwd2(const BwdArgs& a, const FPlan& p, cudaStream_t st, float* ckpt_out);
+cudaError_t launch_bwd(const BwdArgs& a, const FPlan& p, cudaStream_t st, float* ckpt_out);
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
 
 // Bytes of what the forward keeps for the backward (ss_fwd_save writes it
 // into the caller's buffer; ss_bwd's checkpoint pass into its workspace):
-// the sub-chunk start states of every (b, d) row, the checkpoints the
-// backward recomputes from, then at ckpt_y0_offset the pre-gate readout y0
-// (f32 [Bsz][L][Dch]).  States layout: [slot t / kSub][b][channel tile][block
-// of CH x N floats]; within a block, float ((w 2 + e) 32 + lane) S + s is
-// state n0 + s of channel c0 + e of the lane (the scan kernels' lane layout),
-// so that a warp's stores and loads of one channel parity are contiguous.
+// the state entering every kSub-th step of every (b, d) row, which the
+// backward recomputes its windows from, then at ckpt_y0_offset the pre-gate
+// readout y0 (f32 [Bsz][L][Dch]).  States layout: [slot t / kSub][b][channel
+// tile][block of CH x N floats]; within a block, lane l of warp w holds 2 S
+// floats at ckpt_slot(w, l, S): S states of its first channel, then S of the
+// second (the scan kernels' lane layout), so that a warp's stores and loads
+// are contiguous.
 inline size_t ckpt_y0_offset(const FPlan& p, int64_t Bsz, int64_t N) {
     return align_up((size_t)Bsz * p.tiles_b * channels_per_block(N) * p.slots * N * sizeof(float), 256);
 }
@@ -273,10 +281,8 @@ inline size_t ckpt_bytes(const FPlan& p, int64_t Bsz, int64_t L, int64_t Dch, in
     return ckpt_y0_offset(p, Bsz, N) + (size_t)Bsz * L * Dch * sizeof(float);
 }
 
-// Float offset of a lane's slot for channel parity e within a saved-state block.
-__host__ __device__ constexpr int64_t ckpt_slot(int w, int e, int lane, int S) {
-    return ((int64_t)(w * 2 + e) * 32 + lane) * S;
-}
+// Float offset of a lane's 2 S saved states within a saved-state block.
+__host__ __device__ constexpr int64_t ckpt_slot(int w, int lane, int S) { return ((int64_t)w * 32 + lane) * 2 * S; }
 
 // Bytes of the forward chunk summaries (0 when nothing is chunked): end
 // states [sparts][CH][N], then the sums of delta_eff [sparts][CH] at the

@@ -118,6 +118,24 @@ __device__ __forceinline__ void sts_words(void* p, const uint32_t* w) {
     }
 }
 
+// S consecutive f32 values of shared memory (16-byte aligned when S = 4,
+// 8-byte aligned when S = 2).
+template <int S>
+__device__ __forceinline__ void ld_f32(const float* p, float (&v)[S]) {
+    if constexpr (S % 4 == 0) {
+#pragma unroll
+        for (int q = 0; q < S; q += 4) {
+            const float4 f = *reinterpret_cast<const float4*>(p + q);
+            v[q] = f.x; v[q + 1] = f.y; v[q + 2] = f.z; v[q + 3] = f.w;
+        }
+    } else if constexpr (S == 2) {
+        const float2 f = *reinterpret_cast<const float2*>(p);
+        v[0] = f.x; v[1] = f.y;
+    } else {
+        v[0] = p[0];
+    }
+}
+
 // B and C values of one f32 state group (S floats of B, then S of C).
 template <int S>
 __device__ __forceinline__ void ld_bc_f32(const float* g, float (&Bv)[S], float (&Cv)[S]) {

@@ -107,16 +107,18 @@ def test_fwd_save_rejects(kw, code):
 
 
 def test_saved_sizes():
-    # one f32 state of N per (b, d) row every 4 steps of L rounded up to 32, however the plan cuts time,
+    # one f32 state of N per (b, d) row every 8 steps of L rounded up to 32, however the plan cuts time,
     # then (at a 256-byte boundary) the forward's pre-gate readout y0, f32 [B, L, D]
     def up(x):
         return -(-x // 256) * 256
 
-    assert ss.saved_bytes(4, 4096, 5120, 16, ss.SS_BF16) == up(4 * 5120 * (4096 // 4) * 16 * 4) + 4 * 4096 * 5120 * 4
-    assert ss.saved_bytes(1, 131072, 1024, 16, ss.SS_BF16) == up(1024 * (131072 // 4) * 16 * 4) + 131072 * 1024 * 4
-    assert ss.saved_bytes(1, 300, 3, 16, ss.SS_F32) == up(32 * (320 // 4) * 16 * 4) + 300 * 3 * 4
-    # channels are stored in whole tiles of 32 (8 channels take a tile): 2 x 32 x 8 slots x 4 states
-    assert ss.saved_bytes(2, 16, 8, 4, ss.SS_F32) == up(2 * 32 * (32 // 4) * 4 * 4) + 2 * 16 * 8 * 4
+    assert ss.saved_bytes(4, 4096, 5120, 16, ss.SS_BF16) == up(4 * 5120 * (4096 // 8) * 16 * 4) + 4 * 4096 * 5120 * 4
+    assert ss.saved_bytes(1, 131072, 1024, 16, ss.SS_BF16) == up(1024 * (131072 // 8) * 16 * 4) + 131072 * 1024 * 4
+    assert ss.saved_bytes(1, 300, 3, 16, ss.SS_F32) == up(32 * (320 // 8) * 16 * 4) + 300 * 3 * 4
+    # channels are stored in whole tiles (64 for N = 4, so 8 channels take a tile): 2 x 64 x 4 slots x 4 states
+    assert ss.saved_bytes(2, 16, 8, 4, ss.SS_F32) == up(2 * 64 * (32 // 8) * 4 * 4) + 2 * 16 * 8 * 4
+    # 16-channel tiles for N = 32
+    assert ss.saved_bytes(1, 64, 20, 32, ss.SS_F32) == up(32 * (64 // 8) * 32 * 4) + 64 * 20 * 4
     assert ss.saved_bytes(0, 16, 8, 4, ss.SS_F32) == 0
     assert _fwd_save(savedb=ss.saved_bytes(2, 16, 8, 4, 0) - 1) == WS_SMALL
     # the saved-state backward needs no room for the states

@@ -23,7 +23,9 @@ SMS = 152
 
 
 def tile_of(N):
-    return 32 if N >= 2 else 64
+    # a lane holds 4 states (all of them below 4) of a channel pair; a warp covers
+    # 16 pairs for N = 8, 16, 8 pairs for N = 32, 32 pairs for N <= 4
+    return {32: 16, 16: 32, 8: 32}.get(N, 64)
 
 
 def round_of(N):
@@ -49,7 +51,7 @@ def test_plan_segments(shape):
         (u0, k0), (u1, k1) = segs
         assert k0 == 1 and u0 % round_of(N) == 0 and u0 > 0 and 0 < u1 < round_of(N) and k1 > 1
         assert ss.fwd_workspace_bytes(Bsz, L, Dch, N, ss.SS_BF16) <= binding.FWD_NOALLOC_MAX_SCRATCH_BYTES
-    slots = -(-L // 32) * 8
+    slots = -(-L // 32) * 4  # one saved state every 8 steps of L rounded up to 32
     states = -(-(units * tile_of(N) * slots * N * 4) // 256) * 256
     assert ss.saved_bytes(Bsz, L, Dch, N, ss.SS_BF16) == states + Bsz * L * Dch * 4  # states, then y0
 
