@@ -78,11 +78,19 @@ struct BCfg {
     static constexpr int RWH = GRP * ESZ >= 4 ? GRP * ESZ / 4 : 1;  // 32-bit words of an item's run
     static constexpr int NB = N * ESZ;
     static constexpr int NWd = NB >= 4 ? NB / 4 : 1;
-    // f32 B / C staging as in the forward: a step's row is B (N values) then C
+    // B / C staging: a step's row is B (N values) then C.  The lanes load S of
+    // each per step as broadcasts, and the shared-memory data pipe -- which
+    // bounds this kernel -- returns one 32-bit word per lane per cycle however
+    // few distinct addresses a warp reads: so bf16 rows stay packed (a lane's
+    // four states are two words, widened by ALU bit operations) and are copied
+    // in raw, double buffered; f32 rows are copied straight in (double
+    // buffered); f16 rows are converted by the prologue
     static constexpr int BCF = 2 * N + 4;
+    static constexpr bool BC_PK = std::is_same<T, __nv_bfloat16>::value && S == 4;
     static constexpr bool BC_DIRECT = ESZ == 4;
-    static constexpr bool BC_RAW = !BC_DIRECT && NB >= 4;
+    static constexpr bool BC_RAW = !BC_DIRECT && !BC_PK && NB >= 4;
     static constexpr int BC_BUFS = BC_DIRECT ? 2 : 1;
+    static constexpr int PKR = 2 * N + 8;           // packed row (bf16 elements), 16-byte multiple
     static constexpr int RAWP = NB >= 32 ? N + 16 / ESZ : N;
     static constexpr int EP = CH + 4;               // padded per-channel rows (floats)
     // plane of per-step channel sums of one lane of a pair: kTT rows of EP floats,
@@ -203,7 +211,9 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
     __shared__ float4 sUS[MAIN ? kTT : 1][MAIN ? PAIRS + 1 : 1];
     // B / C rows as f32 (B then C); with f32 io double buffered, the next tile's
     // rows being copied in while the current tile is walked
-    __shared__ __align__(16) float sBC[C::BC_BUFS][kTT][BCF];
+    __shared__ __align__(16) float sBC[C::BC_BUFS][C::BC_PK ? 1 : kTT][C::BC_PK ? 4 : BCF];
+    // packed bf16 B / C rows (B, then C), double buffered: the walk reads them directly
+    __shared__ __align__(16) T sBCpk[C::BC_PK ? 2 : 1][C::BC_PK ? kTT : 1][C::BC_PK ? C::PKR : 8];
     // raw 16-bit B / C rows of the next tile (converted into sBC by the prologue)
     __shared__ __align__(16) T sBCraw[2][C::BC_RAW ? kTT : 1][C::BC_RAW ? C::RAWP : 2];
     // raw runs of delta, u, dy, z of the next tile, copied in asynchronously by
@@ -352,7 +362,15 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
             const int half = MAIN ? id / kTT : 1, r = id % kTT;
             const int64_t t = tt + r;
             const T* src = (half ? Cm : Bm) + (b * L + (t < t_end ? t : 0)) * N;
-            if constexpr (C::BC_DIRECT) {
+            if constexpr (C::BC_PK) {
+                T* dst = &sBCpk[buf][r][half * N];
+                if (t < t_end) {
+                    cp_async_bytes<N * C::ESZ>(dst, src);
+                } else {
+#pragma unroll
+                    for (int n = 0; n < N; n += 2) *reinterpret_cast<uint32_t*>(dst + n) = 0u;
+                }
+            } else if constexpr (C::BC_DIRECT) {
                 float* dst = &sBC[buf][r][half * N];
                 if (t < t_end) {
                     cp_async_bytes<N * 4>(dst, src);
@@ -447,7 +465,7 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
                 if (z && rv) store_run<GRP>(a.dz + (b * L + t) * Dch + d0 + cg, vdz, d0 + cg, Dch, ofast);
             }
         }
-        if constexpr (!C::BC_DIRECT) {
+        if constexpr (!C::BC_DIRECT && !C::BC_PK) {
             // 16-bit B / C rows of the tile's steps (the reverse summary needs only C),
             // converted by the thread that copied them (or loaded here when too short to copy)
             for (int id = tid; id < (MAIN ? 2 : 1) * kTT; id += THREADS) {
@@ -466,6 +484,12 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
         __syncthreads();  // staging complete; every thread is done reading sRaw / sY0 / sBCraw
         if (m > 0) issue(m - 1);
         const float* bcrow = &sBC[C::BC_DIRECT ? buf : 0][0][0];
+        const T* pkrow = &sBCpk[C::BC_PK ? buf : 0][0][0];
+        // S values of row i's B (half 0) or C (half 1) from the lane's states
+        auto ld_bc = [&](int i, int half, float (&v)[S]) {
+            if constexpr (C::BC_PK) ld_bf16x4(pkrow + i * C::PKR + half * N + n0, v);
+            else ld_f32<S>(bcrow + i * BCF + half * N + n0, v);
+        };
 
         if constexpr (!MAIN) {
             // ---- reverse summary: adjoint walk from a zero carry and the chunk's
@@ -477,7 +501,7 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
                 sd[0] += du.x;
                 sd[1] += du.y;
                 float Cv[S];
-                ld_f32<S>(bcrow + i * BCF + N + n0, Cv);
+                ld_bc(i, 1, Cv);
 #pragma unroll
                 for (int e = 0; e < 2; e++) {
                     const float2 dl = splat2(e ? du.y : du.x), gg = splat2(e ? g2.y : g2.x);
@@ -516,7 +540,7 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
                 for (int i = 0; i < kTT; i++) {
                     const float4 du = sDU[i][pp];
                     float Bv[S];
-                    ld_f32<S>(bcrow + i * BCF + n0, Bv);
+                    ld_bc(i, 0, Bv);
 #pragma unroll
                     for (int e = 0; e < 2; e++) {
                         const float2 dl = splat2(e ? du.y : du.x), dlu = splat2(e ? du.w : du.z);
@@ -539,8 +563,8 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
             auto prepw = [&](int i) {
                 duN = sDU[i][pp];
                 gN = sG[i][pp];
-                ld_f32<S>(bcrow + i * BCF + n0, BN);
-                ld_f32<S>(bcrow + i * BCF + N + n0, CN);
+                ld_bc(i, 0, BN);
+                ld_bc(i, 1, CN);
 #pragma unroll
                 for (int e = 0; e < 2; e++) {
                     const float2 dl = splat2(e ? duN.y : duN.x);

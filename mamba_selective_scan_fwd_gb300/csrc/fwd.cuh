@@ -69,7 +69,10 @@ struct FCfg {
     static constexpr int NWd = NB >= 4 ? NB / 4 : 1;  // 32-bit words per B / C row
     // f32 B / C staging: a step's row is the N values of B, then the N of C,
     // padded by 4 floats.  f32 io is copied straight into it (double
-    // buffered); 16-bit rows are copied raw and converted once.
+    // buffered); 16-bit rows are copied raw and converted once.  (Unlike the
+    // backward, the forward keeps no packed bf16 rows: it is bound by latency,
+    // not by the shared-memory data pipe, and widening them in the scan sits
+    // on the path to the decays.)
     static constexpr int BCF = 2 * N + 4;
     static constexpr bool BC_DIRECT = ESZ == 4;
     static constexpr bool BC_RAW = !BC_DIRECT && NB >= 4;
@@ -293,27 +296,29 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
 
         // ---- scan: 32 steps of the lane's 2 x S states.  Steps past t_end (last
         // tile only) carry delta_eff = 0 and B = 0: the state stays unchanged.
-        // Software-pipelined by one step: the decays and input terms of step
-        // i + 1 (loads, exponents, MUFU) are formed before the recurrence of
+        // Software-pipelined by two steps: the decays and input terms of step
+        // i + 2 (loads, exponents, MUFU) are formed before the recurrence of
         // step i, which is the only part that waits on the previous state.
         const float* bcrow = &sBC[C::BC_DIRECT ? buf : 0][0][0];
-        float2 daN[S], xbN[S];  // decays and input terms of the next step
-        float cN[S] = {};       // its C values
-        auto prep = [&](int i) {
+        // decays, input terms and C values of the next two steps, by step parity
+        float2 daQ[2][S], xbQ[2][S];
+        float cQ[2][S] = {};
+        auto prep = [&](int i, int sl) {
             const float4 du = sDU[i][pp];
             const float2 dl2 = make_float2(du.x, du.y), dlu2 = make_float2(du.z, du.w);
             if (SUMMARY) sdp = add2(sdp, dl2);  // delta_eff of steps past t_end is zero
             float Bv[S];
             ld_f32<S>(bcrow + i * BCF + n0, Bv);
-            if (!NOY) ld_f32<S>(bcrow + i * BCF + N + n0, cN);
+            if (!NOY) ld_f32<S>(bcrow + i * BCF + N + n0, cQ[sl]);
 #pragma unroll
             for (int s = 0; s < S; s++) {
                 const float2 ex = mul2(dl2, A2[s]);
-                daN[s] = make_float2(ex2a(ex.x), ex2a(ex.y));
-                xbN[s] = mul2(dlu2, splat2(Bv[s]));
+                daQ[sl][s] = make_float2(ex2a(ex.x), ex2a(ex.y));
+                xbQ[sl][s] = mul2(dlu2, splat2(Bv[s]));
             }
         };
-        prep(0);
+        prep(0, 0);
+        prep(1, 1);
 #pragma unroll
         for (int i = 0; i < kRow; i++) {
             if (SAVE && (i % kSub) == 0) {
@@ -333,15 +338,16 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
                     }
                 }
             }
+            const int sl = i & 1;
             float2 da[S], xb[S];
             float Cv[S];
 #pragma unroll
             for (int s = 0; s < S; s++) {
-                da[s] = daN[s];
-                xb[s] = xbN[s];
-                Cv[s] = cN[s];
+                da[s] = daQ[sl][s];
+                xb[s] = xbQ[sl][s];
+                Cv[s] = cQ[sl][s];
             }
-            if (i + 1 < kRow) prep(i + 1);
+            if (i + 2 < kRow) prep(i + 2, sl);
 #pragma unroll
             for (int s = 0; s < S; s++) h[s] = fma2(da[s], h[s], xb[s]);
             if (!NOY) {

@@ -136,6 +136,23 @@ __device__ __forceinline__ float2 sigmoid2(float2 x) {
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// The low bf16 of w as f32 by a byte permute (kept off the FP32 pipe, where a
+// shift may be issued as an integer multiply-add).
+__device__ __forceinline__ float bf16lo_prmt(uint32_t w) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, 0x1044;" : "=r"(r) : "r"(w), "r"(0u));
+    return __uint_as_float(r);
+}
+
+// Four consecutive bf16 values at p (8-byte aligned shared memory) as f32.
+__device__ __forceinline__ void ld_bf16x4(const void* p, float (&v)[4]) {
+    const uint2 w = *reinterpret_cast<const uint2*>(p);
+    v[0] = bf16lo_prmt(w.x);
+    v[1] = bf16hi(w.x);
+    v[2] = bf16lo_prmt(w.y);
+    v[3] = bf16hi(w.y);
+}
+
 // Round-to-nearest-even f32 -> bf16 of two values, packed lo | hi << 16.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
