@@ -72,6 +72,11 @@ def a_from_log(A_log):
     return -np.exp(np.asarray(A_log, np.float64))
 
 
+def dA_log_rows(dA_rows, A_rows):
+    """Chain rule of A = -exp(A_log): dA_log = dA * dA/dA_log = dA * A, per row's (d, n)."""
+    return dA_rows * A_rows
+
+
 @dataclass
 class BwdResult:
     du: np.ndarray
@@ -165,9 +170,9 @@ class Oracle:
                                     _ptr(dC), nthreads or default_threads(), _ptr(h0), _ptr(dlast), _ptr(dh0))
         if rc != 0:
             raise RuntimeError(f"ss_oracle_bwd failed with code {rc}")
-        if A_log is not None:  # chain rule of A = -exp(A_log): dA_log = dA * A, per row's (d, n)
+        if A_log is not None:  # chain rule of A = -exp(A_log), per row's (d, n)
             d_of_row = (r if r is not None else np.arange(Bsz * Dch)) % Dch
-            dA_rows = dA_rows * A[d_of_row]
+            dA_rows = dA_log_rows(dA_rows, A[d_of_row])
         res = BwdResult(du, dd, dz, None, None, None, dB, dC, dA_rows, dD_rows, db_rows, dh0)
         if rows is None:
             res.du = du.reshape(Bsz, Dch, L).transpose(0, 2, 1).copy()

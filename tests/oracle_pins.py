@@ -423,6 +423,50 @@ def check_finite_differences_state(orc):
             assert err < 1e-6, (f"finite differences {gname} (h0, dlast, A_log)", ci, v, err)
 
 
+def check_a_log_map(orc):
+    """The A_log form against the A form.  A_log = log(n + 1) for the workload's
+    A = -(n + 1) gives the same forward; for random A_log, A = -exp(A_log) formed here
+    from the convention mamba-rs trains A through gives the same forward bit for bit,
+    and the backward's dA_log equals dA * A (the chain rule of that map), every other
+    gradient unchanged."""
+    x = _inputs(150, 2, 9, 3, 4)
+    r_a = _fwd_s(orc, x)
+    r_l = _fwd_s(orc, x, A_log=np.log(np.arange(1, 5, dtype=np.float64))[None, :].repeat(3, axis=0))
+    assert np.allclose(x["A"], -np.arange(1, 5)[None, :]), "workload A = -(n + 1)"
+    assert normwise(r_l.y, r_a.y) < 1e-13 and normwise(r_l.last_state, r_a.last_state) < 1e-13, "A_log = log(n + 1)"
+    rng = _rng(151)
+    A_log = rng.uniform(-1.5, 1.0, size=x["A"].shape)
+    xa = dict(x)
+    xa["A"] = -np.exp(A_log)
+    rf, rl = _fwd_s(orc, xa), _fwd_s(orc, x, A_log=A_log)
+    assert np.array_equal(rf.y, rl.y) and np.array_equal(rf.last_state, rl.last_state), "A_log forward"
+    gf, gl = _bwd_s(orc, xa), _bwd_s(orc, x, A_log=A_log)
+    assert normwise(gl.dA, gf.dA * xa["A"]) < 1e-13, "dA_log = dA * A"
+    for k in ("du", "ddelta", "dz", "dB", "dC", "dD", "ddelta_bias"):
+        assert np.array_equal(getattr(gl, k), getattr(gf, k)), ("A_log backward", k)
+
+
+def check_bwd_rows_subset(orc):
+    """A row-subset backward reproduces the full backward: du, ddelta, dz and each
+    row's dA / dD / ddelta_bias contributions element by element for a shuffled row
+    list, and dB / dC of a whole batch entry when the subset is that entry's rows."""
+    Bsz, L, Dch, N = 2, 11, 5, 3
+    x = _inputs(160, Bsz, L, Dch, N)
+    args = (x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], True)
+    full = orc.bwd(*args, dy=x["dy"], nthreads=2)
+    rows = np.array([7, 0, 3, 9, 5])
+    r = orc.bwd(*args, dy=x["dy"], rows=rows, want_dBdC=False, nthreads=2)
+    for i, row in enumerate(rows):
+        b, d = divmod(int(row), Dch)
+        for k in ("du", "ddelta", "dz"):
+            assert np.array_equal(getattr(r, k)[i], getattr(full, k)[b, :, d]), ("rows backward", k, row)
+        assert np.array_equal(r.dA_rows[i], full.dA_rows[row]), ("rows backward dA", row)
+        assert r.dD_rows[i] == full.dD_rows[row] and r.dbias_rows[i] == full.dbias_rows[row], ("rows dD / dbias", row)
+    entry = orc.bwd(*args, dy=x["dy"], rows=np.arange(Dch, 2 * Dch), want_dBdC=True, nthreads=2)
+    assert normwise(entry.dB[1], full.dB[1]) < 1e-14 and normwise(entry.dC[1], full.dC[1]) < 1e-14, "entry dB / dC"
+    assert not np.any(entry.dB[0]) and not np.any(entry.dC[0]), "rows of one entry add nothing to the other"
+
+
 ALL_CHECKS = [
     check_L1_closed_form,
     check_N1_geometric,
@@ -437,4 +481,6 @@ ALL_CHECKS = [
     check_h0_one_step,
     check_h0_split,
     check_finite_differences_state,
+    check_a_log_map,
+    check_bwd_rows_subset,
 ]

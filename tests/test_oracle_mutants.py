@@ -9,6 +9,7 @@ i.e. the pins would have caught that mistake in the real oracle.
 
 import os
 
+import numpy as np
 import pytest
 
 import oracle
@@ -61,6 +62,17 @@ MUTANTS = [
     ("bwd: dlast ignored", "s->lam[n] = p->dlast ? p->dlast[at_bdn(p, b, d, n)] : 0.0;", "s->lam[n] = 0.0;", 0),
     ("bwd: dh0 without the first decay", "dh0[n] = L > 0 ? s->a[n] * s->lam[n] : s->lam[n];", "dh0[n] = s->lam[n];", 0),
     ("bwd: dh0 with the last decay", "dh0[n] = L > 0 ? s->a[n] * s->lam[n]", "dh0[n] = L > 0 ? s->a[(L - 1) * N + n] * s->lam[n]", 0),
+    ("bwd: row list ignored", "int64_t r = row_id(j, i), b = r / p->Dch, d = r % p->Dch;\n            bwd_row",
+     "int64_t r = i, b = r / p->Dch, d = r % p->Dch;\n            bwd_row", 0),
+]
+
+# Mistakes in the oracle's Python layer (the A_log map and its chain rule):
+# (label, module attribute, replacement)
+PY_MUTANTS = [
+    ("A_log: sign", "a_from_log", lambda A_log: np.exp(np.asarray(A_log, np.float64))),
+    ("A_log: exp dropped", "a_from_log", lambda A_log: -np.asarray(A_log, np.float64)),
+    ("dA_log: chain rule dropped", "dA_log_rows", lambda dA_rows, A_rows: dA_rows),
+    ("dA_log: divided by A", "dA_log_rows", lambda dA_rows, A_rows: dA_rows / A_rows),
 ]
 
 
@@ -89,3 +101,19 @@ def test_pins_catch_mutant(tmp_path, label, old, new, occ):
         except (AssertionError, RuntimeError, FloatingPointError) as e:  # noqa: PERF203
             caught.append((check.__name__, str(e)[:80]))
     assert caught, f"no pin caught mutant: {label}"
+
+
+def _caught(orc):
+    caught = []
+    for check in P.ALL_CHECKS:
+        try:
+            check(orc)
+        except (AssertionError, RuntimeError, FloatingPointError) as e:  # noqa: PERF203
+            caught.append((check.__name__, str(e)[:80]))
+    return caught
+
+
+@pytest.mark.parametrize("label,name,fn", PY_MUTANTS, ids=[m[0] for m in PY_MUTANTS])
+def test_pins_catch_python_mutant(monkeypatch, label, name, fn):
+    monkeypatch.setattr(oracle, name, fn)
+    assert _caught(oracle.Oracle()), f"no pin caught mutant: {label}"
