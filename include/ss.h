@@ -98,7 +98,10 @@ int ss_fwd(const void *u, const void *delta, const float *A, const void *B, cons
  * calls on one stream are safe.  Nothing in the array needs clearing between
  * calls.  The first call on a device that uses the scratch looks up the
  * array's device address (cudaGetSymbolAddress) with that device current;
- * make that first call before any stream capture.
+ * make that first call before any stream capture.  That address is kept per
+ * device ordinal for the life of the process, which assumes the runtime's one
+ * primary context per device: a process that calls cudaDeviceReset on a
+ * device must not call this function on it afterwards.
  */
 #define SS_FWD_NOALLOC_MAX_SCRATCH_BYTES ((size_t)2 << 20)
 int ss_fwd_noalloc(const void *u, const void *delta, const float *A, const void *B, const void *C, const float *D,
@@ -111,10 +114,10 @@ int ss_fwd_noalloc(const void *u, const void *delta, const float *A, const void 
  * the forward walk ss_bwd has to redo.  The pages this library follows have
  * a backward-owned record of every state (baracuda-kernels
  * `selective_scan.rs`, "Workspace": B * D * L * N elements written by the
- * backward's first pass); here the forward keeps one state in four steps.
+ * backward's first pass); here the forward keeps one state in eight steps.
  *   saved         device buffer of at least ss_saved_bytes(...) bytes, 16-byte
  *                 aligned; opaque to the caller.  It receives the f32 state h
- *                 of every (b, d) row at every 4th step of L rounded up to 32
+ *                 of every (b, d) row at every 8th step of L rounded up to 32
  *                 steps and, when z is given, the f32 pre-gate readout
  *                 sum_n h C + D u of every (b, t, d) (which the backward's dz
  *                 needs); without z that last part is left unwritten and

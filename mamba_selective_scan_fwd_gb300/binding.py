@@ -130,11 +130,36 @@ def _p(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def stream_handle(stream=None):
+def stream_handle(stream=None, device=None):
+    """The CUDA stream handle of ``stream``, or of the current stream of ``device``
+    (the current device when None)."""
     import torch
 
-    s = stream if stream is not None else torch.cuda.current_stream()
+    s = stream if stream is not None else torch.cuda.current_stream(device)
     return ctypes.c_void_p(s.cuda_stream)
+
+
+class _on_device:
+    """Run a library call with the tensors' GPU as the current device: the library
+    launches on the current device and reads its per-device state there, so the
+    tensors, the stream and the current device must agree.  A caller's stream on
+    another device is refused."""
+
+    def __init__(self, t, stream):
+        import torch
+
+        if t.device.type != "cuda":
+            raise ValueError(f"tensors must be CUDA tensors, got {t.device}")
+        if stream is not None and stream.device != t.device:
+            raise ValueError(f"stream is on {stream.device}, the tensors on {t.device}")
+        self._ctx = torch.cuda.device(t.device)
+
+    def __enter__(self):
+        self._ctx.__enter__()
+        return self
+
+    def __exit__(self, *exc):
+        return self._ctx.__exit__(*exc)
 
 
 def _require(t, name, shape, dtype, device):
@@ -203,7 +228,9 @@ def _nbytes(t):
     return 0 if t is None else t.numel() * t.element_size()
 
 
-def _fwd_prepare(u, delta, A, B, C, D, z, delta_bias, y, last_state, return_last_state):
+def _fwd_prepare(u, delta, A, B, C, D, z, delta_bias, y, last_state, return_last_state, allocate=True):
+    """Check the forward's tensors (shapes, dtypes, contiguity, one device) and, when
+    ``allocate``, create y and last_state that are not given."""
     import torch
 
     Bsz, L, Dch = u.shape
@@ -222,9 +249,11 @@ def _fwd_prepare(u, delta, A, B, C, D, z, delta_bias, y, last_state, return_last
     if delta_bias is not None:
         _require(delta_bias, "delta_bias", (Dch,), torch.float32, dev)
     if y is None:
+        if not allocate:
+            raise ValueError("y must be given (this entry point allocates nothing)")
         y = torch.empty((Bsz, L, Dch), dtype=io, device=dev)
     _require(y, "y", (Bsz, L, Dch), io, dev)
-    if last_state is None and return_last_state:
+    if last_state is None and return_last_state and allocate:
         last_state = torch.empty((Bsz, Dch, N), dtype=torch.float32, device=dev)
     if last_state is not None:
         _require(last_state, "last_state", (Bsz, Dch, N), torch.float32, dev)
@@ -237,9 +266,10 @@ def ss_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, y=
     (Bsz, L, Dch, N), y, last_state = _fwd_prepare(u, delta, A, B, C, D, z, delta_bias, y, last_state,
                                                    return_last_state)
     dt = dtype_id(u)
-    workspace, wsb = _workspace(fwd_workspace_bytes(Bsz, L, Dch, N, dt), u.device, workspace)
-    rc = lib().ss_fwd(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias), int(bool(softplus)),
-                      _p(y), _p(last_state), Bsz, L, Dch, N, dt, _p(workspace), wsb, stream_handle(stream))
+    with _on_device(u, stream):
+        workspace, wsb = _workspace(fwd_workspace_bytes(Bsz, L, Dch, N, dt), u.device, workspace)
+        rc = lib().ss_fwd(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias), int(bool(softplus)),
+                          _p(y), _p(last_state), Bsz, L, Dch, N, dt, _p(workspace), wsb, stream_handle(stream, u.device))
     _check("ss_fwd", rc)
     return y, last_state
 
@@ -254,12 +284,13 @@ def ss_fwd_save(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=Tru
     (Bsz, L, Dch, N), y, last_state = _fwd_prepare(u, delta, A, B, C, D, z, delta_bias, y, last_state,
                                                    return_last_state)
     dt = dtype_id(u)
-    if saved is None:
-        saved = torch.empty(max(saved_bytes(Bsz, L, Dch, N, dt), 16), dtype=torch.uint8, device=u.device)
-    workspace, wsb = _workspace(fwd_workspace_bytes(Bsz, L, Dch, N, dt), u.device, workspace)
-    rc = lib().ss_fwd_save(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias),
-                           int(bool(softplus)), _p(y), _p(last_state), _p(saved), _nbytes(saved), Bsz, L, Dch, N,
-                           dt, _p(workspace), wsb, stream_handle(stream))
+    with _on_device(u, stream):
+        if saved is None:
+            saved = torch.empty(max(saved_bytes(Bsz, L, Dch, N, dt), 16), dtype=torch.uint8, device=u.device)
+        workspace, wsb = _workspace(fwd_workspace_bytes(Bsz, L, Dch, N, dt), u.device, workspace)
+        rc = lib().ss_fwd_save(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias),
+                               int(bool(softplus)), _p(y), _p(last_state), _p(saved), _nbytes(saved), Bsz, L, Dch, N,
+                               dt, _p(workspace), wsb, stream_handle(stream, u.device))
     _check("ss_fwd_save", rc)
     return y, last_state, saved
 
@@ -268,13 +299,16 @@ def ss_fwd_noalloc(u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state=
     """Forward selective scan that allocates nothing, for callers that cannot
     allocate device memory at the call site: y (and last_state, if given) must
     be preallocated, and the chunk-carry scratch is the library's own fixed
-    device array instead of a workspace.  Raises SSError when the problem
-    needs more scratch than that array holds."""
-    Bsz, L, Dch = u.shape
-    N = A.shape[1]
-    rc = lib().ss_fwd_noalloc(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias),
-                              int(bool(softplus)), _p(y), _p(last_state), Bsz, L, Dch, N, dtype_id(u),
-                              stream_handle(stream))
+    device array instead of a workspace.  The tensors are checked like ss_fwd's
+    (and y=None is refused rather than allocated).  Raises SSError when the
+    problem needs more scratch than that array holds."""
+    (Bsz, L, Dch, N), y, last_state = _fwd_prepare(u, delta, A, B, C, D, z, delta_bias, y, last_state,
+                                                   False, allocate=False)
+    dt = dtype_id(u)
+    with _on_device(u, stream):
+        rc = lib().ss_fwd_noalloc(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias),
+                                  int(bool(softplus)), _p(y), _p(last_state), Bsz, L, Dch, N, dt,
+                                  stream_handle(stream, u.device))
     _check("ss_fwd_noalloc", rc)
     return y, last_state
 
@@ -323,9 +357,11 @@ def ss_bwd(u, delta, A, B, C, D, z, delta_bias, softplus, dy, out=None, workspac
     ddelta_bias (f32; the optional ones are None when their input is None)."""
     (Bsz, L, Dch, N), out = _bwd_prepare(u, delta, A, B, C, D, z, delta_bias, dy, out)
     dt = dtype_id(u)
-    workspace, wsb = _workspace(bwd_workspace_bytes(Bsz, L, Dch, N, dt), u.device, workspace)
-    rc = lib().ss_bwd(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias), int(bool(softplus)),
-                      _p(dy), *_grad_ptrs(out), Bsz, L, Dch, N, dt, _p(workspace), wsb, stream_handle(stream))
+    with _on_device(u, stream):
+        workspace, wsb = _workspace(bwd_workspace_bytes(Bsz, L, Dch, N, dt), u.device, workspace)
+        rc = lib().ss_bwd(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias), int(bool(softplus)),
+                          _p(dy), *_grad_ptrs(out), Bsz, L, Dch, N, dt, _p(workspace), wsb,
+                          stream_handle(stream, u.device))
     _check("ss_bwd", rc)
     return out
 
@@ -334,10 +370,11 @@ def ss_bwd_saved(u, delta, A, B, C, D, z, delta_bias, softplus, dy, saved, out=N
     """ss_bwd reading the states ss_fwd_save stored in ``saved`` for the same inputs."""
     (Bsz, L, Dch, N), out = _bwd_prepare(u, delta, A, B, C, D, z, delta_bias, dy, out)
     dt = dtype_id(u)
-    workspace, wsb = _workspace(bwd_saved_workspace_bytes(Bsz, L, Dch, N, dt), u.device, workspace)
-    rc = lib().ss_bwd_saved(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias),
-                            int(bool(softplus)), _p(dy), _p(saved), _nbytes(saved), *_grad_ptrs(out), Bsz, L, Dch, N,
-                            dt, _p(workspace), wsb, stream_handle(stream))
+    with _on_device(u, stream):
+        workspace, wsb = _workspace(bwd_saved_workspace_bytes(Bsz, L, Dch, N, dt), u.device, workspace)
+        rc = lib().ss_bwd_saved(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias),
+                                int(bool(softplus)), _p(dy), _p(saved), _nbytes(saved), *_grad_ptrs(out), Bsz, L, Dch,
+                                N, dt, _p(workspace), wsb, stream_handle(stream, u.device))
     _check("ss_bwd_saved", rc)
     return out
 
@@ -373,7 +410,9 @@ def ss_fwd_ex(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True,
     d.saved_bytes, d.workspace_bytes = _nbytes(saved), wsb
     d.Bsz, d.L, d.Dch, d.N = Bsz, L, Dch, N
     d.dtype, d.softplus, d.a_is_log, d.reserved = dt, int(bool(softplus)), int(bool(a_is_log)), 0
-    _check("ss_fwd_ex", lib().ss_fwd_ex(ctypes.byref(d), stream_handle(stream)))
+    with _on_device(u, stream):
+        rc = lib().ss_fwd_ex(ctypes.byref(d), stream_handle(stream, u.device))
+    _check("ss_fwd_ex", rc)
     return y, last_state, saved
 
 
@@ -408,7 +447,9 @@ def ss_bwd_ex(u, delta, A, B, C, D, z, delta_bias, softplus, dy, h0=None, dlast_
     d.saved_bytes, d.workspace_bytes = _nbytes(saved), wsb
     d.Bsz, d.L, d.Dch, d.N = Bsz, L, Dch, N
     d.dtype, d.softplus, d.a_is_log, d.reserved = dt, int(bool(softplus)), int(bool(a_is_log)), 0
-    _check("ss_bwd_ex", lib().ss_bwd_ex(ctypes.byref(d), stream_handle(stream)))
+    with _on_device(u, stream):
+        rc = lib().ss_bwd_ex(ctypes.byref(d), stream_handle(stream, dev))
+    _check("ss_bwd_ex", rc)
     return out
 
 
@@ -433,8 +474,9 @@ def ss_decode_step(u, delta, A, B, C, D, z, delta_bias, softplus, state, y=None,
     if y is None:
         y = torch.empty((Bsz, Dch), dtype=io, device=dev)
     _require(y, "y", (Bsz, Dch), io, dev)
-    rc = lib().ss_decode_step(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias),
-                              int(bool(softplus)), int(bool(a_is_log)), _p(state), _p(y), Bsz, Dch, N, dtype_id(u),
-                              stream_handle(stream))
+    with _on_device(u, stream):
+        rc = lib().ss_decode_step(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias),
+                                  int(bool(softplus)), int(bool(a_is_log)), _p(state), _p(y), Bsz, Dch, N,
+                                  dtype_id(u), stream_handle(stream, dev))
     _check("ss_decode_step", rc)
     return y

@@ -22,7 +22,11 @@
 // cudaGetSymbolAddress and cached: the first call on a device that uses the
 // scratch (a problem cut into several time chunks) does this set-up with
 // that device current.  That first call should come before any stream
-// capture begins.
+// capture begins.  The cache is keyed by device ordinal and assumes the
+// runtime's one primary context per device for the life of the process: after
+// cudaDeviceReset (which destroys that context and unloads the library's
+// device code) the cached address is stale, so a process that resets a device
+// must not call this entry point on it again.
 #include <cuda_runtime.h>
 
 #include <mutex>

@@ -11,10 +11,16 @@ Tolerances (Mamba-1 selective scan accuracy targets):
 "Normwise relative error" of a tensor is max|got - ref| / max|ref| (a
 reference tensor that is all zero is compared absolutely).  An elementwise
 ratio is not used because y = sum_n h C cancels: near-zero outputs would
-measure the cancellation, not the kernel.
+measure the cancellation, not the kernel.  The parity gates take that measure
+per row -- each (b, d) row of the [B, L, D] outputs, each batch row of dB / dC
+-- and bound the worst row, so that an error confined to rows of small
+magnitude is not hidden under the largest row's scale.
 """
 
 from __future__ import annotations
+
+import json
+import os
 
 import numpy as np
 import torch
@@ -56,6 +62,55 @@ def normwise(got, ref) -> float:
     scale = np.max(np.abs(ref))
     err = np.max(np.abs(got - ref))
     return float(err / scale) if scale > 0 else float(err)
+
+
+def normwise_rows(got, ref, rows_axis) -> float:
+    """The worst per-row normwise error: rows_axis names the axes that index a row
+    (the others are reduced within it): (0, 2) for the (b, d) rows of [B, L, D],
+    (0,) for the batch rows of [B, L, N], () for the whole tensor."""
+    if isinstance(got, torch.Tensor):
+        got = got.detach().float().cpu().double().numpy()
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    if ref.size == 0:
+        return 0.0
+    if not np.array_equal(np.isfinite(got), np.isfinite(ref)):
+        return float("inf")
+    red = tuple(a for a in range(ref.ndim) if a not in rows_axis)
+    err = np.max(np.abs(got - ref), axis=red, keepdims=False)
+    scale = np.max(np.abs(ref), axis=red, keepdims=False)
+    rel = np.where(scale > 0, err / np.where(scale > 0, scale, 1.0), err)
+    return float(np.max(rel))
+
+
+# axes that index a row of each output (see normwise_rows)
+ROWS = {"y": (0, 2), "du": (0, 2), "ddelta": (0, 2), "dz": (0, 2), "dB": (0,), "dC": (0,), "last_state": (),
+        "dA": (), "dD": (), "ddelta_bias": ()}
+
+
+def elementwise_diag(got, ref) -> dict:
+    """The elementwise diagnostic |got - ref| / (|ref| + 1e-3 rms(ref)): its maximum
+    and 99th percentile (reported, not gated)."""
+    if isinstance(got, torch.Tensor):
+        got = got.detach().float().cpu().double().numpy()
+    got = np.asarray(got, np.float64).reshape(-1)
+    ref = np.asarray(ref, np.float64).reshape(-1)
+    rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
+    e = np.abs(got - ref) / (np.abs(ref) + 1e-3 * rms + 1e-300)
+    return {"max": float(np.max(e)) if e.size else 0.0, "p99": float(np.percentile(e, 99)) if e.size else 0.0}
+
+
+def report(config: str, output: str, got, ref, rows_axis=None):
+    """Append the achieved errors of one output to the JSON-lines file named by the
+    SS_PARITY_REPORT environment variable (nothing when it is unset)."""
+    path = os.environ.get("SS_PARITY_REPORT")
+    if not path:
+        return
+    rec = {"config": config, "output": output, "normwise": normwise(got, ref),
+           "normwise_rows": normwise_rows(got, ref, ROWS.get(output, ()) if rows_axis is None else rows_axis)}
+    rec.update({f"elementwise_{k}": v for k, v in elementwise_diag(got, ref).items()})
+    with open(path, "a") as f:
+        f.write(json.dumps(rec) + "\n")
 
 
 def gpu_fwd(t, softplus=True):

@@ -270,3 +270,31 @@ def test_source_digest_sees_code_not_comments():
     assert build._code(a) == build._code(b)
     assert build._code(a) != build._code(a.replace("x + 1", "x + 2"))
     assert '"a // b"' in build._code(a)
+
+
+def test_binding_checks_before_any_launch():
+    """The Python wrappers refuse malformed tensors before calling the library:
+    a transposed (non-contiguous) u, a B of another dtype, y = None for the
+    entry point that allocates nothing, and tensors that are not on a GPU."""
+    import torch
+
+    from mamba_selective_scan_fwd_gb300 import binding
+
+    Bsz, L, Dch, N = 1, 8, 4, 4
+    u = torch.zeros((Bsz, L, Dch))
+    A = -torch.ones((Dch, N))
+    Bm = torch.zeros((Bsz, L, N))
+    y = torch.zeros((Bsz, L, Dch))
+    ut = torch.zeros((Bsz, Dch, L)).transpose(1, 2)
+    with pytest.raises(ValueError, match="contiguous"):
+        binding.ss_fwd_noalloc(ut, u, A, Bm, Bm, None, None, None, True, y)
+    with pytest.raises(TypeError, match="dtype"):
+        binding.ss_fwd_noalloc(u, u, A, Bm.to(torch.float64), Bm, None, None, None, True, y)
+    with pytest.raises(ValueError, match="allocates nothing"):
+        binding.ss_fwd_noalloc(u, u, A, Bm, Bm, None, None, None, True, None)
+    with pytest.raises(ValueError, match="shape"):
+        binding.ss_fwd_noalloc(u, u, A, Bm, Bm, None, None, None, True, torch.zeros((Bsz, L, Dch + 1)))
+    with pytest.raises(ValueError, match="CUDA"):
+        binding.ss_fwd_noalloc(u, u, A, Bm, Bm, None, None, None, True, y)
+    with pytest.raises(ValueError, match="CUDA"):
+        binding.ss_fwd(u, u, A, Bm, Bm)

@@ -5,8 +5,11 @@ allocator must not be bypassed, cannot hand the library a freshly allocated
 workspace.  ss_fwd_noalloc keeps the forward's chunk-carry scratch in a fixed
 device array owned by the library instead.  These tests call it through the
 C ABI on problems that are cut into many time chunks (so the scratch is
-really used, up to exactly its 2 MiB limit), twice in a row, and compare
-each result with the regular ss_fwd given a caller-allocated workspace.  A
+really used, up to exactly its 2 MiB limit), twice in a row with a
+different chunked problem run through the same scratch in between, and
+require each result to equal, bit for bit, the regular ss_fwd given a
+caller-allocated workspace (same plan, same kernels: only the scratch's
+address differs, so any read of summaries the call did not write shows).  A
 problem that needs more scratch than the array holds must be rejected.
 
 This file is collected last so that a run stopping at the first failure has
@@ -21,7 +24,7 @@ import torch
 import mamba_selective_scan_fwd_gb300 as ss
 from mamba_selective_scan_fwd_gb300 import binding
 from mamba_selective_scan_fwd_gb300.inputs import small_inputs
-from gpu_util import TOL, IO_DTYPE, normwise, to_device
+from gpu_util import IO_DTYPE, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -51,14 +54,19 @@ def test_noalloc_matches_regular_forward_twice(shape, io):
     x = small_inputs(Bsz, L, Dch, N, io=io, seed=4242 + L)
     t = to_device(x, io)
     y_ref, last_ref = ss.ss_fwd(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"], True)
+    # another chunked problem, run through the same scratch between the two calls
+    xo = small_inputs(1, 3000, 40, 16, io="f32", seed=99)
+    to = to_device(xo, "f32")
+    assert ss.fwd_workspace_bytes(1, 3000, 40, 16, binding.SS_F32) > 0
+    yo = torch.empty((1, 3000, 40), dtype=torch.float32, device="cuda")
     torch.cuda.synchronize()
     for _ in range(2):
         y = torch.full((Bsz, L, Dch), float("nan"), dtype=IO_DTYPE[io], device="cuda")
         last = torch.full((Bsz, Dch, N), float("nan"), dtype=torch.float32, device="cuda")
         assert _noalloc_raw(t, y, last, io) == 0
         torch.cuda.synchronize()
-        assert normwise(y, y_ref.float().cpu().double().numpy()) <= TOL[io]["fwd"]
-        assert normwise(last, last_ref.cpu().double().numpy()) <= TOL[io]["fwd"]
+        assert torch.equal(y, y_ref) and torch.equal(last, last_ref)
+        assert _noalloc_raw(to, yo, None, "f32") == 0
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
