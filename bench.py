@@ -36,6 +36,9 @@ from mamba_selective_scan_fwd_gb300.inputs import WORKLOADS, make_inputs  # noqa
 METRIC = "selective-scan fwd+bwd elements/s (B·L·D) and HBM GB/s vs GB300 peak"
 UNIT = "elements/s"
 WORKLOAD = WORKLOADS[3]  # mamba2.8b-layer-bf16: the workload the metric is quoted on
+# the other full-size workloads, each timed as a block of its own: the
+# Mamba-130M layer forward (bf16) and training step (f32), and the long sequence
+PER_WORKLOAD = (1, 2, 4)
 
 
 def pick_workload(name):
@@ -79,8 +82,8 @@ def mufu_counts(w):
 # figure stale, and it is reported as null.
 TRAFFIC = {
     # both launches of the main pass (608 one-chunk units; 32 units x 19 chunks)
-    ("k_bwd2_main", "mamba2.8b-layer-bf16"): 3626368256,  # 2233.0 + 119.1 MB read, 1241.8 + 32.5 MB written
-    ("k_fwd2_y", "mamba2.8b-layer-bf16"): 2228526336,     # 479.7 + 26.8 MB read, 1690.9 + 31.1 MB written
+    ("k_bwd_main", "mamba2.8b-layer-bf16"): 3626368256,  # 2233.0 + 119.1 MB read, 1241.8 + 32.5 MB written
+    ("k_fwd_y", "mamba2.8b-layer-bf16"): 2228526336,     # 479.7 + 26.8 MB read, 1690.9 + 31.1 MB written
 }
 TRAFFIC_SRC_DIGEST = "2a8d031df0ea7598"
 
@@ -100,12 +103,6 @@ def load_peaks():
             p = json.load(f)
         return float(p["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
-
-
-# MUFU ex2 results per clock per SM on GB300 (sm_103a), measured by a
-# dependent-free ex2.approx.f32 throughput loop; the SFU roofline of the scan
-# is B*L*D*N exponentials per direction at SMs x this rate x SM clock.
-EX2_PER_CLK_PER_SM = 32.0
 
 
 class ClockSampler:
@@ -242,101 +239,275 @@ def measure_decode(dev, hbm_peak, peak_kind, steps=50):
                          "algorithmic_bytes": nbytes}}
 
 
-def run_ours(args):
+IO_KEYS = ("u", "delta", "B", "C", "z", "dy")
+
+
+def config_of(w, world):
+    """The ``config`` dict of a workload's line (the same in both arms)."""
+    fwd_b, bwd_b = algorithmic_bytes(w)
+    step_b = fwd_b + (bwd_b if w.backward else 0)
+    return {"workload": w.name, "Bsz": w.Bsz, "L": w.L, "Dch": w.Dch, "N": w.N, "io": w.io,
+            "step": "ss_fwd_save + ss_bwd_saved" if w.backward else "ss_fwd",
+            "terms": "D, z, delta_bias, softplus, last_state",
+            "l2": f"no flush: each step moves {step_b / 1e6:.0f} MB, above the 129 MB L2",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
+class Runner:
+    """Device-resident inputs, outputs and workspaces of one workload, and its calls."""
+
+    def __init__(self, w, x, dev, stream, pin=False):
+        import torch
+
+        import mamba_selective_scan_fwd_gb300 as ss
+        from mamba_selective_scan_fwd_gb300 import binding
+
+        self.ss, self.w, self.dev, self.stream = ss, w, dev, stream
+        io_dt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[w.io]
+        self.host = {}
+        for k, v in x.items():
+            if v is None:
+                continue
+            t = torch.from_numpy(v)
+            if k in IO_KEYS:
+                t = t.to(io_dt)
+            self.host[k] = t.pin_memory() if pin else t
+        self.d = {k: v.to(dev) for k, v in self.host.items()}
+        for k in ("D", "z", "delta_bias", "dy"):
+            self.d.setdefault(k, None)
+        dt = binding.dtype_id(self.d["u"])
+        dims = (w.Bsz, w.L, w.Dch, w.N, dt)
+        self.plan = ss.plan_info(*dims)
+        self.staging = "tma" if ss.staging_uses_tma(*dims) else "asynchronous copies"
+        u8 = torch.uint8
+        self.ws_f = torch.empty(max(ss.fwd_workspace_bytes(*dims), 256), dtype=u8, device=dev)
+        self.y = torch.empty((w.Bsz, w.L, w.Dch), dtype=io_dt, device=dev)
+        self.last = torch.empty((w.Bsz, w.Dch, w.N), dtype=torch.float32, device=dev)
+        self.grads = {}
+        if w.backward:
+            self.ws_b = torch.empty(ss.bwd_saved_workspace_bytes(*dims), dtype=u8, device=dev)
+            self.saved = torch.empty(ss.saved_bytes(*dims), dtype=u8, device=dev)
+            self.ws_r = None  # the recomputing backward's workspace, made on first use
+
+    def _args(self, d):
+        return (d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"], self.w.softplus)
+
+    def fwd(self):
+        self.ss.ss_fwd(*self._args(self.d), y=self.y, last_state=self.last, workspace=self.ws_f, stream=self.stream)
+
+    def fwd_save(self):
+        self.ss.ss_fwd_save(*self._args(self.d), y=self.y, last_state=self.last, saved=self.saved,
+                            workspace=self.ws_f, stream=self.stream)
+
+    def bwd_saved(self):
+        self.grads.update(self.ss.ss_bwd_saved(*self._args(self.d), self.d["dy"], self.saved, out=self.grads,
+                                               workspace=self.ws_b, stream=self.stream))
+
+    def bwd(self):
+        import torch
+
+        if self.ws_r is None:
+            w = self.w
+            dims = (w.Bsz, w.L, w.Dch, w.N, 0 if w.io == "f32" else 2 if w.io == "bf16" else 1)
+            self.ws_r = torch.empty(self.ss.bwd_workspace_bytes(*dims), dtype=torch.uint8, device=self.dev)
+        self.grads.update(self.ss.ss_bwd(*self._args(self.d), self.d["dy"], out=self.grads, workspace=self.ws_r,
+                                         stream=self.stream))
+
+    def first(self):
+        """The step's first call: the saving forward (or the forward of a forward-only step)."""
+        return self.fwd_save() if self.w.backward else self.fwd()
+
+    def step(self):
+        self.first()
+        if self.w.backward:
+            self.bwd_saved()
+
+    def step_recompute(self):
+        self.fwd()
+        self.bwd()
+
+    def launches(self):
+        return self.plan["fwd_kernels"] + (self.plan["bwd_saved_kernels"] if self.w.backward else 0)
+
+
+def time_steps(fn, K, dev, stream, world):
+    """Device time of exactly K calls of fn between two events on the launching stream (max over ranks)."""
     import torch
 
-    import mamba_selective_scan_fwd_gb300 as ss
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    return max_over_ranks(e0.elapsed_time(e1), world)
+
+
+def attribute(r, K):
+    """K more steps with events around each call and between the library's own
+    launches (it records them there): per-call and per-kernel average ms."""
+    import torch
+
     from mamba_selective_scan_fwd_gb300 import binding
 
-    world, rank, local = dist_setup("nccl")
-    dev = torch.device("cuda", local if world > 1 else 0)
-    w = pick_workload(args.workload)
-    x = make_inputs(w, with_dy=True)
-    io_dt = torch.bfloat16 if w.io == "bf16" else torch.float32
-    io_keys = ("u", "delta", "B", "C", "z", "dy")
-    host = {}
-    for k, v in x.items():
-        if v is None:
-            continue
-        t = torch.from_numpy(v)
-        if k in io_keys:
-            t = t.to(io_dt)
-        host[k] = t.pin_memory()
-    d = {k: v.to(dev, non_blocking=False) for k, v in host.items()}
-    for k in ("D", "z", "delta_bias"):
-        d.setdefault(k, None)
-    dtid = binding.dtype_id(d["u"])
-    plan = ss.plan_info(w.Bsz, w.L, w.Dch, w.N, dtid)
-    ws_f = torch.empty(max(ss.fwd_workspace_bytes(w.Bsz, w.L, w.Dch, w.N, dtid), 256), dtype=torch.uint8, device=dev)
-    ws_b = torch.empty(ss.bwd_saved_workspace_bytes(w.Bsz, w.L, w.Dch, w.N, dtid), dtype=torch.uint8, device=dev)
-    saved = torch.empty(ss.saved_bytes(w.Bsz, w.L, w.Dch, w.N, dtid), dtype=torch.uint8, device=dev)
-    y = torch.empty((w.Bsz, w.L, w.Dch), dtype=io_dt, device=dev)
-    last = torch.empty((w.Bsz, w.Dch, w.N), dtype=torch.float32, device=dev)
-    grads = {}
-    stream = torch.cuda.current_stream(dev)
-
-    def fwd():
-        ss.ss_fwd_save(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"], w.softplus,
-                       y=y, last_state=last, saved=saved, workspace=ws_f, stream=stream)
-
-    def bwd():
-        g = ss.ss_bwd_saved(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"], w.softplus,
-                            d["dy"], saved, out=grads, workspace=ws_b, stream=stream)
-        grads.update(g)
-
-    def step():
-        fwd()
-        bwd()
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
-
-    # ---- device-resident timing: exactly K steps between two events on the
-    # launching stream, nothing else in between
-    K = args.steps
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(local if world > 1 else 0)
-    clocks.start()
-    time.sleep(0.3)
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    start.record(stream)
-    for i in range(K):
-        step()
-    end.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    clk = clocks.stop()
-
-    # ---- attribution: the same K steps again with per-call and per-kernel
-    # events (the library records them between its own launches)
-    nf, nb = plan["fwd_kernels"], plan["bwd_saved_kernels"]
+    plan, stream = r.plan, r.stream
+    nf, nb = plan["fwd_kernels"], (plan["bwd_saved_kernels"] if r.w.backward else 0)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     kev_f = [[torch.cuda.Event(enable_timing=True) for _ in range(nf + 1)] for _ in range(K)]
     kev_b = [[torch.cuda.Event(enable_timing=True) for _ in range(nb + 1)] for _ in range(K)]
     for e in [e for row in kev_f + kev_b for e in row]:
         e.record(stream)  # creates the event handles the library records
-    torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(r.dev)
     for i in range(K):
         evs[i][0].record(stream)
         binding.profile_events(kev_f[i])
-        fwd()
+        r.first()
         evs[i][1].record(stream)
-        binding.profile_events(kev_b[i])
-        bwd()
+        if r.w.backward:
+            binding.profile_events(kev_b[i])
+            r.bwd_saved()
         evs[i][2].record(stream)
     binding.profile_events([])
-    torch.cuda.synchronize(dev)
-    total_ms = start.elapsed_time(end)
+    torch.cuda.synchronize(r.dev)
     t_fwd = sum(e[0].elapsed_time(e[1]) for e in evs) / K
-    t_bwd = sum(e[1].elapsed_time(e[2]) for e in evs) / K
-    # per-kernel averages: kernel j of a call runs between its events j and j + 1
-    k_fwd = [sum(r[j].elapsed_time(r[j + 1]) for r in kev_f) / K for j in range(nf)]
-    k_bwd = [sum(r[j].elapsed_time(r[j + 1]) for r in kev_b) / K for j in range(nb)]
-    total_ms = max_over_ranks(total_ms, world)
+    t_bwd = sum(e[1].elapsed_time(e[2]) for e in evs) / K if r.w.backward else 0.0
+    # kernel j of a call runs between its events j and j + 1
+    k_fwd = [sum(row[j].elapsed_time(row[j + 1]) for row in kev_f) / K for j in range(nf)]
+    k_bwd = [sum(row[j].elapsed_time(row[j + 1]) for row in kev_b) / K for j in range(nb)]
+    return t_fwd, t_bwd, k_fwd, k_bwd
+
+
+def analyse(w, plan, ms_per_step, t_fwd, t_bwd, k_fwd, k_bwd, peaks):
+    """Rooflines of the step, of its dominant kernel and of the forward's main pass.
+
+    A direction's roofline time is the slower of its algorithmic bytes at the
+    measured HBM copy bandwidth and its B*L*D*N scan exponentials at the
+    measured MUFU ex2 rate (SMs x ex2 per clock per SM x the sampled SM clock)."""
+    fwd_bytes, bwd_bytes = algorithmic_bytes(w)
+    # the backward's main kernel writes everything but dB / dC and dA / dD / ddelta_bias (the reductions do)
+    bwd_main_bytes = bwd_bytes - 2 * w.Bsz * w.L * w.N * 4 - 4 * (w.Dch * w.N + 2 * w.Dch)
+    hbm_peak = peaks["hbm_gbs"]
+    exp_peak = peaks["sms"] * peaks["ex2_per_clk_per_sm"] * peaks["sm_mhz"] * 1e6  # ex2 / s
+    exps = w.bld * w.N
+
+    def roof(bytes_, t_ms):
+        t_hbm = bytes_ / (hbm_peak * 1e9)
+        t_sfu = exps / exp_peak
+        if t_hbm >= t_sfu:
+            ach = bytes_ / (t_ms / 1e3) / 1e9
+            return {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
+                    "frac": round(ach / hbm_peak, 4), "peak_kind": f"{peaks['hbm_kind']} HBM copy",
+                    "roofline_ms": round(t_hbm * 1e3, 4), "algorithmic_bytes": bytes_}
+        ach = exps / (t_ms / 1e3) / 1e9
+        pk = exp_peak / 1e9
+        return {"bound": "alu", "achieved": round(ach, 1), "peak": round(pk, 1), "unit": "Gexp2/s",
+                "frac": round(ach / pk, 4),
+                "peak_kind": (f"MUFU ex2 (measured): {peaks['sms']} SMs x {peaks['ex2_per_clk_per_sm']:.2f}/clk x "
+                              f"{peaks['sm_mhz']:g} MHz (median sampled)"),
+                "roofline_ms": round(t_sfu * 1e3, 4), "algorithmic_bytes": bytes_}
+
+    # launch order of a call: the summary passes of the chunked segments, then
+    # each segment's main pass (then, in the backward, the two reductions)
+    segs = plan["segments"]
+    tag = [f"{u} units x {k} chunk{'s' if k > 1 else ''}" for u, k in segs]
+    first = "y + saved states" if w.backward else "y"
+    fwd_names = ([f"k_fwd chunk summary ({tag[i]})" for i, (_, k) in enumerate(segs) if k > 1] +
+                 [f"k_fwd {first} ({t})" for t in tag])
+    bwd_names = ([f"k_bwd reverse summary ({tag[i]})" for i, (_, k) in enumerate(segs) if k > 1] +
+                 [f"k_bwd main ({t})" for t in tag] + ["k_bwd_reduce_bc", "k_bwd_reduce_params"])
+    n_sum = sum(1 for _, k in segs if k > 1)
+    main = range(n_sum, n_sum + len(segs))  # a direction's main pass: one launch per segment
+    t_main_f = sum(k_fwd[j] for j in main)
+    launches = f"{len(segs)} launch{'es' if len(segs) > 1 else ''}"
+    r_fwd = roof(fwd_bytes, t_main_f)
+    r_fwd.update({"kernel": f"k_fwd main pass ({'ss_fwd_save' if w.backward else 'ss_fwd'}; {launches})",
+                  "ms": round(t_main_f, 4), "traffic": measured_traffic("k_fwd_y", w)})
+    out = {"hbm_gbs": round((fwd_bytes + (bwd_bytes if w.backward else 0)) / (ms_per_step / 1e3) / 1e9, 1),
+           "ns_per_element": round(ms_per_step * 1e6 / w.bld, 5)}
+    t_roof = roof(fwd_bytes, t_fwd)["roofline_ms"]
+    if w.backward:
+        t_main_b = sum(k_bwd[j] for j in main)
+        r_bwd = roof(bwd_main_bytes, t_main_b)
+        r_bwd.update({"kernel": f"k_bwd main pass (ss_bwd_saved; {launches})", "ms": round(t_main_b, 4),
+                      "traffic": measured_traffic("k_bwd_main", w)})
+        t_roof += roof(bwd_bytes, t_bwd)["roofline_ms"]
+        out.update({"roofline": r_bwd, "roofline_fwd": r_fwd})
+    else:
+        out["roofline"] = r_fwd
+    out["roofline_step_frac"] = round(t_roof / ms_per_step, 4)
+    out["fwd_ms"] = round(t_fwd, 4)
+    if w.backward:
+        out["bwd_ms"] = round(t_bwd, 4)
+    names = fwd_names + (bwd_names if w.backward else [])
+    out["kernel_ms"] = {n: round(v, 4) for n, v in zip(names, k_fwd + k_bwd)}
+    return out
+
+
+def measure_ex2_rate():
+    """MUFU ex2 results per clock per SM, measured by the library's probe kernel
+    (the first run warms up; the second is reported)."""
+    from mamba_selective_scan_fwd_gb300 import binding
+
+    binding.measure_ex2_rate(1024)
+    return binding.measure_ex2_rate(4096)
+
+
+def run_workload(w, dev, stream, world, K, warmup, peaks, cpu_seconds, rank):
+    """One per-workload block: the step's throughput and rooflines, and the oracle's rate."""
+    import torch
+
+    x = make_inputs(w, with_dy=w.backward)
+    r = Runner(w, x, dev, stream)
+    for _ in range(warmup):
+        r.step()
+    total = time_steps(r.step, K, dev, stream, world)
+    ms = total / K
+    t_fwd, t_bwd, k_fwd, k_bwd = attribute(r, K)
+    block = {"config": config_of(w, world), "steps": K, "ms_per_step": round(ms, 4),
+             "value": round(job_throughput(w.bld * K, world, total), 1), "unit": UNIT, "staging": r.staging,
+             "chunks": r.plan["chunks"]}
+    block.update(analyse(w, r.plan, ms, t_fwd, t_bwd, k_fwd, k_bwd, peaks))
+    del r
+    torch.cuda.empty_cache()
+    if rank == 0 and cpu_seconds > 0:
+        block["cpu_baseline"] = cpu_baseline(w, x, budget_s=cpu_seconds)
+    return block
+
+
+def run_ours(args):
+    import torch
+
+    world, rank, local = dist_setup("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    w = pick_workload(args.workload)
+    x = make_inputs(w, with_dy=True)
+    stream = torch.cuda.current_stream(dev)
+    r = Runner(w, x, dev, stream, pin=True)
+
+    for _ in range(args.warmup):
+        r.step()
+    torch.cuda.synchronize(dev)
+
+    # ---- device-resident timing: exactly K steps between two events on the
+    # launching stream, nothing else in between; clocks sampled meanwhile
+    K = args.steps
+    clocks = ClockSampler(local if world > 1 else 0)
+    clocks.start()
+    time.sleep(0.3)
+    total_ms = time_steps(r.step, K, dev, stream, world)
+    clk = clocks.stop()
     ms_per_step = total_ms / K
     value = job_throughput(w.bld * K, world, total_ms)
+    t_fwd, t_bwd, k_fwd, k_bwd = attribute(r, K)
+
+    # ---- the recomputing pair (ss_fwd + ss_bwd: the backward recomputes the
+    # restart states itself) on the same inputs
+    for _ in range(3):
+        r.step_recompute()
+    recompute_ms = time_steps(r.step_recompute, K, dev, stream, world) / K
 
     # ---- end to end through the public API with host buffers.  Every step copies
     # its inputs from pinned host memory and its outputs back; two sets of device
@@ -345,11 +516,12 @@ def run_ours(args):
     # step i + 1's (the restart states and workspaces stay on the compute
     # stream).  The output copy bounds it (1178 MB per step); splitting each
     # copy over two streams per direction was no faster.
+    ss, host, d = r.ss, r.host, r.d
     in_keys = [k for k in ("u", "delta", "A", "B", "C", "D", "z", "delta_bias", "dy") if k in host]
     h2d = sum(host[k].numel() * host[k].element_size() for k in in_keys)
-    out_host = {"y": torch.empty(y.shape, dtype=y.dtype).pin_memory(),
-                "last_state": torch.empty(last.shape, dtype=last.dtype).pin_memory()}
-    for k, v in grads.items():
+    out_host = {"y": torch.empty(r.y.shape, dtype=r.y.dtype).pin_memory(),
+                "last_state": torch.empty(r.last.shape, dtype=r.last.dtype).pin_memory()}
+    for k, v in r.grads.items():
         if v is not None:
             out_host[k] = torch.empty(v.shape, dtype=v.dtype).pin_memory()
     d2h = sum(v.numel() * v.element_size() for v in out_host.values())
@@ -357,7 +529,7 @@ def run_ours(args):
     sets = []
     for _ in range(2):
         di = {k: (None if v is None else torch.empty_like(v)) for k, v in d.items()}
-        sets.append({"d": di, "y": torch.empty_like(y), "last": torch.empty_like(last), "g": {}})
+        sets.append({"d": di, "y": torch.empty_like(r.y), "last": torch.empty_like(r.last), "g": {}})
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "done", "out")}
 
@@ -378,10 +550,11 @@ def run_ours(args):
                 stream.wait_event(ev["out"][j])  # step i - 2's outputs have left this set
             di = bs["d"]
             ss.ss_fwd_save(di["u"], di["delta"], di["A"], di["B"], di["C"], di["D"], di["z"], di["delta_bias"],
-                           w.softplus, y=bs["y"], last_state=bs["last"], saved=saved, workspace=ws_f, stream=stream)
+                           w.softplus, y=bs["y"], last_state=bs["last"], saved=r.saved, workspace=r.ws_f,
+                           stream=stream)
             bs["g"].update(ss.ss_bwd_saved(di["u"], di["delta"], di["A"], di["B"], di["C"], di["D"], di["z"],
-                                           di["delta_bias"], w.softplus, di["dy"], saved, out=bs["g"],
-                                           workspace=ws_b, stream=stream))
+                                           di["delta_bias"], w.softplus, di["dy"], r.saved, out=bs["g"],
+                                           workspace=r.ws_b, stream=stream))
             ev["done"][j].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev["done"][j])
@@ -410,75 +583,45 @@ def run_ours(args):
         e2e_runs.append(max_over_ranks(e0.elapsed_time(e1), world))
     e2e_ms = sorted(e2e_runs)[1]
     e2e_value = job_throughput(w.bld * e2e_steps, world, e2e_ms)
+    staging, plan, launches = r.staging, r.plan, r.launches()
+    gstatus = ss.device_status(stream)
+    del sets, r
+    torch.cuda.empty_cache()
 
-    # ---- roofline of the dominant kernel (the backward's main kernel) and of the forward kernel
+    # ---- peaks: the measured HBM copy bandwidth and MUFU ex2 rate
     hbm_peak, peak_kind = load_peaks()
-    fwd_bytes, bwd_bytes = algorithmic_bytes(w)
-    # the main backward kernel writes everything but dB / dC and dA / dD / ddelta_bias (the reductions do)
-    bwd_main_bytes = bwd_bytes - 2 * w.Bsz * w.L * w.N * 4 - 4 * (w.Dch * w.N + 2 * w.Dch)
-    props = torch.cuda.get_device_properties(dev)
-    sms = props.multi_processor_count
-    sm_mhz = clk.get("sm_mhz") or 2070.0
-    exp_peak = sms * EX2_PER_CLK_PER_SM * sm_mhz * 1e6  # ex2 / s
-    exps = w.bld * w.N
-
-    def roof(bytes_, t_ms):
-        t_hbm = bytes_ / (hbm_peak * 1e9)
-        t_sfu = exps / exp_peak
-        if t_hbm >= t_sfu:
-            ach = bytes_ / (t_ms / 1e3) / 1e9
-            return {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
-                    "frac": round(ach / hbm_peak, 4), "peak_kind": f"{peak_kind} HBM copy",
-                    "roofline_ms": round(t_hbm * 1e3, 4), "algorithmic_bytes": bytes_}
-        ach = exps / (t_ms / 1e3) / 1e9
-        pk = exp_peak / 1e9
-        return {"bound": "alu", "achieved": round(ach, 1), "peak": round(pk, 1), "unit": "Gexp2/s",
-                "frac": round(ach / pk, 4),
-                "peak_kind": f"MUFU ex2: {sms} SMs x {EX2_PER_CLK_PER_SM:g}/clk x {sm_mhz:g} MHz (median sampled)",
-                "roofline_ms": round(t_sfu * 1e3, 4), "algorithmic_bytes": bytes_}
-
-    # launch order of a call: the summary passes of the chunked segments, then
-    # each segment's main pass (then, in the backward, the two reductions)
-    segs = plan["segments"]
-    seg_tag = [f"{u} units x {k} chunk{'s' if k > 1 else ''}" for u, k in segs]
-    fwd_names = ([f"k_fwd2 chunk summary ({seg_tag[i]})" for i, (_, k) in enumerate(segs) if k > 1] +
-                 [f"k_fwd2 y + saved states ({t})" for t in seg_tag])
-    bwd_names = ([f"k_bwd2 reverse summary ({seg_tag[i]})" for i, (_, k) in enumerate(segs) if k > 1] +
-                 [f"k_bwd2 main ({t})" for t in seg_tag] + ["k_bwd2_reduce_bc", "k_bwd2_reduce_params"])
-    n_sum = sum(1 for _, k in segs if k > 1)
-    main_f = range(n_sum, n_sum + len(segs))  # the forward's main pass: one launch per segment
-    main_b = range(n_sum, n_sum + len(segs))
-    t_main_f = sum(k_fwd[j] for j in main_f)
-    t_main_b = sum(k_bwd[j] for j in main_b)
-    r_bwd = roof(bwd_main_bytes, t_main_b)
-    r_bwd.update({"kernel": f"k_bwd2 main pass (ss_bwd_saved; {len(segs)} launch{'es' if len(segs) > 1 else ''})",
-                  "ms": round(t_main_b, 4), "traffic": measured_traffic("k_bwd2_main", w)})
-    r_fwd = roof(fwd_bytes, t_main_f)
-    r_fwd.update({"kernel": f"k_fwd2 main pass (ss_fwd_save; {len(segs)} launch{'es' if len(segs) > 1 else ''})",
-                  "ms": round(t_main_f, 4), "traffic": measured_traffic("k_fwd2_y", w)})
-    t_roof = roof(fwd_bytes, t_fwd)["roofline_ms"] + roof(bwd_bytes, t_bwd)["roofline_ms"]
-    kernel_ms = {n: round(v, 4) for n, v in zip(fwd_names + bwd_names, k_fwd + k_bwd)}
+    ex2 = measure_ex2_rate()
+    peaks = {"hbm_gbs": hbm_peak, "hbm_kind": peak_kind, "ex2_per_clk_per_sm": ex2,
+             "sms": torch.cuda.get_device_properties(dev).multi_processor_count,
+             "sm_mhz": clk.get("sm_mhz") or 2070.0}
+    stats = analyse(w, plan, ms_per_step, t_fwd, t_bwd, k_fwd, k_bwd, peaks)
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": w.name, "Bsz": w.Bsz, "L": w.L, "Dch": w.Dch, "N": w.N, "io": w.io,
-                   "terms": "D, z, delta_bias, softplus, last_state", "chunks": plan["chunks"],
-                   "l2": "no flush: each step reads and writes > 2 GB, far above the 129 MB L2",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
-        "hbm_gbs": round((fwd_bytes + bwd_bytes) / (ms_per_step / 1e3) / 1e9, 1),
-        "roofline": r_bwd, "roofline_fwd": r_fwd,
-        "roofline_step_frac": round(t_roof / ms_per_step, 4), "mufu_ops": mufu_counts(w),
-        "fwd_ms": round(t_fwd, 4), "bwd_ms": round(t_bwd, 4), "kernel_ms": kernel_ms,
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config_of(w, world),
+        "chunks": plan["chunks"], "staging": staging,
+    }
+    line.update(stats)
+    line.update({
+        "step_recompute_ms": round(recompute_ms, 4),
+        "mufu_ops": mufu_counts(w), "ex2_per_clk_per_sm": round(ex2, 3),
         "clocks": clk,
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "runs": [round(job_throughput(w.bld * e2e_steps, world, v), 1) for v in e2e_runs],
                 "of_runs": "median"},
-        "gpu_launches": K * (plan["fwd_kernels"] + plan["bwd_saved_kernels"]),  # the timed region only
-    }
+        "gpu_launches": K * launches,  # the timed region only
+        "device_status": ss.status_string(gstatus),
+    })
     if not args.no_decode:
         line["decode"] = measure_decode(dev, hbm_peak, peak_kind)
+    if not args.no_per_workload:
+        pw = {}
+        for wi in PER_WORKLOAD:
+            w2 = WORKLOADS[wi]
+            pw[w2.name] = run_workload(w2, dev, stream, world, max(3, min(K, 20)), 3, peaks,
+                                       args.cpu_seconds_per_workload, rank)
+        line["per_workload"] = pw
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, x, budget_s=args.cpu_seconds)
     if rank == 0:
@@ -490,11 +633,13 @@ def run_ours(args):
 
 
 def _oracle_sample(orc, w, x, rows):
-    """The oracle's forward and backward on a row sample of the workload; returns seconds."""
+    """The oracle's forward (and backward, for a training step) on a row sample of
+    the workload; returns seconds."""
     t0 = time.perf_counter()
     orc.fwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], w.softplus, rows=rows)
-    orc.bwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], w.softplus, dy=x["dy"],
-            rows=rows, want_dBdC=True)
+    if w.backward:
+        orc.bwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], w.softplus, dy=x["dy"],
+                rows=rows, want_dBdC=True)
     return time.perf_counter() - t0
 
 
@@ -521,8 +666,9 @@ def cpu_baseline(w, x, budget_s=15.0):
         done += rows.size
         n = min(2 * n, perm.size - done)
     return {"value": round(done * w.L / spent, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{done} of {w.Bsz * w.Dch} (b, d) rows, full L={w.L}, forward + backward incl. dB/dC "
-                      f"contributions, f64, {spent:.1f} s"}
+            "sample": f"{done} of {w.Bsz * w.Dch} (b, d) rows, full L={w.L}, "
+                      f"{'forward + backward incl. dB/dC contributions' if w.backward else 'forward'}, f64, "
+                      f"{spent:.1f} s"}
 
 
 def run_reference(args):
@@ -556,7 +702,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "Bsz": w.Bsz, "L": w.L, "Dch": w.Dch, "N": w.N, "io": w.io},
+        "config": config_of(w, world),
         "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -571,6 +717,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-seconds-per-workload", type=float, default=6.0,
+                    help="oracle seconds for each per-workload block's cpu_baseline (0: none)")
+    ap.add_argument("--no-per-workload", action="store_true", help="time the headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the single-step decoding measurement")
     ap.add_argument("--workload", default=WORKLOAD.name,

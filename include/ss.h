@@ -57,7 +57,9 @@ typedef enum {
     SS_ERR_INVALID_PROBLEM = 1,     /* negative extent, missing required pointer, optional-term mismatch */
     SS_ERR_UNSUPPORTED = 2,         /* dtype, N outside {1,2,4,8,16,32}, size limit, pointer not 16-byte aligned */
     SS_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes below the matching *_workspace_bytes() query */
-    SS_ERR_CUDA = 4                 /* a CUDA runtime call or launch failed */
+    SS_ERR_CUDA = 4,                /* a CUDA runtime call or launch failed */
+    SS_ERR_DEVICE_TIMEOUT = 5,      /* from ss_device_status: a kernel gave up waiting for its tile copies */
+    SS_ERR_STAGING_FALLBACK = 6     /* from ss_device_status: a kernel could not use TMA (results intact) */
 } ss_status;
 
 /* Bytes of device workspace ss_fwd needs for these sizes (0 when the scan
@@ -315,13 +317,72 @@ int ss_decode_step(const void *u, const void *delta, const float *A, const void 
                    const void *z, const float *delta_bias, int softplus, int a_is_log, float *state, void *y,
                    int64_t Bsz, int64_t Dch, int64_t N, int dtype, void *stream);
 
+/* Device-side failures.  The scan kernels stage their tiles into shared
+ * memory with TMA copies (cp.async.bulk.tensor) that complete on an mbarrier;
+ * a copy lands within microseconds, and every wait on one gives up after two
+ * seconds.  A block that gives up leaves SS_ERR_DEVICE_TIMEOUT in the
+ * library's device status word (one per device, shared by all calls), waits
+ * once more (bounded) for its own copies and returns, so the context stays
+ * usable; the outputs of that call are then incomplete.  A launch returns
+ * before its kernels run, so this failure is not part of the calls' return
+ * codes.
+ *
+ * A block also checks, before its first copy, that its shared-memory tile
+ * buffers have the 128-byte alignment TMA boxes need; if not (not expected:
+ * they are declared so), it stages with per-thread copies and notes that in
+ * the status word.
+ *
+ * ss_device_status: waits for `stream` (the current device's), reads the
+ * status word and clears it.  SS_OK when nothing was noted since the last
+ * read; SS_ERR_DEVICE_TIMEOUT when a kernel gave up waiting (this wins over
+ * the next); SS_ERR_STAGING_FALLBACK when a kernel staged without TMA;
+ * SS_ERR_CUDA when the read failed.  Kernels on other streams still running
+ * are not waited for.
+ */
+int ss_device_status(void *stream);
+
+/* Runs one block on `stream` that waits on a barrier nothing completes, for
+ * limit_ns nanoseconds (0 .. 2e9; else SS_ERR_INVALID_PROBLEM), then reports
+ * the wait as failed in the status word exactly as a scan kernel does.  For
+ * testing the status path without any failure of the GPU.  Returns the
+ * launch's status; read the outcome with ss_device_status.
+ */
+int ss_selftest_wait_timeout(int64_t limit_ns, void *stream);
+
+/* Staging choice for the following calls of the process: 0 (the default)
+ * uses TMA wherever the problem allows it (D and N times the element size
+ * multiples of 16 bytes, D a multiple of 4), 1 stages every tile with
+ * per-thread asynchronous copies instead.  Both produce identical results;
+ * the switch exists to test that.  Returns the previous setting.  Not ordered
+ * against calls running on other host threads.
+ */
+int ss_set_copies_only(int enable);
+
+/* 1 when the scan kernels of a problem of these sizes stage their tiles with
+ * TMA under the current setting of ss_set_copies_only, else 0 (also for
+ * invalid or empty problems, and where the driver offers no tensor-map
+ * encoder).  Touches no device memory. */
+int ss_staging_uses_tma(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype);
+
+/* Throughput of the GPU's exponential unit: MUFU ex2.approx.f32 results per
+ * SM clock cycle per SM on the current device, measured by one block per SM
+ * running `iters` rounds of eight independent exponential chains per thread
+ * (1 .. 2^20; about 0.5 ms at 4096), each block timed by its SM's cycle
+ * counter; the median over the SMs.  This is the peak of the scan's
+ * exponential roofline (one 2^x per (t, d, n) and direction).  Synchronous;
+ * allocates and frees a few bytes of device memory.
+ */
+int ss_measure_ex2_rate(int iters, double *per_clk_per_sm);
+
 /* Static description of a status code. */
 const char *ss_status_string(int status);
 
 /* ABI version (2: ss_fwd_save / ss_bwd_saved added, ss_plan_info gained
  * bwd_saved_kernels; 3: ss_fwd_ex / ss_bwd_ex / ss_decode_step added; 4:
  * ss_plan_segments added, the saved-state buffer sized by L rounded up to 32
- * steps); bumped on any incompatible change. */
+ * steps; 5: a saved state every 8 steps, ss_device_status /
+ * ss_selftest_wait_timeout / ss_set_copies_only added); bumped on any
+ * incompatible change. */
 int ss_abi_version(void);
 
 #ifdef __cplusplus

@@ -16,15 +16,19 @@ LIB_PATH = os.path.join(PKG, "libss.so")
 
 SS_F32, SS_F16, SS_BF16 = 0, 1, 2
 SS_OK = 0
+SS_ERR_DEVICE_TIMEOUT = 5
+SS_ERR_STAGING_FALLBACK = 6
 STATUS_NAMES = {0: "SS_OK", 1: "SS_ERR_INVALID_PROBLEM", 2: "SS_ERR_UNSUPPORTED", 3: "SS_ERR_WORKSPACE_TOO_SMALL",
-                4: "SS_ERR_CUDA"}
+                4: "SS_ERR_CUDA", 5: "SS_ERR_DEVICE_TIMEOUT",
+                6: "SS_ERR_STAGING_FALLBACK"}
 
 # Every function include/ss.h declares.
 EXPORTS = ["ss_fwd", "ss_bwd", "ss_fwd_workspace_bytes", "ss_bwd_workspace_bytes", "ss_plan_info",
            "ss_status_string", "ss_abi_version", "ss_fwd_noalloc", "ss_saved_bytes", "ss_fwd_save",
            "ss_bwd_saved_workspace_bytes", "ss_bwd_saved", "ss_profile_events", "ss_fwd_ex", "ss_bwd_ex",
-           "ss_decode_step", "ss_plan_segments"]
-ABI_VERSION = 4
+           "ss_decode_step", "ss_plan_segments", "ss_device_status", "ss_selftest_wait_timeout",
+           "ss_set_copies_only", "ss_staging_uses_tma", "ss_measure_ex2_rate"]
+ABI_VERSION = 5
 
 # Size of the library-owned scratch behind ss_fwd_noalloc (SS_FWD_NOALLOC_MAX_SCRATCH_BYTES).
 FWD_NOALLOC_MAX_SCRATCH_BYTES = 2 << 20
@@ -99,6 +103,16 @@ def lib() -> ctypes.CDLL:
     L.ss_fwd_ex.argtypes = [ctypes.POINTER(FwdDesc), _P]
     L.ss_bwd_ex.restype = ctypes.c_int
     L.ss_bwd_ex.argtypes = [ctypes.POINTER(BwdDesc), _P]
+    L.ss_device_status.restype = ctypes.c_int
+    L.ss_device_status.argtypes = [_P]
+    L.ss_selftest_wait_timeout.restype = ctypes.c_int
+    L.ss_selftest_wait_timeout.argtypes = [_I64, _P]
+    L.ss_set_copies_only.restype = ctypes.c_int
+    L.ss_set_copies_only.argtypes = [ctypes.c_int]
+    L.ss_measure_ex2_rate.restype = ctypes.c_int
+    L.ss_measure_ex2_rate.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_double)]
+    L.ss_staging_uses_tma.restype = ctypes.c_int
+    L.ss_staging_uses_tma.argtypes = [_I64] * 4 + [ctypes.c_int]
     L.ss_decode_step.restype = ctypes.c_int
     L.ss_decode_step.argtypes = [_P] * 8 + [ctypes.c_int, ctypes.c_int, _P, _P] + [_I64] * 3 + [ctypes.c_int, _P]
     _lib = L
@@ -213,6 +227,45 @@ def profile_events(events):
     i-th.  An empty list switches the recording off."""
     handles = (ctypes.c_void_p * max(1, len(events)))(*[ctypes.c_void_p(e.cuda_event) for e in events])
     _check("ss_profile_events", lib().ss_profile_events(handles, len(events)))
+
+
+def device_status(stream=None, device=None) -> int:
+    """Wait for ``stream`` (default: the current stream of ``device``), then read and
+    clear the library's device status word: SS_OK; SS_ERR_DEVICE_TIMEOUT when a
+    kernel gave up waiting for its tile copies since the last read;
+    SS_ERR_STAGING_FALLBACK when a kernel staged its tiles without TMA."""
+    import torch
+
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        rc = lib().ss_device_status(stream_handle(stream, dev))
+    if rc not in (SS_OK, SS_ERR_DEVICE_TIMEOUT, SS_ERR_STAGING_FALLBACK):
+        _check("ss_device_status", rc)
+    return rc
+
+
+def selftest_wait_timeout(limit_ns: int, stream=None) -> None:
+    """Launch one block whose wait on a barrier nothing completes runs out after
+    limit_ns; it records the failure in the device status word."""
+    _check("ss_selftest_wait_timeout", lib().ss_selftest_wait_timeout(int(limit_ns), stream_handle(stream)))
+
+
+def set_copies_only(enable: bool) -> bool:
+    """Stage every tile with per-thread asynchronous copies instead of TMA (for the
+    following calls of the process); returns the previous setting."""
+    return bool(lib().ss_set_copies_only(1 if enable else 0))
+
+
+def measure_ex2_rate(iters: int = 4096) -> float:
+    """MUFU ex2 results per clock cycle per SM on the current device (median over SMs)."""
+    r = ctypes.c_double()
+    _check("ss_measure_ex2_rate", lib().ss_measure_ex2_rate(int(iters), ctypes.byref(r)))
+    return r.value
+
+
+def staging_uses_tma(Bsz, L, Dch, N, dtype) -> bool:
+    """Whether the scan kernels of a problem of these sizes stage their tiles with TMA."""
+    return bool(lib().ss_staging_uses_tma(Bsz, L, Dch, N, dtype))
 
 
 def _workspace(nbytes, device, workspace):

@@ -23,7 +23,7 @@ LIB = os.path.join(PKG, "libss.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
 SOURCES = ["api.cu", "dispatch.cu", "fwd_f32.cu", "fwd_bf16.cu", "fwd_f16.cu", "bwd_f32.cu",
-           "bwd_bf16.cu", "bwd_f16.cu", "decode.cu", "fwd_noalloc.cu"]
+           "bwd_bf16.cu", "bwd_f16.cu", "decode.cu", "fwd_noalloc.cu", "probe.cu"]
 
 
 def nvcc() -> str:

@@ -6,8 +6,12 @@
 // tensors are invalid problems, unsupported dtypes / state sizes are
 // unsupported, a short workspace is reported before any launch.  Everything
 // is checked before the first CUDA call; on error nothing is written.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <atomic>
+#include <mutex>
 
 #include "ss.h"
 #include "common.cuh"
@@ -16,6 +20,109 @@
 using namespace ss;
 
 namespace {
+
+// ---------------------------------------------------------------- device status word
+// A kernel that gives up waiting for one of its copies leaves a code here
+// (kDevWaitTimeout) and returns; ss_device_status reads and clears it.
+static __device__ int g_status;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_status_mutex;
+int* g_status_ptr[kMaxDevices] = {};
+
+// Device address of g_status on the current device (looked up once per device).
+int status_for_current_device(int** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SS_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return SS_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_status_mutex);
+    if (g_status_ptr[dev] == nullptr) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_status) != cudaSuccess || ptr == nullptr) return SS_ERR_CUDA;
+        g_status_ptr[dev] = static_cast<int*>(ptr);
+    }
+    *out = g_status_ptr[dev];
+    return SS_OK;
+}
+
+// One block that waits on a barrier nothing completes, for at most limit_ns:
+// the wait runs out and the block records it like a scan kernel would.
+__global__ void k_wait_timeout(int* status, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_proxy_async_smem();
+        if (!mbar_wait(&bar, 0, limit_ns)) atomicOr(status, kDevWaitTimeout);
+    }
+}
+
+// ---------------------------------------------------------------- tensor maps
+// cuTensorMapEncodeTiled, taken from the driver through the runtime (no link
+// against the driver library).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+std::once_flag g_encode_once;
+EncodeTiledFn g_encode = nullptr;
+
+EncodeTiledFn encode_fn() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    });
+    return g_encode;
+}
+
+// 0: TMA staging wherever the problem allows it; 1: asynchronous copies only.
+std::atomic<int> g_copies_only{0};
+
+// A [Bsz, L, inner] tensor as a 3-D map {inner, L, Bsz} with boxes of
+// {box_x, rows, 1}; rows and channels outside the tensor read as zero.
+bool encode_map(CUtensorMap* m, const void* base, CUtensorMapDataType type, int esz, int64_t Bsz, int64_t L,
+                int64_t inner, int box_x, int rows) {
+    const cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)L, (cuuint64_t)Bsz};
+    const cuuint64_t strides[2] = {(cuuint64_t)(inner * esz), (cuuint64_t)(inner * L * esz)};
+    const cuuint32_t box[3] = {(cuuint32_t)box_x, (cuuint32_t)rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return encode_fn()(m, type, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                       CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Whether the scan kernels of this problem stage their tiles with TMA: every
+// box's row is a whole number of 16-byte units (D and N times the element
+// size), the tensors' row strides are multiples of 16 bytes, the strides and
+// coordinates fit the map's ranges, and the driver provides the encoder.
+bool tma_eligible(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype) {
+    if (g_copies_only.load(std::memory_order_relaxed)) return false;
+    const int64_t esz = dtype == SS_F32 ? 4 : 2;
+    if ((Dch * esz) % 16 != 0 || (N * esz) % 16 != 0 || Dch % 4 != 0) return false;
+    if (L >= (1ll << 31) || Bsz >= (1ll << 31) || Dch * L * 4 >= (1ll << 40)) return false;
+    return encode_fn() != nullptr;
+}
+
+// The maps a forward (rows = steps per tile of the forward) or a backward
+// (rows = steps per recompute window) loads its tiles through; y0 (f32, the
+// forward's pre-gate readout kept for dz) only for the backward.
+bool make_maps(TmaMaps& mp, const FwdArgs& f, const void* dy, const float* y0, int rows) {
+    const CUtensorMapDataType io = f.dtype == SS_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : f.dtype == SS_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const int esz = f.dtype == SS_F32 ? 4 : 2;
+    const int CH = (int)channels_per_block((int)f.N);
+    bool ok = encode_map(&mp.m[kMapDelta], f.delta, io, esz, f.Bsz, f.L, f.Dch, CH, rows) &&
+              encode_map(&mp.m[kMapU], f.u, io, esz, f.Bsz, f.L, f.Dch, CH, rows) &&
+              encode_map(&mp.m[kMapB], f.B, io, esz, f.Bsz, f.L, f.N, (int)f.N, rows) &&
+              encode_map(&mp.m[kMapC], f.C, io, esz, f.Bsz, f.L, f.N, (int)f.N, rows);
+    if (ok && f.z) ok = encode_map(&mp.m[kMapZ], f.z, io, esz, f.Bsz, f.L, f.Dch, CH, rows);
+    if (ok && dy) ok = encode_map(&mp.m[kMapDy], dy, io, esz, f.Bsz, f.L, f.Dch, CH, rows);
+    if (ok && y0) ok = encode_map(&mp.m[kMapY0], y0, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, f.Bsz, f.L, f.Dch, CH, rows);
+    return ok;
+}
 
 bool n_supported(int64_t N) { return N == 1 || N == 2 || N == 4 || N == 8 || N == 16 || N == 32; }
 
@@ -83,7 +190,11 @@ int fwd_impl(const void* u, const void* delta, const float* A, const void* B, co
     a.ws_fsd = workspace ? reinterpret_cast<float*>(static_cast<char*>(workspace) + fsum_offset_sd(p, N)) : nullptr;
     float* ck = save ? static_cast<float*>(saved) : nullptr;
     a.y0 = save ? reinterpret_cast<float*>(static_cast<char*>(saved) + ckpt_y0_offset(p, Bsz, N)) : nullptr;
-    return launch_fwd(a, p, st, kModeY, ck) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+    rc = status_for_current_device(&a.status);
+    if (rc != SS_OK) return rc;
+    TmaMaps maps;
+    a.use_tma = tma_eligible(Bsz, L, Dch, N, dtype) && make_maps(maps, a, nullptr, nullptr, kFwdRows) ? 1 : 0;
+    return launch_fwd(a, p, st, kModeY, ck, maps) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
 // Backward; with from_saved the restart states come from ss_fwd_save /
@@ -168,7 +279,15 @@ int bwd_impl(const void* u, const void* delta, const float* A, const void* B, co
     a.ws_dA = reinterpret_cast<float*>(ws + w.dA);
     a.ws_dD = reinterpret_cast<float*>(ws + w.dD);
     a.ws_db = reinterpret_cast<float*>(ws + w.db);
-    return launch_bwd(a, p, st, ckpt_out) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+    rc = status_for_current_device(&a.f.status);
+    if (rc != SS_OK) return rc;
+    // the forward passes that store the restart states use the forward's maps
+    TmaMaps fmaps, bmaps;
+    a.f.use_tma = tma_eligible(Bsz, L, Dch, N, dtype) && make_maps(fmaps, a.f, nullptr, nullptr, kFwdRows) &&
+                          make_maps(bmaps, a.f, dy, z ? a.y0 : nullptr, kSub)
+                      ? 1
+                      : 0;
+    return launch_bwd(a, p, st, ckpt_out, fmaps, bmaps) == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
 // An entry point's launches between prof_begin and prof_end.
@@ -198,7 +317,36 @@ int ss_profile_events(void* const* events, int count) {
     return SS_OK;
 }
 
-int ss_abi_version(void) { return 4; }
+int ss_abi_version(void) { return 5; }
+
+int ss_device_status(void* stream) {
+    int* status = nullptr;
+    int rc = status_for_current_device(&status);
+    if (rc != SS_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int host = 0;
+    if (cudaMemcpyAsync(&host, status, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
+        return SS_ERR_CUDA;
+    if (host & kDevWaitTimeout) return SS_ERR_DEVICE_TIMEOUT;
+    return host & kDevMisaligned ? SS_ERR_STAGING_FALLBACK : SS_OK;
+}
+
+int ss_selftest_wait_timeout(int64_t limit_ns, void* stream) {
+    if (limit_ns < 0 || limit_ns > (int64_t)kWaitLimitNs) return SS_ERR_INVALID_PROBLEM;
+    int* status = nullptr;
+    int rc = status_for_current_device(&status);
+    if (rc != SS_OK) return rc;
+    k_wait_timeout<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status, (uint64_t)limit_ns);
+    return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}
+
+int ss_set_copies_only(int enable) { return g_copies_only.exchange(enable ? 1 : 0); }
+
+int ss_staging_uses_tma(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype) {
+    if (check_sizes(Bsz, L, Dch, N, dtype) != SS_OK || Bsz == 0 || L == 0 || Dch == 0) return 0;
+    return tma_eligible(Bsz, L, Dch, N, dtype) ? 1 : 0;
+}
 
 const char* ss_status_string(int status) {
     switch (status) {
@@ -207,6 +355,8 @@ const char* ss_status_string(int status) {
         case SS_ERR_UNSUPPORTED: return "unsupported (dtype, state size, size limit or pointer alignment)";
         case SS_ERR_WORKSPACE_TOO_SMALL: return "workspace or saved-state buffer too small (query its *_bytes function)";
         case SS_ERR_CUDA: return "CUDA runtime error";
+        case SS_ERR_DEVICE_TIMEOUT: return "a kernel gave up waiting for its tile copies (see ss_device_status)";
+        case SS_ERR_STAGING_FALLBACK: return "a kernel staged its tiles without TMA (results intact; see ss_device_status)";
         default: return "unknown status";
     }
 }

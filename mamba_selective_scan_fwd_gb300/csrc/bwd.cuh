@@ -85,13 +85,12 @@ struct BCfg {
     // four states are two words, widened by ALU bit operations) and are copied
     // in raw, double buffered; f32 rows are copied straight in (double
     // buffered); f16 rows are converted by the prologue
-    static constexpr int BCF = 2 * N + 4;
+    // (each staged as one dense [step][N] array per tensor: the layout a TMA
+    // box lands in)
     static constexpr bool BC_PK = std::is_same<T, __nv_bfloat16>::value && S == 4;
     static constexpr bool BC_DIRECT = ESZ == 4;
     static constexpr bool BC_RAW = !BC_DIRECT && !BC_PK && NB >= 4;
     static constexpr int BC_BUFS = BC_DIRECT ? 2 : 1;
-    static constexpr int PKR = 2 * N + 8;           // packed row (bf16 elements), 16-byte multiple
-    static constexpr int RAWP = NB >= 32 ? N + 16 / ESZ : N;
     static constexpr int EP = CH + 4;               // padded per-channel rows (floats)
     // plane of per-step channel sums of one lane of a pair: kTT rows of EP floats,
     // planes 16 mod 32 floats apart so that the 8-byte stores of the lanes of
@@ -198,12 +197,13 @@ constexpr int kRevMain = 0, kRevSummary = 1;
 
 template <typename T, int N, int MODE, bool STATE>
 __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(BwdArgs a, FPlan p, int si,
-                                                                              int64_t k_lo) {
+                                                                              int64_t k_lo,
+                                                                              const __grid_constant__ TmaMaps maps) {
     using C = BCfg<T, N>;
     constexpr bool MAIN = MODE == kRevMain;
     constexpr int NW = C::NW, NPW = C::NPW, S = C::S, SP = C::SP, G = C::G, PAIRS = C::PAIRS, CH = C::CH,
                   THREADS = C::THREADS, GRP = C::GRP, NGRP = C::NGRP, ITEMS = C::ITEMS, RWH = C::RWH,
-                  NWd = C::NWd, BCF = C::BCF, EP = C::EP, BLK = C::BLK;
+                  NWd = C::NWd, EP = C::EP, BLK = C::BLK;
     // per-(t, d) staging of the walk, one entry per channel pair
     __shared__ float4 sDU[kTT][PAIRS + 1];  // (Delta of both channels, Delta*u of both channels)
     __shared__ float2 sG[kTT][PAIRS + 2];   // g of both channels
@@ -211,16 +211,18 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
     __shared__ float4 sUS[MAIN ? kTT : 1][MAIN ? PAIRS + 1 : 1];
     // B / C rows as f32 (B then C); with f32 io double buffered, the next tile's
     // rows being copied in while the current tile is walked
-    __shared__ __align__(16) float sBC[C::BC_BUFS][C::BC_PK ? 1 : kTT][C::BC_PK ? 4 : BCF];
+    __shared__ __align__(128) float sBC[2][C::BC_BUFS][C::BC_PK ? 1 : kTT][C::BC_PK ? 4 : N];
     // packed bf16 B / C rows (B, then C), double buffered: the walk reads them directly
-    __shared__ __align__(16) T sBCpk[C::BC_PK ? 2 : 1][C::BC_PK ? kTT : 1][C::BC_PK ? C::PKR : 8];
+    __shared__ __align__(128) T sBCpk[2][C::BC_PK ? 2 : 1][C::BC_PK ? kTT : 1][C::BC_PK ? N : 8];
     // raw 16-bit B / C rows of the next tile (converted into sBC by the prologue)
-    __shared__ __align__(16) T sBCraw[2][C::BC_RAW ? kTT : 1][C::BC_RAW ? C::RAWP : 2];
+    __shared__ __align__(128) T sBCraw[2][C::BC_RAW ? kTT : 1][C::BC_RAW ? N : 8];
+    // completion of the TMA copies into the two tile buffers
+    __shared__ __align__(8) uint64_t sBar[2];
     // raw runs of delta, u, dy, z of the next tile, copied in asynchronously by
     // the thread that later converts them
-    __shared__ __align__(16) T sRaw[4][kTT][CH];
+    __shared__ __align__(128) T sRaw[4][kTT][CH];
     // the forward's pre-gate readout y0 of the next tile (for dz), likewise
-    __shared__ __align__(16) float sY0[MAIN ? kTT : 1][MAIN ? CH : 4];
+    __shared__ __align__(128) float sY0[MAIN ? kTT : 1][MAIN ? CH : 4];
     // dB / dC contributions of the tile's kTT steps, per warp: block (j, tau)
     // holds a row of NPW floats per pair
     __shared__ __align__(16) float sR[MAIN ? NW : 1][MAIN ? kTT * 2 * BLK : 4];
@@ -232,7 +234,7 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
     __shared__ float sAcc[MAIN ? 2 : 1][MAIN ? ITEMS * GRP : 1][THREADS];
     // the state entering each tile (the recompute window's start), 2 S floats
     // per lane (S of each channel), double buffered by tile
-    __shared__ __align__(16) float sH[MAIN ? 2 : 1][MAIN ? THREADS * 2 * S : 4];
+    __shared__ __align__(128) float sH[MAIN ? 2 : 1][MAIN ? THREADS * 2 * S : 4];
     __shared__ float sBias[CH], sDv[CH];
 
     const FwdArgs& f = a.f;
@@ -320,7 +322,18 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
 #pragma unroll
     for (int c = 0; c < ITEMS * GRP; c++) accD[c] = accB[c] = 0.f;
 
-    const bool pfast = ((Dch * (int64_t)sizeof(T)) % 16 == 0) && (d0 + CH <= Dch);
+    // TMA boxes land on 128-byte aligned shared memory; a block whose buffers are
+    // not (never expected) records it and stages with asynchronous copies instead
+    bool tma = f.use_tma != 0;
+    if (tma && !(smem_aligned128(&sRaw[0][0][0]) && smem_aligned128(&sBC[0][0][0][0]) &&
+                 smem_aligned128(&sBCpk[0][0][0][0]) && smem_aligned128(&sBCraw[0][0][0]) &&
+                 smem_aligned128(&sY0[0][0]) && smem_aligned128(&sH[0][0]))) {
+        if (tid == 0) atomicOr(f.status, kDevMisaligned);
+        tma = false;
+    }
+    // the tile's runs are read from shared memory: TMA boxes (zero-filled past Dch),
+    // or whole aligned vectors copied in asynchronously
+    const bool pfast = tma || (((Dch * (int64_t)sizeof(T)) % 16 == 0) && (d0 + CH <= Dch));
     const bool ofast = (Dch % 4 == 0) && (d0 + CH <= Dch);
     const int64_t t_begin = k * sgm.Lc;
     const int64_t t_end = t_begin + sgm.Lc < L ? t_begin + sgm.Lc : L;
@@ -334,14 +347,46 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
     float* bc1 = a.ws_bc + ((int64_t)(p.tiles_b + tile) * f.Bsz + b) * L * N;    // dC partials
     float* sRw = &sR[MAIN ? w : 0][0];
 
-    // Asynchronous copies of tile mm, one commit group: the thread's item runs
-    // and y0 runs (when the tile's rows are whole aligned vectors), the B / C
-    // rows (f32 into sBC[mm & 1]; 16-bit raw into sBCraw), and the lane's state
-    // entering the tile into its own slot of sH[mm & 1].  Each thread converts
-    // the runs it copied; the state is read by the lane that copied it.
+    // Copies of tile mm into buffer mm & 1.  With TMA: one thread issues a box per
+    // tensor (delta, u, dy, z as [kTT][CH], y0 as f32 [kTT][CH], B and C as
+    // [kTT][N]: bf16 packed into sBCpk, f32 into sBC, f16 raw into sBCraw) and
+    // the tile's block of saved states (CH x N floats, in lane order) into sH,
+    // on the buffer's barrier.  Otherwise, one commit group of asynchronous
+    // copies: the thread's item runs and y0 runs (when the tile's rows are whole
+    // aligned vectors), the B / C rows, and the lane's state entering the tile
+    // into its own slot of sH; each thread converts the runs it copied and the
+    // state is read by the lane that copied it.
+    const TmaMaps& mp = maps;
     auto issue = [&](int64_t mm) {
         const int64_t tt = t_begin + mm * kTT;
         const int buf = (int)(mm & 1);
+        if (tma) {
+            if (tid == 0) {
+                constexpr uint32_t run = kTT * CH * C::ESZ, row = kTT * N * C::ESZ, state = CH * N * 4;
+                const uint32_t bytes = (MAIN ? 3 : 2) * run + (z ? run : 0) + (MAIN && z ? kTT * CH * 4 : 0) +
+                                       (MAIN ? 2 : 1) * row + (MAIN ? state : 0);
+                mbar_expect_tx(&sBar[buf], bytes);
+                const int x = (int)d0, y = (int)tt, zc = (int)b;
+                tma_load_3d(&sRaw[0][0][0], &mp.m[kMapDelta], x, y, zc, &sBar[buf]);
+                if (MAIN) tma_load_3d(&sRaw[1][0][0], &mp.m[kMapU], x, y, zc, &sBar[buf]);
+                tma_load_3d(&sRaw[2][0][0], &mp.m[kMapDy], x, y, zc, &sBar[buf]);
+                if (z) tma_load_3d(&sRaw[3][0][0], &mp.m[kMapZ], x, y, zc, &sBar[buf]);
+                if (MAIN && z) tma_load_3d(&sY0[0][0], &mp.m[kMapY0], x, y, zc, &sBar[buf]);
+#pragma unroll
+                for (int half = MAIN ? 0 : 1; half < 2; half++) {
+                    void* dst;
+                    if constexpr (C::BC_PK) dst = &sBCpk[half][buf][0][0];
+                    else if constexpr (C::BC_DIRECT) dst = &sBC[half][buf][0][0];
+                    else dst = &sBCraw[half][0][0];
+                    tma_load_3d(dst, &mp.m[half ? kMapC : kMapB], 0, y, zc, &sBar[buf]);
+                }
+                if (MAIN) {
+                    const float* blk = ck_lane - ckpt_slot(w, lane, S) + (tt - t_begin) / kSub * ck_stride;
+                    bulk_load(&sH[buf][0], blk, state, &sBar[buf]);
+                }
+            }
+            return;
+        }
         if (pfast) {
 #pragma unroll
             for (int it = 0; it < ITEMS; it++) {
@@ -363,7 +408,7 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
             const int64_t t = tt + r;
             const T* src = (half ? Cm : Bm) + (b * L + (t < t_end ? t : 0)) * N;
             if constexpr (C::BC_PK) {
-                T* dst = &sBCpk[buf][r][half * N];
+                T* dst = &sBCpk[half][buf][r][0];
                 if (t < t_end) {
                     cp_async_bytes<N * C::ESZ>(dst, src);
                 } else {
@@ -371,7 +416,7 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
                     for (int n = 0; n < N; n += 2) *reinterpret_cast<uint32_t*>(dst + n) = 0u;
                 }
             } else if constexpr (C::BC_DIRECT) {
-                float* dst = &sBC[buf][r][half * N];
+                float* dst = &sBC[half][buf][r][0];
                 if (t < t_end) {
                     cp_async_bytes<N * 4>(dst, src);
                 } else {
@@ -385,13 +430,24 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
         if (MAIN) cp_async_bytes<2 * S * 4>(&sH[buf][tid * 2 * S], ck_lane + (tt - t_begin) / kSub * ck_stride);
         cp_async_commit();
     };
+    if (tma && tid == 0) {
+        mbar_init(&sBar[0], 1);
+        mbar_init(&sBar[1], 1);
+        fence_proxy_async_smem();
+    }
     issue(ntile - 1);
-    __syncthreads();  // sBias / sDv before the first prologue
+    __syncthreads();  // sBias / sDv and the barriers before the first prologue
 
     for (int64_t m = ntile - 1; m >= 0; m--) {
         const int64_t t0 = t_begin + m * kTT;
         const int buf = (int)(m & 1);
-        cp_async_wait<0>();  // this thread's copies of the tile
+        // the tile's copies: this thread's own (asynchronous copies), or the TMA
+        // boxes (the tiles are visited from the last, so the buffer's barrier
+        // completes its phase (ntile - 1 - m) / 2 mod 2)
+        const uint32_t phase = (uint32_t)(((ntile - 1 - m) >> 1) & 1);
+        bool ok = true;
+        if (tma) ok = mbar_wait(&sBar[buf], phase);
+        else cp_async_wait<0>();
         // ---- prologue: (step, GRP-channel group) items of the tile; dz is final here
 #pragma unroll
         for (int it = 0; it < ITEMS; it++) {
@@ -476,19 +532,28 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
                     if constexpr (C::BC_RAW) lds_words<C::NB, NWd>(&sBCraw[half][r][0], wv);
                     else load_words<C::NB, NWd>((half ? Cm : Bm) + (b * L + t) * N, wv);
                 }
-                float* dst = &sBC[0][r][half * N];
+                float* dst = &sBC[half][0][r][0];
 #pragma unroll
                 for (int n = 0; n < N; n++) dst[n] = t < t_end ? elem<T>(wv, n) : 0.f;
             }
         }
-        __syncthreads();  // staging complete; every thread is done reading sRaw / sY0 / sBCraw
+        // Staging complete; every thread is done reading sRaw / sY0 / sBCraw.  A
+        // thread whose wait for the tile ran out makes the whole block give up
+        // (the block agrees here, so no thread is left at a later barrier): the
+        // status word records it and the thread that issued the copies waits once
+        // more for them before the block's shared memory is released.
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                atomicOr(f.status, kDevWaitTimeout);
+                mbar_wait(&sBar[buf], phase);
+            }
+            return;
+        }
         if (m > 0) issue(m - 1);
-        const float* bcrow = &sBC[C::BC_DIRECT ? buf : 0][0][0];
-        const T* pkrow = &sBCpk[C::BC_PK ? buf : 0][0][0];
         // S values of row i's B (half 0) or C (half 1) from the lane's states
         auto ld_bc = [&](int i, int half, float (&v)[S]) {
-            if constexpr (C::BC_PK) ld_bf16x4(pkrow + i * C::PKR + half * N + n0, v);
-            else ld_f32<S>(bcrow + i * BCF + half * N + n0, v);
+            if constexpr (C::BC_PK) ld_bf16x4(&sBCpk[half][buf][i][n0], v);
+            else ld_f32<S>(&sBC[half][C::BC_DIRECT ? buf : 0][i][n0], v);
         };
 
         if constexpr (!MAIN) {
@@ -796,11 +861,12 @@ cudaError_t prefer_max_shared(K kernel, std::atomic<uint64_t>& done) {
 }
 
 template <typename T, int N>
-cudaError_t launch_bwd_t(const BwdArgs& a, const FPlan& p, cudaStream_t st, float* ckpt_out) {
+cudaError_t launch_bwd_t(const BwdArgs& a, const FPlan& p, cudaStream_t st, float* ckpt_out, const TmaMaps& fmaps,
+                         const TmaMaps& bmaps) {
     cudaError_t e = cudaSuccess;
     if (ckpt_out) {
         // checkpoint pass (with forward summaries first when the sequence is chunked)
-        e = launch_fwd(a.f, p, st, kModeCkpt, ckpt_out);
+        e = launch_fwd(a.f, p, st, kModeCkpt, ckpt_out, fmaps);
         if (e != cudaSuccess) return e;
     }
     constexpr int threads = BCfg<T, N>::THREADS;
@@ -809,7 +875,8 @@ cudaError_t launch_bwd_t(const BwdArgs& a, const FPlan& p, cudaStream_t st, floa
         const int64_t K = p.seg[si].K;
         if (K > 1) {
             prof_mark(st);
-            k_bwd<T, N, kRevSummary, false><<<(unsigned)(p.seg[si].nu * (K - 1)), threads, 0, st>>>(a, p, si, 1);
+            k_bwd<T, N, kRevSummary, false><<<(unsigned)(p.seg[si].nu * (K - 1)), threads, 0, st>>>(a, p, si, 1,
+                                                                                                     bmaps);
         }
     }
     const bool state = a.dlast != nullptr || a.dh0 != nullptr;
@@ -820,21 +887,22 @@ cudaError_t launch_bwd_t(const BwdArgs& a, const FPlan& p, cudaStream_t st, floa
     if (e != cudaSuccess) return e;
     for (int si = 0; si < p.nseg; si++) {
         prof_mark(st);
-        main_kernel<<<(unsigned)(p.seg[si].nu * p.seg[si].K), threads, 0, st>>>(a, p, si, 0);
+        main_kernel<<<(unsigned)(p.seg[si].nu * p.seg[si].K), threads, 0, st>>>(a, p, si, 0, bmaps);
     }
     return cudaGetLastError();
 }
 
 // Backward launcher of one io type: switches on N.
 template <typename T>
-cudaError_t launch_bwd_io(const BwdArgs& a, const FPlan& p, cudaStream_t st, float* ckpt_out) {
+cudaError_t launch_bwd_io(const BwdArgs& a, const FPlan& p, cudaStream_t st, float* ckpt_out, const TmaMaps& fmaps,
+                          const TmaMaps& bmaps) {
     switch (a.f.N) {
-        case 1: return launch_bwd_t<T, 1>(a, p, st, ckpt_out);
-        case 2: return launch_bwd_t<T, 2>(a, p, st, ckpt_out);
-        case 4: return launch_bwd_t<T, 4>(a, p, st, ckpt_out);
-        case 8: return launch_bwd_t<T, 8>(a, p, st, ckpt_out);
-        case 16: return launch_bwd_t<T, 16>(a, p, st, ckpt_out);
-        case 32: return launch_bwd_t<T, 32>(a, p, st, ckpt_out);
+        case 1: return launch_bwd_t<T, 1>(a, p, st, ckpt_out, fmaps, bmaps);
+        case 2: return launch_bwd_t<T, 2>(a, p, st, ckpt_out, fmaps, bmaps);
+        case 4: return launch_bwd_t<T, 4>(a, p, st, ckpt_out, fmaps, bmaps);
+        case 8: return launch_bwd_t<T, 8>(a, p, st, ckpt_out, fmaps, bmaps);
+        case 16: return launch_bwd_t<T, 16>(a, p, st, ckpt_out, fmaps, bmaps);
+        case 32: return launch_bwd_t<T, 32>(a, p, st, ckpt_out, fmaps, bmaps);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -2,5 +2,6 @@
 #include "bwd.cuh"
 
 namespace ss {
-template cudaError_t launch_bwd_io<__nv_bfloat16>(const BwdArgs&, const FPlan&, cudaStream_t, float*);
+template cudaError_t launch_bwd_io<__nv_bfloat16>(const BwdArgs&, const FPlan&, cudaStream_t, float*, const TmaMaps&,
+                                              const TmaMaps&);
 }  // namespace ss

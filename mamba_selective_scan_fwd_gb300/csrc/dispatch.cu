@@ -12,21 +12,22 @@ namespace ss {
 // and the pre-gate readout into a.y0 when ckpt is given; mode kModeCkpt:
 // the same walk writing only those states and the pre-gate readout (used by
 // the backward), no y.
-cudaError_t launch_fwd(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt) {
-    if (a.dtype == 0) return launch_fwd_io<float>(a, p, st, mode, ckpt);
-    if (a.dtype == 1) return launch_fwd_io<__half>(a, p, st, mode, ckpt);
-    return launch_fwd_io<__nv_bfloat16>(a, p, st, mode, ckpt);
+cudaError_t launch_fwd(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt, const TmaMaps& maps) {
+    if (a.dtype == 0) return launch_fwd_io<float>(a, p, st, mode, ckpt, maps);
+    if (a.dtype == 1) return launch_fwd_io<__half>(a, p, st, mode, ckpt, maps);
+    return launch_fwd_io<__nv_bfloat16>(a, p, st, mode, ckpt, maps);
 }
 
 __global__ void k_bwd_reduce_bc(BwdArgs a, FPlan p);
 __global__ void k_bwd_reduce_params(BwdArgs a, FPlan p);
 
 // The backward's scan kernels (io-typed), then the two reductions.
-cudaError_t launch_bwd(const BwdArgs& a, const FPlan& p, cudaStream_t st, float* ckpt_out) {
+cudaError_t launch_bwd(const BwdArgs& a, const FPlan& p, cudaStream_t st, float* ckpt_out, const TmaMaps& fmaps,
+                       const TmaMaps& bmaps) {
     cudaError_t e;
-    if (a.f.dtype == 0) e = launch_bwd_io<float>(a, p, st, ckpt_out);
-    else if (a.f.dtype == 1) e = launch_bwd_io<__half>(a, p, st, ckpt_out);
-    else e = launch_bwd_io<__nv_bfloat16>(a, p, st, ckpt_out);
+    if (a.f.dtype == 0) e = launch_bwd_io<float>(a, p, st, ckpt_out, fmaps, bmaps);
+    else if (a.f.dtype == 1) e = launch_bwd_io<__half>(a, p, st, ckpt_out, fmaps, bmaps);
+    else e = launch_bwd_io<__nv_bfloat16>(a, p, st, ckpt_out, fmaps, bmaps);
     if (e != cudaSuccess) return e;
     const int64_t n_bc = 2 * a.f.Bsz * a.f.L * a.f.N / (a.f.N % 4 == 0 ? 4 : 1);  // threads
     prof_mark(st);

@@ -48,7 +48,7 @@
 
 namespace ss {
 
-constexpr int kRow = 32;  // time steps per forward tile
+constexpr int kRow = kFwdRows;  // time steps per forward tile
 static_assert(kRow % kSub == 0, "a tile holds whole save intervals");
 
 template <typename T, int N>
@@ -67,19 +67,15 @@ struct FCfg {
     static constexpr int RW = GRP * ESZ / 4;        // 32-bit words of an item's run of one tensor
     static constexpr int NB = N * ESZ;              // bytes of a B / C row
     static constexpr int NWd = NB >= 4 ? NB / 4 : 1;  // 32-bit words per B / C row
-    // f32 B / C staging: a step's row is the N values of B, then the N of C,
-    // padded by 4 floats.  f32 io is copied straight into it (double
-    // buffered); 16-bit rows are copied raw and converted once.  (Unlike the
-    // backward, the forward keeps no packed bf16 rows: it is bound by latency,
-    // not by the shared-memory data pipe, and widening them in the scan sits
-    // on the path to the decays.)
-    static constexpr int BCF = 2 * N + 4;
+    // f32 B / C staging, one dense [step][N] array per tensor (the layout a TMA
+    // box lands in).  f32 io is copied straight into it (double buffered);
+    // 16-bit rows are copied raw and converted once.  (Unlike the backward, the
+    // forward keeps no packed bf16 rows: it is bound by latency, not by the
+    // shared-memory data pipe, and widening them in the scan sits on the path
+    // to the decays.)
     static constexpr bool BC_DIRECT = ESZ == 4;
     static constexpr bool BC_RAW = !BC_DIRECT && NB >= 4;
     static constexpr int BC_BUFS = BC_DIRECT ? 2 : 1;
-    // raw row length (elements): rows of 32 bytes or more padded by 16 bytes, so
-    // that the 16-byte loads of consecutive rows fall in different bank groups
-    static constexpr int RAWP = NB >= 32 ? N + 16 / ESZ : N;
     static constexpr int YP = CH + 4;               // padded row of partial readouts (floats)
     // plane of one lane of a pair's partial readouts: kRow rows of YP floats,
     // planes 16 mod 32 floats apart so that the 8-byte stores of the lanes of
@@ -92,7 +88,7 @@ struct FCfg {
 
 template <typename T, int N, int MODE>
 __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8)
-    k_fwd(FwdArgs a, FPlan p, int si, int64_t k_lo, float* ckpt) {
+    k_fwd(FwdArgs a, FPlan p, int si, int64_t k_lo, float* ckpt, const __grid_constant__ TmaMaps maps) {
     constexpr bool SUMMARY = MODE == kModeSummary;
     constexpr bool NOY = MODE == kModeSummary;                       // no readout (a chunk summary)
     constexpr bool GATE = MODE == kModeY || MODE == kModeYSave;      // gate and y (the checkpoint pass has neither)
@@ -100,20 +96,23 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
     using C = FCfg<T, N>;
     constexpr int NW = C::NW, NPW = C::NPW, S = C::S, G = C::G, PAIRS = C::PAIRS, CH = C::CH,
                   THREADS = C::THREADS, GRP = C::GRP, NGRP = C::NGRP, ITEMS = C::ITEMS, RW = C::RW,
-                  NWd = C::NWd, YP = C::YP, BCF = C::BCF;
+                  NWd = C::NWd, YP = C::YP;
     // per-(t, d) staging of the scan, one float4 per channel pair:
     // (delta_eff of both channels, delta_eff * u of both channels)
     __shared__ float4 sDU[kRow][PAIRS + 1];
     // (gate of both channels, D * u of both channels), read by the epilogue
     __shared__ float4 sGD[NOY ? 1 : kRow][NOY ? 1 : PAIRS + 1];
-    // B / C rows as f32; with f32 io double buffered, the next tile's rows
-    // being copied in while the scan reads the current one's
-    __shared__ __align__(16) float sBC[C::BC_BUFS][kRow][BCF];
-    // raw 16-bit B / C rows of the next tile (converted into sBC by the prologue)
-    __shared__ __align__(16) T sBCraw[2][C::BC_RAW ? kRow : 1][C::BC_RAW ? C::RAWP : 2];
-    // raw runs of delta, u, z of the next tile, copied in asynchronously by the
-    // thread that later converts them
-    __shared__ __align__(16) T sRaw[GATE ? 3 : 2][kRow][CH];
+    // B / C rows as f32 [tensor][buffer][step][N]; with f32 io double buffered,
+    // the next tile's rows being copied in while the scan reads the current one's
+    __shared__ __align__(128) float sBC[2][C::BC_BUFS][kRow][N];
+    // raw 16-bit B / C rows of the next tile [tensor][step][N] (converted into sBC
+    // by the prologue)
+    __shared__ __align__(128) T sBCraw[2][C::BC_RAW ? kRow : 1][C::BC_RAW ? N : 8];
+    // raw runs of delta, u, z of the next tile (a TMA box each, or copied in
+    // asynchronously by the thread that later converts them)
+    __shared__ __align__(128) T sRaw[GATE ? 3 : 2][kRow][CH];
+    // completion of the TMA copies into the two tile buffers
+    __shared__ __align__(8) uint64_t sBar[2];
     // per-warp partial readouts, one plane per lane of a pair (float g YPL + i YP
     // + c: lane g's sum over its states, step i, channel c)
     __shared__ __align__(16) float sY[NOY ? 1 : NW][NOY ? 1 : G * C::YPL];
@@ -130,7 +129,19 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
     const int64_t s_first = sgm.s0 + ul * sgm.K;  // summary index of the unit's chunk 0
     const int64_t L = a.L, Dch = a.Dch;
     const int64_t d0 = tile * CH;
-    const bool fast = ((Dch * (int64_t)sizeof(T)) % 16 == 0) && (d0 + CH <= Dch);
+    // TMA boxes land on 128-byte aligned shared memory; a block whose buffers are
+    // not (never expected) records it and stages with asynchronous copies instead
+    bool tma = a.use_tma != 0;
+    if (tma && !(smem_aligned128(&sRaw[0][0][0]) && smem_aligned128(&sBC[0][0][0][0]) &&
+                 smem_aligned128(&sBCraw[0][0][0]))) {
+        if (threadIdx.x == 0) atomicOr(a.status, kDevMisaligned);
+        tma = false;
+    }
+    // the tile's runs are read from shared memory: TMA boxes (zero-filled past Dch),
+    // or whole aligned vectors copied in asynchronously
+    // whole aligned vectors of y / y0 per row: stores need the tile inside Dch
+    const bool sfast = ((Dch * (int64_t)sizeof(T)) % 16 == 0) && (d0 + CH <= Dch);
+    const bool fast = tma || sfast;
     const T* u = static_cast<const T*>(a.u);
     const T* delta = static_cast<const T*>(a.delta);
     const T* Bm = static_cast<const T*>(a.B);
@@ -141,6 +152,11 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
         const int64_t dc = d0 + c < Dch ? d0 + c : Dch - 1;
         sBias[c] = a.delta_bias ? a.delta_bias[dc] : 0.f;
         sDv[c] = a.D ? a.D[dc] : 0.f;
+    }
+    if (tma && tid == 0) {
+        mbar_init(&sBar[0], 1);
+        mbar_init(&sBar[1], 1);
+        fence_proxy_async_smem();
     }
 
     // scan-lane identity: channel pair pp (channels c0, c0 + 1 of the block),
@@ -191,10 +207,32 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
     float* ck_lane =
         SAVE ? ckpt + (t_begin / kSub) * ck_stride + (b * ntiles + tile) * (CH * N) + ckpt_slot(w, lane, S) : nullptr;
 
-    // Asynchronous copies of the tile starting at tt: the thread's item runs
-    // (when the tile's rows are whole aligned vectors) and the B / C rows (f32
-    // into sBC[buf]; 16-bit raw into sBCraw); one commit group.
+    // Copies of the tile starting at tt into buffer buf.  With TMA: one thread
+    // issues a box per tensor (delta, u, z as [kRow][CH], B and C as
+    // [kRow][N]: f32 into sBC[.][buf], 16-bit raw into sBCraw) on the buffer's
+    // barrier.  Otherwise: each thread copies its item runs (when the tile's
+    // rows are whole aligned vectors) and B / C rows asynchronously; one commit
+    // group.
+    const TmaMaps& mp = maps;
     auto issue = [&](int64_t tt, int buf) {
+        if (tma) {
+            if (tid == 0) {
+                constexpr uint32_t run = kRow * CH * C::ESZ, row = kRow * N * C::ESZ;
+                mbar_expect_tx(&sBar[buf], (GATE && z ? 3 : 2) * run + (NOY ? 1 : 2) * row);
+                const int x = (int)d0, y = (int)tt, zc = (int)b;
+                tma_load_3d(&sRaw[0][0][0], &mp.m[kMapDelta], x, y, zc, &sBar[buf]);
+                tma_load_3d(&sRaw[1][0][0], &mp.m[kMapU], x, y, zc, &sBar[buf]);
+                if (GATE && z) tma_load_3d(&sRaw[GATE ? 2 : 1][0][0], &mp.m[kMapZ], x, y, zc, &sBar[buf]);
+                if constexpr (C::BC_DIRECT) {
+                    tma_load_3d(&sBC[0][buf][0][0], &mp.m[kMapB], 0, y, zc, &sBar[buf]);
+                    if (!NOY) tma_load_3d(&sBC[1][buf][0][0], &mp.m[kMapC], 0, y, zc, &sBar[buf]);
+                } else {
+                    tma_load_3d(&sBCraw[0][0][0], &mp.m[kMapB], 0, y, zc, &sBar[buf]);
+                    if (!NOY) tma_load_3d(&sBCraw[1][0][0], &mp.m[kMapC], 0, y, zc, &sBar[buf]);
+                }
+            }
+            return;
+        }
         if (fast) {
 #pragma unroll
             for (int it = 0; it < ITEMS; it++) {
@@ -214,7 +252,7 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
             const int64_t t = tt + r;
             const T* src = (half ? Cm : Bm) + (b * L + (t < t_end ? t : 0)) * N;
             if constexpr (C::BC_DIRECT) {
-                float* dst = &sBC[buf][r][half * N];
+                float* dst = &sBC[half][buf][r][0];
                 if (t < t_end) {
                     cp_async_bytes<N * 4>(dst, src);
                 } else {
@@ -228,11 +266,16 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
         cp_async_commit();
     };
     issue(t_begin, 0);
-    __syncthreads();  // sBias / sDv
+    __syncthreads();  // sBias / sDv, the barriers
 
     for (int64_t t0 = t_begin; t0 < t_end; t0 += kRow) {
-        const int buf = (int)(((t0 - t_begin) / kRow) & 1);
-        cp_async_wait<0>();  // this thread's copies of the tile
+        const int64_t jt = (t0 - t_begin) / kRow;  // tile index within the chunk
+        const int buf = (int)(jt & 1);
+        // the tile's copies: this thread's own (asynchronous copies), or the
+        // TMA boxes (the buffer's barrier completes its phase jt / 2 mod 2)
+        bool ok = true;
+        if (tma) ok = mbar_wait(&sBar[buf], (uint32_t)((jt >> 1) & 1));
+        else cp_async_wait<0>();
         // ---- prologue: (step, 8-channel group) items, then the B / C rows
 #pragma unroll
         for (int it = 0; it < ITEMS; it++) {
@@ -286,12 +329,23 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
                     if constexpr (C::BC_RAW) lds_words<C::NB, NWd>(&sBCraw[half][r][0], wv);
                     else load_words<C::NB, NWd>((half ? Cm : Bm) + (b * L + t) * N, wv);
                 }
-                float* dst = &sBC[0][r][half * N];
+                float* dst = &sBC[half][0][r][0];
 #pragma unroll
                 for (int n = 0; n < N; n++) dst[n] = t < t_end ? elem<T>(wv, n) : 0.f;
             }
         }
-        __syncthreads();  // staging complete; every thread is done reading sRaw / sBCraw
+        // Staging complete; every thread is done reading sRaw / sBCraw.  A thread
+        // whose wait for the tile ran out makes the whole block give up (the
+        // block agrees here, so no thread is left at a later barrier): the status
+        // word records it and the thread that issued the copies waits once more
+        // for them before the block's shared memory is released.
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                atomicOr(a.status, kDevWaitTimeout);
+                mbar_wait(&sBar[buf], (uint32_t)((jt >> 1) & 1));
+            }
+            return;
+        }
         if (t0 + kRow < t_end) issue(t0 + kRow, buf ^ 1);
 
         // ---- scan: 32 steps of the lane's 2 x S states.  Steps past t_end (last
@@ -299,7 +353,8 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
         // Software-pipelined by two steps: the decays and input terms of step
         // i + 2 (loads, exponents, MUFU) are formed before the recurrence of
         // step i, which is the only part that waits on the previous state.
-        const float* bcrow = &sBC[C::BC_DIRECT ? buf : 0][0][0];
+        const float* brow = &sBC[0][C::BC_DIRECT ? buf : 0][0][0];
+        const float* crow = &sBC[1][C::BC_DIRECT ? buf : 0][0][0];
         // decays, input terms and C values of the next two steps, by step parity
         float2 daQ[2][S], xbQ[2][S];
         float cQ[2][S] = {};
@@ -308,8 +363,8 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
             const float2 dl2 = make_float2(du.x, du.y), dlu2 = make_float2(du.z, du.w);
             if (SUMMARY) sdp = add2(sdp, dl2);  // delta_eff of steps past t_end is zero
             float Bv[S];
-            ld_f32<S>(bcrow + i * BCF + n0, Bv);
-            if (!NOY) ld_f32<S>(bcrow + i * BCF + N + n0, cQ[sl]);
+            ld_f32<S>(brow + i * N + n0, Bv);
+            if (!NOY) ld_f32<S>(crow + i * N + n0, cQ[sl]);
 #pragma unroll
             for (int s = 0; s < S; s++) {
                 const float2 ex = mul2(dl2, A2[s]);
@@ -403,7 +458,7 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
                     if (a.y0 && z) {
                         // kept for the backward's dz (f32; the same alignment as the io runs)
                         float* y0row = a.y0 + off;
-                        if (fast) {
+                        if (sfast) {
 #pragma unroll
                             for (int c = 0; c < GRP; c += 4)
                                 *reinterpret_cast<float4*>(y0row + c) = make_float4(y0v[c], y0v[c + 1], y0v[c + 2], y0v[c + 3]);
@@ -415,7 +470,7 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
                     }
                     if (!GATE) continue;
                     T* yrow = static_cast<T*>(a.y) + off;
-                    if (fast) {
+                    if (sfast) {
                         uint32_t wv[RW];
                         if constexpr (sizeof(T) == 4) {
 #pragma unroll
@@ -464,24 +519,26 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
 // One launch of mode MODE over chunks k_lo .. k_hi of segment si.
 template <typename T, int N, int MODE>
 void launch_fwd_mode(const FwdArgs& a, const FPlan& p, int si, cudaStream_t st, int64_t k_lo, int64_t k_hi,
-                     float* ckpt) {
+                     float* ckpt, const TmaMaps& maps) {
     prof_mark(st);
-    k_fwd<T, N, MODE><<<(unsigned)(p.seg[si].nu * (k_hi - k_lo)), FCfg<T, N>::THREADS, 0, st>>>(a, p, si, k_lo, ckpt);
+    k_fwd<T, N, MODE><<<(unsigned)(p.seg[si].nu * (k_hi - k_lo)), FCfg<T, N>::THREADS, 0, st>>>(a, p, si, k_lo, ckpt,
+                                                                                               maps);
 }
 
 // The chunk summaries of every chunked segment, then each segment's main pass.
 template <typename T, int N>
-cudaError_t launch_fwd_t(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt) {
+cudaError_t launch_fwd_t(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt,
+                         const TmaMaps& maps) {
     for (int si = 0; si < p.nseg; si++)
-        if (p.seg[si].K > 1) launch_fwd_mode<T, N, kModeSummary>(a, p, si, st, 0, p.seg[si].K - 1, nullptr);
+        if (p.seg[si].K > 1) launch_fwd_mode<T, N, kModeSummary>(a, p, si, st, 0, p.seg[si].K - 1, nullptr, maps);
     for (int si = 0; si < p.nseg; si++) {
         const int64_t K = p.seg[si].K;
         if (mode == kModeCkpt) {
-            launch_fwd_mode<T, N, kModeCkpt>(a, p, si, st, 0, K, ckpt);
+            launch_fwd_mode<T, N, kModeCkpt>(a, p, si, st, 0, K, ckpt, maps);
         } else if (ckpt) {
-            launch_fwd_mode<T, N, kModeYSave>(a, p, si, st, 0, K, ckpt);
+            launch_fwd_mode<T, N, kModeYSave>(a, p, si, st, 0, K, ckpt, maps);
         } else {
-            launch_fwd_mode<T, N, kModeY>(a, p, si, st, 0, K, nullptr);
+            launch_fwd_mode<T, N, kModeY>(a, p, si, st, 0, K, nullptr, maps);
         }
     }
     return cudaGetLastError();
@@ -489,14 +546,15 @@ cudaError_t launch_fwd_t(const FwdArgs& a, const FPlan& p, cudaStream_t st, int 
 
 // Forward launcher of one io type: switches on N.
 template <typename T>
-cudaError_t launch_fwd_io(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt) {
+cudaError_t launch_fwd_io(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt,
+                          const TmaMaps& maps) {
     switch (a.N) {
-        case 1: return launch_fwd_t<T, 1>(a, p, st, mode, ckpt);
-        case 2: return launch_fwd_t<T, 2>(a, p, st, mode, ckpt);
-        case 4: return launch_fwd_t<T, 4>(a, p, st, mode, ckpt);
-        case 8: return launch_fwd_t<T, 8>(a, p, st, mode, ckpt);
-        case 16: return launch_fwd_t<T, 16>(a, p, st, mode, ckpt);
-        case 32: return launch_fwd_t<T, 32>(a, p, st, mode, ckpt);
+        case 1: return launch_fwd_t<T, 1>(a, p, st, mode, ckpt, maps);
+        case 2: return launch_fwd_t<T, 2>(a, p, st, mode, ckpt, maps);
+        case 4: return launch_fwd_t<T, 4>(a, p, st, mode, ckpt, maps);
+        case 8: return launch_fwd_t<T, 8>(a, p, st, mode, ckpt, maps);
+        case 16: return launch_fwd_t<T, 16>(a, p, st, mode, ckpt, maps);
+        case 32: return launch_fwd_t<T, 32>(a, p, st, mode, ckpt, maps);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -2,5 +2,6 @@
 #include "fwd.cuh"
 
 namespace ss {
-template cudaError_t launch_fwd_io<float>(const FwdArgs&, const FPlan&, cudaStream_t, int, float*);
+template cudaError_t launch_fwd_io<float>(const FwdArgs&, const FPlan&, cudaStream_t, int, float*,
+                                              const TmaMaps&);
 }  // namespace ss

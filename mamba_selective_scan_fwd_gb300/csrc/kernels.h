@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include "common.cuh"
+#include "tma.cuh"
 
 namespace ss {
 
@@ -26,6 +27,11 @@ struct FwdArgs {
     // saving and checkpoint passes for the backward's dz when z is given
     // (null: not stored)
     float* y0;
+    // tiles staged by TMA through the kernel's tensor maps (else by per-thread
+    // asynchronous copies), and the library's device status word, where a
+    // kernel that gave up waiting for a copy leaves kDevWaitTimeout
+    int use_tma;
+    int* status;
 };
 
 // A[d, n] of the scan: the input itself, or -exp(A_log) in the A_log form.
@@ -87,6 +93,7 @@ __host__ __device__ constexpr int64_t channels_per_block(int64_t N) {
 }
 
 constexpr int kSub = 8;  // steps between saved states (the backward's recompute window)
+constexpr int kFwdRows = 32;  // steps per forward tile
 
 // Launch plan.  A unit is one (batch row, channel tile): unit u = b tiles_b +
 // tile.  Units are grouped into at most two segments; a segment cuts the time
@@ -253,15 +260,21 @@ void prof_mark(cudaStream_t st);
 // Launchers of one io type T (float, __half, __nv_bfloat16), defined in the
 // per-io translation units.
 template <typename T>
-cudaError_t launch_fwd_io(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt);
+cudaError_t launch_fwd_io(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt,
+                          const TmaMaps& maps);
 template <typename T>
-cudaError_t launch_bwd_io(const BwdArgs& a, const FPlan& p, cudaStream_t st, float* ckpt_out);
+cudaError_t launch_bwd_io(const BwdArgs& a, const FPlan& p, cudaStream_t st, float* ckpt_out, const TmaMaps& fmaps,
+                          const TmaMaps& bmaps);
 
 // ckpt: where the Y-mode forward also stores the states entering every kSub-th step (may be null).
-cudaError_t launch_fwd(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt);
+// maps: the forward's tensor maps (boxes of kFwdRows steps), used when a.use_tma.
+cudaError_t launch_fwd(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt, const TmaMaps& maps);
 // ckpt_out: the checkpoint buffer to fill first, or null when a.ws_ckpt already
 // holds the states saved by the forward.
-cudaError_t launch_bwd(const BwdArgs& a, const FPlan& p, cudaStream_t st, float* ckpt_out);
+// fmaps / bmaps: tensor maps of the forward (checkpoint pass) and of the backward
+// (boxes of kSub steps), used when a.f.use_tma.
+cudaError_t launch_bwd(const BwdArgs& a, const FPlan& p, cudaStream_t st, float* ckpt_out, const TmaMaps& fmaps,
+                       const TmaMaps& bmaps);
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
 

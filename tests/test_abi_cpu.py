@@ -37,13 +37,29 @@ def test_library_exports_every_declared_symbol():
     lib = ss.lib()
     for name in declared_functions():
         assert hasattr(lib, name), name
-    assert lib.ss_abi_version() == binding.ABI_VERSION == 4
+    assert lib.ss_abi_version() == binding.ABI_VERSION == 5
 
 
 def test_status_strings():
-    for code in range(5):
+    for code in range(7):
         assert len(ss.status_string(code)) >= 2
     assert "unknown" in ss.status_string(99)
+
+
+def test_selftest_wait_limit_checked_before_any_launch():
+    # the limit is validated before the first CUDA call
+    assert ss.lib().ss_selftest_wait_timeout(-1, None) == INVALID
+    assert ss.lib().ss_selftest_wait_timeout(2_000_000_001, None) == INVALID
+
+
+def test_copies_only_switch_round_trips():
+    prev = ss.set_copies_only(True)
+    try:
+        assert ss.set_copies_only(True) is True
+        assert ss.set_copies_only(False) is True
+        assert ss.set_copies_only(False) is False
+    finally:
+        ss.set_copies_only(prev)
 
 
 def test_workspace_queries_are_pure_and_sized():

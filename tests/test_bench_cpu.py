@@ -44,11 +44,11 @@ def test_job_throughput_is_all_ranks_over_the_slowest():
 def test_traffic_reported_only_for_its_sources(monkeypatch):
     w = bench.pick_workload("mamba2.8b-layer-bf16")
     monkeypatch.setattr(build, "source_digest", lambda: bench.TRAFFIC_SRC_DIGEST)
-    assert bench.measured_traffic("k_bwd2_main", w) == bench.TRAFFIC[("k_bwd2_main", w.name)]
-    assert bench.measured_traffic("k_fwd2_y", w) == bench.TRAFFIC[("k_fwd2_y", w.name)]
-    assert bench.measured_traffic("k_bwd2_main", bench.pick_workload("long-seq-bf16")) is None
+    assert bench.measured_traffic("k_bwd_main", w) == bench.TRAFFIC[("k_bwd_main", w.name)]
+    assert bench.measured_traffic("k_fwd_y", w) == bench.TRAFFIC[("k_fwd_y", w.name)]
+    assert bench.measured_traffic("k_bwd_main", bench.pick_workload("long-seq-bf16")) is None
     monkeypatch.setattr(build, "source_digest", lambda: "0" * 16)
-    assert bench.measured_traffic("k_bwd2_main", w) is None
+    assert bench.measured_traffic("k_bwd_main", w) is None
 
 
 def test_traffic_figures_are_plausible():
@@ -57,8 +57,8 @@ def test_traffic_figures_are_plausible():
     w = bench.pick_workload("mamba2.8b-layer-bf16")
     fwd, bwd = bench.algorithmic_bytes(w)
     bwd_main = bwd - 2 * w.Bsz * w.L * w.N * 4 - 4 * (w.Dch * w.N + 2 * w.Dch)
-    assert bwd_main <= bench.TRAFFIC[("k_bwd2_main", w.name)] <= 3 * bwd_main
-    assert fwd <= bench.TRAFFIC[("k_fwd2_y", w.name)] <= 4 * fwd
+    assert bwd_main <= bench.TRAFFIC[("k_bwd_main", w.name)] <= 3 * bwd_main
+    assert fwd <= bench.TRAFFIC[("k_fwd_y", w.name)] <= 4 * fwd
 
 
 def test_unknown_workload_exits():
@@ -72,3 +72,52 @@ def test_mufu_counts():
     # 83,886,080 (t, d) elements x 16 states: the 1.342 G exponentials of each direction's scan
     assert m["scan_ex2_per_direction"] == 1_342_177_280
     assert m["fwd_all"] == 83_886_080 * 20 and m["bwd_all"] == 83_886_080 * 21
+
+
+def test_reference_arm_reports_the_same_config():
+    w = bench.pick_workload("mamba2.8b-layer-bf16")
+    c = bench.config_of(w, 1)
+    assert c == bench.config_of(w, 1)
+    assert (c["workload"], c["Bsz"], c["L"], c["Dch"], c["N"], c["io"]) == ("mamba2.8b-layer-bf16", 4, 4096, 5120, 16,
+                                                                           "bf16")
+    assert c["step"] == "ss_fwd_save + ss_bwd_saved"
+    assert bench.config_of(bench.pick_workload("mamba130m-layer-bf16-fwd"), 1)["step"] == "ss_fwd"
+
+
+def _peaks():
+    return {"hbm_gbs": 7000.0, "hbm_kind": "measured", "ex2_per_clk_per_sm": 32.0, "sms": 152, "sm_mhz": 2000.0}
+
+
+def test_analyse_rooflines_of_a_training_step():
+    w = bench.pick_workload("mamba2.8b-layer-bf16")
+    plan = {"segments": [(608, 1), (32, 19)]}
+    # launches: fwd = summary, main(seg0), main(seg1); bwd = summary, main x2, reduce_bc, reduce_params
+    k_fwd = [0.05, 0.4, 0.1]
+    k_bwd = [0.06, 0.9, 0.2, 0.05, 0.01]
+    out = bench.analyse(w, plan, 2.0, sum(k_fwd), sum(k_bwd), k_fwd, k_bwd, _peaks())
+    fwd_b, bwd_b = bench.algorithmic_bytes(w)
+    # backward main pass: HBM-bound at 7000 GB/s (its bytes exclude dB / dC and the parameter gradients)
+    bwd_main = bwd_b - 2 * w.Bsz * w.L * w.N * 4 - 4 * (w.Dch * w.N + 2 * w.Dch)
+    r = out["roofline"]
+    assert r["bound"] == "hbm" and r["ms"] == pytest.approx(1.1)
+    assert r["achieved"] == pytest.approx(bwd_main / 1.1e-3 / 1e9, rel=1e-3)
+    # forward: 1.342 G exponentials at 152 x 32 x 2000 MHz = 9728 Gexp2/s -> 0.138 ms, above 673.8 MB / 7 TB/s
+    rf = out["roofline_fwd"]
+    assert rf["bound"] == "alu" and rf["peak"] == pytest.approx(9728.0)
+    assert rf["roofline_ms"] == pytest.approx(1_342_177_280 / 9.728e12 * 1e3, rel=1e-3)
+    t_roof = rf["roofline_ms"] + bwd_b / 7e12 * 1e3
+    assert out["roofline_step_frac"] == pytest.approx(t_roof / 2.0, abs=1e-4)
+    assert list(out["kernel_ms"]) == [
+        "k_fwd chunk summary (32 units x 19 chunks)", "k_fwd y + saved states (608 units x 1 chunk)",
+        "k_fwd y + saved states (32 units x 19 chunks)", "k_bwd reverse summary (32 units x 19 chunks)",
+        "k_bwd main (608 units x 1 chunk)", "k_bwd main (32 units x 19 chunks)", "k_bwd_reduce_bc",
+        "k_bwd_reduce_params"]
+
+
+def test_analyse_forward_only_step():
+    w = bench.pick_workload("mamba130m-layer-bf16-fwd")
+    plan = {"segments": [(384, 2)]}
+    out = bench.analyse(w, plan, 0.2, 0.2, 0.0, [0.05, 0.15], [], _peaks())
+    assert "roofline_fwd" not in out and "bwd_ms" not in out
+    assert out["roofline"]["ms"] == pytest.approx(0.15)
+    assert list(out["kernel_ms"]) == ["k_fwd chunk summary (384 units x 2 chunks)", "k_fwd y (384 units x 2 chunks)"]
