@@ -281,9 +281,10 @@ int bwd_impl(const void* u, const void* delta, const float* A, const void* B, co
     a.ws_db = reinterpret_cast<float*>(ws + w.db);
     rc = status_for_current_device(&a.f.status);
     if (rc != SS_OK) return rc;
-    // the forward passes that store the restart states use the forward's maps
+    // the forward passes that store the restart states and the reverse summaries
+    // use the forward's 32-step boxes, the main pass its own
     TmaMaps fmaps, bmaps;
-    a.f.use_tma = tma_eligible(Bsz, L, Dch, N, dtype) && make_maps(fmaps, a.f, nullptr, nullptr, kFwdRows) &&
+    a.f.use_tma = tma_eligible(Bsz, L, Dch, N, dtype) && make_maps(fmaps, a.f, dy, nullptr, kFwdRows) &&
                           make_maps(bmaps, a.f, dy, z ? a.y0 : nullptr, kSub)
                       ? 1
                       : 0;

@@ -842,6 +842,12 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
     }
 }
 
+}  // namespace ss
+
+#include "rsum.cuh"
+
+namespace ss {
+
 // Ask for the largest shared-memory carveout for `kernel`, so that shared
 // memory does not cap residency: once per device (a kernel attribute of the
 // current device, not a stream operation, so that calls captured into a CUDA
@@ -870,13 +876,26 @@ cudaError_t launch_bwd_t(const BwdArgs& a, const FPlan& p, cudaStream_t st, floa
         if (e != cudaSuccess) return e;
     }
     constexpr int threads = BCfg<T, N>::THREADS;
-    // reverse summaries of every chunked segment (chunks 1 .. K-1)
+    // reverse summaries of every chunked segment (chunks 1 .. K-1): the
+    // dedicated kernel for two-warp blocks (32-step tiles through the forward's
+    // maps), the main kernel's summary mode for one-warp blocks (whose 32- or
+    // 64-channel tiles would need too much shared memory there)
+    static std::atomic<uint64_t> rsum_carveout_done{0};
+    if constexpr (BCfg<T, N>::NW == 2) {
+        bool any = false;
+        for (int si = 0; si < p.nseg; si++) any = any || p.seg[si].K > 1;
+        if (any) {
+            e = prefer_max_shared(k_bwd_rsum<T, N>, rsum_carveout_done);
+            if (e != cudaSuccess) return e;
+        }
+    }
     for (int si = 0; si < p.nseg; si++) {
         const int64_t K = p.seg[si].K;
         if (K > 1) {
             prof_mark(st);
-            k_bwd<T, N, kRevSummary, false><<<(unsigned)(p.seg[si].nu * (K - 1)), threads, 0, st>>>(a, p, si, 1,
-                                                                                                     bmaps);
+            const unsigned grid = (unsigned)(p.seg[si].nu * (K - 1));
+            if constexpr (BCfg<T, N>::NW == 2) k_bwd_rsum<T, N><<<grid, threads, 0, st>>>(a, p, si, 1, fmaps);
+            else k_bwd<T, N, kRevSummary, false><<<grid, threads, 0, st>>>(a, p, si, 1, bmaps);
         }
     }
     const bool state = a.dlast != nullptr || a.dh0 != nullptr;
