@@ -62,7 +62,7 @@ __device__ __forceinline__ void ld_row(const T* p, float (&v)[S]) {
 }
 
 template <typename T, int N>
-__global__ void __launch_bounds__(32 * scan_warps(N), 4) k_bwd_rsum(BwdArgs a, FPlan p, int si, int64_t k_lo,
+__global__ void __launch_bounds__(32 * scan_warps(N), 6) k_bwd_rsum(BwdArgs a, FPlan p, int si, int64_t k_lo,
                                                                const __grid_constant__ TmaMaps maps) {
     using C = RCfg<T, N>;
     constexpr int NPW = C::NPW, S = C::S, SP = C::SP, G = C::G, PAIRS = C::PAIRS, CH = C::CH,
