@@ -12,8 +12,8 @@ import torch
 
 import mamba_selective_scan_fwd_gb300 as ss
 from mamba_selective_scan_fwd_gb300.inputs import small_inputs
-from gpu_util import (TOL, gpu_bwd, gpu_bwd_saved, gpu_fwd, gpu_fwd_save, normwise, oracle_bwd, oracle_fwd, ref_y,
-                      to_device)
+from gpu_util import (TOL, gpu_bwd, gpu_bwd_saved, gpu_fwd, gpu_fwd_save, normwise, normwise_rows, oracle_bwd,
+                      oracle_fwd, ref_y, to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -114,3 +114,39 @@ def test_split_plan_parity_one_warp_blocks(orc):
     assert normwise(last[1, d0:], rf.last_state[1, d0:]) <= tf
     for k in ("du", "ddelta", "dz"):
         assert normwise(g[k][1, :, d0:], getattr(rb, k)[1, :, d0:]) <= tb, k
+
+
+# 384 units (6 batch rows x 64 channel tiles) hold fewer than 8 warps per SM:
+# every unit is cut into 3 chunks, and the 768 forward summaries (chunks 0, 1)
+# are more blocks than one round of the main kernel, which takes the dedicated
+# summary kernel for 16-bit io (f32 io keeps the summary mode of k_fwd)
+WIDE = (6, 320, 2048, 16)
+
+
+def test_wide_summary_plan():
+    p = ss.plan_info(*WIDE, ss.SS_BF16)
+    assert p["segments"] == [(384, 3)]
+
+
+@pytest.mark.parametrize("io", ["bf16", "f16", "f32"])
+def test_wide_summary_parity(orc, io):
+    x = small_inputs(*WIDE, io=io, seed=5300)
+    t = to_device(x, io)
+    y, last, saved = gpu_fwd_save(t)
+    g = gpu_bwd_saved(t, saved)
+    torch.cuda.synchronize()
+    rows = np.random.default_rng(5301).choice(WIDE[0] * WIDE[2], 96, replace=False)
+    rows[0] = WIDE[0] * WIDE[2] - 1
+    rf = oracle_fwd(orc, x, rows=rows)
+    rb = oracle_bwd(orc, x, rows=rows, want_dBdC=False)
+    bi = torch.as_tensor(rows // WIDE[2], device=y.device)
+    di = torch.as_tensor(rows % WIDE[2], device=y.device)
+    tf, tb = TOL[io]["fwd"], TOL[io]["bwd"]
+    # sampled rows [n_rows, L], each bounded on its own scale
+    assert normwise_rows(y[bi, :, di].float().cpu().numpy(), ref_y(rf.y, io), (0,)) <= tf
+    assert normwise(last[bi, di].cpu().numpy(), rf.last_state) <= tf
+    for k in ("du", "ddelta", "dz"):
+        assert normwise_rows(g[k][bi, :, di].cpu().numpy(), getattr(rb, k), (0,)) <= tb, k
+    # the plain forward gives the same bits as the saving one
+    y2, last2 = gpu_fwd(t)
+    assert torch.equal(y, y2) and torch.equal(last, last2)
