@@ -314,3 +314,12 @@ def test_binding_checks_before_any_launch():
         binding.ss_fwd_noalloc(u, u, A, Bm, Bm, None, None, None, True, y)
     with pytest.raises(ValueError, match="CUDA"):
         binding.ss_fwd(u, u, A, Bm, Bm)
+
+
+def test_ex2_probe_checks_arguments_before_any_launch():
+    import ctypes
+
+    out = ctypes.c_double()
+    assert ss.lib().ss_measure_ex2_rate(0, ctypes.byref(out)) == INVALID
+    assert ss.lib().ss_measure_ex2_rate(1 << 21, ctypes.byref(out)) == INVALID
+    assert ss.lib().ss_measure_ex2_rate(16, None) == INVALID

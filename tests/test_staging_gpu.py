@@ -93,3 +93,12 @@ def test_wait_timeout_is_reported_and_context_survives():
     torch.cuda.synchronize()
     assert torch.equal(y_before, y_after)
     assert ss.device_status() == ss.SS_OK
+
+
+def test_ex2_rate_probe():
+    # MUFU ex2 results per clock per SM: a whole number of results per cycle per
+    # sub-partition on any part this library builds for (GB300: 32 per SM)
+    r = ss.binding.measure_ex2_rate(2048)
+    assert 8.0 <= r <= 64.0
+    assert abs(r - round(r / 4) * 4) < 0.5
+    assert ss.device_status() == ss.SS_OK
