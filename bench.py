@@ -486,7 +486,7 @@ def run_ours(args):
     dev = torch.device("cuda", local if world > 1 else 0)
     ss.set_copies_only(args.staging == "copies")
     w = pick_workload(args.workload)
-    x = make_inputs(w, with_dy=True)
+    x = make_inputs(w, with_dy=w.backward)
     stream = torch.cuda.current_stream(dev)
     r = Runner(w, x, dev, stream, pin=True)
 
@@ -507,10 +507,12 @@ def run_ours(args):
     t_fwd, t_bwd, k_fwd, k_bwd = attribute(r, K)
 
     # ---- the recomputing pair (ss_fwd + ss_bwd: the backward recomputes the
-    # restart states itself) on the same inputs
-    for _ in range(3):
-        r.step_recompute()
-    recompute_ms = time_steps(r.step_recompute, K, dev, stream, world) / K
+    # restart states itself) on the same inputs (a forward-only workload has none)
+    recompute_ms = None
+    if w.backward:
+        for _ in range(3):
+            r.step_recompute()
+        recompute_ms = time_steps(r.step_recompute, K, dev, stream, world) / K
 
     # ---- end to end through the public API with host buffers.  Every step copies
     # its inputs from pinned host memory and its outputs back; two sets of device
@@ -552,12 +554,14 @@ def run_ours(args):
             if i >= 2:
                 stream.wait_event(ev["out"][j])  # step i - 2's outputs have left this set
             di = bs["d"]
-            ss.ss_fwd_save(di["u"], di["delta"], di["A"], di["B"], di["C"], di["D"], di["z"], di["delta_bias"],
-                           w.softplus, y=bs["y"], last_state=bs["last"], saved=r.saved, workspace=r.ws_f,
-                           stream=stream)
-            bs["g"].update(ss.ss_bwd_saved(di["u"], di["delta"], di["A"], di["B"], di["C"], di["D"], di["z"],
-                                           di["delta_bias"], w.softplus, di["dy"], r.saved, out=bs["g"],
-                                           workspace=r.ws_b, stream=stream))
+            fargs = (di["u"], di["delta"], di["A"], di["B"], di["C"], di["D"], di["z"], di["delta_bias"], w.softplus)
+            if w.backward:
+                ss.ss_fwd_save(*fargs, y=bs["y"], last_state=bs["last"], saved=r.saved, workspace=r.ws_f,
+                               stream=stream)
+                bs["g"].update(ss.ss_bwd_saved(*fargs, di["dy"], r.saved, out=bs["g"], workspace=r.ws_b,
+                                               stream=stream))
+            else:
+                ss.ss_fwd(*fargs, y=bs["y"], last_state=bs["last"], workspace=r.ws_f, stream=stream)
             ev["done"][j].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev["done"][j])
@@ -607,7 +611,7 @@ def run_ours(args):
     }
     line.update(stats)
     line.update({
-        "step_recompute_ms": round(recompute_ms, 4),
+        "step_recompute_ms": None if recompute_ms is None else round(recompute_ms, 4),
         "mufu_ops": mufu_counts(w), "ex2_per_clk_per_sm": round(ex2, 3),
         "clocks": clk,
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
