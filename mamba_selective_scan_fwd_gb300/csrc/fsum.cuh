@@ -11,8 +11,8 @@
 // packed f32x2 operations per state pair next to the per-(t, d) softplus of
 // the prologue.  Like the reverse summaries, this kernel stages 32-step tiles
 // (delta, u and B through TMA, one tile ahead) with one block barrier per
-// tile: the tile's (delta_eff, delta_eff u) and its B rows widened to f32 go
-// to shared-memory buffers of their own by tile parity.  The sum of
+// tile: the tile's (delta_eff, delta_eff u) and its B rows (widened to f32 for
+// 16-bit io) go to shared-memory buffers of their own by tile parity.  The sum of
 // delta_eff is formed by the prologue threads over their own items, then
 // added across them in a fixed order.  Block and lane layout are the forward
 // main kernel's (FCfg), registers pairing a lane's two channels at one state,
@@ -49,17 +49,23 @@ __global__ void __launch_bounds__(32 * scan_warps(N), 6) k_fwd_fsum(FwdArgs a, F
     using C = FSCfg<T, N>;
     constexpr int NPW = C::NPW, S = C::S, G = C::G, PAIRS = C::PAIRS, CH = C::CH, THREADS = C::THREADS,
                   GRP = C::GRP, NGRP = C::NGRP, ITEMS = C::ITEMS, RW = C::RW;
+    // f32 io: the scan reads B straight from the tile's buffer (no widened copy),
+    // which keeps the block at 36 KB so that 6 fit on an SM
+    constexpr bool DIRECT = sizeof(T) == 4;
     // raw runs of delta, u and the B rows of a tile, double buffered (a TMA box
     // each, or loaded by the prologue)
     __shared__ __align__(128) T sRaw[2][2][kFsTT][CH];
     __shared__ __align__(128) T sBr[2][kFsTT][N];
     // (delta_eff of both channels, delta_eff u of both channels) per step and
-    // channel pair, and the B rows as f32, double buffered by tile
+    // channel pair, and the B rows widened to f32 (16-bit io), double buffered by tile
     __shared__ float4 sDU[2][kFsTT][PAIRS];
-    __shared__ __align__(16) float sB[2][kFsTT][N];
+    __shared__ __align__(16) float sB[2][DIRECT ? 1 : kFsTT][DIRECT ? 4 : N];
     __shared__ __align__(8) uint64_t sBar[2];
     __shared__ float sBias[CH];
-    __shared__ float sSD[THREADS][GRP + 1];
+    // per-thread sums of delta_eff over its items, added at the end: in the raw
+    // runs' buffer, free by then (every thread is past its last prologue)
+    static_assert(sizeof(T) * 2 * 2 * kFsTT * CH >= sizeof(float) * THREADS * (GRP + 1), "room for the sums");
+    float(*sSD)[GRP + 1] = reinterpret_cast<float(*)[GRP + 1]>(&sRaw[0][0][0][0]);
 
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const Seg sgm = seg_at(p, si);
@@ -166,18 +172,22 @@ __global__ void __launch_bounds__(32 * scan_warps(N), 6) k_fwd_fsum(FwdArgs a, F
                 sDU[buf][r][(cg + c) / 2] = make_float4(dl.x, dl.y, dlu.x, dlu.y);
             }
         }
-        // the tile's B rows as f32 (zero past t_end)
+        // the tile's B rows as f32 (zero past t_end): widened from the TMA box, or
+        // loaded; f32 rows that TMA brought in are read where they landed
+        if (!DIRECT || !tma) {
 #pragma unroll
-        for (int v = 0; v < C::ROWS; v++) {
-            const int id = tid + v * THREADS;
-            const int r = id / N, n = id % N;
-            const int64_t t = t0 + r;
-            float bv = 0.f;
-            if (t < t_end) {
-                if (tma) bv = (float)sBr[buf][r][n];
-                else bv = (float)Bm[(b * L + t) * N + n];
+            for (int v = 0; v < C::ROWS; v++) {
+                const int id = tid + v * THREADS;
+                const int r = id / N, n = id % N;
+                const int64_t t = t0 + r;
+                float bv = 0.f;
+                if (t < t_end) {
+                    if (tma) bv = (float)sBr[buf][r][n];
+                    else bv = (float)Bm[(b * L + t) * N + n];
+                }
+                if constexpr (DIRECT) sBr[buf][r][n] = bv;
+                else sB[buf][r][n] = bv;
             }
-            sB[buf][r][n] = bv;
         }
         // A thread whose wait for the tile ran out makes the block give up (the
         // block agrees here): the status word records it, and the thread that
@@ -200,7 +210,8 @@ __global__ void __launch_bounds__(32 * scan_warps(N), 6) k_fwd_fsum(FwdArgs a, F
             const float4 du = sDU[buf][i][pp];
             const float2 dl2 = make_float2(du.x, du.y), dlu2 = make_float2(du.z, du.w);
             float Bv[S];
-            ld_f32<S>(&sB[buf][i][n0], Bv);
+            if constexpr (DIRECT) ld_f32<S>(reinterpret_cast<const float*>(&sBr[buf][i][n0]), Bv);
+            else ld_f32<S>(&sB[buf][i][n0], Bv);
 #pragma unroll
             for (int s = 0; s < S; s++) {
                 const float2 x = mul2(dl2, A2[s]);

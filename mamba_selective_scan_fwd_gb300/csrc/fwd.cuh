@@ -534,12 +534,10 @@ namespace ss {
 // The chunk summaries of every chunked segment, then each segment's main pass.
 // A summary launch of more blocks than one round of the main kernel's
 // residency (4 two-warp blocks per SM) runs the dedicated k_fwd_fsum, built
-// for 6 resident blocks per SM so that it still takes one wave (16-bit io:
-// 33 KB of shared memory per block; the f32 version's 43 KB allow only 5).
-// Otherwise the summary mode of k_fwd, which is about 3 % faster per step on
-// long chunks (measured: the Mamba-130M bf16 forward's 768-block summaries
-// 0.096 -> 0.076 ms with k_fwd_fsum; the long sequence's 576 blocks 0.509 ->
-// 0.522 ms, the f32 130M workload's 768 blocks 0.096 -> 0.103 ms).
+// for 6 resident blocks per SM so that it still takes one wave.  Otherwise the
+// summary mode of k_fwd, which is about 3 % faster per step on long chunks
+// (measured: the Mamba-130M bf16 forward's 768-block summaries 0.096 -> 0.076
+// ms with k_fwd_fsum; the long sequence's 576 blocks 0.509 -> 0.522 ms).
 template <typename T, int N>
 cudaError_t launch_fwd_t(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mode, float* ckpt,
                          const TmaMaps& maps) {
@@ -547,7 +545,7 @@ cudaError_t launch_fwd_t(const FwdArgs& a, const FPlan& p, cudaStream_t st, int 
         const int64_t K = p.seg[si].K;
         if (K < 2) continue;
         const int64_t blocks = p.seg[si].nu * (K - 1);
-        if constexpr (scan_warps(N) == 2 && sizeof(T) == 2) {
+        if constexpr (scan_warps(N) == 2) {
             if (blocks > round_blocks(N)) {
                 prof_mark(st);
                 k_fwd_fsum<T, N><<<(unsigned)blocks, FSCfg<T, N>::THREADS, 0, st>>>(a, p, si, 0, maps);

@@ -119,7 +119,7 @@ def test_split_plan_parity_one_warp_blocks(orc):
 # 384 units (6 batch rows x 64 channel tiles) hold fewer than 8 warps per SM:
 # every unit is cut into 3 chunks, and the 768 forward summaries (chunks 0, 1)
 # are more blocks than one round of the main kernel, which takes the dedicated
-# summary kernel for 16-bit io (f32 io keeps the summary mode of k_fwd)
+# summary kernel
 WIDE = (6, 320, 2048, 16)
 
 

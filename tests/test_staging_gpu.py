@@ -51,6 +51,7 @@ def _all_outputs(t):
     ((1, 4100, 8, 4), "f32", True),       # few units: the sequence is cut into chunks
     ((2, 300, 9920, 16), "bf16", True),   # split plan: 608 one-chunk units, then a chunked segment
     ((6, 320, 2048, 16), "bf16", True),   # 384 units x 3 chunks: 768 forward summaries (their own kernel)
+    ((6, 320, 2048, 16), "f32", True),    # the same with f32 rows read where TMA put them
 ])
 def test_tma_and_copies_stage_identical_tiles(shape, io, gate):
     Bsz, L, Dch, N = shape
