@@ -12,7 +12,10 @@ from gpu_util import TOL, normwise, ref_y, to_device
 
 pytestmark = pytest.mark.gpu
 
-SHAPES = [(3, 70, 16), (2, 5, 32), (4, 33, 8), (1, 9, 4), (2, 7, 2), (3, 11, 1), (8, 1536, 16)]
+# N = 16 with at least 256 channels runs the channel-major kernel (blocks of 256
+# channels x 16 batch rows): (8, 1536, 16) and (37, 300, 16), the latter with a
+# ragged channel block and a ragged block of rows
+SHAPES = [(3, 70, 16), (2, 5, 32), (4, 33, 8), (1, 9, 4), (2, 7, 2), (3, 11, 1), (8, 1536, 16), (37, 300, 16)]
 
 
 @pytest.mark.parametrize("a_is_log", [False, True])
@@ -37,9 +40,11 @@ def test_decode_step_parity(orc, shape, io, a_is_log):
     assert normwise(state, r.last_state) <= tol
 
 
-def test_decode_steps_continue_a_sequence():
-    """k decoding steps from h0 give the forward of the k-step sequence from h0."""
-    Bsz, L, Dch, N = 2, 12, 40, 16
+@pytest.mark.parametrize("Dch", [40, 272])
+def test_decode_steps_continue_a_sequence(Dch):
+    """k decoding steps from h0 give the forward of the k-step sequence from h0
+    (both decode kernels: 40 channels row-major, 272 channel-major)."""
+    Bsz, L, N = 2, 12, 16
     x = small_inputs(Bsz, L, Dch, N, io="f32", seed=4200)
     t = to_device(x, "f32")
     h0 = torch.randn((Bsz, Dch, N), device="cuda")
