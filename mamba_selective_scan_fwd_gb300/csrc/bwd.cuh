@@ -91,6 +91,12 @@ struct BCfg {
     static constexpr bool BC_DIRECT = ESZ == 4;
     static constexpr bool BC_RAW = !BC_DIRECT && !BC_PK && NB >= 4;
     static constexpr int BC_BUFS = BC_DIRECT ? 2 : 1;
+    // u and the softplus derivative of a thread's prologue items stay in its
+    // registers for its epilogue items (the same items) when they are few; else
+    // the prologue stages them in shared memory
+    static constexpr bool KEEP = ITEMS * (RWH + GRP) <= 8;
+    // likewise delta_eff and g (which the walk reads from shared memory)
+    static constexpr bool KEEP2 = KEEP && ITEMS * GRP <= 4;
     static constexpr int EP = CH + 4;               // padded per-channel rows (floats)
     // plane of per-step channel sums of one lane of a pair: kTT rows of EP floats,
     // planes 16 mod 32 floats apart so that the 8-byte stores of the lanes of
@@ -208,7 +214,8 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
     __shared__ float4 sDU[kTT][PAIRS + 1];  // (Delta of both channels, Delta*u of both channels)
     __shared__ float2 sG[kTT][PAIRS + 2];   // g of both channels
     // (u of both channels, sig(delta + bias) of both channels), for the epilogue
-    __shared__ float4 sUS[MAIN ? kTT : 1][MAIN ? PAIRS + 1 : 1];
+    // when they do not stay in registers
+    __shared__ float4 sUS[MAIN && !C::KEEP ? kTT : 1][MAIN && !C::KEEP ? PAIRS + 1 : 1];
     // B / C rows as f32 (B then C); with f32 io double buffered, the next tile's
     // rows being copied in while the current tile is walked
     __shared__ __align__(128) float sBC[2][C::BC_BUFS][C::BC_PK ? 1 : kTT][C::BC_PK ? 4 : N];
@@ -321,6 +328,10 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
     float accD[ITEMS * GRP], accB[ITEMS * GRP];
 #pragma unroll
     for (int c = 0; c < ITEMS * GRP; c++) accD[c] = accB[c] = 0.f;
+    // the raw run of u and the softplus derivatives of the thread's items, from
+    // its prologue to its epilogue (when they stay in registers)
+    uint32_t kU[C::KEEP ? ITEMS : 1][RWH];
+    float kS[C::KEEP ? ITEMS : 1][GRP], kDl[C::KEEP2 ? ITEMS : 1][GRP], kG[C::KEEP2 ? ITEMS : 1][GRP];
 
     // TMA boxes land on 128-byte aligned shared memory; a block whose buffers are
     // not (never expected) records it and stages with asynchronous copies instead
@@ -460,6 +471,8 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
             float vy0[GRP];
 #pragma unroll
             for (int c = 0; c < GRP; c++) vy0[c] = 0.f;
+#pragma unroll
+            for (int v = 0; v < RWH; v++) ru[v] = 0u;
             if (rv) {
                 if (pfast) {
                     lds_words<GRP * C::ESZ, RWH>(&sRaw[0][r][cg], rd);
@@ -511,7 +524,18 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
                 sDU[r][pr] = make_float4(dl2.x, dl2.y, dlu2.x, dlu2.y);
                 sG[r][pr] = gg2;
                 if (MAIN) {
-                    sUS[r][pr] = make_float4(uu2.x, uu2.y, sg2.x, sg2.y);
+                    if constexpr (C::KEEP2) {
+                        kDl[it][c] = dl2.x;
+                        kDl[it][c + 1] = dl2.y;
+                        kG[it][c] = gg2.x;
+                        kG[it][c + 1] = gg2.y;
+                    }
+                    if constexpr (C::KEEP) {
+                        kS[it][c] = sg2.x;
+                        kS[it][c + 1] = sg2.y;
+                    } else {
+                        sUS[r][pr] = make_float4(uu2.x, uu2.y, sg2.x, sg2.y);
+                    }
                     accD[it * GRP + c] = fmaf(gg2.x, uu2.x, accD[it * GRP + c]);  // g = u = 0 past t_end
                     accD[it * GRP + c + 1] = fmaf(gg2.y, uu2.y, accD[it * GRP + c + 1]);
                 }
@@ -519,6 +543,10 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
             }
             if (MAIN) {
                 if (z && rv) store_run<GRP>(a.dz + (b * L + t) * Dch + d0 + cg, vdz, d0 + cg, Dch, ofast);
+            }
+            if constexpr (MAIN && C::KEEP) {
+#pragma unroll
+                for (int v = 0; v < RWH; v++) kU[it][v] = ru[v];
             }
         }
         if constexpr (!C::BC_DIRECT && !C::BC_PK) {
@@ -757,10 +785,21 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
                     // two channels at a time with packed arithmetic; the item's per-(t, d)
                     // terms as its prologue staged them
                     const int pr = (cg + c) / 2;
-                    const float4 dlu = sDU[r][pr], us = sUS[r][pr];
+                    float2 dl2, gg2;
+                    if constexpr (C::KEEP2) {
+                        dl2 = make_float2(kDl[it][c], kDl[it][c + 1]);
+                        gg2 = make_float2(kG[it][c], kG[it][c + 1]);
+                    } else {
+                        const float4 dlu = sDU[r][pr];
+                        dl2 = make_float2(dlu.x, dlu.y);
+                        gg2 = sG[r][pr];
+                    }
+                    float4 us;
+                    if constexpr (C::KEEP) us = make_float4(elem<T>(kU[it], c), elem<T>(kU[it], c + 1), kS[it][c], kS[it][c + 1]);
+                    else us = sUS[r][pr];
                     const float2 Dv = make_float2(sDv[cg + c], sDv[cg + c + 1]);
                     const float2 su2 = make_float2(su[c], su[c + 1]);
-                    const float2 du2 = fma2(sG[r][pr], Dv, mul2(make_float2(dlu.x, dlu.y), su2));
+                    const float2 du2 = fma2(gg2, Dv, mul2(dl2, su2));
                     const float2 dx2 = mul2(fma2(make_float2(us.x, us.y), su2,
                                                  mul2(make_float2(sdv[c], sdv[c + 1]), splat2(kLn2))),
                                             make_float2(us.z, us.w));

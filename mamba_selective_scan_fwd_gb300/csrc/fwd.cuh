@@ -20,16 +20,21 @@
 // 8-byte store of both channels.
 // Work per 32-step tile:
 //   prologue  threads take (step, 8-channel group) items: the group's runs
-//             of delta, u, z (copied in with the previous tile), delta_eff,
-//             delta_eff * u, the gate and D * u of each channel pair into
-//             shared memory; the B / C rows of the tile become f32 rows;
+//             of delta, u, z (copied in with the previous tile), delta_eff
+//             and delta_eff * u of each channel pair into shared memory; the
+//             runs of u and z stay in the thread's registers for its
+//             epilogue items (the same items); the B / C rows of the tile
+//             become f32 rows;
 //   scan      each lane walks the 32 steps for its 2 x S states, storing the
 //             state entering every kSub-th step when the states are kept
 //             for the backward;
 //   epilogue  the (step, 8-channel group) items add the lanes' and warps'
 //             partial readouts and D * u (the pre-gate readout y0, stored
 //             as f32 for the backward's dz when the states are kept and z
-//             is given), apply the gate and store the group's run of y.
+//             is given), apply the gate z sigmoid(z) and store the group's
+//             run of y.  (Forming D * u and the gate here rather than in the
+//             prologue keeps them out of shared memory: the tile's shared-
+//             memory data pipe is the forward's busiest unit.)
 // Modes: Y (y, last_state), YSave (also the states entering every kSub-th
 // step and y0), Ckpt (the backward's checkpoint pass: the states and y0, no
 // gate and no y), Summary (a chunk's end state and sum of delta_eff, no
@@ -70,12 +75,17 @@ struct FCfg {
     // f32 B / C staging, one dense [step][N] array per tensor (the layout a TMA
     // box lands in).  f32 io is copied straight into it (double buffered);
     // 16-bit rows are copied raw and converted once.  (Unlike the backward, the
-    // forward keeps no packed bf16 rows: it is bound by latency, not by the
-    // shared-memory data pipe, and widening them in the scan sits on the path
-    // to the decays.)
+    // forward keeps no packed bf16 rows: widening them in the scan sits on the
+    // path to the decays, and measured slower -- 0.476 -> 0.553 ms for the
+    // Mamba-2.8B layer's main pass -- although it halves the scan's B / C
+    // shared-memory wavefronts.)
     static constexpr bool BC_DIRECT = ESZ == 4;
     static constexpr bool BC_RAW = !BC_DIRECT && NB >= 4;
     static constexpr int BC_BUFS = BC_DIRECT ? 2 : 1;
+    // the raw u / z runs of a thread's items stay in registers from its prologue
+    // to its epilogue when they are few (else the prologue stages the gate and
+    // D * u in shared memory)
+    static constexpr bool KEEP = ITEMS * RW <= 16;
     static constexpr int YP = CH + 4;               // padded row of partial readouts (floats)
     // plane of one lane of a pair's partial readouts: kRow rows of YP floats,
     // planes 16 mod 32 floats apart so that the 8-byte stores of the lanes of
@@ -100,8 +110,9 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
     // per-(t, d) staging of the scan, one float4 per channel pair:
     // (delta_eff of both channels, delta_eff * u of both channels)
     __shared__ float4 sDU[kRow][PAIRS + 1];
-    // (gate of both channels, D * u of both channels), read by the epilogue
-    __shared__ float4 sGD[NOY ? 1 : kRow][NOY ? 1 : PAIRS + 1];
+    // (gate of both channels, D * u of both channels) for the epilogue, when the
+    // raw runs do not stay in registers
+    __shared__ float4 sGD[NOY || C::KEEP ? 1 : kRow][NOY || C::KEEP ? 1 : PAIRS + 1];
     // B / C rows as f32 [tensor][buffer][step][N]; with f32 io double buffered,
     // the next tile's rows being copied in while the scan reads the current one's
     __shared__ __align__(128) float sBC[2][C::BC_BUFS][kRow][N];
@@ -267,6 +278,11 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
     };
     issue(t_begin, 0);
     __syncthreads();  // sBias / sDv, the barriers
+    // raw runs of u and z of the thread's prologue items, kept in registers for
+    // its epilogue items (the same (step, group) items), which form D * u and
+    // the gate from them
+    constexpr bool KEEP = C::KEEP;
+    uint32_t kU[NOY || !KEEP ? 1 : ITEMS][RW], kZ[GATE && KEEP ? ITEMS : 1][RW];
 
     for (int64_t t0 = t_begin; t0 < t_end; t0 += kRow) {
         const int64_t jt = (t0 - t_begin) / kRow;  // tile index within the chunk
@@ -285,6 +301,8 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
             const bool rv = t < t_end;
             const int cg = q * GRP;  // first channel of the group
             uint32_t rd[RW], ru[RW], rz[RW];
+#pragma unroll
+            for (int v = 0; v < RW; v++) rz[v] = 0u;
             if (rv) {
                 if (fast) {
                     lds_words<GRP * C::ESZ, RW>(&sRaw[0][r][cg], rd);
@@ -300,22 +318,31 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
 #pragma unroll
             for (int c = 0; c < GRP; c += 2) {
                 // two channels at a time with packed arithmetic
-                float2 dl = make_float2(0.f, 0.f), dlu = dl, gt = make_float2(1.f, 1.f), dun = dl;
+                float2 dl = make_float2(0.f, 0.f), dlu = dl;
                 if (rv) {
                     const float2 x = make_float2(elem<T>(rd, c) + sBias[cg + c], elem<T>(rd, c + 1) + sBias[cg + c + 1]);
                     dl = a.softplus ? softplus2(x) : x;
                     const float2 uu = make_float2(elem<T>(ru, c), elem<T>(ru, c + 1));
                     dlu = mul2(dl, uu);
-                    if (!NOY) {
+                    if constexpr (!NOY && !KEEP) {
+                        float2 gt = make_float2(1.f, 1.f);
                         if (GATE && z) {
                             const float2 zz = make_float2(elem<T>(rz, c), elem<T>(rz, c + 1));
                             gt = mul2(zz, sigmoid2(zz));
                         }
-                        dun = mul2(make_float2(sDv[cg + c], sDv[cg + c + 1]), uu);
+                        const float2 dun = mul2(make_float2(sDv[cg + c], sDv[cg + c + 1]), uu);
+                        sGD[r][(cg + c) / 2] = make_float4(gt.x, gt.y, dun.x, dun.y);
                     }
                 }
                 sDU[r][(cg + c) / 2] = make_float4(dl.x, dl.y, dlu.x, dlu.y);
-                if (!NOY) sGD[r][(cg + c) / 2] = make_float4(gt.x, gt.y, dun.x, dun.y);
+            }
+            if constexpr (!NOY && KEEP) {
+#pragma unroll
+                for (int v = 0; v < RW; v++) kU[it][v] = ru[v];
+            }
+            if constexpr (GATE && KEEP) {
+#pragma unroll
+                for (int v = 0; v < RW; v++) kZ[it][v] = rz[v];
             }
         }
         if constexpr (!C::BC_DIRECT) {
@@ -444,15 +471,29 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
                             }
                         }
                         // the pre-gate readout y0 = sum_n h C + D u, then the gate
-                        const float4 g01 = sGD[r][(cg + c) / 2], g23 = sGD[r][(cg + c) / 2 + 1];
-                        y0v[c] = acc.x + g01.z;
-                        y0v[c + 1] = acc.y + g01.w;
-                        y0v[c + 2] = acc.z + g23.z;
-                        y0v[c + 3] = acc.w + g23.w;
-                        yv[c] = y0v[c] * g01.x;
-                        yv[c + 1] = y0v[c + 1] * g01.y;
-                        yv[c + 2] = y0v[c + 2] * g23.x;
-                        yv[c + 3] = y0v[c + 3] * g23.y;
+                        const float sum4[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+                        for (int e = 0; e < 4; e += 2) {
+                            const int cc = c + e;
+                            float2 y0, gt = make_float2(1.f, 1.f);
+                            if constexpr (KEEP) {
+                                const float2 uu = make_float2(elem<T>(kU[it], cc), elem<T>(kU[it], cc + 1));
+                                y0 = fma2(make_float2(sDv[cg + cc], sDv[cg + cc + 1]), uu,
+                                          make_float2(sum4[e], sum4[e + 1]));
+                                if (GATE && z) {
+                                    const float2 zz = make_float2(elem<T>(kZ[it], cc), elem<T>(kZ[it], cc + 1));
+                                    gt = mul2(zz, sigmoid2(zz));
+                                }
+                            } else {
+                                const float4 gd = sGD[r][(cg + cc) / 2];
+                                y0 = add2(make_float2(sum4[e], sum4[e + 1]), make_float2(gd.z, gd.w));
+                                gt = make_float2(gd.x, gd.y);
+                            }
+                            y0v[cc] = y0.x;
+                            y0v[cc + 1] = y0.y;
+                            yv[cc] = y0.x * gt.x;
+                            yv[cc + 1] = y0.y * gt.y;
+                        }
                     }
                     const int64_t off = (b * L + t) * Dch + d0 + cg;
                     if (a.y0 && z) {
