@@ -77,7 +77,6 @@ struct BCfg {
     static constexpr int ITEMS = kTT * NGRP / THREADS;  // items per thread per tile
     static constexpr int RWH = GRP * ESZ >= 4 ? GRP * ESZ / 4 : 1;  // 32-bit words of an item's run
     static constexpr int NB = N * ESZ;
-    static constexpr int NWd = NB >= 4 ? NB / 4 : 1;
     // B / C staging: a step's row is B (N values) then C.  The lanes load S of
     // each per step as broadcasts, and the shared-memory data pipe -- which
     // bounds this kernel -- returns one 32-bit word per lane per cycle however
@@ -91,6 +90,10 @@ struct BCfg {
     static constexpr bool BC_DIRECT = ESZ == 4;
     static constexpr bool BC_RAW = !BC_DIRECT && !BC_PK && NB >= 4;
     static constexpr int BC_BUFS = BC_DIRECT ? 2 : 1;
+    // f16 rows are copied and converted in units of BCV values of one row,
+    // consecutive threads taking consecutive units (free of bank conflicts)
+    static constexpr int BCV = N >= 4 ? 4 : N;
+    static constexpr int BCU = N / BCV;             // units per row
     // u and the softplus derivative of a thread's prologue items stay in its
     // registers for its epilogue items (the same items) when they are few; else
     // the prologue stages them in shared memory
@@ -104,9 +107,11 @@ struct BCfg {
     static constexpr int OPL = kTT * EP + 16;
     // dB / dC staging of one warp: block (step j, tensor tau) holds PAIRS rows
     // of NPW floats (the warp's states, summed over the pair's two channels),
-    // padded by 4 floats so that the 16-byte reads of a warp (32 (step, tensor,
-    // state quad) units of one pair) spread over all banks
-    static constexpr int BLK = PAIRS * NPW + 4;
+    // padded to a stride of NPW floats mod 32: the reads of reduce_staged (lane
+    // = (block, run of states), one pair's row at a time) then cover the 32
+    // banks exactly once per wavefront of lanes (8 lanes of 16-byte reads)
+    static constexpr int BLK = PAIRS * NPW + ((NPW - PAIRS * NPW) % 32 + 32) % 32;
+    static_assert(BLK % 32 == NPW % 32, "staging stride");
     // blocks per SM the register budget must allow: one round of the plan on
     // every SM (8 warps: 4 two-warp or 8 one-warp blocks), which leaves the
     // walk up to 255 registers
@@ -209,7 +214,7 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
     constexpr bool MAIN = MODE == kRevMain;
     constexpr int NW = C::NW, NPW = C::NPW, S = C::S, SP = C::SP, G = C::G, PAIRS = C::PAIRS, CH = C::CH,
                   THREADS = C::THREADS, GRP = C::GRP, NGRP = C::NGRP, ITEMS = C::ITEMS, RWH = C::RWH,
-                  NWd = C::NWd, EP = C::EP, BLK = C::BLK;
+                  EP = C::EP, BLK = C::BLK;
     // per-(t, d) staging of the walk, one entry per channel pair
     __shared__ float4 sDU[kTT][PAIRS + 1];  // (Delta of both channels, Delta*u of both channels)
     __shared__ float2 sG[kTT][PAIRS + 2];   // g of both channels
@@ -353,7 +358,7 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
     // (slot, batch, channel tile), the lane's 2 S floats at its slot
     const int64_t ck_stride = f.Bsz * p.tiles_b * CH * N;
     const float* ck_lane =
-        a.ws_ckpt + (t_begin / kSub) * ck_stride + (b * p.tiles_b + tile) * (CH * N) + ckpt_slot(w, lane, S);
+        a.ws_ckpt + (t_begin / kSub) * ck_stride + (b * p.tiles_b + tile) * (CH * N) + ckpt_slot(w, lane, S, 0);
     float* bc0 = a.ws_bc + ((int64_t)tile * f.Bsz + b) * L * N;                  // dB partials of this tile
     float* bc1 = a.ws_bc + ((int64_t)(p.tiles_b + tile) * f.Bsz + b) * L * N;    // dC partials
     float* sRw = &sR[MAIN ? w : 0][0];
@@ -365,7 +370,7 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
     // on the buffer's barrier.  Otherwise, one commit group of asynchronous
     // copies: the thread's item runs and y0 runs (when the tile's rows are whole
     // aligned vectors), the B / C rows, and the lane's state entering the tile
-    // into its own slot of sH; each thread converts the runs it copied and the
+    // into its own slots of sH; each thread converts the runs it copied and the
     // state is read by the lane that copied it.
     const TmaMaps& mp = maps;
     auto issue = [&](int64_t mm) {
@@ -392,7 +397,7 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
                     tma_load_3d(dst, &mp.m[half ? kMapC : kMapB], 0, y, zc, &sBar[buf]);
                 }
                 if (MAIN) {
-                    const float* blk = ck_lane - ckpt_slot(w, lane, S) + (tt - t_begin) / kSub * ck_stride;
+                    const float* blk = ck_lane - ckpt_slot(w, lane, S, 0) + (tt - t_begin) / kSub * ck_stride;
                     bulk_load(&sH[buf][0], blk, state, &sBar[buf]);
                 }
             }
@@ -434,11 +439,24 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
 #pragma unroll
                     for (int n = 0; n < N; n++) dst[n] = 0.f;
                 }
-            } else if constexpr (C::BC_RAW) {
-                if (t < t_end) cp_async_bytes<N * C::ESZ>(&sBCraw[half][r][0], src);
             }
         }
-        if (MAIN) cp_async_bytes<2 * S * 4>(&sH[buf][tid * 2 * S], ck_lane + (tt - t_begin) / kSub * ck_stride);
+        if constexpr (C::BC_RAW) {
+            // in the prologue's conversion units
+            for (int id = tid; id < (MAIN ? 2 : 1) * kTT * C::BCU; id += THREADS) {
+                const int row = id / C::BCU, n = (id % C::BCU) * C::BCV;
+                const int half = MAIN ? row / kTT : 1, r = row % kTT;
+                const int64_t t = tt + r;
+                if (t < t_end) cp_async_bytes<C::BCV * C::ESZ>(&sBCraw[half][r][n], (half ? Cm : Bm) + (b * L + t) * N + n);
+            }
+        }
+        if (MAIN) {
+            // the block's layout: the lane's S states of each channel at its two slots
+            const float* src = ck_lane + (tt - t_begin) / kSub * ck_stride;
+            float* dst = &sH[buf][ckpt_slot(w, lane, S, 0)];
+            cp_async_bytes<S * 4>(dst, src);
+            cp_async_bytes<S * 4>(dst + 32 * S, src + 32 * S);
+        }
         cp_async_commit();
     };
     if (tma && tid == 0) {
@@ -551,18 +569,21 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
         }
         if constexpr (!C::BC_DIRECT && !C::BC_PK) {
             // 16-bit B / C rows of the tile's steps (the reverse summary needs only C),
-            // converted by the thread that copied them (or loaded here when too short to copy)
-            for (int id = tid; id < (MAIN ? 2 : 1) * kTT; id += THREADS) {
-                const int half = MAIN ? id / kTT : 1, r = id % kTT;
+            // in units of BCV values of one row, converted by the thread that copied
+            // them (or loaded here when too short to copy)
+            constexpr int BCV = C::BCV, BCU = C::BCU, VW = BCV * C::ESZ >= 4 ? BCV * C::ESZ / 4 : 1;
+            for (int id = tid; id < (MAIN ? 2 : 1) * kTT * BCU; id += THREADS) {
+                const int row = id / BCU, n = (id % BCU) * BCV;
+                const int half = MAIN ? row / kTT : 1, r = row % kTT;
                 const int64_t t = t0 + r;
-                uint32_t wv[NWd];
+                uint32_t wv[VW];
                 if (t < t_end) {
-                    if constexpr (C::BC_RAW) lds_words<C::NB, NWd>(&sBCraw[half][r][0], wv);
-                    else load_words<C::NB, NWd>((half ? Cm : Bm) + (b * L + t) * N, wv);
+                    if constexpr (C::BC_RAW) lds_words<BCV * C::ESZ, VW>(&sBCraw[half][r][n], wv);
+                    else load_words<BCV * C::ESZ, VW>((half ? Cm : Bm) + (b * L + t) * N + n, wv);
                 }
-                float* dst = &sBC[half][0][r][0];
+                float* dst = &sBC[half][0][r][n];
 #pragma unroll
-                for (int n = 0; n < N; n++) dst[n] = t < t_end ? elem<T>(wv, n) : 0.f;
+                for (int v = 0; v < BCV; v++) dst[v] = t < t_end ? elem<T>(wv, v) : 0.f;
             }
         }
         // Staging complete; every thread is done reading sRaw / sY0 / sBCraw.  A
@@ -614,13 +635,13 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
             // (last tile only) hold Delta = g = 0 and B = C = 0 in the staging: they
             // leave the state and the adjoint unchanged and add nothing; only their
             // per-step stores are skipped.
-            // the state entering the tile (the lane's copy in sH), as state pairs
-            const float* hsrc = &sH[buf][tid * 2 * S];
+            // the state entering the tile (the lane's slots in sH), as state pairs
+            const float* hsrc = &sH[buf][ckpt_slot(w, lane, S, 0)];
             auto load_hs = [&](float2 (&hs)[2][SP]) {
 #pragma unroll
                 for (int e = 0; e < 2; e++) {
                     float v[S];
-                    ld_f32<S>(hsrc + e * S, v);
+                    ld_f32<S>(hsrc + e * 32 * S, v);  // ckpt_slot(w, lane, S, e)
 #pragma unroll
                     for (int j = 0; j < SP; j++) hs[e][j] = make_float2(v[2 * j], S >= 2 ? v[2 * j + 1] : 0.f);
                 }

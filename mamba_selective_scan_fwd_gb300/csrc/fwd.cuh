@@ -71,7 +71,6 @@ struct FCfg {
     static constexpr int ITEMS = kRow * NGRP / THREADS;  // items per thread per tile
     static constexpr int RW = GRP * ESZ / 4;        // 32-bit words of an item's run of one tensor
     static constexpr int NB = N * ESZ;              // bytes of a B / C row
-    static constexpr int NWd = NB >= 4 ? NB / 4 : 1;  // 32-bit words per B / C row
     // f32 B / C staging, one dense [step][N] array per tensor (the layout a TMA
     // box lands in).  f32 io is copied straight into it (double buffered);
     // 16-bit rows are copied raw and converted once.  (Unlike the backward, the
@@ -82,6 +81,10 @@ struct FCfg {
     static constexpr bool BC_DIRECT = ESZ == 4;
     static constexpr bool BC_RAW = !BC_DIRECT && NB >= 4;
     static constexpr int BC_BUFS = BC_DIRECT ? 2 : 1;
+    // 16-bit rows are copied and converted in units of BCV values of one row,
+    // consecutive threads taking consecutive units (free of bank conflicts)
+    static constexpr int BCV = N >= 4 ? 4 : N;
+    static constexpr int BCU = N / BCV;             // units per row
     // the raw u / z runs of a thread's items stay in registers from its prologue
     // to its epilogue when they are few (else the prologue stages the gate and
     // D * u in shared memory)
@@ -106,7 +109,7 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
     using C = FCfg<T, N>;
     constexpr int NW = C::NW, NPW = C::NPW, S = C::S, G = C::G, PAIRS = C::PAIRS, CH = C::CH,
                   THREADS = C::THREADS, GRP = C::GRP, NGRP = C::NGRP, ITEMS = C::ITEMS, RW = C::RW,
-                  NWd = C::NWd, YP = C::YP;
+                  YP = C::YP;
     // per-(t, d) staging of the scan, one float4 per channel pair:
     // (delta_eff of both channels, delta_eff * u of both channels)
     __shared__ float4 sDU[kRow][PAIRS + 1];
@@ -216,7 +219,7 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
     // (slot t / kSub, batch, channel tile), the lane's 2 S floats at its slot
     const int64_t ck_stride = a.Bsz * ntiles * CH * N;
     float* ck_lane =
-        SAVE ? ckpt + (t_begin / kSub) * ck_stride + (b * ntiles + tile) * (CH * N) + ckpt_slot(w, lane, S) : nullptr;
+        SAVE ? ckpt + (t_begin / kSub) * ck_stride + (b * ntiles + tile) * (CH * N) + ckpt_slot(w, lane, S, 0) : nullptr;
 
     // Copies of the tile starting at tt into buffer buf.  With TMA: one thread
     // issues a box per tensor (delta, u, z as [kRow][CH], B and C as
@@ -258,20 +261,25 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
                 }
             }
         }
-        for (int id = tid; id < (NOY ? 1 : 2) * kRow; id += THREADS) {
-            const int half = id / kRow, r = id % kRow;
-            const int64_t t = tt + r;
-            const T* src = (half ? Cm : Bm) + (b * L + (t < t_end ? t : 0)) * N;
-            if constexpr (C::BC_DIRECT) {
+        if constexpr (C::BC_DIRECT) {
+            for (int id = tid; id < (NOY ? 1 : 2) * kRow; id += THREADS) {
+                const int half = id / kRow, r = id % kRow;
+                const int64_t t = tt + r;
                 float* dst = &sBC[half][buf][r][0];
                 if (t < t_end) {
-                    cp_async_bytes<N * 4>(dst, src);
+                    cp_async_bytes<N * 4>(dst, (half ? Cm : Bm) + (b * L + t) * N);
                 } else {
 #pragma unroll
                     for (int n = 0; n < N; n++) dst[n] = 0.f;
                 }
-            } else if constexpr (C::BC_RAW) {
-                if (t < t_end) cp_async_bytes<N * C::ESZ>(&sBCraw[half][r][0], src);
+            }
+        } else if constexpr (C::BC_RAW) {
+            // in the prologue's conversion units
+            for (int id = tid; id < (NOY ? 1 : 2) * kRow * C::BCU; id += THREADS) {
+                const int row = id / C::BCU, n = (id % C::BCU) * C::BCV;
+                const int half = row / kRow, r = row % kRow;
+                const int64_t t = tt + r;
+                if (t < t_end) cp_async_bytes<C::BCV * C::ESZ>(&sBCraw[half][r][n], (half ? Cm : Bm) + (b * L + t) * N + n);
             }
         }
         cp_async_commit();
@@ -346,19 +354,22 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
             }
         }
         if constexpr (!C::BC_DIRECT) {
-            // 16-bit B / C rows of the tile's steps, row id = (tensor, step), converted
-            // by the thread that copied them (or loaded here when too short to copy)
-            for (int id = tid; id < (NOY ? 1 : 2) * kRow; id += THREADS) {
-                const int half = id / kRow, r = id % kRow;
+            // 16-bit B / C rows of the tile's steps, in units of BCV values of one
+            // row (tensor, step), converted by the thread that copied them (or
+            // loaded here when too short to copy)
+            constexpr int BCV = C::BCV, BCU = C::BCU, VW = BCV * C::ESZ >= 4 ? BCV * C::ESZ / 4 : 1;
+            for (int id = tid; id < (NOY ? 1 : 2) * kRow * BCU; id += THREADS) {
+                const int row = id / BCU, n = (id % BCU) * BCV;
+                const int half = row / kRow, r = row % kRow;
                 const int64_t t = t0 + r;
-                uint32_t wv[NWd];
+                uint32_t wv[VW];
                 if (t < t_end) {
-                    if constexpr (C::BC_RAW) lds_words<C::NB, NWd>(&sBCraw[half][r][0], wv);
-                    else load_words<C::NB, NWd>((half ? Cm : Bm) + (b * L + t) * N, wv);
+                    if constexpr (C::BC_RAW) lds_words<BCV * C::ESZ, VW>(&sBCraw[half][r][n], wv);
+                    else load_words<BCV * C::ESZ, VW>((half ? Cm : Bm) + (b * L + t) * N + n, wv);
                 }
-                float* dst = &sBC[half][0][r][0];
+                float* dst = &sBC[half][0][r][n];
 #pragma unroll
-                for (int n = 0; n < N; n++) dst[n] = t < t_end ? elem<T>(wv, n) : 0.f;
+                for (int v = 0; v < BCV; v++) dst[v] = t < t_end ? elem<T>(wv, v) : 0.f;
             }
         }
         // Staging complete; every thread is done reading sRaw / sBCraw.  A thread
@@ -404,19 +415,20 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
 #pragma unroll
         for (int i = 0; i < kRow; i++) {
             if (SAVE && (i % kSub) == 0) {
-                // the state entering step t0 + i, channel-major (S states of c0, then of c1);
-                // every slot is written: channels past Dch hold a zero state, and the
-                // slots of the last tile past the sequence end (L rounded up to 32)
-                // the final state
+                // the state entering step t0 + i (S states of c0 at the lane's slot of
+                // channel 0, S of c1 at its slot of channel 1); every slot is written:
+                // channels past Dch hold a zero state, and the slots of the last tile
+                // past the sequence end (L rounded up to 32) the final state
                 float* dst = ck_lane + ((t0 - t_begin + i) / kSub) * ck_stride;
+                constexpr int E1 = 32 * S;  // ckpt_slot(w, lane, S, 1) - ckpt_slot(w, lane, S, 0)
                 if constexpr (S == 4) {
                     *reinterpret_cast<float4*>(dst) = make_float4(h[0].x, h[1].x, h[2].x, h[3].x);
-                    *reinterpret_cast<float4*>(dst + 4) = make_float4(h[0].y, h[1].y, h[2].y, h[3].y);
+                    *reinterpret_cast<float4*>(dst + E1) = make_float4(h[0].y, h[1].y, h[2].y, h[3].y);
                 } else {
 #pragma unroll
                     for (int s = 0; s < S; s++) {
                         dst[s] = h[s].x;
-                        dst[S + s] = h[s].y;
+                        dst[E1 + s] = h[s].y;
                     }
                 }
             }

@@ -283,10 +283,12 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
 // the state entering every kSub-th step of every (b, d) row, which the
 // backward recomputes its windows from, then at ckpt_y0_offset the pre-gate
 // readout y0 (f32 [Bsz][L][Dch]).  States layout: [slot t / kSub][b][channel
-// tile][block of CH x N floats]; within a block, lane l of warp w holds 2 S
-// floats at ckpt_slot(w, l, S): S states of its first channel, then S of the
-// second (the scan kernels' lane layout), so that a warp's stores and loads
-// are contiguous.
+// tile][block of CH x N floats]; within a block, lane l of warp w holds S
+// states of its first channel at ckpt_slot(w, l, S, 0) and S of its second
+// at ckpt_slot(w, l, S, 1) (the scan kernels' lane layout): the 32 lanes' runs
+// of one channel of their pair are contiguous, so that a warp's 16-byte
+// stores and loads of them are 512 contiguous bytes (and free of shared-
+// memory bank conflicts once staged).
 inline size_t ckpt_y0_offset(const FPlan& p, int64_t Bsz, int64_t N) {
     return align_up((size_t)Bsz * p.tiles_b * channels_per_block(N) * p.slots * N * sizeof(float), 256);
 }
@@ -294,8 +296,11 @@ inline size_t ckpt_bytes(const FPlan& p, int64_t Bsz, int64_t L, int64_t Dch, in
     return ckpt_y0_offset(p, Bsz, N) + (size_t)Bsz * L * Dch * sizeof(float);
 }
 
-// Float offset of a lane's 2 S saved states within a saved-state block.
-__host__ __device__ constexpr int64_t ckpt_slot(int w, int lane, int S) { return ((int64_t)w * 32 + lane) * 2 * S; }
+// Float offset of lane's S saved states of channel e (0: the first of its
+// pair, 1: the second) within a saved-state block.
+__host__ __device__ constexpr int64_t ckpt_slot(int w, int lane, int S, int e) {
+    return ((int64_t)(2 * w + e) * 32 + lane) * S;
+}
 
 // Bytes of the forward chunk summaries (0 when nothing is chunked): end
 // states [sparts][CH][N], then the sums of delta_eff [sparts][CH] at the
