@@ -65,6 +65,17 @@ def algorithmic_bytes(w):
     return fwd, bwd
 
 
+# FP32 operations (multiplies, adds and fused multiply-adds, one FP32-pipe
+# result each) of one state update (t, d, n), as the method's arithmetic needs
+# them.  Forward: the exponent delta_eff * A, the input term (delta_eff u) * B,
+# the recurrence a h + x and the readout h C.  Backward, recomputing the
+# states from the saved ones as the method prescribes: those first three, then
+# lam = g C + carry, carry' = a lam, sum_n lam B, q = carry' h_prev,
+# sum_n A q, dA += delta_eff q, dB += lam (delta_eff u), dC += g h.
+F32_OPS_FWD = 4
+F32_OPS_BWD = 11
+
+
 def mufu_counts(w):
     """MUFU operations of one call of each direction on workload w (softplus on,
     z given): the scan's ex2 per (t, d, n), which the roofline counts, and all
@@ -383,31 +394,47 @@ def attribute(r, K):
 def analyse(w, plan, ms_per_step, t_fwd, t_bwd, k_fwd, k_bwd, peaks):
     """Rooflines of the step, of its dominant kernel and of the forward's main pass.
 
-    A direction's roofline time is the slower of its algorithmic bytes at the
-    measured HBM copy bandwidth and its B*L*D*N scan exponentials at the
-    measured MUFU ex2 rate (SMs x ex2 per clock per SM x the sampled SM clock)."""
+    A kernel's (or direction's) roofline time is the slowest of three floors:
+    its algorithmic bytes at the measured HBM copy bandwidth, its B*L*D*N
+    scan exponentials at the measured MUFU ex2 rate, and its algorithmic FP32
+    operations (F32_OPS_* per state update) at the measured FP32-pipe rate
+    (SMs x results per clock per SM x the sampled SM clock).  The binding
+    floor names the bound; the others are kept beside it."""
     fwd_bytes, bwd_bytes = algorithmic_bytes(w)
     # the backward's main kernel writes everything but dB / dC and dA / dD / ddelta_bias (the reductions do)
     bwd_main_bytes = bwd_bytes - 2 * w.Bsz * w.L * w.N * 4 - 4 * (w.Dch * w.N + 2 * w.Dch)
     hbm_peak = peaks["hbm_gbs"]
+    clk = f"{peaks['sm_mhz']:g} MHz (median sampled)"
     exp_peak = peaks["sms"] * peaks["ex2_per_clk_per_sm"] * peaks["sm_mhz"] * 1e6  # ex2 / s
+    fma_peak = peaks["sms"] * peaks["fma_per_clk_per_sm"] * peaks["sm_mhz"] * 1e6  # f32 results / s
     exps = w.bld * w.N
 
-    def roof(bytes_, t_ms):
-        t_hbm = bytes_ / (hbm_peak * 1e9)
-        t_sfu = exps / exp_peak
-        if t_hbm >= t_sfu:
-            ach = bytes_ / (t_ms / 1e3) / 1e9
-            return {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
-                    "frac": round(ach / hbm_peak, 4), "peak_kind": f"{peaks['hbm_kind']} HBM copy",
-                    "roofline_ms": round(t_hbm * 1e3, 4), "algorithmic_bytes": bytes_}
-        ach = exps / (t_ms / 1e3) / 1e9
-        pk = exp_peak / 1e9
-        return {"bound": "alu", "achieved": round(ach, 1), "peak": round(pk, 1), "unit": "Gexp2/s",
-                "frac": round(ach / pk, 4),
-                "peak_kind": (f"MUFU ex2 (measured): {peaks['sms']} SMs x {peaks['ex2_per_clk_per_sm']:.2f}/clk x "
-                              f"{peaks['sm_mhz']:g} MHz (median sampled)"),
-                "roofline_ms": round(t_sfu * 1e3, 4), "algorithmic_bytes": bytes_}
+    def roof(bytes_, f32ops, t_ms):
+        floors = {"hbm": bytes_ / (hbm_peak * 1e9), "fp32": f32ops / fma_peak, "mufu": exps / exp_peak}
+        bound = max(floors, key=floors.get)
+        t_s = t_ms / 1e3
+        hbm = {"achieved": round(bytes_ / t_s / 1e9, 1), "peak": hbm_peak, "unit": "GB/s",
+               "frac": round(bytes_ / t_s / 1e9 / hbm_peak, 4)}
+        if bound == "hbm":
+            r = dict(hbm, bound="hbm", peak_kind=f"{peaks['hbm_kind']} HBM copy")
+        elif bound == "fp32":
+            pk = fma_peak / 1e9
+            r = {"bound": "alu", "achieved": round(f32ops / t_s / 1e9, 1), "peak": round(pk, 1), "unit": "Gop/s",
+                 "frac": round(f32ops / t_s / 1e9 / pk, 4),
+                 "peak_kind": (f"FP32 pipe (measured): {peaks['sms']} SMs x {peaks['fma_per_clk_per_sm']:.1f} "
+                               f"f32 results/clk x {clk}"),
+                 "algorithmic_f32_ops": f32ops}
+        else:
+            pk = exp_peak / 1e9
+            r = {"bound": "alu", "achieved": round(exps / t_s / 1e9, 1), "peak": round(pk, 1), "unit": "Gexp2/s",
+                 "frac": round(exps / t_s / 1e9 / pk, 4),
+                 "peak_kind": (f"MUFU ex2 (measured): {peaks['sms']} SMs x {peaks['ex2_per_clk_per_sm']:.2f}/clk x "
+                               f"{clk}")}
+        r.update({"roofline_ms": round(floors[bound] * 1e3, 4), "algorithmic_bytes": bytes_,
+                  "floors_ms": {k: round(v * 1e3, 4) for k, v in floors.items()}})
+        if bound != "hbm":
+            r["hbm"] = hbm
+        return r
 
     # launch order of a call: the summary passes of the chunked segments, then
     # each segment's main pass (then, in the backward, the two reductions)
@@ -422,18 +449,19 @@ def analyse(w, plan, ms_per_step, t_fwd, t_bwd, k_fwd, k_bwd, peaks):
     main = range(n_sum, n_sum + len(segs))  # a direction's main pass: one launch per segment
     t_main_f = sum(k_fwd[j] for j in main)
     launches = f"{len(segs)} launch{'es' if len(segs) > 1 else ''}"
-    r_fwd = roof(fwd_bytes, t_main_f)
+    f32_fwd, f32_bwd = F32_OPS_FWD * exps, F32_OPS_BWD * exps
+    r_fwd = roof(fwd_bytes, f32_fwd, t_main_f)
     r_fwd.update({"kernel": f"k_fwd main pass ({'ss_fwd_save' if w.backward else 'ss_fwd'}; {launches})",
                   "ms": round(t_main_f, 4), "traffic": measured_traffic("k_fwd_y", w)})
     out = {"hbm_gbs": round((fwd_bytes + (bwd_bytes if w.backward else 0)) / (ms_per_step / 1e3) / 1e9, 1),
            "ns_per_element": round(ms_per_step * 1e6 / w.bld, 5)}
-    t_roof = roof(fwd_bytes, t_fwd)["roofline_ms"]
+    t_roof = roof(fwd_bytes, f32_fwd, t_fwd)["roofline_ms"]
     if w.backward:
         t_main_b = sum(k_bwd[j] for j in main)
-        r_bwd = roof(bwd_main_bytes, t_main_b)
+        r_bwd = roof(bwd_main_bytes, f32_bwd, t_main_b)
         r_bwd.update({"kernel": f"k_bwd main pass (ss_bwd_saved; {launches})", "ms": round(t_main_b, 4),
                       "traffic": measured_traffic("k_bwd_main", w)})
-        t_roof += roof(bwd_bytes, t_bwd)["roofline_ms"]
+        t_roof += roof(bwd_bytes, f32_bwd, t_bwd)["roofline_ms"]
         out.update({"roofline": r_bwd, "roofline_fwd": r_fwd})
     else:
         out["roofline"] = r_fwd
@@ -446,13 +474,16 @@ def analyse(w, plan, ms_per_step, t_fwd, t_bwd, k_fwd, k_bwd, peaks):
     return out
 
 
-def measure_ex2_rate():
-    """MUFU ex2 results per clock per SM, measured by the library's probe kernel
-    (the first run warms up; the second is reported)."""
+def measure_unit_rates():
+    """MUFU ex2 and FP32-pipe (f32 FMA) results per clock per SM, measured by
+    the library's probe kernels (the first run of each warms up; the second is
+    reported)."""
     from mamba_selective_scan_fwd_gb300 import binding
 
     binding.measure_ex2_rate(1024)
-    return binding.measure_ex2_rate(4096)
+    ex2 = binding.measure_ex2_rate(4096)
+    binding.measure_fma_rate(1024)
+    return ex2, binding.measure_fma_rate(4096)
 
 
 def run_workload(w, dev, stream, world, K, warmup, peaks, cpu_seconds, rank):
@@ -595,10 +626,10 @@ def run_ours(args):
     del sets, r
     torch.cuda.empty_cache()
 
-    # ---- peaks: the measured HBM copy bandwidth and MUFU ex2 rate
+    # ---- peaks: the measured HBM copy bandwidth, MUFU ex2 rate and FP32-pipe rate
     hbm_peak, peak_kind = load_peaks()
-    ex2 = measure_ex2_rate()
-    peaks = {"hbm_gbs": hbm_peak, "hbm_kind": peak_kind, "ex2_per_clk_per_sm": ex2,
+    ex2, fma = measure_unit_rates()
+    peaks = {"hbm_gbs": hbm_peak, "hbm_kind": peak_kind, "ex2_per_clk_per_sm": ex2, "fma_per_clk_per_sm": fma,
              "sms": torch.cuda.get_device_properties(dev).multi_processor_count,
              "sm_mhz": clk.get("sm_mhz") or 2070.0}
     stats = analyse(w, plan, ms_per_step, t_fwd, t_bwd, k_fwd, k_bwd, peaks)
@@ -612,7 +643,7 @@ def run_ours(args):
     line.update(stats)
     line.update({
         "step_recompute_ms": None if recompute_ms is None else round(recompute_ms, 4),
-        "mufu_ops": mufu_counts(w), "ex2_per_clk_per_sm": round(ex2, 3),
+        "mufu_ops": mufu_counts(w), "ex2_per_clk_per_sm": round(ex2, 3), "fma_per_clk_per_sm": round(fma, 2),
         "clocks": clk,
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "runs": [round(job_throughput(w.bld * e2e_steps, world, v), 1) for v in e2e_runs],

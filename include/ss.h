@@ -374,6 +374,17 @@ int ss_staging_uses_tma(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtyp
  */
 int ss_measure_ex2_rate(int iters, double *per_clk_per_sm);
 
+/* Throughput of the GPU's FP32 pipe: f32 results of fused multiply-adds per
+ * SM clock cycle per SM on the current device, measured like
+ * ss_measure_ex2_rate with eight independent chains of packed f32x2 FMAs per
+ * thread (each two results; the form the scan kernels issue their
+ * multiplies and multiply-adds in).  This is the peak of the scan's FP32
+ * roofline: every f32 multiply, add or multiply-add of a state update takes
+ * one such result slot.  Same arguments, errors and side effects as
+ * ss_measure_ex2_rate.
+ */
+int ss_measure_fma_rate(int iters, double *per_clk_per_sm);
+
 /* Static description of a status code. */
 const char *ss_status_string(int status);
 
@@ -381,8 +392,10 @@ const char *ss_status_string(int status);
  * bwd_saved_kernels; 3: ss_fwd_ex / ss_bwd_ex / ss_decode_step added; 4:
  * ss_plan_segments added, the saved-state buffer sized by L rounded up to 32
  * steps; 5: a saved state every 8 steps, ss_device_status /
- * ss_selftest_wait_timeout / ss_set_copies_only added); bumped on any
- * incompatible change. */
+ * ss_selftest_wait_timeout / ss_set_copies_only added; 6: the saved states
+ * of ss_fwd_save interleaved by channel within a block (a buffer written by
+ * an earlier version is not read correctly), ss_measure_fma_rate added);
+ * bumped on any incompatible change. */
 int ss_abi_version(void);
 
 #ifdef __cplusplus

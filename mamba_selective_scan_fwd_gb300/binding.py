@@ -27,8 +27,9 @@ EXPORTS = ["ss_fwd", "ss_bwd", "ss_fwd_workspace_bytes", "ss_bwd_workspace_bytes
            "ss_status_string", "ss_abi_version", "ss_fwd_noalloc", "ss_saved_bytes", "ss_fwd_save",
            "ss_bwd_saved_workspace_bytes", "ss_bwd_saved", "ss_profile_events", "ss_fwd_ex", "ss_bwd_ex",
            "ss_decode_step", "ss_plan_segments", "ss_device_status", "ss_selftest_wait_timeout",
-           "ss_set_copies_only", "ss_staging_uses_tma", "ss_measure_ex2_rate"]
-ABI_VERSION = 5
+           "ss_set_copies_only", "ss_staging_uses_tma", "ss_measure_ex2_rate",
+           "ss_measure_fma_rate"]
+ABI_VERSION = 6
 
 # Size of the library-owned scratch behind ss_fwd_noalloc (SS_FWD_NOALLOC_MAX_SCRATCH_BYTES).
 FWD_NOALLOC_MAX_SCRATCH_BYTES = 2 << 20
@@ -111,6 +112,8 @@ def lib() -> ctypes.CDLL:
     L.ss_set_copies_only.argtypes = [ctypes.c_int]
     L.ss_measure_ex2_rate.restype = ctypes.c_int
     L.ss_measure_ex2_rate.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_double)]
+    L.ss_measure_fma_rate.restype = ctypes.c_int
+    L.ss_measure_fma_rate.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_double)]
     L.ss_staging_uses_tma.restype = ctypes.c_int
     L.ss_staging_uses_tma.argtypes = [_I64] * 4 + [ctypes.c_int]
     L.ss_decode_step.restype = ctypes.c_int
@@ -260,6 +263,13 @@ def measure_ex2_rate(iters: int = 4096) -> float:
     """MUFU ex2 results per clock cycle per SM on the current device (median over SMs)."""
     r = ctypes.c_double()
     _check("ss_measure_ex2_rate", lib().ss_measure_ex2_rate(int(iters), ctypes.byref(r)))
+    return r.value
+
+
+def measure_fma_rate(iters: int = 4096) -> float:
+    """f32 FMA results (packed f32x2 issue) per clock cycle per SM on the current device (median over SMs)."""
+    r = ctypes.c_double()
+    _check("ss_measure_fma_rate", lib().ss_measure_fma_rate(int(iters), ctypes.byref(r)))
     return r.value
 
 

@@ -318,7 +318,7 @@ int ss_profile_events(void* const* events, int count) {
     return SS_OK;
 }
 
-int ss_abi_version(void) { return 5; }
+int ss_abi_version(void) { return 6; }
 
 int ss_device_status(void* stream) {
     int* status = nullptr;

@@ -217,7 +217,9 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
                   EP = C::EP, BLK = C::BLK;
     // per-(t, d) staging of the walk, one entry per channel pair
     __shared__ float4 sDU[kTT][PAIRS + 1];  // (Delta of both channels, Delta*u of both channels)
-    __shared__ float2 sG[kTT][PAIRS + 2];   // g of both channels
+    // g of both channels (rows of PAIRS + 1 entries: the prologue's 8-byte stores
+    // of two rows, a half-warp, fall on distinct banks)
+    __shared__ float2 sG[kTT][PAIRS + 1];
     // (u of both channels, sig(delta + bias) of both channels), for the epilogue
     // when they do not stay in registers
     __shared__ float4 sUS[MAIN && !C::KEEP ? kTT : 1][MAIN && !C::KEEP ? PAIRS + 1 : 1];
@@ -647,8 +649,8 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
                 }
             };
             float2 hv[kTT][2][SP];  // the states after each step of the window
+            float2 hs[2][SP];       // the state entering it (kept for the walk's last step)
             {
-                float2 hs[2][SP];
                 load_hs(hs);
 #pragma unroll
                 for (int i = 0; i < kTT; i++) {
@@ -713,7 +715,10 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
 #pragma unroll
                         for (int j = 0; j < SP; j++) hp[e][j] = hv[i - 1][e][j];
                 } else {
-                    load_hs(hp);
+#pragma unroll
+                    for (int e = 0; e < 2; e++)
+#pragma unroll
+                        for (int j = 0; j < SP; j++) hp[e][j] = hs[e][j];
                 }
                 float2 cB[SP], cC[SP];
                 float sumB[2], sumQ[2];

@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol():
     lib = ss.lib()
     for name in declared_functions():
         assert hasattr(lib, name), name
-    assert lib.ss_abi_version() == binding.ABI_VERSION == 5
+    assert lib.ss_abi_version() == binding.ABI_VERSION == 6
 
 
 def test_status_strings():
@@ -316,10 +316,13 @@ def test_binding_checks_before_any_launch():
         binding.ss_fwd(u, u, A, Bm, Bm)
 
 
-def test_ex2_probe_checks_arguments_before_any_launch():
+def test_rate_probes_check_arguments_before_any_launch():
     import ctypes
 
     out = ctypes.c_double()
     assert ss.lib().ss_measure_ex2_rate(0, ctypes.byref(out)) == INVALID
     assert ss.lib().ss_measure_ex2_rate(1 << 21, ctypes.byref(out)) == INVALID
     assert ss.lib().ss_measure_ex2_rate(16, None) == INVALID
+    assert ss.lib().ss_measure_fma_rate(0, ctypes.byref(out)) == INVALID
+    assert ss.lib().ss_measure_fma_rate(1 << 21, ctypes.byref(out)) == INVALID
+    assert ss.lib().ss_measure_fma_rate(16, None) == INVALID

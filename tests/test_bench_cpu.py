@@ -84,8 +84,11 @@ def test_reference_arm_reports_the_same_config():
     assert bench.config_of(bench.pick_workload("mamba130m-layer-bf16-fwd"), 1)["step"] == "ss_fwd"
 
 
-def _peaks():
-    return {"hbm_gbs": 7000.0, "hbm_kind": "measured", "ex2_per_clk_per_sm": 32.0, "sms": 152, "sm_mhz": 2000.0}
+def _peaks(**kw):
+    p = {"hbm_gbs": 7000.0, "hbm_kind": "measured", "ex2_per_clk_per_sm": 30.0, "fma_per_clk_per_sm": 128.0,
+         "sms": 152, "sm_mhz": 2000.0}
+    p.update(kw)
+    return p
 
 
 def test_analyse_rooflines_of_a_training_step():
@@ -96,17 +99,30 @@ def test_analyse_rooflines_of_a_training_step():
     k_bwd = [0.06, 0.9, 0.2, 0.05, 0.01]
     out = bench.analyse(w, plan, 2.0, sum(k_fwd), sum(k_bwd), k_fwd, k_bwd, _peaks())
     fwd_b, bwd_b = bench.algorithmic_bytes(w)
-    # backward main pass: HBM-bound at 7000 GB/s (its bytes exclude dB / dC and the parameter gradients)
+    exps = 1_342_177_280  # B L D N
+    fp32_peak = 152 * 128 * 2000e6  # f32 results / s
+    # backward main pass: FP32-bound, 11 operations per state update at 38.9 Top/s -> 0.379 ms, above its
+    # bytes (which exclude dB / dC and the parameter gradients) at 7000 GB/s (0.240 ms) and its exponentials
     bwd_main = bwd_b - 2 * w.Bsz * w.L * w.N * 4 - 4 * (w.Dch * w.N + 2 * w.Dch)
     r = out["roofline"]
-    assert r["bound"] == "hbm" and r["ms"] == pytest.approx(1.1)
-    assert r["achieved"] == pytest.approx(bwd_main / 1.1e-3 / 1e9, rel=1e-3)
-    # forward: 1.342 G exponentials at 152 x 32 x 2000 MHz = 9728 Gexp2/s -> 0.138 ms, above 673.8 MB / 7 TB/s
+    assert r["bound"] == "alu" and r["unit"] == "Gop/s" and r["ms"] == pytest.approx(1.1)
+    assert r["roofline_ms"] == pytest.approx(11 * exps / fp32_peak * 1e3, rel=1e-3)
+    assert r["achieved"] == pytest.approx(11 * exps / 1.1e-3 / 1e9, rel=1e-3)
+    assert r["frac"] == pytest.approx(11 * exps / 1.1e-3 / fp32_peak, rel=1e-3)
+    assert r["floors_ms"]["hbm"] == pytest.approx(bwd_main / 7e12 * 1e3, rel=1e-3)
+    assert r["hbm"]["achieved"] == pytest.approx(bwd_main / 1.1e-3 / 1e9, rel=1e-3)
+    # forward: 1.342 G exponentials at 152 x 30 x 2000 MHz = 9120 Gexp2/s -> 0.147 ms, above its 4 FP32
+    # operations per update (0.138 ms) and 673.8 MB / 7 TB/s
     rf = out["roofline_fwd"]
-    assert rf["bound"] == "alu" and rf["peak"] == pytest.approx(9728.0)
-    assert rf["roofline_ms"] == pytest.approx(1_342_177_280 / 9.728e12 * 1e3, rel=1e-3)
-    t_roof = rf["roofline_ms"] + bwd_b / 7e12 * 1e3
+    assert rf["bound"] == "alu" and rf["unit"] == "Gexp2/s" and rf["peak"] == pytest.approx(9120.0)
+    assert rf["roofline_ms"] == pytest.approx(exps / 9.12e12 * 1e3, rel=1e-3)
+    assert rf["floors_ms"]["fp32"] == pytest.approx(4 * exps / fp32_peak * 1e3, rel=1e-3)
+    t_roof = rf["roofline_ms"] + 11 * exps / fp32_peak * 1e3
     assert out["roofline_step_frac"] == pytest.approx(t_roof / 2.0, abs=1e-4)
+    # a slow memory makes the same pass HBM-bound
+    slow = bench.analyse(w, plan, 2.0, sum(k_fwd), sum(k_bwd), k_fwd, k_bwd, _peaks(hbm_gbs=1000.0))
+    assert slow["roofline"]["bound"] == "hbm" and slow["roofline"]["unit"] == "GB/s"
+    assert slow["roofline"]["achieved"] == pytest.approx(bwd_main / 1.1e-3 / 1e9, rel=1e-3)
     assert list(out["kernel_ms"]) == [
         "k_fwd chunk summary (32 units x 19 chunks)", "k_fwd y + saved states (608 units x 1 chunk)",
         "k_fwd y + saved states (32 units x 19 chunks)", "k_bwd reverse summary (32 units x 19 chunks)",
