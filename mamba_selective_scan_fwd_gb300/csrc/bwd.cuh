@@ -492,53 +492,62 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
 #pragma unroll
             for (int c = 0; c < GRP; c++) vy0[c] = 0.f;
 #pragma unroll
-            for (int v = 0; v < RWH; v++) ru[v] = 0u;
-            if (rv) {
-                if (pfast) {
-                    lds_words<GRP * C::ESZ, RWH>(&sRaw[0][r][cg], rd);
-                    lds_words<GRP * C::ESZ, RWH>(&sRaw[1][r][cg], ru);
-                    lds_words<GRP * C::ESZ, RWH>(&sRaw[2][r][cg], rg);
-                    if (z) lds_words<GRP * C::ESZ, RWH>(&sRaw[3][r][cg], rz);
-                    if (MAIN && z) ld_f32<GRP>(&sY0[r][cg], vy0);
-                } else {
-                    const int64_t off = (b * L + t) * Dch + d0 + cg;
-                    load_run<T, GRP, RWH>(delta, off, d0 + cg, Dch, false, rd);
-                    load_run<T, GRP, RWH>(u, off, d0 + cg, Dch, false, ru);
-                    load_run<T, GRP, RWH>(dy, off, d0 + cg, Dch, false, rg);
-                    if (z) load_run<T, GRP, RWH>(z, off, d0 + cg, Dch, false, rz);
-                    if (MAIN && z) {
-                        const float* y0r = a.y0 + off;
+            for (int v = 0; v < RWH; v++) rd[v] = ru[v] = rz[v] = rg[v] = 0u;
+            // The terms are formed for every row without branching (the thread's
+            // items then interleave); rows past t_end keep zero terms.  Shared-
+            // memory runs are read for every row: TMA zero-fills rows past the
+            // tensor, and other rows past t_end hold earlier data, discarded below.
+            if (pfast) {
+                lds_words<GRP * C::ESZ, RWH>(&sRaw[0][r][cg], rd);
+                lds_words<GRP * C::ESZ, RWH>(&sRaw[1][r][cg], ru);
+                lds_words<GRP * C::ESZ, RWH>(&sRaw[2][r][cg], rg);
+                if (z) lds_words<GRP * C::ESZ, RWH>(&sRaw[3][r][cg], rz);
+                if (MAIN && z) ld_f32<GRP>(&sY0[r][cg], vy0);
+            } else if (rv) {
+                const int64_t off = (b * L + t) * Dch + d0 + cg;
+                load_run<T, GRP, RWH>(delta, off, d0 + cg, Dch, false, rd);
+                load_run<T, GRP, RWH>(u, off, d0 + cg, Dch, false, ru);
+                load_run<T, GRP, RWH>(dy, off, d0 + cg, Dch, false, rg);
+                if (z) load_run<T, GRP, RWH>(z, off, d0 + cg, Dch, false, rz);
+                if (MAIN && z) {
+                    const float* y0r = a.y0 + off;
 #pragma unroll
-                        for (int c = 0; c < GRP; c++) vy0[c] = d0 + cg + c < Dch ? y0r[c] : 0.f;
-                    }
+                    for (int c = 0; c < GRP; c++) vy0[c] = d0 + cg + c < Dch ? y0r[c] : 0.f;
                 }
+            }
+            if (!rv) {
+                // discarded rows: zero u, dy, z and y0 (then g, dz and the dD terms
+                // are exactly zero, whatever the staging held)
+#pragma unroll
+                for (int v = 0; v < RWH; v++) ru[v] = rg[v] = rz[v] = 0u;
+#pragma unroll
+                for (int c = 0; c < GRP; c++) vy0[c] = 0.f;
             }
             float vdz[GRP];
 #pragma unroll
             for (int c = 0; c < GRP; c += 2) {
                 // two channels at a time with packed arithmetic
-                float2 dl2 = make_float2(0.f, 0.f), sg2 = dl2, uu2 = dl2, dlu2 = dl2, gg2 = dl2, dz2 = dl2;
-                if (rv) {
-                    const float2 x = make_float2(elem<T>(rd, c) + sBias[cg + c], elem<T>(rd, c + 1) + sBias[cg + c + 1]);
-                    if (f.softplus) {
-                        softplus_sigmoid2(x, dl2, sg2);
-                    } else {
-                        dl2 = x;
-                        sg2 = make_float2(1.f, 1.f);
-                    }
-                    uu2 = make_float2(elem<T>(ru, c), elem<T>(ru, c + 1));
-                    dlu2 = mul2(dl2, uu2);
-                    const float2 dyv = make_float2(elem<T>(rg, c), elem<T>(rg, c + 1));
-                    gg2 = dyv;
-                    if (z) {
-                        const float2 zz = make_float2(elem<T>(rz, c), elem<T>(rz, c + 1));
-                        const float2 sz = sigmoid2(zz);
-                        const float2 dsz = mul2(dyv, sz);
-                        gg2 = mul2(dsz, zz);
-                        // dz = dy sig(z) (1 + z (1 - sig(z))) y0
-                        const float2 dzf = mul2(dsz, fma2(zz, add2(splat2(1.f), make_float2(-sz.x, -sz.y)), splat2(1.f)));
-                        dz2 = mul2(dzf, make_float2(vy0[c], vy0[c + 1]));
-                    }
+                float2 dl2, sg2, dz2 = make_float2(0.f, 0.f);
+                const float2 x = make_float2(elem<T>(rd, c) + sBias[cg + c], elem<T>(rd, c + 1) + sBias[cg + c + 1]);
+                if (f.softplus) {
+                    softplus_sigmoid2(x, dl2, sg2);
+                } else {
+                    dl2 = x;
+                    sg2 = make_float2(1.f, 1.f);
+                }
+                dl2 = rv ? dl2 : make_float2(0.f, 0.f);
+                const float2 uu2 = make_float2(elem<T>(ru, c), elem<T>(ru, c + 1));
+                const float2 dlu2 = mul2(dl2, uu2);
+                const float2 dyv = make_float2(elem<T>(rg, c), elem<T>(rg, c + 1));
+                float2 gg2 = dyv;
+                if (z) {
+                    const float2 zz = make_float2(elem<T>(rz, c), elem<T>(rz, c + 1));
+                    const float2 sz = sigmoid2(zz);
+                    const float2 dsz = mul2(dyv, sz);
+                    gg2 = mul2(dsz, zz);
+                    // dz = dy sig(z) (1 + z (1 - sig(z))) y0
+                    const float2 dzf = mul2(dsz, fma2(zz, add2(splat2(1.f), make_float2(-sz.x, -sz.y)), splat2(1.f)));
+                    dz2 = mul2(dzf, make_float2(vy0[c], vy0[c + 1]));
                 }
                 const int pr = (cg + c) / 2;
                 sDU[r][pr] = make_float4(dl2.x, dl2.y, dlu2.x, dlu2.y);

@@ -310,37 +310,38 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
             const int cg = q * GRP;  // first channel of the group
             uint32_t rd[RW], ru[RW], rz[RW];
 #pragma unroll
-            for (int v = 0; v < RW; v++) rz[v] = 0u;
-            if (rv) {
-                if (fast) {
-                    lds_words<GRP * C::ESZ, RW>(&sRaw[0][r][cg], rd);
-                    lds_words<GRP * C::ESZ, RW>(&sRaw[1][r][cg], ru);
-                    if (GATE && z) lds_words<GRP * C::ESZ, RW>(&sRaw[GATE ? 2 : 1][r][cg], rz);
-                } else {
-                    const int64_t off = (b * L + t) * Dch + d0 + cg;
-                    load_run<T, GRP, RW>(delta, off, d0 + cg, Dch, false, rd);
-                    load_run<T, GRP, RW>(u, off, d0 + cg, Dch, false, ru);
-                    if (GATE && z) load_run<T, GRP, RW>(z, off, d0 + cg, Dch, false, rz);
-                }
+            for (int v = 0; v < RW; v++) rd[v] = ru[v] = rz[v] = 0u;
+            // The terms are formed for every row without branching (the thread's
+            // items then interleave); rows past t_end store zero delta_eff and
+            // input terms.  Shared-memory runs are read for every row: TMA
+            // zero-fills rows past the tensor, and other rows past t_end hold
+            // earlier data, discarded below.
+            if (fast) {
+                lds_words<GRP * C::ESZ, RW>(&sRaw[0][r][cg], rd);
+                lds_words<GRP * C::ESZ, RW>(&sRaw[1][r][cg], ru);
+                if (GATE && z) lds_words<GRP * C::ESZ, RW>(&sRaw[GATE ? 2 : 1][r][cg], rz);
+            } else if (rv) {
+                const int64_t off = (b * L + t) * Dch + d0 + cg;
+                load_run<T, GRP, RW>(delta, off, d0 + cg, Dch, false, rd);
+                load_run<T, GRP, RW>(u, off, d0 + cg, Dch, false, ru);
+                if (GATE && z) load_run<T, GRP, RW>(z, off, d0 + cg, Dch, false, rz);
             }
 #pragma unroll
             for (int c = 0; c < GRP; c += 2) {
                 // two channels at a time with packed arithmetic
-                float2 dl = make_float2(0.f, 0.f), dlu = dl;
-                if (rv) {
-                    const float2 x = make_float2(elem<T>(rd, c) + sBias[cg + c], elem<T>(rd, c + 1) + sBias[cg + c + 1]);
-                    dl = a.softplus ? softplus2(x) : x;
-                    const float2 uu = make_float2(elem<T>(ru, c), elem<T>(ru, c + 1));
-                    dlu = mul2(dl, uu);
-                    if constexpr (!NOY && !KEEP) {
-                        float2 gt = make_float2(1.f, 1.f);
-                        if (GATE && z) {
-                            const float2 zz = make_float2(elem<T>(rz, c), elem<T>(rz, c + 1));
-                            gt = mul2(zz, sigmoid2(zz));
-                        }
-                        const float2 dun = mul2(make_float2(sDv[cg + c], sDv[cg + c + 1]), uu);
-                        sGD[r][(cg + c) / 2] = make_float4(gt.x, gt.y, dun.x, dun.y);
+                const float2 x = make_float2(elem<T>(rd, c) + sBias[cg + c], elem<T>(rd, c + 1) + sBias[cg + c + 1]);
+                const float2 sp = a.softplus ? softplus2(x) : x;
+                const float2 uu = make_float2(elem<T>(ru, c), elem<T>(ru, c + 1));
+                const float2 spu = mul2(sp, uu);
+                const float2 dl = rv ? sp : make_float2(0.f, 0.f), dlu = rv ? spu : make_float2(0.f, 0.f);
+                if constexpr (!NOY && !KEEP) {
+                    float2 gt = make_float2(1.f, 1.f);
+                    if (GATE && z) {
+                        const float2 zz = make_float2(elem<T>(rz, c), elem<T>(rz, c + 1));
+                        gt = mul2(zz, sigmoid2(zz));
                     }
+                    const float2 dun = mul2(make_float2(sDv[cg + c], sDv[cg + c + 1]), uu);
+                    sGD[r][(cg + c) / 2] = make_float4(gt.x, gt.y, dun.x, dun.y);  // read for rows before t_end only
                 }
                 sDU[r][(cg + c) / 2] = make_float4(dl.x, dl.y, dlu.x, dlu.y);
             }
