@@ -468,6 +468,15 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
     }
     issue(ntile - 1);
     __syncthreads();  // sBias / sDv and the barriers before the first prologue
+    // the thread's prologue / epilogue items cover the same channel group in every
+    // tile (THREADS is a multiple of NGRP): its biases and D stay in registers
+    static_assert(THREADS % NGRP == 0, "one channel group per thread");
+    float biasv[GRP], dvv[GRP];
+#pragma unroll
+    for (int c = 0; c < GRP; c++) {
+        biasv[c] = sBias[(tid % NGRP) * GRP + c];
+        dvv[c] = sDv[(tid % NGRP) * GRP + c];
+    }
 
     for (int64_t m = ntile - 1; m >= 0; m--) {
         const int64_t t0 = t_begin + m * kTT;
@@ -524,11 +533,13 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
                 for (int c = 0; c < GRP; c++) vy0[c] = 0.f;
             }
             float vdz[GRP];
+            float4 dv[GRP / 2];  // the item's sDU and sG entries, stored after its arithmetic
+            float2 gv[GRP / 2];
 #pragma unroll
             for (int c = 0; c < GRP; c += 2) {
                 // two channels at a time with packed arithmetic
                 float2 dl2, sg2, dz2 = make_float2(0.f, 0.f);
-                const float2 x = make_float2(elem<T>(rd, c) + sBias[cg + c], elem<T>(rd, c + 1) + sBias[cg + c + 1]);
+                const float2 x = make_float2(elem<T>(rd, c) + biasv[c], elem<T>(rd, c + 1) + biasv[c + 1]);
                 if (f.softplus) {
                     softplus_sigmoid2(x, dl2, sg2);
                 } else {
@@ -550,8 +561,8 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
                     dz2 = mul2(dzf, make_float2(vy0[c], vy0[c + 1]));
                 }
                 const int pr = (cg + c) / 2;
-                sDU[r][pr] = make_float4(dl2.x, dl2.y, dlu2.x, dlu2.y);
-                sG[r][pr] = gg2;
+                dv[c / 2] = make_float4(dl2.x, dl2.y, dlu2.x, dlu2.y);
+                gv[c / 2] = gg2;
                 if (MAIN) {
                     if constexpr (C::KEEP2) {
                         kDl[it][c] = dl2.x;
@@ -569,6 +580,11 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
                     accD[it * GRP + c + 1] = fmaf(gg2.y, uu2.y, accD[it * GRP + c + 1]);
                 }
                 vdz[c] = dz2.x; vdz[c + 1] = dz2.y;
+            }
+#pragma unroll
+            for (int j = 0; j < GRP / 2; j++) {
+                sDU[r][cg / 2 + j] = dv[j];
+                sG[r][cg / 2 + j] = gv[j];
             }
             if (MAIN) {
                 if (z && rv) store_run<GRP>(a.dz + (b * L + t) * Dch + d0 + cg, vdz, d0 + cg, Dch, ofast);
@@ -832,7 +848,7 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
                     float4 us;
                     if constexpr (C::KEEP) us = make_float4(elem<T>(kU[it], c), elem<T>(kU[it], c + 1), kS[it][c], kS[it][c + 1]);
                     else us = sUS[r][pr];
-                    const float2 Dv = make_float2(sDv[cg + c], sDv[cg + c + 1]);
+                    const float2 Dv = make_float2(dvv[c], dvv[c + 1]);
                     const float2 su2 = make_float2(su[c], su[c + 1]);
                     const float2 du2 = fma2(gg2, Dv, mul2(dl2, su2));
                     const float2 dx2 = mul2(fma2(make_float2(us.x, us.y), su2,

@@ -286,6 +286,16 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
     };
     issue(t_begin, 0);
     __syncthreads();  // sBias / sDv, the barriers
+    // the thread's prologue / epilogue items cover the same channel group in every
+    // tile (THREADS is a multiple of NGRP): its biases stay in registers
+    static_assert(THREADS % NGRP == 0, "one channel group per thread");
+    const int cg = (tid % NGRP) * GRP;
+    float biasv[GRP], dvv[GRP];
+#pragma unroll
+    for (int c = 0; c < GRP; c++) {
+        biasv[c] = sBias[cg + c];
+        dvv[c] = sDv[cg + c];
+    }
     // raw runs of u and z of the thread's prologue items, kept in registers for
     // its epilogue items (the same (step, group) items), which form D * u and
     // the gate from them
@@ -300,77 +310,113 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
         bool ok = true;
         if (tma) ok = mbar_wait(&sBar[buf], (uint32_t)((jt >> 1) & 1));
         else cp_async_wait<0>();
-        // ---- prologue: (step, 8-channel group) items, then the B / C rows
-#pragma unroll
-        for (int it = 0; it < ITEMS; it++) {
-            const int id = tid + it * THREADS;
-            const int r = id / NGRP, q = id % NGRP;
-            const int64_t t = t0 + r;
-            const bool rv = t < t_end;
-            const int cg = q * GRP;  // first channel of the group
-            uint32_t rd[RW], ru[RW], rz[RW];
-#pragma unroll
-            for (int v = 0; v < RW; v++) rd[v] = ru[v] = rz[v] = 0u;
-            // The terms are formed for every row without branching (the thread's
-            // items then interleave); rows past t_end store zero delta_eff and
-            // input terms.  Shared-memory runs are read for every row: TMA
-            // zero-fills rows past the tensor, and other rows past t_end hold
-            // earlier data, discarded below.
-            if (fast) {
-                lds_words<GRP * C::ESZ, RW>(&sRaw[0][r][cg], rd);
-                lds_words<GRP * C::ESZ, RW>(&sRaw[1][r][cg], ru);
-                if (GATE && z) lds_words<GRP * C::ESZ, RW>(&sRaw[GATE ? 2 : 1][r][cg], rz);
-            } else if (rv) {
-                const int64_t off = (b * L + t) * Dch + d0 + cg;
-                load_run<T, GRP, RW>(delta, off, d0 + cg, Dch, false, rd);
-                load_run<T, GRP, RW>(u, off, d0 + cg, Dch, false, ru);
-                if (GATE && z) load_run<T, GRP, RW>(z, off, d0 + cg, Dch, false, rz);
-            }
-#pragma unroll
-            for (int c = 0; c < GRP; c += 2) {
-                // two channels at a time with packed arithmetic
-                const float2 x = make_float2(elem<T>(rd, c) + sBias[cg + c], elem<T>(rd, c + 1) + sBias[cg + c + 1]);
-                const float2 sp = a.softplus ? softplus2(x) : x;
-                const float2 uu = make_float2(elem<T>(ru, c), elem<T>(ru, c + 1));
-                const float2 spu = mul2(sp, uu);
-                const float2 dl = rv ? sp : make_float2(0.f, 0.f), dlu = rv ? spu : make_float2(0.f, 0.f);
-                if constexpr (!NOY && !KEEP) {
-                    float2 gt = make_float2(1.f, 1.f);
-                    if (GATE && z) {
-                        const float2 zz = make_float2(elem<T>(rz, c), elem<T>(rz, c + 1));
-                        gt = mul2(zz, sigmoid2(zz));
-                    }
-                    const float2 dun = mul2(make_float2(sDv[cg + c], sDv[cg + c + 1]), uu);
-                    sGD[r][(cg + c) / 2] = make_float4(gt.x, gt.y, dun.x, dun.y);  // read for rows before t_end only
-                }
-                sDU[r][(cg + c) / 2] = make_float4(dl.x, dl.y, dlu.x, dlu.y);
-            }
-            if constexpr (!NOY && KEEP) {
-#pragma unroll
-                for (int v = 0; v < RW; v++) kU[it][v] = ru[v];
-            }
-            if constexpr (GATE && KEEP) {
-#pragma unroll
-                for (int v = 0; v < RW; v++) kZ[it][v] = rz[v];
-            }
-        }
+        // ---- prologue: (step, 8-channel group) items, then the B / C rows.  All
+        // of the thread's shared-memory reads come first, then the arithmetic of
+        // every item, then the stores: with no store between them, the items'
+        // dependency chains (two MUFU steps and a polynomial each) interleave.
+        // The terms are formed for every row without branching; rows past t_end
+        // store zero delta_eff and input terms.  Shared-memory runs are read for
+        // every row: TMA zero-fills rows past the tensor, and other rows past
+        // t_end hold earlier data, discarded by the selects.
+        // 16-bit B / C rows of the tile's steps, in units of BCV values of one row
+        // (tensor, step), converted by the thread that copied them (or loaded here
+        // when too short to copy)
+        constexpr int BCV = C::BCV, BCU = C::BCU, VW = BCV * C::ESZ >= 4 ? BCV * C::ESZ / 4 : 1;
+        constexpr int BCUT = C::BC_DIRECT ? 1 : (NOY ? 1 : 2) * kRow * BCU / THREADS;  // units per thread
+        uint32_t wv[BCUT][VW];
         if constexpr (!C::BC_DIRECT) {
-            // 16-bit B / C rows of the tile's steps, in units of BCV values of one
-            // row (tensor, step), converted by the thread that copied them (or
-            // loaded here when too short to copy)
-            constexpr int BCV = C::BCV, BCU = C::BCU, VW = BCV * C::ESZ >= 4 ? BCV * C::ESZ / 4 : 1;
-            for (int id = tid; id < (NOY ? 1 : 2) * kRow * BCU; id += THREADS) {
+            static_assert((NOY ? 1 : 2) * kRow * BCU % THREADS == 0, "whole conversion units per thread");
+#pragma unroll
+            for (int k = 0; k < BCUT; k++) {
+                const int id = tid + k * THREADS;
                 const int row = id / BCU, n = (id % BCU) * BCV;
                 const int half = row / kRow, r = row % kRow;
                 const int64_t t = t0 + r;
-                uint32_t wv[VW];
+#pragma unroll
+                for (int v = 0; v < VW; v++) wv[k][v] = 0u;
                 if (t < t_end) {
-                    if constexpr (C::BC_RAW) lds_words<BCV * C::ESZ, VW>(&sBCraw[half][r][n], wv);
-                    else load_words<BCV * C::ESZ, VW>((half ? Cm : Bm) + (b * L + t) * N + n, wv);
+                    if constexpr (C::BC_RAW) lds_words<BCV * C::ESZ, VW>(&sBCraw[half][r][n], wv[k]);
+                    else load_words<BCV * C::ESZ, VW>((half ? Cm : Bm) + (b * L + t) * N + n, wv[k]);
                 }
+            }
+        }
+        // (items in batches of IB, which bounds the registers they hold)
+        constexpr int IB = ITEMS < 2 ? ITEMS : 2;
+        static_assert(ITEMS % IB == 0, "whole batches of items");
+#pragma unroll
+        for (int ib = 0; ib < ITEMS; ib += IB) {
+            uint32_t rd[IB][RW], ru[IB][RW], rz[IB][RW];
+#pragma unroll
+            for (int k = 0; k < IB; k++) {
+                const int it = ib + k;
+                const int id = tid + it * THREADS;
+                const int r = id / NGRP;
+                const int64_t t = t0 + r;
+#pragma unroll
+                for (int v = 0; v < RW; v++) rd[k][v] = ru[k][v] = rz[k][v] = 0u;
+                if (fast) {
+                    lds_words<GRP * C::ESZ, RW>(&sRaw[0][r][cg], rd[k]);
+                    lds_words<GRP * C::ESZ, RW>(&sRaw[1][r][cg], ru[k]);
+                    if (GATE && z) lds_words<GRP * C::ESZ, RW>(&sRaw[GATE ? 2 : 1][r][cg], rz[k]);
+                } else if (t < t_end) {
+                    const int64_t off = (b * L + t) * Dch + d0 + cg;
+                    load_run<T, GRP, RW>(delta, off, d0 + cg, Dch, false, rd[k]);
+                    load_run<T, GRP, RW>(u, off, d0 + cg, Dch, false, ru[k]);
+                    if (GATE && z) load_run<T, GRP, RW>(z, off, d0 + cg, Dch, false, rz[k]);
+                }
+            }
+            float4 dv[IB][GRP / 2], gd[NOY || KEEP ? 1 : IB][GRP / 2];
+#pragma unroll
+            for (int k = 0; k < IB; k++) {
+                const int it = ib + k;
+                const bool rv = t0 + (tid + it * THREADS) / NGRP < t_end;
+#pragma unroll
+                for (int c = 0; c < GRP; c += 2) {
+                    // two channels at a time with packed arithmetic
+                    const float2 x = make_float2(elem<T>(rd[k], c) + biasv[c], elem<T>(rd[k], c + 1) + biasv[c + 1]);
+                    const float2 sp = a.softplus ? softplus2(x) : x;
+                    const float2 uu = make_float2(elem<T>(ru[k], c), elem<T>(ru[k], c + 1));
+                    const float2 spu = mul2(sp, uu);
+                    const float2 dl = rv ? sp : make_float2(0.f, 0.f), dlu = rv ? spu : make_float2(0.f, 0.f);
+                    dv[k][c / 2] = make_float4(dl.x, dl.y, dlu.x, dlu.y);
+                    if constexpr (!NOY && !KEEP) {
+                        float2 gt = make_float2(1.f, 1.f);
+                        if (GATE && z) {
+                            const float2 zz = make_float2(elem<T>(rz[k], c), elem<T>(rz[k], c + 1));
+                            gt = mul2(zz, sigmoid2(zz));
+                        }
+                        const float2 dun = mul2(make_float2(dvv[c], dvv[c + 1]), uu);
+                        gd[k][c / 2] = make_float4(gt.x, gt.y, dun.x, dun.y);  // read for rows before t_end only
+                    }
+                }
+                if constexpr (!NOY && KEEP) {
+#pragma unroll
+                    for (int v = 0; v < RW; v++) kU[it][v] = ru[k][v];
+                }
+                if constexpr (GATE && KEEP) {
+#pragma unroll
+                    for (int v = 0; v < RW; v++) kZ[it][v] = rz[k][v];
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < IB; k++) {
+                const int r = (tid + (ib + k) * THREADS) / NGRP;
+#pragma unroll
+                for (int c = 0; c < GRP; c += 2) {
+                    sDU[r][(cg + c) / 2] = dv[k][c / 2];
+                    if constexpr (!NOY && !KEEP) sGD[r][(cg + c) / 2] = gd[k][c / 2];
+                }
+            }
+        }
+        if constexpr (!C::BC_DIRECT) {
+#pragma unroll
+            for (int k = 0; k < BCUT; k++) {
+                const int id = tid + k * THREADS;
+                const int row = id / BCU, n = (id % BCU) * BCV;
+                const int half = row / kRow, r = row % kRow;
                 float* dst = &sBC[half][0][r][n];
 #pragma unroll
-                for (int v = 0; v < BCV; v++) dst[v] = t < t_end ? elem<T>(wv, v) : 0.f;
+                for (int v = 0; v < BCV; v++) dst[v] = elem<T>(wv[k], v);  // zero past t_end
             }
         }
         // Staging complete; every thread is done reading sRaw / sBCraw.  A thread
@@ -455,16 +501,17 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
         }
         __syncthreads();
 
-        // ---- epilogue: (step, 8-channel group) items
+        // ---- epilogue: (step, 8-channel group) items; all items' sums and gates
+        // first (rows past t_end too: their partial readouts are finite), then the
+        // stores of the rows before t_end
         if (!NOY) {
 #pragma unroll
-            for (int it = 0; it < ITEMS; it++) {
-                const int id = tid + it * THREADS;
-                const int r = id / NGRP, q = id % NGRP;
-                const int64_t t = t0 + r;
-                const int cg = q * GRP;
-                if (t < t_end) {
-                    float yv[GRP], y0v[GRP];
+            for (int ib = 0; ib < ITEMS; ib += IB) {
+                float yv[IB][GRP], y0v[IB][GRP];
+#pragma unroll
+                for (int k = 0; k < IB; k++) {
+                    const int it = ib + k;
+                    const int r = (tid + it * THREADS) / NGRP;
 #pragma unroll
                     for (int c = 0; c < GRP; c += 4) {
                         // per warp, the sum of its G lanes' planes; then the warps in order
@@ -491,8 +538,7 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
                             float2 y0, gt = make_float2(1.f, 1.f);
                             if constexpr (KEEP) {
                                 const float2 uu = make_float2(elem<T>(kU[it], cc), elem<T>(kU[it], cc + 1));
-                                y0 = fma2(make_float2(sDv[cg + cc], sDv[cg + cc + 1]), uu,
-                                          make_float2(sum4[e], sum4[e + 1]));
+                                y0 = fma2(make_float2(dvv[cc], dvv[cc + 1]), uu, make_float2(sum4[e], sum4[e + 1]));
                                 if (GATE && z) {
                                     const float2 zz = make_float2(elem<T>(kZ[it], cc), elem<T>(kZ[it], cc + 1));
                                     gt = mul2(zz, sigmoid2(zz));
@@ -502,12 +548,17 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
                                 y0 = add2(make_float2(sum4[e], sum4[e + 1]), make_float2(gd.z, gd.w));
                                 gt = make_float2(gd.x, gd.y);
                             }
-                            y0v[cc] = y0.x;
-                            y0v[cc + 1] = y0.y;
-                            yv[cc] = y0.x * gt.x;
-                            yv[cc + 1] = y0.y * gt.y;
+                            y0v[k][cc] = y0.x;
+                            y0v[k][cc + 1] = y0.y;
+                            yv[k][cc] = y0.x * gt.x;
+                            yv[k][cc + 1] = y0.y * gt.y;
                         }
                     }
+                }
+#pragma unroll
+                for (int k = 0; k < IB; k++) {
+                    const int64_t t = t0 + (tid + (ib + k) * THREADS) / NGRP;
+                    if (t >= t_end) continue;
                     const int64_t off = (b * L + t) * Dch + d0 + cg;
                     if (a.y0 && z) {
                         // kept for the backward's dz (f32; the same alignment as the io runs)
@@ -515,11 +566,12 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
                         if (sfast) {
 #pragma unroll
                             for (int c = 0; c < GRP; c += 4)
-                                *reinterpret_cast<float4*>(y0row + c) = make_float4(y0v[c], y0v[c + 1], y0v[c + 2], y0v[c + 3]);
+                                *reinterpret_cast<float4*>(y0row + c) =
+                                    make_float4(y0v[k][c], y0v[k][c + 1], y0v[k][c + 2], y0v[k][c + 3]);
                         } else {
 #pragma unroll
                             for (int c = 0; c < GRP; c++)
-                                if (d0 + cg + c < Dch) y0row[c] = y0v[c];
+                                if (d0 + cg + c < Dch) y0row[c] = y0v[k][c];
                         }
                     }
                     if (!GATE) continue;
@@ -528,19 +580,18 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
                         uint32_t wv[RW];
                         if constexpr (sizeof(T) == 4) {
 #pragma unroll
-                            for (int c = 0; c < GRP; c++) wv[c] = __float_as_uint(yv[c]);
+                            for (int c = 0; c < GRP; c++) wv[c] = __float_as_uint(yv[k][c]);
                         } else {
 #pragma unroll
-                            for (int c = 0; c < GRP; c += 2) wv[c >> 1] = pack2<T>(yv[c], yv[c + 1]);
+                            for (int c = 0; c < GRP; c += 2) wv[c >> 1] = pack2<T>(yv[k][c], yv[k][c + 1]);
                         }
 #pragma unroll
                         for (int v = 0; v < RW / 4; v++)
-                            reinterpret_cast<uint4*>(yrow)[v] =
-                                make_uint4(wv[4 * v], wv[4 * v + 1], wv[4 * v + 2], wv[4 * v + 3]);
+                            reinterpret_cast<uint4*>(yrow)[v] = make_uint4(wv[4 * v], wv[4 * v + 1], wv[4 * v + 2], wv[4 * v + 3]);
                     } else {
 #pragma unroll
                         for (int c = 0; c < GRP; c++)
-                            if (d0 + cg + c < Dch) st(yrow + c, yv[c]);
+                            if (d0 + cg + c < Dch) st(yrow + c, yv[k][c]);
                     }
                 }
             }
