@@ -106,8 +106,9 @@ bool tma_eligible(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype) {
 }
 
 // The maps a forward (rows = steps per tile of the forward) or a backward
-// (rows = steps per recompute window) loads its tiles through; y0 (f32, the
-// forward's pre-gate readout kept for dz) only for the backward.
+// (rows = steps per staging copy: two recompute windows for two-warp blocks,
+// one otherwise) loads its tiles through; y0 (f32, the forward's pre-gate
+// readout kept for dz) only for the backward.
 bool make_maps(TmaMaps& mp, const FwdArgs& f, const void* dy, const float* y0, int rows) {
     const CUtensorMapDataType io = f.dtype == SS_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                    : f.dtype == SS_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
@@ -285,7 +286,7 @@ int bwd_impl(const void* u, const void* delta, const float* A, const void* B, co
     // use the forward's 32-step boxes, the main pass its own
     TmaMaps fmaps, bmaps;
     a.f.use_tma = tma_eligible(Bsz, L, Dch, N, dtype) && make_maps(fmaps, a.f, dy, nullptr, kFwdRows) &&
-                          make_maps(bmaps, a.f, dy, z ? a.y0 : nullptr, kSub)
+                          make_maps(bmaps, a.f, dy, z ? a.y0 : nullptr, (scan_warps(N) == 2 ? 2 : 1) * kSub)
                       ? 1
                       : 0;
     return launch_bwd(a, p, st, ckpt_out, fmaps, bmaps) == cudaSuccess ? SS_OK : SS_ERR_CUDA;

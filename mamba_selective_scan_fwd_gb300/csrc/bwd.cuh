@@ -116,6 +116,12 @@ struct BCfg {
     // every SM (8 warps: 4 two-warp or 8 one-warp blocks), which leaves the
     // walk up to 255 registers
     static constexpr int MINB = NW == 2 ? 4 : 8;
+    // Tiles per staging copy ("a pair"): two for two-warp blocks.  A TMA copy
+    // holds its issuing thread for some 60 - 100 cycles whatever its size, so
+    // the copies of a tile's eight tensors cost about as much as its recompute;
+    // a copy of two tiles halves that per step, for 8 KB more shared memory (a
+    // one-warp block keeps one tile per copy: 8 of them share an SM).
+    static constexpr int TPP = NW == 2 ? 2 : 1;
     static_assert(kTT * NGRP % THREADS == 0, "whole items per thread");
     static_assert(CH == channels_per_block(N), "channel tile of the plan");
     static_assert(S * G * NW == N, "the lanes cover the states");
@@ -214,7 +220,8 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
     constexpr bool MAIN = MODE == kRevMain;
     constexpr int NW = C::NW, NPW = C::NPW, S = C::S, SP = C::SP, G = C::G, PAIRS = C::PAIRS, CH = C::CH,
                   THREADS = C::THREADS, GRP = C::GRP, NGRP = C::NGRP, ITEMS = C::ITEMS, RWH = C::RWH,
-                  EP = C::EP, BLK = C::BLK;
+                  EP = C::EP, BLK = C::BLK, TPP = C::TPP;
+    constexpr int kSTT = TPP * kTT;  // steps per staging copy
     // per-(t, d) staging of the walk, one entry per channel pair
     __shared__ float4 sDU[kTT][PAIRS + 1];  // (Delta of both channels, Delta*u of both channels)
     // g of both channels (rows of PAIRS + 1 entries: the prologue's 8-byte stores
@@ -223,20 +230,24 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
     // (u of both channels, sig(delta + bias) of both channels), for the epilogue
     // when they do not stay in registers
     __shared__ float4 sUS[MAIN && !C::KEEP ? kTT : 1][MAIN && !C::KEEP ? PAIRS + 1 : 1];
-    // B / C rows as f32 (B then C); with f32 io double buffered, the next tile's
-    // rows being copied in while the current tile is walked
-    __shared__ __align__(128) float sBC[2][C::BC_BUFS][C::BC_PK ? 1 : kTT][C::BC_PK ? 4 : N];
-    // packed bf16 B / C rows (B, then C), double buffered: the walk reads them directly
-    __shared__ __align__(128) T sBCpk[2][C::BC_PK ? 2 : 1][C::BC_PK ? kTT : 1][C::BC_PK ? N : 8];
-    // raw 16-bit B / C rows of the next tile (converted into sBC by the prologue)
-    __shared__ __align__(128) T sBCraw[2][C::BC_RAW ? kTT : 1][C::BC_RAW ? N : 8];
-    // completion of the TMA copies into the two tile buffers
+    // Staging is by pairs of TPP tiles (kSTT steps): tile m is part m % TPP of
+    // pair m / TPP, whose buffer is (m / TPP) & 1.
+    // B / C rows as f32 (B then C): with f32 io the pairs' rows double buffered,
+    // the next pair's being copied in while the current one is walked; with f16
+    // the current tile's rows, converted by its prologue
+    __shared__ __align__(128) float sBC[2][C::BC_BUFS][C::BC_PK ? 1 : (C::BC_DIRECT ? kSTT : kTT)][C::BC_PK ? 4 : N];
+    // packed bf16 B / C rows (B, then C) of the pairs, double buffered: the walk
+    // reads them directly
+    __shared__ __align__(128) T sBCpk[2][C::BC_PK ? 2 : 1][C::BC_PK ? kSTT : 1][C::BC_PK ? N : 8];
+    // raw 16-bit B / C rows of the next pair (converted into sBC by the prologues)
+    __shared__ __align__(128) T sBCraw[2][C::BC_RAW ? kSTT : 1][C::BC_RAW ? N : 8];
+    // completion of the TMA copies into the two pair buffers
     __shared__ __align__(8) uint64_t sBar[2];
-    // raw runs of delta, u, dy, z of the next tile, copied in asynchronously by
+    // raw runs of delta, u, dy, z of the next pair, copied in asynchronously by
     // the thread that later converts them
-    __shared__ __align__(128) T sRaw[4][kTT][CH];
-    // the forward's pre-gate readout y0 of the next tile (for dz), likewise
-    __shared__ __align__(128) float sY0[MAIN ? kTT : 1][MAIN ? CH : 4];
+    __shared__ __align__(128) T sRaw[4][kSTT][CH];
+    // the forward's pre-gate readout y0 of the next pair (for dz), likewise
+    __shared__ __align__(128) float sY0[MAIN ? kSTT : 1][MAIN ? CH : 4];
     // dB / dC contributions of the tile's kTT steps, per warp: block (j, tau)
     // holds a row of NPW floats per pair
     __shared__ __align__(16) float sR[MAIN ? NW : 1][MAIN ? kTT * 2 * BLK : 4];
@@ -246,9 +257,9 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
     __shared__ __align__(16) float sOd[MAIN ? NW : 1][MAIN ? G * C::OPL : 4];
     // dD / ddelta_bias partials of each epilogue thread's items at the end (thread fastest)
     __shared__ float sAcc[MAIN ? 2 : 1][MAIN ? ITEMS * GRP : 1][THREADS];
-    // the state entering each tile (the recompute window's start), 2 S floats
-    // per lane (S of each channel), double buffered by tile
-    __shared__ __align__(128) float sH[MAIN ? 2 : 1][MAIN ? THREADS * 2 * S : 4];
+    // the states entering the tiles of a pair (the recompute windows' starts:
+    // TPP saved-state blocks of 2 S floats per lane), double buffered
+    __shared__ __align__(128) float sH[MAIN ? 2 : 1][MAIN ? TPP * THREADS * 2 * S : 4];
     __shared__ float sBias[CH], sDv[CH];
 
     const FwdArgs& f = a.f;
@@ -357,31 +368,32 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
     const int64_t t_end = t_begin + sgm.Lc < L ? t_begin + sgm.Lc : L;
     const int64_t ntile = (t_end - t_begin + kTT - 1) / kTT;
     // saved states (layout of ckpt_bytes): one block of CH x N floats per
-    // (slot, batch, channel tile), the lane's 2 S floats at its slot
-    const int64_t ck_stride = f.Bsz * p.tiles_b * CH * N;
-    const float* ck_lane =
-        a.ws_ckpt + (t_begin / kSub) * ck_stride + (b * p.tiles_b + tile) * (CH * N) + ckpt_slot(w, lane, S, 0);
+    // (batch, channel tile, slot), consecutive slots contiguous; the lane's 2 S
+    // floats at its slots
+    const float* ck_unit = a.ws_ckpt + ckpt_block(p, b, tile, t_begin / kSub, N);  // the chunk's first slot
     float* bc0 = a.ws_bc + ((int64_t)tile * f.Bsz + b) * L * N;                  // dB partials of this tile
     float* bc1 = a.ws_bc + ((int64_t)(p.tiles_b + tile) * f.Bsz + b) * L * N;    // dC partials
     float* sRw = &sR[MAIN ? w : 0][0];
+    constexpr int HB = THREADS * 2 * S;  // floats of one saved-state block
 
-    // Copies of tile mm into buffer mm & 1.  With TMA: one thread issues a box per
-    // tensor (delta, u, dy, z as [kTT][CH], y0 as f32 [kTT][CH], B and C as
-    // [kTT][N]: bf16 packed into sBCpk, f32 into sBC, f16 raw into sBCraw) and
-    // the tile's block of saved states (CH x N floats, in lane order) into sH,
+    // Copies of tile pair pp (its tiles TPP pp .. TPP pp + TPP - 1) into buffer pp & 1.
+    // With TMA: one thread issues a box per tensor (delta, u, dy, z as
+    // [kSTT][CH], y0 as f32 [kSTT][CH], B and C as [kSTT][N]: bf16 packed into
+    // sBCpk, f32 into sBC, f16 raw into sBCraw) and one bulk copy of the pair's
+    // TPP blocks of saved states (CH x N floats each, in lane order) into sH,
     // on the buffer's barrier.  Otherwise, one commit group of asynchronous
-    // copies: the thread's item runs and y0 runs (when the tile's rows are whole
-    // aligned vectors), the B / C rows, and the lane's state entering the tile
-    // into its own slots of sH; each thread converts the runs it copied and the
-    // state is read by the lane that copied it.
+    // copies: the thread's item runs and y0 runs of the pair's tiles (when the
+    // rows are whole aligned vectors), the B / C rows, and the lane's states
+    // entering the tiles into its own slots of sH; each thread converts the
+    // runs it copied and the states are read by the lane that copied them.
     const TmaMaps& mp = maps;
-    auto issue = [&](int64_t mm) {
-        const int64_t tt = t_begin + mm * kTT;
-        const int buf = (int)(mm & 1);
+    auto issue = [&](int64_t pp) {
+        const int64_t tt = t_begin + pp * kSTT;
+        const int buf = (int)(pp & 1);
         if (tma) {
             if (tid == 0) {
-                constexpr uint32_t run = kTT * CH * C::ESZ, row = kTT * N * C::ESZ, state = CH * N * 4;
-                const uint32_t bytes = (MAIN ? 3 : 2) * run + (z ? run : 0) + (MAIN && z ? kTT * CH * 4 : 0) +
+                constexpr uint32_t run = kSTT * CH * C::ESZ, row = kSTT * N * C::ESZ, state = TPP * CH * N * 4;
+                const uint32_t bytes = (MAIN ? 3 : 2) * run + (z ? run : 0) + (MAIN && z ? kSTT * CH * 4 : 0) +
                                        (MAIN ? 2 : 1) * row + (MAIN ? state : 0);
                 mbar_expect_tx(&sBar[buf], bytes);
                 const int x = (int)d0, y = (int)tt, zc = (int)b;
@@ -398,10 +410,8 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
                     else dst = &sBCraw[half][0][0];
                     tma_load_3d(dst, &mp.m[half ? kMapC : kMapB], 0, y, zc, &sBar[buf]);
                 }
-                if (MAIN) {
-                    const float* blk = ck_lane - ckpt_slot(w, lane, S, 0) + (tt - t_begin) / kSub * ck_stride;
-                    bulk_load(&sH[buf][0], blk, state, &sBar[buf]);
-                }
+                // the pair's slots always exist: slots run to L rounded up to 32 steps
+                if (MAIN) bulk_load(&sH[buf][0], ck_unit + (tt - t_begin) / kSub * (CH * N), state, &sBar[buf]);
             }
             return;
         }
@@ -409,20 +419,24 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
 #pragma unroll
             for (int it = 0; it < ITEMS; it++) {
                 const int id = tid + it * THREADS;
-                const int r = id / NGRP, cg = (id % NGRP) * GRP;
-                const int64_t t = tt + r;
-                if (t < t_end) {
-                    const int64_t off = (b * L + t) * Dch + d0 + cg;
-                    cp_async_bytes<GRP * C::ESZ>(&sRaw[0][r][cg], delta + off);
-                    cp_async_bytes<GRP * C::ESZ>(&sRaw[1][r][cg], u + off);
-                    cp_async_bytes<GRP * C::ESZ>(&sRaw[2][r][cg], dy + off);
-                    if (z) cp_async_bytes<GRP * C::ESZ>(&sRaw[3][r][cg], z + off);
-                    if (MAIN && z) cp_async_bytes<GRP * 4>(&sY0[r][cg], a.y0 + off);
+                const int r0 = id / NGRP, cg = (id % NGRP) * GRP;
+#pragma unroll
+                for (int hh = 0; hh < TPP; hh++) {
+                    const int r = hh * kTT + r0;
+                    const int64_t t = tt + r;
+                    if (t < t_end) {
+                        const int64_t off = (b * L + t) * Dch + d0 + cg;
+                        cp_async_bytes<GRP * C::ESZ>(&sRaw[0][r][cg], delta + off);
+                        cp_async_bytes<GRP * C::ESZ>(&sRaw[1][r][cg], u + off);
+                        cp_async_bytes<GRP * C::ESZ>(&sRaw[2][r][cg], dy + off);
+                        if (z) cp_async_bytes<GRP * C::ESZ>(&sRaw[3][r][cg], z + off);
+                        if (MAIN && z) cp_async_bytes<GRP * 4>(&sY0[r][cg], a.y0 + off);
+                    }
                 }
             }
         }
-        for (int id = tid; id < (MAIN ? 2 : 1) * kTT; id += THREADS) {
-            const int half = MAIN ? id / kTT : 1, r = id % kTT;
+        for (int id = tid; id < (MAIN ? 2 : 1) * kSTT; id += THREADS) {
+            const int half = MAIN ? id / kSTT : 1, r = id % kSTT;
             const int64_t t = tt + r;
             const T* src = (half ? Cm : Bm) + (b * L + (t < t_end ? t : 0)) * N;
             if constexpr (C::BC_PK) {
@@ -445,19 +459,22 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
         }
         if constexpr (C::BC_RAW) {
             // in the prologue's conversion units
-            for (int id = tid; id < (MAIN ? 2 : 1) * kTT * C::BCU; id += THREADS) {
+            for (int id = tid; id < (MAIN ? 2 : 1) * kSTT * C::BCU; id += THREADS) {
                 const int row = id / C::BCU, n = (id % C::BCU) * C::BCV;
-                const int half = MAIN ? row / kTT : 1, r = row % kTT;
+                const int half = MAIN ? row / kSTT : 1, r = row % kSTT;
                 const int64_t t = tt + r;
                 if (t < t_end) cp_async_bytes<C::BCV * C::ESZ>(&sBCraw[half][r][n], (half ? Cm : Bm) + (b * L + t) * N + n);
             }
         }
         if (MAIN) {
             // the block's layout: the lane's S states of each channel at its two slots
-            const float* src = ck_lane + (tt - t_begin) / kSub * ck_stride;
-            float* dst = &sH[buf][ckpt_slot(w, lane, S, 0)];
-            cp_async_bytes<S * 4>(dst, src);
-            cp_async_bytes<S * 4>(dst + 32 * S, src + 32 * S);
+#pragma unroll
+            for (int hh = 0; hh < TPP; hh++) {
+                const float* src = ck_unit + ((tt - t_begin) / kSub + hh) * (CH * N) + ckpt_slot(w, lane, S, 0);
+                float* dst = &sH[buf][hh * HB + ckpt_slot(w, lane, S, 0)];
+                cp_async_bytes<S * 4>(dst, src);
+                cp_async_bytes<S * 4>(dst + 32 * S, src + 32 * S);
+            }
         }
         cp_async_commit();
     };
@@ -466,7 +483,8 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
         mbar_init(&sBar[1], 1);
         fence_proxy_async_smem();
     }
-    issue(ntile - 1);
+    const int64_t npair = (ntile + TPP - 1) / TPP;
+    issue(npair - 1);
     __syncthreads();  // sBias / sDv and the barriers before the first prologue
     // the thread's prologue / epilogue items cover the same channel group in every
     // tile (THREADS is a multiple of NGRP): its biases and D stay in registers
@@ -480,14 +498,20 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
 
     for (int64_t m = ntile - 1; m >= 0; m--) {
         const int64_t t0 = t_begin + m * kTT;
-        const int buf = (int)(m & 1);
-        // the tile's copies: this thread's own (asynchronous copies), or the TMA
-        // boxes (the tiles are visited from the last, so the buffer's barrier
-        // completes its phase (ntile - 1 - m) / 2 mod 2)
-        const uint32_t phase = (uint32_t)(((ntile - 1 - m) >> 1) & 1);
+        const int64_t pr = m / TPP;            // the tile's pair
+        const int buf = (int)(pr & 1);         // its staging buffer
+        const int part = (int)(m % TPP);       // the tile's part of the pair
+        const int hrow = part * kTT;           // its rows within the pair's staging
+        // the pair's copies, awaited by the first of its tiles to be visited (the
+        // last one): this thread's own (asynchronous copies), or the TMA boxes
+        // (the pairs are visited from the last, so the buffer's barrier completes
+        // its phase (npair - 1 - pr) / 2 mod 2)
+        const uint32_t phase = (uint32_t)(((npair - 1 - pr) >> 1) & 1);
         bool ok = true;
-        if (tma) ok = mbar_wait(&sBar[buf], phase);
-        else cp_async_wait<0>();
+        if (part == TPP - 1 || m == ntile - 1) {
+            if (tma) ok = mbar_wait(&sBar[buf], phase);
+            else cp_async_wait<0>();
+        }
         // ---- prologue: (step, GRP-channel group) items of the tile; dz is final here
 #pragma unroll
         for (int it = 0; it < ITEMS; it++) {
@@ -507,11 +531,11 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
             // memory runs are read for every row: TMA zero-fills rows past the
             // tensor, and other rows past t_end hold earlier data, discarded below.
             if (pfast) {
-                lds_words<GRP * C::ESZ, RWH>(&sRaw[0][r][cg], rd);
-                lds_words<GRP * C::ESZ, RWH>(&sRaw[1][r][cg], ru);
-                lds_words<GRP * C::ESZ, RWH>(&sRaw[2][r][cg], rg);
-                if (z) lds_words<GRP * C::ESZ, RWH>(&sRaw[3][r][cg], rz);
-                if (MAIN && z) ld_f32<GRP>(&sY0[r][cg], vy0);
+                lds_words<GRP * C::ESZ, RWH>(&sRaw[0][hrow + r][cg], rd);
+                lds_words<GRP * C::ESZ, RWH>(&sRaw[1][hrow + r][cg], ru);
+                lds_words<GRP * C::ESZ, RWH>(&sRaw[2][hrow + r][cg], rg);
+                if (z) lds_words<GRP * C::ESZ, RWH>(&sRaw[3][hrow + r][cg], rz);
+                if (MAIN && z) ld_f32<GRP>(&sY0[hrow + r][cg], vy0);
             } else if (rv) {
                 const int64_t off = (b * L + t) * Dch + d0 + cg;
                 load_run<T, GRP, RWH>(delta, off, d0 + cg, Dch, false, rd);
@@ -605,7 +629,7 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
                 const int64_t t = t0 + r;
                 uint32_t wv[VW];
                 if (t < t_end) {
-                    if constexpr (C::BC_RAW) lds_words<BCV * C::ESZ, VW>(&sBCraw[half][r][n], wv);
+                    if constexpr (C::BC_RAW) lds_words<BCV * C::ESZ, VW>(&sBCraw[half][hrow + r][n], wv);
                     else load_words<BCV * C::ESZ, VW>((half ? Cm : Bm) + (b * L + t) * N + n, wv);
                 }
                 float* dst = &sBC[half][0][r][n];
@@ -625,11 +649,14 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
             }
             return;
         }
-        if (m > 0) issue(m - 1);
+        // the pair's staging has been read by all its tiles' prologues once its
+        // first tile (part 0, visited last) passes this barrier
+        if (part == 0 && pr > 0) issue(pr - 1);
         // S values of row i's B (half 0) or C (half 1) from the lane's states
         auto ld_bc = [&](int i, int half, float (&v)[S]) {
-            if constexpr (C::BC_PK) ld_bf16x4(&sBCpk[half][buf][i][n0], v);
-            else ld_f32<S>(&sBC[half][C::BC_DIRECT ? buf : 0][i][n0], v);
+            if constexpr (C::BC_PK) ld_bf16x4(&sBCpk[half][buf][hrow + i][n0], v);
+            else if constexpr (C::BC_DIRECT) ld_f32<S>(&sBC[half][buf][hrow + i][n0], v);
+            else ld_f32<S>(&sBC[half][0][i][n0], v);
         };
 
         if constexpr (!MAIN) {
@@ -663,7 +690,7 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
             // leave the state and the adjoint unchanged and add nothing; only their
             // per-step stores are skipped.
             // the state entering the tile (the lane's slots in sH), as state pairs
-            const float* hsrc = &sH[buf][ckpt_slot(w, lane, S, 0)];
+            const float* hsrc = &sH[buf][part * HB + ckpt_slot(w, lane, S, 0)];
             auto load_hs = [&](float2 (&hs)[2][SP]) {
 #pragma unroll
                 for (int e = 0; e < 2; e++) {

@@ -216,10 +216,8 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
     const int64_t t_begin = k * sgm.Lc;
     const int64_t t_end = t_begin + sgm.Lc < L ? t_begin + sgm.Lc : L;
     // saved states (layout of ckpt_bytes): one block of CH x N floats per
-    // (slot t / kSub, batch, channel tile), the lane's 2 S floats at its slot
-    const int64_t ck_stride = a.Bsz * ntiles * CH * N;
-    float* ck_lane =
-        SAVE ? ckpt + (t_begin / kSub) * ck_stride + (b * ntiles + tile) * (CH * N) + ckpt_slot(w, lane, S, 0) : nullptr;
+    // (batch, channel tile, slot t / kSub), the lane's 2 S floats at its slots
+    float* ck_lane = SAVE ? ckpt + ckpt_block(p, b, tile, t_begin / kSub, N) + ckpt_slot(w, lane, S, 0) : nullptr;
 
     // Copies of the tile starting at tt into buffer buf.  With TMA: one thread
     // issues a box per tensor (delta, u, z as [kRow][CH], B and C as
@@ -466,7 +464,7 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
                 // channel 0, S of c1 at its slot of channel 1); every slot is written:
                 // channels past Dch hold a zero state, and the slots of the last tile
                 // past the sequence end (L rounded up to 32) the final state
-                float* dst = ck_lane + ((t0 - t_begin + i) / kSub) * ck_stride;
+                float* dst = ck_lane + ((t0 - t_begin + i) / kSub) * (CH * N);  // consecutive slots
                 constexpr int E1 = 32 * S;  // ckpt_slot(w, lane, S, 1) - ckpt_slot(w, lane, S, 0)
                 if constexpr (S == 4) {
                     *reinterpret_cast<float4*>(dst) = make_float4(h[0].x, h[1].x, h[2].x, h[3].x);

@@ -282,18 +282,24 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
 // into the caller's buffer; ss_bwd's checkpoint pass into its workspace):
 // the state entering every kSub-th step of every (b, d) row, which the
 // backward recomputes its windows from, then at ckpt_y0_offset the pre-gate
-// readout y0 (f32 [Bsz][L][Dch]).  States layout: [slot t / kSub][b][channel
-// tile][block of CH x N floats]; within a block, lane l of warp w holds S
-// states of its first channel at ckpt_slot(w, l, S, 0) and S of its second
-// at ckpt_slot(w, l, S, 1) (the scan kernels' lane layout): the 32 lanes' runs
-// of one channel of their pair are contiguous, so that a warp's 16-byte
-// stores and loads of them are 512 contiguous bytes (and free of shared-
-// memory bank conflicts once staged).
+// readout y0 (f32 [Bsz][L][Dch]).  States layout: [b][channel tile][slot t /
+// kSub][block of CH x N floats] (ckpt_block): the blocks of consecutive slots
+// of a unit are contiguous, so that the backward copies two at a time.
+// Within a block, lane l of warp w holds S states of its first channel at
+// ckpt_slot(w, l, S, 0) and S of its second at ckpt_slot(w, l, S, 1) (the
+// scan kernels' lane layout): the 32 lanes' runs of one channel of their pair
+// are contiguous, so that a warp's 16-byte stores and loads of them are 512
+// contiguous bytes (and free of shared-memory bank conflicts once staged).
 inline size_t ckpt_y0_offset(const FPlan& p, int64_t Bsz, int64_t N) {
     return align_up((size_t)Bsz * p.tiles_b * channels_per_block(N) * p.slots * N * sizeof(float), 256);
 }
 inline size_t ckpt_bytes(const FPlan& p, int64_t Bsz, int64_t L, int64_t Dch, int64_t N) {
     return ckpt_y0_offset(p, Bsz, N) + (size_t)Bsz * L * Dch * sizeof(float);
+}
+
+// Float offset of the saved-state block of (batch row b, channel tile, slot).
+__host__ __device__ inline int64_t ckpt_block(const FPlan& p, int64_t b, int64_t tile, int64_t slot, int64_t N) {
+    return ((b * p.tiles_b + tile) * p.slots + slot) * (channels_per_block(N) * N);
 }
 
 // Float offset of lane's S saved states of channel e (0: the first of its
