@@ -93,10 +93,13 @@ def mufu_counts(w):
 # figure stale, and it is reported as null.
 TRAFFIC = {
     # both launches of the main pass (608 one-chunk units; 32 units x 19 chunks)
-    ("k_bwd_main", "mamba2.8b-layer-bf16"): 2947489000,  # 1595.4 + 85.5 MB read, 1236.9 + 29.7 MB written
-    ("k_fwd_y", "mamba2.8b-layer-bf16"): 1574638432,     # 480.0 + 26.8 MB read, 1058.8 + 9.1 MB written
+    ("k_bwd_main", "mamba2.8b-layer-bf16"): 2948370000,  # 1595.8 + 85.5 MB read, 1238.2 + 28.9 MB written
+    ("k_fwd_y", "mamba2.8b-layer-bf16"): 1572698752,     # 480.0 + 26.8 MB read, 1059.2 + 6.6 MB written
 }
-TRAFFIC_SRC_DIGEST = "ca60dcc4301bee81"
+TRAFFIC_SRC_DIGEST = "908fb9597f19d6a2"
+
+# timed end-to-end runs (their median is reported)
+E2E_RUNS = 5
 
 
 def measured_traffic(kernel, w):
@@ -606,11 +609,11 @@ def run_ours(args):
 
     e2e_run(2)
     torch.cuda.synchronize(dev)
-    # three timed runs of e2e_steps steps: the host link is shared with other
+    # five timed runs of e2e_steps steps: the host link is shared with other
     # work on the machine and its throughput varies from run to run (seen: 2x),
     # so the median is reported and every run is listed
     e2e_runs = []
-    for _ in range(3):
+    for _ in range(E2E_RUNS):
         barrier(world)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -619,7 +622,7 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
         barrier(world)
         e2e_runs.append(max_over_ranks(e0.elapsed_time(e1), world))
-    e2e_ms = sorted(e2e_runs)[1]
+    e2e_ms = sorted(e2e_runs)[E2E_RUNS // 2]
     e2e_value = job_throughput(w.bld * e2e_steps, world, e2e_ms)
     staging, plan, launches = r.staging, r.plan, r.launches()
     gstatus = ss.device_status(stream)
