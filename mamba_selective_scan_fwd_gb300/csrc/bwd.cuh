@@ -19,11 +19,13 @@
 // channel; a lane holds S states of a channel pair):
 //   * the forward (ss_fwd_save) or a checkpoint pass stores the state
 //     entering every kSub-th step, and the pre-gate readout y0 that dz needs;
-//   * this kernel visits kSub-step tiles from the end of the chunk backwards.
-//     The tile prologue computes the per-(t, d) terms once (softplus and its
-//     derivative, the gate, g, dz, which it stores at once) into shared
-//     memory: the walk's (delta_eff, delta_eff * u, g), and u and the softplus
-//     derivative for the epilogue.  Each lane then recomputes the tile's
+//   * this kernel visits kSub-step tiles from the end of the chunk backwards
+//     (staged by TMA in pairs of tiles for two-warp blocks).  The tile
+//     prologue computes the per-(t, d) terms once (softplus and its
+//     derivative, the gate, g, dz, which it stores at once): the walk's
+//     (delta_eff, delta_eff * u, g) into shared memory, and u, the softplus
+//     derivative, delta_eff and g in the item thread's registers for its
+//     epilogue (in shared memory where they do not fit).  Each lane then recomputes the tile's
 //     states forward from the saved one, keeping the kSub states in
 //     registers, and walks the adjoint backwards, evaluating each step's
 //     decays again, one step ahead of the adjoint that needs them (MUFU has
