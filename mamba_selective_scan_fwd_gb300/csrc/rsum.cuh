@@ -151,6 +151,12 @@ __global__ void __launch_bounds__(32 * scan_warps(N), 6) k_bwd_rsum(BwdArgs a, F
     }
     issue(ntile - 1);
     __syncthreads();  // sBias and the barriers
+    // the thread's items cover the same channel group in every tile: its biases
+    // stay in registers
+    const int cg = (tid % NGRP) * GRP;
+    float biasv[GRP];
+#pragma unroll
+    for (int c = 0; c < GRP; c++) biasv[c] = sBias[cg + c];
 
     for (int64_t m = ntile - 1; m >= 0; m--) {
         const int64_t t0 = t_begin + m * kRsTT;
@@ -160,43 +166,56 @@ __global__ void __launch_bounds__(32 * scan_warps(N), 6) k_bwd_rsum(BwdArgs a, F
         bool ok = true;
         if (tma) ok = mbar_wait(&sBar[buf], phase);
         // ---- prologue: (step, GRP-channel group) items; steps past t_end get
-        // delta_eff = g = 0, which leave the carry unchanged
+        // delta_eff = g = 0, which leave the carry unchanged.  All of the items'
+        // loads come first, then their arithmetic (no branch on the row's
+        // validity: selects zero the rows past t_end, whose shared-memory runs
+        // hold finite data -- TMA zero fill past the tensor, the next chunk
+        // before it), then the stores: with no store between them, the items'
+        // dependency chains interleave.
+        uint32_t rd[ITEMS][RW], rg[ITEMS][RW], rz[ITEMS][RW];
 #pragma unroll
         for (int it = 0; it < ITEMS; it++) {
-            const int id = tid + it * THREADS;
-            const int r = id / NGRP, cg = (id % NGRP) * GRP;
+            const int r = (tid + it * THREADS) / NGRP;
             const int64_t t = t0 + r;
-            const bool rv = t < t_end;
-            uint32_t rd[RW], rg[RW], rz[RW];
-            if (rv) {
-                if (tma) {
-                    lds_words<GRP * C::ESZ, RW>(&sRaw[buf][0][r][cg], rd);
-                    lds_words<GRP * C::ESZ, RW>(&sRaw[buf][1][r][cg], rg);
-                    if (z) lds_words<GRP * C::ESZ, RW>(&sRaw[buf][2][r][cg], rz);
-                } else {
-                    const int64_t off = (b * L + t) * Dch + d0 + cg;
-                    load_run<T, GRP, RW>(delta, off, d0 + cg, Dch, vfast, rd);
-                    load_run<T, GRP, RW>(dy, off, d0 + cg, Dch, vfast, rg);
-                    if (z) load_run<T, GRP, RW>(z, off, d0 + cg, Dch, vfast, rz);
-                }
+#pragma unroll
+            for (int v = 0; v < RW; v++) rd[it][v] = rg[it][v] = rz[it][v] = 0u;
+            if (tma) {
+                lds_words<GRP * C::ESZ, RW>(&sRaw[buf][0][r][cg], rd[it]);
+                lds_words<GRP * C::ESZ, RW>(&sRaw[buf][1][r][cg], rg[it]);
+                if (z) lds_words<GRP * C::ESZ, RW>(&sRaw[buf][2][r][cg], rz[it]);
+            } else if (t < t_end) {
+                const int64_t off = (b * L + t) * Dch + d0 + cg;
+                load_run<T, GRP, RW>(delta, off, d0 + cg, Dch, vfast, rd[it]);
+                load_run<T, GRP, RW>(dy, off, d0 + cg, Dch, vfast, rg[it]);
+                if (z) load_run<T, GRP, RW>(z, off, d0 + cg, Dch, vfast, rz[it]);
             }
+        }
+        float4 dv[ITEMS][GRP / 2];
+#pragma unroll
+        for (int it = 0; it < ITEMS; it++) {
+            const bool rv = t0 + (tid + it * THREADS) / NGRP < t_end;
 #pragma unroll
             for (int c = 0; c < GRP; c += 2) {
-                float2 dl = make_float2(0.f, 0.f), gg = dl;
-                if (rv) {
-                    const float2 x = make_float2(elem<T>(rd, c) + sBias[cg + c], elem<T>(rd, c + 1) + sBias[cg + c + 1]);
-                    dl = f.softplus ? softplus2(x) : x;
-                    const float2 dyv = make_float2(elem<T>(rg, c), elem<T>(rg, c + 1));
-                    gg = dyv;
-                    if (z) {
-                        const float2 zz = make_float2(elem<T>(rz, c), elem<T>(rz, c + 1));
-                        gg = mul2(mul2(dyv, sigmoid2(zz)), zz);
-                    }
+                const float2 x = make_float2(elem<T>(rd[it], c) + biasv[c], elem<T>(rd[it], c + 1) + biasv[c + 1]);
+                const float2 sp = f.softplus ? softplus2(x) : x;
+                const float2 dyv = make_float2(elem<T>(rg[it], c), elem<T>(rg[it], c + 1));
+                float2 gg = dyv;
+                if (z) {
+                    const float2 zz = make_float2(elem<T>(rz[it], c), elem<T>(rz[it], c + 1));
+                    gg = mul2(mul2(dyv, sigmoid2(zz)), zz);
                 }
+                const float2 dl = rv ? sp : make_float2(0.f, 0.f);
+                gg = rv ? gg : make_float2(0.f, 0.f);
                 sdp[c] += dl.x;
                 sdp[c + 1] += dl.y;
-                sDG[buf][r][(cg + c) / 2] = make_float4(dl.x, dl.y, gg.x, gg.y);
+                dv[it][c / 2] = make_float4(dl.x, dl.y, gg.x, gg.y);
             }
+        }
+#pragma unroll
+        for (int it = 0; it < ITEMS; it++) {
+            const int r = (tid + it * THREADS) / NGRP;
+#pragma unroll
+            for (int c = 0; c < GRP; c += 2) sDG[buf][r][(cg + c) / 2] = dv[it][c / 2];
         }
         if (!tma) {
             // the C rows of the tile, zero past t_end
