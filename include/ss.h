@@ -393,8 +393,9 @@ const char *ss_status_string(int status);
  * ss_plan_segments added, the saved-state buffer sized by L rounded up to 32
  * steps; 5: a saved state every 8 steps, ss_device_status /
  * ss_selftest_wait_timeout / ss_set_copies_only added; 6: the saved states
- * of ss_fwd_save interleaved by channel within a block (a buffer written by
- * an earlier version is not read correctly), ss_measure_fma_rate added);
+ * of ss_fwd_save laid out by (batch row, channel tile) then time and
+ * interleaved by channel within a block (a buffer written by an earlier
+ * version is not read correctly), ss_measure_fma_rate added);
  * bumped on any incompatible change. */
 int ss_abi_version(void);
 
