@@ -566,25 +566,30 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
                 // two channels at a time with packed arithmetic
                 float2 dl2, sg2, dz2 = make_float2(0.f, 0.f);
                 const float2 x = make_float2(elem<T>(rd, c) + biasv[c], elem<T>(rd, c + 1) + biasv[c + 1]);
-                if (f.softplus) {
-                    softplus_sigmoid2(x, dl2, sg2);
-                } else {
-                    dl2 = x;
-                    sg2 = make_float2(1.f, 1.f);
+                // the softplus and the gate terms are formed unconditionally and selected
+                // by the call's flags: a branch, even a uniform one, would split the
+                // items' interleaved chains (without z the run rz holds zeros)
+                {
+                    float2 spd, sgd;
+                    softplus_sigmoid2(x, spd, sgd);
+                    dl2 = f.softplus ? spd : x;
+                    sg2 = f.softplus ? sgd : make_float2(1.f, 1.f);
                 }
                 dl2 = rv ? dl2 : make_float2(0.f, 0.f);
                 const float2 uu2 = make_float2(elem<T>(ru, c), elem<T>(ru, c + 1));
                 const float2 dlu2 = mul2(dl2, uu2);
                 const float2 dyv = make_float2(elem<T>(rg, c), elem<T>(rg, c + 1));
-                float2 gg2 = dyv;
-                if (z) {
+                float2 gg2;
+                {
                     const float2 zz = make_float2(elem<T>(rz, c), elem<T>(rz, c + 1));
                     const float2 sz = sigmoid2(zz);
                     const float2 dsz = mul2(dyv, sz);
-                    gg2 = mul2(dsz, zz);
+                    const float2 gz = mul2(dsz, zz);
                     // dz = dy sig(z) (1 + z (1 - sig(z))) y0
                     const float2 dzf = mul2(dsz, fma2(zz, add2(splat2(1.f), make_float2(-sz.x, -sz.y)), splat2(1.f)));
-                    dz2 = mul2(dzf, make_float2(vy0[c], vy0[c + 1]));
+                    const float2 dzv = mul2(dzf, make_float2(vy0[c], vy0[c + 1]));
+                    gg2 = z ? gz : dyv;
+                    dz2 = z ? dzv : make_float2(0.f, 0.f);
                 }
                 const int pr = (cg + c) / 2;
                 dv[c / 2] = make_float4(dl2.x, dl2.y, dlu2.x, dlu2.y);

@@ -372,7 +372,10 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
                 for (int c = 0; c < GRP; c += 2) {
                     // two channels at a time with packed arithmetic
                     const float2 x = make_float2(elem<T>(rd[k], c) + biasv[c], elem<T>(rd[k], c + 1) + biasv[c + 1]);
-                    const float2 sp = a.softplus ? softplus2(x) : x;
+                    // formed unconditionally and selected by the call's flag: a branch, even a
+                    // uniform one, would split the items' interleaved chains
+                    const float2 spf = softplus2(x);
+                    const float2 sp = a.softplus ? spf : x;
                     const float2 uu = make_float2(elem<T>(ru[k], c), elem<T>(ru[k], c + 1));
                     const float2 spu = mul2(sp, uu);
                     const float2 dl = rv ? sp : make_float2(0.f, 0.f), dlu = rv ? spu : make_float2(0.f, 0.f);
@@ -537,9 +540,10 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
                             if constexpr (KEEP) {
                                 const float2 uu = make_float2(elem<T>(kU[it], cc), elem<T>(kU[it], cc + 1));
                                 y0 = fma2(make_float2(dvv[cc], dvv[cc + 1]), uu, make_float2(sum4[e], sum4[e + 1]));
-                                if (GATE && z) {
+                                if constexpr (GATE) {
                                     const float2 zz = make_float2(elem<T>(kZ[it], cc), elem<T>(kZ[it], cc + 1));
-                                    gt = mul2(zz, sigmoid2(zz));
+                                    const float2 gz = mul2(zz, sigmoid2(zz));  // selected, not branched on
+                                    gt = z ? gz : make_float2(1.f, 1.f);
                                 }
                             } else {
                                 const float4 gd = sGD[r][(cg + cc) / 2];

@@ -197,13 +197,14 @@ __global__ void __launch_bounds__(32 * scan_warps(N), 6) k_bwd_rsum(BwdArgs a, F
 #pragma unroll
             for (int c = 0; c < GRP; c += 2) {
                 const float2 x = make_float2(elem<T>(rd[it], c) + biasv[c], elem<T>(rd[it], c + 1) + biasv[c + 1]);
-                const float2 sp = f.softplus ? softplus2(x) : x;
+                // selected by the call's flags rather than branched on (without z the run
+                // rz holds zeros)
+                const float2 spf = softplus2(x);
+                const float2 sp = f.softplus ? spf : x;
                 const float2 dyv = make_float2(elem<T>(rg[it], c), elem<T>(rg[it], c + 1));
-                float2 gg = dyv;
-                if (z) {
-                    const float2 zz = make_float2(elem<T>(rz[it], c), elem<T>(rz[it], c + 1));
-                    gg = mul2(mul2(dyv, sigmoid2(zz)), zz);
-                }
+                const float2 zz = make_float2(elem<T>(rz[it], c), elem<T>(rz[it], c + 1));
+                const float2 gz = mul2(mul2(dyv, sigmoid2(zz)), zz);
+                float2 gg = z ? gz : dyv;
                 const float2 dl = rv ? sp : make_float2(0.f, 0.f);
                 gg = rv ? gg : make_float2(0.f, 0.f);
                 sdp[c] += dl.x;
