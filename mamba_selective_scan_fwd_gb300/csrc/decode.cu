@@ -186,13 +186,17 @@ __global__ void __launch_bounds__(256, dec_cm_blocks_per_sm<T>()) k_decode_cm(De
     };
     if (b0 < b1) load(b0, h, uu, xd, zz);
     for (int b = b0; b < b1; b++) {
-        if (b + 1 < b1) load(b + 1, hn, un, xn, zn);
+        // the next row's inputs (the last row's again after it, unused): no branch
+        // splits the row's loads from its arithmetic
+        load(b + 1 < b1 ? b + 1 : b, hn, un, xn, zn);
         // B and C of row b: the same words for every thread of the block
         uint32_t wb[BW], wc[BW];
         ldu_words<BW>(Bm + b * N, wb);
         ldu_words<BW>(Cm + b * N, wc);
         const float x = xd + bias;
-        const float dl = a.softplus ? softplus_fast(x) : x;
+        // softplus and the gate selected by the call's flags rather than branched on
+        const float sp = softplus_fast(x);
+        const float dl = a.softplus ? sp : x;
         const float dlu = dl * uu;
         float yp = 0.f;
 #pragma unroll
@@ -201,13 +205,13 @@ __global__ void __launch_bounds__(256, dec_cm_blocks_per_sm<T>()) k_decode_cm(De
             h[n] = fmaf(dA, h[n], dlu * elem<T>(wb, n));
             yp = fmaf(elem<T>(wc, n), h[n], yp);
         }
+        const float gz = zz * sigmoid_fast(zz);
+        const float yv = (yp + Dv * uu) * (z ? gz : 1.f);
         if (live) {
             const int64_t row = b * a.Dch + d;
 #pragma unroll
             for (int q = 0; q < N; q += 4)
                 __stcs(reinterpret_cast<float4*>(a.state + row * N + q), make_float4(h[q], h[q + 1], h[q + 2], h[q + 3]));
-            float yv = yp + Dv * uu;
-            if (z) yv *= zz * sigmoid_fast(zz);
             st(static_cast<T*>(a.y) + row, yv);
         }
 #pragma unroll

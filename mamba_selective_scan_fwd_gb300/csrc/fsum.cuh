@@ -164,7 +164,8 @@ __global__ void __launch_bounds__(32 * scan_warps(N), 6) k_fwd_fsum(FwdArgs a, F
                 float2 dl = make_float2(0.f, 0.f), dlu = dl;
                 if (rv) {
                     const float2 x = make_float2(elem<T>(rd, c) + sBias[cg + c], elem<T>(rd, c + 1) + sBias[cg + c + 1]);
-                    dl = a.softplus ? softplus2(x) : x;
+                    const float2 spf = softplus2(x);  // selected, not branched on
+                    dl = a.softplus ? spf : x;
                     dlu = mul2(dl, make_float2(elem<T>(ru, c), elem<T>(ru, c + 1)));
                 }
                 sdp[c] += dl.x;
