@@ -25,11 +25,11 @@
 //     derivative, the gate, g, dz, which it stores at once): the walk's
 //     (delta_eff, delta_eff * u, g) into shared memory, and u, the softplus
 //     derivative, delta_eff and g in the item thread's registers for its
-//     epilogue (in shared memory where they do not fit).  Each lane then recomputes the tile's
-//     states forward from the saved one, keeping the kSub states in
-//     registers, and walks the adjoint backwards, evaluating each step's
-//     decays again, one step ahead of the adjoint that needs them (MUFU has
-//     room to spare; the registers do not);
+//     epilogue (in shared memory where they do not fit).  Each lane then
+//     recomputes the tile's states forward from the saved one, keeping the
+//     kSub states in registers, and walks the adjoint backwards, evaluating
+//     each step's decays again, one step ahead of the adjoint that needs them
+//     (MUFU has room to spare; the registers do not);
 //   * per step each lane stores its two channels' sums over its states, and
 //     each warp sums dB / dC of its states over the block's channels through
 //     shared memory in a fixed order; the tile epilogue adds the lanes' and
@@ -120,9 +120,10 @@ struct BCfg {
     static constexpr int MINB = NW == 2 ? 4 : 8;
     // Tiles per staging copy ("a pair"): two for two-warp blocks.  A TMA copy
     // holds its issuing thread for some 60 - 100 cycles whatever its size, so
-    // the copies of a tile's eight tensors cost about as much as its recompute;
-    // a copy of two tiles halves that per step, for 8 KB more shared memory (a
-    // one-warp block keeps one tile per copy: 8 of them share an SM).
+    // the copies of a tile's eight tensors cost the issuing warp about as much
+    // as the tile's recompute; a copy of two tiles halves that per step, for
+    // 8 KB more shared memory (a one-warp block keeps one tile per copy: 8 of
+    // them share an SM).
     static constexpr int TPP = NW == 2 ? 2 : 1;
     static_assert(kTT * NGRP % THREADS == 0, "whole items per thread");
     static_assert(CH == channels_per_block(N), "channel tile of the plan");

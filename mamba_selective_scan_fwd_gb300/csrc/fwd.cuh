@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(32 * scan_warps(N), scan_warps(N) == 2 ? 4 : 8
     issue(t_begin, 0);
     __syncthreads();  // sBias / sDv, the barriers
     // the thread's prologue / epilogue items cover the same channel group in every
-    // tile (THREADS is a multiple of NGRP): its biases stay in registers
+    // tile (THREADS is a multiple of NGRP): its biases and D stay in registers
     static_assert(THREADS % NGRP == 0, "one channel group per thread");
     const int cg = (tid % NGRP) * GRP;
     float biasv[GRP], dvv[GRP];
