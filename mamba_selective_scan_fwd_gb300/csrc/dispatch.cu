@@ -80,23 +80,51 @@ __global__ void k_bwd_reduce_bc(BwdArgs a, FPlan p) {
 }
 
 // dA / dD / ddelta_bias: sum over the parts of each channel -- batch rows
-// ascending, and within a row the chunks of its unit ascending.
+// ascending, and within a row the chunks of its unit ascending.  The parts are
+// visited in batches of kPB whose loads are all issued before their sums (the
+// order of the sums is unchanged), so a thread waits for memory once per
+// batch rather than once per part.
 __global__ void k_bwd_reduce_params(BwdArgs a, FPlan p) {
-    const int64_t Dch = a.f.Dch, N = a.f.N, CH = channels_per_block(N);
+    const int64_t Dch = a.f.Dch, N = a.f.N, CH = channels_per_block(N), Bsz = a.f.Bsz;
     const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (e >= Dch * N) return;
     const int64_t d = e / N, n = e % N;
     const int64_t tile = d / CH, c = d % CH;
+    constexpr int kPB = 8;
     float acc = 0.f, accD = 0.f, accb = 0.f;
-    for (int64_t b = 0; b < a.f.Bsz; b++) {
-        const int64_t unit = b * p.tiles_b + tile;
-        const Seg sg = seg_of(p, unit);
-        const int64_t q0 = sg.q0 + (unit - sg.u_lo) * sg.K;
-        for (int64_t k = 0; k < sg.K; k++) {
-            acc += a.ws_dA[((q0 + k) * CH + c) * N + n];
-            if (n == 0) {
-                accD += a.ws_dD[(q0 + k) * CH + c];
-                accb += a.ws_db[(q0 + k) * CH + c];
+    int64_t b = 0, k = 0;  // the next part: chunk k of batch row b's unit
+    Seg sg = seg_of(p, tile);
+    while (b < Bsz) {
+        int64_t qv[kPB];
+#pragma unroll
+        for (int j = 0; j < kPB; j++) {
+            qv[j] = -1;
+            if (b < Bsz) {
+                qv[j] = sg.q0 + (b * p.tiles_b + tile - sg.u_lo) * sg.K + k;
+                if (++k == sg.K) {
+                    k = 0;
+                    if (++b < Bsz) sg = seg_of(p, b * p.tiles_b + tile);
+                }
+            }
+        }
+        float v[kPB], vD[kPB], vb[kPB];
+#pragma unroll
+        for (int j = 0; j < kPB; j++) {
+            v[j] = vD[j] = vb[j] = 0.f;
+            if (qv[j] >= 0) {
+                v[j] = a.ws_dA[(qv[j] * CH + c) * N + n];
+                if (n == 0) {
+                    vD[j] = a.ws_dD[qv[j] * CH + c];
+                    vb[j] = a.ws_db[qv[j] * CH + c];
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kPB; j++) {
+            if (qv[j] >= 0) {
+                acc += v[j];
+                accD += vD[j];
+                accb += vb[j];
             }
         }
     }
