@@ -439,18 +439,21 @@ def analyse(w, plan, ms_per_step, t_fwd, t_bwd, k_fwd, k_bwd, peaks):
             r["hbm"] = hbm
         return r
 
-    # launch order of a call: the summary passes of the chunked segments, then
-    # each segment's main pass (then, in the backward, the two reductions)
+    # launch order of a call: the summary passes of the chunked segments (in the
+    # backward followed by their carry passes), then each segment's main pass
+    # (then, in the backward, the two reductions)
     segs = plan["segments"]
     tag = [f"{u} units x {k} chunk{'s' if k > 1 else ''}" for u, k in segs]
     first = "y + saved states" if w.backward else "y"
-    fwd_names = ([f"k_fwd chunk summary ({tag[i]})" for i, (_, k) in enumerate(segs) if k > 1] +
-                 [f"k_fwd {first} ({t})" for t in tag])
-    bwd_names = ([f"k_bwd reverse summary ({tag[i]})" for i, (_, k) in enumerate(segs) if k > 1] +
+    chunked = [i for i, (_, k) in enumerate(segs) if k > 1]
+    fwd_names = [f"k_fwd chunk summary ({tag[i]})" for i in chunked] + [f"k_fwd {first} ({t})" for t in tag]
+    bwd_names = ([f"k_bwd reverse summary ({tag[i]})" for i in chunked] +
+                 [f"k_bwd_carry ({tag[i]})" for i in chunked] +
                  [f"k_bwd main ({t})" for t in tag] + ["k_bwd_reduce_bc", "k_bwd_reduce_params"])
-    n_sum = sum(1 for _, k in segs if k > 1)
-    main = range(n_sum, n_sum + len(segs))  # a direction's main pass: one launch per segment
-    t_main_f = sum(k_fwd[j] for j in main)
+    # a direction's main pass: one launch per segment
+    main_f = range(len(chunked), len(chunked) + len(segs))
+    main_b = range(2 * len(chunked), 2 * len(chunked) + len(segs))
+    t_main_f = sum(k_fwd[j] for j in main_f)
     launches = f"{len(segs)} launch{'es' if len(segs) > 1 else ''}"
     f32_fwd, f32_bwd = F32_OPS_FWD * exps, F32_OPS_BWD * exps
     r_fwd = roof(fwd_bytes, f32_fwd, t_main_f)
@@ -460,7 +463,7 @@ def analyse(w, plan, ms_per_step, t_fwd, t_bwd, k_fwd, k_bwd, peaks):
            "ns_per_element": round(ms_per_step * 1e6 / w.bld, 5)}
     t_roof = roof(fwd_bytes, f32_fwd, t_fwd)["roofline_ms"]
     if w.backward:
-        t_main_b = sum(k_bwd[j] for j in main)
+        t_main_b = sum(k_bwd[j] for j in main_b)
         r_bwd = roof(bwd_main_bytes, f32_bwd, t_main_b)
         r_bwd.update({"kernel": f"k_bwd main pass (ss_bwd_saved; {launches})", "ms": round(t_main_b, 4),
                       "traffic": measured_traffic("k_bwd_main", w)})

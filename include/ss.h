@@ -196,8 +196,10 @@ int ss_plan_info(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype, int6
  * appears when the units fill the GPU but leave a last partial round of
  * blocks (a round: 8 warps on each of its 152 SMs, 608 blocks for N >= 16):
  * those units are cut in time so that every SM gets an equal share.  The kernels of each call run in this order: the summary
- * passes of the chunked segments, then each segment's main pass (segment 0
- * first), then, in the backward, the two reductions.  units and chunks point
+ * passes of the chunked segments (in the backward followed by their carry
+ * passes, which fold the reverse summaries into each chunk's incoming
+ * adjoint carry), then each segment's main pass (segment 0 first), then, in
+ * the backward, the two reductions.  units and chunks point
  * at 2 entries each (or NULL); nseg may be NULL.  Returns a status.
  */
 int ss_plan_segments(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype, int *nseg, int64_t *units,
@@ -395,7 +397,9 @@ const char *ss_status_string(int status);
  * ss_selftest_wait_timeout / ss_set_copies_only added; 6: the saved states
  * of ss_fwd_save laid out by (batch row, channel tile) then time and
  * interleaved by channel within a block (a buffer written by an earlier
- * version is not read correctly), ss_measure_fma_rate added);
+ * version is not read correctly), ss_measure_fma_rate added; 7: in the
+ * backward a chunked segment runs a carry pass between its reverse summaries
+ * and its main pass, which ss_plan_info counts and ss_profile_events marks);
  * bumped on any incompatible change. */
 int ss_abi_version(void);
 

@@ -29,7 +29,7 @@ EXPORTS = ["ss_fwd", "ss_bwd", "ss_fwd_workspace_bytes", "ss_bwd_workspace_bytes
            "ss_decode_step", "ss_plan_segments", "ss_device_status", "ss_selftest_wait_timeout",
            "ss_set_copies_only", "ss_staging_uses_tma", "ss_measure_ex2_rate",
            "ss_measure_fma_rate"]
-ABI_VERSION = 6
+ABI_VERSION = 7
 
 # Size of the library-owned scratch behind ss_fwd_noalloc (SS_FWD_NOALLOC_MAX_SCRATCH_BYTES).
 FWD_NOALLOC_MAX_SCRATCH_BYTES = 2 << 20

@@ -319,7 +319,7 @@ int ss_profile_events(void* const* events, int count) {
     return SS_OK;
 }
 
-int ss_abi_version(void) { return 6; }
+int ss_abi_version(void) { return 7; }
 
 int ss_device_status(void* stream) {
     int* status = nullptr;
@@ -396,15 +396,19 @@ int ss_plan_info(int64_t Bsz, int64_t L, int64_t Dch, int64_t N, int dtype, int6
     const bool empty = Bsz == 0 || L == 0 || Dch == 0;
     const FPlan fp = make_fplan(Bsz, L, Dch, N);
     if (chunks) *chunks = empty ? 0 : fp.Kmax;
-    // per segment: [a summary pass if it is chunked] + its main pass; the forward
-    // (with or without saving) runs the forward passes, the backward from saved
-    // states the reverse ones and 2 reductions, the backward the forward
-    // checkpoint passes first
-    int scans = 0;
-    for (int i = 0; i < fp.nseg; i++) scans += 1 + (fp.seg[i].K > 1 ? 1 : 0);
-    if (fwd_kernels) *fwd_kernels = empty ? 0 : scans;
-    if (bwd_kernels) *bwd_kernels = empty ? 0 : 2 * scans + 2;
-    if (bwd_saved_kernels) *bwd_saved_kernels = empty ? 0 : scans + 2;
+    // per segment: its main pass, after a summary pass if it is chunked (and in
+    // the backward a carry pass after that); the forward (with or without
+    // saving) runs the forward passes, the backward from saved states the
+    // reverse ones and 2 reductions, the backward the forward checkpoint passes
+    // first
+    int fscans = 0, rscans = 0;
+    for (int i = 0; i < fp.nseg; i++) {
+        fscans += 1 + (fp.seg[i].K > 1 ? 1 : 0);
+        rscans += 1 + (fp.seg[i].K > 1 ? 2 : 0);
+    }
+    if (fwd_kernels) *fwd_kernels = empty ? 0 : fscans;
+    if (bwd_kernels) *bwd_kernels = empty ? 0 : fscans + rscans + 2;
+    if (bwd_saved_kernels) *bwd_saved_kernels = empty ? 0 : rscans + 2;
     return SS_OK;
 }
 

@@ -323,25 +323,16 @@ __global__ void __launch_bounds__(32 * scan_warps(N), BCfg<T, N>::MINB) k_bwd(Bw
         }
     }
     if (MAIN && k + 1 < sgm.K) {
-        // carry into the end of chunk k: rho_{j-1} = M_j + P_j rho_j from the
-        // reverse summaries of the unit's chunks K-1 .. k+1 (P_j = exp2(A2 *
-        // sum of delta_eff over chunk j)), with rho_{K-1} the carry into the end
-        // of the sequence
+        // carry into the end of chunk k (rho_{j-1} = M_j + P_j rho_j over the
+        // reverse summaries of the unit's chunks K-1 .. k+1, P_j = exp2(A2 * sum
+        // of delta_eff over chunk j), from rho_{K-1} the carry into the end of
+        // the sequence), which k_bwd_carry left over the summary of chunk k + 1
 #pragma unroll
         for (int e = 0; e < 2; e++) {
-            for (int64_t jj = sgm.K - 1; jj > k; jj--) {
-                const int64_t q = s_first + jj;
-                const float* M = a.ws_rsum + (q * CH + c0 + e) * N + n0;
-                const float2 sdj = splat2(a.ws_rsd[q * CH + c0 + e]);
+            const float* M = a.ws_rsum + ((s_first + k + 1) * CH + c0 + e) * N + n0;
 #pragma unroll
-                for (int j = 0; j < SP; j++) {
-                    const float2 x = mul2(A2[e][j], sdj);
-                    const float2 Mj = make_float2(M[2 * j], S >= 2 ? M[2 * j + 1] : 0.f);
-                    carry[e][j] = fma2(make_float2(ex2a(x.x), ex2a(x.y)), carry[e][j], Mj);
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < SP; j++) carry[e][j] = ok[e] ? carry[e][j] : make_float2(0.f, 0.f);
+            for (int j = 0; j < SP; j++)
+                carry[e][j] = ok[e] ? make_float2(M[2 * j], S >= 2 ? M[2 * j + 1] : 0.f) : make_float2(0.f, 0.f);
         }
     }
     // dD / ddelta_bias partials of the thread's epilogue items (the same channels
@@ -1022,6 +1013,12 @@ cudaError_t launch_bwd_t(const BwdArgs& a, const FPlan& p, cudaStream_t st, floa
             if constexpr (BCfg<T, N>::NW == 2) k_bwd_rsum<T, N><<<grid, threads, 0, st>>>(a, p, si, 1, fmaps);
             else k_bwd<T, N, kRevSummary, false><<<grid, threads, 0, st>>>(a, p, si, 1, bmaps);
         }
+    }
+    // their carry passes: each chunk's incoming adjoint carry from the later chunks' summaries
+    for (int si = 0; si < p.nseg; si++) {
+        if (p.seg[si].K < 2) continue;
+        e = launch_bwd_carry(a, p, si, st);
+        if (e != cudaSuccess) return e;
     }
     const bool state = a.dlast != nullptr || a.dh0 != nullptr;
     auto main_kernel = state ? k_bwd<T, N, kRevMain, true> : k_bwd<T, N, kRevMain, false>;

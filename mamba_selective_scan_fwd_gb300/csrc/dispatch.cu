@@ -38,6 +38,59 @@ cudaError_t launch_bwd(const BwdArgs& a, const FPlan& p, cudaStream_t st, float*
     return cudaGetLastError();
 }
 
+// Carry pass of a time-cut segment in the backward (one thread per (unit,
+// channel, state)): from the reverse chunk summaries it forms the adjoint
+// carry into the end of every chunk, so that a main-pass block reads its
+// carry instead of folding the summaries of all the unit's later chunks
+// itself.  r_{K-1} = d(last_state) (zero without one) and r_{k-1} = P_k r_k +
+// M_k for k = K-1 .. 1, with M_k the carry chunk k passes back from a zero
+// incoming adjoint and P_k = exp2(A log2(e) * the chunk's sum of delta_eff):
+// each step is the one the main pass would take, in the same order and
+// arithmetic, so the results are the same bits.  r_{k-1}, the carry into the
+// end of chunk k - 1, is written over M_k, which nothing reads after it.  The
+// summaries of eight chunks are loaded before they are folded, so that a
+// thread waits for memory once per eight chunks.
+constexpr int kCarryBatch = 8;
+
+__global__ void k_bwd_carry(BwdArgs a, FPlan p, int si) {
+    const FwdArgs& f = a.f;
+    const Seg sgm = seg_at(p, si);
+    const int64_t N = f.N, CH = channels_per_block(N), Dch = f.Dch;
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= sgm.nu * CH * N) return;
+    const int64_t ul = e / (CH * N), c = (e / N) % CH, n = e % N;
+    const int64_t unit = sgm.u_lo + ul, b = unit / p.tiles_b, d = (unit % p.tiles_b) * CH + c;
+    const bool ok = d < Dch;  // channels past Dch: read as zero by the main pass
+    const float A2 = ok ? scan_A(f, d * N + n) * kLog2eF : 0.f;
+    float r = ok && a.dlast ? a.dlast[(b * Dch + d) * N + n] : 0.f;
+    const int64_t s_first = sgm.s0 + ul * sgm.K;         // reverse summaries of chunks 1 .. K-1
+    float* M = a.ws_rsum + (s_first * CH + c) * N + n;  // chunk j at M[j CH N]
+    const float* sd = a.ws_rsd + s_first * CH + c;     // chunk j at sd[j CH]
+    for (int64_t j0 = sgm.K - 1; j0 >= 1; j0 -= kCarryBatch) {
+        float mv[kCarryBatch], sv[kCarryBatch];
+#pragma unroll
+        for (int i = 0; i < kCarryBatch; i++) {
+            const int64_t j = j0 - i >= 1 ? j0 - i : 1;  // below chunk 1: read, not folded
+            mv[i] = M[j * CH * N];
+            sv[i] = sd[j * CH];
+        }
+#pragma unroll
+        for (int i = 0; i < kCarryBatch; i++) {
+            if (j0 - i >= 1) {
+                r = fmaf(ex2a(A2 * sv[i]), r, mv[i]);
+                M[(j0 - i) * CH * N] = r;  // the carry into the end of chunk j0 - i - 1
+            }
+        }
+    }
+}
+
+cudaError_t launch_bwd_carry(const BwdArgs& a, const FPlan& p, int si, cudaStream_t st) {
+    const int64_t n = p.seg[si].nu * channels_per_block(a.f.N) * a.f.N;
+    prof_mark(st);
+    k_bwd_carry<<<(unsigned)ceil_div(n, 256), 256, 0, st>>>(a, p, si);
+    return cudaGetLastError();
+}
+
 // dB / dC: sum of the per-tile partials, tiles in ascending order.  A thread
 // owns 4 consecutive outputs (16-byte streaming loads, 8 tiles in flight)
 // when N is a multiple of 4, one output otherwise.

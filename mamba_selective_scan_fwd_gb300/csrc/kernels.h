@@ -276,6 +276,11 @@ cudaError_t launch_fwd(const FwdArgs& a, const FPlan& p, cudaStream_t st, int mo
 cudaError_t launch_bwd(const BwdArgs& a, const FPlan& p, cudaStream_t st, float* ckpt_out, const TmaMaps& fmaps,
                        const TmaMaps& bmaps);
 
+// Carry pass of time-cut segment si (K > 1) in the backward, between the reverse
+// summaries and the main pass: it folds the summaries into the adjoint carry
+// into the end of every chunk, in place over the summaries the main pass reads.
+cudaError_t launch_bwd_carry(const BwdArgs& a, const FPlan& p, int si, cudaStream_t st);
+
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
 
 // Bytes of what the forward keeps for the backward (ss_fwd_save writes it

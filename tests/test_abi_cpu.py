@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol():
     lib = ss.lib()
     for name in declared_functions():
         assert hasattr(lib, name), name
-    assert lib.ss_abi_version() == binding.ABI_VERSION == 6
+    assert lib.ss_abi_version() == binding.ABI_VERSION == 7
 
 
 def test_status_strings():
@@ -146,13 +146,13 @@ def test_saved_sizes():
 def test_plan_info_counts():
     # 640 units over 152 SMs: 608 one-chunk units, the last 32 cut into 19 chunks
     p = ss.plan_info(4, 4096, 5120, 16, ss.SS_BF16)
-    assert p == {"chunks": 19, "fwd_kernels": 3, "bwd_kernels": 8, "bwd_saved_kernels": 5,
+    assert p == {"chunks": 19, "fwd_kernels": 3, "bwd_kernels": 9, "bwd_saved_kernels": 6,
                  "segments": [(608, 1), (32, 19)]}
     # 608 units: a whole number of rounds, no split
     p = ss.plan_info(4, 4096, 4864, 16, ss.SS_BF16)
     assert p == {"chunks": 1, "fwd_kernels": 1, "bwd_kernels": 4, "bwd_saved_kernels": 3, "segments": [(608, 1)]}
     q = ss.plan_info(1, 131072, 1024, 16, ss.SS_BF16)
-    assert q["chunks"] > 1 and q["fwd_kernels"] == 2 and q["bwd_kernels"] == 6 and q["bwd_saved_kernels"] == 4
+    assert q["chunks"] > 1 and q["fwd_kernels"] == 2 and q["bwd_kernels"] == 7 and q["bwd_saved_kernels"] == 5
     assert q["segments"] == [(32, q["chunks"])]
     e = ss.plan_info(0, 16, 8, 4, 0)
     assert e["fwd_kernels"] == 0 and e["segments"] == []

@@ -94,9 +94,9 @@ def _peaks(**kw):
 def test_analyse_rooflines_of_a_training_step():
     w = bench.pick_workload("mamba2.8b-layer-bf16")
     plan = {"segments": [(608, 1), (32, 19)]}
-    # launches: fwd = summary, main(seg0), main(seg1); bwd = summary, main x2, reduce_bc, reduce_params
+    # launches: fwd = summary, main(seg0), main(seg1); bwd = summary, carry, main x2, reduce_bc, reduce_params
     k_fwd = [0.05, 0.4, 0.1]
-    k_bwd = [0.06, 0.9, 0.2, 0.05, 0.01]
+    k_bwd = [0.06, 0.004, 0.9, 0.2, 0.05, 0.01]
     out = bench.analyse(w, plan, 2.0, sum(k_fwd), sum(k_bwd), k_fwd, k_bwd, _peaks())
     fwd_b, bwd_b = bench.algorithmic_bytes(w)
     exps = 1_342_177_280  # B L D N
@@ -126,8 +126,8 @@ def test_analyse_rooflines_of_a_training_step():
     assert list(out["kernel_ms"]) == [
         "k_fwd chunk summary (32 units x 19 chunks)", "k_fwd y + saved states (608 units x 1 chunk)",
         "k_fwd y + saved states (32 units x 19 chunks)", "k_bwd reverse summary (32 units x 19 chunks)",
-        "k_bwd main (608 units x 1 chunk)", "k_bwd main (32 units x 19 chunks)", "k_bwd_reduce_bc",
-        "k_bwd_reduce_params"]
+        "k_bwd_carry (32 units x 19 chunks)", "k_bwd main (608 units x 1 chunk)", "k_bwd main (32 units x 19 chunks)",
+        "k_bwd_reduce_bc", "k_bwd_reduce_params"]
 
 
 def test_analyse_forward_only_step():

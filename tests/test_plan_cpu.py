@@ -45,8 +45,9 @@ def test_plan_segments(shape):
     assert sum(u for u, _ in segs) == units
     assert p["chunks"] == max(k for _, k in segs)
     assert p["fwd_kernels"] == sum(1 + (k > 1) for _, k in segs)
-    assert p["bwd_saved_kernels"] == p["fwd_kernels"] + 2
-    assert p["bwd_kernels"] == 2 * p["fwd_kernels"] + 2
+    # the backward adds a carry pass after each chunked segment's reverse summaries
+    assert p["bwd_saved_kernels"] == p["fwd_kernels"] + sum(k > 1 for _, k in segs) + 2
+    assert p["bwd_kernels"] == p["fwd_kernels"] + p["bwd_saved_kernels"]
     if len(segs) == 2:
         (u0, k0), (u1, k1) = segs
         assert k0 == 1 and u0 % round_of(N) == 0 and u0 > 0 and 0 < u1 < round_of(N) and k1 > 1
