@@ -1,6 +1,7 @@
 // Launch dispatch on the io type (the kernels of each io type live in their
-// own translation unit: fwd_*.cu, bwd_*.cu), and the two backward
-// reduction kernels, which do not depend on it.
+// own translation unit: fwd_*.cu, bwd_*.cu), and the backward's kernels that
+// do not depend on it: the carry pass of time-cut segments and the two
+// reductions.
 #include "common.cuh"
 #include "kernels.h"
 #include "simd.cuh"
